@@ -1,0 +1,111 @@
+"""Seeded synthetic workloads shared by the tests, the smoke check and the benchmark.
+
+This module only draws random numbers and describes shapes; it holds none of
+the attention arithmetic, so the CUDA path and the CPU oracle can both be fed
+from it without sharing any of the method.
+
+Recipe (the same for every workload): a ``torch.Generator('cpu')`` seeded with
+the workload's seed draws, in this order, the valid lengths (non-causal only,
+uniform integers in [lo, hi]), then Q, K, V and the upstream gradient G, each
+i.i.d. N(0, 1) in fp32, and only then casts to the workload's dtype.  Decode
+draws q_t, k_t, v_t (in that order) once per step from one generator.
+
+The shapes follow the pages' workloads: 784-token (28x28) and 3072-token
+(32x32x3) autoregressive image sequences with 8 heads of 64 dims, long
+speech-like non-causal sequences with 6 heads and lengths between 800 and 2048,
+and 256 independent decode streams.  The pages' datasets (MNIST, CIFAR-10, WSJ)
+are not used: these normal draws stand in for their activations.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str  # "causal" | "noncausal" | "decode"
+    B: int
+    H: int
+    N: int  # sequence length; decode: number of steps T
+    D: int
+    M: int
+    dtype: str  # "f32" | "bf16"
+    seed: int
+    len_range: tuple = field(default=None)  # non-causal: (lo, hi) inclusive
+
+    @property
+    def torch_dtype(self):
+        return DTYPES[self.dtype]
+
+
+WORKLOADS = {
+    "causal_tiny_f32": Workload("causal_tiny_f32", "causal", 1, 1, 64, 16, 16, "f32", 1),
+    "causal_mnist_bf16": Workload("causal_mnist_bf16", "causal", 8, 8, 784, 64, 64, "bf16", 2),
+    "causal_cifar_bf16": Workload("causal_cifar_bf16", "causal", 4, 8, 3072, 64, 64, "bf16", 3),
+    "noncausal_speech_f32": Workload("noncausal_speech_f32", "noncausal", 16, 6, 2048, 64, 64,
+                                     "f32", 4, (800, 2048)),
+    "decode_f32": Workload("decode_f32", "decode", 256, 8, 3072, 64, 64, "f32", 5),
+}
+
+
+def causal_inputs(B, H, N, D, M, dtype="f32", seed=0):
+    """q, k [B,H,N,D]; v, g [B,H,N,M] on the CPU in the requested dtype."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    q = torch.randn(B, H, N, D, generator=gen)
+    k = torch.randn(B, H, N, D, generator=gen)
+    v = torch.randn(B, H, N, M, generator=gen)
+    g = torch.randn(B, H, N, M, generator=gen)
+    dt = DTYPES[dtype]
+    return q.to(dt), k.to(dt), v.to(dt), g.to(dt)
+
+
+def noncausal_inputs(B, H, N, D, M, dtype="f32", seed=0, len_range=None):
+    """(lengths int32 [B], q, k, v, g); lengths drawn first, uniform in
+    [lo, hi] (all N when len_range is None)."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    if len_range is None:
+        lengths = torch.full((B,), N, dtype=torch.int32)
+    else:
+        lo, hi = len_range
+        lengths = torch.randint(lo, hi + 1, (B,), generator=gen).to(torch.int32)
+    q = torch.randn(B, H, N, D, generator=gen)
+    k = torch.randn(B, H, N, D, generator=gen)
+    v = torch.randn(B, H, N, M, generator=gen)
+    g = torch.randn(B, H, N, M, generator=gen)
+    dt = DTYPES[dtype]
+    return lengths, q.to(dt), k.to(dt), v.to(dt), g.to(dt)
+
+
+class DecodeStream:
+    """Per-step decode inputs: each call to ``step()`` draws q_t, k_t [B,H,D]
+    and v_t [B,H,M] from one seeded generator."""
+
+    def __init__(self, B, H, D, M, dtype="f32", seed=0):
+        self.B, self.H, self.D, self.M = B, H, D, M
+        self.dt = DTYPES[dtype]
+        self.gen = torch.Generator("cpu").manual_seed(seed)
+
+    def step(self):
+        q = torch.randn(self.B, self.H, self.D, generator=self.gen)
+        k = torch.randn(self.B, self.H, self.D, generator=self.gen)
+        v = torch.randn(self.B, self.H, self.M, generator=self.gen)
+        return q.to(self.dt), k.to(self.dt), v.to(self.dt)
+
+    def steps(self, T):
+        """T steps stacked: q, k [T,B,H,D]; v [T,B,H,M]."""
+        qs, ks, vs = zip(*(self.step() for _ in range(T)))
+        return torch.stack(qs), torch.stack(ks), torch.stack(vs)
+
+
+def workload_inputs(w: Workload):
+    """Inputs of a named workload (causal: q,k,v,g; non-causal: lengths,q,k,v,g)."""
+    if w.kind == "causal":
+        return causal_inputs(w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed)
+    if w.kind == "noncausal":
+        return noncausal_inputs(w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed, w.len_range)
+    raise ValueError("decode workloads are drawn step by step with DecodeStream")

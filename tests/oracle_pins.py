@@ -1,0 +1,280 @@
+"""Checks that pin the fp64 oracle to facts that do not come from the oracle.
+
+Each ``pin_*`` function takes an oracle instance and raises AssertionError when
+the oracle disagrees with something the pages or the mathematics fix: a second,
+independent form of the same quantity, a closed form, an invariant, a library
+routine (torch's ELU, numpy matmul), or central finite differences.  The
+mutation tests run the same pins against deliberately broken builds of the
+oracle to show that each plausible slip is caught.
+
+Sources: "Transformers are RNNs -- part 2/3": eq. 7 (phi = elu + 1), §3.3
+eq. 8 (masked quadratic form) and eq. 10-12 (recurrence), §3.3.1 eq. 13-15
+(gradients), §3.4 eq. 16-19 (RNN form); "Linear Attention/zh": kernel
+reformulation (shared S, z for the non-causal form).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+RNG_SHAPES = [  # (B, H, N, D, M): D != M catches transposed operands
+    (1, 1, 1, 3, 5),
+    (1, 2, 7, 3, 5),
+    (2, 1, 13, 4, 2),
+]
+
+
+def rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+def phi_lib(x):
+    """elu(x) + 1 through torch's own ELU (alpha = 1)."""
+    return torch.nn.functional.elu(torch.as_tensor(x, dtype=torch.float64)).numpy() + 1.0
+
+
+def rel(a, b, floor=1e-300):
+    """max |a - b| / max |b| (normwise-max), with max |b| floored at ``floor``
+    for quantities whose exact value is zero."""
+    a, b = np.asarray(a), np.asarray(b)
+    scale = max(np.max(np.abs(b)), floor)
+    return float(np.max(np.abs(a - b)) / scale)
+
+
+# ---------------------------------------------------------------- feature map
+
+def pin_phi(orc):
+    """eq. 7 against torch's ELU + 1, and phi' against autograd through it."""
+    x = np.concatenate([rand(200, 1, 3.0), [0.0, -0.0, 1e-300, -1e-300, 50.0, -50.0]])
+    y, dy = orc.phi(x)
+    assert rel(y, phi_lib(x)) < 1e-15, "phi != elu + 1"
+    xt = torch.tensor(x, requires_grad=True)
+    (torch.nn.functional.elu(xt) + 1.0).sum().backward()
+    assert rel(dy, xt.grad.numpy()) < 1e-15, "phi' != d(elu + 1)/dx"
+    assert np.all(y > 0), "phi must be positive"
+
+
+# ------------------------------------------------------------ causal forward
+
+def pin_causal_forms_agree(orc):
+    """eq. 8 (explicit masked matrix) and eq. 10-12 (recurrence) are the same
+    function: two independent algorithms must agree."""
+    for i, (B, H, N, D, M) in enumerate(RNG_SHAPES + [(1, 1, 64, 16, 16)]):
+        q, k, v = rand((B, H, N, D), 10 + i), rand((B, H, N, D), 20 + i), rand((B, H, N, M), 30 + i)
+        o1, d1 = orc.causal_fwd(q, k, v, "quadratic")
+        o2, d2 = orc.causal_fwd(q, k, v, "recurrent")
+        assert rel(o1, o2) < 1e-12 and rel(d1, d2) < 1e-12, "causal forms disagree"
+
+
+def pin_causal_closed_forms(orc):
+    """Closed forms of eq. 8:
+      * Q = K = 0 gives phi = 1, every weight equals D, so V'_i is the running
+        mean of V_1..V_i and den_i = D * i;
+      * V'_1 = V_1 (only one key is visible);
+      * constant value rows are reproduced exactly;
+      * V'_i lies in the per-coordinate hull of V_1..V_i (positive weights);
+      * den > 0."""
+    B, H, N, D, M = 2, 3, 9, 4, 6
+    v = rand((B, H, N, M), 1)
+    zeros = np.zeros((B, H, N, D))
+    for form in ("quadratic", "recurrent"):
+        o, den = orc.causal_fwd(zeros, zeros, v, form)
+        mean = np.cumsum(v, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+        assert rel(o, mean) < 1e-14, "Q=K=0 must give the running mean"
+        assert rel(den, D * np.broadcast_to(np.arange(1, N + 1), den.shape)) < 1e-15
+        q, k = rand((B, H, N, D), 2, 2.0), rand((B, H, N, D), 3, 2.0)
+        o, den = orc.causal_fwd(q, k, v, form)
+        assert np.array_equal(o[:, :, 0], v[:, :, 0]) or rel(o[:, :, 0], v[:, :, 0]) < 1e-15, \
+            "V'_1 must equal V_1"
+        assert np.all(den > 0), "den must be positive"
+        lo = np.minimum.accumulate(v, axis=2)
+        hi = np.maximum.accumulate(v, axis=2)
+        assert np.all(o >= lo - 1e-12) and np.all(o <= hi + 1e-12), "V' outside the hull"
+        c = rand((B, H, 1, M), 4)
+        oc, _ = orc.causal_fwd(q, k, np.broadcast_to(c, (B, H, N, M)), form)
+        assert rel(oc, np.broadcast_to(c, oc.shape)) < 1e-14, "constant V not reproduced"
+
+
+def pin_grad_single_token(orc):
+    """N = 1: V'_1 = V_1 whatever Q and K are, so dQ = dK = 0 and dV = G."""
+    q, k, v, g = rand((2, 2, 1, 3), 15), rand((2, 2, 1, 3), 16), rand((2, 2, 1, 4), 17), rand((2, 2, 1, 4), 18)
+    for form in ("recurrent", "quadratic"):
+        dq, dk, dv = orc.causal_bwd(q, k, v, g, form)
+        assert np.max(np.abs(dq)) < 1e-14 and np.max(np.abs(dk)) < 1e-14, "N=1 gradient not zero"
+        assert rel(dv, g) < 1e-15, "N=1: dV != G"
+
+
+# --------------------------------------------------------------- non-causal
+
+def pin_noncausal_gemm(orc):
+    """Non-causal form = two textbook products (kernel reformulation of
+    "Linear Attention/zh"): S = phi(K)^T V, z = phi(K)^T 1, V' = phi(Q) S / phi(Q) z,
+    computed with numpy matmul and torch's ELU."""
+    B, H, N, D, M = 2, 2, 11, 3, 5
+    q, k, v = rand((B, H, N, D), 5), rand((B, H, N, D), 6), rand((B, H, N, M), 7)
+    fq, fk = phi_lib(q), phi_lib(k)
+    S = np.matmul(np.swapaxes(fk, -1, -2), v)
+    Z = fk.sum(axis=2)
+    den = np.matmul(fq, Z[..., None])[..., 0]
+    ref = np.matmul(fq, S) / den[..., None]
+    for form in ("recurrent", "quadratic"):
+        o, d, S2, Z2 = orc.noncausal_fwd(q, k, v, None, form)
+        assert rel(o, ref) < 1e-13 and rel(d, den) < 1e-13, "non-causal != GEMM form"
+        if S2 is not None:
+            assert rel(S2, S) < 1e-13 and rel(Z2, Z) < 1e-13, "S, Z != phi(K)^T [V, 1]"
+
+
+def pin_noncausal_last_row(orc):
+    """With every position valid, the non-causal output equals the causal one at
+    the last position (both read S_N, Z_N)."""
+    B, H, N, D, M = 1, 2, 10, 3, 4
+    q, k, v = rand((B, H, N, D), 8), rand((B, H, N, D), 9), rand((B, H, N, M), 10)
+    oc, dc = orc.causal_fwd(q, k, v, "quadratic")
+    on, dn, _, _ = orc.noncausal_fwd(q, k, v, None, "recurrent")
+    assert rel(on[:, :, -1], oc[:, :, -1]) < 1e-13 and rel(dn[:, :, -1], dc[:, :, -1]) < 1e-13
+
+
+def pin_noncausal_lengths(orc):
+    """Padding: a batch entry of valid length L gives the same result as the
+    unpadded sequence truncated to L, zeros beyond it, and no dependence on the
+    padded contents."""
+    B, H, N, D, M = 3, 2, 12, 3, 4
+    lengths = np.array([12, 5, 1], dtype=np.int32)
+    q, k, v, g = (rand((B, H, N, D), 11), rand((B, H, N, D), 12), rand((B, H, N, M), 13),
+                  rand((B, H, N, M), 14))
+    for form in ("recurrent", "quadratic"):
+        o, den, _, _ = orc.noncausal_fwd(q, k, v, lengths, form)
+        dq, dk, dv = orc.noncausal_bwd(q, k, v, g, lengths, form)
+        for b, L in enumerate(lengths):
+            sl = (slice(b, b + 1), slice(None), slice(0, L))
+            ot, dt, _, _ = orc.noncausal_fwd(q[sl], k[sl], v[sl], None, form)
+            gq, gk, gv = orc.noncausal_bwd(q[sl], k[sl], v[sl], g[sl], None, form)
+            assert rel(o[sl], ot) < 1e-13 and rel(den[sl], dt) < 1e-13, "length mask wrong"
+            for a, r in ((dq, gq), (dk, gk), (dv, gv)):
+                assert rel(a[sl], r) < 1e-12, "length mask wrong in gradients"
+            pad = (b, slice(None), slice(L, None))
+            for a in (o, den, dq, dk, dv):
+                assert np.all(a[pad] == 0), "padded rows must be zero"
+        # scramble the padding: nothing may change
+        q2, k2, v2, g2 = q.copy(), k.copy(), v.copy(), g.copy()
+        for b, L in enumerate(lengths):
+            for a in (q2, k2, v2, g2):
+                a[b, :, L:] = 1e3 * np.sign(a[b, :, L:]) + 7.0
+        o2, _, _, _ = orc.noncausal_fwd(q2, k2, v2, lengths, form)
+        d2 = orc.noncausal_bwd(q2, k2, v2, g2, lengths, form)
+        assert np.array_equal(o, o2), "output depends on padding"
+        for a, r in zip((dq, dk, dv), d2):
+            assert np.array_equal(a, r), "gradient depends on padding"
+
+
+# ------------------------------------------------------------------ gradients
+
+def _loss(orc, kind, q, k, v, g, lengths):
+    if kind == "causal":
+        o, _ = orc.causal_fwd(q, k, v, "quadratic")
+    else:
+        o, _, _, _ = orc.noncausal_fwd(q, k, v, lengths, "quadratic")
+    return float(np.sum(g * o))
+
+
+def fd_grads(orc, kind, q, k, v, g, lengths=None, h=1e-6):
+    """Central finite differences of L = sum(G * V') through the quadratic
+    forward (no gradient code involved)."""
+    out = []
+    for x in (q, k, v):
+        d = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            x0 = x[idx]
+            x[idx] = x0 + h
+            lp = _loss(orc, kind, q, k, v, g, lengths)
+            x[idx] = x0 - h
+            lm = _loss(orc, kind, q, k, v, g, lengths)
+            x[idx] = x0
+            d[idx] = (lp - lm) / (2 * h)
+        out.append(d)
+    return out
+
+
+def pin_grad_fd(orc):
+    """Both gradient forms (cumulative sums, eq. 13-15 with the quotient rule;
+    and the explicit pairwise form) match central finite differences."""
+    cases = [("causal", (1, 1, 6, 3, 4), None), ("causal", (1, 2, 5, 2, 3), None),
+             ("noncausal", (2, 1, 6, 3, 2), np.array([6, 4], dtype=np.int32))]
+    for n, (kind, (B, H, N, D, M), lengths) in enumerate(cases):
+        q, k = rand((B, H, N, D), 40 + n), rand((B, H, N, D), 50 + n)
+        v, g = rand((B, H, N, M), 60 + n), rand((B, H, N, M), 70 + n)
+        ref = fd_grads(orc, kind, q, k, v, g, lengths)
+        for form in ("recurrent", "quadratic"):
+            if kind == "causal":
+                got = orc.causal_bwd(q, k, v, g, form)
+            else:
+                got = orc.noncausal_bwd(q, k, v, g, lengths, form)
+            for name, a, r in zip("qkv", got, ref):
+                assert rel(a, r) < 1e-7, f"{kind} d{name} ({form}) != finite differences"
+
+
+def pin_grad_forms_agree(orc):
+    """Cumulative-sum gradients (eq. 13-15) equal the pairwise gradients on
+    larger inputs than finite differences can afford."""
+    for i, (B, H, N, D, M) in enumerate(RNG_SHAPES + [(1, 1, 64, 16, 16)]):
+        q, k = rand((B, H, N, D), 80 + i), rand((B, H, N, D), 81 + i)
+        v, g = rand((B, H, N, M), 82 + i), rand((B, H, N, M), 83 + i)
+        a = orc.causal_bwd(q, k, v, g, "recurrent")
+        b = orc.causal_bwd(q, k, v, g, "quadratic")
+        for x, y in zip(a, b):
+            assert rel(x, y, floor=1.0) < 1e-11, "causal gradient forms disagree"
+        lengths = np.full(B, max(N - 2, 0), dtype=np.int32)
+        a = orc.noncausal_bwd(q, k, v, g, lengths, "recurrent")
+        b = orc.noncausal_bwd(q, k, v, g, lengths, "quadratic")
+        for x, y in zip(a, b):
+            assert rel(x, y, floor=1.0) < 1e-11, "non-causal gradient forms disagree"
+
+
+def pin_grad_invariants(orc):
+    """Symmetries of the quotient, exact in exact arithmetic:
+      * V'_i is unchanged by scaling phi(Q_i), so phi(Q_i) . grad_phi(Q_i) = 0;
+      * V' is unchanged by scaling every phi(K_j) by one factor, so
+        sum_j phi(K_j) . grad_phi(K_j) = 0;
+      * adding one row c to every V_j adds c to every V'_i, so
+        sum_j grad V_j = sum_i G_i."""
+    B, H, N, D, M = 2, 2, 33, 5, 7
+    q, k = rand((B, H, N, D), 90), rand((B, H, N, D), 91)
+    v, g = rand((B, H, N, M), 92), rand((B, H, N, M), 93)
+    fq, dfq = orc.phi(q)
+    fk, dfk = orc.phi(k)
+    for form in ("recurrent", "quadratic"):
+        dq, dk, dv = orc.causal_bwd(q, k, v, g, form)
+        gq, gk = dq / dfq, dk / dfk
+        scale = np.max(np.abs(gq * fq))
+        assert np.max(np.abs(np.sum(fq * gq, axis=-1))) < 1e-12 * scale * D
+        assert np.max(np.abs(np.sum(fk * gk, axis=(-1, -2)))) < 1e-11 * np.max(np.abs(fk * gk)) * N
+        assert rel(dv.sum(axis=2), g.sum(axis=2)) < 1e-12
+
+
+# --------------------------------------------------------------------- decode
+
+def pin_decode(orc):
+    """RNN form (eq. 16-19) against the causal quadratic form on the stacked
+    sequence (the "transformers are RNNs" equivalence), the final state against
+    numpy products S_T = phi(K)^T V and Z_T = sum phi(K), and resuming from a
+    saved state against one uninterrupted run."""
+    T, B, H, D, M = 9, 2, 3, 4, 5
+    q, k, v = rand((T, B, H, D), 94), rand((T, B, H, D), 95), rand((T, B, H, M), 96)
+    y, S, Z = orc.decode(q, k, v)
+    perm = lambda x: np.ascontiguousarray(np.transpose(x, (1, 2, 0, 3)))  # -> [B,H,T,.]
+    oc, _ = orc.causal_fwd(perm(q), perm(k), perm(v), "quadratic")
+    assert rel(perm(y), oc) < 1e-13, "decode != causal forward"
+    fk = phi_lib(perm(k))
+    assert rel(S, np.matmul(np.swapaxes(fk, -1, -2), perm(v))) < 1e-13, "S_T != phi(K)^T V"
+    assert rel(Z, fk.sum(axis=2)) < 1e-14, "Z_T != sum phi(K)"
+    y1, S1, Z1 = orc.decode(q[:4], k[:4], v[:4])
+    y2, S2, Z2 = orc.decode(q[4:], k[4:], v[4:], S1, Z1)
+    assert np.array_equal(np.concatenate([y1, y2]), y), "resumed decode differs"
+    assert np.array_equal(S2, S) and np.array_equal(Z2, Z)
+
+
+ALL_PINS = [pin_phi, pin_causal_forms_agree, pin_causal_closed_forms, pin_grad_single_token, pin_noncausal_gemm,
+            pin_noncausal_last_row, pin_noncausal_lengths, pin_grad_fd, pin_grad_forms_agree,
+            pin_grad_invariants, pin_decode]

@@ -1,0 +1,56 @@
+"""Plant plausible slips in a copy of the oracle's C source and check that the
+pins catch every one (the pins would otherwise prove nothing).  CPU only: the
+mutated copies are built with gcc into a temporary directory."""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins as P
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, original text, replacement, which occurrence (0-based))
+MUTATIONS = [
+    ("phi_dropped_plus_one", "return x > 0.0 ? x + 1.0 : exp(x);", "return x > 0.0 ? x : exp(x);", 0),
+    ("dphi_zero_for_negative", "return x > 0.0 ? 1.0 : exp(x);", "return x > 0.0 ? 1.0 : 0.0;", 0),
+    ("quadratic_mask_strict", "for (int j = 0; j <= i; ++j) {\n        double a", "for (int j = 0; j < i; ++j) {\n        double a", 0),
+    ("recurrent_off_by_one_key", "        double fk = phi(K[(size_t)i * D + d]);\n        for (int m = 0; m < M; ++m) S[(size_t)d * M + m] += fk * V[(size_t)i * M + m];",
+     "        double fk = phi(K[(size_t)(i > 0 ? i - 1 : 0) * D + d]);\n        for (int m = 0; m < M; ++m) S[(size_t)d * M + m] += fk * V[(size_t)(i > 0 ? i - 1 : 0) * M + m];", 0),
+    ("bwd_dropped_denominator_term", "double acc = gam[i] * Z[d];", "double acc = 0.0;", 0),
+    ("bwd_gamma_sign", "gam[i] = -gv / s;", "gam[i] = gv / s;", 0),
+    ("bwd_dropped_r", "        double acc = r[d];\n        for (int m = 0; m < M; ++m) acc += R[(size_t)d * M + m] * V[(size_t)i * M + m];",
+     "        double acc = 0.0;\n        for (int m = 0; m < M; ++m) acc += R[(size_t)d * M + m] * V[(size_t)i * M + m];", 0),
+    ("bwd_dv_uses_phiq", "acc += R[(size_t)d * M + m] * phi(K[(size_t)i * D + d]);", "acc += R[(size_t)d * M + m] * phi(Q[(size_t)i * D + d]);", 0),
+    ("bwd_reverse_sweep_forward", "for (int i = N - 1; i >= 0; --i) {", "for (int i = 0; i < N; ++i) {", 0),
+    ("noncausal_ignores_length", "    for (int j = 0; j < L; ++j)\n      for (int d = 0; d < D; ++d) {\n        double fk", "    for (int j = 0; j < N; ++j)\n      for (int d = 0; d < D; ++d) {\n        double fk", 0),
+    ("noncausal_bwd_missing_gamma", "double gam = -gv / s;", "double gam = 0.0 * gv / s;", 0),
+    ("decode_no_denominator", "yt[m] = acc / den;", "yt[m] = acc;", 0),
+    ("decode_transposed_update", "s[(size_t)d * M + m] += fk * vt[m];", "s[(size_t)d * M + m] += fk * vt[d % M];", 0),
+]
+
+
+def _mutate(src, old, new, occ):
+    pos = -1
+    for _ in range(occ + 1):
+        pos = src.find(old, pos + 1)
+        assert pos >= 0, f"mutation anchor not found: {old!r}"
+    return src[:pos] + new + src[pos + len(old):]
+
+
+@pytest.mark.parametrize("name,old,new,occ", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_mutation(tmp_path, name, old, new, occ):
+    src = open(SRC).read()
+    mutated = _mutate(src, old, new, occ)
+    assert mutated != src
+    c = tmp_path / "oracle_mut.c"
+    c.write_text(mutated)
+    lib = oracle.compile_c(str(c), str(tmp_path / "liboracle_mut.so"))
+    orc = oracle.Oracle(lib)
+    failed = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, FloatingPointError, ValueError) as e:
+            failed.append(pin.__name__)
+    assert failed, f"mutation {name} passed every pin"
