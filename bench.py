@@ -1,0 +1,480 @@
+#!/usr/bin/env python3
+"""Benchmark of the causal linear-attention training step on GB300.
+
+One step = one causal forward (la_causal_fwd) plus one causal backward
+(la_causal_bwd) through the C ABI over a batch of B=4 sequences x H=8 heads of
+N=3072 tokens with D=M=64, bf16 in and out, fp32 accumulation (the 32x32x3
+autoregressive-image workload of "Transformers are RNNs").  Inputs are seeded
+N(0, 1) draws, resident in HBM before the timed region; L2 is flushed (a
+256 MiB write) before every timed step, outside the step's events.
+
+Prints one JSON line.  `value` is tokens/s = B*N / (device time of one step),
+summed over ranks (independent replicas, weak scaling).  Extra objects:
+  roofline      the dominant call (la_causal_bwd), algorithmic bytes per call /
+                its live CUDA-event duration, against the measured HBM copy rate
+  cpu_baseline  the fp64 CPU oracle (recurrent form, fwd+bwd) on the host cores
+  e2e           the same step with pinned host buffers and the copies inside
+  secondary     non-causal fwd+bwd and decode-step measurements
+  clocks        nvidia-smi samples taken during the timed region
+
+`--impl reference` times the CPU oracle itself (rank 0 only) on the same
+workload, one bounded sample per step.
+
+Multi-GPU (torchrun, one process per GPU): every rank runs the same workload
+on its own GPU; there is no collective on the data path (the sequences are
+independent); timing is the max over ranks between barriers.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal linear-attn fwd+bwd tokens/s (N=3072, D=M=64) and % of roofline"
+WORKLOAD = "causal_cifar_bf16"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the non-causal/decode lines")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ plumbing
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend, rank=self.rank, world_size=self.world)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float, device=None) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons, n = [], None, set(), 0
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            n += 1
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def kernel_source_hash():
+    """Hash of the CUDA sources, to tell whether stored ncu counters still
+    describe the kernels being timed."""
+    csrc = os.path.join(ROOT, "kernelized_causal_attention_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel_key):
+    """DRAM bytes per call from the committed ncu summary, or None when the
+    kernels changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        d = json.load(open(p))
+    except (OSError, ValueError):
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get("per_call_dram_bytes", {}).get(kernel_key)
+
+
+# ------------------------------------------------------------- byte counting
+
+def causal_bytes(B, H, N, D, M, elt):
+    """Algorithmic bytes per call (recurrence form: every input read once and
+    every output written once)."""
+    th = B * H * N
+    fwd = th * (elt * (2 * D + M) + elt * M + 4)                   # q,k,v in; out, den out
+    bwd = th * (elt * (2 * D + M) + 2 * elt * M + 4 + elt * (2 * D + M))  # q,k,v,out,dout,den; dq,dk,dv
+    return fwd, bwd
+
+
+# ------------------------------------------------------------------ our arm
+
+def time_calls(fns, steps, flush, torch, dist, dev):
+    """Runs `steps` iterations of the call sequence `fns`, with an L2 flush
+    before each; returns per-call mean ms and per-step mean ms (device time)."""
+    n = len(fns)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        ev[i][0].record()
+        for j, fn in enumerate(fns):
+            fn()
+            ev[i][j + 1].record()
+    torch.cuda.synchronize()
+    per_call = [statistics.fmean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
+                for j in range(n)]
+    per_step = statistics.fmean(ev[i][0].elapsed_time(ev[i][n]) for i in range(steps))
+    return per_call, per_step
+
+
+def run_ours(args, dist):
+    import torch
+
+    import kernelized_causal_attention_gb300 as la
+    from kernelized_causal_attention_gb300.workloads import WORKLOADS, causal_inputs
+
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    dist.init("nccl" if dist.world > 1 else "gloo")
+    la.lib()
+    w = WORKLOADS[WORKLOAD]
+    B, H, N, D, M = w.B, w.H, w.N, w.D, w.M
+    dt = la.LA_BF16
+    q, k, v, g = causal_inputs(B, H, N, D, M, w.dtype, w.seed + dist.rank * 1000)
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+    out = torch.empty(B, H, N, M, dtype=torch.bfloat16, device=dev)
+    den = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    wsf = la.workspace(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, dt, dev)
+    wsb = la.workspace(la.LA_OP_CAUSAL_BWD, B, H, N, D, M, dt, dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.zero_()
+
+    fwd = lambda: la.la_causal_fwd(qd, kd, vd, out, den, wsf, B, H, N, D, M, dt)
+    bwd = lambda: la.la_causal_bwd(qd, kd, vd, out, den, gd, dq, dk, dv, wsb, B, H, N, D, M, dt)
+
+    for _ in range(max(3, args.warmup)):
+        flush()
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    (ms_fwd, ms_bwd), ms_step = time_calls([fwd, bwd], args.steps, flush, torch, dist, dev)
+    torch.cuda.synchronize()
+    dist.barrier()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+
+    ms_step_max = dist.max(ms_step, dev)
+    ms_bwd_max = dist.max(ms_bwd, dev)
+    ms_fwd_max = dist.max(ms_fwd, dev)
+    tokens = B * N
+    value = dist.world * tokens / (ms_step_max / 1e3)
+    launches = args.steps * (la.la_kernel_launches(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, dt)
+                             + la.la_kernel_launches(la.LA_OP_CAUSAL_BWD, B, H, N, D, M, dt))
+
+    peaks = measured_peaks()
+    fwd_b, bwd_b = causal_bytes(B, H, N, D, M, 2)
+    achieved = bwd_b / (ms_bwd_max / 1e3) / 1e9
+    traffic = stored_traffic("la_causal_bwd")
+    roofline = {"bound": "hbm", "kernel": "la_causal_bwd", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": traffic, "alg_bytes": bwd_b, "ms": round(ms_bwd_max, 5),
+                "peak_source": peaks["source"]}
+    step_alg = (fwd_b + bwd_b) / (ms_step_max / 1e3) / 1e9
+    step_roof = {"alg_bytes": fwd_b + bwd_b, "achieved_gbs": round(step_alg, 1),
+                 "frac": round(step_alg / peaks["hbm_gbs"], 4), "fwd_ms": round(ms_fwd_max, 5),
+                 "fwd_gbs": round(fwd_b / (ms_fwd_max / 1e3) / 1e9, 1)}
+
+    e2e = measure_e2e(la, torch, dev, q, k, v, g, out, den, wsf, wsb, B, H, N, D, M, dt,
+                      max(3, min(args.steps, 200)), flush, dist)
+
+    res = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": dist.world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 5),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic",
+           "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "M": M,
+                      "in_dtype": "bf16", "accumulate": "fp32", "global_batch": B * dist.world,
+                      "seq_len": N, "parallelism": f"replicas{dist.world}",
+                      "l2": "flushed before every timed step (256 MiB write, untimed)"},
+           "roofline": roofline, "step_roofline": step_roof, "e2e": e2e,
+           "gpu_launches": launches, "clocks": clk, "wall_s_timed_region": round(wall, 3)}
+    if not args.no_secondary:
+        res["secondary"] = secondary(la, torch, dev, flush, peaks)
+    if dist.rank == 0 and not args.no_cpu:
+        res["cpu_baseline"] = cpu_baseline(q, k, v, g, B, H, N)
+    dist.close()
+    return res
+
+
+def measure_e2e(la, torch, dev, q, k, v, g, out, den, wsf, wsb, B, H, N, D, M, dt, steps, flush,
+                dist):
+    """The step through the public API with pinned host inputs and results:
+    H2D of q, k, v, dout, both calls, D2H of dq, dk, dv, all on one stream."""
+    hq, hk, hv, hg = (t.pin_memory() for t in (q, k, v, g))
+    dq_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    dk_h = torch.empty(k.shape, dtype=k.dtype).pin_memory()
+    dv_h = torch.empty(v.shape, dtype=v.dtype).pin_memory()
+    dq_, dk_, dv_ = (torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (q, k, v))
+    qd, kd, vd, gd = (torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (q, k, v, g))
+
+    def step():
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        gd.copy_(hg, non_blocking=True)
+        la.la_causal_fwd(qd, kd, vd, out, den, wsf, B, H, N, D, M, dt)
+        la.la_causal_bwd(qd, kd, vd, out, den, gd, dq_, dk_, dv_, wsb, B, H, N, D, M, dt)
+        dq_h.copy_(dq_, non_blocking=True)
+        dk_h.copy_(dk_, non_blocking=True)
+        dv_h.copy_(dv_, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    _, ms = time_calls([step], steps, flush, torch, dist, dev)
+    ms = dist.max(ms, dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
+    d2h = sum(t.numel() * t.element_size() for t in (dq_h, dk_h, dv_h))
+    return {"value": round(dist.world * B * N / (ms / 1e3), 1), "unit": "tokens/s",
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def secondary(la, torch, dev, flush, peaks):
+    """Non-causal fwd+bwd (long speech-like sequences with padding) and the
+    decode step (256 and 2048 streams x 8 heads), each against its roofline."""
+    from kernelized_causal_attention_gb300.workloads import WORKLOADS, noncausal_inputs
+    res = {}
+    w = WORKLOADS["noncausal_speech_f32"]
+    B, H, N, D, M = w.B, w.H, w.N, w.D, w.M
+    lengths, q, k, v, g = noncausal_inputs(B, H, N, D, M, w.dtype, w.seed, w.len_range)
+    qd, kd, vd, gd, ld = (t.to(dev) for t in (q, k, v, g, lengths))
+    out = torch.empty_like(vd)
+    den = torch.empty(B, H, N, device=dev)
+    S = torch.empty(B, H, D, M, device=dev)
+    Z = torch.empty(B, H, D, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    wf = la.workspace(la.LA_OP_NONCAUSAL_FWD, B, H, N, D, M, 0, dev)
+    wb = la.workspace(la.LA_OP_NONCAUSAL_BWD, B, H, N, D, M, 0, dev)
+    fwd = lambda: la.la_noncausal_fwd(qd, kd, vd, ld, out, den, S, Z, wf, B, H, N, D, M, 0)
+    bwd = lambda: la.la_noncausal_bwd(qd, kd, vd, ld, out, den, S, Z, gd, dq, dk, dv, wb, B, H, N,
+                                      D, M, 0)
+    for _ in range(3):
+        fwd()
+        bwd()
+    (mf, mb), ms = time_calls([fwd, bwd], 50, flush, torch, None, dev)
+    valid = int(lengths.sum()) * H  # valid token-heads
+    alg = valid * (4 * (2 * D + M) + 4 * M + 4) + valid * (4 * (2 * D + M) + 8 * M + 4 + 4 * (2 * D + M))
+    flops = valid * 12 * D * M
+    gbs = alg / (ms / 1e3) / 1e9
+    res["noncausal_speech_f32"] = {
+        "value": round(int(lengths.sum()) / (ms / 1e3), 1), "unit": "valid tokens/s",
+        "ms_per_step": round(ms, 5), "fwd_ms": round(mf, 5), "bwd_ms": round(mb, 5),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": alg},
+        "fp32_tflops": round(flops / (ms / 1e3) / 1e12, 2)}
+
+    for Bd in (256, 2048):
+        Hd, Dd, Md = 8, 64, 64
+        S = torch.zeros(Bd, Hd, Dd, Md, device=dev)
+        Z = torch.ones(Bd, Hd, Dd, device=dev)
+        gen = torch.Generator(device="cpu").manual_seed(5)
+        qd = torch.randn(Bd, Hd, Dd, generator=gen).to(dev)
+        kd = torch.randn(Bd, Hd, Dd, generator=gen).to(dev)
+        vd = torch.randn(Bd, Hd, Md, generator=gen).to(dev)
+        y = torch.empty(Bd, Hd, Md, device=dev)
+        stepf = lambda: la.la_decode_step(qd, kd, vd, S, Z, y, Bd, Hd, Dd, Md, 0)
+        per = 64  # steps per CUDA graph replay
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                stepf()
+        torch.cuda.current_stream().wait_stream(s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(per):
+                stepf()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * per)
+        alg = Bd * Hd * (2 * 4 * Dd * Md + 2 * 4 * Dd + 4 * (2 * Dd) + 4 * 2 * Md)
+        gbs = alg / (us / 1e6) / 1e9
+        res[f"decode_f32_B{Bd}"] = {
+            "us_per_step": round(us, 3), "unit": "us/step",
+            "stream_tokens_per_s": round(Bd * Hd / (us / 1e6), 1),
+            "state_bytes": Bd * Hd * (Dd * Md + Dd) * 4,
+            "l2_resident": Bd * Hd * (Dd * Md + Dd) * 4 < 100e6,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": alg},
+            "timing": "CUDA graph of 64 steps, 20 replays, state kept warm"}
+    return res
+
+
+# -------------------------------------------------------------- CPU oracle
+
+def _cores(orc_mod):
+    return orc_mod.default_threads() if orc_mod.openmp_enabled() else 1
+
+
+def cpu_baseline(q, k, v, g, B, H, N, budget_s=12.0):
+    """The fp64 oracle as it stands (recurrent form, fwd then bwd) on all host
+    cores, repeated over the full workload until about `budget_s` seconds."""
+    import oracle
+    cores = _cores(oracle)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.causal_fwd(q, k, v, "recurrent", nthreads=cores)
+        oracle.causal_bwd(q, k, v, g, "recurrent", nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return {"value": round(reps * B * N / el, 1), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"full workload (B={B}, H={H}, N={N}) x {reps} repetitions, "
+                      f"{el:.1f} s, fp64 recurrent form, fwd+bwd"}
+
+
+def run_reference(args, dist):
+    """The CPU oracle as the reference arm: rank 0 times K steps, each a
+    bounded sample of the workload (whole heads of the N=3072 sequences)."""
+    if dist.rank != 0:
+        return None
+    import oracle
+    from kernelized_causal_attention_gb300.workloads import WORKLOADS, causal_inputs
+    w = WORKLOADS[WORKLOAD]
+    B, H, N, D, M = w.B, w.H, w.N, w.D, w.M
+    q, k, v, g = causal_inputs(B, H, N, D, M, w.dtype, w.seed)
+    cores = _cores(oracle)
+    # calibrate: one head
+    t0 = time.perf_counter()
+    oracle.causal_fwd(q[:1, :1], k[:1, :1], v[:1, :1], "recurrent", nthreads=1)
+    oracle.causal_bwd(q[:1, :1], k[:1, :1], v[:1, :1], g[:1, :1], "recurrent", nthreads=1)
+    per_head_1core = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)  # whole run within ~2.5 minutes
+    heads = int(max(1, min(B * H, budget * cores / max(per_head_1core, 1e-6))))
+    qs, ks, vs, gs = (t.reshape(1, B * H, N, -1)[:, :heads].contiguous() for t in (q, k, v, g))
+    step = lambda: (oracle.causal_fwd(qs, ks, vs, "recurrent", nthreads=cores),
+                    oracle.causal_bwd(qs, ks, vs, gs, "recurrent", nthreads=cores))
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    ms = statistics.fmean(times) * 1e3
+    tokens = heads * N / H  # a sample of whole heads counts as that fraction of the batch
+    value = tokens / (ms / 1e3)
+    sample = f"{heads} of {B * H} heads x N={N} per step (fp64 recurrent form, fwd+bwd)"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "M": M},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    dist = Dist()
+    if args.impl == "reference":
+        res = run_reference(args, dist)
+    else:
+        res = run_ours(args, dist)
+    if res is not None and dist.rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,142 @@
+/*
+ * linattn.h -- C ABI of the GB300 (sm_103a) elu(x)+1 linear-attention library.
+ *
+ * The operations are those of Katharopoulos et al., "Transformers are RNNs:
+ * Fast Autoregressive Transformers with Linear Attention" (part 2/3 of the
+ * paper text): the feature map phi(x) = elu(x) + 1 (eq. 7), causal linear
+ * attention (§3.3, eq. 9-12), its cumulative-sum gradients (§3.3.1,
+ * eq. 13-15, completed with the denominator by the quotient rule), the
+ * non-causal form with one shared S and Z ("Linear Attention/zh", kernel
+ * reformulation), and the RNN-form decode step (§3.4, eq. 16-19).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pointers named q, k, v, out, dout, dq, dk, dv, den, S, Z, lengths and
+ *    workspace are DEVICE pointers (or managed memory) of the current CUDA
+ *    device.  The caller owns every buffer; the library never allocates,
+ *    frees or retains memory and keeps no state between calls.
+ *  - Layouts are dense row-major: q, k, dq, dk [B][H][N][D]; v, out, dout, dv
+ *    [B][H][N][M]; den [B][H][N]; S [B][H][D][M]; Z [B][H][D]; lengths [B].
+ *    Decode tensors drop N: q, k [B][H][D], v, y [B][H][M].
+ *  - dtype selects the element type of q, k, v, out, dout, dq, dk, dv and y:
+ *    LA_F32 (float) or LA_BF16 (bfloat16).  den, S and Z are always float.
+ *    Arithmetic accumulates in fp32.  The feature map uses no 1/sqrt(D)
+ *    temperature and the denominator no epsilon.
+ *  - Every pointer must be 16-byte aligned.  Supported head sizes: D and M in
+ *    {16, 32, 64}.  Limits: 1 <= B*H <= 2^20, 1 <= N <= 2^24.
+ *  - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls are asynchronous on it; results are ready when the
+ *    stream reaches them.  Calls that share a workspace must be ordered.
+ *  - Return value: LA_OK, or an error code.  Argument errors are detected on
+ *    the host before anything is launched, so nothing was written.
+ *    LA_ERR_CUDA reports a launch failure (cudaGetLastError after the
+ *    launch).  The library never prints, exits or aborts.
+ *  - Workspace: calls that take `workspace` need at least
+ *    la_workspace_bytes(op, ...) bytes of device scratch (may be NULL when
+ *    that size is 0).  Its contents on entry do not matter and are garbage on
+ *    return.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define LA_OK 0
+#define LA_ERR_INVALID_ARG 1 /* null/misaligned pointer, bad size, bad dtype */
+#define LA_ERR_UNSUPPORTED 2 /* valid but unsupported (D or M not in the set) */
+#define LA_ERR_CUDA 3        /* a CUDA launch or runtime call failed */
+#define LA_ERR_WORKSPACE 4   /* workspace missing or smaller than required */
+
+/* element types */
+#define LA_F32 0
+#define LA_BF16 1
+
+/* operation ids for la_workspace_bytes */
+#define LA_OP_CAUSAL_FWD 0
+#define LA_OP_CAUSAL_BWD 1
+#define LA_OP_NONCAUSAL_FWD 2
+#define LA_OP_NONCAUSAL_BWD 3
+#define LA_OP_DECODE 4
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* la_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+int la_version(void);
+
+/* Bytes of device workspace the operation needs for these sizes; 0 when it
+ * needs none or when the arguments are invalid. */
+size_t la_workspace_bytes(int op, int B, int H, int N, int D, int M, int dtype);
+
+/* Number of kernel launches one call of `op` makes for these sizes (for
+ * launch accounting by callers and benchmarks); 0 for invalid arguments. */
+int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype);
+
+/*
+ * Causal forward, eq. 9-12:
+ *   S_i = sum_{j<=i} phi(K_j) V_j^T,  Z_i = sum_{j<=i} phi(K_j),
+ *   out_i = phi(Q_i)^T S_i / phi(Q_i)^T Z_i,   den_i = phi(Q_i)^T Z_i.
+ * Inputs q, k, v; outputs out (dtype) and den (float, may be NULL when no
+ * backward pass follows; la_causal_bwd needs it).
+ */
+int la_causal_fwd(const void* q, const void* k, const void* v, void* out, float* den,
+                  void* workspace, size_t workspace_bytes, int B, int H, int N, int D,
+                  int M, int dtype, void* stream);
+
+/*
+ * Causal backward: gradients of L = sum_i dout_i . out_i with respect to q, k
+ * and v, by the cumulative sums of eq. 13-15 (forward sum of S for dq,
+ * reverse sums of phi(Q) (dout/den)^T for dk and dv) plus the denominator
+ * terms.  No S_i is stored.  out and den are the forward's outputs.
+ * Outputs dq, dk (dtype, [B][H][N][D]) and dv ([B][H][N][M]).
+ */
+int la_causal_bwd(const void* q, const void* k, const void* v, const void* out,
+                  const float* den, const void* dout, void* dq, void* dk, void* dv,
+                  void* workspace, size_t workspace_bytes, int B, int H, int N, int D,
+                  int M, int dtype, void* stream);
+
+/*
+ * Non-causal forward with one shared state per (b, h):
+ *   S = sum_{j<L_b} phi(K_j) V_j^T,  Z = sum_{j<L_b} phi(K_j),
+ *   out_i = phi(Q_i)^T S / phi(Q_i)^T Z  for i < L_b, and 0 for i >= L_b.
+ * lengths: device int32 [B] of valid lengths (values are clamped to [0, N]),
+ * or NULL for "all N".  Outputs out, den (0 on padded rows), S and Z (both
+ * required: the backward pass reads them).
+ */
+int la_noncausal_fwd(const void* q, const void* k, const void* v, const int* lengths,
+                     void* out, float* den, float* S, float* Z, void* workspace,
+                     size_t workspace_bytes, int B, int H, int N, int D, int M, int dtype,
+                     void* stream);
+
+/*
+ * Non-causal backward: gradients of L = sum_i dout_i . out_i over the valid
+ * rows; eq. 13-15 with full sums in place of cumulative ones.  Padded rows
+ * of dq, dk, dv are written as 0.  out, den, S, Z come from la_noncausal_fwd.
+ */
+int la_noncausal_bwd(const void* q, const void* k, const void* v, const int* lengths,
+                     const void* out, const float* den, const float* S, const float* Z,
+                     const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                     size_t workspace_bytes, int B, int H, int N, int D, int M, int dtype,
+                     void* stream);
+
+/*
+ * One RNN decode step for B*H independent streams, eq. 16-19 (state update,
+ * then read-out; the layer's f_l and residual of eq. 20 are not applied):
+ *   S <- S + phi(k) v^T,  Z <- Z + phi(k),  y = phi(q)^T S / phi(q)^T Z.
+ * S [B][H][D][M] and Z [B][H][D] are read and updated in place (start from
+ * zeros for eq. 16-17).  q, k [B][H][D], v and y [B][H][M] in dtype.
+ * Needs no workspace.
+ */
+int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z,
+                   void* y, int B, int H, int D, int M, int dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */

@@ -1,0 +1,267 @@
+"""GB300 (sm_103a) elu(x)+1 linear attention: Python binding of the C ABI.
+
+This module only marshals arguments: it loads ``_lib/liblinattn.so`` (built by
+``_build.py``), passes tensor data pointers and the current CUDA stream to the
+C entry points declared in ``include/linattn.h``, and turns error codes into
+exceptions.  Every step of the computation runs in the library's CUDA
+kernels; there is no fallback of any kind, and using any entry point without
+the built library raises.
+
+Raw entry points (same names and argument order as the C ABI, tensors in
+place of pointers): ``la_causal_fwd``, ``la_causal_bwd``, ``la_noncausal_fwd``,
+``la_noncausal_bwd``, ``la_decode_step``, ``la_workspace_bytes``.
+Convenience wrappers that allocate outputs with torch: ``causal_fwd``,
+``causal_bwd``, ``noncausal_fwd``, ``noncausal_bwd``, ``decode_step`` and the
+autograd functions ``causal_linear_attention`` / ``noncausal_linear_attention``.
+
+The method is Katharopoulos et al., "Transformers are RNNs" (part 2/3):
+eq. 7 (phi), §3.3 eq. 9-12, §3.3.1 eq. 13-15, §3.4 eq. 16-19.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "liblinattn.so")
+
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_WORKSPACE = 0, 1, 2, 3, 4
+LA_F32, LA_BF16 = 0, 1
+LA_OP_CAUSAL_FWD, LA_OP_CAUSAL_BWD, LA_OP_NONCAUSAL_FWD, LA_OP_NONCAUSAL_BWD, LA_OP_DECODE = range(5)
+
+# exported symbols and their ctypes signatures ("p" pointer, "i" int, "z" size_t)
+_SIGS = {
+    "la_status_string": ("i", ctypes.c_char_p),
+    "la_version": ("", ctypes.c_int),
+    "la_workspace_bytes": ("i i i i i i i", ctypes.c_size_t),
+    "la_kernel_launches": ("i i i i i i i", ctypes.c_int),
+    "la_causal_fwd": ("p p p p p p z i i i i i i p", ctypes.c_int),
+    "la_causal_bwd": ("p p p p p p p p p p z i i i i i i p", ctypes.c_int),
+    "la_noncausal_fwd": ("p p p p p p p p p z i i i i i i p", ctypes.c_int),
+    "la_noncausal_bwd": ("p p p p p p p p p p p p p z i i i i i i p", ctypes.c_int),
+    "la_decode_step": ("p p p p p p i i i i i p", ctypes.c_int),
+}
+EXPORTED = tuple(_SIGS)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (code {code})")
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def lib():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"CUDA library not built: {LIB_PATH} is missing. Build it with "
+                    "`python -m kernelized_causal_attention_gb300._build` (needs nvcc).")
+            h = ctypes.CDLL(LIB_PATH)
+            kinds = {"p": ctypes.c_void_p, "i": ctypes.c_int, "z": ctypes.c_size_t}
+            for name, (sig, res) in _SIGS.items():
+                fn = getattr(h, name)
+                fn.argtypes = [kinds[c] for c in sig.split()]
+                fn.restype = res
+            _lib = h
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().la_status_string(int(code)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return LA_F32
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        return int(t)  # a raw address
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(rc: int, where: str):
+    if rc != LA_OK:
+        raise LinAttnError(rc, where)
+
+
+def _nbytes(ws):
+    return 0 if ws is None else ws.numel() * ws.element_size()
+
+
+# ------------------------------------------------------------------ raw C ABI
+
+def la_workspace_bytes(op, B, H, N, D, M, dtype) -> int:
+    return int(lib().la_workspace_bytes(op, B, H, N, D, M, dtype))
+
+
+def la_kernel_launches(op, B, H, N, D, M, dtype) -> int:
+    return int(lib().la_kernel_launches(op, B, H, N, D, M, dtype))
+
+
+def la_causal_fwd(q, k, v, out, den, workspace, B, H, N, D, M, dtype, stream=None):
+    _check(lib().la_causal_fwd(_p(q), _p(k), _p(v), _p(out), _p(den), _p(workspace),
+                               _nbytes(workspace), B, H, N, D, M, dtype, _stream(stream)),
+           "la_causal_fwd")
+
+
+def la_causal_bwd(q, k, v, out, den, dout, dq, dk, dv, workspace, B, H, N, D, M, dtype,
+                  stream=None):
+    _check(lib().la_causal_bwd(_p(q), _p(k), _p(v), _p(out), _p(den), _p(dout), _p(dq), _p(dk),
+                               _p(dv), _p(workspace), _nbytes(workspace), B, H, N, D, M, dtype,
+                               _stream(stream)), "la_causal_bwd")
+
+
+def la_noncausal_fwd(q, k, v, lengths, out, den, S, Z, workspace, B, H, N, D, M, dtype,
+                     stream=None):
+    _check(lib().la_noncausal_fwd(_p(q), _p(k), _p(v), _p(lengths), _p(out), _p(den), _p(S),
+                                  _p(Z), _p(workspace), _nbytes(workspace), B, H, N, D, M, dtype,
+                                  _stream(stream)), "la_noncausal_fwd")
+
+
+def la_noncausal_bwd(q, k, v, lengths, out, den, S, Z, dout, dq, dk, dv, workspace, B, H, N, D,
+                     M, dtype, stream=None):
+    _check(lib().la_noncausal_bwd(_p(q), _p(k), _p(v), _p(lengths), _p(out), _p(den), _p(S),
+                                  _p(Z), _p(dout), _p(dq), _p(dk), _p(dv), _p(workspace),
+                                  _nbytes(workspace), B, H, N, D, M, dtype, _stream(stream)),
+           "la_noncausal_bwd")
+
+
+def la_decode_step(q, k, v, S, Z, y, B, H, D, M, dtype, stream=None):
+    _check(lib().la_decode_step(_p(q), _p(k), _p(v), _p(S), _p(Z), _p(y), B, H, D, M, dtype,
+                                _stream(stream)), "la_decode_step")
+
+
+# --------------------------------------------------- allocating convenience API
+
+def workspace(op, B, H, N, D, M, dtype, device):
+    n = la_workspace_bytes(op, B, H, N, D, M, dtype)
+    return None if n == 0 else torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def causal_fwd(q, k, v, stream=None):
+    """(out, den) of the causal form; q, k [B,H,N,D], v [B,H,N,M] on the GPU."""
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    out = torch.empty(B, H, N, M, dtype=q.dtype, device=q.device)
+    den = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+    ws = workspace(LA_OP_CAUSAL_FWD, B, H, N, D, M, dt, q.device)
+    la_causal_fwd(q, k, v, out, den, ws, B, H, N, D, M, dt, stream)
+    return out, den
+
+
+def causal_bwd(q, k, v, out, den, dout, stream=None):
+    """(dq, dk, dv) of sum(dout * out) for the causal form."""
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = workspace(LA_OP_CAUSAL_BWD, B, H, N, D, M, dt, q.device)
+    la_causal_bwd(q, k, v, out, den, dout, dq, dk, dv, ws, B, H, N, D, M, dt, stream)
+    return dq, dk, dv
+
+
+def noncausal_fwd(q, k, v, lengths=None, stream=None):
+    """(out, den, S, Z) of the non-causal form; lengths: int32 [B] on the GPU or None."""
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    out = torch.empty(B, H, N, M, dtype=q.dtype, device=q.device)
+    den = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+    S = torch.empty(B, H, D, M, dtype=torch.float32, device=q.device)
+    Z = torch.empty(B, H, D, dtype=torch.float32, device=q.device)
+    ws = workspace(LA_OP_NONCAUSAL_FWD, B, H, N, D, M, dt, q.device)
+    la_noncausal_fwd(q, k, v, lengths, out, den, S, Z, ws, B, H, N, D, M, dt, stream)
+    return out, den, S, Z
+
+
+def noncausal_bwd(q, k, v, lengths, out, den, S, Z, dout, stream=None):
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = workspace(LA_OP_NONCAUSAL_BWD, B, H, N, D, M, dt, q.device)
+    la_noncausal_bwd(q, k, v, lengths, out, den, S, Z, dout, dq, dk, dv, ws, B, H, N, D, M, dt,
+                     stream)
+    return dq, dk, dv
+
+
+def decode_step(q, k, v, S, Z, stream=None):
+    """One RNN step; S [B,H,D,M] and Z [B,H,D] (float32) are updated in place.
+    Returns y [B,H,M]."""
+    B, H, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    y = torch.empty(B, H, M, dtype=q.dtype, device=q.device)
+    la_decode_step(q, k, v, S, Z, y, B, H, D, M, dt, stream)
+    return y
+
+
+class _Causal(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        out, den = causal_fwd(q, k, v)
+        ctx.save_for_backward(q, k, v, out, den)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, den = ctx.saved_tensors
+        return causal_bwd(q, k, v, out, den, dout.contiguous())
+
+
+class _NonCausal(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, lengths):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        out, den, S, Z = noncausal_fwd(q, k, v, lengths)
+        ctx.save_for_backward(q, k, v, out, den, S, Z)
+        ctx.lengths = lengths
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, den, S, Z = ctx.saved_tensors
+        dq, dk, dv = noncausal_bwd(q, k, v, ctx.lengths, out, den, S, Z, dout.contiguous())
+        return dq, dk, dv, None
+
+
+def causal_linear_attention(q, k, v):
+    """Causal elu+1 linear attention with the constant-memory backward."""
+    return _Causal.apply(q, k, v)
+
+
+def noncausal_linear_attention(q, k, v, lengths=None):
+    """Non-causal elu+1 linear attention (shared S, Z per sequence)."""
+    return _NonCausal.apply(q, k, v, lengths)

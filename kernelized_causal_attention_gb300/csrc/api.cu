@@ -1,0 +1,162 @@
+// C ABI of the library (declared in include/linattn.h): argument checks,
+// workspace sizing and dispatch to the kernel launchers.  Nothing here
+// allocates device memory, prints or aborts.
+#include <stdint.h>
+
+#include <initializer_list>
+
+#include "../../include/linattn.h"
+#include "launch.h"
+
+namespace {
+
+using la::Shape;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_dim(int x) { return x == 16 || x == 32 || x == 64; }
+
+// Checks shared by the sequence calls; returns LA_OK or the error code.
+int check_shape(int B, int H, int N, int D, int M, int dtype) {
+  if (B < 1 || H < 1 || N < 1) return LA_ERR_INVALID_ARG;
+  if ((long long)B * H > (1ll << 20) || N > (1 << 24)) return LA_ERR_INVALID_ARG;
+  if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+  if (D < 1 || M < 1) return LA_ERR_INVALID_ARG;
+  if (!supported_dim(D) || !supported_dim(M)) return LA_ERR_UNSUPPORTED;
+  return LA_OK;
+}
+
+// Every listed pointer must be non-null and 16-byte aligned.
+int check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p == nullptr || !aligned16(p)) return LA_ERR_INVALID_ARG;
+  return LA_OK;
+}
+
+int check_opt_ptr(const void* p) { return (p == nullptr || aligned16(p)) ? LA_OK : LA_ERR_INVALID_ARG; }
+
+size_t ws_bytes(int op, const Shape& s) {
+  switch (op) {
+    case LA_OP_CAUSAL_FWD: return 4 * la::causal_fwd_ws_floats(s);
+    case LA_OP_CAUSAL_BWD: return 4 * la::causal_bwd_ws_floats(s);
+    case LA_OP_NONCAUSAL_FWD: return 4 * la::noncausal_fwd_ws_floats(s);
+    case LA_OP_NONCAUSAL_BWD: return 4 * la::noncausal_bwd_ws_floats(s);
+    default: return 0;
+  }
+}
+
+int check_ws(int op, const Shape& s, const void* ws, size_t bytes) {
+  const size_t need = ws_bytes(op, s);
+  if (need == 0) return LA_OK;
+  if (ws == nullptr || bytes < need) return LA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LA_ERR_INVALID_ARG;
+  return LA_OK;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+}  // namespace
+
+#define LA_TRY(x)              \
+  do {                         \
+    const int rc_ = (x);       \
+    if (rc_ != LA_OK) return rc_; \
+  } while (0)
+
+extern "C" {
+
+const char* la_status_string(int status) {
+  switch (status) {
+    case LA_OK: return "ok";
+    case LA_ERR_INVALID_ARG: return "invalid argument";
+    case LA_ERR_UNSUPPORTED: return "unsupported head size";
+    case LA_ERR_CUDA: return "CUDA error";
+    case LA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int la_version(void) { return 100; }
+
+size_t la_workspace_bytes(int op, int B, int H, int N, int D, int M, int dtype) {
+  if (op == LA_OP_DECODE) return 0;
+  if (check_shape(B, H, N, D, M, dtype) != LA_OK) return 0;
+  return ws_bytes(op, Shape{B, H, N, D, M, dtype});
+}
+
+int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype) {
+  if (check_shape(B, H, op == LA_OP_DECODE ? 1 : N, D, M, dtype) != LA_OK) return 0;
+  const Shape s{B, H, N, D, M, dtype};
+  switch (op) {
+    case LA_OP_CAUSAL_FWD: return la::causal_fwd_launches(s);
+    case LA_OP_CAUSAL_BWD: return la::causal_bwd_launches(s);
+    case LA_OP_NONCAUSAL_FWD: return la::noncausal_fwd_launches(s);
+    case LA_OP_NONCAUSAL_BWD: return la::noncausal_bwd_launches(s);
+    case LA_OP_DECODE: return 1;
+    default: return 0;
+  }
+}
+
+int la_causal_fwd(const void* q, const void* k, const void* v, void* out, float* den,
+                  void* workspace, size_t workspace_bytes, int B, int H, int N, int D, int M,
+                  int dtype, void* stream) {
+  LA_TRY(check_shape(B, H, N, D, M, dtype));
+  LA_TRY(check_ptrs({q, k, v, out}));
+  LA_TRY(check_opt_ptr(den));
+  const Shape s{B, H, N, D, M, dtype};
+  LA_TRY(check_ws(LA_OP_CAUSAL_FWD, s, workspace, workspace_bytes));
+  return from_cuda(la::causal_fwd_cc(q, k, v, out, den, static_cast<float*>(workspace), s,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int la_causal_bwd(const void* q, const void* k, const void* v, const void* out, const float* den,
+                  const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                  size_t workspace_bytes, int B, int H, int N, int D, int M, int dtype,
+                  void* stream) {
+  LA_TRY(check_shape(B, H, N, D, M, dtype));
+  LA_TRY(check_ptrs({q, k, v, out, den, dout, dq, dk, dv}));
+  const Shape s{B, H, N, D, M, dtype};
+  LA_TRY(check_ws(LA_OP_CAUSAL_BWD, s, workspace, workspace_bytes));
+  return from_cuda(la::causal_bwd_cc(q, k, v, out, den, dout, dq, dk, dv,
+                                     static_cast<float*>(workspace), s,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int la_noncausal_fwd(const void* q, const void* k, const void* v, const int* lengths, void* out,
+                     float* den, float* S, float* Z, void* workspace, size_t workspace_bytes,
+                     int B, int H, int N, int D, int M, int dtype, void* stream) {
+  LA_TRY(check_shape(B, H, N, D, M, dtype));
+  LA_TRY(check_ptrs({q, k, v, out, S, Z}));
+  LA_TRY(check_opt_ptr(den));
+  LA_TRY(check_opt_ptr(lengths));
+  const Shape s{B, H, N, D, M, dtype};
+  LA_TRY(check_ws(LA_OP_NONCAUSAL_FWD, s, workspace, workspace_bytes));
+  return from_cuda(la::noncausal_fwd_cc(q, k, v, lengths, out, den, S, Z,
+                                        static_cast<float*>(workspace), s,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int la_noncausal_bwd(const void* q, const void* k, const void* v, const int* lengths,
+                     const void* out, const float* den, const float* S, const float* Z,
+                     const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                     size_t workspace_bytes, int B, int H, int N, int D, int M, int dtype,
+                     void* stream) {
+  LA_TRY(check_shape(B, H, N, D, M, dtype));
+  LA_TRY(check_ptrs({q, k, v, out, den, S, Z, dout, dq, dk, dv}));
+  LA_TRY(check_opt_ptr(lengths));
+  const Shape s{B, H, N, D, M, dtype};
+  LA_TRY(check_ws(LA_OP_NONCAUSAL_BWD, s, workspace, workspace_bytes));
+  return from_cuda(la::noncausal_bwd_cc(q, k, v, lengths, out, den, S, Z, dout, dq, dk, dv,
+                                        static_cast<float*>(workspace), s,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* y,
+                   int B, int H, int D, int M, int dtype, void* stream) {
+  LA_TRY(check_shape(B, H, 1, D, M, dtype));
+  LA_TRY(check_ptrs({q, k, v, S, Z, y}));
+  const Shape s{B, H, 1, D, M, dtype};
+  return from_cuda(la::decode_step(q, k, v, S, Z, y, s, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,545 @@
+// Causal linear attention on CUDA cores (fp32 FFMA), any supported dtype.
+//
+// Method: "Transformers are RNNs" (part 2/3), §3.3 eq. 9-12 (forward) and
+// §3.3.1 eq. 13-15 (cumulative-sum backward, completed here with the
+// denominator terms by the quotient rule).
+//
+// Work decomposition (the GB300 design, not the pages'): every (b, h)
+// sequence is cut into segments of whole 64-token chunks so that the grid
+// fills the 152 SMs.  A first kernel writes each segment's partial sums
+// (dS = sum phi(K) V^T, dz = sum phi(K); for the backward also
+// dR = sum phi(Q) gt^T, dr = sum gam phi(Q)) to the workspace, a scan kernel
+// turns them into exclusive prefix (S, z) and suffix (R, r) sums, and the
+// main kernel walks its segment chunk by chunk, carrying S/z forward (or R/r
+// backward) in fp32.  Inside a chunk the masked chunk-local terms are explicit
+// 64 x 64 products, exactly the quadratic form of eq. 8 restricted to the
+// chunk, and the earlier chunks enter through the carried state.
+#include "common.cuh"
+#include "launch.h"
+
+namespace la {
+namespace {
+
+constexpr int C = kChunk;
+constexpr int NT = 256;
+
+// ---------------------------------------------------------------- partial sums
+
+// Per-segment sums of the forward state, eq. 10-11 restricted to the segment:
+//   ws[bh][p] = [ dS (D x M) | dz (D) ].
+// The last segment's sums are never read (only exclusive prefixes are used).
+template <int D, int M, typename T>
+__global__ void __launch_bounds__(NT) k_seg_state_fwd(const T* __restrict__ k,
+                                                      const T* __restrict__ v, float* ws, int N,
+                                                      int nseg, int seg_len) {
+  const int p = blockIdx.x, bh = blockIdx.y;
+  if (p == nseg - 1) return;
+  extern __shared__ float sm[];
+  float* sK = sm;                  // phi(K) [C][D+1]
+  float* sV = sK + C * (D + 1);    // V      [C][M+1]
+  const long nb = (long)p * seg_len, ne = min((long)N, nb + seg_len);
+  const T* kh = k + (long)bh * N * D;
+  const T* vh = v + (long)bh * N * M;
+  float acc[D / 16][M / 16];
+  zero_acc(acc);
+  float zacc = 0.f;
+  for (long n0 = nb; n0 < ne; n0 += C) {
+    load_tile<T, C, D, false, kPhi>(sK, D + 1, kh, n0, ne);
+    load_tile<T, C, M, false, kRaw>(sV, M + 1, vh, n0, ne);
+    __syncthreads();
+    smem_mm<D / 16, M / 16, C>(acc, sK, 1, D + 1, sV, M + 1, 1);
+    if (threadIdx.x < D)
+      for (int j = 0; j < C; ++j) zacc += sK[j * (D + 1) + threadIdx.x];
+    __syncthreads();
+  }
+  float* dst = ws + ((long)bh * nseg + p) * (D * M + D);
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll
+  for (int r = 0; r < D / 16; ++r)
+#pragma unroll
+    for (int c = 0; c < M / 16; ++c) dst[(ty + 16 * r) * M + tx + 16 * c] = acc[r][c];
+  if (threadIdx.x < D) dst[D * M + threadIdx.x] = zacc;
+}
+
+// Loads the chunk's G and O, forms gt = G / den in place and
+// gam = -(gt . O) per row (the quotient-rule terms of the backward pass).
+// Rows past ne have G = 0, so gt = 0 and gam = 0 there.
+template <typename T, int M>
+__device__ __forceinline__ void load_grad_terms(float* sG, float* sO, float* sden, float* sgam,
+                                                const T* gh, const T* oh, const float* denh,
+                                                long n0, long ne) {
+  load_tile<T, C, M, false, kRaw>(sG, M + 1, gh, n0, ne);
+  load_tile<T, C, M, false, kRaw>(sO, M + 1, oh, n0, ne);
+  if (threadIdx.x < C) sden[threadIdx.x] = (n0 + threadIdx.x < ne) ? denh[n0 + threadIdx.x] : 1.f;
+  __syncthreads();
+  for (int e = threadIdx.x; e < C * M; e += NT) {
+    const int i = e / M, m = e % M;
+    sG[i * (M + 1) + m] = sG[i * (M + 1) + m] / sden[i];
+  }
+  __syncthreads();
+  if (threadIdx.x < C) {
+    float s = 0.f;
+    for (int m = 0; m < M; ++m) s += sG[threadIdx.x * (M + 1) + m] * sO[threadIdx.x * (M + 1) + m];
+    sgam[threadIdx.x] = -s;
+  }
+}
+
+// Per-segment sums for the backward pass:
+//   ws[bh][p] = [ dS (D x M) | dz (D) | dR (D x M) | dr (D) ]
+// with dR = sum_i phi(Q_i) gt_i^T and dr = sum_i gam_i phi(Q_i) (the terms of
+// the reverse cumulative sums of eq. 14-15).  dS/dz are skipped for the last
+// segment and dR/dr for the first (never read).
+template <int D, int M, typename T>
+__global__ void __launch_bounds__(NT) k_seg_state_bwd(const T* __restrict__ q,
+                                                      const T* __restrict__ k,
+                                                      const T* __restrict__ v,
+                                                      const T* __restrict__ o,
+                                                      const float* __restrict__ den,
+                                                      const T* __restrict__ g, float* ws, int N,
+                                                      int nseg, int seg_len) {
+  const int p = blockIdx.x, bh = blockIdx.y;
+  const bool want_s = p < nseg - 1, want_r = p > 0;
+  extern __shared__ float sm[];
+  float* sK = sm;                  // phi(K) [C][D+1]
+  float* sQ = sK + C * (D + 1);    // phi(Q) [C][D+1]
+  float* sV = sQ + C * (D + 1);    // V      [C][M+1]
+  float* sG = sV + C * (M + 1);    // gt     [C][M+1]
+  float* sO = sG + C * (M + 1);    // O      [C][M+1]
+  float* sden = sO + C * (M + 1);  // [C]
+  float* sgam = sden + C;          // [C]
+  const long nb = (long)p * seg_len, ne = min((long)N, nb + seg_len);
+  const long hq = (long)bh * N * D, hv = (long)bh * N * M;
+  float accS[D / 16][M / 16], accR[D / 16][M / 16];
+  zero_acc(accS);
+  zero_acc(accR);
+  float zacc = 0.f, racc = 0.f;
+  for (long n0 = nb; n0 < ne; n0 += C) {
+    if (want_s) {
+      load_tile<T, C, D, false, kPhi>(sK, D + 1, k + hq, n0, ne);
+      load_tile<T, C, M, false, kRaw>(sV, M + 1, v + hv, n0, ne);
+    }
+    if (want_r) {
+      load_tile<T, C, D, false, kPhi>(sQ, D + 1, q + hq, n0, ne);
+      load_grad_terms<T, M>(sG, sO, sden, sgam, g + hv, o + hv, den + (long)bh * N, n0, ne);
+    }
+    __syncthreads();
+    if (want_s) {
+      smem_mm<D / 16, M / 16, C>(accS, sK, 1, D + 1, sV, M + 1, 1);
+      if (threadIdx.x < D)
+        for (int j = 0; j < C; ++j) zacc += sK[j * (D + 1) + threadIdx.x];
+    }
+    if (want_r) {
+      smem_mm<D / 16, M / 16, C>(accR, sQ, 1, D + 1, sG, M + 1, 1);
+      if (threadIdx.x < D)
+        for (int i = 0; i < C; ++i) racc += sgam[i] * sQ[i * (D + 1) + threadIdx.x];
+    }
+    __syncthreads();
+  }
+  float* dst = ws + ((long)bh * nseg + p) * 2 * (D * M + D);
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll
+  for (int r = 0; r < D / 16; ++r)
+#pragma unroll
+    for (int c = 0; c < M / 16; ++c) {
+      dst[(ty + 16 * r) * M + tx + 16 * c] = accS[r][c];
+      dst[D * M + D + (ty + 16 * r) * M + tx + 16 * c] = accR[r][c];
+    }
+  if (threadIdx.x < D) {
+    dst[D * M + threadIdx.x] = zacc;
+    dst[2 * D * M + D + threadIdx.x] = racc;
+  }
+}
+
+// In-place exclusive scans over the segments of each (b, h): entries
+// [0, wf) of every record become prefix sums over earlier segments, entries
+// [ro, ro + wr) suffix sums over later segments.
+__global__ void k_seg_scan(float* ws, int nseg, int stride, int wf, int ro, int wr) {
+  float* base = ws + (long)blockIdx.x * nseg * stride;
+  for (int e = threadIdx.x; e < wf; e += blockDim.x) {
+    float run = 0.f;
+    for (int p = 0; p < nseg; ++p) {
+      const float x = base[(long)p * stride + e];
+      base[(long)p * stride + e] = run;
+      run += x;
+    }
+  }
+  for (int e = threadIdx.x; e < wr; e += blockDim.x) {
+    float run = 0.f;
+    for (int p = nseg - 1; p >= 0; --p) {
+      const float x = base[(long)p * stride + ro + e];
+      base[(long)p * stride + ro + e] = run;
+      run += x;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- forward
+
+// Causal forward, one CTA per (segment, b*h).  Per chunk:
+//   A   = mask(phi(Q) phi(K)^T)                  (eq. 8 inside the chunk)
+//   den = rowsum(A) + phi(Q) z                   (eq. 12 denominator)
+//   out = (A V + phi(Q) S) / den                 (eq. 12 numerator)
+//   S  += phi(K)^T V,  z += sum phi(K)           (eq. 10-11)
+template <int D, int M, typename T>
+__global__ void __launch_bounds__(NT) k_causal_fwd(const T* __restrict__ q,
+                                                   const T* __restrict__ k,
+                                                   const T* __restrict__ v, T* __restrict__ out,
+                                                   float* __restrict__ den,
+                                                   const float* __restrict__ ws, int N, int nseg,
+                                                   int seg_len) {
+  const int p = blockIdx.x, bh = blockIdx.y;
+  extern __shared__ float sm[];
+  float* sQ = sm;                  // phi(Q) [C][D+1]
+  float* sK = sQ + C * (D + 1);    // phi(K) [C][D+1]
+  float* sV = sK + C * (D + 1);    // V      [C][M+1]
+  float* sA = sV + C * (M + 1);    // A      [C][C+1]
+  float* sS = sA + C * (C + 1);    // S      [D][M+1]
+  float* sz = sS + D * (M + 1);    // z      [D]
+  float* sden = sz + D;            // [C]
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const long nb = (long)p * seg_len, ne = min((long)N, nb + seg_len);
+  const long hq = (long)bh * N * D, hv = (long)bh * N * M;
+
+  // exclusive prefix state of this segment
+  const float* pre = ws + ((long)bh * nseg + p) * (D * M + D);
+  float accS[D / 16][M / 16];
+#pragma unroll
+  for (int r = 0; r < D / 16; ++r)
+#pragma unroll
+    for (int c = 0; c < M / 16; ++c) {
+      const int d = ty + 16 * r, m = tx + 16 * c;
+      accS[r][c] = p > 0 ? pre[d * M + m] : 0.f;
+      sS[d * (M + 1) + m] = accS[r][c];
+    }
+  if (threadIdx.x < D) sz[threadIdx.x] = p > 0 ? pre[D * M + threadIdx.x] : 0.f;
+
+  for (long n0 = nb; n0 < ne; n0 += C) {
+    load_tile<T, C, D, false, kPhi>(sQ, D + 1, q + hq, n0, ne);
+    load_tile<T, C, D, false, kPhi>(sK, D + 1, k + hq, n0, ne);
+    load_tile<T, C, M, false, kRaw>(sV, M + 1, v + hv, n0, ne);
+    __syncthreads();
+    {  // A = mask(phi(Q) phi(K)^T)
+      float a[C / 16][C / 16];
+      zero_acc(a);
+      smem_mm<C / 16, C / 16, D>(a, sQ, D + 1, 1, sK, 1, D + 1);
+#pragma unroll
+      for (int r = 0; r < C / 16; ++r)
+#pragma unroll
+        for (int c = 0; c < C / 16; ++c) {
+          const int i = ty + 16 * r, j = tx + 16 * c;
+          sA[i * (C + 1) + j] = j <= i ? a[r][c] : 0.f;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < C) {
+      const int i = threadIdx.x;
+      float s = 0.f;
+      for (int j = 0; j <= i; ++j) s += sA[i * (C + 1) + j];
+      for (int d = 0; d < D; ++d) s += sQ[i * (D + 1) + d] * sz[d];
+      sden[i] = s;
+      if (den != nullptr && n0 + i < ne) den[(long)bh * N + n0 + i] = s;
+    }
+    __syncthreads();
+    {  // out = (A V + phi(Q) S) / den
+      float o[C / 16][M / 16];
+      zero_acc(o);
+      smem_mm<C / 16, M / 16, C>(o, sA, C + 1, 1, sV, M + 1, 1);
+      smem_mm<C / 16, M / 16, D>(o, sQ, D + 1, 1, sS, M + 1, 1);
+#pragma unroll
+      for (int r = 0; r < C / 16; ++r) {
+        const int i = ty + 16 * r;
+        if (n0 + i < ne) {
+          const float inv = 1.f / sden[i];
+#pragma unroll
+          for (int c = 0; c < M / 16; ++c)
+            out[hv + (n0 + i) * M + tx + 16 * c] = from_f<T>(o[r][c] * inv);
+        }
+      }
+    }
+    __syncthreads();
+    // S += phi(K)^T V, z += sum phi(K)
+    smem_mm<D / 16, M / 16, C>(accS, sK, 1, D + 1, sV, M + 1, 1);
+#pragma unroll
+    for (int r = 0; r < D / 16; ++r)
+#pragma unroll
+      for (int c = 0; c < M / 16; ++c) sS[(ty + 16 * r) * (M + 1) + tx + 16 * c] = accS[r][c];
+    if (threadIdx.x < D) {
+      float s = sz[threadIdx.x];
+      for (int j = 0; j < C; ++j) s += sK[j * (D + 1) + threadIdx.x];
+      sz[threadIdx.x] = s;
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- backward
+
+// Causal backward, grid (segment, b*h, role).
+// role 0 walks the segment forward carrying S, z (eq. 13 plus the
+// denominator term):
+//   dA       = mask(gt V^T + gam 1^T)
+//   grad_phiQ = dA phi(K) + gt S^T + gam z^T,  dq = grad_phiQ * phi'(Q)
+// role 1 walks it backward carrying R, r (eq. 14-15 plus the denominator):
+//   A = mask(phi(Q) phi(K)^T),  dA as above
+//   grad_phiK = dA^T phi(Q) + V R^T + r,        dk = grad_phiK * phi'(K)
+//   dv        = A^T gt + phi(K) R
+//   R += phi(Q)^T gt,  r += phi(Q)^T gam
+template <int D, int M, typename T>
+__global__ void __launch_bounds__(NT) k_causal_bwd(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+    const T* __restrict__ o, const float* __restrict__ den, const T* __restrict__ g,
+    T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv, const float* __restrict__ ws,
+    int N, int nseg, int seg_len) {
+  const int p = blockIdx.x, bh = blockIdx.y, role = blockIdx.z;
+  extern __shared__ float sm[];
+  float* sQ = sm;                  // phi(Q) [C][D+1]
+  float* sK = sQ + C * (D + 1);    // phi(K) [C][D+1]
+  float* sV = sK + C * (D + 1);    // V      [C][M+1]
+  float* sG = sV + C * (M + 1);    // gt     [C][M+1]
+  float* sO = sG + C * (M + 1);    // O      [C][M+1]
+  float* sA = sO + C * (M + 1);    // A      [C][C+1]
+  float* sdA = sA + C * (C + 1);   // dA     [C][C+1]
+  float* sS = sdA + C * (C + 1);   // S or R [D][M+1]
+  float* sz = sS + D * (M + 1);    // z or r [D]
+  float* sden = sz + D;            // [C]
+  float* sgam = sden + C;          // [C]
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const long nb = (long)p * seg_len, ne = min((long)N, nb + seg_len);
+  const long hq = (long)bh * N * D, hv = (long)bh * N * M;
+  const float* rec = ws + ((long)bh * nseg + p) * 2 * (D * M + D);
+  // role 0: exclusive prefix (S, z) of the segment; role 1: exclusive suffix (R, r)
+  const float* st = rec + (role == 0 ? 0 : D * M + D);
+  const bool has = role == 0 ? p > 0 : p < nseg - 1;
+  float acc[D / 16][M / 16];
+#pragma unroll
+  for (int r = 0; r < D / 16; ++r)
+#pragma unroll
+    for (int c = 0; c < M / 16; ++c) {
+      const int d = ty + 16 * r, m = tx + 16 * c;
+      acc[r][c] = has ? st[d * M + m] : 0.f;
+      sS[d * (M + 1) + m] = acc[r][c];
+    }
+  if (threadIdx.x < D) sz[threadIdx.x] = has ? st[D * M + threadIdx.x] : 0.f;
+
+  const int nchunks = (int)((ne - nb + C - 1) / C);
+  for (int ci = 0; ci < nchunks; ++ci) {
+    const long n0 = role == 0 ? nb + (long)ci * C : nb + (long)(nchunks - 1 - ci) * C;
+    if (role == 1) load_tile<T, C, D, false, kPhi>(sQ, D + 1, q + hq, n0, ne);
+    load_tile<T, C, D, false, kPhi>(sK, D + 1, k + hq, n0, ne);
+    load_tile<T, C, M, false, kRaw>(sV, M + 1, v + hv, n0, ne);
+    load_grad_terms<T, M>(sG, sO, sden, sgam, g + hv, o + hv, den + (long)bh * N, n0, ne);
+    __syncthreads();
+    {  // dA = mask(gt V^T + gam); role 1 also A = mask(phi(Q) phi(K)^T)
+      float a[C / 16][C / 16];
+      zero_acc(a);
+      smem_mm<C / 16, C / 16, M>(a, sG, M + 1, 1, sV, 1, M + 1);
+#pragma unroll
+      for (int r = 0; r < C / 16; ++r)
+#pragma unroll
+        for (int c = 0; c < C / 16; ++c) {
+          const int i = ty + 16 * r, j = tx + 16 * c;
+          sdA[i * (C + 1) + j] = j <= i ? a[r][c] + sgam[i] : 0.f;
+        }
+      if (role == 1) {
+        zero_acc(a);
+        smem_mm<C / 16, C / 16, D>(a, sQ, D + 1, 1, sK, 1, D + 1);
+#pragma unroll
+        for (int r = 0; r < C / 16; ++r)
+#pragma unroll
+          for (int c = 0; c < C / 16; ++c) {
+            const int i = ty + 16 * r, j = tx + 16 * c;
+            sA[i * (C + 1) + j] = j <= i ? a[r][c] : 0.f;
+          }
+      }
+    }
+    __syncthreads();
+    if (role == 0) {
+      float t[C / 16][D / 16];
+      zero_acc(t);
+      smem_mm<C / 16, D / 16, C>(t, sdA, C + 1, 1, sK, D + 1, 1);   // dA phi(K)
+      smem_mm<C / 16, D / 16, M>(t, sG, M + 1, 1, sS, 1, M + 1);    // gt S^T
+#pragma unroll
+      for (int r = 0; r < C / 16; ++r) {
+        const int i = ty + 16 * r;
+        if (n0 + i < ne) {
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            const int d = tx + 16 * c;
+            const long idx = hq + (n0 + i) * D + d;
+            const float gq = t[r][c] + sgam[i] * sz[d];
+            dq[idx] = from_f<T>(gq * dphi(to_f(q[idx])));
+          }
+        }
+      }
+    } else {
+      float t[C / 16][D / 16];
+      zero_acc(t);
+      smem_mm<C / 16, D / 16, C>(t, sdA, 1, C + 1, sQ, D + 1, 1);   // dA^T phi(Q)
+      smem_mm<C / 16, D / 16, M>(t, sV, M + 1, 1, sS, 1, M + 1);    // V R^T
+#pragma unroll
+      for (int r = 0; r < C / 16; ++r) {
+        const int j = ty + 16 * r;
+        if (n0 + j < ne) {
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            const int d = tx + 16 * c;
+            const long idx = hq + (n0 + j) * D + d;
+            const float gk = t[r][c] + sz[d];
+            dk[idx] = from_f<T>(gk * dphi(to_f(k[idx])));
+          }
+        }
+      }
+      float u[C / 16][M / 16];
+      zero_acc(u);
+      smem_mm<C / 16, M / 16, C>(u, sA, 1, C + 1, sG, M + 1, 1);    // A^T gt
+      smem_mm<C / 16, M / 16, D>(u, sK, D + 1, 1, sS, M + 1, 1);    // phi(K) R
+#pragma unroll
+      for (int r = 0; r < C / 16; ++r) {
+        const int j = ty + 16 * r;
+        if (n0 + j < ne) {
+#pragma unroll
+          for (int c = 0; c < M / 16; ++c) dv[hv + (n0 + j) * M + tx + 16 * c] = from_f<T>(u[r][c]);
+        }
+      }
+    }
+    __syncthreads();
+    if (role == 0) {  // S += phi(K)^T V, z += sum phi(K)
+      smem_mm<D / 16, M / 16, C>(acc, sK, 1, D + 1, sV, M + 1, 1);
+      if (threadIdx.x < D) {
+        float s = sz[threadIdx.x];
+        for (int j = 0; j < C; ++j) s += sK[j * (D + 1) + threadIdx.x];
+        sz[threadIdx.x] = s;
+      }
+    } else {          // R += phi(Q)^T gt, r += phi(Q)^T gam
+      smem_mm<D / 16, M / 16, C>(acc, sQ, 1, D + 1, sG, M + 1, 1);
+      if (threadIdx.x < D) {
+        float s = sz[threadIdx.x];
+        for (int i = 0; i < C; ++i) s += sgam[i] * sQ[i * (D + 1) + threadIdx.x];
+        sz[threadIdx.x] = s;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < D / 16; ++r)
+#pragma unroll
+      for (int c = 0; c < M / 16; ++c) sS[(ty + 16 * r) * (M + 1) + tx + 16 * c] = acc[r][c];
+    __syncthreads();
+  }
+}
+
+template <int D, int M>
+constexpr size_t fwd_smem() {
+  return sizeof(float) * (2 * C * (D + 1) + C * (M + 1) + C * (C + 1) + D * (M + 1) + D + C);
+}
+template <int D, int M>
+constexpr size_t bwd_smem() {
+  return sizeof(float) *
+         (2 * C * (D + 1) + 3 * C * (M + 1) + 2 * C * (C + 1) + D * (M + 1) + D + 2 * C);
+}
+template <int D, int M>
+constexpr size_t state_fwd_smem() {
+  return sizeof(float) * (C * (D + 1) + C * (M + 1));
+}
+template <int D, int M>
+constexpr size_t state_bwd_smem() {
+  return sizeof(float) * (2 * C * (D + 1) + 3 * C * (M + 1) + 2 * C);
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int D, int M, typename T>
+cudaError_t run_fwd(const T* q, const T* k, const T* v, T* out, float* den, float* ws,
+                    const Shape& s, cudaStream_t st) {
+  const int BH = s.B * s.H;
+  const SegPlan pl = plan_segments(BH, s.N);
+  cudaError_t e;
+  if (pl.nseg > 1) {
+    auto ks = k_seg_state_fwd<D, M, T>;
+    if ((e = set_smem(ks, state_fwd_smem<D, M>())) != cudaSuccess) return e;
+    ks<<<dim3(pl.nseg, BH), NT, state_fwd_smem<D, M>(), st>>>(k, v, ws, s.N, pl.nseg, pl.seg_len);
+    k_seg_scan<<<BH, 256, 0, st>>>(ws, pl.nseg, D * M + D, D * M + D, 0, 0);
+  }
+  auto kf = k_causal_fwd<D, M, T>;
+  if ((e = set_smem(kf, fwd_smem<D, M>())) != cudaSuccess) return e;
+  kf<<<dim3(pl.nseg, BH), NT, fwd_smem<D, M>(), st>>>(q, k, v, out, den, ws, s.N, pl.nseg,
+                                                      pl.seg_len);
+  return cudaGetLastError();
+}
+
+template <int D, int M, typename T>
+cudaError_t run_bwd(const T* q, const T* k, const T* v, const T* o, const float* den, const T* g,
+                    T* dq, T* dk, T* dv, float* ws, const Shape& s, cudaStream_t st) {
+  const int BH = s.B * s.H;
+  const SegPlan pl = plan_segments(BH, s.N);
+  cudaError_t e;
+  if (pl.nseg > 1) {
+    auto ks = k_seg_state_bwd<D, M, T>;
+    if ((e = set_smem(ks, state_bwd_smem<D, M>())) != cudaSuccess) return e;
+    ks<<<dim3(pl.nseg, BH), NT, state_bwd_smem<D, M>(), st>>>(q, k, v, o, den, g, ws, s.N,
+                                                              pl.nseg, pl.seg_len);
+    k_seg_scan<<<BH, 256, 0, st>>>(ws, pl.nseg, 2 * (D * M + D), D * M + D, D * M + D,
+                                   D * M + D);
+  }
+  auto kb = k_causal_bwd<D, M, T>;
+  if ((e = set_smem(kb, bwd_smem<D, M>())) != cudaSuccess) return e;
+  kb<<<dim3(pl.nseg, BH, 2), NT, bwd_smem<D, M>(), st>>>(q, k, v, o, den, g, dq, dk, dv, ws,
+                                                         s.N, pl.nseg, pl.seg_len);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t causal_fwd_ws_floats(const Shape& s) {
+  const SegPlan pl = plan_segments(s.B * s.H, s.N);
+  return pl.nseg > 1 ? (size_t)s.B * s.H * pl.nseg * (s.D * s.M + s.D) : 0;
+}
+
+size_t causal_bwd_ws_floats(const Shape& s) {
+  const SegPlan pl = plan_segments(s.B * s.H, s.N);
+  return pl.nseg > 1 ? (size_t)s.B * s.H * pl.nseg * 2 * (s.D * s.M + s.D) : 0;
+}
+
+int causal_fwd_launches(const Shape& s) {
+  return plan_segments(s.B * s.H, s.N).nseg > 1 ? 3 : 1;
+}
+
+int causal_bwd_launches(const Shape& s) {
+  return plan_segments(s.B * s.H, s.N).nseg > 1 ? 3 : 1;
+}
+
+cudaError_t causal_fwd_cc(const void* q, const void* k, const void* v, void* out, float* den,
+                          float* ws, const Shape& s, cudaStream_t st) {
+  if (s.dtype == 0) {
+    using T = float;
+    LA_DISPATCH_DM(s.D, s.M, return (run_fwd<D_, M_, T>((const T*)q, (const T*)k, (const T*)v,
+                                                         (T*)out, den, ws, s, st)));
+  } else {
+    using T = __nv_bfloat16;
+    LA_DISPATCH_DM(s.D, s.M, return (run_fwd<D_, M_, T>((const T*)q, (const T*)k, (const T*)v,
+                                                         (T*)out, den, ws, s, st)));
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t causal_bwd_cc(const void* q, const void* k, const void* v, const void* out,
+                          const float* den, const void* dout, void* dq, void* dk, void* dv,
+                          float* ws, const Shape& s, cudaStream_t st) {
+  if (s.dtype == 0) {
+    using T = float;
+    LA_DISPATCH_DM(s.D, s.M,
+                   return (run_bwd<D_, M_, T>((const T*)q, (const T*)k, (const T*)v,
+                                              (const T*)out, den, (const T*)dout, (T*)dq, (T*)dk,
+                                              (T*)dv, ws, s, st)));
+  } else {
+    using T = __nv_bfloat16;
+    LA_DISPATCH_DM(s.D, s.M,
+                   return (run_bwd<D_, M_, T>((const T*)q, (const T*)k, (const T*)v,
+                                              (const T*)out, den, (const T*)dout, (T*)dq, (T*)dk,
+                                              (T*)dv, ws, s, st)));
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace la

@@ -1,0 +1,79 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace la {
+
+constexpr int kChunk = 64;            // tokens per chunk in the CUDA-core kernels
+constexpr int kTargetCtas = 2 * 152;  // segments are sized to fill GB300's 152 SMs twice
+
+// Split of each (b, h) sequence into segments of whole chunks.
+struct SegPlan {
+  int nseg;     // segments per (b, h)
+  int seg_len;  // tokens per segment (a multiple of the chunk length)
+};
+
+inline SegPlan plan_segments(int BH, int N, int chunk = kChunk, int target = kTargetCtas) {
+  const int nch = (N + chunk - 1) / chunk;
+  int want = (target + BH - 1) / BH;
+  if (want < 1) want = 1;
+  if (want > nch) want = nch;
+  const int per = (nch + want - 1) / want;  // chunks per segment
+  SegPlan p;
+  p.seg_len = per * chunk;
+  p.nseg = (N + p.seg_len - 1) / p.seg_len;
+  return p;
+}
+
+struct Shape {
+  int B, H, N, D, M;
+  int dtype;  // 0 = fp32, 1 = bf16
+};
+
+// Workspace (floats) each path needs.
+size_t causal_fwd_ws_floats(const Shape& s);
+size_t causal_bwd_ws_floats(const Shape& s);
+size_t noncausal_fwd_ws_floats(const Shape& s);
+size_t noncausal_bwd_ws_floats(const Shape& s);
+
+// Kernel launches per call (must match the launchers below).
+int causal_fwd_launches(const Shape& s);
+int causal_bwd_launches(const Shape& s);
+int noncausal_fwd_launches(const Shape& s);
+int noncausal_bwd_launches(const Shape& s);
+
+// CUDA-core (FFMA) paths; every kernel of the library is launched from these.
+cudaError_t causal_fwd_cc(const void* q, const void* k, const void* v, void* out, float* den,
+                          float* ws, const Shape& s, cudaStream_t st);
+cudaError_t causal_bwd_cc(const void* q, const void* k, const void* v, const void* out,
+                          const float* den, const void* dout, void* dq, void* dk, void* dv,
+                          float* ws, const Shape& s, cudaStream_t st);
+cudaError_t noncausal_fwd_cc(const void* q, const void* k, const void* v, const int* lengths,
+                             void* out, float* den, float* S, float* Z, float* ws, const Shape& s,
+                             cudaStream_t st);
+cudaError_t noncausal_bwd_cc(const void* q, const void* k, const void* v, const int* lengths,
+                             const void* out, const float* den, const float* S, const float* Z,
+                             const void* dout, void* dq, void* dk, void* dv, float* ws,
+                             const Shape& s, cudaStream_t st);
+cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* y,
+                        const Shape& s, cudaStream_t st);
+
+}  // namespace la
+
+// Expands BODY once per supported (D, M) pair with constexpr D_ and M_ in scope.
+#define LA_DISPATCH_DM(Dv, Mv, BODY)                         \
+  switch ((Dv) * 1000 + (Mv)) {                              \
+    case 16016: { constexpr int D_ = 16, M_ = 16; BODY; } break; \
+    case 16032: { constexpr int D_ = 16, M_ = 32; BODY; } break; \
+    case 16064: { constexpr int D_ = 16, M_ = 64; BODY; } break; \
+    case 32016: { constexpr int D_ = 32, M_ = 16; BODY; } break; \
+    case 32032: { constexpr int D_ = 32, M_ = 32; BODY; } break; \
+    case 32064: { constexpr int D_ = 32, M_ = 64; BODY; } break; \
+    case 64016: { constexpr int D_ = 64, M_ = 16; BODY; } break; \
+    case 64032: { constexpr int D_ = 64, M_ = 32; BODY; } break; \
+    case 64064: { constexpr int D_ = 64, M_ = 64; BODY; } break; \
+    default: return cudaErrorInvalidValue;                   \
+  }

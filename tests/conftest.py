@@ -17,3 +17,21 @@ def pytest_configure(config):
 def orc():
     import oracle
     return oracle.default()
+
+
+@pytest.fixture(scope="session")
+def linattn():
+    """The CUDA library's Python binding, built in-tree first if needed."""
+    from kernelized_causal_attention_gb300 import _build
+    _build.build()
+    import kernelized_causal_attention_gb300 as la
+    la.lib()
+    return la
+
+
+@pytest.fixture(scope="session")
+def cuda(linattn):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")

@@ -1,0 +1,102 @@
+"""The C ABI on the host: the library loads, exports every symbol that
+include/linattn.h declares, sizes workspaces, and rejects bad arguments before
+launching anything (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "linattn.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    for n in ("la_causal_fwd", "la_causal_bwd", "la_noncausal_fwd", "la_noncausal_bwd",
+              "la_decode_step", "la_workspace_bytes", "la_status_string", "la_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(linattn):
+    h = ctypes.CDLL(linattn.library_path())
+    for name in declared_symbols():
+        assert hasattr(h, name), f"{name} declared in linattn.h but not exported"
+    assert set(declared_symbols()) <= set(linattn.EXPORTED) | {"la_workspace_bytes"}
+
+
+def test_version_and_status_strings(linattn):
+    assert linattn.lib().la_version() == 100
+    for code in range(5):
+        assert linattn.status_string(code)
+    assert linattn.status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(linattn):
+    la = linattn
+    # one segment per sequence needs no workspace for the causal path
+    assert la.la_workspace_bytes(la.LA_OP_CAUSAL_FWD, 1, 1, 64, 16, 16, la.LA_F32) == 0
+    n = la.la_workspace_bytes(la.LA_OP_CAUSAL_FWD, 4, 8, 3072, 64, 64, la.LA_BF16)
+    assert n > 0 and n % 16 == 0
+    assert la.la_workspace_bytes(la.LA_OP_CAUSAL_BWD, 4, 8, 3072, 64, 64, la.LA_BF16) == 2 * n
+    assert la.la_workspace_bytes(la.LA_OP_DECODE, 256, 8, 1, 64, 64, la.LA_F32) == 0
+    assert la.la_workspace_bytes(la.LA_OP_NONCAUSAL_FWD, 16, 6, 2048, 64, 64, la.LA_F32) > 0
+    # invalid arguments size to 0
+    assert la.la_workspace_bytes(la.LA_OP_CAUSAL_FWD, 0, 8, 3072, 64, 64, la.LA_BF16) == 0
+    assert la.la_workspace_bytes(la.LA_OP_CAUSAL_FWD, 1, 8, 3072, 48, 64, la.LA_BF16) == 0
+
+
+FAKE = 1 << 20  # an aligned, never-dereferenced address: every call below fails its checks first
+
+
+def _fwd(la, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, den=FAKE, ws=None, wsb=0, B=1, H=1, N=64, D=16, M=16,
+             dt=la.LA_F32)
+    a.update(kw)
+    return la.lib().la_causal_fwd(a["q"], a["k"], a["v"], a["out"], a["den"], a["ws"], a["wsb"],
+                                  a["B"], a["H"], a["N"], a["D"], a["M"], a["dt"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(out=None), 1),
+    (dict(q=FAKE + 4), 1), (dict(den=FAKE + 8), 1),
+    (dict(N=0), 1), (dict(B=0), 1), (dict(H=-1), 1), (dict(N=(1 << 24) + 1), 1),
+    (dict(dt=7), 1), (dict(D=48), 2), (dict(M=128), 2), (dict(D=0), 1),
+    (dict(B=4, H=8, N=3072, D=64, M=64), 4),          # needs workspace, none given
+    (dict(B=4, H=8, N=3072, D=64, M=64, ws=FAKE, wsb=16), 4),
+    (dict(B=4, H=8, N=3072, D=64, M=64, ws=FAKE + 4, wsb=1 << 30), 1),
+])
+def test_causal_fwd_rejects(linattn, kw, code):
+    assert _fwd(linattn, **kw) == code
+
+
+def test_other_calls_reject(linattn):
+    L = linattn.lib()
+    F = FAKE
+    # causal bwd: den is required
+    assert L.la_causal_bwd(F, F, F, F, None, F, F, F, F, None, 0, 1, 1, 64, 16, 16, 0, None) == 1
+    # non-causal: S and Z required, lengths optional but aligned
+    assert L.la_noncausal_fwd(F, F, F, None, F, F, None, F, F, 1 << 30, 1, 1, 64, 16, 16, 0, None) == 1
+    assert L.la_noncausal_fwd(F, F, F, F + 4, F, F, F, F, F, 1 << 30, 1, 1, 64, 16, 16, 0, None) == 1
+    assert L.la_noncausal_fwd(F, F, F, None, F, F, F, F, None, 0, 1, 1, 64, 16, 16, 0, None) == 4
+    assert L.la_noncausal_bwd(F, F, F, None, F, F, F, F, F, F, F, None, F, 1 << 30, 1, 1, 64, 16,
+                              16, 0, None) == 1
+    # decode
+    assert L.la_decode_step(F, F, None, F, F, F, 1, 1, 64, 64, 0, None) == 1
+    assert L.la_decode_step(F, F, F, F, F, F, 1, 1, 64, 96, 0, None) == 2
+    assert L.la_decode_step(F, F, F, F, F, F, 0, 1, 64, 64, 0, None) == 1
+
+
+def test_binding_requires_library(monkeypatch, tmp_path):
+    """Without the built library the binding raises instead of falling back."""
+    import kernelized_causal_attention_gb300 as la
+    monkeypatch.setattr(la, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(la, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        la.lib()

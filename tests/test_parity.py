@@ -1,0 +1,187 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle on
+the same seeded inputs, element by element.
+
+Tolerance: max |gpu - oracle| / max |oracle| per tensor (normwise-max
+relative error), <= 1e-4 for fp32 inputs and <= 2e-2 for bf16 inputs with
+fp32 accumulation.  For bf16 the oracle receives exactly the bf16-rounded
+inputs, widened to fp64.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kernelized_causal_attention_gb300.workloads import (WORKLOADS, DecodeStream, causal_inputs,
+                                                         noncausal_inputs)
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def rel_err(gpu, ref):
+    g = gpu.detach().double().cpu().numpy() if isinstance(gpu, torch.Tensor) else gpu
+    ref = np.asarray(ref)
+    assert g.shape == ref.shape
+    assert np.all(np.isfinite(g)), "non-finite values in the GPU result"
+    return float(np.max(np.abs(g - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def _to(dev, *ts):
+    return [t.to(dev).contiguous() for t in ts]
+
+
+def check_causal(la, dev, B, H, N, D, M, dtype, seed):
+    q, k, v, g = causal_inputs(B, H, N, D, M, dtype, seed)
+    qd, kd, vd, gd = _to(dev, q, k, v, g)
+    out, den = la.causal_fwd(qd, kd, vd)
+    dq, dk, dv = la.causal_bwd(qd, kd, vd, out, den, gd)
+    torch.cuda.synchronize()
+    o_ref, den_ref = oracle.causal_fwd(q, k, v)
+    dq_ref, dk_ref, dv_ref = oracle.causal_bwd(q, k, v, g)
+    tol = TOL[dtype]
+    errs = {"out": rel_err(out, o_ref), "den": rel_err(den, den_ref), "dv": rel_err(dv, dv_ref)}
+    if N == 1:
+        # a single token: out = v whatever q and k are, so dq = dk = 0 exactly;
+        # a relative error against zero is meaningless, check the absolute size
+        errs["dq_abs"] = float(dq.abs().max())
+        errs["dk_abs"] = float(dk.abs().max())
+    else:
+        errs["dq"] = rel_err(dq, dq_ref)
+        errs["dk"] = rel_err(dk, dk_ref)
+    bad = {k_: e for k_, e in errs.items() if not e <= tol}
+    assert not bad, f"causal B={B} H={H} N={N} D={D} M={M} {dtype}: {errs}"
+    return errs
+
+
+# small and ragged cases first: N=1, N below one chunk, ragged tails, many
+# segments per head (small B*H), D != M, every supported head size
+SMALL = [
+    (1, 1, 1, 16, 16, "f32"),
+    (1, 1, 5, 32, 16, "f32"),
+    (1, 1, 64, 16, 16, "f32"),
+    (2, 3, 100, 32, 64, "f32"),
+    (1, 2, 333, 64, 32, "f32"),
+    (1, 1, 1000, 64, 64, "f32"),
+    (3, 1, 129, 16, 64, "f32"),
+    (1, 2, 200, 64, 32, "bf16"),
+    (2, 2, 257, 64, 64, "bf16"),
+    (1, 1, 2049, 32, 32, "bf16"),
+    (2, 1, 77, 16, 16, "bf16"),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,M,dtype", SMALL)
+def test_causal_small(cuda, linattn, B, H, N, D, M, dtype):
+    check_causal(linattn, cuda, B, H, N, D, M, dtype, seed=1000 + N)
+
+
+@pytest.mark.parametrize("name", ["causal_tiny_f32", "causal_mnist_bf16", "causal_cifar_bf16"])
+def test_causal_workloads(cuda, linattn, name):
+    w = WORKLOADS[name]
+    errs = check_causal(linattn, cuda, w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed)
+    print(name, errs)
+
+
+def check_noncausal(la, dev, B, H, N, D, M, dtype, seed, len_range):
+    lengths, q, k, v, g = noncausal_inputs(B, H, N, D, M, dtype, seed, len_range)
+    qd, kd, vd, gd = _to(dev, q, k, v, g)
+    ld = lengths.to(dev) if len_range is not None else None
+    out, den, S, Z = la.noncausal_fwd(qd, kd, vd, ld)
+    dq, dk, dv = la.noncausal_bwd(qd, kd, vd, ld, out, den, S, Z, gd)
+    torch.cuda.synchronize()
+    lens = lengths if len_range is not None else None
+    o_ref, den_ref, S_ref, Z_ref = oracle.noncausal_fwd(q, k, v, lens)
+    dq_ref, dk_ref, dv_ref = oracle.noncausal_bwd(q, k, v, g, lens)
+    tol = TOL[dtype]
+    errs = {"out": rel_err(out, o_ref), "den": rel_err(den, den_ref), "S": rel_err(S, S_ref),
+            "Z": rel_err(Z, Z_ref), "dv": rel_err(dv, dv_ref)}
+    if N == 1:  # one valid token: dq = dk = 0 exactly (see the causal case)
+        errs["dq_abs"] = float(dq.abs().max())
+        errs["dk_abs"] = float(dk.abs().max())
+    else:
+        errs["dq"] = rel_err(dq, dq_ref)
+        errs["dk"] = rel_err(dk, dk_ref)
+    bad = {k_: e for k_, e in errs.items() if not e <= tol}
+    assert not bad, f"non-causal B={B} H={H} N={N} D={D} M={M} {dtype}: {errs}"
+    # padded rows are exactly zero
+    for b, L in enumerate(lengths.tolist() if len_range is not None else [N] * B):
+        for t in (out, den, dq, dk, dv):
+            assert torch.all(t[b, :, L:] == 0)
+    return errs
+
+
+@pytest.mark.parametrize("B,H,N,D,M,dtype,lr", [
+    (1, 1, 1, 16, 16, "f32", None),
+    (2, 3, 100, 32, 64, "f32", (1, 100)),
+    (4, 2, 300, 64, 64, "f32", (0, 300)),
+    (3, 2, 513, 64, 32, "bf16", (200, 513)),
+    (2, 1, 64, 16, 16, "f32", (64, 64)),
+])
+def test_noncausal_small(cuda, linattn, B, H, N, D, M, dtype, lr):
+    check_noncausal(linattn, cuda, B, H, N, D, M, dtype, 2000 + N, lr)
+
+
+def test_noncausal_workload(cuda, linattn):
+    w = WORKLOADS["noncausal_speech_f32"]
+    errs = check_noncausal(linattn, cuda, w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed, w.len_range)
+    print(w.name, errs)
+
+
+def run_decode(la, dev, B, H, D, M, dtype, seed, T, sample_heads=None, chunk=64):
+    """Runs T steps on the GPU; checks y_t for every step and the final
+    state against the oracle on a sample of heads (all heads if None)."""
+    stream = DecodeStream(B, H, D, M, dtype, seed)
+    S = torch.zeros(B, H, D, M, dtype=torch.float32, device=dev)
+    Z = torch.zeros(B, H, D, dtype=torch.float32, device=dev)
+    flat = lambda t: t.reshape(t.shape[0], B * H, -1)
+    heads = np.arange(B * H) if sample_heads is None else np.asarray(sample_heads)
+    S_ref = np.zeros((1, len(heads), D, M))
+    Z_ref = np.zeros((1, len(heads), D))
+    worst = 0.0
+    for t0 in range(0, T, chunk):
+        n = min(chunk, T - t0)
+        qs, ks, vs = stream.steps(n)
+        ys = []
+        for t in range(n):
+            qd, kd, vd = _to(dev, qs[t], ks[t], vs[t])
+            ys.append(la.decode_step(qd, kd, vd, S, Z))
+        y = torch.stack(ys)
+        qh, kh, vh = (flat(x)[:, heads][:, None] for x in (qs, ks, vs))
+        y_ref, S_ref, Z_ref = oracle.decode(qh, kh, vh, S_ref, Z_ref)
+        worst = max(worst, rel_err(flat(y)[:, heads][:, None], y_ref))
+    s_err = rel_err(S.reshape(B * H, D, M)[heads][None], S_ref)
+    z_err = rel_err(Z.reshape(B * H, D)[heads][None], Z_ref)
+    return worst, s_err, z_err
+
+
+@pytest.mark.parametrize("B,H,D,M,dtype,T", [
+    (2, 3, 16, 16, "f32", 40), (1, 4, 64, 32, "f32", 70), (3, 1, 32, 64, "bf16", 33),
+    (2, 2, 64, 64, "f32", 130)])
+def test_decode_small(cuda, linattn, B, H, D, M, dtype, T):
+    y_err, s_err, z_err = run_decode(linattn, cuda, B, H, D, M, dtype, 3000 + T, T)
+    tol = TOL[dtype]
+    assert y_err <= tol and s_err <= 1e-4 and z_err <= 1e-4, (y_err, s_err, z_err)
+
+
+def test_decode_matches_causal(cuda, linattn):
+    """T decode steps reproduce the causal forward on the stacked sequence."""
+    B, H, D, M, T = 2, 2, 64, 64, 200
+    q, k, v, _ = causal_inputs(B, H, T, D, M, "f32", 77)
+    out, _ = linattn.causal_fwd(*_to(cuda, q, k, v))
+    S = torch.zeros(B, H, D, M, device=cuda)
+    Z = torch.zeros(B, H, D, device=cuda)
+    ys = [linattn.decode_step(*_to(cuda, q[:, :, t], k[:, :, t], v[:, :, t]), S, Z) for t in range(T)]
+    y = torch.stack(ys, dim=2)
+    assert rel_err(y, out.double().cpu().numpy()) < 1e-5
+
+
+def test_decode_workload(cuda, linattn):
+    """256 streams x 8 heads, 3072 steps; every step's y and the final S, Z on
+    64 sampled heads against the oracle."""
+    w = WORKLOADS["decode_f32"]
+    heads = np.random.default_rng(0).choice(w.B * w.H, size=64, replace=False)
+    y_err, s_err, z_err = run_decode(linattn, cuda, w.B, w.H, w.D, w.M, w.dtype, w.seed, w.N,
+                                     sample_heads=np.sort(heads), chunk=256)
+    print(w.name, y_err, s_err, z_err)
+    assert y_err <= 1e-4 and s_err <= 1e-4 and z_err <= 1e-4, (y_err, s_err, z_err)
