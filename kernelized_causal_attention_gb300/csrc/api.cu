@@ -37,8 +37,10 @@ int check_opt_ptr(const void* p) { return (p == nullptr || aligned16(p)) ? LA_OK
 
 size_t ws_bytes(int op, const Shape& s) {
   switch (op) {
-    case LA_OP_CAUSAL_FWD: return 4 * la::causal_fwd_ws_floats(s);
-    case LA_OP_CAUSAL_BWD: return 4 * la::causal_bwd_ws_floats(s);
+    case LA_OP_CAUSAL_FWD:
+      return 4 * (la::tc_eligible(s) ? la::causal_fwd_tc_ws_floats(s) : la::causal_fwd_ws_floats(s));
+    case LA_OP_CAUSAL_BWD:
+      return 4 * (la::tc_eligible(s) ? la::causal_bwd_tc_ws_floats(s) : la::causal_bwd_ws_floats(s));
     case LA_OP_NONCAUSAL_FWD: return 4 * la::noncausal_fwd_ws_floats(s);
     case LA_OP_NONCAUSAL_BWD: return 4 * la::noncausal_bwd_ws_floats(s);
     default: return 0;
@@ -88,8 +90,10 @@ int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype) {
   if (check_shape(B, H, op == LA_OP_DECODE ? 1 : N, D, M, dtype) != LA_OK) return 0;
   const Shape s{B, H, N, D, M, dtype};
   switch (op) {
-    case LA_OP_CAUSAL_FWD: return la::causal_fwd_launches(s);
-    case LA_OP_CAUSAL_BWD: return la::causal_bwd_launches(s);
+    case LA_OP_CAUSAL_FWD:
+      return la::tc_eligible(s) ? la::causal_fwd_tc_launches(s) : la::causal_fwd_launches(s);
+    case LA_OP_CAUSAL_BWD:
+      return la::tc_eligible(s) ? la::causal_bwd_tc_launches(s) : la::causal_bwd_launches(s);
     case LA_OP_NONCAUSAL_FWD: return la::noncausal_fwd_launches(s);
     case LA_OP_NONCAUSAL_BWD: return la::noncausal_bwd_launches(s);
     case LA_OP_DECODE: return 1;
@@ -105,6 +109,9 @@ int la_causal_fwd(const void* q, const void* k, const void* v, void* out, float*
   LA_TRY(check_opt_ptr(den));
   const Shape s{B, H, N, D, M, dtype};
   LA_TRY(check_ws(LA_OP_CAUSAL_FWD, s, workspace, workspace_bytes));
+  if (la::tc_eligible(s))
+    return from_cuda(la::causal_fwd_tc(q, k, v, out, den, static_cast<float*>(workspace), s,
+                                       static_cast<cudaStream_t>(stream)));
   return from_cuda(la::causal_fwd_cc(q, k, v, out, den, static_cast<float*>(workspace), s,
                                      static_cast<cudaStream_t>(stream)));
 }
@@ -117,6 +124,10 @@ int la_causal_bwd(const void* q, const void* k, const void* v, const void* out, 
   LA_TRY(check_ptrs({q, k, v, out, den, dout, dq, dk, dv}));
   const Shape s{B, H, N, D, M, dtype};
   LA_TRY(check_ws(LA_OP_CAUSAL_BWD, s, workspace, workspace_bytes));
+  if (la::tc_eligible(s))
+    return from_cuda(la::causal_bwd_tc(q, k, v, out, den, dout, dq, dk, dv,
+                                       static_cast<float*>(workspace), s,
+                                       static_cast<cudaStream_t>(stream)));
   return from_cuda(la::causal_bwd_cc(q, k, v, out, den, dout, dq, dk, dv,
                                      static_cast<float*>(workspace), s,
                                      static_cast<cudaStream_t>(stream)));

@@ -152,10 +152,11 @@ __global__ void __launch_bounds__(NT) k_seg_state_bwd(const T* __restrict__ q,
 
 // In-place exclusive scans over the segments of each (b, h): entries
 // [0, wf) of every record become prefix sums over earlier segments, entries
-// [ro, ro + wr) suffix sums over later segments.
+// [ro, ro + wr) suffix sums over later segments.  One thread per entry.
 __global__ void k_seg_scan(float* ws, int nseg, int stride, int wf, int ro, int wr) {
   float* base = ws + (long)blockIdx.x * nseg * stride;
-  for (int e = threadIdx.x; e < wf; e += blockDim.x) {
+  const int e = blockIdx.y * blockDim.x + threadIdx.x;
+  if (e < wf) {
     float run = 0.f;
     for (int p = 0; p < nseg; ++p) {
       const float x = base[(long)p * stride + e];
@@ -163,7 +164,7 @@ __global__ void k_seg_scan(float* ws, int nseg, int stride, int wf, int ro, int 
       run += x;
     }
   }
-  for (int e = threadIdx.x; e < wr; e += blockDim.x) {
+  if (e < wr) {
     float run = 0.f;
     for (int p = nseg - 1; p >= 0; --p) {
       const float x = base[(long)p * stride + ro + e];
@@ -459,7 +460,8 @@ cudaError_t run_fwd(const T* q, const T* k, const T* v, T* out, float* den, floa
     auto ks = k_seg_state_fwd<D, M, T>;
     if ((e = set_smem(ks, state_fwd_smem<D, M>())) != cudaSuccess) return e;
     ks<<<dim3(pl.nseg, BH), NT, state_fwd_smem<D, M>(), st>>>(k, v, ws, s.N, pl.nseg, pl.seg_len);
-    k_seg_scan<<<BH, 256, 0, st>>>(ws, pl.nseg, D * M + D, D * M + D, 0, 0);
+    k_seg_scan<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(ws, pl.nseg, D * M + D,
+                                                                  D * M + D, 0, 0);
   }
   auto kf = k_causal_fwd<D, M, T>;
   if ((e = set_smem(kf, fwd_smem<D, M>())) != cudaSuccess) return e;
@@ -479,8 +481,8 @@ cudaError_t run_bwd(const T* q, const T* k, const T* v, const T* o, const float*
     if ((e = set_smem(ks, state_bwd_smem<D, M>())) != cudaSuccess) return e;
     ks<<<dim3(pl.nseg, BH), NT, state_bwd_smem<D, M>(), st>>>(q, k, v, o, den, g, ws, s.N,
                                                               pl.nseg, pl.seg_len);
-    k_seg_scan<<<BH, 256, 0, st>>>(ws, pl.nseg, 2 * (D * M + D), D * M + D, D * M + D,
-                                   D * M + D);
+    k_seg_scan<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(
+        ws, pl.nseg, 2 * (D * M + D), D * M + D, D * M + D, D * M + D);
   }
   auto kb = k_causal_bwd<D, M, T>;
   if ((e = set_smem(kb, bwd_smem<D, M>())) != cudaSuccess) return e;
@@ -490,6 +492,12 @@ cudaError_t run_bwd(const T* q, const T* k, const T* v, const T* o, const float*
 }
 
 }  // namespace
+
+void k_seg_scan_ext(float* ws, int BH, int nseg, int stride, int wf, int ro, int wr,
+                    cudaStream_t st) {
+  const int w = wf > wr ? wf : wr;
+  k_seg_scan<<<dim3(BH, (w + 255) / 256), 256, 0, st>>>(ws, nseg, stride, wf, ro, wr);
+}
 
 size_t causal_fwd_ws_floats(const Shape& s) {
   const SegPlan pl = plan_segments(s.B * s.H, s.N);

@@ -45,6 +45,25 @@ int causal_bwd_launches(const Shape& s);
 int noncausal_fwd_launches(const Shape& s);
 int noncausal_bwd_launches(const Shape& s);
 
+// In-place exclusive scans over the nseg records (stride floats each) of
+// every (b, h) in ws: entries [0, wf) become prefix sums over earlier
+// records, entries [ro, ro + wr) suffix sums over later records.
+void k_seg_scan_ext(float* ws, int BH, int nseg, int stride, int wf, int ro, int wr,
+                    cudaStream_t st);
+
+// tcgen05 path (bf16, D = M = 64).
+SegPlan tc_plan(int BH, int N);
+bool tc_eligible(const Shape& s);
+size_t causal_fwd_tc_ws_floats(const Shape& s);
+int causal_fwd_tc_launches(const Shape& s);
+cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out, float* den,
+                          float* ws, const Shape& s, cudaStream_t st);
+size_t causal_bwd_tc_ws_floats(const Shape& s);
+int causal_bwd_tc_launches(const Shape& s);
+cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const void* out,
+                          const float* den, const void* dout, void* dq, void* dk, void* dv,
+                          float* ws, const Shape& s, cudaStream_t st);
+
 // CUDA-core (FFMA) paths; every kernel of the library is launched from these.
 cudaError_t causal_fwd_cc(const void* q, const void* k, const void* v, void* out, float* den,
                           float* ws, const Shape& s, cudaStream_t st);

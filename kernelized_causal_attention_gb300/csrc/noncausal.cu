@@ -126,7 +126,8 @@ __global__ void __launch_bounds__(NT) k_nc_state_bwd(const T* __restrict__ q,
 __global__ void k_seg_sum(const float* ws, int nseg, int DM, int D, float* dA, float* dB) {
   const int bh = blockIdx.x, stride = DM + D;
   const float* base = ws + (long)bh * nseg * stride;
-  for (int e = threadIdx.x; e < stride; e += blockDim.x) {
+  const int e = blockIdx.y * blockDim.x + threadIdx.x;
+  if (e < stride) {
     float s = 0.f;
     for (int p = 0; p < nseg; ++p) s += base[(long)p * stride + e];
     if (e < DM)
@@ -295,7 +296,7 @@ cudaError_t run_fwd(const T* q, const T* k, const T* v, const int* lengths, T* o
   if ((e = set_smem(ks, sm_state)) != cudaSuccess) return e;
   if ((e = set_smem(ko, sm_out)) != cudaSuccess) return e;
   ks<<<dim3(pl.nseg, BH), NT, sm_state, st>>>(k, v, lengths, ws, s.N, s.H, pl.nseg, pl.seg_len);
-  k_seg_sum<<<BH, 256, 0, st>>>(ws, pl.nseg, D * M, D, S, Z);
+  k_seg_sum<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(ws, pl.nseg, D * M, D, S, Z);
   ko<<<dim3(pl.nseg, BH), NT, sm_out, st>>>(q, S, Z, lengths, out, den, s.N, s.H, pl.nseg,
                                             pl.seg_len);
   return cudaGetLastError();
@@ -319,7 +320,7 @@ cudaError_t run_bwd(const T* q, const T* k, const T* v, const int* lengths, cons
   if ((e = set_smem(kb, sm_main)) != cudaSuccess) return e;
   ks<<<dim3(pl.nseg, BH), NT, sm_state, st>>>(q, o, den, g, lengths, ws, s.N, s.H, pl.nseg,
                                               pl.seg_len);
-  k_seg_sum<<<BH, 256, 0, st>>>(ws, pl.nseg, D * M, D, R, r);
+  k_seg_sum<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(ws, pl.nseg, D * M, D, R, r);
   kb<<<dim3(pl.nseg, BH), NT, sm_main, st>>>(q, k, v, o, den, g, S, Z, R, r, lengths, dq, dk, dv,
                                              s.N, s.H, pl.nseg, pl.seg_len);
   return cudaGetLastError();

@@ -68,6 +68,13 @@ SMALL = [
     (2, 2, 257, 64, 64, "bf16"),
     (1, 1, 2049, 32, 32, "bf16"),
     (2, 1, 77, 16, 16, "bf16"),
+    # bf16 with D = M = 64 runs on the tensor cores: 128-token chunks, segments
+    (1, 1, 1, 64, 64, "bf16"),
+    (1, 1, 100, 64, 64, "bf16"),
+    (1, 3, 128, 64, 64, "bf16"),
+    (3, 1, 1000, 64, 64, "bf16"),
+    (40, 4, 300, 64, 64, "bf16"),
+    (1, 1, 4097, 64, 64, "bf16"),
 ]
 
 
