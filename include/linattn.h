@@ -101,6 +101,28 @@ int la_causal_bwd(const void* q, const void* k, const void* v, const void* out,
                   int M, int dtype, void* stream);
 
 /*
+ * la_causal_fwd for callers that cannot allocate device memory: the same
+ * operation and arguments minus the workspace, which is taken from a fixed
+ * scratch array built into the library (LA_NOALLOC_SCRATCH_BYTES per GPU that
+ * loads the library, held until the process exits).  The paper has no
+ * counterpart; this exists for code that runs inside a host application that
+ * owns all device memory (e.g. a plug-in with a fixed memory budget) or in
+ * loops where a cudaMalloc, which may synchronise the device, is not allowed.
+ *  - Returns LA_ERR_WORKSPACE, launching nothing, when the problem needs more
+ *    scratch than the array holds (la_workspace_bytes(LA_OP_CAUSAL_FWD, ...) >
+ *    LA_NOALLOC_SCRATCH_BYTES); other errors as la_causal_fwd.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents; calls that overlap on the GPU (other streams, other threads)
+ *    race on it, so order them on one stream or serialise them.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES (4u << 20)
+int la_causal_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* den,
+                          int B, int H, int N, int D, int M, int dtype, void* stream);
+
+/*
  * Non-causal forward with one shared state per (b, h):
  *   S = sum_{j<L_b} phi(K_j) V_j^T,  Z = sum_{j<L_b} phi(K_j),
  *   out_i = phi(Q_i)^T S / phi(Q_i)^T Z  for i < L_b, and 0 for i >= L_b.

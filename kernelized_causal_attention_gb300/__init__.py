@@ -43,6 +43,7 @@ _SIGS = {
     "la_noncausal_fwd": ("p p p p p p p p p z i i i i i i p", ctypes.c_int),
     "la_noncausal_bwd": ("p p p p p p p p p p p p p z i i i i i i p", ctypes.c_int),
     "la_decode_step": ("p p p p p p i i i i i p", ctypes.c_int),
+    "la_causal_fwd_noalloc": ("p p p p p i i i i i i p", ctypes.c_int),
 }
 EXPORTED = tuple(_SIGS)
 
@@ -159,6 +160,13 @@ def la_noncausal_bwd(q, k, v, lengths, out, den, S, Z, dout, dq, dk, dv, workspa
 def la_decode_step(q, k, v, S, Z, y, B, H, D, M, dtype, stream=None):
     _check(lib().la_decode_step(_p(q), _p(k), _p(v), _p(S), _p(Z), _p(y), B, H, D, M, dtype,
                                 _stream(stream)), "la_decode_step")
+
+
+def la_causal_fwd_noalloc(q, k, v, out, den, B, H, N, D, M, dtype, stream=None):
+    """la_causal_fwd with the library's built-in scratch instead of a workspace
+    (for callers that may not allocate device memory)."""
+    _check(lib().la_causal_fwd_noalloc(_p(q), _p(k), _p(v), _p(out), _p(den), B, H, N, D, M,
+                                       dtype, _stream(stream)), "la_causal_fwd_noalloc")
 
 
 # --------------------------------------------------- allocating convenience API
