@@ -67,11 +67,11 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
-      mbar_init(&bar_phi[s], 128);
+      mbar_init(&bar_phi[s], NCOMP);
     }
     mbar_init(&bar_a, 1);
-    mbar_init(&bar_p, 128);
-    mbar_init(&bar_sp, 128);
+    mbar_init(&bar_p, NCOMP);
+    mbar_init(&bar_sp, NCOMP);
     mbar_init(&bar_o, 1);
     mbar_init(&bar_s, 1);
     fence_barrier_init();
@@ -82,19 +82,20 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (warp == 1) tmem_alloc(&tmem_base, 512);
   if (warp >= 2) {  // the constant ones tile: column 0 = 1, the rest 0
     const int t = threadIdx.x - 64;
-    for (int v = t; v < TILE / 16; v += 128) {
+    for (int v = t; v < TILE / 16; v += NCOMP) {
       const int r = v >> 3, c = (v & 7) ^ (r & 7);  // logical 16-byte chunk of this vector
       *reinterpret_cast<uint4*>(sm + F_ONES + v * 16) =
           c == 0 ? make_uint4(0x3f80u, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
     }
     if (MODE == 1)
-      for (int v = t; v < 8192 / 16; v += 128)
+      for (int v = t; v < 8192 / 16; v += NCOMP)
         *reinterpret_cast<uint4*>(sm + F_SP + 8192 + v * 16) = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_wait();  // the previous kernel's outputs are visible from here on
   const uint32_t tm = tmem_base;
   const uint32_t TA = tm, TO = tm + 128, TS = tm + 256;
 
@@ -122,48 +123,57 @@ __global__ void __launch_bounds__(NTHR, 1)
       constexpr uint32_t ID_O = idesc_bf16(128, TC_MA, false, true);
       constexpr uint32_t ID_S = idesc_bf16(64, TC_MA, true, true);
       const uint32_t ones = smem_u32(sm + F_ONES);
-      const uint32_t pb = smem_u32(sm + F_P), spb = smem_u32(sm + F_SP);
+      const uint64_t dP = sdesc(smem_u32(sm + F_P), 16, 1024);
+      const uint64_t dSP = sdesc(smem_u32(sm + F_SP), 8192, 1024);
       for (int c = 0; c < nch; ++c) {
         const int s = c % NST;
         const uint32_t q = smem_u32(sm + s * F_STAGE), k = q + TILE, v = q + 2 * TILE;
+        const uint64_t dQ = sdesc(q, 16, 1024), dK = sdesc(k, 16, 1024);
+        const uint64_t dVt = sdesc(v, ones - v, 1024);  // [V | ones] as an MN-major operand
         if (!mbar_wait(&bar_phi[s], (c / NST) & 1, WAIT_NS)) {
           fail(err, 12);
           break;
         }
         tc_fence_after();
         if (MODE == 1) {
+#pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // A = phi(Q) phi(K)^T
-            mma_bf16(TA, sdesc(q + 32 * kk, 16, 1024), sdesc(k + 32 * kk, 16, 1024), ID_A, kk > 0);
+            mma_bf16(TA, dadd(dQ, 32 * kk), dadd(dK, 32 * kk), ID_A, kk > 0);
           mma_commit(&bar_a);
           if (!mbar_wait(&bar_p, c & 1, WAIT_NS) || !mbar_wait(&bar_sp, c & 1, WAIT_NS)) {
             fail(err, 13);
             break;
           }
           tc_fence_after();
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // O~ = P V~
-            mma_bf16(TO, sdesc(pb + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024),
-                     sdesc(v + kk * 2048, ones - v, 1024), ID_O, kk > 0);
+            mma_bf16(TO, dadd(dP, (kk >> 2) * TILE + (kk & 3) * 32), dadd(dVt, kk * 2048), ID_O, kk > 0);
+#pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // O~ += phi(Q) S~_prev
-            mma_bf16(TO, sdesc(q + 32 * kk, 16, 1024), sdesc(spb + kk * 2048, 8192, 1024), ID_O, 1);
+            mma_bf16(TO, dadd(dQ, 32 * kk), dadd(dSP, kk * 2048), ID_O, 1);
           mma_commit(&bar_o);
         }
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // S~ += phi(K)^T V~
-          mma_bf16(TS, sdesc(k + kk * 2048, 16, 1024), sdesc(v + kk * 2048, ones - v, 1024), ID_S, 1);
+          mma_bf16(TS, dadd(dK, kk * 2048), dadd(dVt, kk * 2048), ID_S, 1);
         if (MODE == 1 || c == nch - 1) mma_commit(&bar_s);  // MODE 0: only the final state
         mma_commit(&bar_empty[s]);
       }
     }
   } else {
     // -------------------------------------------------------- compute warps
-    const int t = threadIdx.x - 64;        // 0..127
+    // Two warpgroups; both cover all 128 rows (TMEM lanes) and split the
+    // columns: warpgroup wg takes keys 64wg.. of A and outputs 32wg.. of O.
+    const int t = threadIdx.x - 64;        // 0 .. NCOMP-1
+    const int wg = t >> 7;
     const int qd = warp & 3;               // TMEM lane quarter of this warp
     const int row = 32 * qd + lane;        // chunk row == TMEM lane
     const uint32_t lq = static_cast<uint32_t>(32 * qd) << 16;
     const bool has_s = lane < 16;          // M=64 accumulators: row 16*qd + lane in lane 32*qd + lane
     const int srow = 16 * qd + lane;
-    float sv[TC_MA];
-    {  // initial state: the exclusive prefix (MODE 1) = sum of the partial
-       // states of the earlier segments written by MODE 0; zero otherwise
+    if (wg == 0) {  // initial state: the sum of the earlier segments' partial
+                    // states written by MODE 0 (MODE 1), zero otherwise
+      float sv[TC_MA];
       for (int j = 0; j < TC_MA; ++j) sv[j] = 0.f;
       if (MODE == 1 && has_s)
         for (int pp = 0; pp < p; ++pp) {
@@ -185,9 +195,9 @@ __global__ void __launch_bounds__(NTHR, 1)
         float z8[8] = {sv[64], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         st_row_chunk(sm + F_SP + 8192, srow, 0, z8);
       }
-      fence_proxy_async();
-      tc_fence_before();
     }
+    fence_proxy_async();
+    tc_fence_before();
     bool ok = true;
     // phi on chunk 0
     if (!mbar_wait(&bar_full[0], 0, WAIT_NS)) {
@@ -205,24 +215,19 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int c = 0; ok && c < nch; ++c) {
       const int n0 = nb + c * TC_C;
       if (MODE == 1) {
-        // P = bf16(mask(A)): row `row` keeps keys j <= row
+        // P = bf16(mask(A)) for keys 64wg .. 64wg+63: row keeps keys j <= row
         if (!mbar_wait(&bar_a, c & 1, WAIT_NS)) {
           fail(err, 15);
           break;
         }
         tc_fence_after();
-        for (int g = 0; g < 4; ++g) {  // 32 keys per group
-          float a[32];
-          tmem_ld16(TA + lq + 32 * g, a);
-          tmem_ld16(TA + lq + 32 * g + 16, a + 16);
-          tmem_ld_wait();
+        float a[64];
+        tmem_ldn<4>(TA + lq + 64 * wg, a);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (32 * g + i > row) a[i] = 0.f;
-          uint8_t* half = sm + F_P + (g >> 1) * TILE;
+        for (int i = 0; i < 64; ++i)
+          if (64 * wg + i > row) a[i] = 0.f;
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) st_row_chunk(half, row, (g & 1) * 4 + c8, a + 8 * c8);
-        }
+        for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(sm + F_P + wg * TILE, row, c8, a + 8 * c8);
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(&bar_p);
@@ -241,39 +246,45 @@ __global__ void __launch_bounds__(NTHR, 1)
         mbar_arrive(&bar_phi[s1]);
       }
       if (MODE == 1) {
-        // out = O~[:, :64] / O~[:, 64]
+        // out = O~[:, :64] / O~[:, 64], columns 32wg .. 32wg+31
         if (!mbar_wait(&bar_o, c & 1, WAIT_NS)) {
           fail(err, 17);
           break;
         }
         tc_fence_after();
-        float o[TC_MA];
-        tmem_ld80(TO + lq, o);
+        float o[48];
+        tmem_ld16(TO + lq + 32 * wg, o);
+        tmem_ld16(TO + lq + 32 * wg + 16, o + 16);
+        tmem_ld16(TO + lq + 64, o + 32);
+        tmem_ld_wait();
         const int n = n0 + row;
         if (n < ne) {
-          const float d = o[64];
+          const float d = o[32];
           const float inv = 1.f / d;
-          uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<long>(bh) * N + n) * 64);
 #pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8)
-            dst[c8] = make_uint4(pack_bf16(o[8 * c8] * inv, o[8 * c8 + 1] * inv),
-                                 pack_bf16(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv),
-                                 pack_bf16(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv),
-                                 pack_bf16(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv));
-          if (den != nullptr) den[static_cast<long>(bh) * N + n] = d;
+          for (int i = 0; i < 32; ++i) o[i] *= inv;
+          store32_bf16(out + (static_cast<long>(bh) * N + n) * 64 + 32 * wg, o);
+          if (den != nullptr && wg == 0) den[static_cast<long>(bh) * N + n] = d;
         }
-        // next chunk's S~_prev in bf16
+        // next chunk's S~_prev in bf16: warpgroup 0 columns 0-47, 1 columns 48-79
         if (c + 1 < nch) {
           if (!mbar_wait(&bar_s, c & 1, WAIT_NS)) {
             fail(err, 18);
             break;
           }
           tc_fence_after();
-          tmem_ld80(TS + lq, sv);
-          if (has_s) {
-            for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(sm + F_SP, srow, c8, sv + 8 * c8);
-            float z8[8] = {sv[64], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            st_row_chunk(sm + F_SP + 8192, srow, 0, z8);
+          float sv[48];
+          if (wg == 0) {
+            tmem_ldn<3>(TS + lq, sv);
+            if (has_s)
+              for (int c8 = 0; c8 < 6; ++c8) st_row_chunk(sm + F_SP, srow, c8, sv + 8 * c8);
+          } else {
+            tmem_ldn<2>(TS + lq + 48, sv);
+            if (has_s) {
+              for (int c8 = 0; c8 < 2; ++c8) st_row_chunk(sm + F_SP, srow, 6 + c8, sv + 8 * c8);
+              float z8[8] = {sv[16], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+              st_row_chunk(sm + F_SP + 8192, srow, 0, z8);
+            }
           }
           fence_proxy_async();
           tc_fence_before();
@@ -287,10 +298,16 @@ __global__ void __launch_bounds__(NTHR, 1)
       if (!done) fail(err, 19);
       if (done) {
         tc_fence_after();
-        tmem_ld80(TS + lq, sv);
-        if (has_s) {
-          float* dst = ws + ((static_cast<long>(bh) * nseg + p) * 64 + srow) * TC_MA;
-          for (int j = 0; j < TC_MA; ++j) dst[j] = sv[j];
+        float sv[48];
+        float* dst = ws + ((static_cast<long>(bh) * nseg + p) * 64 + srow) * TC_MA;
+        if (wg == 0) {
+          tmem_ldn<3>(TS + lq, sv);
+          if (has_s)
+            for (int j = 0; j < 48; ++j) dst[j] = sv[j];
+        } else {
+          tmem_ldn<2>(TS + lq + 48, sv);
+          if (has_s)
+            for (int j = 0; j < 32; ++j) dst[48 + j] = sv[j];
         }
       }
     }
@@ -370,11 +387,15 @@ cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out
     return e;
   if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
   if (pl.nseg > 1) {
-    k_tc_fwd<0><<<dim3(pl.nseg, BH), NTHR, F_SMEM, st>>>(mq, mk, mv, nullptr, nullptr, ws, s.N,
-                                                         pl.nseg, pl.seg_len, err);
+    if ((e = launch_pdl(k_tc_fwd<0>, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv,
+                        static_cast<bf16*>(nullptr), static_cast<float*>(nullptr), ws, s.N,
+                        pl.nseg, pl.seg_len, err)) != cudaSuccess)
+      return e;
   }
-  k_tc_fwd<1><<<dim3(pl.nseg, BH), NTHR, F_SMEM, st>>>(mq, mk, mv, static_cast<bf16*>(out), den,
-                                                       ws, s.N, pl.nseg, pl.seg_len, err);
+  if ((e = launch_pdl(k_tc_fwd<1>, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv,
+                      static_cast<bf16*>(out), den, ws, s.N, pl.nseg, pl.seg_len, err)) !=
+      cudaSuccess)
+    return e;
   return cudaGetLastError();
 }
 

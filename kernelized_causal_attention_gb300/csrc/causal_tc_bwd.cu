@@ -8,18 +8,19 @@
 //   grad_phiQ  = dP phi(K) + gt S_prev^T + gam z_prev^T          (forward sums)
 //   grad_phiK  = dP^T phi(Q) + V R_next^T + r_next                (reverse sums)
 //   dv         = P^T gt + phi(K) R_next
-//   S += phi(K)^T V, z += sum phi(K);  R += phi(Q)^T gt, r += sum gam phi(Q)
+//   S += phi(K)^T V, z += phi(K)^T 1;  R += phi(Q)^T gt, r += phi(Q)^T gam
 // with P = bf16(mask(phi(Q) phi(K)^T)) and dP = bf16(mask(dA)); then
-// dq = grad_phiQ * phi'(Q), dk = grad_phiK * phi'(K).
+// dq = grad_phiQ * phi'(Q), dk = grad_phiK * phi'(K), and phi'(x) = min(phi(x), 1).
 //
-// Two passes over segments of whole 128-token chunks.  MODE 0 (one CTA per
-// segment) reads dout, out and den once, writes gt (bf16) and gam to the
-// workspace, and the segment's partial S, z, R, r.  MODE 1 runs two roles per
-// segment (grid z): role 0 walks forward carrying S, z and writes dq; role 1
-// walks backward carrying R, r and writes dk and dv.  Each CTA adds up the
-// partial states of the segments before (role 0) or after (role 1) it.  The
-// matrix terms run on tcgen05 (operands TMA-fed, 128-byte swizzle); the
-// vector terms z, r and the gam corrections run on CUDA cores in fp32.
+// Two passes.  MODE 0 (one CTA per sub-segment of whole 128-token chunks)
+// reads q, k, v, dout, out and den once; it stores phi(Q), phi(K) and
+// gt = dout / den (bf16, TMA stores) and gam (fp32) in the workspace, and the
+// sub-segment's partial S, z, R, r.  MODE 1 runs two roles per segment
+// (grid z): role 0 walks forward carrying S, z and writes dq; role 1 walks
+// backward carrying R, r and writes dk and dv.  Each CTA first adds up the
+// partial states of the sub-segments before (role 0) or after (role 1) it.
+// Every product, including the vector sums z and r (against a ones column
+// or the gam column), runs on tcgen05 with TMA-fed operands.
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
@@ -32,131 +33,106 @@ using namespace tc;
 using namespace tcc;
 
 constexpr int DM = 64 * 64;
-constexpr int REC = 2 * (DM + 64);  // per-segment record [S | z | R | r]
+constexpr int REC = 2 * (DM + 64);  // per-sub-segment record [S | z | R | r]
 
-// MODE 0 shared memory: stages of Q, K, V, dout, out; the bf16 gt tile
+// MODE 0 shared memory: stages of q, k, v, dout, out; two gt tiles; ones; two gam tiles
 constexpr int S_STAGE = 5 * TILE;
 constexpr int S_GT = NST * S_STAGE;
-constexpr int S_SMEM = S_GT + TILE + 1024;
-// MODE 1 shared memory: stages of Q, K, V, gt; P; dP; bf16 carried state
+constexpr int S_ONES = S_GT + 2 * TILE;
+constexpr int S_GAMT = S_ONES + 1024;
+constexpr int S_SMEM = S_GAMT + 2 * 2048 + 1024;
+// MODE 1 shared memory: stages of phi(Q), phi(K), v, gt; P; dP; two bf16
+// state tiles; ones; two gam tiles
 constexpr int M_STAGE = 4 * TILE;
 constexpr int M_P = NST * M_STAGE;
 constexpr int M_DP = M_P + 2 * TILE;
 constexpr int M_RP = M_DP + 2 * TILE;
-constexpr int M_SMEM = M_RP + 8192 + 1024;
+constexpr int M_ONES = M_RP + 2 * 8192;
+constexpr int M_GAMT = M_ONES + 1024;
+constexpr int M_SMEM = M_GAMT + 2 * 2048 + 1024;
 static_assert(S_SMEM + 2048 <= 232448 && M_SMEM + 2048 <= 232448, "shared memory");
 
-__device__ __forceinline__ void compute_sync() {  // the four compute warps only
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+// The ones tile (1 KB, every element 1) and two zeroed gam tiles (2 KB each): B
+// operands of the N = 8 products that give z = phi(K)^T 1 and r = phi(Q)^T gam.
+__device__ __forceinline__ void init_vec_tiles(uint8_t* ones, uint8_t* gamt, int t) {
+  for (int v = t; v < 1024 / 16; v += NCOMP)
+    *reinterpret_cast<uint4*>(ones + v * 16) =
+        make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+  for (int v = t; v < 2 * 2048 / 16; v += NCOMP)
+    *reinterpret_cast<uint4*>(gamt + v * 16) = make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Element (r, d) of a swizzled [128][64] bf16 tile, as float.
-__device__ __forceinline__ float tile_at(const uint8_t* tile, int r, int d) {
-  const uint32_t off = static_cast<uint32_t>(r) * 128u +
-                       ((static_cast<uint32_t>(d >> 3) ^ (r & 7u)) << 4) + (d & 7) * 2;
-  return __bfloat162float(*reinterpret_cast<const bf16*>(tile + off));
+// gam_i into row 0, column i of the gam tile (K-major, 128-byte swizzle,
+// two 64-column atoms; row 0 is not permuted by the swizzle).
+__device__ __forceinline__ void put_gam(uint8_t* gamt, int i, float g) {
+  *reinterpret_cast<bf16*>(gamt + (i >> 6) * 1024 + (i & 63) * 2) = __float2bfloat16_rn(g);
 }
 
-// Row r of a swizzled [128][64] bf16 tile as 64 floats.
-__device__ __forceinline__ void tile_row(const uint8_t* tile, int r, float* x) {
+// Reads the 64 fp32 columns at `taddr` (keys 64h .. 64h+63 of row `row`),
+// adds `add`, keeps keys j <= row and stores them as bf16 row `row` of the
+// swizzled [128][64] tile `dst`.
+__device__ __forceinline__ void mask_half_to_smem(uint32_t taddr, float add, uint8_t* dst, int row,
+                                                  int h) {
+  float a[64];
+  tmem_ldn<4>(taddr, a);
 #pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8) {
-    const uint4 u = *reinterpret_cast<const uint4*>(tile + r * 128 + ((c8 ^ (r & 7)) << 4));
-    Vec16<bf16>::unpack(u, x + 8 * c8);
-  }
-}
-
-// Column sums over half of a chunk: thread t sums column (t & 63) over rows
-// 64 (t >> 6) .. + 63, weighted by w[row] when w is given.
-__device__ __forceinline__ float half_colsum(const uint8_t* tile, const float* w, int t) {
-  const int d = t & 63, r0 = (t >> 6) * 64;
-  float acc = 0.f;
-  for (int r = r0; r < r0 + 64; ++r) {
-    const float x = tile_at(tile, r, d);
-    acc = w != nullptr ? fmaf(w[r], x, acc) : acc + x;
-  }
-  return acc;
-}
-
-// 64 fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
-  tmem_ld16(taddr, v);
-  tmem_ld16(taddr + 16, v + 16);
-  tmem_ld16(taddr + 32, v + 32);
-  tmem_ld16(taddr + 48, v + 48);
-  tmem_ld_wait();
-}
-
-// Reads the 128 fp32 columns of row `row` of an accumulator, adds `add`,
-// keeps keys j <= row and stores bf16 row `row` of a [128][128] operand held
-// as two swizzled [128][64] tiles.
-__device__ __forceinline__ void mask_row_to_smem(uint32_t taddr, float add, uint8_t* dst, int row) {
-#pragma unroll 1
-  for (int h = 0; h < 2; ++h) {
-    float a[64];
-    tmem_ld64(taddr + 64 * h, a);
+  for (int i = 0; i < 64; ++i) a[i] = (64 * h + i <= row) ? a[i] + add : 0.f;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) a[i] = (64 * h + i <= row) ? a[i] + add : 0.f;
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(dst + h * TILE, row, c8, a + 8 * c8);
-  }
+  for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(dst, row, c8, a + 8 * c8);
 }
 
-__device__ __forceinline__ void store_row_bf16(bf16* dst, const float* f) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8)
-    d[c8] = make_uint4(pack_bf16(f[8 * c8], f[8 * c8 + 1]), pack_bf16(f[8 * c8 + 2], f[8 * c8 + 3]),
-                       pack_bf16(f[8 * c8 + 4], f[8 * c8 + 5]),
-                       pack_bf16(f[8 * c8 + 6], f[8 * c8 + 7]));
-}
+struct BwdMaps {
+  CUtensorMap q, k, v, g, o;  // MODE 0 inputs
+  CUtensorMap fq, fk, gt;     // MODE 0 outputs, MODE 1 inputs
+};
 
 template <int MODE>
 __global__ void __launch_bounds__(NTHR, 1)
-    k_tc_bwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-             const __grid_constant__ CUtensorMap tmO, const float* __restrict__ den,
-             float* __restrict__ rec, bf16* __restrict__ gt_out, float* __restrict__ gam,
-             bf16* __restrict__ dq, bf16* __restrict__ dk, bf16* __restrict__ dv, int N, int nseg,
-             int seg_len, int* err) {
+    k_tc_bwd(const __grid_constant__ BwdMaps maps, const float* __restrict__ den,
+             float* __restrict__ rec, float* __restrict__ gam, bf16* __restrict__ dq,
+             bf16* __restrict__ dk, bf16* __restrict__ dv, int N, int seg_len, int nsub,
+             int subs_per_seg, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;
   const int role = MODE == 0 ? 2 : static_cast<int>(blockIdx.z);  // 0 dq, 1 dk/dv, 2 partials
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   __shared__ uint64_t bar_full[NST], bar_empty[NST];
-  __shared__ uint64_t bar_in, bar_a, bar_p, bar_rp, bar_o, bar_s;
+  __shared__ uint64_t bar_in, bar_a, bar_p, bar_rp, bar_o, bar_s, bar_s2[2];
   __shared__ uint32_t tmem_base;
-  __shared__ float s_vec[64];        // carried z (role 0) or r (role 1)
-  __shared__ float s_part[2][64];    // per-half column sums of the current chunk
-  __shared__ float s_part2[2][64];   // MODE 0: second set (r)
-  __shared__ float s_gam[TC_C];
+  __shared__ float s_vec[2][64];    // carried z (role 0) or r (role 1) before chunk c, by c & 1
+  __shared__ float s_dot[2][TC_C];  // MODE 0: half-row dot products for gam
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = p * seg_len;
   const int ne = min(N, nb + seg_len);
   const int nch = (ne - nb + TC_C - 1) / TC_C;
   const int stage_bytes = MODE == 0 ? S_STAGE : M_STAGE;
+  uint8_t* ones = sm + (MODE == 0 ? S_ONES : M_ONES);
+  uint8_t* gamt = sm + (MODE == 0 ? S_GAMT : M_GAMT);  // two 2 KB tiles, by chunk parity
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], MODE == 0 ? 1 : 1 + 128);
+      // MODE 0: the MMAs and the thread that TMA-stores from the stage;
+      // MODE 1: the MMAs and every compute thread (epilogues read the stage)
+      mbar_init(&bar_empty[s], MODE == 0 ? 2 : 1 + NCOMP);
     }
-    mbar_init(&bar_in, 128);
+    mbar_init(&bar_in, NCOMP);
     mbar_init(&bar_a, 1);
-    mbar_init(&bar_p, 128);
-    mbar_init(&bar_rp, 128);
+    mbar_init(&bar_p, NCOMP);
+    mbar_init(&bar_rp, NCOMP);
     mbar_init(&bar_o, 1);
     mbar_init(&bar_s, 1);
+    mbar_init(&bar_s2[0], 1);
+    mbar_init(&bar_s2[1], 1);
     fence_barrier_init();
-    prefetch_tensormap(&tmQ);
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-    prefetch_tensormap(&tmG);
-    if (MODE == 0) prefetch_tensormap(&tmO);
+    s_abort = 0;
   }
-  if (threadIdx.x == 0) s_abort = 0;
   if (warp == 1) tmem_alloc(&tmem_base, 512);
+  if (warp >= 2) {
+    init_vec_tiles(ones, gamt, threadIdx.x - 64);
+    fence_proxy_async();
+  }
   // Bounded wait shared by all roles: after the first failure every later
   // wait gives up at once, so all threads still reach the block-wide barriers.
   auto wt = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
@@ -169,8 +145,10 @@ __global__ void __launch_bounds__(NTHR, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_wait();  // the previous kernel's outputs are visible from here on
   const uint32_t tm = tmem_base;
   const uint32_t TA = tm, TDA = tm + 128, TG1 = tm + 256, TG2 = tm + 320, TST = tm + 384;
+  const uint32_t TV = tm + 448, TV2 = tm + 464;  // N = 8 vector accumulators (z / r)
   auto chunk_at = [&](int c) { return role == 1 ? nch - 1 - c : c; };
 
   if (warp == 0) {
@@ -183,123 +161,191 @@ __global__ void __launch_bounds__(NTHR, 1)
         uint8_t* st = sm + s * stage_bytes;
         mbar_arrive_expect_tx(&bar_full[s], ntile * TILE);
         const int n0 = nb + chunk_at(c) * TC_C;
-        tma_load_3d(st, &tmQ, &bar_full[s], 0, n0, bh);
-        tma_load_3d(st + TILE, &tmK, &bar_full[s], 0, n0, bh);
-        tma_load_3d(st + 2 * TILE, &tmV, &bar_full[s], 0, n0, bh);
-        tma_load_3d(st + 3 * TILE, &tmG, &bar_full[s], 0, n0, bh);
-        if (MODE == 0) tma_load_3d(st + 4 * TILE, &tmO, &bar_full[s], 0, n0, bh);
+        if (MODE == 0) {
+          tma_load_3d(st, &maps.q, &bar_full[s], 0, n0, bh);
+          tma_load_3d(st + TILE, &maps.k, &bar_full[s], 0, n0, bh);
+          tma_load_3d(st + 2 * TILE, &maps.v, &bar_full[s], 0, n0, bh);
+          tma_load_3d(st + 3 * TILE, &maps.g, &bar_full[s], 0, n0, bh);
+          tma_load_3d(st + 4 * TILE, &maps.o, &bar_full[s], 0, n0, bh);
+        } else {
+          tma_load_3d(st, &maps.fq, &bar_full[s], 0, n0, bh);
+          tma_load_3d(st + TILE, &maps.fk, &bar_full[s], 0, n0, bh);
+          tma_load_3d(st + 2 * TILE, &maps.v, &bar_full[s], 0, n0, bh);
+          tma_load_3d(st + 3 * TILE, &maps.gt, &bar_full[s], 0, n0, bh);
+        }
       }
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
+    // Per chunk: A and dA, then the carried-state update (it only needs the
+    // stage and frees the compute warps to stage the next state while the
+    // gradient products run), then the gradient products.
     if (lane == 0) {
       constexpr uint32_t ID_AA = idesc_bf16(128, 128, false, false);
       constexpr uint32_t ID_G = idesc_bf16(128, 64, false, false);
       constexpr uint32_t ID_GMN = idesc_bf16(128, 64, false, true);
       constexpr uint32_t ID_GTT = idesc_bf16(128, 64, true, true);
       constexpr uint32_t ID_ST = idesc_bf16(64, 64, true, true);
-      const uint32_t pp = smem_u32(sm + M_P), dp = smem_u32(sm + M_DP), rp = smem_u32(sm + M_RP);
+      constexpr uint32_t ID_V = idesc_bf16(64, 8, true, false);  // phi^T x (ones | gam)
+      const uint64_t dP0 = sdesc(smem_u32(sm + M_P), TILE, 1024);
+      const uint64_t dDP = sdesc(smem_u32(sm + M_DP), 16, 1024);
+      const uint64_t dDPT = sdesc(smem_u32(sm + M_DP), TILE, 1024);
+      const uint64_t dOnes = sdesc(smem_u32(ones), 16, 1024);
       for (int c = 0; c < nch; ++c) {
         const int s = c % NST;
-        const uint32_t qs = smem_u32(sm + s * stage_bytes), ks = qs + TILE, vs = qs + 2 * TILE;
-        const uint32_t gs = MODE == 0 ? smem_u32(sm + S_GT) : qs + 3 * TILE;  // gt operand
+        const uint32_t qs = smem_u32(sm + s * stage_bytes);
+        const uint32_t gs = MODE == 0 ? smem_u32(sm + S_GT + (c & 1) * TILE) : qs + 3 * TILE;
+        const uint64_t dQ = sdesc(qs, 16, 1024), dK = sdesc(qs + TILE, 16, 1024);
+        const uint64_t dV = sdesc(qs + 2 * TILE, 16, 1024), dG = sdesc(gs, 16, 1024);
+        const uint64_t dGam = sdesc(smem_u32(gamt + (c & 1) * 2048), 16, 1024);
+        const uint64_t dRP = sdesc(smem_u32(sm + M_RP + (c & 1) * 8192), 16, 1024);
         if (!wt(&bar_in, c & 1, 22)) break;
         tc_fence_after();
         if (MODE == 0) {
-          for (int kk = 0; kk < 8; ++kk)  // S += phi(K)^T V
-            mma_bf16(TG1, sdesc(ks + kk * 2048, 16, 1024), sdesc(vs + kk * 2048, 16, 1024), ID_ST, 1);
-          for (int kk = 0; kk < 8; ++kk)  // R += phi(Q)^T gt
-            mma_bf16(TST, sdesc(qs + kk * 2048, 16, 1024), sdesc(gs + kk * 2048, 16, 1024), ID_ST, 1);
-          mma_commit(&bar_s);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // S += phi(K)^T V, z += phi(K)^T 1
+            mma_bf16(TG1, dadd(dK, kk * 2048), dadd(dV, kk * 2048), ID_ST, 1);
+            mma_bf16(TV, dadd(dK, kk * 2048), dadd(dOnes, 32 * (kk & 3)), ID_V, 1);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // R += phi(Q)^T gt, r += phi(Q)^T gam
+            mma_bf16(TST, dadd(dQ, kk * 2048), dadd(dG, kk * 2048), ID_ST, 1);
+            mma_bf16(TV2, dadd(dQ, kk * 2048), dadd(dGam, (kk >> 2) * 1024 + 32 * (kk & 3)), ID_V, 1);
+          }
+          mma_commit(&bar_s2[c & 1]);
           mma_commit(&bar_empty[s]);
           continue;
         }
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // dA (without gam) = gt V^T
-          mma_bf16(TDA, sdesc(gs + 32 * kk, 16, 1024), sdesc(vs + 32 * kk, 16, 1024), ID_AA, kk > 0);
+          mma_bf16(TDA, dadd(dG, 32 * kk), dadd(dV, 32 * kk), ID_AA, kk > 0);
         if (role == 1)
+#pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // A = phi(Q) phi(K)^T
-            mma_bf16(TA, sdesc(qs + 32 * kk, 16, 1024), sdesc(ks + 32 * kk, 16, 1024), ID_AA, kk > 0);
+            mma_bf16(TA, dadd(dQ, 32 * kk), dadd(dK, 32 * kk), ID_AA, kk > 0);
         mma_commit(&bar_a);
-        if (!wt(&bar_p, c & 1, 23) || !wt(&bar_rp, c & 1, 23)) break;
+        if (!wt(&bar_rp, c & 1, 23)) break;  // the carried state has been read out
         tc_fence_after();
         if (role == 0) {
-          for (int kk = 0; kk < 8; ++kk)  // dP phi(K)
-            mma_bf16(TG1, sdesc(dp + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024),
-                     sdesc(ks + kk * 2048, 16, 1024), ID_GMN, kk > 0);
-          for (int kk = 0; kk < 4; ++kk)  // + gt S_prev^T
-            mma_bf16(TG1, sdesc(gs + 32 * kk, 16, 1024), sdesc(rp + 32 * kk, 16, 1024), ID_G, 1);
-          mma_commit(&bar_o);
-          for (int kk = 0; kk < 8; ++kk)  // S += phi(K)^T V
-            mma_bf16(TST, sdesc(ks + kk * 2048, 16, 1024), sdesc(vs + kk * 2048, 16, 1024), ID_ST, 1);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // S += phi(K)^T V, z += phi(K)^T 1
+            mma_bf16(TST, dadd(dK, kk * 2048), dadd(dV, kk * 2048), ID_ST, 1);
+            mma_bf16(TV, dadd(dK, kk * 2048), dadd(dOnes, 32 * (kk & 3)), ID_V, 1);
+          }
         } else {
-          for (int kk = 0; kk < 8; ++kk)  // dP^T phi(Q)
-            mma_bf16(TG1, sdesc(dp + kk * 2048, TILE, 1024), sdesc(qs + kk * 2048, 16, 1024), ID_GTT,
-                     kk > 0);
-          for (int kk = 0; kk < 4; ++kk)  // + V R^T
-            mma_bf16(TG1, sdesc(vs + 32 * kk, 16, 1024), sdesc(rp + 32 * kk, 16, 1024), ID_G, 1);
-          for (int kk = 0; kk < 8; ++kk)  // P^T gt
-            mma_bf16(TG2, sdesc(pp + kk * 2048, TILE, 1024), sdesc(gs + kk * 2048, 16, 1024), ID_GTT,
-                     kk > 0);
-          for (int kk = 0; kk < 4; ++kk)  // + phi(K) R
-            mma_bf16(TG2, sdesc(ks + 32 * kk, 16, 1024), sdesc(rp + kk * 2048, 16, 1024), ID_GMN, 1);
-          mma_commit(&bar_o);
-          for (int kk = 0; kk < 8; ++kk)  // R += phi(Q)^T gt
-            mma_bf16(TST, sdesc(qs + kk * 2048, 16, 1024), sdesc(gs + kk * 2048, 16, 1024), ID_ST, 1);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // R += phi(Q)^T gt, r += phi(Q)^T gam
+            mma_bf16(TST, dadd(dQ, kk * 2048), dadd(dG, kk * 2048), ID_ST, 1);
+            mma_bf16(TV, dadd(dQ, kk * 2048), dadd(dGam, (kk >> 2) * 1024 + 32 * (kk & 3)), ID_V, 1);
+          }
         }
         mma_commit(&bar_s);
+        if (!wt(&bar_p, c & 1, 23)) break;
+        tc_fence_after();
+        if (role == 0) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dP phi(K)
+            mma_bf16(TG1, dadd(dDP, (kk >> 2) * TILE + (kk & 3) * 32), dadd(sdesc(qs + TILE, 16, 1024), kk * 2048),
+                     ID_GMN, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // + gt S_prev^T
+            mma_bf16(TG1, dadd(dG, 32 * kk), dadd(dRP, 32 * kk), ID_G, 1);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dP^T phi(Q)
+            mma_bf16(TG1, dadd(dDPT, kk * 2048), dadd(dQ, kk * 2048), ID_GTT, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // + V R^T
+            mma_bf16(TG1, dadd(dV, 32 * kk), dadd(dRP, 32 * kk), ID_G, 1);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // P^T gt
+            mma_bf16(TG2, dadd(dP0, kk * 2048), dadd(dG, kk * 2048), ID_GTT, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // + phi(K) R
+            mma_bf16(TG2, dadd(dK, 32 * kk), dadd(dRP, kk * 2048), ID_GMN, 1);
+        }
+        mma_commit(&bar_o);
         mma_commit(&bar_empty[s]);
       }
     }
   } else {
     // ---------------------------------------------------------- compute warps
-    const int t = threadIdx.x - 64;
+    // Two warpgroups; both cover all 128 rows (TMEM lanes) and split the
+    // columns: warpgroup wg takes keys 64wg.. of A / dA and outputs 32wg..
+    const int t = threadIdx.x - 64;  // 0 .. NCOMP-1
+    const int wg = t >> 7;
     const int qd = warp & 3;
     const int row = 32 * qd + lane;
     const uint32_t lq = static_cast<uint32_t>(32 * qd) << 16;
     const bool has_s = lane < 16;  // M=64 accumulators: row 16*qd + lane in lane 32*qd + lane
     const int srow = 16 * qd + lane;
+    const int c0 = 32 * wg;        // this warpgroup's output columns
     const long hb = static_cast<long>(bh) * N;
-    float sv[64];
+    auto gam_at = [&](int c) {     // gam of this thread's row in chunk c
+      const int n0 = nb + chunk_at(c) * TC_C;
+      return row < min(TC_C, ne - n0) ? gam[hb + n0 + row] : 0.f;
+    };
     if (MODE == 1) {
-      // carried state: role 0 sums the records of earlier segments (S, z),
-      // role 1 those of later segments (R, r)
-      const int lo = role == 0 ? 0 : p + 1, hi = role == 0 ? p : nseg;
-      const int off = role == 0 ? 0 : DM + 64;
-      for (int j = 0; j < 64; ++j) sv[j] = 0.f;
-      float vec = 0.f;
-      for (int pp = lo; pp < hi; ++pp) {
-        const float* r0 = rec + (static_cast<long>(bh) * nseg + pp) * REC + off;
-        if (has_s) {
-          const float4* rr = reinterpret_cast<const float4*>(r0 + srow * 64);
+      // carried state: role 0 sums the records of the sub-segments before this
+      // segment (S, z), role 1 those after it (R, r); warpgroup 0 loads it
+      if (wg == 0) {
+        const int lo = role == 0 ? 0 : (p + 1) * subs_per_seg;
+        const int hi = role == 0 ? p * subs_per_seg : nsub;
+        const int off = role == 0 ? 0 : DM + 64;
+        float sv[64], vv[16];
+        for (int j = 0; j < 64; ++j) sv[j] = 0.f;
+        for (int j = 0; j < 16; ++j) vv[j] = 0.f;
+        for (int pp = lo; pp < hi; ++pp) {
+          const float* r0 = rec + (static_cast<long>(bh) * nsub + pp) * REC + off;
+          if (has_s) {
+            const float4* rr = reinterpret_cast<const float4*>(r0 + srow * 64);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float4 x = rr[j];
-            sv[4 * j] += x.x;
-            sv[4 * j + 1] += x.y;
-            sv[4 * j + 2] += x.z;
-            sv[4 * j + 3] += x.w;
+            for (int j = 0; j < 16; ++j) {
+              const float4 x = rr[j];
+              sv[4 * j] += x.x;
+              sv[4 * j + 1] += x.y;
+              sv[4 * j + 2] += x.z;
+              sv[4 * j + 3] += x.w;
+            }
+            vv[0] += r0[DM + srow];
           }
         }
-        if (t < 64) vec += r0[DM + t];
+        for (int j = 0; j < 64; j += 16) tmem_st16(TST + lq + j, sv + j);
+        for (int j = 1; j < 8; ++j) vv[j] = vv[0];
+        tmem_st16(TV + lq, vv);
+        tmem_st_wait();
+        if (has_s) {
+          for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(sm + M_RP, srow, c8, sv + 8 * c8);
+          s_vec[0][srow] = vv[0];
+        }
       }
-      if (t < 64) s_vec[t] = vec;
-      for (int j = 0; j < 64; j += 16) tmem_st16(TST + lq + j, sv + j);
-      tmem_st_wait();
-      if (has_s)
-        for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(sm + M_RP, srow, c8, sv + 8 * c8);
       fence_proxy_async();
+      compute_sync();
       tc_fence_before();
       mbar_arrive(&bar_rp);
-    } else {
-      for (int j = 0; j < 64; ++j) sv[j] = 0.f;
-      for (int j = 0; j < 64; j += 16) {
-        tmem_st16(TG1 + lq + j, sv + j);
-        tmem_st16(TST + lq + j, sv + j);
+      // chunk 0 inputs
+      const float g0 = gam_at(0);
+      wt(&bar_full[0], 0, 25);
+      if (role == 1 && wg == 0) {
+        put_gam(gamt, row, g0);
+        fence_proxy_async();
       }
-      tmem_st_wait();
+      mbar_arrive(&bar_in);
+    } else {
+      if (wg == 0) {
+        float zero[16];
+        for (int j = 0; j < 16; ++j) zero[j] = 0.f;
+        for (int j = 0; j < 64; j += 16) {
+          tmem_st16(TG1 + lq + j, zero);
+          tmem_st16(TST + lq + j, zero);
+        }
+        tmem_st16(TV + lq, zero);
+        tmem_st16(TV2 + lq, zero);
+        tmem_st_wait();
+      }
       tc_fence_before();
     }
-    float zacc = 0.f, racc = 0.f;  // MODE 0 column-sum accumulators
+    float gm = MODE == 1 ? gam_at(0) : 0.f;
     for (int c = 0; c < nch; ++c) {
       const int s = c % NST;
       const int n0 = nb + chunk_at(c) * TC_C;
@@ -308,113 +354,134 @@ __global__ void __launch_bounds__(NTHR, 1)
       uint8_t* st = sm + s * stage_bytes;
       if (MODE == 0) {
         const float dn = rv ? den[hb + n0 + row] : 1.f;
-        if (c > 0) {  // the gt tile is free once the previous chunk's MMAs finished
-          wt(&bar_s, (c - 1) & 1, 24);
+        if (c > 0 && t == 0) {  // chunk c-1's stores have read its stage: release it
+          if (c > 1) {
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          } else {
+            bulk_wait_read();
+          }
+          mbar_arrive(&bar_empty[(c - 1) % NST]);
+        }
+        if (c > 1) {  // gt / gam tiles of parity c & 1 are free once chunk c-2's MMAs finished
+          wt(&bar_s2[c & 1], ((c - 2) >> 1) & 1, 24);
           tc_fence_after();
         }
+        compute_sync();
         wt(&bar_full[s], (c / NST) & 1, 25);
-        // gt = dout / den, gam = -(gt . out) for this row
-        float g[64], o[64];
-        tile_row(st + 3 * TILE, row, g);
-        tile_row(st + 4 * TILE, row, o);
+        uint8_t* gtile = sm + S_GT + (c & 1) * TILE;
+        // gt = dout / den on this warpgroup's half row; gam = -(gt . out)
+        float g[32], o[32];
+        tile_row_half(st + 3 * TILE, row, wg, g);
+        tile_row_half(st + 4 * TILE, row, wg, o);
         const float inv = 1.f / dn;
         float acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
+        for (int i = 0; i < 32; ++i) {
           g[i] = rv ? g[i] * inv : 0.f;
           acc = fmaf(g[i], o[i], acc);
         }
-        const float gm = rv ? -acc : 0.f;
-        s_gam[row] = gm;
+        s_dot[wg][row] = acc;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(sm + S_GT, row, c8, g + 8 * c8);
-        if (rv) {
-          store_row_bf16(gt_out + (hb + n0 + row) * 64, g);
-          gam[hb + n0 + row] = gm;
-        }
+        for (int c8 = 0; c8 < 4; ++c8) st_row_chunk(gtile, row, 4 * wg + c8, g + 8 * c8);
         phi_tile(st, valid, t);
         phi_tile(st + TILE, valid, t);
         compute_sync();
-        zacc += half_colsum(st + TILE, nullptr, t);
-        racc += half_colsum(st, s_gam, t);
+        if (wg == 0) {
+          const float gmv = rv ? -(s_dot[0][row] + s_dot[1][row]) : 0.f;
+          put_gam(gamt + (c & 1) * 2048, row, gmv);
+          if (rv) gam[hb + n0 + row] = gmv;
+        }
         fence_proxy_async();
+        compute_sync();
+        if (t == 0) {  // phi(Q), phi(K) and gt of this chunk to the workspace
+          tma_store_3d(&maps.fq, st, 0, n0, bh);
+          tma_store_3d(&maps.fk, st + TILE, 0, n0, bh);
+          tma_store_3d(&maps.gt, gtile, 0, n0, bh);
+          bulk_commit();
+        }
         tc_fence_before();
         mbar_arrive(&bar_in);
         continue;
       }
       // ------------------------------------------------------------- MODE 1
-      const float gm = rv ? gam[hb + n0 + row] : 0.f;
-      wt(&bar_full[s], (c / NST) & 1, 25);
-      if (role == 1) phi_tile(st, valid, t);
-      phi_tile(st + TILE, valid, t);
-      if (role == 1) s_gam[row] = gm;
-      compute_sync();
-      const float part = role == 0 ? half_colsum(st + TILE, nullptr, t) : half_colsum(st, s_gam, t);
-      s_part[t >> 6][t & 63] = part;
-      fence_proxy_async();
-      tc_fence_before();
-      mbar_arrive(&bar_in);
-
+      // P, dP of chunk c
       wt(&bar_a, c & 1, 26);
       tc_fence_after();
-      mask_row_to_smem(TDA + lq, gm, sm + M_DP, row);
-      if (role == 1) mask_row_to_smem(TA + lq, 0.f, sm + M_P, row);
+      mask_half_to_smem(TDA + lq + 64 * wg, gm, sm + M_DP + wg * TILE, row, wg);
+      if (role == 1) mask_half_to_smem(TA + lq + 64 * wg, 0.f, sm + M_P + wg * TILE, row, wg);
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&bar_p);
-
+      // inputs of chunk c+1 (the tensor cores may start on it)
+      float gm_next = 0.f;
+      if (c + 1 < nch) {
+        gm_next = gam_at(c + 1);
+        wt(&bar_full[(c + 1) % NST], ((c + 1) / NST) & 1, 25);
+        if (role == 1 && wg == 0) {
+          put_gam(gamt + ((c + 1) & 1) * 2048, row, gm_next);
+          fence_proxy_async();
+        }
+        mbar_arrive(&bar_in);
+      }
+      // carried state for chunk c+1 (after this chunk's update)
+      if (c + 1 < nch) {
+        wt(&bar_s, c & 1, 28);
+        tc_fence_after();
+        float sv[32], vv[16];
+        tmem_ldn<2>(TST + lq + c0, sv);
+        tmem_ldn<1>(TV + lq, vv);
+        if (has_s) {
+          for (int c8 = 0; c8 < 4; ++c8)
+            st_row_chunk(sm + M_RP + ((c + 1) & 1) * 8192, srow, 4 * wg + c8, sv + 8 * c8);
+          if (wg == 0) s_vec[(c + 1) & 1][srow] = vv[0];
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        mbar_arrive(&bar_rp);
+      }
+      // gradients of chunk c
       wt(&bar_o, c & 1, 27);
       tc_fence_after();
       {
-        float gv[64], x[64];
-        tmem_ld64(TG1 + lq, gv);
-        if (role == 0) {  // dq = (grad_phiQ + gam z_prev) * phi'(Q), raw Q in the stage
-          tile_row(st, row, x);
+        const float* vec = s_vec[c & 1];
+        float gv[32], x[32];
+        tmem_ldn<2>(TG1 + lq + c0, gv);
+        if (role == 0) {  // dq = (grad_phiQ + gam z_prev) * phi'(Q)
+          tile_row_half(st, row, wg, x);
 #pragma unroll
-          for (int i = 0; i < 64; ++i) gv[i] = (gv[i] + gm * s_vec[i]) * (x[i] > 0.f ? 1.f : __expf(x[i]));
-          if (rv) store_row_bf16(dq + (hb + n0 + row) * 64, gv);
-        } else {          // dk = (grad_phiK + r_next) * phi'(K), phi'(K) = min(phi(K), 1)
-          tile_row(st + TILE, row, x);
+          for (int i = 0; i < 32; ++i) gv[i] = (gv[i] + gm * vec[c0 + i]) * fminf(x[i], 1.f);
+          if (rv) store32_bf16(dq + (hb + n0 + row) * 64 + c0, gv);
+        } else {          // dk = (grad_phiK + r_next) * phi'(K)
+          tile_row_half(st + TILE, row, wg, x);
 #pragma unroll
-          for (int i = 0; i < 64; ++i) gv[i] = (gv[i] + s_vec[i]) * fminf(x[i], 1.f);
-          if (rv) store_row_bf16(dk + (hb + n0 + row) * 64, gv);
-          tmem_ld64(TG2 + lq, gv);
-          if (rv) store_row_bf16(dv + (hb + n0 + row) * 64, gv);
+          for (int i = 0; i < 32; ++i) gv[i] = (gv[i] + vec[c0 + i]) * fminf(x[i], 1.f);
+          if (rv) store32_bf16(dk + (hb + n0 + row) * 64 + c0, gv);
+          tmem_ldn<2>(TG2 + lq + c0, gv);
+          if (rv) store32_bf16(dv + (hb + n0 + row) * 64 + c0, gv);
         }
       }
       tc_fence_before();
       mbar_arrive(&bar_empty[s]);  // this thread is done with the stage
-      compute_sync();
-      if (t < 64) s_vec[t] += s_part[0][t] + s_part[1][t];  // z or r now includes this chunk
-      wt(&bar_s, c & 1, 28);
-      tc_fence_after();
-      if (c + 1 < nch) {
-        tmem_ld64(TST + lq, sv);
-        if (has_s)
-          for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(sm + M_RP, srow, c8, sv + 8 * c8);
-        fence_proxy_async();
-        compute_sync();  // s_vec updated before the next chunk's epilogue reads it
-        tc_fence_before();
-        mbar_arrive(&bar_rp);
-      }
+      compute_sync();              // s_vec[c & 1] and the P / dP tiles are free again
+      gm = gm_next;
     }
     if (MODE == 0) {
-      s_part[t >> 6][t & 63] = zacc;
-      s_part2[t >> 6][t & 63] = racc;
-      if (wt(&bar_s, (nch - 1) & 1, 29)) {
+      if (t == 0) bulk_wait_all();
+      bool done = true;
+      for (int c = max(0, nch - 2); c < nch; ++c)  // the last two state updates, in order
+        done = wt(&bar_s2[c & 1], (c >> 1) & 1, 29) && done;
+      if (done) {
         tc_fence_after();
-        float* r0 = rec + (static_cast<long>(bh) * nseg + p) * REC;
-        tmem_ld64(TG1 + lq, sv);
+        float* r0 = rec + (static_cast<long>(bh) * nsub + p) * REC;
+        float sv[32], vv[16];
+        tmem_ldn<2>(TG1 + lq + c0, sv);
         if (has_s)
-          for (int j = 0; j < 64; ++j) r0[srow * 64 + j] = sv[j];
-        tmem_ld64(TST + lq, sv);
+          for (int j = 0; j < 32; ++j) r0[srow * 64 + c0 + j] = sv[j];
+        tmem_ldn<2>(TST + lq + c0, sv);
         if (has_s)
-          for (int j = 0; j < 64; ++j) r0[DM + 64 + srow * 64 + j] = sv[j];
-        compute_sync();
-        if (t < 64) {
-          r0[DM + t] = s_part[0][t] + s_part[1][t];
-          r0[2 * DM + 64 + t] = s_part2[0][t] + s_part2[1][t];
-        }
+          for (int j = 0; j < 32; ++j) r0[DM + 64 + srow * 64 + c0 + j] = sv[j];
+        tmem_ldn<1>((wg == 0 ? TV : TV2) + lq, vv);
+        if (has_s) r0[(wg == 0 ? DM : 2 * DM + 64) + srow] = vv[0];
       }
     }
   }
@@ -424,15 +491,61 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (warp == 1) tmem_dealloc(tm, 512);
 }
 
+struct BwdPlan {
+  SegPlan main;   // segments of the second pass (two roles each)
+  int subs;       // sub-segments per segment in the first pass
+  int sub_len;    // tokens per sub-segment
+  int nsub;       // sub-segments per (b, h)
+};
+
+BwdPlan bwd_plan(int BH, int N) {
+  BwdPlan b;
+  b.main = tc_plan(2 * BH, N);
+  const int per = b.main.seg_len / TC_C;
+  b.subs = 1;
+  for (int f = per; f >= 1; --f)
+    if (per % f == 0 && static_cast<long>(b.main.nseg) * f * BH <= 152) {
+      b.subs = f;
+      break;
+    }
+  b.sub_len = b.main.seg_len / b.subs;
+  b.nsub = (N + b.sub_len - 1) / b.sub_len;
+  return b;
+}
+
+struct BwdWs {
+  float* rec;
+  bf16 *gt, *fq, *fk;
+  float* gam;
+  int* err;
+  size_t floats;
+};
+
+BwdWs bwd_ws(float* ws, int BH, int N, const BwdPlan& pl) {
+  BwdWs w;
+  const size_t tok = static_cast<size_t>(BH) * N;
+  w.rec = ws;
+  size_t off = static_cast<size_t>(BH) * pl.nsub * REC;
+  w.gt = reinterpret_cast<bf16*>(ws + off);
+  off += tok * 32;
+  w.fq = reinterpret_cast<bf16*>(ws + off);
+  off += tok * 32;
+  w.fk = reinterpret_cast<bf16*>(ws + off);
+  off += tok * 32;
+  w.gam = ws + off;
+  off += tok;
+  w.err = reinterpret_cast<int*>(ws + off);
+  w.floats = off + 4;
+  return w;
+}
+
 }  // namespace
 
-SegPlan tc_plan_bwd(int BH, int N) { return tc_plan(2 * BH, N); }
-
-// workspace: records [BH][nseg][REC] fp32 | gt bf16 [BH][N][64] | gam fp32 [BH][N] | status
+// workspace: records [BH][nsub][REC] | gt, phi(Q), phi(K) bf16 [BH][N][64] |
+// gam fp32 [BH][N] | status word
 size_t causal_bwd_tc_ws_floats(const Shape& s) {
-  const size_t BH = static_cast<size_t>(s.B) * s.H;
-  const SegPlan pl = tc_plan_bwd(s.B * s.H, s.N);
-  return BH * pl.nseg * REC + BH * s.N * 32 + BH * s.N + 4;
+  const int BH = s.B * s.H;
+  return bwd_ws(nullptr, BH, s.N, bwd_plan(BH, s.N)).floats;
 }
 
 int causal_bwd_tc_launches(const Shape&) { return 2; }
@@ -441,15 +554,13 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
                           const float* den, const void* dout, void* dq, void* dk, void* dv,
                           float* ws, const Shape& s, cudaStream_t st) {
   const int BH = s.B * s.H;
-  const SegPlan pl = tc_plan_bwd(BH, s.N);
-  float* rec = ws;
-  bf16* gt = reinterpret_cast<bf16*>(ws + static_cast<size_t>(BH) * pl.nseg * REC);
-  float* gam = ws + static_cast<size_t>(BH) * pl.nseg * REC + static_cast<size_t>(BH) * s.N * 32;
-  int* err = reinterpret_cast<int*>(gam + static_cast<size_t>(BH) * s.N);
-  CUtensorMap mq, mk, mv, mg, mo, mgt;
-  if (!make_bf16_map(&mq, q, BH, s.N) || !make_bf16_map(&mk, k, BH, s.N) ||
-      !make_bf16_map(&mv, v, BH, s.N) || !make_bf16_map(&mg, dout, BH, s.N) ||
-      !make_bf16_map(&mo, out, BH, s.N) || !make_bf16_map(&mgt, gt, BH, s.N))
+  const BwdPlan pl = bwd_plan(BH, s.N);
+  const BwdWs w = bwd_ws(ws, BH, s.N, pl);
+  BwdMaps m;
+  if (!make_bf16_map(&m.q, q, BH, s.N) || !make_bf16_map(&m.k, k, BH, s.N) ||
+      !make_bf16_map(&m.v, v, BH, s.N) || !make_bf16_map(&m.g, dout, BH, s.N) ||
+      !make_bf16_map(&m.o, out, BH, s.N) || !make_bf16_map(&m.fq, w.fq, BH, s.N) ||
+      !make_bf16_map(&m.fk, w.fk, BH, s.N) || !make_bf16_map(&m.gt, w.gt, BH, s.N))
     return cudaErrorInvalidValue;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(k_tc_bwd<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -458,13 +569,17 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
   if ((e = cudaFuncSetAttribute(k_tc_bwd<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 M_SMEM)) != cudaSuccess)
     return e;
-  if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
-  k_tc_bwd<0><<<dim3(pl.nseg, BH, 1), NTHR, S_SMEM, st>>>(mq, mk, mv, mg, mo, den, rec, gt, gam,
-                                                          nullptr, nullptr, nullptr, s.N, pl.nseg,
-                                                          pl.seg_len, err);
-  k_tc_bwd<1><<<dim3(pl.nseg, BH, 2), NTHR, M_SMEM, st>>>(
-      mq, mk, mv, mgt, mgt, den, rec, gt, gam, static_cast<bf16*>(dq), static_cast<bf16*>(dk),
-      static_cast<bf16*>(dv), s.N, pl.nseg, pl.seg_len, err);
+  if ((e = cudaMemsetAsync(w.err, 0, sizeof(int), st)) != cudaSuccess) return e;
+  if ((e = launch_pdl(k_tc_bwd<0>, dim3(pl.nsub, BH, 1), dim3(NTHR), S_SMEM, st, m, den, w.rec,
+                      w.gam, static_cast<bf16*>(nullptr), static_cast<bf16*>(nullptr),
+                      static_cast<bf16*>(nullptr), s.N, pl.sub_len, pl.nsub, pl.subs, w.err)) !=
+      cudaSuccess)
+    return e;
+  if ((e = launch_pdl(k_tc_bwd<1>, dim3(pl.main.nseg, BH, 2), dim3(NTHR), M_SMEM, st, m, den,
+                      w.rec, w.gam, static_cast<bf16*>(dq), static_cast<bf16*>(dk),
+                      static_cast<bf16*>(dv), s.N, pl.main.seg_len, pl.nsub, pl.subs, w.err)) !=
+      cudaSuccess)
+    return e;
   return cudaGetLastError();
 }
 

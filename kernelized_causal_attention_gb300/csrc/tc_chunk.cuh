@@ -4,6 +4,9 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <utility>
 
 #include "tc.cuh"
 
@@ -16,7 +19,8 @@ using bf16 = __nv_bfloat16;
 constexpr int TC_C = 128;                  // tokens per chunk (MMA M)
 constexpr int NST = 2;                     // TMA ring stages
 constexpr int TILE = TC_C * 64 * 2;        // one [128][64] bf16 tile
-constexpr int NTHR = 192;                  // warp 0 TMA, warp 1 MMA, warps 2-5 compute
+constexpr int NCOMP = 256;                 // compute threads: two warpgroups
+constexpr int NTHR = 64 + NCOMP;           // warp 0 TMA, warp 1 MMA, warps 2-9 compute
 constexpr uint64_t WAIT_NS = 2000000000ull;  // bound on every wait
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -27,30 +31,47 @@ __device__ __forceinline__ void fail(int* err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
 }
 
-// phi applied in place to a swizzled [128][64] bf16 tile by the 128 compute
+// phi(x) = elu(x) + 1 (eq. 7) on a pair of bf16 values, written as
+// max(x, 0) + min(exp(x), 1): x + 1 for x > 0 and exp(x) otherwise.  The
+// exponential is the hardware base-2 exponential on bf16 pairs,
+// exp(x) = 2^(x log2 e), with x log2 e formed in fp32 and rounded to bf16.
+__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+  constexpr float kLog2e = 1.4426950408889634f;
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo * kLog2e, hi * kLog2e);
+  uint32_t e;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(*reinterpret_cast<uint32_t*>(&t)));
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f), one = __float2bfloat162_rn(1.f);
+  const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w);
+  const __nv_bfloat162 ex = *reinterpret_cast<const __nv_bfloat162*>(&e);
+  const __nv_bfloat162 r = __hadd2(__hmax2(x, zero), __hmin2(ex, one));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// phi applied in place to a swizzled [128][64] bf16 tile by the NCOMP compute
 // threads (elementwise, so the swizzle does not matter).  Rows at or past
 // `valid` are zeroed: a zero phi(K) row adds nothing to any sum.
 __device__ __forceinline__ void phi_tile(uint8_t* tile, int valid, int t) {
-  for (int v = t; v < TILE / 16; v += 128) {
+  for (int v = t; v < TILE / 16; v += NCOMP) {
     uint4* ptr = reinterpret_cast<uint4*>(tile + v * 16);
     uint4 u = *ptr;
-    if ((v >> 3) >= valid) {
+    if ((v >> 3) >= valid)
       u = make_uint4(0u, 0u, 0u, 0u);
-    } else {
-      uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-        const float plo = lo > 0.f ? lo + 1.f : __expf(lo);
-        const float phi_ = hi > 0.f ? hi + 1.f : __expf(hi);
-        __nv_bfloat162 b = __floats2bfloat162_rn(plo, phi_);
-        w[i] = *reinterpret_cast<uint32_t*>(&b);
-      }
-      u = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    else
+      u = make_uint4(phi_bf16x2(u.x), phi_bf16x2(u.y), phi_bf16x2(u.z), phi_bf16x2(u.w));
     *ptr = u;
   }
 }
+
+// A shared-memory descriptor advanced by `bytes` (the start-address field is
+// the low 14 bits in 16-byte units; shared addresses stay below 256 KB).
+__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its memory is visible.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -76,7 +97,63 @@ __device__ __forceinline__ void tmem_ld80(uint32_t taddr, float* v) {
   tmem_ld_wait();
 }
 
+// 16 * n fp32 columns of this thread's TMEM lane (n = 1..4), one wait.
+template <int n>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, float* v) {
+#pragma unroll
+  for (int i = 0; i < n; ++i) tmem_ld16(taddr + 16 * i, v + 16 * i);
+  tmem_ld_wait();
+}
+
+// Columns 32h .. 32h+31 of row r of a swizzled [128][64] bf16 tile as floats.
+__device__ __forceinline__ void tile_row_half(const uint8_t* tile, int r, int h, float* x) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int c8 = 4 * h + c;
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + r * 128 + ((c8 ^ (r & 7)) << 4));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[8 * c + 2 * i] = __uint_as_float(w[i] << 16);
+      x[8 * c + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+}
+
+// 32 floats as bf16 to global memory (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void store32_bf16(bf16* dst, const float* f) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    d[c] = make_uint4(pack_bf16(f[8 * c], f[8 * c + 1]), pack_bf16(f[8 * c + 2], f[8 * c + 3]),
+                      pack_bf16(f[8 * c + 4], f[8 * c + 5]), pack_bf16(f[8 * c + 6], f[8 * c + 7]));
+}
+
+__device__ __forceinline__ void compute_sync() {  // the compute warps only
+  asm volatile("bar.sync 1, %0;" ::"n"(NCOMP) : "memory");
+}
+
 }  // namespace tcc
+
+// Launches `kernel` with programmatic stream serialisation, so that its CTAs
+// may start (and run their prologue) while the previous kernel drains.  The
+// kernel must call grid_dep_wait() before touching memory the previous
+// kernel writes.
+template <typename... Exp, typename... Act>
+cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
+}
 
 // [BH][N][64] bf16 viewed as a 3-D TMA tensor with 64 x 128 x 1 boxes and the
 // 128-byte swizzle (defined in causal_tc.cu).
