@@ -14,13 +14,14 @@
 //
 // Two passes.  MODE 0 (one CTA per sub-segment of whole 128-token chunks)
 // reads q, k, v, dout, out and den once; it stores phi(Q), phi(K) and
-// gt = dout / den (bf16, TMA stores) and gam (fp32) in the workspace, and the
+// gt = dout / den (bf16) and gam (fp32) in the workspace, and the
 // sub-segment's partial S, z, R, r.  MODE 1 runs two roles per segment
 // (grid z): role 0 walks forward carrying S, z and writes dq; role 1 walks
 // backward carrying R, r and writes dk and dv.  Each CTA first adds up the
 // partial states of the sub-segments before (role 0) or after (role 1) it.
 // Every product, including the vector sums z and r (against a ones column
-// or the gam column), runs on tcgen05 with TMA-fed operands.
+// or the gam column), runs on tcgen05 with TMA-fed operands; dq, dk and dv
+// are staged in shared memory and written with TMA stores.
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
@@ -81,16 +82,41 @@ __device__ __forceinline__ void mask_half_to_smem(uint32_t taddr, float add, uin
   for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(dst, row, c8, a + 8 * c8);
 }
 
+// Role 1: the masked bf16 rows of dA (+ gam) and of A for keys 64h..64h+63,
+// loaded together so that one wait covers both accumulators.
+__device__ __forceinline__ void mask2_half_to_smem(uint32_t tda, uint32_t ta, float add,
+                                                   uint8_t* ddst, uint8_t* adst, int row, int h) {
+  float d[64], a[64];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    tmem_ld16(tda + 16 * i, d + 16 * i);
+    tmem_ld16(ta + 16 * i, a + 16 * i);
+  }
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const bool keep = 64 * h + i <= row;
+    d[i] = keep ? d[i] + add : 0.f;
+    a[i] = keep ? a[i] : 0.f;
+  }
+#pragma unroll
+  for (int c8 = 0; c8 < 8; ++c8) {
+    st_row_chunk(ddst, row, c8, d + 8 * c8);
+    st_row_chunk(adst, row, c8, a + 8 * c8);
+  }
+}
+
 struct BwdMaps {
   CUtensorMap q, k, v, g, o;  // MODE 0 inputs
   CUtensorMap fq, fk, gt;     // MODE 0 outputs, MODE 1 inputs
+  CUtensorMap dq, dk, dv;     // MODE 1 outputs (TMA stores)
 };
 
 template <int MODE>
 __global__ void __launch_bounds__(NTHR, 1)
     k_tc_bwd(const __grid_constant__ BwdMaps maps, const float* __restrict__ den,
-             float* __restrict__ rec, float* __restrict__ gam, bf16* __restrict__ dq,
-             bf16* __restrict__ dk, bf16* __restrict__ dv, int N, int seg_len, int nsub,
+             float* __restrict__ rec, float* __restrict__ gam, bf16* __restrict__ gt_out,
+             bf16* __restrict__ fq_out, bf16* __restrict__ fk_out, int N, int seg_len, int nsub,
              int subs_per_seg, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;
   const int role = MODE == 0 ? 2 : static_cast<int>(blockIdx.z);  // 0 dq, 1 dk/dv, 2 partials
@@ -113,9 +139,9 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bar_full[s], 1);
-      // MODE 0: the MMAs and the thread that TMA-stores from the stage;
-      // MODE 1: the MMAs and every compute thread (epilogues read the stage)
-      mbar_init(&bar_empty[s], MODE == 0 ? 2 : 1 + NCOMP);
+      // MODE 0: the MMAs; MODE 1: the MMAs and every compute thread
+      // (the epilogues read phi from the stage)
+      mbar_init(&bar_empty[s], MODE == 0 ? 1 : 1 + NCOMP);
     }
     mbar_init(&bar_in, NCOMP);
     mbar_init(&bar_a, 1);
@@ -354,14 +380,6 @@ __global__ void __launch_bounds__(NTHR, 1)
       uint8_t* st = sm + s * stage_bytes;
       if (MODE == 0) {
         const float dn = rv ? den[hb + n0 + row] : 1.f;
-        if (c > 0 && t == 0) {  // chunk c-1's stores have read its stage: release it
-          if (c > 1) {
-            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-          } else {
-            bulk_wait_read();
-          }
-          mbar_arrive(&bar_empty[(c - 1) % NST]);
-        }
         if (c > 1) {  // gt / gam tiles of parity c & 1 are free once chunk c-2's MMAs finished
           wt(&bar_s2[c & 1], ((c - 2) >> 1) & 1, 24);
           tc_fence_after();
@@ -383,8 +401,9 @@ __global__ void __launch_bounds__(NTHR, 1)
         s_dot[wg][row] = acc;
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) st_row_chunk(gtile, row, 4 * wg + c8, g + 8 * c8);
-        phi_tile(st, valid, t);
-        phi_tile(st + TILE, valid, t);
+        if (rv) store32_bf16(gt_out + (hb + n0 + row) * 64 + c0, g);
+        phi_tile_store(st, valid, t, fq_out + (hb + n0) * 64);
+        phi_tile_store(st + TILE, valid, t, fk_out + (hb + n0) * 64);
         compute_sync();
         if (wg == 0) {
           const float gmv = rv ? -(s_dot[0][row] + s_dot[1][row]) : 0.f;
@@ -392,13 +411,6 @@ __global__ void __launch_bounds__(NTHR, 1)
           if (rv) gam[hb + n0 + row] = gmv;
         }
         fence_proxy_async();
-        compute_sync();
-        if (t == 0) {  // phi(Q), phi(K) and gt of this chunk to the workspace
-          tma_store_3d(&maps.fq, st, 0, n0, bh);
-          tma_store_3d(&maps.fk, st + TILE, 0, n0, bh);
-          tma_store_3d(&maps.gt, gtile, 0, n0, bh);
-          bulk_commit();
-        }
         tc_fence_before();
         mbar_arrive(&bar_in);
         continue;
@@ -407,8 +419,13 @@ __global__ void __launch_bounds__(NTHR, 1)
       // P, dP of chunk c
       wt(&bar_a, c & 1, 26);
       tc_fence_after();
-      mask_half_to_smem(TDA + lq + 64 * wg, gm, sm + M_DP + wg * TILE, row, wg);
-      if (role == 1) mask_half_to_smem(TA + lq + 64 * wg, 0.f, sm + M_P + wg * TILE, row, wg);
+      if (t == 0) bulk_wait_read();  // the previous chunk's output tiles have left P / dP
+      compute_sync();
+      if (role == 1)
+        mask2_half_to_smem(TDA + lq + 64 * wg, TA + lq + 64 * wg, gm, sm + M_DP + wg * TILE,
+                           sm + M_P + wg * TILE, row, wg);
+      else
+        mask_half_to_smem(TDA + lq + 64 * wg, gm, sm + M_DP + wg * TILE, row, wg);
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&bar_p);
@@ -439,7 +456,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         tc_fence_before();
         mbar_arrive(&bar_rp);
       }
-      // gradients of chunk c
+      // gradients of chunk c, staged in the free P / dP tiles and TMA-stored
       wt(&bar_o, c & 1, 27);
       tc_fence_after();
       {
@@ -450,23 +467,37 @@ __global__ void __launch_bounds__(NTHR, 1)
           tile_row_half(st, row, wg, x);
 #pragma unroll
           for (int i = 0; i < 32; ++i) gv[i] = (gv[i] + gm * vec[c0 + i]) * fminf(x[i], 1.f);
-          if (rv) store32_bf16(dq + (hb + n0 + row) * 64 + c0, gv);
-        } else {          // dk = (grad_phiK + r_next) * phi'(K)
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) st_row_chunk(sm + M_DP, row, 4 * wg + c8, gv + 8 * c8);
+        } else {          // dk = (grad_phiK + r_next) * phi'(K), dv
           tile_row_half(st + TILE, row, wg, x);
 #pragma unroll
           for (int i = 0; i < 32; ++i) gv[i] = (gv[i] + vec[c0 + i]) * fminf(x[i], 1.f);
-          if (rv) store32_bf16(dk + (hb + n0 + row) * 64 + c0, gv);
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) st_row_chunk(sm + M_P, row, 4 * wg + c8, gv + 8 * c8);
           tmem_ldn<2>(TG2 + lq + c0, gv);
-          if (rv) store32_bf16(dv + (hb + n0 + row) * 64 + c0, gv);
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8)
+            st_row_chunk(sm + M_P + TILE, row, 4 * wg + c8, gv + 8 * c8);
         }
       }
+      fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&bar_empty[s]);  // this thread is done with the stage
-      compute_sync();              // s_vec[c & 1] and the P / dP tiles are free again
+      compute_sync();              // s_vec[c & 1] is free again; the output tiles are complete
+      if (t == 0) {
+        if (role == 0) {
+          tma_store_3d(&maps.dq, sm + M_DP, 0, n0, bh);
+        } else {
+          tma_store_3d(&maps.dk, sm + M_P, 0, n0, bh);
+          tma_store_3d(&maps.dv, sm + M_P + TILE, 0, n0, bh);
+        }
+        bulk_commit();
+      }
       gm = gm_next;
     }
+    if (MODE == 1 && t == 0) bulk_wait_all();
     if (MODE == 0) {
-      if (t == 0) bulk_wait_all();
       bool done = true;
       for (int c = max(0, nch - 2); c < nch; ++c)  // the last two state updates, in order
         done = wt(&bar_s2[c & 1], (c >> 1) & 1, 29) && done;
@@ -560,7 +591,9 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
   if (!make_bf16_map(&m.q, q, BH, s.N) || !make_bf16_map(&m.k, k, BH, s.N) ||
       !make_bf16_map(&m.v, v, BH, s.N) || !make_bf16_map(&m.g, dout, BH, s.N) ||
       !make_bf16_map(&m.o, out, BH, s.N) || !make_bf16_map(&m.fq, w.fq, BH, s.N) ||
-      !make_bf16_map(&m.fk, w.fk, BH, s.N) || !make_bf16_map(&m.gt, w.gt, BH, s.N))
+      !make_bf16_map(&m.fk, w.fk, BH, s.N) || !make_bf16_map(&m.gt, w.gt, BH, s.N) ||
+      !make_bf16_map(&m.dq, dq, BH, s.N) || !make_bf16_map(&m.dk, dk, BH, s.N) ||
+      !make_bf16_map(&m.dv, dv, BH, s.N))
     return cudaErrorInvalidValue;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(k_tc_bwd<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -571,14 +604,12 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
     return e;
   if ((e = cudaMemsetAsync(w.err, 0, sizeof(int), st)) != cudaSuccess) return e;
   if ((e = launch_pdl(k_tc_bwd<0>, dim3(pl.nsub, BH, 1), dim3(NTHR), S_SMEM, st, m, den, w.rec,
-                      w.gam, static_cast<bf16*>(nullptr), static_cast<bf16*>(nullptr),
-                      static_cast<bf16*>(nullptr), s.N, pl.sub_len, pl.nsub, pl.subs, w.err)) !=
+                      w.gam, w.gt, w.fq, w.fk, s.N, pl.sub_len, pl.nsub, pl.subs, w.err)) !=
       cudaSuccess)
     return e;
   if ((e = launch_pdl(k_tc_bwd<1>, dim3(pl.main.nseg, BH, 2), dim3(NTHR), M_SMEM, st, m, den,
-                      w.rec, w.gam, static_cast<bf16*>(dq), static_cast<bf16*>(dk),
-                      static_cast<bf16*>(dv), s.N, pl.main.seg_len, pl.nsub, pl.subs, w.err)) !=
-      cudaSuccess)
+                      w.rec, w.gam, w.gt, w.fq, w.fk, s.N, pl.main.seg_len, pl.nsub, pl.subs,
+                      w.err)) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }

@@ -63,6 +63,25 @@ __device__ __forceinline__ void phi_tile(uint8_t* tile, int valid, int t) {
   }
 }
 
+// phi_tile that also writes the transformed rows below `valid` to the
+// row-major [*][64] bf16 global rows starting at `g` (16-byte stores; the
+// eight vectors of a row are written by consecutive threads).
+__device__ __forceinline__ void phi_tile_store(uint8_t* tile, int valid, int t, bf16* g) {
+  for (int v = t; v < TILE / 16; v += NCOMP) {
+    uint4* ptr = reinterpret_cast<uint4*>(tile + v * 16);
+    const int r = v >> 3;
+    uint4 u = *ptr;
+    if (r >= valid) {
+      u = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      u = make_uint4(phi_bf16x2(u.x), phi_bf16x2(u.y), phi_bf16x2(u.z), phi_bf16x2(u.w));
+      const int lc = (v & 7) ^ (r & 7);  // logical 16-byte chunk of this vector
+      *reinterpret_cast<uint4*>(g + r * 64 + lc * 8) = u;
+    }
+    *ptr = u;
+  }
+}
+
 // A shared-memory descriptor advanced by `bytes` (the start-address field is
 // the low 14 bits in 16-byte units; shared addresses stay below 256 KB).
 __device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) {
