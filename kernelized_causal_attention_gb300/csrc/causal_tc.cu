@@ -48,7 +48,7 @@ constexpr int F_SMEM = F_BYTES + 1024;
 template <int MODE>
 __global__ void __launch_bounds__(NTHR, 1)
     k_tc_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-             const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ out,
+             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmOut,
              float* __restrict__ den, float* __restrict__ ws, int N, int nseg, int seg_len,
              int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;
@@ -162,8 +162,8 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
   } else {
     // -------------------------------------------------------- compute warps
-    // Two warpgroups; both cover all 128 rows (TMEM lanes) and split the
-    // columns: warpgroup wg takes keys 64wg.. of A and outputs 32wg.. of O.
+    // NWG warpgroups; each covers all 128 rows (TMEM lanes) and takes a slice
+    // of the columns: KW keys of A from k0, OW output columns from c0.
     const int t = threadIdx.x - 64;        // 0 .. NCOMP-1
     const int wg = t >> 7;
     const int qd = warp & 3;               // TMEM lane quarter of this warp
@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     const uint32_t lq = static_cast<uint32_t>(32 * qd) << 16;
     const bool has_s = lane < 16;          // M=64 accumulators: row 16*qd + lane in lane 32*qd + lane
     const int srow = 16 * qd + lane;
+    const int c0 = OW * wg, k0 = KW * wg;
     if (wg == 0) {  // initial state: the sum of the earlier segments' partial
                     // states written by MODE 0 (MODE 1), zero otherwise
       float sv[TC_MA];
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       for (int j = 0; j < TC_MA; j += 16) tmem_st16(TS + lq + j, sv + j);
       tmem_st_wait();
       if (MODE == 1 && has_s) {
-        for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(sm + F_SP, srow, c8, sv + 8 * c8);
+        tile_put_cols<64>(sm + F_SP, srow, 0, sv);
         float z8[8] = {sv[64], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         st_row_chunk(sm + F_SP + 8192, srow, 0, z8);
       }
@@ -215,19 +216,15 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int c = 0; ok && c < nch; ++c) {
       const int n0 = nb + c * TC_C;
       if (MODE == 1) {
-        // P = bf16(mask(A)) for keys 64wg .. 64wg+63: row keeps keys j <= row
+        // P = bf16(mask(A)) for keys k0 .. k0+KW-1: row keeps keys j <= row
         if (!mbar_wait(&bar_a, c & 1, WAIT_NS)) {
           fail(err, 15);
           break;
         }
         tc_fence_after();
-        float a[64];
-        tmem_ldn<4>(TA + lq + 64 * wg, a);
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (64 * wg + i > row) a[i] = 0.f;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(sm + F_P + wg * TILE, row, c8, a + 8 * c8);
+        if (t == 0) bulk_wait_read();  // the previous output tile has left P
+        compute_sync();
+        mask_cols<KW>(TA + lq + k0, 0.f, sm + F_P + (k0 >> 6) * TILE, row, k0);
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(&bar_p);
@@ -246,43 +243,38 @@ __global__ void __launch_bounds__(NTHR, 1)
         mbar_arrive(&bar_phi[s1]);
       }
       if (MODE == 1) {
-        // out = O~[:, :64] / O~[:, 64], columns 32wg .. 32wg+31
+        // out = O~[:, :64] / O~[:, 64] for columns c0 .., staged in P (free
+        // once O~ is complete) and written with a TMA store
         if (!mbar_wait(&bar_o, c & 1, WAIT_NS)) {
           fail(err, 17);
           break;
         }
         tc_fence_after();
-        float o[48];
-        tmem_ld16(TO + lq + 32 * wg, o);
-        tmem_ld16(TO + lq + 32 * wg + 16, o + 16);
-        tmem_ld16(TO + lq + 64, o + 32);
+        float o[OW], dd[16];
+        tmem_ld16(TO + lq + c0, o);
+        tmem_ld16(TO + lq + 64, dd);
         tmem_ld_wait();
-        const int n = n0 + row;
-        if (n < ne) {
-          const float d = o[32];
-          const float inv = 1.f / d;
+        const float d = dd[0];
+        const float inv = 1.f / d;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= inv;
-          store32_bf16(out + (static_cast<long>(bh) * N + n) * 64 + 32 * wg, o);
-          if (den != nullptr && wg == 0) den[static_cast<long>(bh) * N + n] = d;
-        }
-        // next chunk's S~_prev in bf16: warpgroup 0 columns 0-47, 1 columns 48-79
+        for (int i = 0; i < OW; ++i) o[i] *= inv;
+        tile_put_cols<OW>(sm + F_P, row, c0, o);
+        if (den != nullptr && wg == 0 && n0 + row < ne) den[static_cast<long>(bh) * N + n0 + row] = d;
+        // next chunk's S~_prev in bf16: warpgroup wg columns 16wg .., the last also z
         if (c + 1 < nch) {
           if (!mbar_wait(&bar_s, c & 1, WAIT_NS)) {
             fail(err, 18);
             break;
           }
           tc_fence_after();
-          float sv[48];
-          if (wg == 0) {
-            tmem_ldn<3>(TS + lq, sv);
-            if (has_s)
-              for (int c8 = 0; c8 < 6; ++c8) st_row_chunk(sm + F_SP, srow, c8, sv + 8 * c8);
-          } else {
-            tmem_ldn<2>(TS + lq + 48, sv);
-            if (has_s) {
-              for (int c8 = 0; c8 < 2; ++c8) st_row_chunk(sm + F_SP, srow, 6 + c8, sv + 8 * c8);
-              float z8[8] = {sv[16], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          float sv[16], zz[16];
+          tmem_ld16(TS + lq + 16 * wg, sv);
+          if (wg == NWG - 1) tmem_ld16(TS + lq + 64, zz);
+          tmem_ld_wait();
+          if (has_s) {
+            tile_put_cols<16>(sm + F_SP, srow, 16 * wg, sv);
+            if (wg == NWG - 1) {
+              float z8[8] = {zz[0], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
               st_row_chunk(sm + F_SP + 8192, srow, 0, z8);
             }
           }
@@ -290,24 +282,30 @@ __global__ void __launch_bounds__(NTHR, 1)
           tc_fence_before();
           mbar_arrive(&bar_sp);
         }
+        fence_proxy_async();
+        compute_sync();  // the output tile is complete
+        if (t == 0) {
+          tma_store_3d(&tmOut, sm + F_P, 0, n0, bh);
+          bulk_commit();
+        }
       }
     }
+    if (MODE == 1 && t == 0) bulk_wait_all();
     if (MODE == 0 && ok) {
       // the segment's partial state: wait for the last S~ update
       const bool done = mbar_wait(&bar_s, 0, WAIT_NS);
       if (!done) fail(err, 19);
       if (done) {
         tc_fence_after();
-        float sv[48];
+        float sv[16], zz[16];
         float* dst = ws + ((static_cast<long>(bh) * nseg + p) * 64 + srow) * TC_MA;
-        if (wg == 0) {
-          tmem_ldn<3>(TS + lq, sv);
-          if (has_s)
-            for (int j = 0; j < 48; ++j) dst[j] = sv[j];
-        } else {
-          tmem_ldn<2>(TS + lq + 48, sv);
-          if (has_s)
-            for (int j = 0; j < 32; ++j) dst[48 + j] = sv[j];
+        tmem_ld16(TS + lq + 16 * wg, sv);
+        if (wg == 0) tmem_ld16(TS + lq + 64, zz);
+        tmem_ld_wait();
+        if (has_s) {
+          for (int j = 0; j < 16; ++j) dst[16 * wg + j] = sv[j];
+          if (wg == 0)
+            for (int j = 0; j < 16; ++j) dst[64 + j] = zz[j];
         }
       }
     }
@@ -374,8 +372,9 @@ cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out
                           float* ws, const Shape& s, cudaStream_t st) {
   const int BH = s.B * s.H;
   const SegPlan pl = tc_plan(BH, s.N);
-  CUtensorMap mq, mk, mv;
-  if (!make_bf16_map(&mq, q, BH, s.N) || !make_bf16_map(&mk, k, BH, s.N) || !make_bf16_map(&mv, v, BH, s.N))
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_bf16_map(&mq, q, BH, s.N) || !make_bf16_map(&mk, k, BH, s.N) ||
+      !make_bf16_map(&mv, v, BH, s.N) || !make_bf16_map(&mo, out, BH, s.N))
     return cudaErrorInvalidValue;
   int* err = reinterpret_cast<int*>(ws + static_cast<size_t>(BH) * pl.nseg * 64 * TC_MA);
   cudaError_t e;
@@ -387,14 +386,13 @@ cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out
     return e;
   if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
   if (pl.nseg > 1) {
-    if ((e = launch_pdl(k_tc_fwd<0>, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv,
-                        static_cast<bf16*>(nullptr), static_cast<float*>(nullptr), ws, s.N,
-                        pl.nseg, pl.seg_len, err)) != cudaSuccess)
+    if ((e = launch_pdl(k_tc_fwd<0>, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv, mo,
+                        static_cast<float*>(nullptr), ws, s.N, pl.nseg, pl.seg_len, err)) !=
+        cudaSuccess)
       return e;
   }
-  if ((e = launch_pdl(k_tc_fwd<1>, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv,
-                      static_cast<bf16*>(out), den, ws, s.N, pl.nseg, pl.seg_len, err)) !=
-      cudaSuccess)
+  if ((e = launch_pdl(k_tc_fwd<1>, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv, mo, den,
+                      ws, s.N, pl.nseg, pl.seg_len, err)) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }

@@ -69,41 +69,25 @@ __device__ __forceinline__ void put_gam(uint8_t* gamt, int i, float g) {
   *reinterpret_cast<bf16*>(gamt + (i >> 6) * 1024 + (i & 63) * 2) = __float2bfloat16_rn(g);
 }
 
-// Reads the 64 fp32 columns at `taddr` (keys 64h .. 64h+63 of row `row`),
-// adds `add`, keeps keys j <= row and stores them as bf16 row `row` of the
-// swizzled [128][64] tile `dst`.
-__device__ __forceinline__ void mask_half_to_smem(uint32_t taddr, float add, uint8_t* dst, int row,
-                                                  int h) {
-  float a[64];
-  tmem_ldn<4>(taddr, a);
+// Role 1: the masked bf16 rows of dA (+ gam) and of A for this warpgroup's
+// KW keys from key0, loaded together so that one wait covers both.
+__device__ __forceinline__ void mask2_cols(uint32_t tda, uint32_t ta, float add, uint8_t* ddst,
+                                           uint8_t* adst, int row, int key0) {
+  float d[KW], a[KW];
 #pragma unroll
-  for (int i = 0; i < 64; ++i) a[i] = (64 * h + i <= row) ? a[i] + add : 0.f;
-#pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(dst, row, c8, a + 8 * c8);
-}
-
-// Role 1: the masked bf16 rows of dA (+ gam) and of A for keys 64h..64h+63,
-// loaded together so that one wait covers both accumulators.
-__device__ __forceinline__ void mask2_half_to_smem(uint32_t tda, uint32_t ta, float add,
-                                                   uint8_t* ddst, uint8_t* adst, int row, int h) {
-  float d[64], a[64];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < KW / 16; ++i) {
     tmem_ld16(tda + 16 * i, d + 16 * i);
     tmem_ld16(ta + 16 * i, a + 16 * i);
   }
   tmem_ld_wait();
 #pragma unroll
-  for (int i = 0; i < 64; ++i) {
-    const bool keep = 64 * h + i <= row;
+  for (int i = 0; i < KW; ++i) {
+    const bool keep = key0 + i <= row;
     d[i] = keep ? d[i] + add : 0.f;
     a[i] = keep ? a[i] : 0.f;
   }
-#pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8) {
-    st_row_chunk(ddst, row, c8, d + 8 * c8);
-    st_row_chunk(adst, row, c8, a + 8 * c8);
-  }
+  tile_put_cols<KW>(ddst, row, key0 & 63, d);
+  tile_put_cols<KW>(adst, row, key0 & 63, a);
 }
 
 struct BwdMaps {
@@ -126,7 +110,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   __shared__ uint64_t bar_in, bar_a, bar_p, bar_rp, bar_o, bar_s, bar_s2[2];
   __shared__ uint32_t tmem_base;
   __shared__ float s_vec[2][64];    // carried z (role 0) or r (role 1) before chunk c, by c & 1
-  __shared__ float s_dot[2][TC_C];  // MODE 0: half-row dot products for gam
+  __shared__ float s_dot[NWG][TC_C];  // MODE 0: partial dot products for gam
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = p * seg_len;
@@ -296,8 +280,8 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
   } else {
     // ---------------------------------------------------------- compute warps
-    // Two warpgroups; both cover all 128 rows (TMEM lanes) and split the
-    // columns: warpgroup wg takes keys 64wg.. of A / dA and outputs 32wg..
+    // NWG warpgroups; each covers all 128 rows (TMEM lanes) and takes a slice
+    // of the columns: KW keys of A / dA from k0, OW output columns from c0.
     const int t = threadIdx.x - 64;  // 0 .. NCOMP-1
     const int wg = t >> 7;
     const int qd = warp & 3;
@@ -305,7 +289,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     const uint32_t lq = static_cast<uint32_t>(32 * qd) << 16;
     const bool has_s = lane < 16;  // M=64 accumulators: row 16*qd + lane in lane 32*qd + lane
     const int srow = 16 * qd + lane;
-    const int c0 = 32 * wg;        // this warpgroup's output columns
+    const int c0 = OW * wg, k0 = KW * wg;
     const long hb = static_cast<long>(bh) * N;
     auto gam_at = [&](int c) {     // gam of this thread's row in chunk c
       const int n0 = nb + chunk_at(c) * TC_C;
@@ -341,7 +325,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         tmem_st16(TV + lq, vv);
         tmem_st_wait();
         if (has_s) {
-          for (int c8 = 0; c8 < 8; ++c8) st_row_chunk(sm + M_RP, srow, c8, sv + 8 * c8);
+          tile_put_cols<64>(sm + M_RP, srow, 0, sv);
           s_vec[0][srow] = vv[0];
         }
       }
@@ -387,26 +371,28 @@ __global__ void __launch_bounds__(NTHR, 1)
         compute_sync();
         wt(&bar_full[s], (c / NST) & 1, 25);
         uint8_t* gtile = sm + S_GT + (c & 1) * TILE;
-        // gt = dout / den on this warpgroup's half row; gam = -(gt . out)
-        float g[32], o[32];
-        tile_row_half(st + 3 * TILE, row, wg, g);
-        tile_row_half(st + 4 * TILE, row, wg, o);
+        // gt = dout / den on this warpgroup's columns; gam = -(gt . out)
+        float g[OW], o[OW];
+        tile_row_cols<OW>(st + 3 * TILE, row, c0, g);
+        tile_row_cols<OW>(st + 4 * TILE, row, c0, o);
         const float inv = 1.f / dn;
         float acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < OW; ++i) {
           g[i] = rv ? g[i] * inv : 0.f;
           acc = fmaf(g[i], o[i], acc);
         }
         s_dot[wg][row] = acc;
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) st_row_chunk(gtile, row, 4 * wg + c8, g + 8 * c8);
-        if (rv) store32_bf16(gt_out + (hb + n0 + row) * 64 + c0, g);
+        tile_put_cols<OW>(gtile, row, c0, g);
+        if (rv) store_bf16<OW>(gt_out + (hb + n0 + row) * 64 + c0, g);
         phi_tile_store(st, valid, t, fq_out + (hb + n0) * 64);
         phi_tile_store(st + TILE, valid, t, fk_out + (hb + n0) * 64);
         compute_sync();
         if (wg == 0) {
-          const float gmv = rv ? -(s_dot[0][row] + s_dot[1][row]) : 0.f;
+          float dot = 0.f;
+#pragma unroll
+          for (int w = 0; w < NWG; ++w) dot += s_dot[w][row];
+          const float gmv = rv ? -dot : 0.f;
           put_gam(gamt + (c & 1) * 2048, row, gmv);
           if (rv) gam[hb + n0 + row] = gmv;
         }
@@ -422,10 +408,10 @@ __global__ void __launch_bounds__(NTHR, 1)
       if (t == 0) bulk_wait_read();  // the previous chunk's output tiles have left P / dP
       compute_sync();
       if (role == 1)
-        mask2_half_to_smem(TDA + lq + 64 * wg, TA + lq + 64 * wg, gm, sm + M_DP + wg * TILE,
-                           sm + M_P + wg * TILE, row, wg);
+        mask2_cols(TDA + lq + k0, TA + lq + k0, gm, sm + M_DP + (k0 >> 6) * TILE,
+                   sm + M_P + (k0 >> 6) * TILE, row, k0);
       else
-        mask_half_to_smem(TDA + lq + 64 * wg, gm, sm + M_DP + wg * TILE, row, wg);
+        mask_cols<KW>(TDA + lq + k0, gm, sm + M_DP + (k0 >> 6) * TILE, row, k0);
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&bar_p);
@@ -444,12 +430,11 @@ __global__ void __launch_bounds__(NTHR, 1)
       if (c + 1 < nch) {
         wt(&bar_s, c & 1, 28);
         tc_fence_after();
-        float sv[32], vv[16];
-        tmem_ldn<2>(TST + lq + c0, sv);
+        float sv[OW], vv[16];
+        tmem_ldn<OW / 16>(TST + lq + c0, sv);
         tmem_ldn<1>(TV + lq, vv);
         if (has_s) {
-          for (int c8 = 0; c8 < 4; ++c8)
-            st_row_chunk(sm + M_RP + ((c + 1) & 1) * 8192, srow, 4 * wg + c8, sv + 8 * c8);
+          tile_put_cols<OW>(sm + M_RP + ((c + 1) & 1) * 8192, srow, c0, sv);
           if (wg == 0) s_vec[(c + 1) & 1][srow] = vv[0];
         }
         fence_proxy_async();
@@ -461,24 +446,20 @@ __global__ void __launch_bounds__(NTHR, 1)
       tc_fence_after();
       {
         const float* vec = s_vec[c & 1];
-        float gv[32], x[32];
-        tmem_ldn<2>(TG1 + lq + c0, gv);
+        float gv[OW], x[OW];
+        tmem_ldn<OW / 16>(TG1 + lq + c0, gv);
         if (role == 0) {  // dq = (grad_phiQ + gam z_prev) * phi'(Q)
-          tile_row_half(st, row, wg, x);
+          tile_row_cols<OW>(st, row, c0, x);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) gv[i] = (gv[i] + gm * vec[c0 + i]) * fminf(x[i], 1.f);
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) st_row_chunk(sm + M_DP, row, 4 * wg + c8, gv + 8 * c8);
+          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + gm * vec[c0 + i]) * fminf(x[i], 1.f);
+          tile_put_cols<OW>(sm + M_DP, row, c0, gv);
         } else {          // dk = (grad_phiK + r_next) * phi'(K), dv
-          tile_row_half(st + TILE, row, wg, x);
+          tile_row_cols<OW>(st + TILE, row, c0, x);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) gv[i] = (gv[i] + vec[c0 + i]) * fminf(x[i], 1.f);
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) st_row_chunk(sm + M_P, row, 4 * wg + c8, gv + 8 * c8);
-          tmem_ldn<2>(TG2 + lq + c0, gv);
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8)
-            st_row_chunk(sm + M_P + TILE, row, 4 * wg + c8, gv + 8 * c8);
+          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + vec[c0 + i]) * fminf(x[i], 1.f);
+          tile_put_cols<OW>(sm + M_P, row, c0, gv);
+          tmem_ldn<OW / 16>(TG2 + lq + c0, gv);
+          tile_put_cols<OW>(sm + M_P + TILE, row, c0, gv);
         }
       }
       fence_proxy_async();
@@ -504,15 +485,17 @@ __global__ void __launch_bounds__(NTHR, 1)
       if (done) {
         tc_fence_after();
         float* r0 = rec + (static_cast<long>(bh) * nsub + p) * REC;
-        float sv[32], vv[16];
-        tmem_ldn<2>(TG1 + lq + c0, sv);
+        float sv[OW], vv[16];
+        tmem_ldn<OW / 16>(TG1 + lq + c0, sv);
         if (has_s)
-          for (int j = 0; j < 32; ++j) r0[srow * 64 + c0 + j] = sv[j];
-        tmem_ldn<2>(TST + lq + c0, sv);
+          for (int j = 0; j < OW; ++j) r0[srow * 64 + c0 + j] = sv[j];
+        tmem_ldn<OW / 16>(TST + lq + c0, sv);
         if (has_s)
-          for (int j = 0; j < 32; ++j) r0[DM + 64 + srow * 64 + c0 + j] = sv[j];
-        tmem_ldn<1>((wg == 0 ? TV : TV2) + lq, vv);
-        if (has_s) r0[(wg == 0 ? DM : 2 * DM + 64) + srow] = vv[0];
+          for (int j = 0; j < OW; ++j) r0[DM + 64 + srow * 64 + c0 + j] = sv[j];
+        if (wg < 2) {
+          tmem_ldn<1>((wg == 0 ? TV : TV2) + lq, vv);
+          if (has_s) r0[(wg == 0 ? DM : 2 * DM + 64) + srow] = vv[0];
+        }
       }
     }
   }

@@ -19,8 +19,11 @@ using bf16 = __nv_bfloat16;
 constexpr int TC_C = 128;                  // tokens per chunk (MMA M)
 constexpr int NST = 2;                     // TMA ring stages
 constexpr int TILE = TC_C * 64 * 2;        // one [128][64] bf16 tile
-constexpr int NCOMP = 256;                 // compute threads: two warpgroups
-constexpr int NTHR = 64 + NCOMP;           // warp 0 TMA, warp 1 MMA, warps 2-9 compute
+constexpr int NWG = 4;                     // compute warpgroups
+constexpr int NCOMP = 128 * NWG;           // compute threads
+constexpr int NTHR = 64 + NCOMP;           // warp 0 TMA, warp 1 MMA, the rest compute
+constexpr int KW = TC_C / NWG;             // key columns of a 128-wide accumulator per warpgroup
+constexpr int OW = 64 / NWG;               // columns of a 64-wide output per warpgroup
 constexpr uint64_t WAIT_NS = 2000000000ull;  // bound on every wait
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -124,11 +127,13 @@ __device__ __forceinline__ void tmem_ldn(uint32_t taddr, float* v) {
   tmem_ld_wait();
 }
 
-// Columns 32h .. 32h+31 of row r of a swizzled [128][64] bf16 tile as floats.
-__device__ __forceinline__ void tile_row_half(const uint8_t* tile, int r, int h, float* x) {
+// NC columns (a multiple of 8) from column col0 of row r of a swizzled
+// [128][64] bf16 tile, as floats.
+template <int NC>
+__device__ __forceinline__ void tile_row_cols(const uint8_t* tile, int r, int col0, float* x) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const int c8 = 4 * h + c;
+  for (int c = 0; c < NC / 8; ++c) {
+    const int c8 = (col0 >> 3) + c;
     const uint4 u = *reinterpret_cast<const uint4*>(tile + r * 128 + ((c8 ^ (r & 7)) << 4));
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -139,13 +144,35 @@ __device__ __forceinline__ void tile_row_half(const uint8_t* tile, int r, int h,
   }
 }
 
-// 32 floats as bf16 to global memory (64 bytes, 16-byte aligned).
-__device__ __forceinline__ void store32_bf16(bf16* dst, const float* f) {
+// NC floats (a multiple of 8) as bf16 columns col0 .. of row r of a
+// swizzled [128][64] bf16 tile.
+template <int NC>
+__device__ __forceinline__ void tile_put_cols(uint8_t* tile, int r, int col0, const float* x) {
+#pragma unroll
+  for (int c = 0; c < NC / 8; ++c) st_row_chunk(tile, r, (col0 >> 3) + c, x + 8 * c);
+}
+
+// NC floats (a multiple of 8) as bf16 to global memory (16-byte aligned).
+template <int NC>
+__device__ __forceinline__ void store_bf16(bf16* dst, const float* f) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
+  for (int c = 0; c < NC / 8; ++c)
     d[c] = make_uint4(pack_bf16(f[8 * c], f[8 * c + 1]), pack_bf16(f[8 * c + 2], f[8 * c + 3]),
                       pack_bf16(f[8 * c + 4], f[8 * c + 5]), pack_bf16(f[8 * c + 6], f[8 * c + 7]));
+}
+
+// Reads NC fp32 columns of this thread's TMEM lane from `taddr` (keys key0 ..
+// of row `row`), adds `add`, keeps keys j <= row and stores them as bf16
+// columns (key0 & 63) .. of row `row` of the swizzled tile `dst`.
+template <int NC>
+__device__ __forceinline__ void mask_cols(uint32_t taddr, float add, uint8_t* dst, int row,
+                                          int key0) {
+  float a[NC];
+  tmem_ldn<NC / 16>(taddr, a);
+#pragma unroll
+  for (int i = 0; i < NC; ++i) a[i] = (key0 + i <= row) ? a[i] + add : 0.f;
+  tile_put_cols<NC>(dst, row, key0 & 63, a);
 }
 
 __device__ __forceinline__ void compute_sync() {  // the compute warps only
