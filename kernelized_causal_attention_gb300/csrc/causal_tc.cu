@@ -6,15 +6,15 @@
 //
 // GB300 design (not the pages'): each (b, h) sequence is cut into segments of
 // whole 128-token chunks, one CTA per segment (one CTA per SM).  Inside a CTA
-// one warp streams raw Q/K/V chunks with TMA into a two-stage shared-memory
-// ring (128-byte swizzle), four compute warps apply phi in place, and one
+// one warp streams raw Q/K/V chunks with TMA into a three-stage shared-memory
+// ring (128-byte swizzle), the compute warps apply phi in place, and one
 // thread issues the tcgen05 MMAs whose fp32 accumulators live in tensor
 // memory.  The value matrix is augmented with a column of ones, V~ = [V | 1],
 // so one accumulator carries both the state and the normaliser,
 // S~ = [S | z] = sum phi(K_j) V~_j^T, and every product that yields a
 // numerator yields its denominator in column 64:
 //   A    = phi(Q) phi(K)^T                        (128 x 128, K = 64)
-//   P    = bf16(mask(A))                           (compute warps, TMEM -> smem)
+//   P    = bf16(mask(A))                           (compute warps, kept in TMEM)
 //   O~   = P V~ + phi(Q) bf16(S~_prev)            (128 x 80)  -> out = O~[:, :64] / O~[:, 64]
 //   S~  += phi(K)^T V~                             (64 x 80, carried across chunks)
 // Segment prefixes are sums of the partial states of a first pass (same
@@ -35,11 +35,12 @@ using namespace tcc;
 constexpr int TC_MA = 80;                  // augmented value width [V | 1 | 0 ...]
 
 // shared-memory map of the forward kernel (offsets from a 1024-aligned base)
+constexpr int FNST = 3;                    // TMA ring stages of the forward
 constexpr int F_STAGE = 3 * TILE;          // Q, K, V
-constexpr int F_ONES = NST * F_STAGE;      // [128][64], column 0 = 1
-constexpr int F_P = F_ONES + TILE;         // P, keys 0-63 then 64-127
-constexpr int F_SP = F_P + 2 * TILE;       // bf16 S~_prev: [64 d][64] then [64 d][z, 0...]
-constexpr int F_BYTES = F_SP + 2 * 8192;
+constexpr int F_ONES = FNST * F_STAGE;     // [128][64], column 0 = 1
+constexpr int F_SP = F_ONES + TILE;        // bf16 S~_prev: [64 d][64] then [64 d][z, 0...]
+constexpr int F_OUT = F_SP + 2 * 8192;     // two output staging tiles (by chunk parity)
+constexpr int F_BYTES = F_OUT + 2 * TILE;
 constexpr int F_SMEM = F_BYTES + 1024;
 
 // Forward kernel.  MODE 0: per-segment partial state dS~ = sum phi(K) V~^T
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (MODE == 0 && p == nseg - 1) return;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
-  __shared__ uint64_t bar_full[NST], bar_empty[NST], bar_phi[NST];
+  __shared__ uint64_t bar_full[FNST], bar_empty[FNST], bar_phi[FNST];
   __shared__ uint64_t bar_a, bar_p, bar_sp, bar_o, bar_s;
   __shared__ uint32_t tmem_base;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int nch = (ne - nb + TC_C - 1) / TC_C;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NST; ++s) {
+    for (int s = 0; s < FNST; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
       mbar_init(&bar_phi[s], NCOMP);
@@ -97,14 +98,14 @@ __global__ void __launch_bounds__(NTHR, 1)
   tc_fence_after();
   grid_dep_wait();  // the previous kernel's outputs are visible from here on
   const uint32_t tm = tmem_base;
-  const uint32_t TA = tm, TO = tm + 128, TS = tm + 256;
+  const uint32_t TA = tm, TO = tm + 128, TS = tm + 256, TP = tm + 384;  // TP: bf16 P (A operand)
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
       for (int c = 0; c < nch; ++c) {
-        const int s = c % NST;
-        if (c >= NST && !mbar_wait(&bar_empty[s], ((c / NST) - 1) & 1, WAIT_NS)) {
+        const int s = c % FNST;
+        if (c >= FNST && !mbar_wait(&bar_empty[s], ((c / FNST) - 1) & 1, WAIT_NS)) {
           fail(err, 11);
           break;
         }
@@ -123,14 +124,13 @@ __global__ void __launch_bounds__(NTHR, 1)
       constexpr uint32_t ID_O = idesc_bf16(128, TC_MA, false, true);
       constexpr uint32_t ID_S = idesc_bf16(64, TC_MA, true, true);
       const uint32_t ones = smem_u32(sm + F_ONES);
-      const uint64_t dP = sdesc(smem_u32(sm + F_P), 16, 1024);
       const uint64_t dSP = sdesc(smem_u32(sm + F_SP), 8192, 1024);
       for (int c = 0; c < nch; ++c) {
-        const int s = c % NST;
+        const int s = c % FNST;
         const uint32_t q = smem_u32(sm + s * F_STAGE), k = q + TILE, v = q + 2 * TILE;
         const uint64_t dQ = sdesc(q, 16, 1024), dK = sdesc(k, 16, 1024);
         const uint64_t dVt = sdesc(v, ones - v, 1024);  // [V | ones] as an MN-major operand
-        if (!mbar_wait(&bar_phi[s], (c / NST) & 1, WAIT_NS)) {
+        if (!mbar_wait(&bar_phi[s], (c / FNST) & 1, WAIT_NS)) {
           fail(err, 12);
           break;
         }
@@ -146,8 +146,8 @@ __global__ void __launch_bounds__(NTHR, 1)
           }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // O~ = P V~
-            mma_bf16(TO, dadd(dP, (kk >> 2) * TILE + (kk & 3) * 32), dadd(dVt, kk * 2048), ID_O, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)  // O~ = P V~, P read from tensor memory
+            mma_bf16_ts(TO, TP + 8 * kk, dadd(dVt, kk * 2048), ID_O, kk > 0);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // O~ += phi(Q) S~_prev
             mma_bf16(TO, dadd(dQ, 32 * kk), dadd(dSP, kk * 2048), ID_O, 1);
@@ -222,17 +222,24 @@ __global__ void __launch_bounds__(NTHR, 1)
           break;
         }
         tc_fence_after();
-        if (t == 0) bulk_wait_read();  // the previous output tile has left P
-        compute_sync();
-        mask_cols<KW>(TA + lq + k0, 0.f, sm + F_P + (k0 >> 6) * TILE, row, k0);
-        fence_proxy_async();
+        {
+          float a[KW];
+          uint32_t pk[KW / 2];
+          tmem_ldn<KW / 16>(TA + lq + k0, a);
+#pragma unroll
+          for (int i = 0; i < KW / 2; ++i)
+            pk[i] = pack_bf16(k0 + 2 * i <= row ? a[2 * i] : 0.f, k0 + 2 * i + 1 <= row ? a[2 * i + 1] : 0.f);
+#pragma unroll
+          for (int i = 0; i < KW / 32; ++i) tmem_st16u(TP + lq + k0 / 2 + 16 * i, pk + 16 * i);
+          tmem_st_wait();
+        }
         tc_fence_before();
         mbar_arrive(&bar_p);
       }
       // phi on the next chunk while the tensor cores work on this one
       if (c + 1 < nch) {
-        const int s1 = (c + 1) % NST;
-        if (!mbar_wait(&bar_full[s1], ((c + 1) / NST) & 1, WAIT_NS)) {
+        const int s1 = (c + 1) % FNST;
+        if (!mbar_wait(&bar_full[s1], ((c + 1) / FNST) & 1, WAIT_NS)) {
           fail(err, 16);
           break;
         }
@@ -258,7 +265,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         const float inv = 1.f / d;
 #pragma unroll
         for (int i = 0; i < OW; ++i) o[i] *= inv;
-        tile_put_cols<OW>(sm + F_P, row, c0, o);
+        tile_put_cols<OW>(sm + F_OUT + (c & 1) * TILE, row, c0, o);
         if (den != nullptr && wg == 0 && n0 + row < ne) den[static_cast<long>(bh) * N + n0 + row] = d;
         // next chunk's S~_prev in bf16: warpgroup wg columns 16wg .., the last also z
         if (c + 1 < nch) {
@@ -283,9 +290,10 @@ __global__ void __launch_bounds__(NTHR, 1)
           mbar_arrive(&bar_sp);
         }
         fence_proxy_async();
-        compute_sync();  // the output tile is complete
+        if (t == 0) bulk_wait_read();  // chunk c-1's store has left the other staging tile
+        compute_sync();                // this chunk's output tile is complete
         if (t == 0) {
-          tma_store_3d(&tmOut, sm + F_P, 0, n0, bh);
+          tma_store_3d(&tmOut, sm + F_OUT + (c & 1) * TILE, 0, n0, bh);
           bulk_commit();
         }
       }
