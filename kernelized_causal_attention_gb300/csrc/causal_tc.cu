@@ -68,11 +68,11 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int s = 0; s < FNST; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
-      mbar_init(&bar_phi[s], NCOMP);
+      mbar_init(&bar_phi[s], MODE == 1 ? NCOMP / 2 : NCOMP);
     }
     mbar_init(&bar_a, 1);
-    mbar_init(&bar_p, NCOMP);
-    mbar_init(&bar_sp, NCOMP);
+    mbar_init(&bar_p, NCOMP / 2);
+    mbar_init(&bar_sp, NCOMP / 2);
     mbar_init(&bar_o, 1);
     mbar_init(&bar_s, 1);
     fence_barrier_init();
@@ -162,8 +162,9 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
   } else {
     // -------------------------------------------------------- compute warps
-    // NWG warpgroups; each covers all 128 rows (TMEM lanes) and takes a slice
-    // of the columns: KW keys of A from k0, OW output columns from c0.
+    // MODE 1: warpgroups 0-1 are consumers (P, read-out, carried state; each
+    // covers all 128 rows and half of the columns), warpgroups 2-3 apply phi
+    // to the chunks ahead on the TMA ring.  MODE 0: every warpgroup applies phi.
     const int t = threadIdx.x - 64;        // 0 .. NCOMP-1
     const int wg = t >> 7;
     const int qd = warp & 3;               // TMEM lane quarter of this warp
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     const uint32_t lq = static_cast<uint32_t>(32 * qd) << 16;
     const bool has_s = lane < 16;          // M=64 accumulators: row 16*qd + lane in lane 32*qd + lane
     const int srow = 16 * qd + lane;
-    const int c0 = OW * wg, k0 = KW * wg;
+    const bool transform = MODE == 0 || wg >= 2;
     if (wg == 0) {  // initial state: the sum of the earlier segments' partial
                     // states written by MODE 0 (MODE 1), zero otherwise
       float sv[TC_MA];
@@ -199,89 +200,80 @@ __global__ void __launch_bounds__(NTHR, 1)
     }
     fence_proxy_async();
     tc_fence_before();
-    bool ok = true;
-    // phi on chunk 0
-    if (!mbar_wait(&bar_full[0], 0, WAIT_NS)) {
-      fail(err, 14);
-      ok = false;
-    }
-    if (ok) {
-      const int valid = min(TC_C, ne - nb);
-      if (MODE == 1) phi_tile(sm + 0, valid, t);
-      phi_tile(sm + TILE, valid, t);
-      fence_proxy_async();
-      mbar_arrive(&bar_phi[0]);
-      if (MODE == 1) mbar_arrive(&bar_sp);
-    }
-    for (int c = 0; ok && c < nch; ++c) {
-      const int n0 = nb + c * TC_C;
-      if (MODE == 1) {
-        // P = bf16(mask(A)) for keys k0 .. k0+KW-1: row keeps keys j <= row
+    if (transform) {
+      // ------------------------------------------------ phi on every chunk
+      const int tt = MODE == 1 ? t - NCOMP / 2 : t;
+      const int nt = MODE == 1 ? NCOMP / 2 : NCOMP;
+      for (int c = 0; c < nch; ++c) {
+        const int s = c % FNST;
+        if (!mbar_wait(&bar_full[s], (c / FNST) & 1, WAIT_NS)) {
+          fail(err, 14);
+          break;
+        }
+        const int valid = min(TC_C, ne - (nb + c * TC_C));
+        if (MODE == 1) phi_tile(sm + s * F_STAGE, valid, tt, nt);
+        phi_tile(sm + s * F_STAGE + TILE, valid, tt, nt);
+        fence_proxy_async();
+        mbar_arrive(&bar_phi[s]);
+      }
+    } else {
+      // ------------------------------------------- consumers (MODE 1 only)
+      const int c0 = 32 * wg, k0 = 64 * wg;  // output columns / keys of this warpgroup
+      mbar_arrive(&bar_sp);
+      for (int c = 0; c < nch; ++c) {
+        const int n0 = nb + c * TC_C;
+        // P = bf16(mask(A)) for keys k0 .. k0+63, kept in TMEM
         if (!mbar_wait(&bar_a, c & 1, WAIT_NS)) {
           fail(err, 15);
           break;
         }
         tc_fence_after();
         {
-          float a[KW];
-          uint32_t pk[KW / 2];
-          tmem_ldn<KW / 16>(TA + lq + k0, a);
+          float a[64];
+          uint32_t pk[32];
+          tmem_ldn<4>(TA + lq + k0, a);
 #pragma unroll
-          for (int i = 0; i < KW / 2; ++i)
+          for (int i = 0; i < 32; ++i)
             pk[i] = pack_bf16(k0 + 2 * i <= row ? a[2 * i] : 0.f, k0 + 2 * i + 1 <= row ? a[2 * i + 1] : 0.f);
-#pragma unroll
-          for (int i = 0; i < KW / 32; ++i) tmem_st16u(TP + lq + k0 / 2 + 16 * i, pk + 16 * i);
+          tmem_st16u(TP + lq + k0 / 2, pk);
+          tmem_st16u(TP + lq + k0 / 2 + 16, pk + 16);
           tmem_st_wait();
         }
         tc_fence_before();
         mbar_arrive(&bar_p);
-      }
-      // phi on the next chunk while the tensor cores work on this one
-      if (c + 1 < nch) {
-        const int s1 = (c + 1) % FNST;
-        if (!mbar_wait(&bar_full[s1], ((c + 1) / FNST) & 1, WAIT_NS)) {
-          fail(err, 16);
-          break;
-        }
-        const int valid = min(TC_C, ne - (n0 + TC_C));
-        if (MODE == 1) phi_tile(sm + s1 * F_STAGE, valid, t);
-        phi_tile(sm + s1 * F_STAGE + TILE, valid, t);
-        fence_proxy_async();
-        mbar_arrive(&bar_phi[s1]);
-      }
-      if (MODE == 1) {
-        // out = O~[:, :64] / O~[:, 64] for columns c0 .., staged in P (free
-        // once O~ is complete) and written with a TMA store
+        // out = O~[:, :64] / O~[:, 64], columns c0 .. c0+31
         if (!mbar_wait(&bar_o, c & 1, WAIT_NS)) {
           fail(err, 17);
           break;
         }
         tc_fence_after();
-        float o[OW], dd[16];
+        float o[32], dd[16];
         tmem_ld16(TO + lq + c0, o);
+        tmem_ld16(TO + lq + c0 + 16, o + 16);
         tmem_ld16(TO + lq + 64, dd);
         tmem_ld_wait();
         const float d = dd[0];
         const float inv = 1.f / d;
 #pragma unroll
-        for (int i = 0; i < OW; ++i) o[i] *= inv;
-        tile_put_cols<OW>(sm + F_OUT + (c & 1) * TILE, row, c0, o);
+        for (int i = 0; i < 32; ++i) o[i] *= inv;
+        tile_put_cols<32>(sm + F_OUT + (c & 1) * TILE, row, c0, o);
         if (den != nullptr && wg == 0 && n0 + row < ne) den[static_cast<long>(bh) * N + n0 + row] = d;
-        // next chunk's S~_prev in bf16: warpgroup wg columns 16wg .., the last also z
+        // next chunk's S~_prev in bf16: warpgroup 0 columns 0-47, 1 columns 48-79
         if (c + 1 < nch) {
           if (!mbar_wait(&bar_s, c & 1, WAIT_NS)) {
             fail(err, 18);
             break;
           }
           tc_fence_after();
-          float sv[16], zz[16];
-          tmem_ld16(TS + lq + 16 * wg, sv);
-          if (wg == NWG - 1) tmem_ld16(TS + lq + 64, zz);
-          tmem_ld_wait();
-          if (has_s) {
-            tile_put_cols<16>(sm + F_SP, srow, 16 * wg, sv);
-            if (wg == NWG - 1) {
-              float z8[8] = {zz[0], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          float sv[48];
+          if (wg == 0) {
+            tmem_ldn<3>(TS + lq, sv);
+            if (has_s) tile_put_cols<48>(sm + F_SP, srow, 0, sv);
+          } else {
+            tmem_ldn<2>(TS + lq + 48, sv);
+            if (has_s) {
+              tile_put_cols<16>(sm + F_SP, srow, 48, sv);
+              float z8[8] = {sv[16], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
               st_row_chunk(sm + F_SP + 8192, srow, 0, z8);
             }
           }
@@ -291,15 +283,15 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
         fence_proxy_async();
         if (t == 0) bulk_wait_read();  // chunk c-1's store has left the other staging tile
-        compute_sync();                // this chunk's output tile is complete
+        half_sync();                   // this chunk's output tile is complete
         if (t == 0) {
           tma_store_3d(&tmOut, sm + F_OUT + (c & 1) * TILE, 0, n0, bh);
           bulk_commit();
         }
       }
+      if (t == 0) bulk_wait_all();
     }
-    if (MODE == 1 && t == 0) bulk_wait_all();
-    if (MODE == 0 && ok) {
+    if (MODE == 0) {
       // the segment's partial state: wait for the last S~ update
       const bool done = mbar_wait(&bar_s, 0, WAIT_NS);
       if (!done) fail(err, 19);

@@ -51,11 +51,11 @@ __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// phi applied in place to a swizzled [128][64] bf16 tile by the NCOMP compute
-// threads (elementwise, so the swizzle does not matter).  Rows at or past
-// `valid` are zeroed: a zero phi(K) row adds nothing to any sum.
-__device__ __forceinline__ void phi_tile(uint8_t* tile, int valid, int t) {
-  for (int v = t; v < TILE / 16; v += NCOMP) {
+// phi applied in place to a swizzled [128][64] bf16 tile by `nthr` threads
+// (t = 0 .. nthr-1; elementwise, so the swizzle does not matter).  Rows at or
+// past `valid` are zeroed: a zero phi(K) row adds nothing to any sum.
+__device__ __forceinline__ void phi_tile(uint8_t* tile, int valid, int t, int nthr = NCOMP) {
+  for (int v = t; v < TILE / 16; v += nthr) {
     uint4* ptr = reinterpret_cast<uint4*>(tile + v * 16);
     uint4 u = *ptr;
     if ((v >> 3) >= valid)
@@ -177,6 +177,12 @@ __device__ __forceinline__ void mask_cols(uint32_t taddr, float add, uint8_t* ds
 
 __device__ __forceinline__ void compute_sync() {  // the compute warps only
   asm volatile("bar.sync 1, %0;" ::"n"(NCOMP) : "memory");
+}
+
+// Named barrier over the first NCOMP / 2 compute threads (the consumer
+// warpgroups of a specialised kernel).
+__device__ __forceinline__ void half_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(NCOMP / 2) : "memory");
 }
 
 }  // namespace tcc
