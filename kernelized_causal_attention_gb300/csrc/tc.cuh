@@ -55,6 +55,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (for polling several
+// barriers from one thread).
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // try_wait with a suspend-time hint: the thread sleeps until the phase
 // completes or about `hint_ns` pass, instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
@@ -102,6 +116,14 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
           reinterpret_cast<uint64_t>(map)),
       "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
       : "memory");
+}
+
+// Untiled bulk copy shared -> global (bulk-group completion); both addresses
+// 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() {

@@ -35,34 +35,59 @@ __device__ __forceinline__ void fail(int* err, int code) {
 }
 
 // phi(x) = elu(x) + 1 (eq. 7) on a pair of bf16 values, written as
-// max(x, 0) + min(exp(x), 1): x + 1 for x > 0 and exp(x) otherwise.  The
-// exponential is the hardware base-2 exponential on bf16 pairs,
-// exp(x) = 2^(x log2 e), with x log2 e formed in fp32 and rounded to bf16.
+// max(x, 0) + 2^min(x log2 e, 0): x + 1 for x > 0 and exp(x) otherwise.  All
+// arithmetic is packed bf16: x log2 e is formed as x c_hi + (x c_lo) with
+// c_hi + c_lo = log2 e to 2^-17 (one rounding of the fused multiply-add, so
+// the product is the correctly rounded bf16 value up to that residual), and
+// the exponential is the hardware base-2 exponential on bf16 pairs.
 __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
-  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-  constexpr float kLog2e = 1.4426950408889634f;
-  __nv_bfloat162 t = __floats2bfloat162_rn(lo * kLog2e, hi * kLog2e);
-  uint32_t e;
-  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(*reinterpret_cast<uint32_t*>(&t)));
-  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f), one = __float2bfloat162_rn(1.f);
   const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w);
-  const __nv_bfloat162 ex = *reinterpret_cast<const __nv_bfloat162*>(&e);
-  const __nv_bfloat162 r = __hadd2(__hmax2(x, zero), __hmin2(ex, one));
+  const __nv_bfloat162 c_hi = __halves2bfloat162(__ushort_as_bfloat16(0x3fb9),
+                                                 __ushort_as_bfloat16(0x3fb9));  // 1.4453125
+  const __nv_bfloat162 c_lo = __halves2bfloat162(__ushort_as_bfloat16(0xbb2c),
+                                                 __ushort_as_bfloat16(0xbb2c));  // -0.0026245
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.f);
+  const __nv_bfloat162 t = __hmin2(__hfma2(x, c_hi, __hmul2(x, c_lo)), zero);
+  uint32_t e;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(*reinterpret_cast<const uint32_t*>(&t)));
+  const __nv_bfloat162 r = __hadd2(__hmax2(x, zero), *reinterpret_cast<const __nv_bfloat162*>(&e));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// phi applied in place to a swizzled [128][64] bf16 tile by `nthr` threads
-// (t = 0 .. nthr-1; elementwise, so the swizzle does not matter).  Rows at or
-// past `valid` are zeroed: a zero phi(K) row adds nothing to any sum.
+__device__ __forceinline__ uint4 phi_vec(uint4 u) {
+  return make_uint4(phi_bf16x2(u.x), phi_bf16x2(u.y), phi_bf16x2(u.z), phi_bf16x2(u.w));
+}
+
+// phi applied in place to NTL swizzled [128][64] bf16 tiles spaced `stride`
+// bytes apart, by NT threads (t = 0 .. NT-1; elementwise, so the swizzle does
+// not matter).  Every thread first loads all of its vectors, then transforms
+// and stores them, so the loads and the exponentials overlap.  Rows at or past
+// `valid` are zeroed: a zero phi row adds nothing to any sum.
+template <int NT, int NTL>
+__device__ __forceinline__ void phi_tiles(uint8_t* tile, int stride, int valid, int t) {
+  constexpr int PER = TILE / 16 / NT;  // vectors per thread and tile
+  static_assert(PER * NT * 16 == TILE, "threads must divide the tile");
+  uint4 u[NTL][PER];
+#pragma unroll
+  for (int k = 0; k < NTL; ++k)
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      u[k][i] = *reinterpret_cast<const uint4*>(tile + k * stride + (t + i * NT) * 16);
+#pragma unroll
+  for (int k = 0; k < NTL; ++k)
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int v = t + i * NT;
+      const uint4 r = (v >> 3) >= valid ? make_uint4(0u, 0u, 0u, 0u) : phi_vec(u[k][i]);
+      *reinterpret_cast<uint4*>(tile + k * stride + v * 16) = r;
+    }
+}
+
+// phi applied in place to a swizzled [128][64] bf16 tile by `nthr` threads.
 __device__ __forceinline__ void phi_tile(uint8_t* tile, int valid, int t, int nthr = NCOMP) {
   for (int v = t; v < TILE / 16; v += nthr) {
     uint4* ptr = reinterpret_cast<uint4*>(tile + v * 16);
-    uint4 u = *ptr;
-    if ((v >> 3) >= valid)
-      u = make_uint4(0u, 0u, 0u, 0u);
-    else
-      u = make_uint4(phi_bf16x2(u.x), phi_bf16x2(u.y), phi_bf16x2(u.z), phi_bf16x2(u.w));
-    *ptr = u;
+    *ptr = (v >> 3) >= valid ? make_uint4(0u, 0u, 0u, 0u) : phi_vec(*ptr);
   }
 }
 
@@ -77,7 +102,7 @@ __device__ __forceinline__ void phi_tile_store(uint8_t* tile, int valid, int t, 
     if (r >= valid) {
       u = make_uint4(0u, 0u, 0u, 0u);
     } else {
-      u = make_uint4(phi_bf16x2(u.x), phi_bf16x2(u.y), phi_bf16x2(u.z), phi_bf16x2(u.w));
+      u = phi_vec(u);
       const int lc = (v & 7) ^ (r & 7);  // logical 16-byte chunk of this vector
       *reinterpret_cast<uint4*>(g + r * 64 + lc * 8) = u;
     }
