@@ -75,47 +75,6 @@ constexpr uint32_t T_Q = 368;    // bf16 phi(Q) per K, V stage, 32 columns each
 // Warp roles of the main pass (warp indices).
 constexpr int W_PHI0 = 2, W_MASK0 = 10, W_EPI0 = 14;
 
-// The constant ones tile: a [128][64] bf16 K-major tile whose column 0 is 1;
-// read as the second 64-wide N atom of the MN-major operand [V | 1].
-__device__ __forceinline__ void init_ones(uint8_t* tile, int t, int nthr) {
-  for (int v = t; v < TILE / 16; v += nthr) {
-    const int r = v >> 3, c = (v & 7) ^ (r & 7);  // logical 16-byte chunk of this vector
-    *reinterpret_cast<uint4*>(tile + v * 16) =
-        c == 0 ? make_uint4(0x3f80u, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
-// Lets the next kernel in the stream start its prologue on free SMs; its
-// griddepcontrol.wait still waits for this whole grid and its memory.
-__device__ __forceinline__ void grid_dep_launch() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Producer epilogue: wait (bounded) for the last loads issued into each stage,
-// so that no TMA write into shared memory is still in flight at exit.
-template <int NS>
-__device__ __forceinline__ void drain_loads(uint64_t* full, int issued) {
-  for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
-    mbar_wait(&full[i % NS], (i / NS) & 1, WAIT_NS);
-}
-
-// 64 bf16 (32 packed words) to a 128-byte global row: 32-byte stores when
-// the row is 32-byte aligned, else 16-byte stores.
-__device__ __forceinline__ void store_row_bf16(bf16* dst, const uint32_t* w, bool v8) {
-  if (v8) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * i),
-                   "r"(w[8 * i]), "r"(w[8 * i + 1]), "r"(w[8 * i + 2]), "r"(w[8 * i + 3]),
-                   "r"(w[8 * i + 4]), "r"(w[8 * i + 5]), "r"(w[8 * i + 6]), "r"(w[8 * i + 7])
-                   : "memory");
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      *reinterpret_cast<uint4*>(dst + 8 * i) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-  }
-}
-
 // ------------------------------------------------------------- state pass
 // Partial state dS~ = sum over the segment of phi(K) V~^T, written to
 // ws[bh][p] ([64][80] fp32) for every segment p but the last.
@@ -157,6 +116,11 @@ __global__ void __launch_bounds__(NTHR, 1)
     *reinterpret_cast<volatile int*>(&s_abort) = 1;
     fail(err, code);
     return false;
+  };
+  // the same, agreed by the whole warp (the tcgen05 loads and stores that
+  // follow are warp-collective)
+  auto wtu = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
+    return __all_sync(0xffffffffu, wt(bar, parity, code));
   };
   tc_fence_before();
   __syncthreads();
@@ -210,7 +174,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     const uint32_t lq = static_cast<uint32_t>(32 * qd) << 16;
     const int srow = 16 * qd + lane;
     float* rec = reinterpret_cast<float*>(sm + S_REC);
-    if (wt(&bar_done, 0, 34)) {
+    if (wtu(&bar_done, 0, 34)) {
       tc_fence_after();
       float sv[16], zz[16];
       tmem_ld16(TS + lq + 16 * wg, sv);
@@ -294,6 +258,11 @@ __global__ void __launch_bounds__(NTHR, 1)
     *reinterpret_cast<volatile int*>(&s_abort) = 1;
     fail(err, code);
     return false;
+  };
+  // the same, agreed by the whole warp (the tcgen05 loads and stores that
+  // follow are warp-collective)
+  auto wtu = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
+    return __all_sync(0xffffffffu, wt(bar, parity, code));
   };
   tc_fence_before();
   __syncthreads();
@@ -421,7 +390,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int c = 0; c < nch; ++c) {
       const int s = c % KNS;
       // full K, V stage c % KNS also means chunk c - KNS is done with phi(Q) slot s
-      if (wt(&bar_kv[s], (c / KNS) & 1, 14) && wt(&bar_q[c % QNS], (c / QNS) & 1, 14)) {
+      if (wtu(&bar_kv[s], (c / KNS) & 1, 14) && wtu(&bar_q[c % QNS], (c / QNS) & 1, 14)) {
         const int valid = min(TC_C, ne - (nb + c * TC_C));
         uint8_t* st = sm + F_KV + s * 2 * TILE;
         const uint8_t* qt = sm + F_Q + (c % QNS) * TILE;
@@ -506,7 +475,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       // qd = i / 32 is the same for the whole warp.
       for (int c = 0; c < nch; ++c) {
         const uint32_t ta = tm + (c & 1) * T_BUF + lq;
-        if (wt(&bar_a[c & 1], (c >> 1) & 1, 15)) {
+        if (wtu(&bar_a[c & 1], (c >> 1) & 1, 15)) {
           tc_fence_after();
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -577,7 +546,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         const int n0 = nb + c * TC_C;
         if (c + 1 < nch) {  // S~ after chunk c -> S~_prev(c+1), in the buffer O~(c-1) read
           uint8_t* sp = sm + F_SP + ((c + 1) & 1) * 16384;
-          if (wt(&bar_s, c & 1, 18)) {
+          if (wtu(&bar_s, c & 1, 18)) {
             tc_fence_after();
             float sv[48];
             tmem_ldn<3>(tm + T_S + lq, sv);  // columns 0-47
@@ -594,7 +563,7 @@ __global__ void __launch_bounds__(NTHR, 1)
           mbar_arrive(&bar_sp);
         }
         // out = O~[:, :64] / O~[:, 64], straight from registers to global memory
-        if (wt(&bar_o[c & 1], (c >> 1) & 1, 17)) {
+        if (wtu(&bar_o[c & 1], (c >> 1) & 1, 17)) {
           tc_fence_after();
           const uint32_t to = tm + (c & 1) * T_BUF + 64 + lq;
           float o[32], dd[16];

@@ -200,6 +200,181 @@ __device__ __forceinline__ void mask_cols(uint32_t taddr, float add, uint8_t* ds
   tile_put_cols<NC>(dst, row, key0 & 63, a);
 }
 
+// Lets the next kernel in the stream start its prologue on free SMs; its
+// griddepcontrol.wait still waits for this whole grid and its memory.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Producer epilogue: wait (bounded) for the last loads issued into each stage,
+// so that no TMA write into shared memory is still in flight at exit.
+template <int NS>
+__device__ __forceinline__ void drain_loads(uint64_t* full, int issued) {
+  for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
+    mbar_wait(&full[i % NS], (i / NS) & 1, WAIT_NS);
+}
+
+// 64 bf16 (32 packed words) to a 128-byte global row: 32-byte stores when
+// the row is 32-byte aligned, else 16-byte stores.
+__device__ __forceinline__ void store_row_bf16(bf16* dst, const uint32_t* w, bool v8) {
+  if (v8) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * i),
+                   "r"(w[8 * i]), "r"(w[8 * i + 1]), "r"(w[8 * i + 2]), "r"(w[8 * i + 3]),
+                   "r"(w[8 * i + 4]), "r"(w[8 * i + 5]), "r"(w[8 * i + 6]), "r"(w[8 * i + 7])
+                   : "memory");
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      *reinterpret_cast<uint4*>(dst + 8 * i) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
+}
+
+// The constant ones tile: a [128][64] bf16 K-major tile whose column 0 is 1;
+// read as the second 64-wide N atom of the MN-major operand [V | 1].
+__device__ __forceinline__ void init_ones(uint8_t* tile, int t, int nthr) {
+  for (int v = t; v < TILE / 16; v += nthr) {
+    const int r = v >> 3, c = (v & 7) ^ (r & 7);  // logical 16-byte chunk of this vector
+    *reinterpret_cast<uint4*>(tile + v * 16) =
+        c == 0 ? make_uint4(0x3f80u, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// An [80]-wide fp32 state in tensor memory (M = 64 layout: row r of the
+// state in lane 32 * (r / 16) + r % 16) as a bf16 operand tile: row r, columns
+// 0-63 into `tile` ([64][64], 128-byte swizzle) and column 64 into column 0 of
+// the second atom at tile + 8192 (whose other columns stay zero).  Called by
+// all four warps of a warpgroup (one per lane quarter); `lq` is the lane-quarter
+// field of this warp.
+__device__ __forceinline__ void state_to_tile(uint32_t tstate, uint32_t lq, int lane, int qd,
+                                              uint8_t* tile) {
+  const bool has_s = lane < 16;
+  const int srow = 16 * qd + lane;
+  float sv[48];
+  tmem_ldn<3>(tstate + lq, sv);  // columns 0-47
+  if (has_s) tile_put_cols<48>(tile, srow, 0, sv);
+  tmem_ldn<2>(tstate + lq + 48, sv);  // columns 48-79: the rest and the vector column
+  if (has_s) {
+    tile_put_cols<16>(tile, srow, 48, sv);
+    const float z8[8] = {sv[16], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    st_row_chunk(tile + 8192, srow, 0, z8);
+  }
+}
+
+// Zeroes the second atoms (tile + 8192, [64][64]) of `n` state tiles spaced
+// `stride` bytes apart, except their column 0 which state_to_tile writes.
+__device__ __forceinline__ void zero_state_atoms(uint8_t* tile, int stride, int n, int t, int nthr) {
+  for (int v = t; v < n * 512; v += nthr) {
+    const int r = (v >> 3) & 63;
+    if ((v & 7) != (r & 7))
+      *reinterpret_cast<uint4*>(tile + (v >> 9) * stride + 8192 + (v & 511) * 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Sum of records [lo, hi) of an [64][80] fp32 state spaced `stride` floats
+// apart, by 256 threads (t = 0 .. 255, 20 values each), into the fp32
+// [64][80] scratch `scr`.  Two records per round trip.
+__device__ __forceinline__ void sum_records(const float* rec0, long stride, int lo, int hi, int t,
+                                            float* scr) {
+  float acc[20];
+#pragma unroll
+  for (int j = 0; j < 20; ++j) acc[j] = 0.f;
+  int pp = lo;
+  for (; pp + 1 < hi; pp += 2) {
+    const float4* r0 = reinterpret_cast<const float4*>(rec0 + pp * stride) + t * 5;
+    const float4* r1 = reinterpret_cast<const float4*>(rec0 + (pp + 1) * stride) + t * 5;
+    float4 x[10];
+#pragma unroll
+    for (int j = 0; j < 5; ++j) {
+      x[j] = r0[j];
+      x[5 + j] = r1[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 5; ++j) {
+      acc[4 * j] += x[j].x + x[5 + j].x;
+      acc[4 * j + 1] += x[j].y + x[5 + j].y;
+      acc[4 * j + 2] += x[j].z + x[5 + j].z;
+      acc[4 * j + 3] += x[j].w + x[5 + j].w;
+    }
+  }
+  if (pp < hi) {
+    const float4* r0 = reinterpret_cast<const float4*>(rec0 + pp * stride) + t * 5;
+#pragma unroll
+    for (int j = 0; j < 5; ++j) {
+      const float4 x = r0[j];
+      acc[4 * j] += x.x;
+      acc[4 * j + 1] += x.y;
+      acc[4 * j + 2] += x.z;
+      acc[4 * j + 3] += x.w;
+    }
+  }
+  float4* d = reinterpret_cast<float4*>(scr) + t * 5;
+#pragma unroll
+  for (int j = 0; j < 5; ++j) d[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+}
+
+// The initial carried state from the fp32 scratch written by sum_records:
+// into tensor memory (80 columns at tstate) and, as bf16, into the operand
+// tile (see state_to_tile).  Called by one warpgroup.
+__device__ __forceinline__ void scratch_to_state(const float* scr, uint32_t tstate, uint32_t lq,
+                                                 int lane, int qd, uint8_t* tile) {
+  const bool has_s = lane < 16;
+  const int srow = 16 * qd + lane;
+  const float4* src = reinterpret_cast<const float4*>(scr) + srow * 20;
+#pragma unroll
+  for (int j = 0; j < 5; ++j) {  // 16 columns at a time
+    float sv[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 x = has_s ? src[4 * j + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      sv[4 * i] = x.x;
+      sv[4 * i + 1] = x.y;
+      sv[4 * i + 2] = x.z;
+      sv[4 * i + 3] = x.w;
+    }
+    tmem_st16(tstate + lq + 16 * j, sv);
+    if (has_s) {
+      if (j < 4) {
+        tile_put_cols<16>(tile, srow, 16 * j, sv);
+      } else {
+        const float z8[8] = {sv[0], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        st_row_chunk(tile + 8192, srow, 0, z8);
+      }
+    }
+  }
+  tmem_st_wait();
+}
+
+// min(phi(x), 1) = phi'(x) on 8 bf16 values (one 16-byte vector), as floats.
+__device__ __forceinline__ void dphi8(uint4 u, float* f) {
+  const uint4 r = phi_vec(u);
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = fminf(__uint_as_float(w[i] << 16), 1.f);
+    f[2 * i + 1] = fminf(__uint_as_float(w[i] & 0xffff0000u), 1.f);
+  }
+}
+
+// Idle accounting of a polling loop: returns false once `limit_ns` have
+// passed without progress (the clock is read every 1024 idle polls), else
+// sleeps briefly so the other warps of this SM quarter keep the issue slots.
+struct PollIdle {
+  uint32_t idle = 0;
+  uint64_t t0 = 0;
+  __device__ __forceinline__ void progress() { idle = 0; }
+  __device__ __forceinline__ bool wait(uint64_t limit_ns) {
+    if ((++idle & 1023u) != 0) {
+      __nanosleep(32);
+      return true;
+    }
+    const uint64_t now = globaltimer_ns();
+    if (idle == 1024) t0 = now;
+    return now - t0 <= limit_ns;
+  }
+};
+
 __device__ __forceinline__ void compute_sync() {  // the compute warps only
   asm volatile("bar.sync 1, %0;" ::"n"(NCOMP) : "memory");
 }
