@@ -36,38 +36,16 @@ using namespace tcc;
 constexpr int DM = 64 * 64;
 constexpr int REC = 2 * (DM + 64);  // per-sub-segment record [S | z | R | r]
 
-// MODE 0 shared memory: stages of q, k, v, dout, out; two gt tiles; ones; two gam tiles
-constexpr int S_STAGE = 5 * TILE;
-constexpr int S_GT = NST * S_STAGE;
-constexpr int S_ONES = S_GT + 2 * TILE;
-constexpr int S_GAMT = S_ONES + 1024;
-constexpr int S_SMEM = S_GAMT + 2 * 2048 + 1024;
-// MODE 1 shared memory: stages of phi(Q), phi(K), v, gt; P; dP; two bf16
-// state tiles; ones; two gam tiles
+// Main-pass shared memory: two stages of phi(Q), phi(K), V, gt; P; dP (both
+// also the output staging); two bf16 state tiles; the vector atom (role 0:
+// ones, the N atom of [V | 1]; role 1: gam in column 0, the N atom of [gt | gam]).
 constexpr int M_STAGE = 4 * TILE;
 constexpr int M_P = NST * M_STAGE;
 constexpr int M_DP = M_P + 2 * TILE;
 constexpr int M_RP = M_DP + 2 * TILE;
-constexpr int M_ONES = M_RP + 2 * 8192;
-constexpr int M_GAMT = M_ONES + 1024;
-constexpr int M_SMEM = M_GAMT + 2 * 2048 + 1024;
-static_assert(S_SMEM + 2048 <= 232448 && M_SMEM + 2048 <= 232448, "shared memory");
-
-// The ones tile (1 KB, every element 1) and two zeroed gam tiles (2 KB each): B
-// operands of the N = 8 products that give z = phi(K)^T 1 and r = phi(Q)^T gam.
-__device__ __forceinline__ void init_vec_tiles(uint8_t* ones, uint8_t* gamt, int t) {
-  for (int v = t; v < 1024 / 16; v += NCOMP)
-    *reinterpret_cast<uint4*>(ones + v * 16) =
-        make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
-  for (int v = t; v < 2 * 2048 / 16; v += NCOMP)
-    *reinterpret_cast<uint4*>(gamt + v * 16) = make_uint4(0u, 0u, 0u, 0u);
-}
-
-// gam_i into row 0, column i of the gam tile (K-major, 128-byte swizzle,
-// two 64-column atoms; row 0 is not permuted by the swizzle).
-__device__ __forceinline__ void put_gam(uint8_t* gamt, int i, float g) {
-  *reinterpret_cast<bf16*>(gamt + (i >> 6) * 1024 + (i & 63) * 2) = __float2bfloat16_rn(g);
-}
+constexpr int M_VEC = M_RP + 2 * 8192;
+constexpr int M_SMEM = M_VEC + TILE + 1024;
+static_assert(M_SMEM + 2048 <= 232448, "shared memory");
 
 // Role 1: the masked bf16 rows of dA (+ gam) and of A for this warpgroup's
 // KW keys from key0, loaded together so that one wait covers both.
@@ -91,41 +69,42 @@ __device__ __forceinline__ void mask2_cols(uint32_t tda, uint32_t ta, float add,
 }
 
 struct BwdMaps {
-  CUtensorMap q, k, v, g, o;  // MODE 0 inputs
-  CUtensorMap fq, fk, gt;     // MODE 0 outputs, MODE 1 inputs
-  CUtensorMap dq, dk, dv;     // MODE 1 outputs (TMA stores)
+  CUtensorMap q, k, v, g, o;  // state-pass inputs
+  CUtensorMap fq, fk, gt;     // state-pass outputs, main-pass inputs
+  CUtensorMap dq, dk, dv;     // main-pass outputs (TMA stores)
 };
 
-template <int MODE>
+// Main pass: two roles per segment (grid z).  Role 0 walks the segment's
+// chunks forward carrying S~ = [S | z] and writes dq; role 1 walks them
+// backward carrying R~ = [R | r] and writes dk and dv.  Per chunk: A and dA,
+// then the carried-state update (it only needs the stage, so the compute warps
+// read the next state out while the gradient products run), then the gradient
+// products.  The vector terms gam z_prev (dq) and r_next (dk) are added in the
+// epilogues.
 __global__ void __launch_bounds__(NTHR, 1)
-    k_tc_bwd(const __grid_constant__ BwdMaps maps, const float* __restrict__ den,
-             float* __restrict__ rec, float* __restrict__ gam, bf16* __restrict__ gt_out,
-             bf16* __restrict__ fq_out, bf16* __restrict__ fk_out, int N, int seg_len, int nsub,
-             int subs_per_seg, int* err) {
+    k_tc_bwd_main(const __grid_constant__ BwdMaps maps, const float* __restrict__ rec,
+                  const float* __restrict__ gam, int N, int seg_len, int nsub, int subs_per_seg,
+                  int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;
-  const int role = MODE == 0 ? 2 : static_cast<int>(blockIdx.z);  // 0 dq, 1 dk/dv, 2 partials
+  const int role = static_cast<int>(blockIdx.z);  // 0 dq, 1 dk / dv
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   __shared__ uint64_t bar_full[NST], bar_empty[NST];
-  __shared__ uint64_t bar_in, bar_a, bar_p, bar_rp, bar_o, bar_s, bar_s2[2];
+  __shared__ uint64_t bar_in, bar_a, bar_p, bar_rp, bar_o, bar_s;
   __shared__ uint32_t tmem_base;
-  __shared__ float s_vec[2][64];    // carried z (role 0) or r (role 1) before chunk c, by c & 1
-  __shared__ float s_dot[NWG][TC_C];  // MODE 0: partial dot products for gam
+  __shared__ float s_vec[2][64];  // carried z (role 0) or r (role 1) before chunk c, by c & 1
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = p * seg_len;
   const int ne = min(N, nb + seg_len);
   const int nch = (ne - nb + TC_C - 1) / TC_C;
-  const int stage_bytes = MODE == 0 ? S_STAGE : M_STAGE;
-  uint8_t* ones = sm + (MODE == 0 ? S_ONES : M_ONES);
-  uint8_t* gamt = sm + (MODE == 0 ? S_GAMT : M_GAMT);  // two 2 KB tiles, by chunk parity
+  uint8_t* vec = sm + M_VEC;
 
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&bar_full[s], 1);
-      // MODE 0: the MMAs; MODE 1: the MMAs and every compute thread
-      // (the epilogues read phi from the stage)
-      mbar_init(&bar_empty[s], MODE == 0 ? 1 : 1 + NCOMP);
+      mbar_init(&bar_empty[s], 1 + NCOMP);  // the MMAs and every compute thread (epilogues read phi)
     }
     mbar_init(&bar_in, NCOMP);
     mbar_init(&bar_a, 1);
@@ -133,18 +112,21 @@ __global__ void __launch_bounds__(NTHR, 1)
     mbar_init(&bar_rp, NCOMP);
     mbar_init(&bar_o, 1);
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_s2[0], 1);
-    mbar_init(&bar_s2[1], 1);
     fence_barrier_init();
     s_abort = 0;
   }
   if (warp == 1) tmem_alloc(&tmem_base, 512);
-  if (warp >= 2) {
-    init_vec_tiles(ones, gamt, threadIdx.x - 64);
+  if (warp >= 2) {  // the vector atom: ones (role 0) or zeros (role 1; gam is written per chunk)
+    const int t = threadIdx.x - 64;
+    for (int v = t; v < TILE / 16; v += NCOMP) {
+      const int r = v >> 3, c = (v & 7) ^ (r & 7);
+      *reinterpret_cast<uint4*>(vec + v * 16) =
+          (role == 0 && c == 0) ? make_uint4(0x3f80u, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    }
     fence_proxy_async();
   }
-  // Bounded wait shared by all roles: after the first failure every later
-  // wait gives up at once, so all threads still reach the block-wide barriers.
+  // Bounded wait: after the first failure every later wait gives up at once,
+  // so all threads still reach the block-wide barriers.
   auto wt = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
     if (*reinterpret_cast<volatile int*>(&s_abort)) return false;
     if (mbar_wait(bar, parity, WAIT_NS)) return true;
@@ -152,80 +134,58 @@ __global__ void __launch_bounds__(NTHR, 1)
     fail(err, code);
     return false;
   };
+  // the same, agreed by the whole warp (tcgen05 loads and stores that follow
+  // are warp-collective)
+  auto wtu = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
+    return __all_sync(0xffffffffu, wt(bar, parity, code));
+  };
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  grid_dep_wait();  // the previous kernel's outputs are visible from here on
+  grid_dep_wait();  // the state pass's outputs are visible from here on
   const uint32_t tm = tmem_base;
   const uint32_t TA = tm, TDA = tm + 128, TG1 = tm + 256, TG2 = tm + 320, TST = tm + 384;
-  const uint32_t TV = tm + 448, TV2 = tm + 464;  // N = 8 vector accumulators (z / r)
   auto chunk_at = [&](int c) { return role == 1 ? nch - 1 - c : c; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int ntile = MODE == 0 ? 5 : 4;
+      int issued = 0;
       for (int c = 0; c < nch; ++c) {
         const int s = c % NST;
         if (c >= NST && !wt(&bar_empty[s], ((c / NST) - 1) & 1, 21)) break;
-        uint8_t* st = sm + s * stage_bytes;
-        mbar_arrive_expect_tx(&bar_full[s], ntile * TILE);
+        uint8_t* st = sm + s * M_STAGE;
+        mbar_arrive_expect_tx(&bar_full[s], 4 * TILE);
         const int n0 = nb + chunk_at(c) * TC_C;
-        if (MODE == 0) {
-          tma_load_3d(st, &maps.q, &bar_full[s], 0, n0, bh);
-          tma_load_3d(st + TILE, &maps.k, &bar_full[s], 0, n0, bh);
-          tma_load_3d(st + 2 * TILE, &maps.v, &bar_full[s], 0, n0, bh);
-          tma_load_3d(st + 3 * TILE, &maps.g, &bar_full[s], 0, n0, bh);
-          tma_load_3d(st + 4 * TILE, &maps.o, &bar_full[s], 0, n0, bh);
-        } else {
-          tma_load_3d(st, &maps.fq, &bar_full[s], 0, n0, bh);
-          tma_load_3d(st + TILE, &maps.fk, &bar_full[s], 0, n0, bh);
-          tma_load_3d(st + 2 * TILE, &maps.v, &bar_full[s], 0, n0, bh);
-          tma_load_3d(st + 3 * TILE, &maps.gt, &bar_full[s], 0, n0, bh);
-        }
+        tma_load_3d(st, &maps.fq, &bar_full[s], 0, n0, bh);
+        tma_load_3d(st + TILE, &maps.fk, &bar_full[s], 0, n0, bh);
+        tma_load_3d(st + 2 * TILE, &maps.v, &bar_full[s], 0, n0, bh);
+        tma_load_3d(st + 3 * TILE, &maps.gt, &bar_full[s], 0, n0, bh);
+        ++issued;
       }
+      for (int i = issued > NST ? issued - NST : 0; i < issued; ++i)  // no load in flight at exit
+        mbar_wait(&bar_full[i % NST], (i / NST) & 1, WAIT_NS);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    // Per chunk: A and dA, then the carried-state update (it only needs the
-    // stage and frees the compute warps to stage the next state while the
-    // gradient products run), then the gradient products.
     if (lane == 0) {
       constexpr uint32_t ID_AA = idesc_bf16(128, 128, false, false);
       constexpr uint32_t ID_G = idesc_bf16(128, 64, false, false);
       constexpr uint32_t ID_GMN = idesc_bf16(128, 64, false, true);
       constexpr uint32_t ID_GTT = idesc_bf16(128, 64, true, true);
-      constexpr uint32_t ID_ST = idesc_bf16(64, 64, true, true);
-      constexpr uint32_t ID_V = idesc_bf16(64, 8, true, false);  // phi^T x (ones | gam)
+      constexpr uint32_t ID_ST = idesc_bf16(64, 80, true, true);  // 64 x 80 state update
       const uint64_t dP0 = sdesc(smem_u32(sm + M_P), TILE, 1024);
       const uint64_t dDP = sdesc(smem_u32(sm + M_DP), 16, 1024);
       const uint64_t dDPT = sdesc(smem_u32(sm + M_DP), TILE, 1024);
-      const uint64_t dOnes = sdesc(smem_u32(ones), 16, 1024);
+      const uint32_t vaddr = smem_u32(vec);
       for (int c = 0; c < nch; ++c) {
         const int s = c % NST;
-        const uint32_t qs = smem_u32(sm + s * stage_bytes);
-        const uint32_t gs = MODE == 0 ? smem_u32(sm + S_GT + (c & 1) * TILE) : qs + 3 * TILE;
-        const uint64_t dQ = sdesc(qs, 16, 1024), dK = sdesc(qs + TILE, 16, 1024);
-        const uint64_t dV = sdesc(qs + 2 * TILE, 16, 1024), dG = sdesc(gs, 16, 1024);
-        const uint64_t dGam = sdesc(smem_u32(gamt + (c & 1) * 2048), 16, 1024);
+        const uint32_t qs = smem_u32(sm + s * M_STAGE), ks = qs + TILE, vs = qs + 2 * TILE, gs = qs + 3 * TILE;
+        const uint64_t dQ = sdesc(qs, 16, 1024), dK = sdesc(ks, 16, 1024);
+        const uint64_t dV = sdesc(vs, 16, 1024), dG = sdesc(gs, 16, 1024);
         const uint64_t dRP = sdesc(smem_u32(sm + M_RP + (c & 1) * 8192), 16, 1024);
         if (!wt(&bar_in, c & 1, 22)) break;
         tc_fence_after();
-        if (MODE == 0) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // S += phi(K)^T V, z += phi(K)^T 1
-            mma_bf16(TG1, dadd(dK, kk * 2048), dadd(dV, kk * 2048), ID_ST, 1);
-            mma_bf16(TV, dadd(dK, kk * 2048), dadd(dOnes, 32 * (kk & 3)), ID_V, 1);
-          }
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // R += phi(Q)^T gt, r += phi(Q)^T gam
-            mma_bf16(TST, dadd(dQ, kk * 2048), dadd(dG, kk * 2048), ID_ST, 1);
-            mma_bf16(TV2, dadd(dQ, kk * 2048), dadd(dGam, (kk >> 2) * 1024 + 32 * (kk & 3)), ID_V, 1);
-          }
-          mma_commit(&bar_s2[c & 1]);
-          mma_commit(&bar_empty[s]);
-          continue;
-        }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // dA (without gam) = gt V^T
           mma_bf16(TDA, dadd(dG, 32 * kk), dadd(dV, 32 * kk), ID_AA, kk > 0);
@@ -237,17 +197,15 @@ __global__ void __launch_bounds__(NTHR, 1)
         if (!wt(&bar_rp, c & 1, 23)) break;  // the carried state has been read out
         tc_fence_after();
         if (role == 0) {
+          const uint64_t dVt = sdesc(vs, vaddr - vs, 1024);  // [V | 1]
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // S += phi(K)^T V, z += phi(K)^T 1
-            mma_bf16(TST, dadd(dK, kk * 2048), dadd(dV, kk * 2048), ID_ST, 1);
-            mma_bf16(TV, dadd(dK, kk * 2048), dadd(dOnes, 32 * (kk & 3)), ID_V, 1);
-          }
+          for (int kk = 0; kk < 8; ++kk)  // S~ += phi(K)^T [V | 1]
+            mma_bf16(TST, dadd(dK, kk * 2048), dadd(dVt, kk * 2048), ID_ST, 1);
         } else {
+          const uint64_t dGt = sdesc(gs, vaddr - gs, 1024);  // [gt | gam]
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // R += phi(Q)^T gt, r += phi(Q)^T gam
-            mma_bf16(TST, dadd(dQ, kk * 2048), dadd(dG, kk * 2048), ID_ST, 1);
-            mma_bf16(TV, dadd(dQ, kk * 2048), dadd(dGam, (kk >> 2) * 1024 + 32 * (kk & 3)), ID_V, 1);
-          }
+          for (int kk = 0; kk < 8; ++kk)  // R~ += phi(Q)^T [gt | gam]
+            mma_bf16(TST, dadd(dQ, kk * 2048), dadd(dGt, kk * 2048), ID_ST, 1);
         }
         mma_commit(&bar_s);
         if (!wt(&bar_p, c & 1, 23)) break;
@@ -255,8 +213,8 @@ __global__ void __launch_bounds__(NTHR, 1)
         if (role == 0) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dP phi(K)
-            mma_bf16(TG1, dadd(dDP, (kk >> 2) * TILE + (kk & 3) * 32), dadd(sdesc(qs + TILE, 16, 1024), kk * 2048),
-                     ID_GMN, kk > 0);
+            mma_bf16(TG1, dadd(dDP, (kk >> 2) * TILE + (kk & 3) * 32), dadd(dK, kk * 2048), ID_GMN,
+                     kk > 0);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // + gt S_prev^T
             mma_bf16(TG1, dadd(dG, 32 * kk), dadd(dRP, 32 * kk), ID_G, 1);
@@ -277,6 +235,9 @@ __global__ void __launch_bounds__(NTHR, 1)
         mma_commit(&bar_o);
         mma_commit(&bar_empty[s]);
       }
+      // every issued MMA has finished before the exit (also after an early break)
+      mma_commit(&bar_s);
+      mbar_wait(&bar_s, nch & 1, WAIT_NS);
     }
   } else {
     // ---------------------------------------------------------- compute warps
@@ -291,172 +252,134 @@ __global__ void __launch_bounds__(NTHR, 1)
     const int srow = 16 * qd + lane;
     const int c0 = OW * wg, k0 = KW * wg;
     const long hb = static_cast<long>(bh) * N;
-    auto gam_at = [&](int c) {     // gam of this thread's row in chunk c
+    auto gam_at = [&](int c) {  // gam of this thread's row in chunk c
       const int n0 = nb + chunk_at(c) * TC_C;
       return row < min(TC_C, ne - n0) ? gam[hb + n0 + row] : 0.f;
     };
-    if (MODE == 1) {
+    // gam_i into row i, column 0 of the vector atom (128-byte swizzle)
+    auto put_gam = [&](float g) {
+      *reinterpret_cast<bf16*>(vec + row * 128 + ((row & 7) << 4)) = __float2bfloat16_rn(g);
+    };
+    {
       // carried state: role 0 sums the records of the sub-segments before this
-      // segment (S, z), role 1 those after it (R, r); warpgroup 0 loads it
-      if (wg == 0) {
-        const int lo = role == 0 ? 0 : (p + 1) * subs_per_seg;
-        const int hi = role == 0 ? p * subs_per_seg : nsub;
-        const int off = role == 0 ? 0 : DM + 64;
-        float sv[64], vv[16];
-        for (int j = 0; j < 64; ++j) sv[j] = 0.f;
-        for (int j = 0; j < 16; ++j) vv[j] = 0.f;
-        for (int pp = lo; pp < hi; ++pp) {
-          const float* r0 = rec + (static_cast<long>(bh) * nsub + pp) * REC + off;
-          if (has_s) {
-            const float4* rr = reinterpret_cast<const float4*>(r0 + srow * 64);
+      // segment ([S | z]), role 1 those after it ([R | r]); every compute
+      // thread adds up a slice, into the P tile (free until the first mask)
+      const int lo = role == 0 ? 0 : (p + 1) * subs_per_seg;
+      const int hi = role == 0 ? p * subs_per_seg : nsub;
+      const int off = role == 0 ? 0 : DM + 64;
+      float* scr = reinterpret_cast<float*>(sm + M_P);
+      for (int j = t; j < (DM + 64) / 4; j += NCOMP) {  // 1040 float4 per state
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int pp = lo;
+        for (; pp + 1 < hi; pp += 2) {  // two records per round trip
+          const float4 x = reinterpret_cast<const float4*>(rec + (static_cast<long>(bh) * nsub + pp) * REC + off)[j];
+          const float4 y = reinterpret_cast<const float4*>(rec + (static_cast<long>(bh) * nsub + pp + 1) * REC + off)[j];
+          acc.x += x.x + y.x;
+          acc.y += x.y + y.y;
+          acc.z += x.z + y.z;
+          acc.w += x.w + y.w;
+        }
+        if (pp < hi) {
+          const float4 x = reinterpret_cast<const float4*>(rec + (static_cast<long>(bh) * nsub + pp) * REC + off)[j];
+          acc.x += x.x;
+          acc.y += x.y;
+          acc.z += x.z;
+          acc.w += x.w;
+        }
+        reinterpret_cast<float4*>(scr)[j] = acc;
+      }
+      compute_sync();
+      if (wg == 0) {  // into TMEM (the MMA's accumulator) and the bf16 state tile
+        float sv[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float4 x = rr[j];
-              sv[4 * j] += x.x;
-              sv[4 * j + 1] += x.y;
-              sv[4 * j + 2] += x.z;
-              sv[4 * j + 3] += x.w;
-            }
-            vv[0] += r0[DM + srow];
+        for (int j = 0; j < 5; ++j) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = 16 * j + i;
+            sv[i] = !has_s ? 0.f : col < 64 ? scr[srow * 64 + col] : col == 64 ? scr[DM + srow] : 0.f;
           }
+          tmem_st16(TST + lq + 16 * j, sv);
+          if (has_s && j < 4) tile_put_cols<16>(sm + M_RP, srow, 16 * j, sv);
+          if (has_s && j == 4) s_vec[0][srow] = sv[0];
         }
-        for (int j = 0; j < 64; j += 16) tmem_st16(TST + lq + j, sv + j);
-        for (int j = 1; j < 8; ++j) vv[j] = vv[0];
-        tmem_st16(TV + lq, vv);
         tmem_st_wait();
-        if (has_s) {
-          tile_put_cols<64>(sm + M_RP, srow, 0, sv);
-          s_vec[0][srow] = vv[0];
-        }
       }
       fence_proxy_async();
-      compute_sync();
+      compute_sync();  // the P tile is free again
       tc_fence_before();
       mbar_arrive(&bar_rp);
       // chunk 0 inputs
       const float g0 = gam_at(0);
       wt(&bar_full[0], 0, 25);
       if (role == 1 && wg == 0) {
-        put_gam(gamt, row, g0);
+        put_gam(g0);
         fence_proxy_async();
       }
       mbar_arrive(&bar_in);
-    } else {
-      if (wg == 0) {
-        float zero[16];
-        for (int j = 0; j < 16; ++j) zero[j] = 0.f;
-        for (int j = 0; j < 64; j += 16) {
-          tmem_st16(TG1 + lq + j, zero);
-          tmem_st16(TST + lq + j, zero);
-        }
-        tmem_st16(TV + lq, zero);
-        tmem_st16(TV2 + lq, zero);
-        tmem_st_wait();
-      }
-      tc_fence_before();
     }
-    float gm = MODE == 1 ? gam_at(0) : 0.f;
+    float gm = gam_at(0);
     for (int c = 0; c < nch; ++c) {
       const int s = c % NST;
       const int n0 = nb + chunk_at(c) * TC_C;
-      const int valid = min(TC_C, ne - n0);
-      const bool rv = row < valid;
-      uint8_t* st = sm + s * stage_bytes;
-      if (MODE == 0) {
-        const float dn = rv ? den[hb + n0 + row] : 1.f;
-        if (c > 1) {  // gt / gam tiles of parity c & 1 are free once chunk c-2's MMAs finished
-          wt(&bar_s2[c & 1], ((c - 2) >> 1) & 1, 24);
-          tc_fence_after();
-        }
-        compute_sync();
-        wt(&bar_full[s], (c / NST) & 1, 25);
-        uint8_t* gtile = sm + S_GT + (c & 1) * TILE;
-        // gt = dout / den on this warpgroup's columns; gam = -(gt . out)
-        float g[OW], o[OW];
-        tile_row_cols<OW>(st + 3 * TILE, row, c0, g);
-        tile_row_cols<OW>(st + 4 * TILE, row, c0, o);
-        const float inv = 1.f / dn;
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < OW; ++i) {
-          g[i] = rv ? g[i] * inv : 0.f;
-          acc = fmaf(g[i], o[i], acc);
-        }
-        s_dot[wg][row] = acc;
-        tile_put_cols<OW>(gtile, row, c0, g);
-        if (rv) store_bf16<OW>(gt_out + (hb + n0 + row) * 64 + c0, g);
-        phi_tile_store(st, valid, t, fq_out + (hb + n0) * 64);
-        phi_tile_store(st + TILE, valid, t, fk_out + (hb + n0) * 64);
-        compute_sync();
-        if (wg == 0) {
-          float dot = 0.f;
-#pragma unroll
-          for (int w = 0; w < NWG; ++w) dot += s_dot[w][row];
-          const float gmv = rv ? -dot : 0.f;
-          put_gam(gamt + (c & 1) * 2048, row, gmv);
-          if (rv) gam[hb + n0 + row] = gmv;
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        mbar_arrive(&bar_in);
-        continue;
-      }
-      // ------------------------------------------------------------- MODE 1
+      uint8_t* st = sm + s * M_STAGE;
       // P, dP of chunk c
-      wt(&bar_a, c & 1, 26);
+      const bool ok_a = wtu(&bar_a, c & 1, 26);
       tc_fence_after();
       if (t == 0) bulk_wait_read();  // the previous chunk's output tiles have left P / dP
       compute_sync();
-      if (role == 1)
-        mask2_cols(TDA + lq + k0, TA + lq + k0, gm, sm + M_DP + (k0 >> 6) * TILE,
-                   sm + M_P + (k0 >> 6) * TILE, row, k0);
-      else
-        mask_cols<KW>(TDA + lq + k0, gm, sm + M_DP + (k0 >> 6) * TILE, row, k0);
+      if (ok_a) {
+        if (role == 1)
+          mask2_cols(TDA + lq + k0, TA + lq + k0, gm, sm + M_DP + (k0 >> 6) * TILE,
+                     sm + M_P + (k0 >> 6) * TILE, row, k0);
+        else
+          mask_cols<KW>(TDA + lq + k0, gm, sm + M_DP + (k0 >> 6) * TILE, row, k0);
+      }
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&bar_p);
+      // carried state for chunk c+1 (after this chunk's update); it must be
+      // read before the next chunk's gam replaces this chunk's in the vector atom
+      if (c + 1 < nch) {
+        if (wtu(&bar_s, c & 1, 28)) {
+          tc_fence_after();
+          float sv[OW], vv[16];
+          tmem_ldn<OW / 16>(TST + lq + c0, sv);
+          tmem_ldn<1>(TST + lq + 64, vv);
+          if (has_s) {
+            tile_put_cols<OW>(sm + M_RP + ((c + 1) & 1) * 8192, srow, c0, sv);
+            if (wg == 0) s_vec[(c + 1) & 1][srow] = vv[0];
+          }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        mbar_arrive(&bar_rp);
+      }
       // inputs of chunk c+1 (the tensor cores may start on it)
       float gm_next = 0.f;
       if (c + 1 < nch) {
         gm_next = gam_at(c + 1);
         wt(&bar_full[(c + 1) % NST], ((c + 1) / NST) & 1, 25);
         if (role == 1 && wg == 0) {
-          put_gam(gamt + ((c + 1) & 1) * 2048, row, gm_next);
+          put_gam(gm_next);
           fence_proxy_async();
         }
         mbar_arrive(&bar_in);
       }
-      // carried state for chunk c+1 (after this chunk's update)
-      if (c + 1 < nch) {
-        wt(&bar_s, c & 1, 28);
-        tc_fence_after();
-        float sv[OW], vv[16];
-        tmem_ldn<OW / 16>(TST + lq + c0, sv);
-        tmem_ldn<1>(TV + lq, vv);
-        if (has_s) {
-          tile_put_cols<OW>(sm + M_RP + ((c + 1) & 1) * 8192, srow, c0, sv);
-          if (wg == 0) s_vec[(c + 1) & 1][srow] = vv[0];
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        mbar_arrive(&bar_rp);
-      }
       // gradients of chunk c, staged in the free P / dP tiles and TMA-stored
-      wt(&bar_o, c & 1, 27);
-      tc_fence_after();
-      {
-        const float* vec = s_vec[c & 1];
+      if (wtu(&bar_o, c & 1, 27)) {
+        tc_fence_after();
+        const float* vcur = s_vec[c & 1];
         float gv[OW], x[OW];
         tmem_ldn<OW / 16>(TG1 + lq + c0, gv);
         if (role == 0) {  // dq = (grad_phiQ + gam z_prev) * phi'(Q)
           tile_row_cols<OW>(st, row, c0, x);
 #pragma unroll
-          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + gm * vec[c0 + i]) * fminf(x[i], 1.f);
+          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + gm * vcur[c0 + i]) * fminf(x[i], 1.f);
           tile_put_cols<OW>(sm + M_DP, row, c0, gv);
         } else {          // dk = (grad_phiK + r_next) * phi'(K), dv
           tile_row_cols<OW>(st + TILE, row, c0, x);
 #pragma unroll
-          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + vec[c0 + i]) * fminf(x[i], 1.f);
+          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + vcur[c0 + i]) * fminf(x[i], 1.f);
           tile_put_cols<OW>(sm + M_P, row, c0, gv);
           tmem_ldn<OW / 16>(TG2 + lq + c0, gv);
           tile_put_cols<OW>(sm + M_P + TILE, row, c0, gv);
@@ -466,7 +389,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       tc_fence_before();
       mbar_arrive(&bar_empty[s]);  // this thread is done with the stage
       compute_sync();              // s_vec[c & 1] is free again; the output tiles are complete
-      if (t == 0) {
+      if (t == 0 && !*reinterpret_cast<volatile int*>(&s_abort)) {
         if (role == 0) {
           tma_store_3d(&maps.dq, sm + M_DP, 0, n0, bh);
         } else {
@@ -477,32 +400,252 @@ __global__ void __launch_bounds__(NTHR, 1)
       }
       gm = gm_next;
     }
-    if (MODE == 1 && t == 0) bulk_wait_all();
-    if (MODE == 0) {
-      bool done = true;
-      for (int c = max(0, nch - 2); c < nch; ++c)  // the last two state updates, in order
-        done = wt(&bar_s2[c & 1], (c >> 1) & 1, 29) && done;
-      if (done) {
-        tc_fence_after();
-        float* r0 = rec + (static_cast<long>(bh) * nsub + p) * REC;
-        float sv[OW], vv[16];
-        tmem_ldn<OW / 16>(TG1 + lq + c0, sv);
-        if (has_s)
-          for (int j = 0; j < OW; ++j) r0[srow * 64 + c0 + j] = sv[j];
-        tmem_ldn<OW / 16>(TST + lq + c0, sv);
-        if (has_s)
-          for (int j = 0; j < OW; ++j) r0[DM + 64 + srow * 64 + c0 + j] = sv[j];
-        if (wg < 2) {
-          tmem_ldn<1>((wg == 0 ? TV : TV2) + lq, vv);
-          if (has_s) r0[(wg == 0 ? DM : 2 * DM + 64) + srow] = vv[0];
-        }
-      }
-    }
+    if (t == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tm, 512);
+}
+
+// ------------------------------------------------------------- state pass
+// One CTA per sub-segment.  Per chunk: phi(Q), phi(K) in place (and to the
+// workspace), gt = dout / den in place over dout (and to the workspace), gam
+// = -(gt . out) (to the workspace and as column 0 of the gam tile), then
+//   S~ += phi(K)^T [V | 1]   and   R~ += phi(Q)^T [gt | gam]
+// as two 64 x 80 products whose last atoms are the ones tile and the gam
+// tile.  The sub-segment's partial [S | z | R | r] leaves by one bulk copy.
+// smem: two stages of [Q | K | V | dout -> gt | out], the ones tile, two gam
+// tiles (one per stage).
+constexpr int SS_STAGE = 5 * TILE;
+constexpr int SS_ONES = 2 * SS_STAGE;
+constexpr int SS_GAMT = SS_ONES + TILE;
+constexpr int SS_SMEM = SS_GAMT + 2 * TILE + 1024;
+constexpr uint32_t ID_ST80 = idesc_bf16(64, 80, true, true);
+
+struct StateMaps {
+  CUtensorMap q, k, v, g, o;
+};
+
+// The constant ones tile ([128][64] bf16, column 0 = 1): the second N atom of
+// the MN-major operand [V | 1].
+__device__ __forceinline__ void ones_tile(uint8_t* tile, int t, int nthr) {
+  for (int v = t; v < TILE / 16; v += nthr) {
+    const int r = v >> 3, c = (v & 7) ^ (r & 7);
+    *reinterpret_cast<uint4*>(tile + v * 16) =
+        c == 0 ? make_uint4(0x3f80u, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__global__ void __launch_bounds__(NTHR, 1)
+    k_tc_bwd_state(const __grid_constant__ StateMaps maps, const float* __restrict__ den,
+                   float* __restrict__ gam, bf16* __restrict__ gt_out, bf16* __restrict__ fq_out,
+                   bf16* __restrict__ fk_out, float* __restrict__ rec, int N, int sub_len, int nsub,
+                   int* err) {
+  const int p = blockIdx.x, bh = blockIdx.y;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  __shared__ uint64_t bar_full[2], bar_empty[2], bar_phi[2], bar_done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = p * sub_len;
+  const int ne = min(N, nb + sub_len);
+  const int nch = (ne - nb + TC_C - 1) / TC_C;
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_phi[s], NCOMP);
+    }
+    mbar_init(&bar_done, 1);
+    fence_barrier_init();
+    prefetch_tensormap(&maps.q);
+    prefetch_tensormap(&maps.k);
+    prefetch_tensormap(&maps.v);
+    prefetch_tensormap(&maps.g);
+    prefetch_tensormap(&maps.o);
+    s_abort = 0;
+  }
+  if (warp == 1) tmem_alloc(&tmem_base, 256);
+  if (warp >= 2) {
+    const int t = threadIdx.x - 64;
+    ones_tile(sm + SS_ONES, t, NCOMP);
+    for (int v = t; v < 2 * TILE / 16; v += NCOMP)
+      *reinterpret_cast<uint4*>(sm + SS_GAMT + v * 16) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async();
+  }
+  auto wt = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
+    if (*reinterpret_cast<volatile int*>(&s_abort)) return false;
+    if (mbar_wait(bar, parity, WAIT_NS)) return true;
+    *reinterpret_cast<volatile int*>(&s_abort) = 1;
+    fail(err, code);
+    return false;
+  };
+  // the same, agreed by the whole warp (shuffles and TMEM loads follow)
+  auto wtu = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
+    return __all_sync(0xffffffffu, wt(bar, parity, code));
+  };
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  grid_dep_wait();
+  const uint32_t tm = tmem_base;  // S~ at column 0, R~ at column 128
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int c = 0; c < nch; ++c) {
+        const int s = c & 1;
+        if (c >= 2 && !wt(&bar_empty[s], ((c >> 1) - 1) & 1, 41)) break;
+        uint8_t* st = sm + s * SS_STAGE;
+        const int n0 = nb + c * TC_C;
+        mbar_arrive_expect_tx(&bar_full[s], 5 * TILE);
+        tma_load_3d(st, &maps.q, &bar_full[s], 0, n0, bh);
+        tma_load_3d(st + TILE, &maps.k, &bar_full[s], 0, n0, bh);
+        tma_load_3d(st + 2 * TILE, &maps.v, &bar_full[s], 0, n0, bh);
+        tma_load_3d(st + 3 * TILE, &maps.g, &bar_full[s], 0, n0, bh);
+        tma_load_3d(st + 4 * TILE, &maps.o, &bar_full[s], 0, n0, bh);
+        ++issued;
+      }
+      for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)  // no load in flight at exit
+        mbar_wait(&bar_full[i & 1], (i >> 1) & 1, WAIT_NS);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t ones = smem_u32(sm + SS_ONES);
+      for (int c = 0; c < nch; ++c) {
+        const int s = c & 1;
+        const uint32_t q = smem_u32(sm + s * SS_STAGE), k = q + TILE, v = q + 2 * TILE, g = q + 3 * TILE;
+        const uint32_t gt = smem_u32(sm + SS_GAMT + s * TILE);
+        const uint64_t dQ = sdesc(q, 16, 1024), dK = sdesc(k, 16, 1024);
+        const uint64_t dVt = sdesc(v, ones - v, 1024), dGt = sdesc(g, gt - g, 1024);
+        if (!wt(&bar_phi[s], (c >> 1) & 1, 42)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // S~ += phi(K)^T [V | 1]
+          mma_bf16(tm, dadd(dK, kk * 2048), dadd(dVt, kk * 2048), ID_ST80, c > 0 || kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // R~ += phi(Q)^T [gt | gam]
+          mma_bf16(tm + 128, dadd(dQ, kk * 2048), dadd(dGt, kk * 2048), ID_ST80, c > 0 || kk > 0);
+        mma_commit(&bar_empty[s]);
+      }
+      mma_commit(&bar_done);  // also after an early exit: every issued MMA has finished
+    }
+  } else {
+    const int t = threadIdx.x - 64;  // 0 .. 511: vectors t and t + 512 of each tile
+    const long hb = static_cast<long>(bh) * N;
+    auto load_inv = [&](int c, float* inv) {  // 1 / den of the two rows, one chunk ahead
+      const int n0 = nb + c * TC_C;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int r = (t >> 3) + 64 * i;
+        inv[i] = (c < nch && n0 + r < ne) ? den[hb + n0 + r] : 1.f;
+      }
+    };
+    float dn_next[2];
+    load_inv(0, dn_next);
+    for (int c = 0; c < nch; ++c) {
+      const int s = c & 1;
+      const int n0 = nb + c * TC_C;
+      const int valid = min(TC_C, ne - n0);
+      uint8_t* st = sm + s * SS_STAGE;
+      const float inv[2] = {1.f / dn_next[0], 1.f / dn_next[1]};
+      load_inv(c + 1, dn_next);
+      if (wtu(&bar_full[s], (c >> 1) & 1, 43)) {
+        uint4 x[3][2], o[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int v = t + i * NCOMP;
+          x[0][i] = *reinterpret_cast<const uint4*>(st + v * 16);             // Q
+          x[1][i] = *reinterpret_cast<const uint4*>(st + TILE + v * 16);      // K
+          x[2][i] = *reinterpret_cast<const uint4*>(st + 3 * TILE + v * 16);  // dout
+          o[i] = *reinterpret_cast<const uint4*>(st + 4 * TILE + v * 16);     // out
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int v = t + i * NCOMP, r = v >> 3, lc = (v & 7) ^ (r & 7);
+          const bool rv = r < valid;
+          const long gofs = (hb + n0 + r) * 64 + lc * 8;
+          // phi(Q), phi(K): in place and to the workspace
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const uint4 f = rv ? phi_vec(x[k][i]) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(st + k * TILE + v * 16) = f;
+            if (rv) *reinterpret_cast<uint4*>((k == 0 ? fq_out : fk_out) + gofs) = f;
+          }
+          // gt = dout / den in place and to the workspace; gam = -(gt . out)
+          float dot = 0.f;
+          uint4 gv = make_uint4(0u, 0u, 0u, 0u);
+          if (rv) {
+            const uint32_t gw[4] = {x[2][i].x, x[2][i].y, x[2][i].z, x[2][i].w};
+            const uint32_t ow[4] = {o[i].x, o[i].y, o[i].z, o[i].w};
+            uint32_t rw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float g0 = __uint_as_float(gw[j] << 16) * inv[i];
+              const float g1 = __uint_as_float(gw[j] & 0xffff0000u) * inv[i];
+              dot = fmaf(g0, __uint_as_float(ow[j] << 16), dot);
+              dot = fmaf(g1, __uint_as_float(ow[j] & 0xffff0000u), dot);
+              rw[j] = pack_bf16(g0, g1);
+            }
+            gv = make_uint4(rw[0], rw[1], rw[2], rw[3]);
+            *reinterpret_cast<uint4*>(gt_out + gofs) = gv;
+          }
+          *reinterpret_cast<uint4*>(st + 3 * TILE + v * 16) = gv;
+          dot += __shfl_xor_sync(0xffffffffu, dot, 1);  // the 8 vectors of row r
+          dot += __shfl_xor_sync(0xffffffffu, dot, 2);  // sit in 8 consecutive lanes
+          dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+          if ((t & 7) == 0) {
+            const float gm = rv ? -dot : 0.f;
+            *reinterpret_cast<bf16*>(sm + SS_GAMT + s * TILE + r * 128 + ((r & 7) << 4)) =
+                __float2bfloat16_rn(gm);
+            if (rv) gam[hb + n0 + r] = gm;
+          }
+        }
+      }
+      fence_proxy_async();
+      mbar_arrive(&bar_phi[s]);
+    }
+    // the partial states [S | z | R | r]: TMEM -> shared memory (stage 0) -> one bulk copy
+    const int qd = warp & 3, wq = (warp - 2) >> 2;  // lane quarter, warp within it
+    const uint32_t lq = static_cast<uint32_t>(32 * qd) << 16;
+    const int srow = 16 * qd + lane;
+    float* stg = reinterpret_cast<float*>(sm);
+    if (wtu(&bar_done, 0, 44)) {
+      tc_fence_after();
+      for (int blk = wq; blk < 10; blk += 4) {  // 16-column blocks: S~ 0-4, R~ 5-9
+        const int which = blk / 5, col = (blk % 5) * 16;
+        float sv[16];
+        tmem_ldn<1>(tm + which * 128 + lq + col, sv);
+        float* base = stg + which * (DM + 64);
+        if (lane < 16) {
+          if (col < 64) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+              *reinterpret_cast<float4*>(base + srow * 64 + col + j) =
+                  make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+          } else {
+            base[DM + srow] = sv[0];  // the vector column
+          }
+        }
+      }
+    }
+    fence_proxy_async();
+    compute_sync();
+    if (t == 0 && !*reinterpret_cast<volatile int*>(&s_abort)) {
+      bulk_store(rec + (static_cast<long>(bh) * nsub + p) * REC, stg, REC * 4);
+      bulk_commit();
+      bulk_wait_all();
+    }
+  }
+  if (warp == 1 && lane == 0) mbar_wait(&bar_done, 0, WAIT_NS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tm, 256);
 }
 
 struct BwdPlan {
@@ -578,21 +721,26 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
       !make_bf16_map(&m.dq, dq, BH, s.N) || !make_bf16_map(&m.dk, dk, BH, s.N) ||
       !make_bf16_map(&m.dv, dv, BH, s.N))
     return cudaErrorInvalidValue;
+  StateMaps smap;
+  smap.q = m.q;
+  smap.k = m.k;
+  smap.v = m.v;
+  smap.g = m.g;
+  smap.o = m.o;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_tc_bwd<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                S_SMEM)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(k_tc_bwd_state, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SS_SMEM)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(k_tc_bwd<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if ((e = cudaFuncSetAttribute(k_tc_bwd_main, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 M_SMEM)) != cudaSuccess)
     return e;
   if ((e = cudaMemsetAsync(w.err, 0, sizeof(int), st)) != cudaSuccess) return e;
-  if ((e = launch_pdl(k_tc_bwd<0>, dim3(pl.nsub, BH, 1), dim3(NTHR), S_SMEM, st, m, den, w.rec,
-                      w.gam, w.gt, w.fq, w.fk, s.N, pl.sub_len, pl.nsub, pl.subs, w.err)) !=
-      cudaSuccess)
+  if ((e = launch_pdl(k_tc_bwd_state, dim3(pl.nsub, BH), dim3(NTHR), SS_SMEM, st, smap, den, w.gam,
+                      w.gt, w.fq, w.fk, w.rec, s.N, pl.sub_len, pl.nsub, w.err)) != cudaSuccess)
     return e;
-  if ((e = launch_pdl(k_tc_bwd<1>, dim3(pl.main.nseg, BH, 2), dim3(NTHR), M_SMEM, st, m, den,
-                      w.rec, w.gam, w.gt, w.fq, w.fk, s.N, pl.main.seg_len, pl.nsub, pl.subs,
-                      w.err)) != cudaSuccess)
+  if ((e = launch_pdl(k_tc_bwd_main, dim3(pl.main.nseg, BH, 2), dim3(NTHR), M_SMEM, st, m,
+                      static_cast<const float*>(w.rec), static_cast<const float*>(w.gam), s.N,
+                      pl.main.seg_len, pl.nsub, pl.subs, w.err)) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }
