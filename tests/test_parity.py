@@ -124,6 +124,13 @@ def check_noncausal(la, dev, B, H, N, D, M, dtype, seed, len_range):
     (4, 2, 300, 64, 64, "f32", (0, 300)),
     (3, 2, 513, 64, 32, "bf16", (200, 513)),
     (2, 1, 64, 16, 16, "f32", (64, 64)),
+    # D = M = 64: several 128-token chunks and segments, ragged tails,
+    # empty sequences, no lengths, one token, forty partial records
+    (2, 3, 1000, 64, 64, "bf16", (0, 1000)),
+    (1, 2, 777, 64, 64, "f32", None),
+    (1, 1, 1, 64, 64, "f32", None),
+    (5, 1, 2500, 64, 64, "f32", (1, 2500)),
+    (100, 10, 100, 64, 64, "f32", (0, 100)),  # enough heads for one CTA per head
 ])
 def test_noncausal_small(cuda, linattn, B, H, N, D, M, dtype, lr):
     check_noncausal(linattn, cuda, B, H, N, D, M, dtype, 2000 + N, lr)
