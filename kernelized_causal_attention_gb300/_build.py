@@ -39,9 +39,21 @@ def _deps():
         + [os.path.join(os.path.dirname(HERE), "include", "linattn.h"), __file__]
 
 
+MANIFEST = os.path.join(LIBDIR, "sources.txt")
+
+
+def _manifest() -> str:
+    return "\n".join(os.path.basename(f) for f in sources())
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    """The library exists, was built from the current set of sources (an
+    added or removed file forces a rebuild) and is newer than every input."""
+    if not os.path.exists(LIB) or not os.path.exists(MANIFEST):
         return False
+    with open(MANIFEST) as f:
+        if f.read() != _manifest():
+            return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
@@ -71,6 +83,8 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(MANIFEST, "w") as f:
+        f.write(_manifest())
     return LIB
 
 

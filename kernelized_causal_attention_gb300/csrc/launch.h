@@ -88,16 +88,16 @@ cudaError_t noncausal64_bwd(const void* q, const void* k, const void* v, const i
                             const void* out, const float* den, const float* S, const float* Z,
                             const void* dout, void* dq, void* dk, void* dv, float* ws,
                             const Shape& s, cudaStream_t st);
-// Non-causal path for fp32, D = M = 64: one cluster launch per direction, no
-// workspace.
-int noncausal_cluster_nseg(int BH, int N);
-cudaError_t noncausal_cluster_fwd(const float* q, const float* k, const float* v,
-                                  const int* lengths, float* out, float* den, float* S, float* Z,
-                                  const Shape& s, cudaStream_t st);
-cudaError_t noncausal_cluster_bwd(const float* q, const float* k, const float* v,
-                                  const int* lengths, const float* out, const float* den,
-                                  const float* S, const float* Z, const float* dout, float* dq,
-                                  float* dk, float* dv, const Shape& s, cudaStream_t st);
+// Non-causal path for fp32, D = M = 64, on the tensor cores: one cluster
+// launch per direction, no workspace.
+int noncausal_tc_nseg(int BH, int N);
+cudaError_t noncausal_tc_fwd(const float* q, const float* k, const float* v, const int* lengths,
+                             float* out, float* den, float* S, float* Z, const Shape& s,
+                             cudaStream_t st);
+cudaError_t noncausal_tc_bwd(const float* q, const float* k, const float* v, const int* lengths,
+                             const float* out, const float* den, const float* S, const float* Z,
+                             const float* dout, float* dq, float* dk, float* dv, const Shape& s,
+                             cudaStream_t st);
 cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* y,
                         const Shape& s, cudaStream_t st);
 

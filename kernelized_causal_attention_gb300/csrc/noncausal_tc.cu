@@ -1,0 +1,875 @@
+// Non-causal path for fp32 inputs with D = M = 64 on the tensor cores.
+//
+// Method: "Linear Attention/zh", kernel reformulation (one shared S, Z per
+// (b, h)) and eq. 13-15 of "Transformers are RNNs" (part 2/3) with full sums
+// over the valid rows i < L:
+//   S = sum_j phi(K_j) V_j^T,  Z = sum_j phi(K_j),
+//   out_i = phi(Q_i)^T S / den_i,  den_i = phi(Q_i)^T Z,
+//   gt_i = dout_i / den_i,  gam_i = -(gt_i . out_i),
+//   R = sum_i phi(Q_i) gt_i^T,  r = sum_i gam_i phi(Q_i),
+//   dq_i = (S gt_i + gam_i Z) * phi'(Q_i),
+//   dk_j = (R V_j + r) * phi'(K_j),  dv_j = R^T phi(K_j).
+// Rows i >= L are padding: they enter no sum and are written as zero.
+//
+// fp32 accuracy from bf16 products.  Every fp32 operand x is split exactly
+// into x_hi = bf16(x) and x_lo = bf16(x - x_hi), so |x - x_hi - x_lo| <=
+// 2^-18 |x|, and a product is taken as a_hi b_hi + a_hi b_lo + a_lo b_hi
+// (the dropped a_lo b_lo is below 2^-18 |a b|), accumulated in fp32 in
+// tensor memory.  Two instructions per 16-deep step carry the three
+// products: A_hi times the N = 128 operand [B_hi | B_lo] (two 64-wide halves
+// of the accumulator) and A_lo times B_hi into the first half; the epilogue
+// adds the halves.
+//
+// Layout of the work.  One thread-block cluster of nseg CTAs per (b, h); the
+// valid rows are cut into 128-token chunks and every CTA takes an equal run.
+//  forward   phase 1: S~ += phi(K)^T [V_hi | V_lo]    (M = 64, state form)
+//            cluster sum of the partial S, Z through distributed shared memory
+//            phase 2: O~ = phi(Q) [S_hi | S_lo]        (M = 128, token form)
+//  backward  phase 1: R~ += phi(Q)^T [gt_hi | gt_lo], dQ~ = gt [S_hi; S_lo]^T
+//            cluster sum of the partial R, r
+//            phase 2: dK~ = V [R_hi; R_lo]^T, dV~ = phi(K) [R_hi | R_lo]
+// The CUDA cores load each chunk (prefetched into registers one chunk
+// ahead), apply phi, 1 / den, gam and the zeroing of invalid rows, split and
+// write the swizzled operand tiles (two buffers), and run the epilogue of
+// chunk c - 1 while the tensor cores work on chunk c.  den, gam, Z and r are
+// plain fp32 dot products on the CUDA cores.
+//
+// gam without out.  out_i = S^T phi(Q_i) / den_i, so
+//   gt_i . out_i = phi(Q_i) . (S gt_i) / den_i,
+// and S gt_i is the accumulator dQ~ already holds for row i: the backward
+// takes gam from it in the dq epilogue and never reads out.
+#include "common.cuh"
+#include "launch.h"
+#include "tc_chunk.cuh"
+
+namespace la {
+namespace {
+
+using namespace tcc;
+
+constexpr int CH = 128;              // tokens per chunk
+constexpr int NTX = 512;             // threads per CTA
+constexpr int NU = CH * 8 / NTX;     // 8-column units of a chunk per thread
+constexpr int NCG = NTX / 128;       // column groups of a 128-lane accumulator readout
+constexpr int CW = 64 / NCG;         // columns per group
+constexpr int BT = CH * 128;         // bytes of a [128][64] bf16 tile
+constexpr int ST = 64 * 128;         // bytes of a [64][64] bf16 tile
+constexpr int BUF = 4 * BT;          // one operand buffer: two tensors, hi and lo each
+constexpr int PREC = 64 * 64 + 64;   // floats of a partial-state record
+constexpr int kMaxSeg = 8;           // CTAs per cluster (portable limit)
+
+// shared memory, bytes from a 1024-aligned base
+constexpr int O_BUF = 0;                  // two operand buffers
+constexpr int O_ST = 2 * BUF;             // state tile hi [64][64], lo right after it
+constexpr int O_P = O_ST + 2 * ST;        // this CTA's partial record (fp32)
+constexpr int O_MISC = O_P + 4 * PREC;    // fp32: per-row [2][128] x 2, vector [64], sums [warps][64], [4][128]
+constexpr int N_MISC = 4 * CH + 64 + (NTX / 32) * 64 + NCG * CH;
+constexpr int O_BAR = O_MISC + 4 * N_MISC;  // mbarriers: MMA done per buffer, final drain; TMEM address
+constexpr int SMEM_TC = O_BAR + 64 + 1024;  // + alignment slack
+
+// TMEM columns
+constexpr uint32_t T_STATE = 0;      // the M = 64 state accumulator (128 columns)
+constexpr uint32_t T_TOK = 128;      // token-form accumulators of phase 1, 128 per buffer
+
+// ------------------------------------------------------------- cluster
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// -------------------------------------------------------------- helpers
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+__device__ __forceinline__ uint32_t bits(__nv_bfloat162 h) {
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// (x0, x1) -> hi and lo bf16 pairs with x = hi + lo to 2^-18 relative.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  hi = bits(h);
+  lo = bits(__floats2bfloat162_rn(x0 - hf.x, x1 - hf.y));
+}
+
+// Columns 8 c8 .. 8 c8 + 7 of row `row` into the swizzled hi and lo tiles.
+__device__ __forceinline__ void put_split8(uint8_t* hi, uint8_t* lo, int row, int c8,
+                                           const float* x) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) split2(x[2 * j], x[2 * j + 1], h[j], l[j]);
+  const uint32_t off = static_cast<uint32_t>(row) * 128u + ((static_cast<uint32_t>(c8) ^ (row & 7u)) << 4);
+  *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Four values (columns col .. col + 3, col a multiple of 4) of row `row`.
+__device__ __forceinline__ void put_split4(uint8_t* hi, uint8_t* lo, int row, int col, float4 x) {
+  uint32_t h0, h1, l0, l1;
+  split2(x.x, x.y, h0, l0);
+  split2(x.z, x.w, h1, l1);
+  const uint32_t off = sw128_offset(row, col);
+  *reinterpret_cast<uint2*>(hi + off) = make_uint2(h0, h1);
+  *reinterpret_cast<uint2*>(lo + off) = make_uint2(l0, l1);
+}
+
+// Columns col0 .. col0 + NC - 1 (NC a multiple of 8) of row `row` as
+// hi + lo (the operand value to 2^-18 relative).
+template <int NC>
+__device__ __forceinline__ void get_row(const uint8_t* hi, const uint8_t* lo, int row, int col0,
+                                       float* x) {
+#pragma unroll
+  for (int m = 0; m < NC / 8; ++m) {
+    const uint32_t off = sw128_offset(row, col0 + 8 * m);
+    const uint4 a = *reinterpret_cast<const uint4*>(hi + off);
+    const uint4 b = *reinterpret_cast<const uint4*>(lo + off);
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[8 * m + 2 * j] = __uint_as_float(wa[j] << 16) + __uint_as_float(wb[j] << 16);
+      x[8 * m + 2 * j + 1] = __uint_as_float(wa[j] & 0xffff0000u) + __uint_as_float(wb[j] & 0xffff0000u);
+    }
+  }
+}
+
+// The CTA's valid rows [r0, r1) in nch chunks, and padded rows [z0, z1).
+struct Rows {
+  long r0, r1, z0, z1;
+  int nch;
+};
+
+__device__ __forceinline__ Rows my_rows(const int* lengths, int b, int N, int p, int nseg) {
+  long L = N;
+  if (lengths != nullptr) {
+    const int l = lengths[b];
+    L = l < 0 ? 0 : (l > N ? N : l);
+  }
+  const long nchv = (L + CH - 1) / CH, per = (nchv + nseg - 1) / nseg;
+  const long c0 = min(nchv, p * per), c1 = min(nchv, c0 + per);
+  Rows w;
+  w.r0 = c0 * CH;
+  w.r1 = min(c1 * CH, L);
+  w.nch = static_cast<int>(c1 - c0);
+  const long zs = (N - L + nseg - 1) / nseg;
+  w.z0 = min(static_cast<long>(N), L + p * zs);
+  w.z1 = min(static_cast<long>(N), w.z0 + zs);
+  return w;
+}
+
+// A thread's share of a chunk: units i < NU, row (t >> 3) + (NTX / 8) i,
+// columns 8 (t & 7) .. + 7 (the 8 lanes of a row are consecutive).
+__device__ __forceinline__ int unit_row(int i) { return (threadIdx.x >> 3) + (NTX / 8) * i; }
+__device__ __forceinline__ int unit_c8() { return threadIdx.x & 7; }
+
+// The thread's share of rows n0 .. n0 + 127 of x ([*][64] fp32); rows at or
+// past ne read as 0.
+__device__ __forceinline__ void fetch(float4 (&r)[2 * NU], const float* x, long n0, long ne) {
+#pragma unroll
+  for (int i = 0; i < NU; ++i) {
+    const long row = n0 + unit_row(i);
+    if (row < ne) {
+      const float* p = x + row * 64 + 8 * unit_c8();
+      r[2 * i] = ld4(p);
+      r[2 * i + 1] = ld4(p + 4);
+    } else {
+      r[2 * i] = r[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
+// The backward's phase-1 share of a chunk: q, dout and den.
+__device__ __forceinline__ void fetch_bwd1(float4 (&ra)[2 * NU], float4 (&rb)[2 * NU],
+                                           float (&rd)[NU], const float* qh, const float* gh,
+                                           const float* dh, long n0, long ne) {
+  fetch(ra, qh, n0, ne);
+  fetch(rb, gh, n0, ne);
+#pragma unroll
+  for (int i = 0; i < NU; ++i) {
+    const long row = n0 + unit_row(i);
+    rd[i] = row < ne ? dh[row] : 1.f;
+  }
+}
+
+__device__ __forceinline__ void unpack8(const float4& a, const float4& b, float* x) {
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ float sum8(float x) {  // over the 8 lanes of a row
+  x += __shfl_xor_sync(0xffffffffu, x, 4);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x;
+}
+
+// ------------------------------------------------------------------ MMAs
+// State form over one chunk: D (M = 64, N = 128) (+)= A^T [B_hi | B_lo]
+// and D[:, 0:64] += A_lo^T B_hi, with A and B [128 tokens][64] tiles read
+// MN-major (16 tokens = 2048 bytes per step).
+__device__ __forceinline__ void mma_state(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi,
+                                          uint32_t b_lo, bool first) {
+  constexpr uint32_t I128 = idesc_bf16(64, 128, true, true);
+  constexpr uint32_t I64 = idesc_bf16(64, 64, true, true);
+  const uint64_t dah = sdesc(a_hi, 16, 1024), dal = sdesc(a_lo, 16, 1024);
+  const uint64_t db2 = sdesc(b_hi, b_lo - b_hi, 1024), db1 = sdesc(b_hi, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    mma_bf16(d, dadd(dah, 2048 * kk), dadd(db2, 2048 * kk), I128, !first || kk > 0);
+    mma_bf16(d, dadd(dal, 2048 * kk), dadd(db1, 2048 * kk), I64, 1);
+  }
+}
+
+// Token form over one chunk: D (M = 128 tokens, N = 128) = A_hi [B_hi | B_lo]
+// and D[:, 0:64] += A_lo B_hi, A a K-major [128][64] tile, B the state tile
+// pair at b (lo at b + ST): MN-major ([K = 64 rows][N]) when b_mn, else
+// K-major ([N rows][K], hi rows then lo rows).
+__device__ __forceinline__ void mma_tok(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b,
+                                        bool b_mn) {
+  const uint64_t dah = sdesc(a_hi, 16, 1024), dal = sdesc(a_lo, 16, 1024);
+  if (b_mn) {
+    constexpr uint32_t I128 = idesc_bf16(128, 128, false, true);
+    constexpr uint32_t I64 = idesc_bf16(128, 64, false, true);
+    const uint64_t db2 = sdesc(b, ST, 1024), db1 = sdesc(b, 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      mma_bf16(d, dadd(dah, 32 * kk), dadd(db2, 2048 * kk), I128, kk > 0);
+      mma_bf16(d, dadd(dal, 32 * kk), dadd(db1, 2048 * kk), I64, 1);
+    }
+  } else {
+    constexpr uint32_t I128 = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t I64 = idesc_bf16(128, 64, false, false);
+    const uint64_t db = sdesc(b, 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      mma_bf16(d, dadd(dah, 32 * kk), dadd(db, 32 * kk), I128, kk > 0);
+      mma_bf16(d, dadd(dal, 32 * kk), dadd(db, 32 * kk), I64, 1);
+    }
+  }
+}
+
+// ------------------------------------------------------ shared pieces
+struct Ctx {
+  uint8_t* sm;
+  uint64_t* bar;  // [0], [1]: MMA of buffer 0 / 1 done; [2]: final drain
+  int* abort;
+  uint32_t tm;
+};
+
+// Waits for the MMAs of global chunk g; agreed by the whole warp (the TMEM
+// loads that follow are warp-collective).  Gives up after WAIT_NS and sets
+// the CTA's abort flag, after which every wait fails at once.
+__device__ __forceinline__ bool wait_chunk(const Ctx& x, uint32_t g) {
+  bool ok = false;
+  if (!*reinterpret_cast<volatile int*>(x.abort)) {
+    ok = mbar_wait(&x.bar[g & 1], (g >> 1) & 1, WAIT_NS);
+    if (!ok) *reinterpret_cast<volatile int*>(x.abort) = 1;
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
+// CW columns (col .. col + CW - 1) of the thread's TMEM lane from the two
+// halves of a 128-column accumulator (col and col + 64); one wait.
+__device__ __forceinline__ void ld_halves(uint32_t taddr, float* a, float* b) {
+#pragma unroll
+  for (int j = 0; j < CW; j += 16) {
+    tmem_ld16(taddr + j, a + j);
+    tmem_ld16(taddr + 64 + j, b + j);
+  }
+  tmem_ld_wait();
+}
+
+// Readout of the M = 64 state accumulator: the thread's CW columns
+// (CW (warp >> 2) ..) of row 16 (warp & 3) + lane (lanes < 16 hold rows),
+// halves added.
+__device__ __forceinline__ void state_readout(const Ctx& x, bool ok, float* P) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, qd = warp & 3, cg = warp >> 2;
+  float a[CW], b[CW];
+  if (ok) {
+    ld_halves(x.tm + T_STATE + ((32u * qd) << 16) + CW * cg, a, b);
+  } else {
+#pragma unroll
+    for (int j = 0; j < CW; ++j) a[j] = b[j] = 0.f;
+  }
+  if (lane < 16) {
+    float* dst = P + (16 * qd + lane) * 64 + CW * cg;
+#pragma unroll
+    for (int j = 0; j < CW; j += 4)
+      st4(dst + j, make_float4(a[j] + b[j], a[j + 1] + b[j + 1], a[j + 2] + b[j + 2], a[j + 3] + b[j + 3]));
+  }
+}
+
+// Column sums of the thread's 8 columns over all threads -> P[4096 + d].
+__device__ __forceinline__ void colsum_to_record(float (&cs)[8], float* scol, float* P) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    cs[j] += __shfl_xor_sync(0xffffffffu, cs[j], 8);
+    cs[j] += __shfl_xor_sync(0xffffffffu, cs[j], 16);
+  }
+  if (lane < 8)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) scol[warp * 64 + 8 * lane + j] = cs[j];
+  __syncthreads();
+  if (threadIdx.x < 64) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < NTX / 32; ++w) s += scol[w * 64 + threadIdx.x];
+    P[64 * 64 + threadIdx.x] = s;
+  }
+}
+
+constexpr int NPC = 1024 / NTX;  // matrix pieces per thread in the cluster sum
+
+// Sum over the cluster of the records P: thread t gets matrix pieces
+// t + NTX i (i < NPC; piece e = row e >> 4, columns 4 (e & 15) ..) and, for
+// t < 16, vector piece t.  Four peers' loads are in flight at a time.
+__device__ __forceinline__ void cluster_sum(const float* P, int nseg, float4 (&m)[NPC], float4& vec) {
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(P));
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < NPC; ++i) m[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  vec = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q0 = 0; q0 < nseg; q0 += 4) {
+    float4 part[4][NPC + 1];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (q0 + u < nseg) {
+        const uint32_t a = map_rank(base, static_cast<uint32_t>(q0 + u));
+#pragma unroll
+        for (int i = 0; i < NPC; ++i) part[u][i] = ld_cluster4(a + 16u * (t + NTX * i));
+        part[u][NPC] = t < 16 ? ld_cluster4(a + 16u * (1024 + t)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+#pragma unroll
+        for (int i = 0; i <= NPC; ++i) part[u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+      for (int i = 0; i < NPC; ++i) m[i] = add4(m[i], part[u][i]);
+      vec = add4(vec, part[u][NPC]);
+    }
+  }
+}
+
+// Setup shared by both kernels: barriers, abort flag, TMEM.
+__device__ __forceinline__ Ctx setup(uint8_t* smraw, int* s_abort) {
+  Ctx x;
+  x.sm = align1024(smraw);
+  x.bar = reinterpret_cast<uint64_t*>(x.sm + O_BAR);
+  x.abort = s_abort;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(x.sm + O_BAR + 32);
+  if (threadIdx.x == 0) {
+    mbar_init(&x.bar[0], 1);
+    mbar_init(&x.bar[1], 1);
+    mbar_init(&x.bar[2], 1);
+    fence_barrier_init();
+    *s_abort = 0;
+  }
+  if ((threadIdx.x >> 5) == 0) tmem_alloc(slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  x.tm = *slot;
+  return x;
+}
+
+// Teardown: no MMA in flight, no peer reading this CTA's record, TMEM freed.
+__device__ __forceinline__ void teardown(const Ctx& x) {
+  if (threadIdx.x == 0) {
+    mma_commit(&x.bar[2]);
+    mbar_wait(&x.bar[2], 0, WAIT_NS);
+  }
+  cluster_wait();  // matches the arrive after the cluster sum
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if ((threadIdx.x >> 5) == 0) tmem_dealloc(x.tm, 512);
+}
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- forward
+__global__ void __launch_bounds__(NTX, 1)
+    k_nc_fwd_tc(const float* __restrict__ q, const float* __restrict__ k,
+                const float* __restrict__ v, const int* __restrict__ lengths,
+                float* __restrict__ out, float* __restrict__ den, float* __restrict__ S,
+                float* __restrict__ Z, int N, int H, int nseg) {
+  extern __shared__ uint8_t smraw[];
+  __shared__ int s_abort;
+  const Ctx x = setup(smraw, &s_abort);
+  uint8_t* sm = x.sm;
+  float* P = reinterpret_cast<float*>(sm + O_P);
+  float* sden = reinterpret_cast<float*>(sm + O_MISC);  // [2][128]
+  float* sz = sden + 2 * CH;                             // Z [64]
+  float* scol = sz + 64;                                 // [warps][64]
+  uint8_t* SH = sm + O_ST;                               // S hi | lo
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, qd = warp & 3, cg = warp >> 2;
+  const int p = static_cast<int>(cluster_rank()), bh = blockIdx.x / nseg;
+  const Rows w = my_rows(lengths, bh / H, N, p, nseg);
+  const long hq = static_cast<long>(bh) * N * 64, hn = static_cast<long>(bh) * N;
+  const int c8 = unit_c8();
+
+  uint32_t g = 0;  // chunks issued so far: buffer g & 1, barrier parity (g >> 1) & 1
+  float4 ra[2 * NU], rb[2 * NU];
+  if (w.nch > 0) {
+    fetch(ra, k + hq, w.r0, w.r1);
+    fetch(rb, v + hq, w.r0, w.r1);
+  }
+
+  // ---- phase 1: partial S~ and Z
+  float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int c = 0; c < w.nch; ++c, ++g) {
+    uint8_t* B0 = sm + O_BUF + (g & 1) * BUF;  // K hi, K lo, V hi, V lo
+    const long n0 = w.r0 + static_cast<long>(c) * CH;
+    const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
+#pragma unroll
+    for (int i = 0; i < NU; ++i) {
+      const int row = unit_row(i);
+      float a[8], b[8];
+      unpack8(ra[2 * i], ra[2 * i + 1], a);
+      unpack8(rb[2 * i], rb[2 * i + 1], b);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        a[j] = row < nv ? phi(a[j]) : 0.f;
+        cs[j] += a[j];
+      }
+      put_split8(B0, B0 + BT, row, c8, a);
+      put_split8(B0 + 2 * BT, B0 + 3 * BT, row, c8, b);
+    }
+    if (c + 1 < w.nch) {
+      fetch(ra, k + hq, n0 + CH, w.r1);
+      fetch(rb, v + hq, n0 + CH, w.r1);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (t == 0 && !s_abort) {
+      tc_fence_after();
+      const uint32_t a0 = saddr(B0);
+      mma_state(x.tm + T_STATE, a0, a0 + BT, a0 + 2 * BT, a0 + 3 * BT, c == 0);
+      mma_commit(&x.bar[g & 1]);
+    }
+    if (c > 0) wait_chunk(x, g - 1);  // frees the other buffer
+  }
+  {
+    const bool ok = w.nch > 0 && wait_chunk(x, g - 1);
+    tc_fence_after();
+    state_readout(x, ok, P);
+  }
+  colsum_to_record(cs, scol, P);
+  tc_fence_before();
+  cluster_arrive();
+  // padded rows, while the slower CTAs of the cluster finish phase 1
+  for (long e = w.z0 * 16 + t; e < w.z1 * 16; e += NTX) st4(out + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
+  if (den != nullptr)
+    for (long i = w.z0 + t; i < w.z1; i += NTX) den[hn + i] = 0.f;
+  cluster_wait();  // every record complete
+
+  // ---- phase 2: out = phi(Q) S / den
+  if (w.nch > 0) fetch(ra, q + hq, w.r0, w.r1);
+  {
+    float4 m[NPC], zv;
+    cluster_sum(P, nseg, m, zv);
+#pragma unroll
+    for (int i = 0; i < NPC; ++i) {
+      const int e = t + NTX * i;
+      put_split4(SH, SH + ST, e >> 4, 4 * (e & 15), m[i]);
+      if (p == 0) st4(S + static_cast<long>(bh) * 4096 + 4 * e, m[i]);
+    }
+    if (t < 16) {
+      st4(sz + 4 * t, zv);
+      if (p == 0) st4(Z + static_cast<long>(bh) * 64 + 4 * t, zv);
+    }
+  }
+  cluster_arrive();  // this CTA no longer reads the others' records
+  fence_proxy_async();
+  __syncthreads();
+  float zc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) zc[j] = sz[8 * c8 + j];
+  const uint32_t tok0 = x.tm + T_TOK;
+  for (int c = 0; c <= w.nch; ++c) {
+    if (c < w.nch) {
+      uint8_t* B0 = sm + O_BUF + (g & 1) * BUF;  // Q hi, Q lo
+      const long n0 = w.r0 + static_cast<long>(c) * CH;
+      const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
+#pragma unroll
+      for (int i = 0; i < NU; ++i) {
+        const int row = unit_row(i);
+        float a[8];
+        unpack8(ra[2 * i], ra[2 * i + 1], a);
+        float dp = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          a[j] = row < nv ? phi(a[j]) : 0.f;
+          dp = fmaf(a[j], zc[j], dp);
+        }
+        dp = sum8(dp);
+        if (c8 == 0) {
+          sden[(g & 1) * CH + row] = dp;
+          if (den != nullptr && row < nv) den[hn + n0 + row] = dp;
+        }
+        put_split8(B0, B0 + BT, row, c8, a);
+      }
+      if (c + 1 < w.nch) fetch(ra, q + hq, n0 + CH, w.r1);
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+      if (t == 0 && !s_abort) {
+        tc_fence_after();
+        const uint32_t a0 = saddr(B0);
+        mma_tok(tok0 + 128 * (g & 1), a0, a0 + BT, saddr(SH), true);
+        mma_commit(&x.bar[g & 1]);
+      }
+      ++g;
+    }
+    if (c > 0) {  // epilogue of chunk c - 1 (global chunk g - 1 or g - 2)
+      const uint32_t ge = c < w.nch ? g - 2 : g - 1;
+      const bool ok = wait_chunk(x, ge);
+      tc_fence_after();
+      if (ok) {
+        const long n0 = w.r0 + static_cast<long>(c - 1) * CH;
+        const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
+        const int row = 32 * qd + lane;
+        float a[CW], b[CW];
+        ld_halves(tok0 + 128 * (ge & 1) + ((32u * qd) << 16) + CW * cg, a, b);
+        if (row < nv) {
+          const float inv = 1.f / sden[(ge & 1) * CH + row];
+          float* dst = out + hq + (n0 + row) * 64 + CW * cg;
+#pragma unroll
+          for (int j = 0; j < CW; j += 4)
+            st4(dst + j, make_float4((a[j] + b[j]) * inv, (a[j + 1] + b[j + 1]) * inv,
+                                     (a[j + 2] + b[j + 2]) * inv, (a[j + 3] + b[j + 3]) * inv));
+        }
+      }
+      tc_fence_before();
+      __syncthreads();  // the next transform rewrites what this epilogue read
+    }
+  }
+  teardown(x);
+}
+
+// --------------------------------------------------------------- backward
+__global__ void __launch_bounds__(NTX, 1)
+    k_nc_bwd_tc(const float* __restrict__ q, const float* __restrict__ k,
+                const float* __restrict__ v, const int* __restrict__ lengths,
+                const float* __restrict__ den, const float* __restrict__ S,
+                const float* __restrict__ Z,
+                const float* __restrict__ gr, float* __restrict__ dq, float* __restrict__ dk,
+                float* __restrict__ dv, int N, int H, int nseg) {
+  extern __shared__ uint8_t smraw[];
+  __shared__ int s_abort;
+  const Ctx x = setup(smraw, &s_abort);
+  uint8_t* sm = x.sm;
+  float* P = reinterpret_cast<float*>(sm + O_P);
+  float* sinv = reinterpret_cast<float*>(sm + O_MISC);  // 1 / den [2][128]
+  float* sz = sinv + 4 * CH;                             // phase 1: Z; phase 2: r
+  float* scol = sz + 64;                                 // [warps][64]
+  float* spart = scol + (NTX / 32) * 64;                 // [NCG][128]
+  uint8_t* SH = sm + O_ST;  // phase 1: S hi | lo; phase 2: R hi | lo
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, qd = warp & 3, cg = warp >> 2;
+  const int p = static_cast<int>(cluster_rank()), bh = blockIdx.x / nseg;
+  const Rows w = my_rows(lengths, bh / H, N, p, nseg);
+  const long hq = static_cast<long>(bh) * N * 64, hn = static_cast<long>(bh) * N;
+  const int c8 = unit_c8();
+
+  uint32_t g = 0;
+  float4 ra[2 * NU], rb[2 * NU];
+  float rd[NU];
+  if (w.nch > 0) fetch_bwd1(ra, rb, rd, q + hq, gr + hq, den + hn, w.r0, w.r1);
+  // S (the forward's state) as hi | lo operand tiles; Z
+#pragma unroll
+  for (int i = 0; i < NPC; ++i) {
+    const int e = t + NTX * i;
+    put_split4(SH, SH + ST, e >> 4, 4 * (e & 15), ld4(S + static_cast<long>(bh) * 4096 + 4 * e));
+  }
+  if (t < 64) sz[t] = Z[static_cast<long>(bh) * 64 + t];
+  fence_proxy_async();
+  __syncthreads();  // S tiles and Z in place
+
+  // ---- phase 1: gt, dq, gam and partial R~, r
+  float rp[CW];  // r over the thread's epilogue rows, columns CW cg ..
+#pragma unroll
+  for (int j = 0; j < CW; ++j) rp[j] = 0.f;
+  const uint32_t tok0 = x.tm + T_TOK;
+  for (int c = 0; c <= w.nch; ++c) {
+    if (c < w.nch) {
+      uint8_t* B0 = sm + O_BUF + (g & 1) * BUF;  // Q hi, Q lo, gt hi, gt lo
+      const long n0 = w.r0 + static_cast<long>(c) * CH;
+      const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
+#pragma unroll
+      for (int i = 0; i < NU; ++i) {
+        const int row = unit_row(i);
+        const bool ok = row < nv;
+        float a[8], b[8];
+        unpack8(ra[2 * i], ra[2 * i + 1], a);
+        unpack8(rb[2 * i], rb[2 * i + 1], b);
+        const float inv = ok ? 1.f / rd[i] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          a[j] = ok ? phi(a[j]) : 0.f;
+          b[j] *= inv;
+        }
+        if (c8 == 0) sinv[(g & 1) * CH + row] = inv;
+        put_split8(B0, B0 + BT, row, c8, a);
+        put_split8(B0 + 2 * BT, B0 + 3 * BT, row, c8, b);
+      }
+      if (c + 1 < w.nch) fetch_bwd1(ra, rb, rd, q + hq, gr + hq, den + hn, n0 + CH, w.r1);
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+      if (t == 0 && !s_abort) {
+        tc_fence_after();
+        const uint32_t a0 = saddr(B0);
+        mma_state(x.tm + T_STATE, a0, a0 + BT, a0 + 2 * BT, a0 + 3 * BT, c == 0);
+        mma_tok(tok0 + 128 * (g & 1), a0 + 2 * BT, a0 + 3 * BT, saddr(SH), false);
+        mma_commit(&x.bar[g & 1]);
+      }
+      ++g;
+    }
+    if (c > 0) {  // gam, dq and r of chunk c - 1
+      const uint32_t ge = c < w.nch ? g - 2 : g - 1;
+      const bool ok = wait_chunk(x, ge);
+      tc_fence_after();
+      const long n0 = w.r0 + static_cast<long>(c - 1) * CH;
+      const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
+      const int row = 32 * qd + lane;
+      const uint8_t* B0 = sm + O_BUF + (ge & 1) * BUF;
+      float a[CW], b[CW], f[CW];
+      if (ok) {
+        ld_halves(tok0 + 128 * (ge & 1) + ((32u * qd) << 16) + CW * cg, a, b);
+      } else {
+#pragma unroll
+        for (int j = 0; j < CW; ++j) a[j] = b[j] = 0.f;
+      }
+      get_row<CW>(B0, B0 + BT, row, CW * cg, f);  // phi(Q) (0 on invalid rows); phi' = min(phi, 1)
+      float part = 0.f;
+#pragma unroll
+      for (int j = 0; j < CW; ++j) {
+        a[j] += b[j];  // S gt
+        part = fmaf(f[j], a[j], part);
+      }
+      spart[cg * CH + row] = part;
+      __syncthreads();
+      float dsum = 0.f;
+#pragma unroll
+      for (int u = 0; u < NCG; ++u) dsum += spart[u * CH + row];
+      const float gm = -dsum * sinv[(ge & 1) * CH + row];
+      if (row < nv) {
+        float* dst = dq + hq + (n0 + row) * 64 + CW * cg;
+#pragma unroll
+        for (int j = 0; j < CW; j += 4) {
+          float r4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) r4[u] = (a[j + u] + gm * sz[CW * cg + j + u]) * fminf(f[j + u], 1.f);
+          st4(dst + j, make_float4(r4[0], r4[1], r4[2], r4[3]));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < CW; ++j) rp[j] = fmaf(gm, f[j], rp[j]);
+      tc_fence_before();
+      __syncthreads();  // the next transform rewrites what this epilogue read
+    }
+  }
+  {
+    const bool ok = w.nch > 0 && !*reinterpret_cast<volatile int*>(x.abort);
+    tc_fence_after();
+    state_readout(x, __all_sync(0xffffffffu, ok), P);
+  }
+  // r: the thread's CW columns summed over its warp's lanes, then over the
+  // four lane quarters of its column group
+#pragma unroll
+  for (int j = 0; j < CW; ++j)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rp[j] += __shfl_xor_sync(0xffffffffu, rp[j], o);
+  if (lane == 0)
+#pragma unroll
+    for (int j = 0; j < CW; ++j) scol[warp * 64 + j] = rp[j];
+  __syncthreads();
+  if (t < 64) {
+    const int gc = t / CW, j = t % CW;
+    float sr = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) sr += scol[(4 * gc + u) * 64 + j];
+    P[64 * 64 + t] = sr;
+  }
+  tc_fence_before();
+  cluster_arrive();
+  // padded rows, while the slower CTAs of the cluster finish phase 1
+  for (long e = w.z0 * 16 + t; e < w.z1 * 16; e += NTX) {
+    st4(dq + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
+    st4(dk + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
+    st4(dv + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
+  }
+  cluster_wait();  // every record complete
+
+  // ---- phase 2: dk = (V R^T + r) * phi'(K), dv = phi(K) R
+  if (w.nch > 0) {
+    fetch(ra, v + hq, w.r0, w.r1);
+    fetch(rb, k + hq, w.r0, w.r1);
+  }
+  {
+    float4 m[NPC], rv;
+    cluster_sum(P, nseg, m, rv);
+#pragma unroll
+    for (int i = 0; i < NPC; ++i) {
+      const int e = t + NTX * i;
+      put_split4(SH, SH + ST, e >> 4, 4 * (e & 15), m[i]);
+    }
+    if (t < 16) st4(sz + 4 * t, rv);
+  }
+  cluster_arrive();
+  fence_proxy_async();
+  __syncthreads();
+  const uint32_t t2 = x.tm;  // phase 2: buffer b uses columns 256 b .. 256 b + 255
+  for (int c = 0; c <= w.nch; ++c) {
+    if (c < w.nch) {
+      uint8_t* B0 = sm + O_BUF + (g & 1) * BUF;  // V hi, V lo, K hi, K lo
+      const long n0 = w.r0 + static_cast<long>(c) * CH;
+      const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
+#pragma unroll
+      for (int i = 0; i < NU; ++i) {
+        const int row = unit_row(i);
+        float a[8], b[8];
+        unpack8(ra[2 * i], ra[2 * i + 1], a);
+        unpack8(rb[2 * i], rb[2 * i + 1], b);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) b[j] = row < nv ? phi(b[j]) : 0.f;
+        put_split8(B0, B0 + BT, row, c8, a);
+        put_split8(B0 + 2 * BT, B0 + 3 * BT, row, c8, b);
+      }
+      if (c + 1 < w.nch) {
+        fetch(ra, v + hq, n0 + CH, w.r1);
+        fetch(rb, k + hq, n0 + CH, w.r1);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+      if (t == 0 && !s_abort) {
+        tc_fence_after();
+        const uint32_t a0 = saddr(B0), d0 = t2 + 256 * (g & 1);
+        mma_tok(d0, a0, a0 + BT, saddr(SH), false);                    // V [R_hi; R_lo]^T
+        mma_tok(d0 + 128, a0 + 2 * BT, a0 + 3 * BT, saddr(SH), true);  // phi(K) [R_hi | R_lo]
+        mma_commit(&x.bar[g & 1]);
+      }
+      ++g;
+    }
+    if (c > 0) {  // dk, dv of chunk c - 1
+      const uint32_t ge = c < w.nch ? g - 2 : g - 1;
+      const bool ok = wait_chunk(x, ge);
+      tc_fence_after();
+      if (ok) {
+        const long n0 = w.r0 + static_cast<long>(c - 1) * CH;
+        const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
+        const int row = 32 * qd + lane;
+        const uint32_t acc = t2 + 256 * (ge & 1) + ((32u * qd) << 16) + CW * cg;
+        const uint8_t* B0 = sm + O_BUF + (ge & 1) * BUF;
+        float a[CW], b[CW];
+        ld_halves(acc, a, b);
+        if (row < nv) {
+          float f[CW];
+          get_row<CW>(B0 + 2 * BT, B0 + 3 * BT, row, CW * cg, f);  // phi(K)
+          float* dst = dk + hq + (n0 + row) * 64 + CW * cg;
+#pragma unroll
+          for (int j = 0; j < CW; j += 4) {
+            float r4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              r4[u] = (a[j + u] + b[j + u] + sz[CW * cg + j + u]) * fminf(f[j + u], 1.f);
+            st4(dst + j, make_float4(r4[0], r4[1], r4[2], r4[3]));
+          }
+        }
+        ld_halves(acc + 128, a, b);
+        if (row < nv) {
+          float* dst = dv + hq + (n0 + row) * 64 + CW * cg;
+#pragma unroll
+          for (int j = 0; j < CW; j += 4)
+            st4(dst + j, make_float4(a[j] + b[j], a[j + 1] + b[j + 1], a[j + 2] + b[j + 2], a[j + 3] + b[j + 3]));
+        }
+      }
+      tc_fence_before();
+      __syncthreads();  // the next transform rewrites what this epilogue read
+    }
+  }
+  teardown(x);
+}
+
+template <typename K, typename... Args>
+cudaError_t launch_cluster(K kernel, int nseg, int BH, cudaStream_t st, Args... args) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TC);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(nseg) * static_cast<unsigned>(BH));
+  cfg.blockDim = dim3(NTX);
+  cfg.dynamicSmemBytes = SMEM_TC;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(nseg);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// CTAs per (b, h): a power of two (clusters of 1, 2, 4 or 8 CTAs pack the
+// GPCs without holes), at most one per 128-token chunk, and about three
+// waves of one CTA per SM over all (b, h).
+int noncausal_tc_nseg(int BH, int N) {
+  const int nch = (N + CH - 1) / CH;
+  const int fill = (3 * 152 + BH - 1) / BH;
+  int n = kMaxSeg;
+  while (n > 1 && (n > nch || n > fill)) n >>= 1;
+  return n;
+}
+
+cudaError_t noncausal_tc_fwd(const float* q, const float* k, const float* v, const int* lengths,
+                             float* out, float* den, float* S, float* Z, const Shape& s,
+                             cudaStream_t st) {
+  const int BH = s.B * s.H, nseg = noncausal_tc_nseg(BH, s.N);
+  return launch_cluster(k_nc_fwd_tc, nseg, BH, st, q, k, v, lengths, out, den, S, Z, s.N, s.H,
+                        nseg);
+}
+
+cudaError_t noncausal_tc_bwd(const float* q, const float* k, const float* v, const int* lengths,
+                             const float* out, const float* den, const float* S, const float* Z,
+                             const float* dout, float* dq, float* dk, float* dv, const Shape& s,
+                             cudaStream_t st) {
+  const int BH = s.B * s.H, nseg = noncausal_tc_nseg(BH, s.N);
+  (void)out;  // gam comes from the dq accumulator; out is not read
+  return launch_cluster(k_nc_bwd_tc, nseg, BH, st, q, k, v, lengths, den, S, Z, dout, dq, dk,
+                        dv, s.N, s.H, nseg);
+}
+
+}  // namespace la
