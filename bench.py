@@ -142,15 +142,18 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+# the files the timed causal tcgen05 kernels are built from
+CAUSAL_TC_SOURCES = ("causal_tc.cu", "causal_tc_bwd.cu", "tc.cuh", "tc_chunk.cuh", "common.cuh")
+
+
 def kernel_source_hash():
-    """Hash of the CUDA sources, to tell whether stored ncu counters still
-    describe the kernels being timed."""
+    """Hash of the causal tcgen05 kernels' sources, to tell whether stored ncu
+    counters still describe the kernels being timed."""
     csrc = os.path.join(ROOT, "kernelized_causal_attention_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in CAUSAL_TC_SOURCES:
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -341,7 +344,9 @@ def secondary(la, torch, dev, flush, peaks):
         bwd()
     (mf, mb), ms = time_calls([fwd, bwd], 50, flush, torch, None, dev)
     valid = int(lengths.sum()) * H  # valid token-heads
-    alg = valid * (4 * (2 * D + M) + 4 * M + 4) + valid * (4 * (2 * D + M) + 8 * M + 4 + 4 * (2 * D + M))
+    # fwd: q, k, v in, out and den out; bwd: q, k, v, dout and den in (out is
+    # not needed: gt . out = phi(Q) . S gt / den), dq, dk, dv out; valid rows only
+    alg = valid * (4 * (2 * D + M) + 4 * M + 4) + valid * (4 * (2 * D + M) + 4 * M + 4 + 4 * (2 * D + M))
     flops = valid * 12 * D * M
     gbs = alg / (ms / 1e3) / 1e9
     res["noncausal_speech_f32"] = {
