@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true", help="skip the non-causal/decode lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--secondary-only", action="store_true",
+                    help="run only the non-causal/decode measurements (one JSON object); for "
+                         "profiling those kernels")
     return ap.parse_args()
 
 
@@ -470,9 +473,26 @@ def run_reference(args, dist):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_secondary_only():
+    """The non-causal and decode measurements alone, on cuda:0."""
+    import torch
+
+    import kernelized_causal_attention_gb300 as la
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    la.lib()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    return {"secondary": secondary(la, torch, dev, lambda: flush_buf.zero_(), measured_peaks())}
+
+
 def main():
     args = parse()
     dist = Dist()
+    if args.secondary_only:
+        if dist.rank == 0:
+            print(json.dumps(run_secondary_only()), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, dist)
     else:

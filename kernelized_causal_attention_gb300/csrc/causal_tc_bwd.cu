@@ -12,12 +12,12 @@
 // with P = bf16(mask(phi(Q) phi(K)^T)) and dP = bf16(mask(dA)); then
 // dq = grad_phiQ * phi'(Q), dk = grad_phiK * phi'(K), and phi'(x) = min(phi(x), 1).
 //
-// Two passes.  MODE 0 (one CTA per sub-segment of whole 128-token chunks)
-// reads q, k, v, dout, out and den once; it stores phi(Q), phi(K) and
-// gt = dout / den (bf16) and gam (fp32) in the workspace, and the
-// sub-segment's partial S, z, R, r.  MODE 1 runs two roles per segment
-// (grid z): role 0 walks forward carrying S, z and writes dq; role 1 walks
-// backward carrying R, r and writes dk and dv.  Each CTA first adds up the
+// Two kernels.  The state pass k_tc_bwd_state (one CTA per sub-segment of
+// whole 128-token chunks) reads q, k, v, dout, out and den once; it stores
+// phi(Q), phi(K) and gt = dout / den (bf16) and gam (fp32) in the workspace,
+// and the sub-segment's partial S, z, R, r.  The main pass k_tc_bwd_main
+// runs two roles per segment (grid z): role 0 walks forward carrying S, z
+// and writes dq; role 1 walks backward carrying R, r and writes dk and dv.  Each CTA first adds up the
 // partial states of the sub-segments before (role 0) or after (role 1) it.
 // Every product, including the vector sums z and r (against a ones column
 // or the gam column), runs on tcgen05 with TMA-fed operands; dq, dk and dv
