@@ -23,7 +23,10 @@
  *    Arithmetic accumulates in fp32.  The feature map uses no 1/sqrt(D)
  *    temperature and the denominator no epsilon.
  *  - Every pointer must be 16-byte aligned.  Supported head sizes: D and M in
- *    {16, 32, 64}.  Limits: 1 <= B*H <= 2^20, 1 <= N <= 2^24.
+ *    {16, 32, 64}.  Limits: 1 <= N <= 2^24; 1 <= B*H <= 65535 for the
+ *    sequence calls (causal and non-causal; one grid row per (b, h)) and
+ *    1 <= B*H <= 2^20 for la_decode_step.  Larger B*H is refused with
+ *    LA_ERR_INVALID_ARG before anything is launched.
  *  - stream is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  Calls are asynchronous on it; results are ready when the
  *    stream reaches them.  Calls that share a workspace must be ordered.

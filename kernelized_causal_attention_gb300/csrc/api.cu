@@ -16,10 +16,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool supported_dim(int x) { return x == 16 || x == 32 || x == 64; }
 
-// Checks shared by the sequence calls; returns LA_OK or the error code.
-int check_shape(int B, int H, int N, int D, int M, int dtype) {
+// Checks shared by all calls; returns LA_OK or the error code.  max_bh is
+// the largest B*H the call's grids take (65535 grid rows for the sequence
+// calls, 2^20 streams for the decode step).
+int check_shape(int B, int H, int N, int D, int M, int dtype, long long max_bh = 65535) {
   if (B < 1 || H < 1 || N < 1) return LA_ERR_INVALID_ARG;
-  if ((long long)B * H > (1ll << 20) || N > (1 << 24)) return LA_ERR_INVALID_ARG;
+  if ((long long)B * H > max_bh || N > (1 << 24)) return LA_ERR_INVALID_ARG;
   if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
   if (D < 1 || M < 1) return LA_ERR_INVALID_ARG;
   if (!supported_dim(D) || !supported_dim(M)) return LA_ERR_UNSUPPORTED;
@@ -87,7 +89,9 @@ size_t la_workspace_bytes(int op, int B, int H, int N, int D, int M, int dtype) 
 }
 
 int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype) {
-  if (check_shape(B, H, op == LA_OP_DECODE ? 1 : N, D, M, dtype) != LA_OK) return 0;
+  if (check_shape(B, H, op == LA_OP_DECODE ? 1 : N, D, M, dtype,
+                  op == LA_OP_DECODE ? (1ll << 20) : 65535) != LA_OK)
+    return 0;
   const Shape s{B, H, N, D, M, dtype};
   switch (op) {
     case LA_OP_CAUSAL_FWD:
@@ -164,7 +168,7 @@ int la_noncausal_bwd(const void* q, const void* k, const void* v, const int* len
 
 int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* y,
                    int B, int H, int D, int M, int dtype, void* stream) {
-  LA_TRY(check_shape(B, H, 1, D, M, dtype));
+  LA_TRY(check_shape(B, H, 1, D, M, dtype, 1ll << 20));
   LA_TRY(check_ptrs({q, k, v, S, Z, y}));
   const Shape s{B, H, 1, D, M, dtype};
   return from_cuda(la::decode_step(q, k, v, S, Z, y, s, static_cast<cudaStream_t>(stream)));

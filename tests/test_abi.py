@@ -73,6 +73,7 @@ def _fwd(la, **kw):
     (dict(q=FAKE + 4), 1), (dict(den=FAKE + 8), 1),
     (dict(N=0), 1), (dict(B=0), 1), (dict(H=-1), 1), (dict(N=(1 << 24) + 1), 1),
     (dict(dt=7), 1), (dict(D=48), 2), (dict(M=128), 2), (dict(D=0), 1),
+    (dict(B=65536), 1), (dict(B=256, H=256), 1),     # B*H above the 65535 grid rows
     (dict(B=4, H=8, N=3072, D=64, M=64), 4),          # needs workspace, none given
     (dict(B=4, H=8, N=3072, D=64, M=64, ws=FAKE, wsb=16), 4),
     (dict(B=4, H=8, N=3072, D=64, M=64, ws=FAKE + 4, wsb=1 << 30), 1),
@@ -96,6 +97,20 @@ def test_other_calls_reject(linattn):
     assert L.la_decode_step(F, F, None, F, F, F, 1, 1, 64, 64, 0, None) == 1
     assert L.la_decode_step(F, F, F, F, F, F, 1, 1, 64, 96, 0, None) == 2
     assert L.la_decode_step(F, F, F, F, F, F, 0, 1, 64, 64, 0, None) == 1
+    assert L.la_decode_step(F, F, F, F, F, F, (1 << 20) + 1, 1, 64, 64, 0, None) == 1
+
+
+def test_head_count_limits(linattn):
+    """B*H limits: 65535 for the sequence calls, 2^20 streams for decode
+    (sizes only: nothing is launched)."""
+    la = linattn
+    for op in (la.LA_OP_CAUSAL_FWD, la.LA_OP_CAUSAL_BWD, la.LA_OP_NONCAUSAL_FWD,
+               la.LA_OP_NONCAUSAL_BWD):
+        assert la.la_kernel_launches(op, 65535, 1, 64, 16, 16, la.LA_F32) > 0
+        assert la.la_kernel_launches(op, 65536, 1, 64, 16, 16, la.LA_F32) == 0
+        assert la.la_workspace_bytes(op, 65536, 1, 64, 16, 16, la.LA_F32) == 0
+    assert la.la_kernel_launches(la.LA_OP_DECODE, 1 << 20, 1, 1, 64, 64, la.LA_F32) == 1
+    assert la.la_kernel_launches(la.LA_OP_DECODE, (1 << 20) + 1, 1, 1, 64, 64, la.LA_F32) == 0
 
 
 def test_binding_requires_library(monkeypatch, tmp_path):
