@@ -282,7 +282,8 @@ def run_ours(args, dist):
            "roofline": roofline, "step_roofline": step_roof, "e2e": e2e,
            "gpu_launches": launches, "clocks": clk, "wall_s_timed_region": round(wall, 3)}
     if not args.no_secondary:
-        res["secondary"] = secondary(la, torch, dev, flush, peaks)
+        res["secondary"] = secondary(la, torch, dev, flush, peaks,
+                                     with_cpu=dist.rank == 0 and not args.no_cpu)
     if dist.rank == 0 and not args.no_cpu:
         res["cpu_baseline"] = cpu_baseline(q, k, v, g, B, H, N)
     dist.close()
@@ -384,9 +385,10 @@ def measure_e2e(la, torch, dev, q, k, v, g, out, den, wsf, wsb, B, H, N, D, M, d
             "serial_ms_per_step": round(ms_serial, 5)}
 
 
-def secondary(la, torch, dev, flush, peaks):
+def secondary(la, torch, dev, flush, peaks, with_cpu=True):
     """Non-causal fwd+bwd (long speech-like sequences with padding) and the
-    decode step (256 and 2048 streams x 8 heads), each against its roofline."""
+    decode step (256 and 2048 streams x 8 heads), each against its roofline,
+    and (with_cpu) the fp64 oracle timed beside each on the host cores."""
     from kernelized_causal_attention_gb300.workloads import WORKLOADS, noncausal_inputs
     res = {}
     w = WORKLOADS["noncausal_speech_f32"]
@@ -419,6 +421,8 @@ def secondary(la, torch, dev, flush, peaks):
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": alg},
         "fp32_tflops": round(flops / (ms / 1e3) / 1e12, 2)}
+    if with_cpu:
+        res["noncausal_speech_f32"]["cpu_baseline"] = cpu_baseline_noncausal(q, k, v, g, lengths)
 
     for Bd in (256, 2048):
         Hd, Dd, Md = 8, 64, 64
@@ -462,6 +466,8 @@ def secondary(la, torch, dev, flush, peaks):
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": alg},
             "timing": "CUDA graph of 64 steps, 20 replays, state kept warm"}
+        if with_cpu and Bd == 256:
+            res[f"decode_f32_B{Bd}"]["cpu_baseline"] = cpu_baseline_decode(Bd, Hd, Dd, Md)
     return res
 
 
@@ -489,6 +495,53 @@ def cpu_baseline(q, k, v, g, B, H, N, budget_s=12.0):
             "kind": "oracle",
             "sample": f"full workload (B={B}, H={H}, N={N}) x {reps} repetitions, "
                       f"{el:.1f} s, fp64 recurrent form, fwd+bwd"}
+
+
+def cpu_baseline_noncausal(q, k, v, g, lengths, budget_s=5.0):
+    """The fp64 oracle's non-causal fwd then bwd on all host cores, over the
+    full workload, repeated until about `budget_s` seconds (at least once)."""
+    import oracle
+    cores = _cores(oracle)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.noncausal_fwd(q, k, v, lengths, nthreads=cores)
+        oracle.noncausal_bwd(q, k, v, g, lengths, nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 20:
+            break
+    B, H, N = q.shape[0], q.shape[1], q.shape[2]
+    return {"value": round(reps * int(lengths.sum()) / el, 1), "unit": "valid tokens/s",
+            "cores": cores, "kind": "oracle",
+            "sample": f"full workload (B={B}, H={H}, N={N}, lengths as the GPU line) x {reps}, "
+                      f"{el:.1f} s, fp64, fwd+bwd"}
+
+
+def cpu_baseline_decode(B, H, D, M, steps=64, budget_s=5.0):
+    """The fp64 oracle's decode steps for all B x H streams on all host cores,
+    `steps` steps per call (synthetic normal q, k, v), until about `budget_s`
+    seconds; reported as stream-steps per second like the GPU line."""
+    import numpy as np
+    import oracle
+    cores = _cores(oracle)
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((steps, B, H, D))
+    k = rng.standard_normal((steps, B, H, D))
+    v = rng.standard_normal((steps, B, H, M))
+    S = np.zeros((B, H, D, M))
+    Z = np.ones((B, H, D))
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        _, S, Z = oracle.decode(q, k, v, S, Z, nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 200:
+            break
+    return {"value": round(reps * steps * B * H / el, 1), "unit": "stream-steps/s",
+            "cores": cores, "kind": "oracle",
+            "sample": f"B={B} x H={H} streams, {reps} x {steps} steps, {el:.1f} s, fp64"}
 
 
 def run_reference(args, dist):
@@ -544,7 +597,8 @@ def run_secondary_only():
     dev = torch.device("cuda", 0)
     la.lib()
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    return {"secondary": secondary(la, torch, dev, lambda: flush_buf.zero_(), measured_peaks())}
+    return {"secondary": secondary(la, torch, dev, lambda: flush_buf.zero_(), measured_peaks(),
+                                   with_cpu=False)}
 
 
 def main():
