@@ -77,27 +77,15 @@ cudaError_t noncausal_bwd_cc(const void* q, const void* k, const void* v, const 
                              const void* out, const float* den, const float* S, const float* Z,
                              const void* dout, void* dq, void* dk, void* dv, float* ws,
                              const Shape& s, cudaStream_t st);
-// Non-causal path for bf16, D = M = 64: two launches per direction.
-SegPlan noncausal64_plan(int BH, int N);
-size_t noncausal64_fwd_ws_floats(const Shape& s);
-size_t noncausal64_bwd_ws_floats(const Shape& s);
-cudaError_t noncausal64_fwd(const void* q, const void* k, const void* v, const int* lengths,
-                            void* out, float* den, float* S, float* Z, float* ws, const Shape& s,
-                            cudaStream_t st);
-cudaError_t noncausal64_bwd(const void* q, const void* k, const void* v, const int* lengths,
-                            const void* out, const float* den, const float* S, const float* Z,
-                            const void* dout, void* dq, void* dk, void* dv, float* ws,
-                            const Shape& s, cudaStream_t st);
-// Non-causal path for fp32, D = M = 64, on the tensor cores: one cluster
-// launch per direction, no workspace.
+// Non-causal path for D = M = 64 (fp32 or bf16) on the tensor cores: one
+// cluster launch per direction, no workspace.
 int noncausal_tc_nseg(int BH, int N);
-cudaError_t noncausal_tc_fwd(const float* q, const float* k, const float* v, const int* lengths,
-                             float* out, float* den, float* S, float* Z, const Shape& s,
+cudaError_t noncausal_tc_fwd(const void* q, const void* k, const void* v, const int* lengths,
+                             void* out, float* den, float* S, float* Z, const Shape& s,
                              cudaStream_t st);
-cudaError_t noncausal_tc_bwd(const float* q, const float* k, const float* v, const int* lengths,
-                             const float* out, const float* den, const float* S, const float* Z,
-                             const float* dout, float* dq, float* dk, float* dv, const Shape& s,
-                             cudaStream_t st);
+cudaError_t noncausal_tc_bwd(const void* q, const void* k, const void* v, const int* lengths,
+                             const float* den, const float* S, const float* Z, const void* dout,
+                             void* dq, void* dk, void* dv, const Shape& s, cudaStream_t st);
 cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* y,
                         const Shape& s, cudaStream_t st);
 

@@ -326,37 +326,30 @@ cudaError_t run_bwd(const T* q, const T* k, const T* v, const int* lengths, cons
   return cudaGetLastError();
 }
 
-bool use64(const Shape& s) { return s.D == 64 && s.M == 64; }
-bool use_tc(const Shape& s) { return use64(s) && s.dtype == 0; }
+bool use_tc(const Shape& s) { return s.D == 64 && s.M == 64; }
 
 }  // namespace
 
 size_t noncausal_fwd_ws_floats(const Shape& s) {
   if (use_tc(s)) return 0;
-  if (use64(s)) return noncausal64_fwd_ws_floats(s);
   const SegPlan pl = plan_segments(s.B * s.H, s.N);
   return (size_t)s.B * s.H * pl.nseg * (s.D * s.M + s.D);
 }
 
 size_t noncausal_bwd_ws_floats(const Shape& s) {
   if (use_tc(s)) return 0;
-  if (use64(s)) return noncausal64_bwd_ws_floats(s);
   const SegPlan pl = plan_segments(s.B * s.H, s.N);
   return (size_t)s.B * s.H * (pl.nseg + 1) * (s.D * s.M + s.D);
 }
 
-int noncausal_fwd_launches(const Shape& s) { return use_tc(s) ? 1 : (use64(s) ? 2 : 3); }
+int noncausal_fwd_launches(const Shape& s) { return use_tc(s) ? 1 : 3; }
 
-int noncausal_bwd_launches(const Shape& s) { return use_tc(s) ? 1 : (use64(s) ? 2 : 3); }
+int noncausal_bwd_launches(const Shape& s) { return use_tc(s) ? 1 : 3; }
 
 cudaError_t noncausal_fwd_cc(const void* q, const void* k, const void* v, const int* lengths,
                              void* out, float* den, float* S, float* Z, float* ws, const Shape& s,
                              cudaStream_t st) {
-  if (use_tc(s))
-    return noncausal_tc_fwd(static_cast<const float*>(q), static_cast<const float*>(k),
-                                 static_cast<const float*>(v), lengths, static_cast<float*>(out),
-                                 den, S, Z, s, st);
-  if (use64(s)) return noncausal64_fwd(q, k, v, lengths, out, den, S, Z, ws, s, st);
+  if (use_tc(s)) return noncausal_tc_fwd(q, k, v, lengths, out, den, S, Z, s, st);
   if (s.dtype == 0) {
     using T = float;
     LA_DISPATCH_DM(s.D, s.M,
@@ -375,14 +368,8 @@ cudaError_t noncausal_bwd_cc(const void* q, const void* k, const void* v, const 
                              const void* out, const float* den, const float* S, const float* Z,
                              const void* dout, void* dq, void* dk, void* dv, float* ws,
                              const Shape& s, cudaStream_t st) {
-  if (use_tc(s))
-    return noncausal_tc_bwd(static_cast<const float*>(q), static_cast<const float*>(k),
-                                 static_cast<const float*>(v), lengths,
-                                 static_cast<const float*>(out), den, S, Z,
-                                 static_cast<const float*>(dout), static_cast<float*>(dq),
-                                 static_cast<float*>(dk), static_cast<float*>(dv), s, st);
-  if (use64(s))
-    return noncausal64_bwd(q, k, v, lengths, out, den, S, Z, dout, dq, dk, dv, ws, s, st);
+  if (use_tc(s))  // out is not read: gam comes from the dq accumulator
+    return noncausal_tc_bwd(q, k, v, lengths, den, S, Z, dout, dq, dk, dv, s, st);
   if (s.dtype == 0) {
     using T = float;
     LA_DISPATCH_DM(s.D, s.M,

@@ -1,4 +1,5 @@
-// Non-causal path for fp32 inputs with D = M = 64 on the tensor cores.
+// Non-causal path with D = M = 64 on the tensor cores, for fp32 and bf16
+// inputs (outputs in the input type; den, S, Z fp32).
 //
 // Method: "Linear Attention/zh", kernel reformulation (one shared S, Z per
 // (b, h)) and eq. 13-15 of "Transformers are RNNs" (part 2/3) with full sums
@@ -184,26 +185,70 @@ __device__ __forceinline__ Rows my_rows(const int* lengths, int b, int N, int p,
 __device__ __forceinline__ int unit_row(int i) { return (threadIdx.x >> 3) + (NTX / 8) * i; }
 __device__ __forceinline__ int unit_c8() { return threadIdx.x & 7; }
 
-// The thread's share of rows n0 .. n0 + 127 of x ([*][64] fp32); rows at or
-// past ne read as 0.
-__device__ __forceinline__ void fetch(float4 (&r)[2 * NU], const float* x, long n0, long ne) {
+// The thread's share of a chunk as loaded (converted to fp32 only when
+// used, so that the loads of the next chunk stay in flight meanwhile).
+template <typename T>
+struct Raw;
+template <>
+struct Raw<float> {
+  float4 v[2 * NU];
+};
+template <>
+struct Raw<__nv_bfloat16> {
+  uint4 v[NU];
+};
+
+// The thread's share of rows n0 .. n0 + 127 of x ([*][64]); rows at or past
+// ne read as 0.
+__device__ __forceinline__ void fetch(Raw<float>& r, const float* x, long n0, long ne) {
 #pragma unroll
   for (int i = 0; i < NU; ++i) {
     const long row = n0 + unit_row(i);
     if (row < ne) {
       const float* p = x + row * 64 + 8 * unit_c8();
-      r[2 * i] = ld4(p);
-      r[2 * i + 1] = ld4(p + 4);
+      r.v[2 * i] = ld4(p);
+      r.v[2 * i + 1] = ld4(p + 4);
     } else {
-      r[2 * i] = r[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      r.v[2 * i] = r.v[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
+__device__ __forceinline__ void fetch(Raw<__nv_bfloat16>& r, const __nv_bfloat16* x, long n0,
+                                      long ne) {
+#pragma unroll
+  for (int i = 0; i < NU; ++i) {
+    const long row = n0 + unit_row(i);
+    r.v[i] = row < ne ? *reinterpret_cast<const uint4*>(x + row * 64 + 8 * unit_c8())
+                      : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Unit i of a fetched share as 8 floats.
+__device__ __forceinline__ void unpack(const Raw<float>& r, int i, float* x) {
+  const float4 a = r.v[2 * i], b = r.v[2 * i + 1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void unpack(const Raw<__nv_bfloat16>& r, int i, float* x) {
+  const uint32_t w[4] = {r.v[i].x, r.v[i].y, r.v[i].z, r.v[i].w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    x[2 * j] = __uint_as_float(w[j] << 16);
+    x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+  }
+}
+
+// Four output values to global memory in the output type.
+__device__ __forceinline__ void st_out(float* dst, float4 v) { st4(dst, v); }
+__device__ __forceinline__ void st_out(__nv_bfloat16* dst, float4 v) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  *reinterpret_cast<uint2*>(dst) = make_uint2(bits(a), bits(b));
+}
 
 // The backward's phase-1 share of a chunk: q, dout and den.
-__device__ __forceinline__ void fetch_bwd1(float4 (&ra)[2 * NU], float4 (&rb)[2 * NU],
-                                           float (&rd)[NU], const float* qh, const float* gh,
-                                           const float* dh, long n0, long ne) {
+template <typename T>
+__device__ __forceinline__ void fetch_bwd1(Raw<T>& ra, Raw<T>& rb, float (&rd)[NU], const T* qh,
+                                           const T* gh, const float* dh, long n0, long ne) {
   fetch(ra, qh, n0, ne);
   fetch(rb, gh, n0, ne);
 #pragma unroll
@@ -213,10 +258,6 @@ __device__ __forceinline__ void fetch_bwd1(float4 (&ra)[2 * NU], float4 (&rb)[2 
   }
 }
 
-__device__ __forceinline__ void unpack8(const float4& a, const float4& b, float* x) {
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
 
 __device__ __forceinline__ float sum8(float x) {  // over the 8 lanes of a row
   x += __shfl_xor_sync(0xffffffffu, x, 4);
@@ -415,10 +456,11 @@ __device__ __forceinline__ uint32_t saddr(const void* p) {
 }
 
 // ---------------------------------------------------------------- forward
+template <typename T>
 __global__ void __launch_bounds__(NTX, 1)
-    k_nc_fwd_tc(const float* __restrict__ q, const float* __restrict__ k,
-                const float* __restrict__ v, const int* __restrict__ lengths,
-                float* __restrict__ out, float* __restrict__ den, float* __restrict__ S,
+    k_nc_fwd_tc(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                const int* __restrict__ lengths, T* __restrict__ out, float* __restrict__ den,
+                float* __restrict__ S,
                 float* __restrict__ Z, int N, int H, int nseg) {
   extern __shared__ uint8_t smraw[];
   __shared__ int s_abort;
@@ -436,7 +478,7 @@ __global__ void __launch_bounds__(NTX, 1)
   const int c8 = unit_c8();
 
   uint32_t g = 0;  // chunks issued so far: buffer g & 1, barrier parity (g >> 1) & 1
-  float4 ra[2 * NU], rb[2 * NU];
+  Raw<T> ra, rb;
   if (w.nch > 0) {
     fetch(ra, k + hq, w.r0, w.r1);
     fetch(rb, v + hq, w.r0, w.r1);
@@ -452,8 +494,8 @@ __global__ void __launch_bounds__(NTX, 1)
     for (int i = 0; i < NU; ++i) {
       const int row = unit_row(i);
       float a[8], b[8];
-      unpack8(ra[2 * i], ra[2 * i + 1], a);
-      unpack8(rb[2 * i], rb[2 * i + 1], b);
+      unpack(ra, i, a);
+      unpack(rb, i, b);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         a[j] = row < nv ? phi(a[j]) : 0.f;
@@ -486,7 +528,7 @@ __global__ void __launch_bounds__(NTX, 1)
   tc_fence_before();
   cluster_arrive();
   // padded rows, while the slower CTAs of the cluster finish phase 1
-  for (long e = w.z0 * 16 + t; e < w.z1 * 16; e += NTX) st4(out + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
+  for (long e = w.z0 * 16 + t; e < w.z1 * 16; e += NTX) st_out(out + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
   if (den != nullptr)
     for (long i = w.z0 + t; i < w.z1; i += NTX) den[hn + i] = 0.f;
   cluster_wait();  // every record complete
@@ -523,7 +565,7 @@ __global__ void __launch_bounds__(NTX, 1)
       for (int i = 0; i < NU; ++i) {
         const int row = unit_row(i);
         float a[8];
-        unpack8(ra[2 * i], ra[2 * i + 1], a);
+        unpack(ra, i, a);
         float dp = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -561,10 +603,10 @@ __global__ void __launch_bounds__(NTX, 1)
         ld_halves(tok0 + 128 * (ge & 1) + ((32u * qd) << 16) + CW * cg, a, b);
         if (row < nv) {
           const float inv = 1.f / sden[(ge & 1) * CH + row];
-          float* dst = out + hq + (n0 + row) * 64 + CW * cg;
+          T* dst = out + hq + (n0 + row) * 64 + CW * cg;
 #pragma unroll
           for (int j = 0; j < CW; j += 4)
-            st4(dst + j, make_float4((a[j] + b[j]) * inv, (a[j + 1] + b[j + 1]) * inv,
+            st_out(dst + j, make_float4((a[j] + b[j]) * inv, (a[j + 1] + b[j + 1]) * inv,
                                      (a[j + 2] + b[j + 2]) * inv, (a[j + 3] + b[j + 3]) * inv));
         }
       }
@@ -576,13 +618,13 @@ __global__ void __launch_bounds__(NTX, 1)
 }
 
 // --------------------------------------------------------------- backward
+template <typename T>
 __global__ void __launch_bounds__(NTX, 1)
-    k_nc_bwd_tc(const float* __restrict__ q, const float* __restrict__ k,
-                const float* __restrict__ v, const int* __restrict__ lengths,
-                const float* __restrict__ den, const float* __restrict__ S,
-                const float* __restrict__ Z,
-                const float* __restrict__ gr, float* __restrict__ dq, float* __restrict__ dk,
-                float* __restrict__ dv, int N, int H, int nseg) {
+    k_nc_bwd_tc(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                const int* __restrict__ lengths, const float* __restrict__ den,
+                const float* __restrict__ S, const float* __restrict__ Z,
+                const T* __restrict__ gr, T* __restrict__ dq, T* __restrict__ dk,
+                T* __restrict__ dv, int N, int H, int nseg) {
   extern __shared__ uint8_t smraw[];
   __shared__ int s_abort;
   const Ctx x = setup(smraw, &s_abort);
@@ -600,7 +642,7 @@ __global__ void __launch_bounds__(NTX, 1)
   const int c8 = unit_c8();
 
   uint32_t g = 0;
-  float4 ra[2 * NU], rb[2 * NU];
+  Raw<T> ra, rb;
   float rd[NU];
   if (w.nch > 0) fetch_bwd1(ra, rb, rd, q + hq, gr + hq, den + hn, w.r0, w.r1);
   // S (the forward's state) as hi | lo operand tiles; Z
@@ -628,8 +670,8 @@ __global__ void __launch_bounds__(NTX, 1)
         const int row = unit_row(i);
         const bool ok = row < nv;
         float a[8], b[8];
-        unpack8(ra[2 * i], ra[2 * i + 1], a);
-        unpack8(rb[2 * i], rb[2 * i + 1], b);
+        unpack(ra, i, a);
+        unpack(rb, i, b);
         const float inv = ok ? 1.f / rd[i] : 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -682,13 +724,13 @@ __global__ void __launch_bounds__(NTX, 1)
       for (int u = 0; u < NCG; ++u) dsum += spart[u * CH + row];
       const float gm = -dsum * sinv[(ge & 1) * CH + row];
       if (row < nv) {
-        float* dst = dq + hq + (n0 + row) * 64 + CW * cg;
+        T* dst = dq + hq + (n0 + row) * 64 + CW * cg;
 #pragma unroll
         for (int j = 0; j < CW; j += 4) {
           float r4[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) r4[u] = (a[j + u] + gm * sz[CW * cg + j + u]) * fminf(f[j + u], 1.f);
-          st4(dst + j, make_float4(r4[0], r4[1], r4[2], r4[3]));
+          st_out(dst + j, make_float4(r4[0], r4[1], r4[2], r4[3]));
         }
       }
 #pragma unroll
@@ -723,9 +765,9 @@ __global__ void __launch_bounds__(NTX, 1)
   cluster_arrive();
   // padded rows, while the slower CTAs of the cluster finish phase 1
   for (long e = w.z0 * 16 + t; e < w.z1 * 16; e += NTX) {
-    st4(dq + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
-    st4(dk + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
-    st4(dv + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
+    st_out(dq + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
+    st_out(dk + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
+    st_out(dv + hq + 4 * e, make_float4(0.f, 0.f, 0.f, 0.f));
   }
   cluster_wait();  // every record complete
 
@@ -757,8 +799,8 @@ __global__ void __launch_bounds__(NTX, 1)
       for (int i = 0; i < NU; ++i) {
         const int row = unit_row(i);
         float a[8], b[8];
-        unpack8(ra[2 * i], ra[2 * i + 1], a);
-        unpack8(rb[2 * i], rb[2 * i + 1], b);
+        unpack(ra, i, a);
+        unpack(rb, i, b);
 #pragma unroll
         for (int j = 0; j < 8; ++j) b[j] = row < nv ? phi(b[j]) : 0.f;
         put_split8(B0, B0 + BT, row, c8, a);
@@ -795,22 +837,22 @@ __global__ void __launch_bounds__(NTX, 1)
         if (row < nv) {
           float f[CW];
           get_row<CW>(B0 + 2 * BT, B0 + 3 * BT, row, CW * cg, f);  // phi(K)
-          float* dst = dk + hq + (n0 + row) * 64 + CW * cg;
+          T* dst = dk + hq + (n0 + row) * 64 + CW * cg;
 #pragma unroll
           for (int j = 0; j < CW; j += 4) {
             float r4[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
               r4[u] = (a[j + u] + b[j + u] + sz[CW * cg + j + u]) * fminf(f[j + u], 1.f);
-            st4(dst + j, make_float4(r4[0], r4[1], r4[2], r4[3]));
+            st_out(dst + j, make_float4(r4[0], r4[1], r4[2], r4[3]));
           }
         }
         ld_halves(acc + 128, a, b);
         if (row < nv) {
-          float* dst = dv + hq + (n0 + row) * 64 + CW * cg;
+          T* dst = dv + hq + (n0 + row) * 64 + CW * cg;
 #pragma unroll
           for (int j = 0; j < CW; j += 4)
-            st4(dst + j, make_float4(a[j] + b[j], a[j + 1] + b[j + 1], a[j + 2] + b[j + 2], a[j + 3] + b[j + 3]));
+            st_out(dst + j, make_float4(a[j] + b[j], a[j + 1] + b[j + 1], a[j + 2] + b[j + 2], a[j + 3] + b[j + 3]));
         }
       }
       tc_fence_before();
@@ -841,6 +883,21 @@ cudaError_t launch_cluster(K kernel, int nseg, int BH, cudaStream_t st, Args... 
   return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t run_fwd(const T* q, const T* k, const T* v, const int* lengths, T* out, float* den,
+                    float* S, float* Z, const Shape& s, int nseg, cudaStream_t st) {
+  return launch_cluster(k_nc_fwd_tc<T>, nseg, s.B * s.H, st, q, k, v, lengths, out, den, S, Z,
+                        s.N, s.H, nseg);
+}
+
+template <typename T>
+cudaError_t run_bwd(const T* q, const T* k, const T* v, const int* lengths, const float* den,
+                    const float* S, const float* Z, const T* dout, T* dq, T* dk, T* dv,
+                    const Shape& s, int nseg, cudaStream_t st) {
+  return launch_cluster(k_nc_bwd_tc<T>, nseg, s.B * s.H, st, q, k, v, lengths, den, S, Z, dout, dq,
+                        dk, dv, s.N, s.H, nseg);
+}
+
 }  // namespace
 
 // CTAs per (b, h): a power of two (clusters of 1, 2, 4 or 8 CTAs pack the
@@ -854,22 +911,34 @@ int noncausal_tc_nseg(int BH, int N) {
   return n;
 }
 
-cudaError_t noncausal_tc_fwd(const float* q, const float* k, const float* v, const int* lengths,
-                             float* out, float* den, float* S, float* Z, const Shape& s,
+cudaError_t noncausal_tc_fwd(const void* q, const void* k, const void* v, const int* lengths,
+                             void* out, float* den, float* S, float* Z, const Shape& s,
                              cudaStream_t st) {
   const int BH = s.B * s.H, nseg = noncausal_tc_nseg(BH, s.N);
-  return launch_cluster(k_nc_fwd_tc, nseg, BH, st, q, k, v, lengths, out, den, S, Z, s.N, s.H,
-                        nseg);
+  if (s.dtype == 0)
+    return run_fwd<float>(static_cast<const float*>(q), static_cast<const float*>(k),
+                          static_cast<const float*>(v), lengths, static_cast<float*>(out), den, S,
+                          Z, s, nseg, st);
+  using B16 = __nv_bfloat16;
+  return run_fwd<B16>(static_cast<const B16*>(q), static_cast<const B16*>(k),
+                      static_cast<const B16*>(v), lengths, static_cast<B16*>(out), den, S, Z, s,
+                      nseg, st);
 }
 
-cudaError_t noncausal_tc_bwd(const float* q, const float* k, const float* v, const int* lengths,
-                             const float* out, const float* den, const float* S, const float* Z,
-                             const float* dout, float* dq, float* dk, float* dv, const Shape& s,
-                             cudaStream_t st) {
+cudaError_t noncausal_tc_bwd(const void* q, const void* k, const void* v, const int* lengths,
+                             const float* den, const float* S, const float* Z, const void* dout,
+                             void* dq, void* dk, void* dv, const Shape& s, cudaStream_t st) {
   const int BH = s.B * s.H, nseg = noncausal_tc_nseg(BH, s.N);
-  (void)out;  // gam comes from the dq accumulator; out is not read
-  return launch_cluster(k_nc_bwd_tc, nseg, BH, st, q, k, v, lengths, den, S, Z, dout, dq, dk,
-                        dv, s.N, s.H, nseg);
+  if (s.dtype == 0)
+    return run_bwd<float>(static_cast<const float*>(q), static_cast<const float*>(k),
+                          static_cast<const float*>(v), lengths, den, S, Z,
+                          static_cast<const float*>(dout), static_cast<float*>(dq),
+                          static_cast<float*>(dk), static_cast<float*>(dv), s, nseg, st);
+  using B16 = __nv_bfloat16;
+  return run_bwd<B16>(static_cast<const B16*>(q), static_cast<const B16*>(k),
+                      static_cast<const B16*>(v), lengths, den, S, Z,
+                      static_cast<const B16*>(dout), static_cast<B16*>(dq), static_cast<B16*>(dk),
+                      static_cast<B16*>(dv), s, nseg, st);
 }
 
 }  // namespace la

@@ -46,11 +46,11 @@ def test_workspace_sizes(linattn):
     assert n > 0 and n % 16 == 0
     assert la.la_workspace_bytes(la.LA_OP_CAUSAL_BWD, 4, 8, 3072, 64, 64, la.LA_BF16) > 0
     assert la.la_workspace_bytes(la.LA_OP_DECODE, 256, 8, 1, 64, 64, la.LA_F32) == 0
-    # the fp32 non-causal path for D = M = 64 reduces its partial states within
-    # a cluster and needs none; the bf16 one and other head sizes need some
-    assert la.la_workspace_bytes(la.LA_OP_NONCAUSAL_FWD, 16, 6, 2048, 64, 64, la.LA_F32) == 0
-    assert la.la_workspace_bytes(la.LA_OP_NONCAUSAL_BWD, 16, 6, 2048, 64, 64, la.LA_F32) == 0
-    assert la.la_workspace_bytes(la.LA_OP_NONCAUSAL_FWD, 16, 6, 2048, 64, 64, la.LA_BF16) > 0
+    # the non-causal path for D = M = 64 reduces its partial states within a
+    # cluster and needs none (either dtype); other head sizes need some
+    for dt in (la.LA_F32, la.LA_BF16):
+        assert la.la_workspace_bytes(la.LA_OP_NONCAUSAL_FWD, 16, 6, 2048, 64, 64, dt) == 0
+        assert la.la_workspace_bytes(la.LA_OP_NONCAUSAL_BWD, 16, 6, 2048, 64, 64, dt) == 0
     assert la.la_workspace_bytes(la.LA_OP_NONCAUSAL_BWD, 16, 6, 2048, 32, 64, la.LA_F32) > 0
     # invalid arguments size to 0
     assert la.la_workspace_bytes(la.LA_OP_CAUSAL_FWD, 0, 8, 3072, 64, 64, la.LA_BF16) == 0
