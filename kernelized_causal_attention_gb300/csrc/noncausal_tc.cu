@@ -12,28 +12,36 @@
 //   dk_j = (R V_j + r) * phi'(K_j),  dv_j = R^T phi(K_j).
 // Rows i >= L are padding: they enter no sum and are written as zero.
 //
-// fp32 accuracy from bf16 products.  Every fp32 operand x is split exactly
-// into x_hi = bf16(x) and x_lo = bf16(x - x_hi), so |x - x_hi - x_lo| <=
-// 2^-18 |x|, and a product is taken as a_hi b_hi + a_hi b_lo + a_lo b_hi
-// (the dropped a_lo b_lo is below 2^-18 |a b|), accumulated in fp32 in
-// tensor memory.  Two instructions per 16-deep step carry the three
-// products: A_hi times the N = 128 operand [B_hi | B_lo] (two 64-wide halves
-// of the accumulator) and A_lo times B_hi into the first half; the epilogue
-// adds the halves.
+// fp32 accuracy from bf16 products.  An operand x is split into bf16 terms
+// x_0 = bf16(x), x_i = bf16(x - x_0 - ... - x_{i-1}); every term takes 9
+// more bits, so n terms leave a remainder below 2^-9n |x|.  With two terms
+// a product is a_0 b_0 + a_0 b_1 + a_1 b_0 (error below 2^-16 |a| |b|); with
+// three, a_0 b_0 + a_0 b_1 + a_1 b_0 + a_0 b_2 + a_1 b_1 + a_2 b_0 (below
+// 2^-25 |a| |b|).  Products accumulate in fp32 in two 64-column halves of a
+// tensor-memory accumulator that the epilogue adds:
+//   two terms:   A_0 [B_0 | B_1] (N = 128), A_1 B_0 -> first half
+//   three terms: A_0 [B_0 | B_1], A_1 [B_0 | B_1], A_0 B_2 -> first half,
+//                A_2 B_0 -> second half
+// Three terms go where the result is a small difference of large sums: dq
+// = S gt + gam Z and dk = R V + r cancel, exactly so for a sequence of one
+// token, so S, R, S gt and R V carry them for fp32 inputs.  out and dv
+// cancel nothing and take two terms, as does everything for bf16 inputs.
 //
 // Layout of the work.  One thread-block cluster of nseg CTAs per (b, h); the
 // valid rows are cut into 128-token chunks and every CTA takes an equal run.
-//  forward   phase 1: S~ += phi(K)^T [V_hi | V_lo]    (M = 64, state form)
+//  forward   phase 1: S~ += phi(K)^T V                  (M = 64, state form)
 //            cluster sum of the partial S, Z through distributed shared memory
-//            phase 2: O~ = phi(Q) [S_hi | S_lo]        (M = 128, token form)
-//  backward  phase 1: R~ += phi(Q)^T [gt_hi | gt_lo], dQ~ = gt [S_hi; S_lo]^T
+//            phase 2: O~ = phi(Q) S                     (M = 128, token form)
+//  backward  phase 1: R~ += phi(Q)^T gt, dQ~ = gt S^T
 //            cluster sum of the partial R, r
-//            phase 2: dK~ = V [R_hi; R_lo]^T, dV~ = phi(K) [R_hi | R_lo]
+//            phase 2: dK~ = V R^T, dV~ = phi(K) R
 // The CUDA cores load each chunk (prefetched into registers one chunk
 // ahead), apply phi, 1 / den, gam and the zeroing of invalid rows, split and
 // write the swizzled operand tiles (two buffers), and run the epilogue of
 // chunk c - 1 while the tensor cores work on chunk c.  den, gam, Z and r are
-// plain fp32 dot products on the CUDA cores.
+// plain fp32 dot products on the CUDA cores.  A CTA's partial record for the
+// cluster sum lives where the state operand tiles go next; a full cluster
+// barrier separates the last remote read of it from the first tile write.
 //
 // gam without out.  out_i = S^T phi(Q_i) / den_i, so
 //   gt_i . out_i = phi(Q_i) . (S gt_i) / den_i,
@@ -55,22 +63,36 @@ constexpr int NCG = NTX / 128;       // column groups of a 128-lane accumulator 
 constexpr int CW = 64 / NCG;         // columns per group
 constexpr int BT = CH * 128;         // bytes of a [128][64] bf16 tile
 constexpr int ST = 64 * 128;         // bytes of a [64][64] bf16 tile
-constexpr int BUF = 4 * BT;          // one operand buffer: two tensors, hi and lo each
 constexpr int PREC = 64 * 64 + 64;   // floats of a partial-state record
+constexpr int N_MISC = 4 * CH + 64 + (NTX / 32) * 64 + NCG * CH;
 constexpr int kMaxSeg = 8;           // CTAs per cluster (portable limit)
 
-// shared memory, bytes from a 1024-aligned base
-constexpr int O_BUF = 0;                  // two operand buffers
-constexpr int O_ST = 2 * BUF;             // state tile hi [64][64], lo right after it
-constexpr int O_P = O_ST + 2 * ST;        // this CTA's partial record (fp32)
-constexpr int O_MISC = O_P + 4 * PREC;    // fp32: per-row [2][128] x 2, vector [64], sums [warps][64], [4][128]
-constexpr int N_MISC = 4 * CH + 64 + (NTX / 32) * 64 + NCG * CH;
-constexpr int O_BAR = O_MISC + 4 * N_MISC;  // mbarriers: MMA done per buffer, final drain; TMEM address
-constexpr int SMEM_TC = O_BAR + 64 + 1024;  // + alignment slack
+// Terms per operand in the cancelling products (fp32 inputs: 3, bf16: 2).
+template <typename T>
+struct Terms {
+  static constexpr int n = 2;
+};
+template <>
+struct Terms<float> {
+  static constexpr int n = 3;
+};
+
+// Shared memory for NT-term operands, bytes from a 1024-aligned base.
+template <int NT>
+struct Lay {
+  static constexpr int BUF = 2 * NT * BT;  // one operand buffer: two tensors of NT tiles
+  static constexpr int O_BUF = 0;          // two operand buffers
+  static constexpr int O_ST = 2 * BUF;     // state tiles, NT x [64][64]; or the partial record (fp32)
+  static constexpr int N_ST = NT * ST > 4 * PREC ? NT * ST : (4 * PREC + 1023) / 1024 * 1024;
+  static constexpr int O_MISC = O_ST + N_ST;  // fp32: per-row [2][128] x 2, vector [64], sums [warps][64], [4][128]
+  static constexpr int O_BAR = O_MISC + 4 * N_MISC;  // mbarriers: MMA done per buffer, final drain; TMEM address
+  static constexpr int SMEM = O_BAR + 64 + 1024;     // + alignment slack
+};
+static_assert(Lay<3>::SMEM <= 232448 - 64, "shared memory of the three-term layout");
 
 // TMEM columns
-constexpr uint32_t T_STATE = 0;      // the M = 64 state accumulator (128 columns)
-constexpr uint32_t T_TOK = 128;      // token-form accumulators of phase 1, 128 per buffer
+constexpr uint32_t T_STATE = 0;      // the state accumulators (M = 128, 2 x 128 columns)
+constexpr uint32_t T_TOK = 256;      // token-form accumulators of phase 1, 128 per buffer
 
 // ------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -108,50 +130,65 @@ __device__ __forceinline__ uint32_t bits(__nv_bfloat162 h) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// (x0, x1) -> hi and lo bf16 pairs with x = hi + lo to 2^-18 relative.
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  hi = bits(h);
-  lo = bits(__floats2bfloat162_rn(x0 - hf.x, x1 - hf.y));
+// (x0, x1) -> NT bf16 pairs w[0], w[1], ...: each term is the bf16 rounding
+// of what the earlier ones leave (the subtraction is exact in fp32), so the
+// terms sum to x within 2^-9NT |x|.
+template <int NT>
+__device__ __forceinline__ void split(float x0, float x1, uint32_t (&w)[NT]) {
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    w[i] = bits(h);
+    if (i + 1 < NT) {
+      const float2 f = __bfloat1622float2(h);
+      x0 -= f.x;
+      x1 -= f.y;
+    }
+  }
 }
 
-// Columns 8 c8 .. 8 c8 + 7 of row `row` into the swizzled hi and lo tiles.
-__device__ __forceinline__ void put_split8(uint8_t* hi, uint8_t* lo, int row, int c8,
-                                           const float* x) {
-  uint32_t h[4], l[4];
+// Columns 8 c8 .. 8 c8 + 7 of row `row` into the swizzled term tiles t,
+// t + stride, ... (NT of them).
+template <int NT>
+__device__ __forceinline__ void put_split8(uint8_t* t, int stride, int row, int c8, const float* x) {
+  uint32_t w[4][NT];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) split2(x[2 * j], x[2 * j + 1], h[j], l[j]);
+  for (int j = 0; j < 4; ++j) split<NT>(x[2 * j], x[2 * j + 1], w[j]);
   const uint32_t off = static_cast<uint32_t>(row) * 128u + ((static_cast<uint32_t>(c8) ^ (row & 7u)) << 4);
-  *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+#pragma unroll
+  for (int i = 0; i < NT; ++i)
+    *reinterpret_cast<uint4*>(t + i * stride + off) = make_uint4(w[0][i], w[1][i], w[2][i], w[3][i]);
 }
 
 // Four values (columns col .. col + 3, col a multiple of 4) of row `row`.
-__device__ __forceinline__ void put_split4(uint8_t* hi, uint8_t* lo, int row, int col, float4 x) {
-  uint32_t h0, h1, l0, l1;
-  split2(x.x, x.y, h0, l0);
-  split2(x.z, x.w, h1, l1);
+template <int NT>
+__device__ __forceinline__ void put_split4(uint8_t* t, int stride, int row, int col, float4 x) {
+  uint32_t a[NT], b[NT];
+  split<NT>(x.x, x.y, a);
+  split<NT>(x.z, x.w, b);
   const uint32_t off = sw128_offset(row, col);
-  *reinterpret_cast<uint2*>(hi + off) = make_uint2(h0, h1);
-  *reinterpret_cast<uint2*>(lo + off) = make_uint2(l0, l1);
+#pragma unroll
+  for (int i = 0; i < NT; ++i) *reinterpret_cast<uint2*>(t + i * stride + off) = make_uint2(a[i], b[i]);
 }
 
-// Columns col0 .. col0 + NC - 1 (NC a multiple of 8) of row `row` as
-// hi + lo (the operand value to 2^-18 relative).
-template <int NC>
-__device__ __forceinline__ void get_row(const uint8_t* hi, const uint8_t* lo, int row, int col0,
-                                       float* x) {
+// Columns col0 .. col0 + NC - 1 (NC a multiple of 8) of row `row` as the sum
+// of the NT term tiles at t, t + stride, ... (smallest term first).
+template <int NC, int NT>
+__device__ __forceinline__ void get_row(const uint8_t* t, int stride, int row, int col0, float* x) {
 #pragma unroll
   for (int m = 0; m < NC / 8; ++m) {
     const uint32_t off = sw128_offset(row, col0 + 8 * m);
-    const uint4 a = *reinterpret_cast<const uint4*>(hi + off);
-    const uint4 b = *reinterpret_cast<const uint4*>(lo + off);
-    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[8 * m + 2 * j] = __uint_as_float(wa[j] << 16) + __uint_as_float(wb[j] << 16);
-      x[8 * m + 2 * j + 1] = __uint_as_float(wa[j] & 0xffff0000u) + __uint_as_float(wb[j] & 0xffff0000u);
+    for (int j = 0; j < 8; ++j) x[8 * m + j] = 0.f;
+#pragma unroll
+    for (int i = NT - 1; i >= 0; --i) {
+      const uint4 a = *reinterpret_cast<const uint4*>(t + i * stride + off);
+      const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[8 * m + 2 * j] += __uint_as_float(wa[j] << 16);
+        x[8 * m + 2 * j + 1] += __uint_as_float(wa[j] & 0xffff0000u);
+      }
     }
   }
 }
@@ -267,47 +304,71 @@ __device__ __forceinline__ float sum8(float x) {  // over the 8 lanes of a row
 }
 
 // ------------------------------------------------------------------ MMAs
-// State form over one chunk: D (M = 64, N = 128) (+)= A^T [B_hi | B_lo]
-// and D[:, 0:64] += A_lo^T B_hi, with A and B [128 tokens][64] tiles read
-// MN-major (16 tokens = 2048 bytes per step).
-__device__ __forceinline__ void mma_state(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi,
-                                          uint32_t b_lo, bool first) {
-  constexpr uint32_t I128 = idesc_bf16(64, 128, true, true);
-  constexpr uint32_t I64 = idesc_bf16(64, 64, true, true);
-  const uint64_t dah = sdesc(a_hi, 16, 1024), dal = sdesc(a_lo, 16, 1024);
-  const uint64_t db2 = sdesc(b_hi, b_lo - b_hi, 1024), db1 = sdesc(b_hi, 16, 1024);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    mma_bf16(d, dadd(dah, 2048 * kk), dadd(db2, 2048 * kk), I128, !first || kk > 0);
-    mma_bf16(d, dadd(dal, 2048 * kk), dadd(db1, 2048 * kk), I64, 1);
+// One 16-deep step of an NT-term product into the accumulator halves d and
+// d + 64: a0..a2 the A term descriptors, b01 the N = 128 pair [B_0 | B_1],
+// b0 and b2 single N = 64 terms.  acc = 0 overwrites on the first
+// instruction.
+template <int NT>
+__device__ __forceinline__ void mma_step(uint32_t d, uint64_t a0, uint64_t a1, uint64_t a2,
+                                         uint64_t b01, uint64_t b0, uint64_t b2, uint32_t i128,
+                                         uint32_t i64, uint32_t acc) {
+  mma_bf16(d, a0, b01, i128, acc);
+  if (NT == 2) {
+    mma_bf16(d, a1, b0, i64, 1);
+  } else {
+    mma_bf16(d, a1, b01, i128, 1);
+    mma_bf16(d, a0, b2, i64, 1);
+    mma_bf16(d + 64, a2, b0, i64, 1);
   }
 }
 
-// Token form over one chunk: D (M = 128 tokens, N = 128) = A_hi [B_hi | B_lo]
-// and D[:, 0:64] += A_lo B_hi, A a K-major [128][64] tile, B the state tile
-// pair at b (lo at b + ST): MN-major ([K = 64 rows][N]) when b_mn, else
-// K-major ([N rows][K], hi rows then lo rows).
-__device__ __forceinline__ void mma_tok(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b,
-                                        bool b_mn) {
-  const uint64_t dah = sdesc(a_hi, 16, 1024), dal = sdesc(a_lo, 16, 1024);
+// State form over one chunk, A^T B with A and B each NT term tiles
+// ([128 tokens][64], BT apart) read MN-major (16 tokens = 2048 bytes per
+// step).  Two terms stacked along M against two along N make one M = N = 128
+// instruction whose quadrants are the four products a_i b_j, i, j < 2:
+//   D   (+)= [A_0; A_1]^T [B_0 | B_1]
+// and with three terms a second accumulator 128 columns on holds
+//   D'  (+)= [A_0; A_2]^T [B_0 | B_2],
+// whose off-diagonal quadrants are a_0 b_2 and a_2 b_0 (the diagonal ones
+// are not used).
+template <int NT>
+__device__ __forceinline__ void mma_state(uint32_t d, uint32_t a, uint32_t b, bool first) {
+  constexpr uint32_t I = idesc_bf16(128, 128, true, true);
+  const uint64_t da01 = sdesc(a, BT, 1024), db01 = sdesc(b, BT, 1024);
+  const uint64_t da02 = sdesc(a, 2 * BT, 1024), db02 = sdesc(b, 2 * BT, 1024);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t o = 2048 * kk, acc = !first || kk > 0;
+    mma_bf16(d, dadd(da01, o), dadd(db01, o), I, acc);
+    if (NT == 3) mma_bf16(d + 128, dadd(da02, o), dadd(db02, o), I, acc);
+  }
+}
+
+// Token form over one chunk: D (M = 128 tokens, N = 128 as two halves) = A B,
+// A NT K-major [128][64] term tiles (BT apart), B NT state term tiles at b
+// (ST apart): MN-major ([K = 64 rows][N]) when b_mn, else K-major ([N rows][K];
+// the first two terms' rows are contiguous, which makes the N = 128 pair).
+template <int NT>
+__device__ __forceinline__ void mma_tok(uint32_t d, uint32_t a, uint32_t b, bool b_mn) {
+  const uint64_t da0 = sdesc(a, 16, 1024), da1 = sdesc(a + BT, 16, 1024),
+                 da2 = sdesc(a + 2 * BT, 16, 1024);
+  const uint64_t db0 = sdesc(b, 16, 1024), db2 = sdesc(b + 2 * ST, 16, 1024);
   if (b_mn) {
     constexpr uint32_t I128 = idesc_bf16(128, 128, false, true);
     constexpr uint32_t I64 = idesc_bf16(128, 64, false, true);
-    const uint64_t db2 = sdesc(b, ST, 1024), db1 = sdesc(b, 16, 1024);
+    const uint64_t db01 = sdesc(b, ST, 1024);
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      mma_bf16(d, dadd(dah, 32 * kk), dadd(db2, 2048 * kk), I128, kk > 0);
-      mma_bf16(d, dadd(dal, 32 * kk), dadd(db1, 2048 * kk), I64, 1);
-    }
+    for (int kk = 0; kk < 4; ++kk)
+      mma_step<NT>(d, dadd(da0, 32 * kk), dadd(da1, 32 * kk), dadd(da2, 32 * kk),
+                   dadd(db01, 2048 * kk), dadd(db0, 2048 * kk), dadd(db2, 2048 * kk), I128, I64,
+                   kk > 0);
   } else {
     constexpr uint32_t I128 = idesc_bf16(128, 128, false, false);
     constexpr uint32_t I64 = idesc_bf16(128, 64, false, false);
-    const uint64_t db = sdesc(b, 16, 1024);
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      mma_bf16(d, dadd(dah, 32 * kk), dadd(db, 32 * kk), I128, kk > 0);
-      mma_bf16(d, dadd(dal, 32 * kk), dadd(db, 32 * kk), I64, 1);
-    }
+    for (int kk = 0; kk < 4; ++kk)
+      mma_step<NT>(d, dadd(da0, 32 * kk), dadd(da1, 32 * kk), dadd(da2, 32 * kk),
+                   dadd(db0, 32 * kk), dadd(db0, 32 * kk), dadd(db2, 32 * kk), I128, I64, kk > 0);
   }
 }
 
@@ -342,24 +403,39 @@ __device__ __forceinline__ void ld_halves(uint32_t taddr, float* a, float* b) {
   tmem_ld_wait();
 }
 
-// Readout of the M = 64 state accumulator: the thread's CW columns
-// (CW (warp >> 2) ..) of row 16 (warp & 3) + lane (lanes < 16 hold rows),
-// halves added.
+// Readout of the state accumulators into P ([64][64] fp32): the thread
+// holds accumulator row 32 (warp & 3) + lane, columns CW (warp >> 2) .. and
+// the same + 64, i.e. state row (that row mod 64).  Rows < 64 are the A_0
+// quadrants (plus a_0 b_2 from the second accumulator's right half), rows
+// >= 64 the A_1 ones (plus a_2 b_0 from its left half); the upper rows are
+// written first and the lower ones added.
+template <int NT>
 __device__ __forceinline__ void state_readout(const Ctx& x, bool ok, float* P) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, qd = warp & 3, cg = warp >> 2;
-  float a[CW], b[CW];
+  const uint32_t ta = x.tm + T_STATE + ((32u * qd) << 16) + CW * cg;
+  float a[CW], b[CW], c[CW];
   if (ok) {
-    ld_halves(x.tm + T_STATE + ((32u * qd) << 16) + CW * cg, a, b);
+#pragma unroll
+    for (int j = 0; j < CW; j += 16) {
+      tmem_ld16(ta + j, a + j);
+      tmem_ld16(ta + 64 + j, b + j);
+      if (NT == 3) tmem_ld16(ta + 128 + (qd < 2 ? 64 : 0) + j, c + j);
+    }
+    tmem_ld_wait();
   } else {
 #pragma unroll
-    for (int j = 0; j < CW; ++j) a[j] = b[j] = 0.f;
+    for (int j = 0; j < CW; ++j) a[j] = b[j] = c[j] = 0.f;
   }
-  if (lane < 16) {
-    float* dst = P + (16 * qd + lane) * 64 + CW * cg;
 #pragma unroll
-    for (int j = 0; j < CW; j += 4)
-      st4(dst + j, make_float4(a[j] + b[j], a[j + 1] + b[j + 1], a[j + 2] + b[j + 2], a[j + 3] + b[j + 3]));
-  }
+  for (int j = 0; j < CW; ++j) a[j] += NT == 3 ? b[j] + c[j] : b[j];
+  float* dst = P + ((32 * qd + lane) & 63) * 64 + CW * cg;
+  if (qd < 2)
+#pragma unroll
+    for (int j = 0; j < CW; j += 4) st4(dst + j, make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]));
+  __syncthreads();
+  if (qd >= 2)
+#pragma unroll
+    for (int j = 0; j < CW; j += 4) st4(dst + j, add4(ld4(dst + j), make_float4(a[j], a[j + 1], a[j + 2], a[j + 3])));
 }
 
 // Column sums of the thread's 8 columns over all threads -> P[4096 + d].
@@ -416,13 +492,13 @@ __device__ __forceinline__ void cluster_sum(const float* P, int nseg, float4 (&m
   }
 }
 
-// Setup shared by both kernels: barriers, abort flag, TMEM.
-__device__ __forceinline__ Ctx setup(uint8_t* smraw, int* s_abort) {
+// Setup shared by both kernels: barriers (at byte o_bar), abort flag, TMEM.
+__device__ __forceinline__ Ctx setup(uint8_t* smraw, int* s_abort, int o_bar) {
   Ctx x;
   x.sm = align1024(smraw);
-  x.bar = reinterpret_cast<uint64_t*>(x.sm + O_BAR);
+  x.bar = reinterpret_cast<uint64_t*>(x.sm + o_bar);
   x.abort = s_abort;
-  uint32_t* slot = reinterpret_cast<uint32_t*>(x.sm + O_BAR + 32);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(x.sm + o_bar + 32);
   if (threadIdx.x == 0) {
     mbar_init(&x.bar[0], 1);
     mbar_init(&x.bar[1], 1);
@@ -438,13 +514,13 @@ __device__ __forceinline__ Ctx setup(uint8_t* smraw, int* s_abort) {
   return x;
 }
 
-// Teardown: no MMA in flight, no peer reading this CTA's record, TMEM freed.
+// Teardown: no MMA in flight, TMEM freed.  (No peer reads this CTA's
+// shared memory any more: the cluster barrier after the sum saw to that.)
 __device__ __forceinline__ void teardown(const Ctx& x) {
   if (threadIdx.x == 0) {
     mma_commit(&x.bar[2]);
     mbar_wait(&x.bar[2], 0, WAIT_NS);
   }
-  cluster_wait();  // matches the arrive after the cluster sum
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -462,15 +538,17 @@ __global__ void __launch_bounds__(NTX, 1)
                 const int* __restrict__ lengths, T* __restrict__ out, float* __restrict__ den,
                 float* __restrict__ S,
                 float* __restrict__ Z, int N, int H, int nseg) {
+  constexpr int NT = Terms<T>::n;
+  using L = Lay<NT>;
   extern __shared__ uint8_t smraw[];
   __shared__ int s_abort;
-  const Ctx x = setup(smraw, &s_abort);
+  const Ctx x = setup(smraw, &s_abort, L::O_BAR);
   uint8_t* sm = x.sm;
-  float* P = reinterpret_cast<float*>(sm + O_P);
-  float* sden = reinterpret_cast<float*>(sm + O_MISC);  // [2][128]
+  float* P = reinterpret_cast<float*>(sm + L::O_ST);     // partial record, then
+  uint8_t* SH = sm + L::O_ST;                            // the S terms 0, 1
+  float* sden = reinterpret_cast<float*>(sm + L::O_MISC);  // [2][128]
   float* sz = sden + 2 * CH;                             // Z [64]
   float* scol = sz + 64;                                 // [warps][64]
-  uint8_t* SH = sm + O_ST;                               // S hi | lo
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31, qd = warp & 3, cg = warp >> 2;
   const int p = static_cast<int>(cluster_rank()), bh = blockIdx.x / nseg;
   const Rows w = my_rows(lengths, bh / H, N, p, nseg);
@@ -487,7 +565,7 @@ __global__ void __launch_bounds__(NTX, 1)
   // ---- phase 1: partial S~ and Z
   float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int c = 0; c < w.nch; ++c, ++g) {
-    uint8_t* B0 = sm + O_BUF + (g & 1) * BUF;  // K hi, K lo, V hi, V lo
+    uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;  // phi(K) terms, V terms
     const long n0 = w.r0 + static_cast<long>(c) * CH;
     const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
 #pragma unroll
@@ -501,8 +579,8 @@ __global__ void __launch_bounds__(NTX, 1)
         a[j] = row < nv ? phi(a[j]) : 0.f;
         cs[j] += a[j];
       }
-      put_split8(B0, B0 + BT, row, c8, a);
-      put_split8(B0 + 2 * BT, B0 + 3 * BT, row, c8, b);
+      put_split8<NT>(B0, BT, row, c8, a);
+      put_split8<NT>(B0 + NT * BT, BT, row, c8, b);
     }
     if (c + 1 < w.nch) {
       fetch(ra, k + hq, n0 + CH, w.r1);
@@ -514,7 +592,7 @@ __global__ void __launch_bounds__(NTX, 1)
     if (t == 0 && !s_abort) {
       tc_fence_after();
       const uint32_t a0 = saddr(B0);
-      mma_state(x.tm + T_STATE, a0, a0 + BT, a0 + 2 * BT, a0 + 3 * BT, c == 0);
+      mma_state<NT>(x.tm + T_STATE, a0, a0 + NT * BT, c == 0);
       mma_commit(&x.bar[g & 1]);
     }
     if (c > 0) wait_chunk(x, g - 1);  // frees the other buffer
@@ -522,7 +600,7 @@ __global__ void __launch_bounds__(NTX, 1)
   {
     const bool ok = w.nch > 0 && wait_chunk(x, g - 1);
     tc_fence_after();
-    state_readout(x, ok, P);
+    state_readout<NT>(x, ok, P);
   }
   colsum_to_record(cs, scol, P);
   tc_fence_before();
@@ -538,18 +616,20 @@ __global__ void __launch_bounds__(NTX, 1)
   {
     float4 m[NPC], zv;
     cluster_sum(P, nseg, m, zv);
+    cluster_arrive();  // this CTA no longer reads the others' records
+    if (p == 0) {
+#pragma unroll
+      for (int i = 0; i < NPC; ++i) st4(S + static_cast<long>(bh) * 4096 + 4 * (t + NTX * i), m[i]);
+      if (t < 16) st4(Z + static_cast<long>(bh) * 64 + 4 * t, zv);
+    }
+    if (t < 16) st4(sz + 4 * t, zv);
+    cluster_wait();  // nor does any other CTA read this one's: the S tiles replace it
 #pragma unroll
     for (int i = 0; i < NPC; ++i) {
       const int e = t + NTX * i;
-      put_split4(SH, SH + ST, e >> 4, 4 * (e & 15), m[i]);
-      if (p == 0) st4(S + static_cast<long>(bh) * 4096 + 4 * e, m[i]);
-    }
-    if (t < 16) {
-      st4(sz + 4 * t, zv);
-      if (p == 0) st4(Z + static_cast<long>(bh) * 64 + 4 * t, zv);
+      put_split4<2>(SH, ST, e >> 4, 4 * (e & 15), m[i]);
     }
   }
-  cluster_arrive();  // this CTA no longer reads the others' records
   fence_proxy_async();
   __syncthreads();
   float zc[8];
@@ -558,7 +638,7 @@ __global__ void __launch_bounds__(NTX, 1)
   const uint32_t tok0 = x.tm + T_TOK;
   for (int c = 0; c <= w.nch; ++c) {
     if (c < w.nch) {
-      uint8_t* B0 = sm + O_BUF + (g & 1) * BUF;  // Q hi, Q lo
+      uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;  // phi(Q) terms 0, 1
       const long n0 = w.r0 + static_cast<long>(c) * CH;
       const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
 #pragma unroll
@@ -577,7 +657,7 @@ __global__ void __launch_bounds__(NTX, 1)
           sden[(g & 1) * CH + row] = dp;
           if (den != nullptr && row < nv) den[hn + n0 + row] = dp;
         }
-        put_split8(B0, B0 + BT, row, c8, a);
+        put_split8<2>(B0, BT, row, c8, a);
       }
       if (c + 1 < w.nch) fetch(ra, q + hq, n0 + CH, w.r1);
       fence_proxy_async();
@@ -586,7 +666,7 @@ __global__ void __launch_bounds__(NTX, 1)
       if (t == 0 && !s_abort) {
         tc_fence_after();
         const uint32_t a0 = saddr(B0);
-        mma_tok(tok0 + 128 * (g & 1), a0, a0 + BT, saddr(SH), true);
+        mma_tok<2>(tok0 + 128 * (g & 1), a0, saddr(SH), true);
         mma_commit(&x.bar[g & 1]);
       }
       ++g;
@@ -625,16 +705,18 @@ __global__ void __launch_bounds__(NTX, 1)
                 const float* __restrict__ S, const float* __restrict__ Z,
                 const T* __restrict__ gr, T* __restrict__ dq, T* __restrict__ dk,
                 T* __restrict__ dv, int N, int H, int nseg) {
+  constexpr int NT = Terms<T>::n;
+  using L = Lay<NT>;
   extern __shared__ uint8_t smraw[];
   __shared__ int s_abort;
-  const Ctx x = setup(smraw, &s_abort);
+  const Ctx x = setup(smraw, &s_abort, L::O_BAR);
   uint8_t* sm = x.sm;
-  float* P = reinterpret_cast<float*>(sm + O_P);
-  float* sinv = reinterpret_cast<float*>(sm + O_MISC);  // 1 / den [2][128]
+  uint8_t* SH = sm + L::O_ST;  // phase 1: the S terms; then the partial record; phase 2: the R terms
+  float* P = reinterpret_cast<float*>(SH);
+  float* sinv = reinterpret_cast<float*>(sm + L::O_MISC);  // 1 / den [2][128]
   float* sz = sinv + 4 * CH;                             // phase 1: Z; phase 2: r
   float* scol = sz + 64;                                 // [warps][64]
   float* spart = scol + (NTX / 32) * 64;                 // [NCG][128]
-  uint8_t* SH = sm + O_ST;  // phase 1: S hi | lo; phase 2: R hi | lo
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31, qd = warp & 3, cg = warp >> 2;
   const int p = static_cast<int>(cluster_rank()), bh = blockIdx.x / nseg;
   const Rows w = my_rows(lengths, bh / H, N, p, nseg);
@@ -645,11 +727,11 @@ __global__ void __launch_bounds__(NTX, 1)
   Raw<T> ra, rb;
   float rd[NU];
   if (w.nch > 0) fetch_bwd1(ra, rb, rd, q + hq, gr + hq, den + hn, w.r0, w.r1);
-  // S (the forward's state) as hi | lo operand tiles; Z
+  // S (the forward's state) as NT operand term tiles; Z
 #pragma unroll
   for (int i = 0; i < NPC; ++i) {
     const int e = t + NTX * i;
-    put_split4(SH, SH + ST, e >> 4, 4 * (e & 15), ld4(S + static_cast<long>(bh) * 4096 + 4 * e));
+    put_split4<NT>(SH, ST, e >> 4, 4 * (e & 15), ld4(S + static_cast<long>(bh) * 4096 + 4 * e));
   }
   if (t < 64) sz[t] = Z[static_cast<long>(bh) * 64 + t];
   fence_proxy_async();
@@ -662,7 +744,7 @@ __global__ void __launch_bounds__(NTX, 1)
   const uint32_t tok0 = x.tm + T_TOK;
   for (int c = 0; c <= w.nch; ++c) {
     if (c < w.nch) {
-      uint8_t* B0 = sm + O_BUF + (g & 1) * BUF;  // Q hi, Q lo, gt hi, gt lo
+      uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;  // phi(Q) terms, gt terms
       const long n0 = w.r0 + static_cast<long>(c) * CH;
       const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
 #pragma unroll
@@ -679,8 +761,8 @@ __global__ void __launch_bounds__(NTX, 1)
           b[j] *= inv;
         }
         if (c8 == 0) sinv[(g & 1) * CH + row] = inv;
-        put_split8(B0, B0 + BT, row, c8, a);
-        put_split8(B0 + 2 * BT, B0 + 3 * BT, row, c8, b);
+        put_split8<NT>(B0, BT, row, c8, a);
+        put_split8<NT>(B0 + NT * BT, BT, row, c8, b);
       }
       if (c + 1 < w.nch) fetch_bwd1(ra, rb, rd, q + hq, gr + hq, den + hn, n0 + CH, w.r1);
       fence_proxy_async();
@@ -689,8 +771,8 @@ __global__ void __launch_bounds__(NTX, 1)
       if (t == 0 && !s_abort) {
         tc_fence_after();
         const uint32_t a0 = saddr(B0);
-        mma_state(x.tm + T_STATE, a0, a0 + BT, a0 + 2 * BT, a0 + 3 * BT, c == 0);
-        mma_tok(tok0 + 128 * (g & 1), a0 + 2 * BT, a0 + 3 * BT, saddr(SH), false);
+        mma_state<NT>(x.tm + T_STATE, a0, a0 + NT * BT, c == 0);
+        mma_tok<NT>(tok0 + 128 * (g & 1), a0 + NT * BT, saddr(SH), false);
         mma_commit(&x.bar[g & 1]);
       }
       ++g;
@@ -702,7 +784,7 @@ __global__ void __launch_bounds__(NTX, 1)
       const long n0 = w.r0 + static_cast<long>(c - 1) * CH;
       const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
       const int row = 32 * qd + lane;
-      const uint8_t* B0 = sm + O_BUF + (ge & 1) * BUF;
+      const uint8_t* B0 = sm + L::O_BUF + (ge & 1) * L::BUF;
       float a[CW], b[CW], f[CW];
       if (ok) {
         ld_halves(tok0 + 128 * (ge & 1) + ((32u * qd) << 16) + CW * cg, a, b);
@@ -710,7 +792,7 @@ __global__ void __launch_bounds__(NTX, 1)
 #pragma unroll
         for (int j = 0; j < CW; ++j) a[j] = b[j] = 0.f;
       }
-      get_row<CW>(B0, B0 + BT, row, CW * cg, f);  // phi(Q) (0 on invalid rows); phi' = min(phi, 1)
+      get_row<CW, NT>(B0, BT, row, CW * cg, f);  // phi(Q) (0 on invalid rows); phi' = min(phi, 1)
       float part = 0.f;
 #pragma unroll
       for (int j = 0; j < CW; ++j) {
@@ -742,7 +824,7 @@ __global__ void __launch_bounds__(NTX, 1)
   {
     const bool ok = w.nch > 0 && !*reinterpret_cast<volatile int*>(x.abort);
     tc_fence_after();
-    state_readout(x, __all_sync(0xffffffffu, ok), P);
+    state_readout<NT>(x, __all_sync(0xffffffffu, ok), P);
   }
   // r: the thread's CW columns summed over its warp's lanes, then over the
   // four lane quarters of its column group
@@ -779,20 +861,21 @@ __global__ void __launch_bounds__(NTX, 1)
   {
     float4 m[NPC], rv;
     cluster_sum(P, nseg, m, rv);
+    cluster_arrive();  // this CTA no longer reads the others' records
+    if (t < 16) st4(sz + 4 * t, rv);
+    cluster_wait();  // nor does any other CTA read this one's: the R tiles replace it
 #pragma unroll
     for (int i = 0; i < NPC; ++i) {
       const int e = t + NTX * i;
-      put_split4(SH, SH + ST, e >> 4, 4 * (e & 15), m[i]);
+      put_split4<NT>(SH, ST, e >> 4, 4 * (e & 15), m[i]);
     }
-    if (t < 16) st4(sz + 4 * t, rv);
   }
-  cluster_arrive();
   fence_proxy_async();
   __syncthreads();
   const uint32_t t2 = x.tm;  // phase 2: buffer b uses columns 256 b .. 256 b + 255
   for (int c = 0; c <= w.nch; ++c) {
     if (c < w.nch) {
-      uint8_t* B0 = sm + O_BUF + (g & 1) * BUF;  // V hi, V lo, K hi, K lo
+      uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;  // V terms, phi(K) terms 0, 1
       const long n0 = w.r0 + static_cast<long>(c) * CH;
       const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
 #pragma unroll
@@ -803,8 +886,8 @@ __global__ void __launch_bounds__(NTX, 1)
         unpack(rb, i, b);
 #pragma unroll
         for (int j = 0; j < 8; ++j) b[j] = row < nv ? phi(b[j]) : 0.f;
-        put_split8(B0, B0 + BT, row, c8, a);
-        put_split8(B0 + 2 * BT, B0 + 3 * BT, row, c8, b);
+        put_split8<NT>(B0, BT, row, c8, a);
+        put_split8<2>(B0 + NT * BT, BT, row, c8, b);
       }
       if (c + 1 < w.nch) {
         fetch(ra, v + hq, n0 + CH, w.r1);
@@ -816,8 +899,8 @@ __global__ void __launch_bounds__(NTX, 1)
       if (t == 0 && !s_abort) {
         tc_fence_after();
         const uint32_t a0 = saddr(B0), d0 = t2 + 256 * (g & 1);
-        mma_tok(d0, a0, a0 + BT, saddr(SH), false);                    // V [R_hi; R_lo]^T
-        mma_tok(d0 + 128, a0 + 2 * BT, a0 + 3 * BT, saddr(SH), true);  // phi(K) [R_hi | R_lo]
+        mma_tok<NT>(d0, a0, saddr(SH), false);                // V R^T
+        mma_tok<2>(d0 + 128, a0 + NT * BT, saddr(SH), true);  // phi(K) R
         mma_commit(&x.bar[g & 1]);
       }
       ++g;
@@ -831,12 +914,12 @@ __global__ void __launch_bounds__(NTX, 1)
         const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
         const int row = 32 * qd + lane;
         const uint32_t acc = t2 + 256 * (ge & 1) + ((32u * qd) << 16) + CW * cg;
-        const uint8_t* B0 = sm + O_BUF + (ge & 1) * BUF;
+        const uint8_t* B0 = sm + L::O_BUF + (ge & 1) * L::BUF;
         float a[CW], b[CW];
         ld_halves(acc, a, b);
         if (row < nv) {
           float f[CW];
-          get_row<CW>(B0 + 2 * BT, B0 + 3 * BT, row, CW * cg, f);  // phi(K)
+          get_row<CW, 2>(B0 + NT * BT, BT, row, CW * cg, f);  // phi(K) to 2^-18, for phi'
           T* dst = dk + hq + (n0 + row) * 64 + CW * cg;
 #pragma unroll
           for (int j = 0; j < CW; j += 4) {
@@ -863,13 +946,13 @@ __global__ void __launch_bounds__(NTX, 1)
 }
 
 template <typename K, typename... Args>
-cudaError_t launch_cluster(K kernel, int nseg, int BH, cudaStream_t st, Args... args) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TC);
+cudaError_t launch_cluster(K kernel, int smem, int nseg, int BH, cudaStream_t st, Args... args) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nseg) * static_cast<unsigned>(BH));
   cfg.blockDim = dim3(NTX);
-  cfg.dynamicSmemBytes = SMEM_TC;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -886,7 +969,7 @@ cudaError_t launch_cluster(K kernel, int nseg, int BH, cudaStream_t st, Args... 
 template <typename T>
 cudaError_t run_fwd(const T* q, const T* k, const T* v, const int* lengths, T* out, float* den,
                     float* S, float* Z, const Shape& s, int nseg, cudaStream_t st) {
-  return launch_cluster(k_nc_fwd_tc<T>, nseg, s.B * s.H, st, q, k, v, lengths, out, den, S, Z,
+  return launch_cluster(k_nc_fwd_tc<T>, Lay<Terms<T>::n>::SMEM, nseg, s.B * s.H, st, q, k, v, lengths, out, den, S, Z,
                         s.N, s.H, nseg);
 }
 
@@ -894,7 +977,7 @@ template <typename T>
 cudaError_t run_bwd(const T* q, const T* k, const T* v, const int* lengths, const float* den,
                     const float* S, const float* Z, const T* dout, T* dq, T* dk, T* dv,
                     const Shape& s, int nseg, cudaStream_t st) {
-  return launch_cluster(k_nc_bwd_tc<T>, nseg, s.B * s.H, st, q, k, v, lengths, den, S, Z, dout, dq,
+  return launch_cluster(k_nc_bwd_tc<T>, Lay<Terms<T>::n>::SMEM, nseg, s.B * s.H, st, q, k, v, lengths, den, S, Z, dout, dq,
                         dk, dv, s.N, s.H, nseg);
 }
 

@@ -136,6 +136,34 @@ def test_noncausal_small(cuda, linattn, B, H, N, D, M, dtype, lr):
     check_noncausal(linattn, cuda, B, H, N, D, M, dtype, 2000 + N, lr)
 
 
+@pytest.mark.parametrize("D,M,dtype", [(64, 64, "f32"), (64, 64, "bf16"), (32, 32, "f32")])
+@pytest.mark.parametrize("raw", [(0, 0, 0, 0), (-5, 0, 301, 1000), (300, -1, 1, 299)])
+def test_noncausal_length_edges(cuda, linattn, D, M, dtype, raw):
+    """Every sequence empty, and lengths outside [0, N], which the ABI clamps:
+    the GPU gets the raw lengths, the oracle the clamped ones."""
+    B, H, N = 4, 2, 300
+    _, q, k, v, g = noncausal_inputs(B, H, N, D, M, dtype, 4242, None)
+    raw_l = torch.tensor(raw, dtype=torch.int32)
+    lens = raw_l.clamp(0, N)
+    qd, kd, vd, gd = _to(cuda, q, k, v, g)
+    out, den, S, Z = linattn.noncausal_fwd(qd, kd, vd, raw_l.to(cuda))
+    dq, dk, dv = linattn.noncausal_bwd(qd, kd, vd, raw_l.to(cuda), out, den, S, Z, gd)
+    torch.cuda.synchronize()
+    o_ref, den_ref, S_ref, Z_ref = oracle.noncausal_fwd(q, k, v, lens)
+    dq_ref, dk_ref, dv_ref = oracle.noncausal_bwd(q, k, v, g, lens)
+    tol = TOL[dtype]
+    errs = {"out": rel_err(out, o_ref), "den": rel_err(den, den_ref), "S": rel_err(S, S_ref),
+            "Z": rel_err(Z, Z_ref), "dq": rel_err(dq, dq_ref), "dk": rel_err(dk, dk_ref),
+            "dv": rel_err(dv, dv_ref)}
+    bad = {k_: e for k_, e in errs.items() if not e <= tol}
+    assert not bad, f"lengths {raw}, D={D} M={M} {dtype}: {errs}"
+    for b, L in enumerate(lens.tolist()):
+        for t in (out, den, dq, dk, dv):
+            assert torch.all(t[b, :, L:] == 0)
+        if L == 0:
+            assert torch.all(S[b] == 0) and torch.all(Z[b] == 0)
+
+
 def test_noncausal_workload(cuda, linattn):
     w = WORKLOADS["noncausal_speech_f32"]
     errs = check_noncausal(linattn, cuda, w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed, w.len_range)
