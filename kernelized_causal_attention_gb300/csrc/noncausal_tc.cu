@@ -77,18 +77,54 @@ struct Terms<float> {
   static constexpr int n = 3;
 };
 
-// Shared memory for NT-term operands, bytes from a 1024-aligned base.
+// Shared memory for NT-term operands, bytes from a 1024-aligned base.  A
+// chunk's two operands X and Y take four tiles of the chunk's buffer: X's
+// terms (the operand an epilogue reads back, if any) and Y's first term, or
+// both terms of each for NT = 2.  For NT = 3, Y's terms 1 and 2 go to one
+// pair of tiles that both buffers share: a chunk writes them once the MMAs
+// of the chunk before have finished.  Ten tiles instead of twelve keep the
+// CTA under 196 KB, which leaves L1 about 60 KB (at 228 KB of shared memory
+// it keeps 28 KB and throttles the register prefetch of the next chunk).
 template <int NT>
 struct Lay {
-  static constexpr int BUF = 2 * NT * BT;  // one operand buffer: two tensors of NT tiles
+  static constexpr int BUF = 4 * BT;       // one operand buffer: four term tiles
   static constexpr int O_BUF = 0;          // two operand buffers
-  static constexpr int O_ST = 2 * BUF;     // state tiles, NT x [64][64]; or the partial record (fp32)
+  static constexpr int O_SHY = 2 * BUF;    // NT = 3: Y's terms 1, 2 (one pair for both buffers)
+  static constexpr int O_ST = O_SHY + (NT == 3 ? 2 * BT : 0);  // state tiles, NT x [64][64]; or the partial record (fp32)
   static constexpr int N_ST = NT * ST > 4 * PREC ? NT * ST : (4 * PREC + 1023) / 1024 * 1024;
   static constexpr int O_MISC = O_ST + N_ST;  // fp32: per-row [2][128] x 2, vector [64], sums [warps][64], [4][128]
   static constexpr int O_BAR = O_MISC + 4 * N_MISC;  // mbarriers: MMA done per buffer, final drain; TMEM address
   static constexpr int SMEM = O_BAR + 64 + 1024;     // + alignment slack
 };
-static_assert(Lay<3>::SMEM <= 232448 - 64, "shared memory of the three-term layout");
+static_assert(Lay<3>::SMEM + 16 + 1024 <= 196 * 1024, "the three-term layout fits the 196 KB carveout");
+static_assert(Lay<2>::SMEM + 16 + 1024 <= 164 * 1024, "the two-term layout fits the 164 KB carveout");
+
+// The term tiles of one operand of one chunk.
+template <int NT>
+struct Terms8 {
+  uint8_t* t[NT];
+};
+// X: NT consecutive tiles from b; Y: see Lay.
+template <int NT>
+__device__ __forceinline__ Terms8<NT> x_tiles(uint8_t* b) {
+  Terms8<NT> r;
+#pragma unroll
+  for (int i = 0; i < NT; ++i) r.t[i] = b + i * BT;
+  return r;
+}
+template <int NT>
+__device__ __forceinline__ Terms8<NT> y_tiles(uint8_t* b, uint8_t* shy) {
+  Terms8<NT> r;
+  if constexpr (NT == 3) {
+    r.t[0] = b + 3 * BT;
+    r.t[1] = shy;
+    r.t[2] = shy + BT;
+  } else {
+    r.t[0] = b + 2 * BT;
+    r.t[1] = b + 3 * BT;
+  }
+  return r;
+}
 
 // TMEM columns
 constexpr uint32_t T_STATE = 0;      // the state accumulators (M = 128, 2 x 128 columns)
@@ -147,17 +183,16 @@ __device__ __forceinline__ void split(float x0, float x1, uint32_t (&w)[NT]) {
   }
 }
 
-// Columns 8 c8 .. 8 c8 + 7 of row `row` into the swizzled term tiles t,
-// t + stride, ... (NT of them).
+// Columns 8 c8 .. 8 c8 + 7 of row `row` into the swizzled term tiles.
 template <int NT>
-__device__ __forceinline__ void put_split8(uint8_t* t, int stride, int row, int c8, const float* x) {
+__device__ __forceinline__ void put_split8(const Terms8<NT>& tl, int row, int c8, const float* x) {
   uint32_t w[4][NT];
 #pragma unroll
   for (int j = 0; j < 4; ++j) split<NT>(x[2 * j], x[2 * j + 1], w[j]);
   const uint32_t off = static_cast<uint32_t>(row) * 128u + ((static_cast<uint32_t>(c8) ^ (row & 7u)) << 4);
 #pragma unroll
   for (int i = 0; i < NT; ++i)
-    *reinterpret_cast<uint4*>(t + i * stride + off) = make_uint4(w[0][i], w[1][i], w[2][i], w[3][i]);
+    *reinterpret_cast<uint4*>(tl.t[i] + off) = make_uint4(w[0][i], w[1][i], w[2][i], w[3][i]);
 }
 
 // Four values (columns col .. col + 3, col a multiple of 4) of row `row`.
@@ -282,12 +317,8 @@ __device__ __forceinline__ void st_out(__nv_bfloat16* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = make_uint2(bits(a), bits(b));
 }
 
-// The backward's phase-1 share of a chunk: q, dout and den.
-template <typename T>
-__device__ __forceinline__ void fetch_bwd1(Raw<T>& ra, Raw<T>& rb, float (&rd)[NU], const T* qh,
-                                           const T* gh, const float* dh, long n0, long ne) {
-  fetch(ra, qh, n0, ne);
-  fetch(rb, gh, n0, ne);
+// The thread's den values of rows n0 .. n0 + 127 (1 at or past ne).
+__device__ __forceinline__ void fetch_den(float (&rd)[NU], const float* dh, long n0, long ne) {
 #pragma unroll
   for (int i = 0; i < NU; ++i) {
     const long row = n0 + unit_row(i);
@@ -322,20 +353,35 @@ __device__ __forceinline__ void mma_step(uint32_t d, uint64_t a0, uint64_t a1, u
   }
 }
 
+// Shared-memory addresses of an operand's term tiles.
+struct TermAddr {
+  uint32_t t[3];  // unused terms repeat the last one
+};
+template <int NT>
+__device__ __forceinline__ TermAddr taddr(const Terms8<NT>& tl) {
+  TermAddr r;
+#pragma unroll
+  for (int i = 0; i < 3; ++i) r.t[i] = static_cast<uint32_t>(__cvta_generic_to_shared(tl.t[i < NT ? i : NT - 1]));
+  return r;
+}
+
 // State form over one chunk, A^T B with A and B each NT term tiles
-// ([128 tokens][64], BT apart) read MN-major (16 tokens = 2048 bytes per
-// step).  Two terms stacked along M against two along N make one M = N = 128
-// instruction whose quadrants are the four products a_i b_j, i, j < 2:
+// ([128 tokens][64]) read MN-major (16 tokens = 2048 bytes per step).  Two
+// terms stacked along M against two along N (the second tile of a pair is
+// reached by the descriptor's leading offset, so it only has to lie above
+// the first) make one M = N = 128 instruction whose quadrants are the four
+// products a_i b_j, i, j < 2:
 //   D   (+)= [A_0; A_1]^T [B_0 | B_1]
 // and with three terms a second accumulator 128 columns on holds
 //   D'  (+)= [A_0; A_2]^T [B_0 | B_2],
 // whose off-diagonal quadrants are a_0 b_2 and a_2 b_0 (the diagonal ones
 // are not used).
 template <int NT>
-__device__ __forceinline__ void mma_state(uint32_t d, uint32_t a, uint32_t b, bool first) {
+__device__ __forceinline__ void mma_state(uint32_t d, const TermAddr& a, const TermAddr& b,
+                                          bool first) {
   constexpr uint32_t I = idesc_bf16(128, 128, true, true);
-  const uint64_t da01 = sdesc(a, BT, 1024), db01 = sdesc(b, BT, 1024);
-  const uint64_t da02 = sdesc(a, 2 * BT, 1024), db02 = sdesc(b, 2 * BT, 1024);
+  const uint64_t da01 = sdesc(a.t[0], a.t[1] - a.t[0], 1024), db01 = sdesc(b.t[0], b.t[1] - b.t[0], 1024);
+  const uint64_t da02 = sdesc(a.t[0], a.t[2] - a.t[0], 1024), db02 = sdesc(b.t[0], b.t[2] - b.t[0], 1024);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t o = 2048 * kk, acc = !first || kk > 0;
@@ -345,13 +391,13 @@ __device__ __forceinline__ void mma_state(uint32_t d, uint32_t a, uint32_t b, bo
 }
 
 // Token form over one chunk: D (M = 128 tokens, N = 128 as two halves) = A B,
-// A NT K-major [128][64] term tiles (BT apart), B NT state term tiles at b
-// (ST apart): MN-major ([K = 64 rows][N]) when b_mn, else K-major ([N rows][K];
-// the first two terms' rows are contiguous, which makes the N = 128 pair).
+// A NT K-major [128][64] term tiles, B NT state term tiles at b (ST apart):
+// MN-major ([K = 64 rows][N]) when b_mn, else K-major ([N rows][K]; the
+// first two terms' rows are contiguous, which makes the N = 128 pair).
 template <int NT>
-__device__ __forceinline__ void mma_tok(uint32_t d, uint32_t a, uint32_t b, bool b_mn) {
-  const uint64_t da0 = sdesc(a, 16, 1024), da1 = sdesc(a + BT, 16, 1024),
-                 da2 = sdesc(a + 2 * BT, 16, 1024);
+__device__ __forceinline__ void mma_tok(uint32_t d, const TermAddr& a, uint32_t b, bool b_mn) {
+  const uint64_t da0 = sdesc(a.t[0], 16, 1024), da1 = sdesc(a.t[1], 16, 1024),
+                 da2 = sdesc(a.t[2], 16, 1024);
   const uint64_t db0 = sdesc(b, 16, 1024), db2 = sdesc(b + 2 * ST, 16, 1024);
   if (b_mn) {
     constexpr uint32_t I128 = idesc_bf16(128, 128, false, true);
@@ -565,37 +611,39 @@ __global__ void __launch_bounds__(NTX, 1)
   // ---- phase 1: partial S~ and Z
   float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int c = 0; c < w.nch; ++c, ++g) {
-    uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;  // phi(K) terms, V terms
+    uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;
+    const Terms8<NT> tx = x_tiles<NT>(B0), ty = y_tiles<NT>(B0, sm + L::O_SHY);  // phi(K), V
     const long n0 = w.r0 + static_cast<long>(c) * CH;
     const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
 #pragma unroll
     for (int i = 0; i < NU; ++i) {
       const int row = unit_row(i);
-      float a[8], b[8];
+      float a[8];
       unpack(ra, i, a);
-      unpack(rb, i, b);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         a[j] = row < nv ? phi(a[j]) : 0.f;
         cs[j] += a[j];
       }
-      put_split8<NT>(B0, BT, row, c8, a);
-      put_split8<NT>(B0 + NT * BT, BT, row, c8, b);
+      put_split8<NT>(tx, row, c8, a);
     }
-    if (c + 1 < w.nch) {
-      fetch(ra, k + hq, n0 + CH, w.r1);
-      fetch(rb, v + hq, n0 + CH, w.r1);
+    if (c + 1 < w.nch) fetch(ra, k + hq, n0 + CH, w.r1);
+    if (c > 0) wait_chunk(x, g - 1);  // the MMAs of the chunk before: frees the shared tiles
+#pragma unroll
+    for (int i = 0; i < NU; ++i) {
+      float b[8];
+      unpack(rb, i, b);
+      put_split8<NT>(ty, unit_row(i), c8, b);
     }
+    if (c + 1 < w.nch) fetch(rb, v + hq, n0 + CH, w.r1);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     if (t == 0 && !s_abort) {
       tc_fence_after();
-      const uint32_t a0 = saddr(B0);
-      mma_state<NT>(x.tm + T_STATE, a0, a0 + NT * BT, c == 0);
+      mma_state<NT>(x.tm + T_STATE, taddr(tx), taddr(ty), c == 0);
       mma_commit(&x.bar[g & 1]);
     }
-    if (c > 0) wait_chunk(x, g - 1);  // frees the other buffer
   }
   {
     const bool ok = w.nch > 0 && wait_chunk(x, g - 1);
@@ -638,7 +686,8 @@ __global__ void __launch_bounds__(NTX, 1)
   const uint32_t tok0 = x.tm + T_TOK;
   for (int c = 0; c <= w.nch; ++c) {
     if (c < w.nch) {
-      uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;  // phi(Q) terms 0, 1
+      uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;
+      const Terms8<2> tx = x_tiles<2>(B0);  // phi(Q), two terms
       const long n0 = w.r0 + static_cast<long>(c) * CH;
       const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
 #pragma unroll
@@ -657,7 +706,7 @@ __global__ void __launch_bounds__(NTX, 1)
           sden[(g & 1) * CH + row] = dp;
           if (den != nullptr && row < nv) den[hn + n0 + row] = dp;
         }
-        put_split8<2>(B0, BT, row, c8, a);
+        put_split8<2>(tx, row, c8, a);
       }
       if (c + 1 < w.nch) fetch(ra, q + hq, n0 + CH, w.r1);
       fence_proxy_async();
@@ -665,8 +714,7 @@ __global__ void __launch_bounds__(NTX, 1)
       __syncthreads();
       if (t == 0 && !s_abort) {
         tc_fence_after();
-        const uint32_t a0 = saddr(B0);
-        mma_tok<2>(tok0 + 128 * (g & 1), a0, saddr(SH), true);
+        mma_tok<2>(tok0 + 128 * (g & 1), taddr(tx), saddr(SH), true);
         mma_commit(&x.bar[g & 1]);
       }
       ++g;
@@ -726,7 +774,11 @@ __global__ void __launch_bounds__(NTX, 1)
   uint32_t g = 0;
   Raw<T> ra, rb;
   float rd[NU];
-  if (w.nch > 0) fetch_bwd1(ra, rb, rd, q + hq, gr + hq, den + hn, w.r0, w.r1);
+  if (w.nch > 0) {
+    fetch(ra, q + hq, w.r0, w.r1);
+    fetch(rb, gr + hq, w.r0, w.r1);
+    fetch_den(rd, den + hn, w.r0, w.r1);
+  }
   // S (the forward's state) as NT operand term tiles; Z
 #pragma unroll
   for (int i = 0; i < NPC; ++i) {
@@ -744,35 +796,44 @@ __global__ void __launch_bounds__(NTX, 1)
   const uint32_t tok0 = x.tm + T_TOK;
   for (int c = 0; c <= w.nch; ++c) {
     if (c < w.nch) {
-      uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;  // phi(Q) terms, gt terms
+      uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;
+      const Terms8<NT> tx = x_tiles<NT>(B0), ty = y_tiles<NT>(B0, sm + L::O_SHY);  // phi(Q), gt
       const long n0 = w.r0 + static_cast<long>(c) * CH;
       const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
 #pragma unroll
       for (int i = 0; i < NU; ++i) {
         const int row = unit_row(i);
-        const bool ok = row < nv;
-        float a[8], b[8];
+        float a[8];
         unpack(ra, i, a);
-        unpack(rb, i, b);
-        const float inv = ok ? 1.f / rd[i] : 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          a[j] = ok ? phi(a[j]) : 0.f;
-          b[j] *= inv;
-        }
-        if (c8 == 0) sinv[(g & 1) * CH + row] = inv;
-        put_split8<NT>(B0, BT, row, c8, a);
-        put_split8<NT>(B0 + NT * BT, BT, row, c8, b);
+        for (int j = 0; j < 8; ++j) a[j] = row < nv ? phi(a[j]) : 0.f;
+        put_split8<NT>(tx, row, c8, a);
       }
-      if (c + 1 < w.nch) fetch_bwd1(ra, rb, rd, q + hq, gr + hq, den + hn, n0 + CH, w.r1);
+      if (c + 1 < w.nch) fetch(ra, q + hq, n0 + CH, w.r1);
+      if (c > 0) wait_chunk(x, g - 1);  // the MMAs of the chunk before: frees the shared tiles
+#pragma unroll
+      for (int i = 0; i < NU; ++i) {
+        const int row = unit_row(i);
+        const float inv = row < nv ? 1.f / rd[i] : 0.f;
+        float b[8];
+        unpack(rb, i, b);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) b[j] *= inv;
+        if (c8 == 0) sinv[(g & 1) * CH + row] = inv;
+        put_split8<NT>(ty, row, c8, b);
+      }
+      if (c + 1 < w.nch) {
+        fetch(rb, gr + hq, n0 + CH, w.r1);
+        fetch_den(rd, den + hn, n0 + CH, w.r1);
+      }
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
       if (t == 0 && !s_abort) {
         tc_fence_after();
-        const uint32_t a0 = saddr(B0);
-        mma_state<NT>(x.tm + T_STATE, a0, a0 + NT * BT, c == 0);
-        mma_tok<NT>(tok0 + 128 * (g & 1), a0 + NT * BT, saddr(SH), false);
+        const TermAddr ay = taddr(ty);
+        mma_state<NT>(x.tm + T_STATE, taddr(tx), ay, c == 0);
+        mma_tok<NT>(tok0 + 128 * (g & 1), ay, saddr(SH), false);
         mma_commit(&x.bar[g & 1]);
       }
       ++g;
@@ -875,32 +936,42 @@ __global__ void __launch_bounds__(NTX, 1)
   const uint32_t t2 = x.tm;  // phase 2: buffer b uses columns 256 b .. 256 b + 255
   for (int c = 0; c <= w.nch; ++c) {
     if (c < w.nch) {
-      uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;  // V terms, phi(K) terms 0, 1
+      uint8_t* B0 = sm + L::O_BUF + (g & 1) * L::BUF;
+      // phi(K): two terms in tiles 2, 3 (the epilogue reads them back);
+      // V: tiles 0, 1 and, for three terms, the first shared tile
+      const Terms8<2> tk = x_tiles<2>(B0 + 2 * BT);
+      Terms8<NT> tv;
+      tv.t[0] = B0;
+      tv.t[1] = B0 + BT;
+      if constexpr (NT == 3) tv.t[2] = sm + L::O_SHY;
       const long n0 = w.r0 + static_cast<long>(c) * CH;
       const int nv = static_cast<int>(min(static_cast<long>(CH), w.r1 - n0));
 #pragma unroll
       for (int i = 0; i < NU; ++i) {
         const int row = unit_row(i);
-        float a[8], b[8];
-        unpack(ra, i, a);
+        float b[8];
         unpack(rb, i, b);
 #pragma unroll
         for (int j = 0; j < 8; ++j) b[j] = row < nv ? phi(b[j]) : 0.f;
-        put_split8<NT>(B0, BT, row, c8, a);
-        put_split8<2>(B0 + NT * BT, BT, row, c8, b);
+        put_split8<2>(tk, row, c8, b);
       }
-      if (c + 1 < w.nch) {
-        fetch(ra, v + hq, n0 + CH, w.r1);
-        fetch(rb, k + hq, n0 + CH, w.r1);
+      if (c + 1 < w.nch) fetch(rb, k + hq, n0 + CH, w.r1);
+      if (NT == 3 && c > 0) wait_chunk(x, g - 1);  // the MMAs of the chunk before: frees the shared tile
+#pragma unroll
+      for (int i = 0; i < NU; ++i) {
+        float a[8];
+        unpack(ra, i, a);
+        put_split8<NT>(tv, unit_row(i), c8, a);
       }
+      if (c + 1 < w.nch) fetch(ra, v + hq, n0 + CH, w.r1);
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
       if (t == 0 && !s_abort) {
         tc_fence_after();
-        const uint32_t a0 = saddr(B0), d0 = t2 + 256 * (g & 1);
-        mma_tok<NT>(d0, a0, saddr(SH), false);                // V R^T
-        mma_tok<2>(d0 + 128, a0 + NT * BT, saddr(SH), true);  // phi(K) R
+        const uint32_t d0 = t2 + 256 * (g & 1);
+        mma_tok<NT>(d0, taddr(tv), saddr(SH), false);       // V R^T
+        mma_tok<2>(d0 + 128, taddr(tk), saddr(SH), true);  // phi(K) R
         mma_commit(&x.bar[g & 1]);
       }
       ++g;
@@ -919,7 +990,7 @@ __global__ void __launch_bounds__(NTX, 1)
         ld_halves(acc, a, b);
         if (row < nv) {
           float f[CW];
-          get_row<CW, 2>(B0 + NT * BT, BT, row, CW * cg, f);  // phi(K) to 2^-18, for phi'
+          get_row<CW, 2>(B0 + 2 * BT, BT, row, CW * cg, f);  // phi(K) to 2^-18, for phi'
           T* dst = dk + hq + (n0 + row) * 64 + CW * cg;
 #pragma unroll
           for (int j = 0; j < CW; j += 4) {
