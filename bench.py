@@ -284,6 +284,7 @@ def run_ours(args, dist):
     if not args.no_secondary:
         res["secondary"] = secondary(la, torch, dev, flush, peaks,
                                      with_cpu=dist.rank == 0 and not args.no_cpu)
+    la.check_device_status()  # raises if a bounded wait inside a kernel ran out
     if dist.rank == 0 and not args.no_cpu:
         res["cpu_baseline"] = cpu_baseline(q, k, v, g, B, H, N)
     dist.close()

@@ -14,7 +14,8 @@
  *  - Pointers named q, k, v, out, dout, dq, dk, dv, den, S, Z, lengths and
  *    workspace are DEVICE pointers (or managed memory) of the current CUDA
  *    device.  The caller owns every buffer; the library never allocates,
- *    frees or retains memory and keeps no state between calls.
+ *    frees or retains memory and keeps no state between calls other than
+ *    one device status word per GPU (see la_device_status).
  *  - Layouts are dense row-major: q, k, dq, dk [B][H][N][D]; v, out, dout, dv
  *    [B][H][N][M]; den [B][H][N]; S [B][H][D][M]; Z [B][H][D]; lengths [B].
  *    Decode tensors drop N: q, k [B][H][D], v, y [B][H][M].
@@ -34,6 +35,13 @@
  *    the host before anything is launched, so nothing was written.
  *    LA_ERR_CUDA reports a launch failure (cudaGetLastError after the
  *    launch).  The library never prints, exits or aborts.
+ *  - Device-side failures: every wait inside a kernel (on a shared-memory
+ *    barrier, a bulk copy or a tensor-core product) is bounded (2 s).  A
+ *    wait that runs out stores a nonzero code in the library's status word
+ *    on that GPU (the first code sticks), and the kernel unwinds: it drains
+ *    its own copies and products with bounded waits, frees its tensor
+ *    memory and returns, leaving its outputs undefined and the CUDA context
+ *    usable.  la_device_status reports and clears it.
  *  - Workspace: calls that take `workspace` need at least
  *    la_workspace_bytes(op, ...) bytes of device scratch (may be NULL when
  *    that size is 0).  Its contents on entry do not matter and are garbage on
@@ -54,6 +62,7 @@ extern "C" {
 #define LA_ERR_UNSUPPORTED 2 /* valid but unsupported (D or M not in the set) */
 #define LA_ERR_CUDA 3        /* a CUDA launch or runtime call failed */
 #define LA_ERR_WORKSPACE 4   /* workspace missing or smaller than required */
+#define LA_ERR_TIMEOUT 5     /* a bounded wait inside a kernel ran out (la_device_status) */
 
 /* element types */
 #define LA_F32 0
@@ -159,6 +168,30 @@ int la_noncausal_bwd(const void* q, const void* k, const void* v, const int* len
  */
 int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z,
                    void* y, int B, int H, int D, int M, int dtype, void* stream);
+
+/*
+ * Reads the status word of the current GPU after all work queued on
+ * `stream` so far (the call synchronises `stream`; other streams' work is
+ * covered once it has finished).  Returns LA_OK when no bounded wait has
+ * run out since the word was last cleared, LA_ERR_TIMEOUT when one has, and
+ * LA_ERR_CUDA when the stream or the copy fails.  *code (if code is not
+ * NULL) receives the word: 0, or the code of the first wait that ran out
+ * (a small integer naming the kernel and the wait).  clear != 0 resets the
+ * word to 0 after reading it.  The first call on a device (this one or any
+ * compute call) looks up the word's device address with that device
+ * current.
+ */
+int la_device_status(void* stream, int clear, int* code);
+
+/*
+ * Diagnostic: launches on `stream` one kernel that waits, with the bounded
+ * wait every kernel uses, on a shared-memory barrier that nothing arrives
+ * at, for limit_ns nanoseconds (1 .. 10^9), and then records code 99 in the
+ * status word and returns.  It shows that a wait which runs out reaches the
+ * host as LA_ERR_TIMEOUT and that the context stays usable.  Returns
+ * LA_ERR_INVALID_ARG for a limit outside the range (nothing launched).
+ */
+int la_selftest_wait(void* stream, unsigned long long limit_ns);
 
 #ifdef __cplusplus
 }

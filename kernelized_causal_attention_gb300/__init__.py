@@ -28,11 +28,12 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "liblinattn.so")
 
-LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_WORKSPACE = 0, 1, 2, 3, 4
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_WORKSPACE, LA_ERR_TIMEOUT = range(6)
 LA_F32, LA_BF16 = 0, 1
 LA_OP_CAUSAL_FWD, LA_OP_CAUSAL_BWD, LA_OP_NONCAUSAL_FWD, LA_OP_NONCAUSAL_BWD, LA_OP_DECODE = range(5)
 
-# exported symbols and their ctypes signatures ("p" pointer, "i" int, "z" size_t)
+# exported symbols and their ctypes signatures ("p" pointer, "i" int, "z" size_t,
+# "u" unsigned long long)
 _SIGS = {
     "la_status_string": ("i", ctypes.c_char_p),
     "la_version": ("", ctypes.c_int),
@@ -44,6 +45,8 @@ _SIGS = {
     "la_noncausal_bwd": ("p p p p p p p p p p p p p z i i i i i i p", ctypes.c_int),
     "la_decode_step": ("p p p p p p i i i i i p", ctypes.c_int),
     "la_causal_fwd_noalloc": ("p p p p p i i i i i i p", ctypes.c_int),
+    "la_device_status": ("p i p", ctypes.c_int),
+    "la_selftest_wait": ("p u", ctypes.c_int),
 }
 EXPORTED = tuple(_SIGS)
 
@@ -71,7 +74,8 @@ def lib():
                     f"CUDA library not built: {LIB_PATH} is missing. Build it with "
                     "`python -m kernelized_causal_attention_gb300._build` (needs nvcc).")
             h = ctypes.CDLL(LIB_PATH)
-            kinds = {"p": ctypes.c_void_p, "i": ctypes.c_int, "z": ctypes.c_size_t}
+            kinds = {"p": ctypes.c_void_p, "i": ctypes.c_int, "z": ctypes.c_size_t,
+                     "u": ctypes.c_ulonglong}
             for name, (sig, res) in _SIGS.items():
                 fn = getattr(h, name)
                 fn.argtypes = [kinds[c] for c in sig.split()]
@@ -167,6 +171,30 @@ def la_causal_fwd_noalloc(q, k, v, out, den, B, H, N, D, M, dtype, stream=None):
     (for callers that may not allocate device memory)."""
     _check(lib().la_causal_fwd_noalloc(_p(q), _p(k), _p(v), _p(out), _p(den), B, H, N, D, M,
                                        dtype, _stream(stream)), "la_causal_fwd_noalloc")
+
+
+def la_device_status(clear=True, stream=None):
+    """(status, code): LA_OK and 0, or LA_ERR_TIMEOUT and the code of the first
+    bounded wait inside a kernel that ran out (after the stream's queued work);
+    clear resets the status word."""
+    code = ctypes.c_int(0)
+    rc = lib().la_device_status(_stream(stream), int(bool(clear)), ctypes.byref(code))
+    if rc not in (LA_OK, LA_ERR_TIMEOUT):
+        raise LinAttnError(rc, "la_device_status")
+    return rc, code.value
+
+
+def la_selftest_wait(limit_ns, stream=None):
+    """Launches the diagnostic kernel whose bounded wait runs out after limit_ns."""
+    _check(lib().la_selftest_wait(_stream(stream), int(limit_ns)), "la_selftest_wait")
+
+
+def check_device_status(stream=None):
+    """Raises LinAttnError(LA_ERR_TIMEOUT) if a kernel's bounded wait ran out
+    (and clears the status word); returns None otherwise."""
+    rc, code = la_device_status(True, stream)
+    if rc != LA_OK:
+        raise LinAttnError(rc, f"device status (wait code {code})")
 
 
 # --------------------------------------------------- allocating convenience API

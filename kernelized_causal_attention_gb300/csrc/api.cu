@@ -76,6 +76,7 @@ const char* la_status_string(int status) {
     case LA_ERR_UNSUPPORTED: return "unsupported head size";
     case LA_ERR_CUDA: return "CUDA error";
     case LA_ERR_WORKSPACE: return "workspace missing or too small";
+    case LA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
     default: return "unknown status";
   }
 }

@@ -80,8 +80,7 @@ constexpr int W_PHI0 = 2, W_MASK0 = 10, W_EPI0 = 14;
 // ws[bh][p] ([64][80] fp32) for every segment p but the last.
 __global__ void __launch_bounds__(NTHR, 1)
     k_tc_fwd_state(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   float* __restrict__ ws, int N, int nseg, int seg_len, int* err,
-                   int clear_err) {
+                   float* __restrict__ ws, int N, int nseg, int seg_len, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -127,9 +126,6 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   tc_fence_after();
   grid_dep_wait();
-  // the call's first kernel clears the status word (no host memset, so the
-  // launch chains with the previous kernel); a timeout only sets it seconds later
-  if (clear_err && err != nullptr && p == 0 && bh == 0 && threadIdx.x == 0) *err = 0;
   const uint32_t TS = tmem_base;
 
   if (warp == 0) {
@@ -214,7 +210,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     k_tc_fwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ out,
                   float* __restrict__ den, const float* __restrict__ ws, int N, int nseg,
-                  int seg_len, int out_v8, int* err, int clear_err) {
+                  int seg_len, int out_v8, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -272,7 +268,6 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   tc_fence_after();
   grid_dep_wait();  // the state pass's records are visible from here on
-  if (clear_err && err != nullptr && p == 0 && bh == 0 && threadIdx.x == 0) *err = 0;
   const uint32_t tm = tmem_base;
 
   if (warp == 0) {
@@ -650,7 +645,7 @@ bool tc_eligible(const Shape& s) { return s.dtype == 1 && s.D == 64 && s.M == 64
 
 size_t causal_fwd_tc_ws_floats(const Shape& s) {
   const SegPlan pl = tc_plan(s.B * s.H, s.N);
-  return static_cast<size_t>(s.B) * s.H * pl.nseg * 64 * TC_MA + 4;
+  return static_cast<size_t>(s.B) * s.H * pl.nseg * 64 * TC_MA;
 }
 
 int causal_fwd_tc_launches(const Shape& s) { return tc_plan(s.B * s.H, s.N).nseg > 1 ? 2 : 1; }
@@ -664,7 +659,7 @@ cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out
       !make_bf16_map(&mv, v, BH, s.N))
     return cudaErrorInvalidValue;
   const int out_v8 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
-  int* err = reinterpret_cast<int*>(ws + static_cast<size_t>(BH) * pl.nseg * 64 * TC_MA);
+  int* err = status_word();
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(k_tc_fwd_state, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 S_SMEM)) != cudaSuccess)
@@ -674,12 +669,12 @@ cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out
     return e;
   if (pl.nseg > 1) {
     if ((e = launch_pdl(k_tc_fwd_state, dim3(pl.nseg - 1, BH), dim3(NTHR), S_SMEM, st, mk, mv, ws,
-                        s.N, pl.nseg, pl.seg_len, err, 1)) != cudaSuccess)
+                        s.N, pl.nseg, pl.seg_len, err)) != cudaSuccess)
       return e;
   }
   if ((e = launch_pdl(k_tc_fwd_main, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv,
                       static_cast<bf16*>(out), den, static_cast<const float*>(ws), s.N, pl.nseg,
-                      pl.seg_len, out_v8, err, pl.nseg > 1 ? 0 : 1)) != cudaSuccess)
+                      pl.seg_len, out_v8, err)) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }

@@ -492,9 +492,6 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   tc_fence_after();
   grid_dep_wait();
-  // the call's first kernel clears the status word (no host memset, so the
-  // launch chains with the previous kernel); a timeout only sets it seconds later
-  if (err != nullptr && p == 0 && bh == 0 && threadIdx.x == 0) *err = 0;
   const uint32_t tm = tmem_base;  // S~ at column 0, R~ at column 128
 
   if (warp == 0) {
@@ -677,7 +674,6 @@ struct BwdWs {
   float* rec;
   bf16 *gt, *fq, *fk;
   float* gam;
-  int* err;
   size_t floats;
 };
 
@@ -693,9 +689,7 @@ BwdWs bwd_ws(float* ws, int BH, int N, const BwdPlan& pl) {
   w.fk = reinterpret_cast<bf16*>(ws + off);
   off += tok * 32;
   w.gam = ws + off;
-  off += tok;
-  w.err = reinterpret_cast<int*>(ws + off);
-  w.floats = off + 4;
+  w.floats = off + tok;
   return w;
 }
 
@@ -738,11 +732,11 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
                                 M_SMEM)) != cudaSuccess)
     return e;
   if ((e = launch_pdl(k_tc_bwd_state, dim3(pl.nsub, BH), dim3(NTHR), SS_SMEM, st, smap, den, w.gam,
-                      w.gt, w.fq, w.fk, w.rec, s.N, pl.sub_len, pl.nsub, w.err)) != cudaSuccess)
+                      w.gt, w.fq, w.fk, w.rec, s.N, pl.sub_len, pl.nsub, status_word())) != cudaSuccess)
     return e;
   if ((e = launch_pdl(k_tc_bwd_main, dim3(pl.main.nseg, BH, 2), dim3(NTHR), M_SMEM, st, m,
                       static_cast<const float*>(w.rec), static_cast<const float*>(w.gam), s.N,
-                      pl.main.seg_len, pl.nsub, pl.subs, w.err)) != cudaSuccess)
+                      pl.main.seg_len, pl.nsub, pl.subs, status_word())) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }

@@ -7,6 +7,11 @@
 
 namespace la {
 
+// The device address of the library's status word on the current device
+// (nullptr if it cannot be had): kernels whose bounded waits run out store
+// a nonzero code there; la_device_status reads it.
+int* status_word();
+
 constexpr int kChunk = 64;            // tokens per chunk in the CUDA-core kernels
 constexpr int kTargetCtas = 2 * 152;  // segments are sized to fill GB300's 152 SMs twice
 

@@ -423,17 +423,23 @@ struct Ctx {
   uint8_t* sm;
   uint64_t* bar;  // [0], [1]: MMA of buffer 0 / 1 done; [2]: final drain
   int* abort;
+  int* err;       // the library's status word
+  int site;       // this kernel's code in it
   uint32_t tm;
 };
 
 // Waits for the MMAs of global chunk g; agreed by the whole warp (the TMEM
-// loads that follow are warp-collective).  Gives up after WAIT_NS and sets
-// the CTA's abort flag, after which every wait fails at once.
+// loads that follow are warp-collective).  Gives up after WAIT_NS, records
+// the kernel's code in the status word and sets the CTA's abort flag, after
+// which every wait fails at once and no further MMA is issued.
 __device__ __forceinline__ bool wait_chunk(const Ctx& x, uint32_t g) {
   bool ok = false;
   if (!*reinterpret_cast<volatile int*>(x.abort)) {
     ok = mbar_wait(&x.bar[g & 1], (g >> 1) & 1, WAIT_NS);
-    if (!ok) *reinterpret_cast<volatile int*>(x.abort) = 1;
+    if (!ok) {
+      *reinterpret_cast<volatile int*>(x.abort) = 1;
+      fail(x.err, x.site);
+    }
   }
   return __all_sync(0xffffffffu, ok);
 }
@@ -539,11 +545,13 @@ __device__ __forceinline__ void cluster_sum(const float* P, int nseg, float4 (&m
 }
 
 // Setup shared by both kernels: barriers (at byte o_bar), abort flag, TMEM.
-__device__ __forceinline__ Ctx setup(uint8_t* smraw, int* s_abort, int o_bar) {
+__device__ __forceinline__ Ctx setup(uint8_t* smraw, int* s_abort, int o_bar, int* err, int site) {
   Ctx x;
   x.sm = align1024(smraw);
   x.bar = reinterpret_cast<uint64_t*>(x.sm + o_bar);
   x.abort = s_abort;
+  x.err = err;
+  x.site = site;
   uint32_t* slot = reinterpret_cast<uint32_t*>(x.sm + o_bar + 32);
   if (threadIdx.x == 0) {
     mbar_init(&x.bar[0], 1);
@@ -560,12 +568,13 @@ __device__ __forceinline__ Ctx setup(uint8_t* smraw, int* s_abort, int o_bar) {
   return x;
 }
 
-// Teardown: no MMA in flight, TMEM freed.  (No peer reads this CTA's
-// shared memory any more: the cluster barrier after the sum saw to that.)
+// Teardown: no MMA in flight (a bounded drain), TMEM freed.  (No peer
+// reads this CTA's shared memory any more: the cluster barrier after the
+// sum saw to that.)
 __device__ __forceinline__ void teardown(const Ctx& x) {
   if (threadIdx.x == 0) {
     mma_commit(&x.bar[2]);
-    mbar_wait(&x.bar[2], 0, WAIT_NS);
+    if (!mbar_wait(&x.bar[2], 0, WAIT_NS)) fail(x.err, x.site + 1);
   }
   tc_fence_before();
   __syncthreads();
@@ -583,12 +592,12 @@ __global__ void __launch_bounds__(NTX, 1)
     k_nc_fwd_tc(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                 const int* __restrict__ lengths, T* __restrict__ out, float* __restrict__ den,
                 float* __restrict__ S,
-                float* __restrict__ Z, int N, int H, int nseg) {
+                float* __restrict__ Z, int N, int H, int nseg, int* err) {
   constexpr int NT = Terms<T>::n;
   using L = Lay<NT>;
   extern __shared__ uint8_t smraw[];
   __shared__ int s_abort;
-  const Ctx x = setup(smraw, &s_abort, L::O_BAR);
+  const Ctx x = setup(smraw, &s_abort, L::O_BAR, err, 31);
   uint8_t* sm = x.sm;
   float* P = reinterpret_cast<float*>(sm + L::O_ST);     // partial record, then
   uint8_t* SH = sm + L::O_ST;                            // the S terms 0, 1
@@ -752,12 +761,12 @@ __global__ void __launch_bounds__(NTX, 1)
                 const int* __restrict__ lengths, const float* __restrict__ den,
                 const float* __restrict__ S, const float* __restrict__ Z,
                 const T* __restrict__ gr, T* __restrict__ dq, T* __restrict__ dk,
-                T* __restrict__ dv, int N, int H, int nseg) {
+                T* __restrict__ dv, int N, int H, int nseg, int* err) {
   constexpr int NT = Terms<T>::n;
   using L = Lay<NT>;
   extern __shared__ uint8_t smraw[];
   __shared__ int s_abort;
-  const Ctx x = setup(smraw, &s_abort, L::O_BAR);
+  const Ctx x = setup(smraw, &s_abort, L::O_BAR, err, 33);
   uint8_t* sm = x.sm;
   uint8_t* SH = sm + L::O_ST;  // phase 1: the S terms; then the partial record; phase 2: the R terms
   float* P = reinterpret_cast<float*>(SH);
@@ -1041,7 +1050,7 @@ template <typename T>
 cudaError_t run_fwd(const T* q, const T* k, const T* v, const int* lengths, T* out, float* den,
                     float* S, float* Z, const Shape& s, int nseg, cudaStream_t st) {
   return launch_cluster(k_nc_fwd_tc<T>, Lay<Terms<T>::n>::SMEM, nseg, s.B * s.H, st, q, k, v, lengths, out, den, S, Z,
-                        s.N, s.H, nseg);
+                        s.N, s.H, nseg, status_word());
 }
 
 template <typename T>
@@ -1049,7 +1058,7 @@ cudaError_t run_bwd(const T* q, const T* k, const T* v, const int* lengths, cons
                     const float* S, const float* Z, const T* dout, T* dq, T* dk, T* dv,
                     const Shape& s, int nseg, cudaStream_t st) {
   return launch_cluster(k_nc_bwd_tc<T>, Lay<Terms<T>::n>::SMEM, nseg, s.B * s.H, st, q, k, v, lengths, den, S, Z, dout, dq,
-                        dk, dv, s.N, s.H, nseg);
+                        dk, dv, s.N, s.H, nseg, status_word());
 }
 
 }  // namespace

@@ -33,9 +33,15 @@ def test_library_exports_every_declared_symbol(linattn):
 
 def test_version_and_status_strings(linattn):
     assert linattn.lib().la_version() == 100
-    for code in range(5):
-        assert linattn.status_string(code)
+    for code in range(6):
+        assert linattn.status_string(code) != "unknown status"
     assert linattn.status_string(99) == "unknown status"
+
+
+def test_selftest_wait_rejects_limits_before_launching(linattn):
+    # checked on the host: no GPU is touched for a limit outside 1 ns .. 1 s
+    for limit in (0, 1_000_000_001, 1 << 63):
+        assert linattn.lib().la_selftest_wait(None, limit) == linattn.LA_ERR_INVALID_ARG
 
 
 def test_workspace_sizes(linattn):
