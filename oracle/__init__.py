@@ -43,6 +43,7 @@ _SIGS = {
     "orc_noncausal_bwd": "i i i i i p p p p p p p p i",
     "orc_noncausal_bwd_quadratic": "i i i i i p p p p p p p p i",
     "orc_decode": "i i i i p p p p p p i",
+    "orc_causal_prefill": "i i i i p p p p p p p i",
 }
 
 
@@ -187,6 +188,21 @@ class Oracle:
                             _ptr(y), nthreads)
         return y, S, Z
 
+    def causal_prefill(self, q, k, v, S=None, Z=None, nthreads=0):
+        """The causal form started from the state (S, Z) (zeros if None):
+        eq. 16-19 over a prompt.  q, k: [B,H,N,D]; v: [B,H,N,M].
+        Returns (out [B,H,N,M], den [B,H,N], S_N [B,H,D,M], Z_N [B,H,D])."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, H, N, D = q.shape
+        M = v.shape[-1]
+        S = np.zeros((B, H, D, M)) if S is None else _f64(S).copy()
+        Z = np.zeros((B, H, D)) if Z is None else _f64(Z).copy()
+        out = np.empty((B, H, N, M))
+        den = np.empty((B, H, N))
+        self.lib.orc_causal_prefill(B * H, N, D, M, _ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(Z),
+                                    _ptr(out), _ptr(den), nthreads)
+        return out, den, S, Z
+
 
 def default() -> Oracle:
     global _default
@@ -222,3 +238,7 @@ def noncausal_bwd(q, k, v, g, lengths=None, form="recurrent", nthreads=0):
 
 def decode(q, k, v, S=None, Z=None, nthreads=0):
     return default().decode(q, k, v, S, Z, nthreads)
+
+
+def causal_prefill(q, k, v, S=None, Z=None, nthreads=0):
+    return default().causal_prefill(q, k, v, S, Z, nthreads)

@@ -543,6 +543,58 @@ void orc_noncausal_bwd_quadratic(int B, int H, int N, int D, int M, const int* l
   }
 }
 
+/* -------------------------------------------- prefill: the causal form from a state */
+
+/* [TR2] §3.4 eq. 16-19 run over a whole prompt: the causal form of §3.3
+ * eq. 10-12 with its sums started from a given state instead of zero,
+ *   S_i = S_0 + sum_{j<=i} phi(K_j) V_j^T,   Z_i = Z_0 + sum_{j<=i} phi(K_j),
+ *   out_i = phi(Q_i)^T S_i / phi(Q_i)^T Z_i,   den_i = phi(Q_i)^T Z_i,
+ * so that a prompt's state feeds the RNN form (eq. 16-19) of the tokens that
+ * follow it.  S [BH][D][M] and Z [BH][D] hold S_0, Z_0 on entry and S_N, Z_N
+ * on exit; q, k: [BH][N][D]; v, out: [BH][N][M]; den: [BH][N]. */
+void orc_causal_prefill(int BH, int N, int D, int M, const double* q, const double* k,
+                        const double* v, double* S, double* Z, double* out, double* den,
+                        int nthreads) {
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic)
+  for (int hh = 0; hh < BH; ++hh) {
+    const double* Qh = q + (size_t)hh * N * D;
+    const double* Kh = k + (size_t)hh * N * D;
+    const double* Vh = v + (size_t)hh * N * M;
+    double* Oh = out + (size_t)hh * N * M;
+    double* st = S + (size_t)hh * D * M;
+    double* zt = Z + (size_t)hh * D;
+    double* sl = (double*)malloc(sizeof(double) * (size_t)D * M);
+    double* zl = (double*)malloc(sizeof(double) * (size_t)D);
+    double* fq = (double*)malloc(sizeof(double) * (size_t)D);
+    memcpy(sl, st, sizeof(double) * (size_t)D * M);
+    for (int d = 0; d < D; ++d) zl[d] = zt[d];
+    for (int i = 0; i < N; ++i) {
+      for (int d = 0; d < D; ++d) {
+        const double fkp = phi(Kh[(size_t)i * D + d]);
+        for (int m = 0; m < M; ++m) sl[(size_t)d * M + m] += fkp * Vh[(size_t)i * M + m];
+        zl[d] += fkp;
+      }
+      double dsum = 0.0;
+      for (int d = 0; d < D; ++d) {
+        fq[d] = phi(Qh[(size_t)i * D + d]);
+        dsum += fq[d] * zl[d];
+      }
+      den[(size_t)hh * N + i] = dsum;
+      for (int m = 0; m < M; ++m) {
+        double num = 0.0;
+        for (int d = 0; d < D; ++d) num += fq[d] * sl[(size_t)d * M + m];
+        Oh[(size_t)i * M + m] = num / dsum;
+      }
+    }
+    for (size_t e = 0; e < (size_t)D * M; ++e) st[e] = sl[e];
+    for (int d = 0; d < D; ++d) zt[d] = zl[d];
+    free(sl);
+    free(zl);
+    free(fq);
+  }
+}
+
 /* ------------------------------------------------------------ RNN-form decode */
 
 /* [TR2] §3.4 eq. 16-19 (and [LA] "recurrent form"): for each step t and each

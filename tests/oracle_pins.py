@@ -9,7 +9,8 @@ oracle to show that each plausible slip is caught.
 
 Sources: "Transformers are RNNs -- part 2/3": eq. 7 (phi = elu + 1), §3.3
 eq. 8 (masked quadratic form) and eq. 10-12 (recurrence), §3.3.1 eq. 13-15
-(gradients), §3.4 eq. 16-19 (RNN form); "Linear Attention/zh": kernel
+(gradients), §3.4 eq. 16-19 (RNN form, also run over a prompt from a given
+state); "Linear Attention/zh": kernel
 reformulation (shared S, z for the non-causal form).
 """
 from __future__ import annotations
@@ -275,6 +276,47 @@ def pin_decode(orc):
     assert np.array_equal(S2, S) and np.array_equal(Z2, Z)
 
 
+# -------------------------------------------------------------------- prefill
+
+def pin_prefill(orc):
+    """The causal form started from a state (eq. 16-19 run over a prompt):
+    from a zero state it is the masked quadratic form of eq. 8; its final state
+    is S_0 + phi(K)^T V and Z_0 + sum phi(K) (numpy products); with phi(K) ~ 0
+    (K = -60) only the state speaks, out = phi(Q) S_0 / phi(Q) Z_0 and
+    den = phi(Q) Z_0 (numpy products); a prompt cut in two, the second part
+    started from the first part's state, gives the outputs and state of one
+    call, and so does the first part followed by RNN steps (the decode
+    function) over the rest."""
+    B, H, N, D, M = 2, 3, 11, 4, 5
+    q, k, v = rand((B, H, N, D), 101), rand((B, H, N, D), 102), rand((B, H, N, M), 103)
+    out0, den0, _, _ = orc.causal_prefill(q, k, v)
+    oc, dc = orc.causal_fwd(q, k, v, "quadratic")
+    assert rel(out0, oc) < 1e-13 and rel(den0, dc) < 1e-13, "prefill from zero != eq. 8"
+    # a state as an earlier prompt leaves it: S of either sign, Z positive
+    S_init = rand((B, H, D, M), 104)
+    Z_init = 3.0 * phi_lib(rand((B, H, D), 105))
+    out, den, S_N, Z_N = orc.causal_prefill(q, k, v, S_init, Z_init)
+    fk = phi_lib(k)
+    assert rel(S_N, S_init + np.matmul(np.swapaxes(fk, -1, -2), v)) < 1e-13, "S_N != S_0 + phi(K)^T V"
+    assert rel(Z_N, Z_init + fk.sum(axis=2)) < 1e-14, "Z_N != Z_0 + sum phi(K)"
+    fq = phi_lib(q)
+    outz, denz, _, _ = orc.causal_prefill(q, np.full_like(k, -60.0), v, S_init, Z_init)
+    dz = np.einsum("bhnd,bhd->bhn", fq, Z_init)
+    assert rel(denz, dz) < 1e-12, "den != phi(Q) Z_0 when phi(K) ~ 0"
+    assert rel(outz, np.matmul(fq, S_init) / dz[..., None]) < 1e-12, "out != phi(Q) S_0 / phi(Q) Z_0"
+    n1 = 4
+    cut = lambda x, a, b: np.ascontiguousarray(x[:, :, a:b])
+    o1, d1, S1, Z1 = orc.causal_prefill(cut(q, 0, n1), cut(k, 0, n1), cut(v, 0, n1), S_init, Z_init)
+    o2, d2, S2, Z2 = orc.causal_prefill(cut(q, n1, N), cut(k, n1, N), cut(v, n1, N), S1, Z1)
+    assert rel(np.concatenate([o1, o2], axis=2), out) < 1e-13, "prefill cut in two differs"
+    assert rel(np.concatenate([d1, d2], axis=2), den) < 1e-13
+    assert rel(S2, S_N) < 1e-13 and rel(Z2, Z_N) < 1e-13
+    steps = lambda x: np.ascontiguousarray(np.transpose(x[:, :, n1:], (2, 0, 1, 3)))  # [T,B,H,.]
+    y, Sd, Zd = orc.decode(steps(q), steps(k), steps(v), S1, Z1)
+    assert rel(np.transpose(y, (1, 2, 0, 3)), out[:, :, n1:]) < 1e-13, "prompt + RNN steps != one prefill"
+    assert rel(Sd, S_N) < 1e-13 and rel(Zd, Z_N) < 1e-13
+
+
 ALL_PINS = [pin_phi, pin_causal_forms_agree, pin_causal_closed_forms, pin_grad_single_token, pin_noncausal_gemm,
             pin_noncausal_last_row, pin_noncausal_lengths, pin_grad_fd, pin_grad_forms_agree,
-            pin_grad_invariants, pin_decode]
+            pin_grad_invariants, pin_decode, pin_prefill]

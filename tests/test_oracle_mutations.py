@@ -27,6 +27,10 @@ MUTATIONS = [
     ("noncausal_bwd_missing_gamma", "double gam = -gv / s;", "double gam = 0.0 * gv / s;", 0),
     ("decode_no_denominator", "yt[m] = acc / den;", "yt[m] = acc;", 0),
     ("decode_transposed_update", "s[(size_t)d * M + m] += fk * vt[m];", "s[(size_t)d * M + m] += fk * vt[d % M];", 0),
+    ("prefill_starts_from_zero", "memcpy(sl, st, sizeof(double) * (size_t)D * M);", "memset(sl, 0, sizeof(double) * (size_t)D * M);", 0),
+    ("prefill_den_without_z0", "for (int d = 0; d < D; ++d) zl[d] = zt[d];", "for (int d = 0; d < D; ++d) zl[d] = 0.0 * zt[d];", 0),
+    ("prefill_state_not_returned", "for (size_t e = 0; e < (size_t)D * M; ++e) st[e] = sl[e];", "for (size_t e = 0; e < (size_t)D * M; ++e) (void)sl[e];", 0),
+    ("prefill_z_misses_prompt_keys", "        zl[d] += fkp;\n      }\n      double dsum = 0.0;", "        zl[d] += 0.0 * fkp;\n      }\n      double dsum = 0.0;", 0),
 ]
 
 
