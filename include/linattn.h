@@ -74,6 +74,7 @@ extern "C" {
 #define LA_OP_NONCAUSAL_FWD 2
 #define LA_OP_NONCAUSAL_BWD 3
 #define LA_OP_DECODE 4
+#define LA_OP_CAUSAL_PREFILL 5
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* la_status_string(int status);
@@ -111,6 +112,23 @@ int la_causal_bwd(const void* q, const void* k, const void* v, const void* out,
                   const float* den, const void* dout, void* dq, void* dk, void* dv,
                   void* workspace, size_t workspace_bytes, int B, int H, int N, int D,
                   int M, int dtype, void* stream);
+
+/*
+ * Prefill: the causal forward started from the state (S, Z) instead of zero,
+ * i.e. the RNN form of §3.4 eq. 16-19 run over a whole prompt:
+ *   S_i = S + sum_{j<=i} phi(k_j) v_j^T,   Z_i = Z + sum_{j<=i} phi(k_j),
+ *   out_i = phi(q_i)^T S_i / phi(q_i)^T Z_i,   den_i = phi(q_i)^T Z_i.
+ * On return S and Z hold S_N and Z_N, the state after the last token, from
+ * which la_decode_step continues (the two compose: prefill of a prompt, then
+ * decode steps, equals prefill of the whole sequence).  S [B][H][D][M] and
+ * Z [B][H][D] are fp32, read and updated in place; zeros give la_causal_fwd
+ * plus the final state.  den may be NULL.  Needs la_workspace_bytes(
+ * LA_OP_CAUSAL_PREFILL, ...) bytes of workspace; other arguments and errors
+ * as la_causal_fwd.
+ */
+int la_causal_prefill(const void* q, const void* k, const void* v, void* out, float* den,
+                      float* S, float* Z, void* workspace, size_t workspace_bytes, int B, int H,
+                      int N, int D, int M, int dtype, void* stream);
 
 /*
  * la_causal_fwd for callers that cannot allocate device memory: the same

@@ -8,10 +8,11 @@ kernels; there is no fallback of any kind, and using any entry point without
 the built library raises.
 
 Raw entry points (same names and argument order as the C ABI, tensors in
-place of pointers): ``la_causal_fwd``, ``la_causal_bwd``, ``la_noncausal_fwd``,
-``la_noncausal_bwd``, ``la_decode_step``, ``la_workspace_bytes``.
+place of pointers): ``la_causal_fwd``, ``la_causal_bwd``, ``la_causal_prefill``,
+``la_noncausal_fwd``, ``la_noncausal_bwd``, ``la_decode_step``,
+``la_workspace_bytes``, ``la_device_status``.
 Convenience wrappers that allocate outputs with torch: ``causal_fwd``,
-``causal_bwd``, ``noncausal_fwd``, ``noncausal_bwd``, ``decode_step`` and the
+``causal_bwd``, ``causal_prefill``, ``noncausal_fwd``, ``noncausal_bwd``, ``decode_step`` and the
 autograd functions ``causal_linear_attention`` / ``noncausal_linear_attention``.
 
 The method is Katharopoulos et al., "Transformers are RNNs" (part 2/3):
@@ -30,7 +31,8 @@ LIB_PATH = os.path.join(_HERE, "_lib", "liblinattn.so")
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_WORKSPACE, LA_ERR_TIMEOUT = range(6)
 LA_F32, LA_BF16 = 0, 1
-LA_OP_CAUSAL_FWD, LA_OP_CAUSAL_BWD, LA_OP_NONCAUSAL_FWD, LA_OP_NONCAUSAL_BWD, LA_OP_DECODE = range(5)
+(LA_OP_CAUSAL_FWD, LA_OP_CAUSAL_BWD, LA_OP_NONCAUSAL_FWD, LA_OP_NONCAUSAL_BWD, LA_OP_DECODE,
+ LA_OP_CAUSAL_PREFILL) = range(6)
 
 # exported symbols and their ctypes signatures ("p" pointer, "i" int, "z" size_t,
 # "u" unsigned long long)
@@ -41,6 +43,7 @@ _SIGS = {
     "la_kernel_launches": ("i i i i i i i", ctypes.c_int),
     "la_causal_fwd": ("p p p p p p z i i i i i i p", ctypes.c_int),
     "la_causal_bwd": ("p p p p p p p p p p z i i i i i i p", ctypes.c_int),
+    "la_causal_prefill": ("p p p p p p p p z i i i i i i p", ctypes.c_int),
     "la_noncausal_fwd": ("p p p p p p p p p z i i i i i i p", ctypes.c_int),
     "la_noncausal_bwd": ("p p p p p p p p p p p p p z i i i i i i p", ctypes.c_int),
     "la_decode_step": ("p p p p p p i i i i i p", ctypes.c_int),
@@ -146,6 +149,12 @@ def la_causal_bwd(q, k, v, out, den, dout, dq, dk, dv, workspace, B, H, N, D, M,
                                _stream(stream)), "la_causal_bwd")
 
 
+def la_causal_prefill(q, k, v, out, den, S, Z, workspace, B, H, N, D, M, dtype, stream=None):
+    _check(lib().la_causal_prefill(_p(q), _p(k), _p(v), _p(out), _p(den), _p(S), _p(Z),
+                                   _p(workspace), _nbytes(workspace), B, H, N, D, M, dtype,
+                                   _stream(stream)), "la_causal_prefill")
+
+
 def la_noncausal_fwd(q, k, v, lengths, out, den, S, Z, workspace, B, H, N, D, M, dtype,
                      stream=None):
     _check(lib().la_noncausal_fwd(_p(q), _p(k), _p(v), _p(lengths), _p(out), _p(den), _p(S),
@@ -214,6 +223,24 @@ def causal_fwd(q, k, v, stream=None):
     ws = workspace(LA_OP_CAUSAL_FWD, B, H, N, D, M, dt, q.device)
     la_causal_fwd(q, k, v, out, den, ws, B, H, N, D, M, dt, stream)
     return out, den
+
+
+def causal_prefill(q, k, v, S=None, Z=None, stream=None):
+    """(out, den, S, Z): the causal form started from the state (S, Z) (zeros
+    if None), which is updated in place to the state after the sequence and
+    returned; la_decode_step continues from it."""
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    out = torch.empty_like(v)
+    den = torch.empty(B, H, N, device=q.device, dtype=torch.float32)
+    if S is None:
+        S = torch.zeros(B, H, D, M, device=q.device, dtype=torch.float32)
+    if Z is None:
+        Z = torch.zeros(B, H, D, device=q.device, dtype=torch.float32)
+    ws = workspace(LA_OP_CAUSAL_PREFILL, B, H, N, D, M, dt, q.device)
+    la_causal_prefill(q, k, v, out, den, S, Z, ws, B, H, N, D, M, dt, stream)
+    return out, den, S, Z
 
 
 def causal_bwd(q, k, v, out, den, dout, stream=None):

@@ -43,6 +43,8 @@ size_t ws_bytes(int op, const Shape& s) {
       return 4 * (la::tc_eligible(s) ? la::causal_fwd_tc_ws_floats(s) : la::causal_fwd_ws_floats(s));
     case LA_OP_CAUSAL_BWD:
       return 4 * (la::tc_eligible(s) ? la::causal_bwd_tc_ws_floats(s) : la::causal_bwd_ws_floats(s));
+    case LA_OP_CAUSAL_PREFILL:
+      return 4 * (la::tc_eligible(s) ? la::causal_fwd_tc_ws_floats(s) : la::causal_prefill_ws_floats(s));
     case LA_OP_NONCAUSAL_FWD: return 4 * la::noncausal_fwd_ws_floats(s);
     case LA_OP_NONCAUSAL_BWD: return 4 * la::noncausal_bwd_ws_floats(s);
     default: return 0;
@@ -99,6 +101,7 @@ int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype) {
       return la::tc_eligible(s) ? la::causal_fwd_tc_launches(s) : la::causal_fwd_launches(s);
     case LA_OP_CAUSAL_BWD:
       return la::tc_eligible(s) ? la::causal_bwd_tc_launches(s) : la::causal_bwd_launches(s);
+    case LA_OP_CAUSAL_PREFILL: return la::tc_eligible(s) ? 3 : 4;
     case LA_OP_NONCAUSAL_FWD: return la::noncausal_fwd_launches(s);
     case LA_OP_NONCAUSAL_BWD: return la::noncausal_bwd_launches(s);
     case LA_OP_DECODE: return 1;
@@ -119,6 +122,21 @@ int la_causal_fwd(const void* q, const void* k, const void* v, void* out, float*
                                        static_cast<cudaStream_t>(stream)));
   return from_cuda(la::causal_fwd_cc(q, k, v, out, den, static_cast<float*>(workspace), s,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+int la_causal_prefill(const void* q, const void* k, const void* v, void* out, float* den, float* S,
+                      float* Z, void* workspace, size_t workspace_bytes, int B, int H, int N,
+                      int D, int M, int dtype, void* stream) {
+  LA_TRY(check_shape(B, H, N, D, M, dtype));
+  LA_TRY(check_ptrs({q, k, v, out, S, Z}));
+  LA_TRY(check_opt_ptr(den));
+  const Shape s{B, H, N, D, M, dtype};
+  LA_TRY(check_ws(LA_OP_CAUSAL_PREFILL, s, workspace, workspace_bytes));
+  if (la::tc_eligible(s))
+    return from_cuda(la::causal_prefill_tc(q, k, v, out, den, S, Z, static_cast<float*>(workspace),
+                                           s, static_cast<cudaStream_t>(stream)));
+  return from_cuda(la::causal_prefill_cc(q, k, v, out, den, S, Z, static_cast<float*>(workspace), s,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 int la_causal_bwd(const void* q, const void* k, const void* v, const void* out, const float* den,

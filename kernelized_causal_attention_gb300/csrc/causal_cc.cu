@@ -26,14 +26,15 @@ constexpr int NT = 256;
 // ---------------------------------------------------------------- partial sums
 
 // Per-segment sums of the forward state, eq. 10-11 restricted to the segment:
-//   ws[bh][p] = [ dS (D x M) | dz (D) ].
-// The last segment's sums are never read (only exclusive prefixes are used).
+//   ws[bh][p] = [ dS (D x M) | dz (D) ]  (nrec records per (b, h)).
+// The last segment's sums are only needed for the state after the sequence
+// (all != 0); the forward itself reads exclusive prefixes only.
 template <int D, int M, typename T>
 __global__ void __launch_bounds__(NT) k_seg_state_fwd(const T* __restrict__ k,
                                                       const T* __restrict__ v, float* ws, int N,
-                                                      int nseg, int seg_len) {
+                                                      int nseg, int seg_len, int nrec, int all) {
   const int p = blockIdx.x, bh = blockIdx.y;
-  if (p == nseg - 1) return;
+  if (p == nseg - 1 && !all) return;
   extern __shared__ float sm[];
   float* sK = sm;                  // phi(K) [C][D+1]
   float* sV = sK + C * (D + 1);    // V      [C][M+1]
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(NT) k_seg_state_fwd(const T* __restrict__ k,
       for (int j = 0; j < C; ++j) zacc += sK[j * (D + 1) + threadIdx.x];
     __syncthreads();
   }
-  float* dst = ws + ((long)bh * nseg + p) * (D * M + D);
+  float* dst = ws + ((long)bh * nrec + p) * (D * M + D);
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
 #pragma unroll
   for (int r = 0; r < D / 16; ++r)
@@ -153,8 +154,9 @@ __global__ void __launch_bounds__(NT) k_seg_state_bwd(const T* __restrict__ q,
 // In-place exclusive scans over the segments of each (b, h): entries
 // [0, wf) of every record become prefix sums over earlier segments, entries
 // [ro, ro + wr) suffix sums over later segments.  One thread per entry.
-__global__ void k_seg_scan(float* ws, int nseg, int stride, int wf, int ro, int wr) {
-  float* base = ws + (long)blockIdx.x * nseg * stride;
+// With nrec > nseg, record nseg receives the forward totals.
+__global__ void k_seg_scan(float* ws, int nseg, int stride, int wf, int ro, int wr, int nrec) {
+  float* base = ws + (long)blockIdx.x * nrec * stride;
   const int e = blockIdx.y * blockDim.x + threadIdx.x;
   if (e < wf) {
     float run = 0.f;
@@ -163,6 +165,7 @@ __global__ void k_seg_scan(float* ws, int nseg, int stride, int wf, int ro, int 
       base[(long)p * stride + e] = run;
       run += x;
     }
+    if (nrec > nseg) base[(long)nseg * stride + e] = run;
   }
   if (e < wr) {
     float run = 0.f;
@@ -181,13 +184,16 @@ __global__ void k_seg_scan(float* ws, int nseg, int stride, int wf, int ro, int 
 //   den = rowsum(A) + phi(Q) z                   (eq. 12 denominator)
 //   out = (A V + phi(Q) S) / den                 (eq. 12 numerator)
 //   S  += phi(K)^T V,  z += sum phi(K)           (eq. 10-11)
+// S0, Z0 (may be null): a state the sums start from (eq. 16-19 over a prompt).
 template <int D, int M, typename T>
 __global__ void __launch_bounds__(NT) k_causal_fwd(const T* __restrict__ q,
                                                    const T* __restrict__ k,
                                                    const T* __restrict__ v, T* __restrict__ out,
                                                    float* __restrict__ den,
                                                    const float* __restrict__ ws, int N, int nseg,
-                                                   int seg_len) {
+                                                   int seg_len, int nrec,
+                                                   const float* __restrict__ S0,
+                                                   const float* __restrict__ Z0) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ float sm[];
   float* sQ = sm;                  // phi(Q) [C][D+1]
@@ -201,18 +207,20 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(const T* __restrict__ q,
   const long nb = (long)p * seg_len, ne = min((long)N, nb + seg_len);
   const long hq = (long)bh * N * D, hv = (long)bh * N * M;
 
-  // exclusive prefix state of this segment
-  const float* pre = ws + ((long)bh * nseg + p) * (D * M + D);
+  // exclusive prefix state of this segment (plus the initial state)
+  const float* pre = ws + ((long)bh * nrec + p) * (D * M + D);
   float accS[D / 16][M / 16];
 #pragma unroll
   for (int r = 0; r < D / 16; ++r)
 #pragma unroll
     for (int c = 0; c < M / 16; ++c) {
       const int d = ty + 16 * r, m = tx + 16 * c;
-      accS[r][c] = p > 0 ? pre[d * M + m] : 0.f;
+      accS[r][c] = (p > 0 ? pre[d * M + m] : 0.f) + (S0 != nullptr ? S0[(long)bh * D * M + d * M + m] : 0.f);
       sS[d * (M + 1) + m] = accS[r][c];
     }
-  if (threadIdx.x < D) sz[threadIdx.x] = p > 0 ? pre[D * M + threadIdx.x] : 0.f;
+  if (threadIdx.x < D)
+    sz[threadIdx.x] = (p > 0 ? pre[D * M + threadIdx.x] : 0.f) +
+                      (Z0 != nullptr ? Z0[(long)bh * D + threadIdx.x] : 0.f);
 
   for (long n0 = nb; n0 < ne; n0 += C) {
     load_tile<T, C, D, false, kPhi>(sQ, D + 1, q + hq, n0, ne);
@@ -459,15 +467,41 @@ cudaError_t run_fwd(const T* q, const T* k, const T* v, T* out, float* den, floa
   if (pl.nseg > 1) {
     auto ks = k_seg_state_fwd<D, M, T>;
     if ((e = set_smem(ks, state_fwd_smem<D, M>())) != cudaSuccess) return e;
-    ks<<<dim3(pl.nseg, BH), NT, state_fwd_smem<D, M>(), st>>>(k, v, ws, s.N, pl.nseg, pl.seg_len);
+    ks<<<dim3(pl.nseg, BH), NT, state_fwd_smem<D, M>(), st>>>(k, v, ws, s.N, pl.nseg, pl.seg_len,
+                                                              pl.nseg, 0);
     k_seg_scan<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(ws, pl.nseg, D * M + D,
-                                                                  D * M + D, 0, 0);
+                                                                  D * M + D, 0, 0, pl.nseg);
   }
   auto kf = k_causal_fwd<D, M, T>;
   if ((e = set_smem(kf, fwd_smem<D, M>())) != cudaSuccess) return e;
   kf<<<dim3(pl.nseg, BH), NT, fwd_smem<D, M>(), st>>>(q, k, v, out, den, ws, s.N, pl.nseg,
-                                                      pl.seg_len);
+                                                      pl.seg_len, pl.nseg, nullptr, nullptr);
   return cudaGetLastError();
+}
+
+// The forward from the state (S, Z), which then receives the state after the
+// sequence: every segment's sums (nseg + 1 records per (b, h), the last one
+// the totals), the forward with S, Z added to each prefix, then S, Z += the
+// totals (after the forward has read them).
+template <int D, int M, typename T>
+cudaError_t run_prefill(const T* q, const T* k, const T* v, T* out, float* den, float* S, float* Z,
+                        float* ws, const Shape& s, cudaStream_t st) {
+  const int BH = s.B * s.H;
+  const SegPlan pl = plan_segments(BH, s.N);
+  const int nrec = pl.nseg + 1;
+  cudaError_t e;
+  auto ks = k_seg_state_fwd<D, M, T>;
+  if ((e = set_smem(ks, state_fwd_smem<D, M>())) != cudaSuccess) return e;
+  ks<<<dim3(pl.nseg, BH), NT, state_fwd_smem<D, M>(), st>>>(k, v, ws, s.N, pl.nseg, pl.seg_len,
+                                                            nrec, 1);
+  k_seg_scan<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(ws, pl.nseg, D * M + D, D * M + D,
+                                                                0, 0, nrec);
+  auto kf = k_causal_fwd<D, M, T>;
+  if ((e = set_smem(kf, fwd_smem<D, M>())) != cudaSuccess) return e;
+  kf<<<dim3(pl.nseg, BH), NT, fwd_smem<D, M>(), st>>>(q, k, v, out, den, ws, s.N, pl.nseg,
+                                                      pl.seg_len, nrec, S, Z);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return state_add_records(ws, BH, nrec, D * M + D, pl.nseg, nrec, D, M, M, D * M, 1, S, Z, st);
 }
 
 template <int D, int M, typename T>
@@ -482,7 +516,7 @@ cudaError_t run_bwd(const T* q, const T* k, const T* v, const T* o, const float*
     ks<<<dim3(pl.nseg, BH), NT, state_bwd_smem<D, M>(), st>>>(q, k, v, o, den, g, ws, s.N,
                                                               pl.nseg, pl.seg_len);
     k_seg_scan<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(
-        ws, pl.nseg, 2 * (D * M + D), D * M + D, D * M + D, D * M + D);
+        ws, pl.nseg, 2 * (D * M + D), D * M + D, D * M + D, D * M + D, pl.nseg);
   }
   auto kb = k_causal_bwd<D, M, T>;
   if ((e = set_smem(kb, bwd_smem<D, M>())) != cudaSuccess) return e;
@@ -496,7 +530,58 @@ cudaError_t run_bwd(const T* q, const T* k, const T* v, const T* o, const float*
 void k_seg_scan_ext(float* ws, int BH, int nseg, int stride, int wf, int ro, int wr,
                     cudaStream_t st) {
   const int w = wf > wr ? wf : wr;
-  k_seg_scan<<<dim3(BH, (w + 255) / 256), 256, 0, st>>>(ws, nseg, stride, wf, ro, wr);
+  k_seg_scan<<<dim3(BH, (w + 255) / 256), 256, 0, st>>>(ws, nseg, stride, wf, ro, wr, nseg);
+}
+
+namespace {
+
+// (S, Z)[bh] += the sum of records r0 .. r1 - 1 of ws[bh] (nrec records of
+// rstride floats per (b, h)); a record holds S[d][m] at d * srow + m and
+// z[d] at zoff + d * zstride.
+__global__ void k_state_add(const float* __restrict__ ws, int nrec, int rstride, int r0, int r1,
+                            int D, int M, int srow, int zoff, int zstride, float* __restrict__ S,
+                            float* __restrict__ Z) {
+  const long bh = blockIdx.x;
+  const float* base = ws + bh * nrec * static_cast<long>(rstride);
+  const int e = blockIdx.y * blockDim.x + threadIdx.x;
+  if (e >= D * M + D) return;
+  const bool isz = e >= D * M;
+  const int off = isz ? zoff + (e - D * M) * zstride : (e / M) * srow + e % M;
+  float acc = 0.f;
+  for (int r = r0; r < r1; ++r) acc += base[static_cast<long>(r) * rstride + off];
+  if (isz)
+    Z[bh * D + (e - D * M)] += acc;
+  else
+    S[bh * D * M + e] += acc;
+}
+
+}  // namespace
+
+cudaError_t state_add_records(const float* ws, int BH, int nrec, int rstride, int r0, int r1, int D,
+                              int M, int srow, int zoff, int zstride, float* S, float* Z,
+                              cudaStream_t st) {
+  k_state_add<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(ws, nrec, rstride, r0, r1, D, M,
+                                                                 srow, zoff, zstride, S, Z);
+  return cudaGetLastError();
+}
+
+size_t causal_prefill_ws_floats(const Shape& s) {
+  const SegPlan pl = plan_segments(s.B * s.H, s.N);
+  return (size_t)s.B * s.H * (pl.nseg + 1) * (s.D * s.M + s.D);
+}
+
+cudaError_t causal_prefill_cc(const void* q, const void* k, const void* v, void* out, float* den,
+                              float* S, float* Z, float* ws, const Shape& s, cudaStream_t st) {
+  if (s.dtype == 0) {
+    using T = float;
+    LA_DISPATCH_DM(s.D, s.M, return (run_prefill<D_, M_, T>((const T*)q, (const T*)k, (const T*)v,
+                                                             (T*)out, den, S, Z, ws, s, st)));
+  } else {
+    using T = __nv_bfloat16;
+    LA_DISPATCH_DM(s.D, s.M, return (run_prefill<D_, M_, T>((const T*)q, (const T*)k, (const T*)v,
+                                                             (T*)out, den, S, Z, ws, s, st)));
+  }
+  return cudaErrorInvalidValue;
 }
 
 size_t causal_fwd_ws_floats(const Shape& s) {

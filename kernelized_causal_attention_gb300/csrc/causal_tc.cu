@@ -210,7 +210,8 @@ __global__ void __launch_bounds__(NTHR, 1)
     k_tc_fwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ out,
                   float* __restrict__ den, const float* __restrict__ ws, int N, int nseg,
-                  int seg_len, int out_v8, int* err) {
+                  int seg_len, int out_v8, int* err, const float* __restrict__ S0,
+                  const float* __restrict__ Z0) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -463,6 +464,21 @@ __global__ void __launch_bounds__(NTHR, 1)
           acc[4 * j + 3] += x.w;
         }
       }
+      if (S0 != nullptr) {  // a state the sums start from (eq. 16-19 over a prompt)
+#pragma unroll
+        for (int j = 0; j < 5; ++j) {
+          const int f = 4 * (tr * 5 + j), row = f / TC_MA, col = f % TC_MA;
+          if (col < 64) {
+            const float4 x = *reinterpret_cast<const float4*>(S0 + (static_cast<long>(bh) * 64 + row) * 64 + col);
+            acc[4 * j] += x.x;
+            acc[4 * j + 1] += x.y;
+            acc[4 * j + 2] += x.z;
+            acc[4 * j + 3] += x.w;
+          } else if (col == 64) {
+            acc[4 * j] += Z0[static_cast<long>(bh) * 64 + row];
+          }
+        }
+      }
       float4* scr = reinterpret_cast<float4*>(sm + F_SCR) + tr * 5;
 #pragma unroll
       for (int j = 0; j < 5; ++j) scr[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
@@ -650,8 +666,14 @@ size_t causal_fwd_tc_ws_floats(const Shape& s) {
 
 int causal_fwd_tc_launches(const Shape& s) { return tc_plan(s.B * s.H, s.N).nseg > 1 ? 2 : 1; }
 
-cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out, float* den,
-                          float* ws, const Shape& s, cudaStream_t st) {
+namespace {
+
+// The forward's launches: the state pass over the first nrec segments (all
+// of them when the state after the sequence is wanted), then the main pass,
+// whose sums start from (S0, Z0) when S0 is not null.
+cudaError_t fwd_tc_launch(const void* q, const void* k, const void* v, void* out, float* den,
+                          float* ws, const Shape& s, cudaStream_t st, const float* S0,
+                          const float* Z0, bool all_records) {
   const int BH = s.B * s.H;
   const SegPlan pl = tc_plan(BH, s.N);
   CUtensorMap mq, mk, mv;
@@ -667,16 +689,36 @@ cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out
   if ((e = cudaFuncSetAttribute(k_tc_fwd_main, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 F_SMEM)) != cudaSuccess)
     return e;
-  if (pl.nseg > 1) {
-    if ((e = launch_pdl(k_tc_fwd_state, dim3(pl.nseg - 1, BH), dim3(NTHR), S_SMEM, st, mk, mv, ws,
+  const int nrec = all_records ? pl.nseg : pl.nseg - 1;
+  if (nrec > 0) {
+    if ((e = launch_pdl(k_tc_fwd_state, dim3(nrec, BH), dim3(NTHR), S_SMEM, st, mk, mv, ws,
                         s.N, pl.nseg, pl.seg_len, err)) != cudaSuccess)
       return e;
   }
   if ((e = launch_pdl(k_tc_fwd_main, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv,
                       static_cast<bf16*>(out), den, static_cast<const float*>(ws), s.N, pl.nseg,
-                      pl.seg_len, out_v8, err)) != cudaSuccess)
+                      pl.seg_len, out_v8, err, S0, Z0)) != cudaSuccess)
     return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out, float* den,
+                          float* ws, const Shape& s, cudaStream_t st) {
+  return fwd_tc_launch(q, k, v, out, den, ws, s, st, nullptr, nullptr, false);
+}
+
+// The state pass writes every segment's record, the main pass adds (S, Z) to
+// each segment's starting state, and after it (S, Z) += the sum of the
+// records ([64][80] each: S~ in columns 0-63, z in column 64).
+cudaError_t causal_prefill_tc(const void* q, const void* k, const void* v, void* out, float* den,
+                              float* S, float* Z, float* ws, const Shape& s, cudaStream_t st) {
+  cudaError_t e = fwd_tc_launch(q, k, v, out, den, ws, s, st, S, Z, true);
+  if (e != cudaSuccess) return e;
+  const int nseg = tc_plan(s.B * s.H, s.N).nseg;
+  return state_add_records(ws, s.B * s.H, nseg, 64 * TC_MA, 0, nseg, 64, 64, TC_MA, 64, TC_MA, S, Z,
+                           st);
 }
 
 }  // namespace la

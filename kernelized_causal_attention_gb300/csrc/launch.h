@@ -56,6 +56,22 @@ int noncausal_bwd_launches(const Shape& s);
 void k_seg_scan_ext(float* ws, int BH, int nseg, int stride, int wf, int ro, int wr,
                     cudaStream_t st);
 
+// (S, Z)[bh] += the sum of records r0 .. r1 - 1 of ws[bh] (nrec records of
+// rstride floats per (b, h)); a record holds S[d][m] at d * srow + m and z[d]
+// at zoff + d * zstride.  One launch.
+cudaError_t state_add_records(const float* ws, int BH, int nrec, int rstride, int r0, int r1, int D,
+                              int M, int srow, int zoff, int zstride, float* S, float* Z,
+                              cudaStream_t st);
+
+// The causal forward from the state (S, Z), which then holds the state after
+// the sequence (eq. 16-19 over a prompt).  CUDA cores: four launches;
+// tcgen05: three.
+size_t causal_prefill_ws_floats(const Shape& s);
+cudaError_t causal_prefill_cc(const void* q, const void* k, const void* v, void* out, float* den,
+                              float* S, float* Z, float* ws, const Shape& s, cudaStream_t st);
+cudaError_t causal_prefill_tc(const void* q, const void* k, const void* v, void* out, float* den,
+                              float* S, float* Z, float* ws, const Shape& s, cudaStream_t st);
+
 // tcgen05 path (bf16, D = M = 64).
 SegPlan tc_plan(int BH, int N);
 bool tc_eligible(const Shape& s);

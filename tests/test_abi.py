@@ -58,6 +58,13 @@ def test_workspace_sizes(linattn):
         assert la.la_workspace_bytes(la.LA_OP_NONCAUSAL_FWD, 16, 6, 2048, 64, 64, dt) == 0
         assert la.la_workspace_bytes(la.LA_OP_NONCAUSAL_BWD, 16, 6, 2048, 64, 64, dt) == 0
     assert la.la_workspace_bytes(la.LA_OP_NONCAUSAL_BWD, 16, 6, 2048, 32, 64, la.LA_F32) > 0
+    # the forward from a state keeps every segment's sums (and the CUDA-core
+    # path one more record), so it always needs a workspace
+    for shape in ((4, 8, 3072, 64, 64, la.LA_BF16), (1, 1, 64, 16, 16, la.LA_F32),
+                  (1, 1, 1, 64, 64, la.LA_BF16)):
+        assert la.la_workspace_bytes(la.LA_OP_CAUSAL_PREFILL, *shape) > 0
+    assert la.la_kernel_launches(la.LA_OP_CAUSAL_PREFILL, 4, 8, 3072, 64, 64, la.LA_BF16) == 3
+    assert la.la_kernel_launches(la.LA_OP_CAUSAL_PREFILL, 4, 8, 3072, 64, 64, la.LA_F32) == 4
     # invalid arguments size to 0
     assert la.la_workspace_bytes(la.LA_OP_CAUSAL_FWD, 0, 8, 3072, 64, 64, la.LA_BF16) == 0
     assert la.la_workspace_bytes(la.LA_OP_CAUSAL_FWD, 1, 8, 3072, 48, 64, la.LA_BF16) == 0
@@ -104,6 +111,17 @@ def test_other_calls_reject(linattn):
     assert L.la_decode_step(F, F, F, F, F, F, 1, 1, 64, 96, 0, None) == 2
     assert L.la_decode_step(F, F, F, F, F, F, 0, 1, 64, 64, 0, None) == 1
     assert L.la_decode_step(F, F, F, F, F, F, (1 << 20) + 1, 1, 64, 64, 0, None) == 1
+
+
+def test_prefill_rejects(linattn):
+    la = linattn
+    call = lambda S, Z, ws=None, wsb=0, N=64: la.lib().la_causal_prefill(
+        FAKE, FAKE, FAKE, FAKE, None, S, Z, ws, wsb, 1, 1, N, 16, 16, la.LA_F32, None)
+    assert call(None, FAKE) == la.LA_ERR_INVALID_ARG      # the state is required
+    assert call(FAKE, None) == la.LA_ERR_INVALID_ARG
+    assert call(FAKE + 4, FAKE) == la.LA_ERR_INVALID_ARG  # misaligned
+    assert call(FAKE, FAKE) == la.LA_ERR_WORKSPACE        # needs a workspace
+    assert call(FAKE, FAKE, N=0) == la.LA_ERR_INVALID_ARG
 
 
 def test_head_count_limits(linattn):

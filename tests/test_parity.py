@@ -90,6 +90,68 @@ def test_causal_workloads(cuda, linattn, name):
     print(name, errs)
 
 
+# ------------------------------------------------------------------ prefill
+
+def earlier_state(B, H, D, M, dtype, seed, P=37):
+    """(S, Z) as an earlier prompt of P tokens leaves them (oracle, fp64,
+    rounded to fp32 -- the GPU and the oracle both start from these values)."""
+    q, k, v, _ = causal_inputs(B, H, P, D, M, dtype, seed)
+    _, _, S, Z = oracle.causal_prefill(q, k, v)
+    return torch.from_numpy(S).float(), torch.from_numpy(Z).float()
+
+
+PREFILL = [
+    (1, 1, 1, 16, 16, "f32"),
+    (2, 3, 100, 32, 64, "f32"),
+    (1, 2, 1000, 64, 64, "f32"),     # several segments on the CUDA cores
+    (2, 1, 77, 16, 16, "bf16"),
+    # bf16, D = M = 64: the tensor cores
+    (1, 1, 1, 64, 64, "bf16"),
+    (1, 1, 100, 64, 64, "bf16"),     # one partial chunk, one segment
+    (3, 1, 1000, 64, 64, "bf16"),    # several segments, ragged tail
+    (40, 4, 300, 64, 64, "bf16"),    # more heads than SMs: one segment each
+    (4, 8, 3072, 64, 64, "bf16"),    # the 3072-token image workload's size
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,M,dtype", PREFILL)
+def test_causal_prefill(cuda, linattn, B, H, N, D, M, dtype):
+    """The causal form from a state (eq. 16-19 over a prompt): out, den and
+    the state after the sequence against the oracle, from the state an
+    earlier prompt left."""
+    q, k, v, _ = causal_inputs(B, H, N, D, M, dtype, 3100 + N)
+    S0, Z0 = earlier_state(B, H, D, M, dtype, 3200 + N)
+    qd, kd, vd, S, Z = _to(cuda, q, k, v, S0, Z0)
+    out, den, S, Z = linattn.causal_prefill(qd, kd, vd, S, Z)
+    torch.cuda.synchronize()
+    o_ref, den_ref, S_ref, Z_ref = oracle.causal_prefill(q, k, v, S0, Z0)
+    errs = {"out": rel_err(out, o_ref), "den": rel_err(den, den_ref), "S": rel_err(S, S_ref),
+            "Z": rel_err(Z, Z_ref)}
+    bad = {k_: e for k_, e in errs.items() if not e <= TOL[dtype]}
+    assert not bad, f"prefill B={B} H={H} N={N} D={D} M={M} {dtype}: {errs}"
+
+
+@pytest.mark.parametrize("D,M,dtype", [(64, 64, "bf16"), (32, 64, "f32")])
+def test_prefill_then_decode(cuda, linattn, D, M, dtype):
+    """A prompt through la_causal_prefill, the rest of the sequence token by
+    token through la_decode_step from the state it leaves: outputs and final
+    state are those of one pass over the whole sequence (oracle)."""
+    B, H, N, n1 = 2, 3, 300, 211
+    q, k, v, _ = causal_inputs(B, H, N, D, M, dtype, 77)
+    qd, kd, vd = _to(cuda, q, k, v)
+    head = lambda x: x[:, :, :n1].contiguous()
+    out1, _, S, Z = linattn.causal_prefill(head(qd), head(kd), head(vd))
+    ys = [linattn.decode_step(qd[:, :, t].contiguous(), kd[:, :, t].contiguous(),
+                              vd[:, :, t].contiguous(), S, Z) for t in range(n1, N)]
+    y = torch.stack(ys, dim=2)
+    torch.cuda.synchronize()
+    o_ref, _, S_ref, Z_ref = oracle.causal_prefill(q, k, v)
+    errs = {"prompt": rel_err(out1, o_ref[:, :, :n1]), "steps": rel_err(y, o_ref[:, :, n1:]),
+            "S": rel_err(S, S_ref), "Z": rel_err(Z, Z_ref)}
+    bad = {k_: e for k_, e in errs.items() if not e <= TOL[dtype]}
+    assert not bad, f"prefill + decode D={D} M={M} {dtype}: {errs}"
+
+
 def check_noncausal(la, dev, B, H, N, D, M, dtype, seed, len_range):
     lengths, q, k, v, g = noncausal_inputs(B, H, N, D, M, dtype, seed, len_range)
     qd, kd, vd, gd = _to(dev, q, k, v, g)
