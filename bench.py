@@ -387,9 +387,10 @@ def measure_e2e(la, torch, dev, q, k, v, g, out, den, wsf, wsb, B, H, N, D, M, d
 
 
 def secondary(la, torch, dev, flush, peaks, with_cpu=True):
-    """Non-causal fwd+bwd (long speech-like sequences with padding) and the
-    decode step (256 and 2048 streams x 8 heads), each against its roofline,
-    and (with_cpu) the fp64 oracle timed beside each on the host cores."""
+    """Non-causal fwd+bwd (long speech-like sequences with padding), the
+    prefill (causal forward from a state), and the decode step (256 and 2048
+    streams x 8 heads), each against its roofline, and (with_cpu) the fp64
+    oracle timed beside each on the host cores."""
     from kernelized_causal_attention_gb300.workloads import WORKLOADS, noncausal_inputs
     res = {}
     w = WORKLOADS["noncausal_speech_f32"]
@@ -424,6 +425,33 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True):
         "fp32_tflops": round(flops / (ms / 1e3) / 1e12, 2)}
     if with_cpu:
         res["noncausal_speech_f32"]["cpu_baseline"] = cpu_baseline_noncausal(q, k, v, g, lengths)
+
+    # prefill: the causal forward from a state, leaving the state after the
+    # sequence (the 3072-token image workload's shape; the state carries over
+    # from call to call like consecutive prompt segments)
+    from kernelized_causal_attention_gb300.workloads import causal_inputs
+    wc = WORKLOADS["causal_cifar_bf16"]
+    B, H, N, D, M = wc.B, wc.H, wc.N, wc.D, wc.M
+    q, k, v, _ = causal_inputs(B, H, N, D, M, wc.dtype, wc.seed)
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    out = torch.empty_like(vd)
+    den = torch.empty(B, H, N, device=dev)
+    S = torch.zeros(B, H, D, M, device=dev)
+    Z = torch.zeros(B, H, D, device=dev)
+    wp = la.workspace(la.LA_OP_CAUSAL_PREFILL, B, H, N, D, M, 1, dev)
+    pre = lambda: la.la_causal_prefill(qd, kd, vd, out, den, S, Z, wp, B, H, N, D, M, 1)
+    for _ in range(3):
+        pre()
+    (mp,), _ = time_calls([pre], 50, flush, torch, None, dev)
+    alg = B * H * N * (2 * (2 * D + M) + 2 * M + 4) + B * H * 2 * 4 * (D * M + D)
+    gbs = alg / (mp / 1e3) / 1e9
+    res["prefill_cifar_bf16"] = {
+        "value": round(B * N / (mp / 1e3), 1), "unit": "tokens/s", "ms_per_call": round(mp, 5),
+        "launches": la.la_kernel_launches(la.LA_OP_CAUSAL_PREFILL, B, H, N, D, M, 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": alg}}
+    if with_cpu:
+        res["prefill_cifar_bf16"]["cpu_baseline"] = cpu_baseline_prefill(q, k, v, B, H, N)
 
     for Bd in (256, 2048):
         Hd, Dd, Md = 8, 64, 64
@@ -517,6 +545,24 @@ def cpu_baseline_noncausal(q, k, v, g, lengths, budget_s=5.0):
             "cores": cores, "kind": "oracle",
             "sample": f"full workload (B={B}, H={H}, N={N}, lengths as the GPU line) x {reps}, "
                       f"{el:.1f} s, fp64, fwd+bwd"}
+
+
+def cpu_baseline_prefill(q, k, v, B, H, N, budget_s=5.0):
+    """The fp64 oracle's prefill (recurrent form from a zero state) on all host
+    cores over the full workload, repeated until about `budget_s` seconds."""
+    import oracle
+    cores = _cores(oracle)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.causal_prefill(q, k, v, nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 20:
+            break
+    return {"value": round(reps * B * N / el, 1), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"full workload (B={B}, H={H}, N={N}) x {reps}, {el:.1f} s, fp64, recurrent form"}
 
 
 def cpu_baseline_decode(B, H, D, M, steps=64, budget_s=5.0):
