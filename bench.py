@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--secondary-only", action="store_true",
                     help="run only the non-causal/decode measurements (one JSON object); for "
                          "profiling those kernels")
+    ap.add_argument("--sweep", action="store_true",
+                    help="sequence-length sweep N = 2^9 .. 2^16 with B * N fixed: causal fwd+bwd "
+                         "time and peak allocated memory per sample (one JSON object)")
     return ap.parse_args()
 
 
@@ -648,12 +651,70 @@ def run_secondary_only():
                                    with_cpu=False)}
 
 
+def run_sweep(steps=20):
+    """Causal attention and its gradients (la_causal_fwd + la_causal_bwd) for
+    N = 2^9 .. 2^16 with the batch inversely proportional to N (B * N = 2^16),
+    H = 8, D = M = 64, bf16 inputs: time and peak allocated device memory per
+    sample, the shape of the pages' memory/computation benchmark.  Peak memory
+    is torch's allocator high-water mark over the inputs, outputs, gradients
+    and workspaces (the library allocates nothing itself); time is the mean of
+    `steps` L2-flushed fwd+bwd pairs on CUDA events."""
+    import torch
+
+    import kernelized_causal_attention_gb300 as la
+    from kernelized_causal_attention_gb300.workloads import causal_inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    la.lib()
+    peaks = measured_peaks()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.zero_()
+    H, D, M, total = 8, 64, 64, 1 << 16
+    points = []
+    for e in range(9, 17):
+        N = 1 << e
+        B = total // N
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+        base = torch.cuda.memory_allocated(dev)
+        q, k, v, g = (t.to(dev) for t in causal_inputs(B, H, N, D, M, "bf16", 900 + e))
+        out = torch.empty_like(v)
+        den = torch.empty(B, H, N, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wf = la.workspace(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, 1, dev)
+        wb = la.workspace(la.LA_OP_CAUSAL_BWD, B, H, N, D, M, 1, dev)
+        fwd = lambda: la.la_causal_fwd(q, k, v, out, den, wf, B, H, N, D, M, 1)
+        bwd = lambda: la.la_causal_bwd(q, k, v, out, den, g, dq, dk, dv, wb, B, H, N, D, M, 1)
+        for _ in range(3):
+            fwd()
+            bwd()
+        (mf, mb), ms = time_calls([fwd, bwd], steps, flush, torch, None, dev)
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        alg = B * H * N * (2 * (2 * D + M) + 2 * M + 4 + 5 * 2 * 64 + 4 + 3 * 2 * 64)
+        gbs = alg / (ms / 1e3) / 1e9
+        points.append({"N": N, "B": B, "ms_fwd_bwd": round(ms, 5), "fwd_ms": round(mf, 5),
+                       "bwd_ms": round(mb, 5), "ms_per_sample": round(ms / B, 6),
+                       "peak_bytes": int(peak), "peak_bytes_per_sample": int(peak // B),
+                       "tokens_per_s": round(B * N / (ms / 1e3), 1),
+                       "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)})
+        del q, k, v, g, out, den, dq, dk, dv, wf, wb
+    la.check_device_status()
+    return {"sweep": "causal fwd+bwd, N = 2^9 .. 2^16, B * N = 2^16, H = 8, D = M = 64, bf16",
+            "data": "synthetic", "l2": "flushed before every timed pair", "points": points}
+
+
 def main():
     args = parse()
     dist = Dist()
     if args.secondary_only:
         if dist.rank == 0:
             print(json.dumps(run_secondary_only()), flush=True)
+        return
+    if args.sweep:
+        if dist.rank == 0:
+            print(json.dumps(run_sweep()), flush=True)
         return
     if args.impl == "reference":
         res = run_reference(args, dist)

@@ -83,6 +83,14 @@ def test_causal_small(cuda, linattn, B, H, N, D, M, dtype):
     check_causal(linattn, cuda, B, H, N, D, M, dtype, seed=1000 + N)
 
 
+@pytest.mark.parametrize("B,H,N,D,M,dtype", [
+    (1, 2, 65536, 64, 64, "bf16"),   # the sweep's longest sequence, tensor cores (74 segments)
+    (1, 1, 16384, 32, 32, "f32"),    # CUDA cores, 256 chunks
+])
+def test_causal_long(cuda, linattn, B, H, N, D, M, dtype):
+    check_causal(linattn, cuda, B, H, N, D, M, dtype, 5000 + N)
+
+
 @pytest.mark.parametrize("name", ["causal_tiny_f32", "causal_mnist_bf16", "causal_cifar_bf16"])
 def test_causal_workloads(cuda, linattn, name):
     w = WORKLOADS[name]
