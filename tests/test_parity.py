@@ -91,6 +91,35 @@ def test_causal_long(cuda, linattn, B, H, N, D, M, dtype):
     check_causal(linattn, cuda, B, H, N, D, M, dtype, 5000 + N)
 
 
+def test_causal_beyond_2_31_elements(cuda, linattn):
+    """Tensors of 1 x 160 x 2^18 x 64 = 2.7e9 elements (5.4 GB each in bf16):
+    the last head starts past element 2^31, so its reads and writes need
+    64-bit offsets.  Inputs are drawn on the GPU from a seeded generator; out,
+    den and dq of a token depend only on the tokens up to it, so the last
+    head's first 2048 tokens are checked against the oracle on that prefix."""
+    if torch.cuda.get_device_properties(cuda).total_memory < 120 * 2**30:
+        pytest.skip("needs about 60 GB of device memory")
+    B, H, N, D, M, P = 1, 160, 1 << 18, 64, 64, 2048
+    gen = torch.Generator(device=cuda).manual_seed(2031)
+    q, k, v, g = (torch.randn(B, H, N, D, generator=gen, device=cuda, dtype=torch.bfloat16)
+                  for _ in range(4))
+    out, den = linattn.causal_fwd(q, k, v)
+    dq, dk, dv = linattn.causal_bwd(q, k, v, out, den, g)
+    torch.cuda.synchronize()
+    h = H - 1
+    assert (h * N * D) > 2**31
+    pre = lambda t: t[:, h:h + 1, :P].cpu()
+    o_ref, den_ref = oracle.causal_fwd(pre(q), pre(k), pre(v))
+    dq_ref, _, _ = oracle.causal_bwd(pre(q), pre(k), pre(v), pre(g))
+    errs = {"out": rel_err(out[:, h:h + 1, :P], o_ref), "den": rel_err(den[:, h:h + 1, :P], den_ref),
+            "dq": rel_err(dq[:, h:h + 1, :P], dq_ref)}
+    assert all(e <= TOL["bf16"] for e in errs.values()), errs
+    # every element written: finite outputs and gradients at the far end too
+    for t in (out, dq, dk, dv):
+        assert torch.isfinite(t[:, h, -P:].float()).all()
+    linattn.check_device_status()
+
+
 @pytest.mark.parametrize("name", ["causal_tiny_f32", "causal_mnist_bf16", "causal_cifar_bf16"])
 def test_causal_workloads(cuda, linattn, name):
     w = WORKLOADS[name]
