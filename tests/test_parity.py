@@ -269,6 +269,36 @@ def test_noncausal_workload(cuda, linattn):
     print(w.name, errs)
 
 
+def test_noncausal_beyond_2_31_elements(cuda, linattn):
+    """fp32 tensors of 2 x 80 x 2^18 x 64 = 2.7e9 elements (10.7 GB each): the
+    second batch entry lies past element 2^31.  Its valid length is 2048, so
+    all of its outputs and gradients depend on its first 2048 tokens only:
+    its last head is checked against the oracle on those, and its padded
+    rows must be zero; the first entry runs all 2^18 tokens."""
+    if torch.cuda.get_device_properties(cuda).total_memory < 160 * 2**30:
+        pytest.skip("needs about 90 GB of device memory")
+    B, H, N, D, M, P = 2, 80, 1 << 18, 64, 64, 2048
+    gen = torch.Generator(device=cuda).manual_seed(2032)
+    q, k, v, g = (torch.randn(B, H, N, D, generator=gen, device=cuda) for _ in range(4))
+    lengths = torch.tensor([N, P], dtype=torch.int32, device=cuda)
+    out, den, S, Z = linattn.noncausal_fwd(q, k, v, lengths)
+    dq, dk, dv = linattn.noncausal_bwd(q, k, v, lengths, out, den, S, Z, g)
+    torch.cuda.synchronize()
+    b, h = 1, H - 1
+    assert (b * H + h) * N * D > 2**31
+    pre = lambda t: t[b:b + 1, h:h + 1, :P].cpu()
+    o_ref, den_ref, S_ref, Z_ref = oracle.noncausal_fwd(pre(q), pre(k), pre(v))
+    dq_ref, dk_ref, dv_ref = oracle.noncausal_bwd(pre(q), pre(k), pre(v), pre(g))
+    got = lambda t: t[b:b + 1, h:h + 1, :P]
+    errs = {"out": rel_err(got(out), o_ref), "den": rel_err(got(den), den_ref),
+            "S": rel_err(S[b:b + 1, h:h + 1], S_ref), "Z": rel_err(Z[b:b + 1, h:h + 1], Z_ref),
+            "dq": rel_err(got(dq), dq_ref), "dk": rel_err(got(dk), dk_ref), "dv": rel_err(got(dv), dv_ref)}
+    assert all(e <= TOL["f32"] for e in errs.values()), errs
+    for t in (out, den, dq, dk, dv):
+        assert torch.all(t[b, :, P:] == 0)
+    linattn.check_device_status()
+
+
 def run_decode(la, dev, B, H, D, M, dtype, seed, T, sample_heads=None, chunk=64):
     """Runs T steps on the GPU; checks y_t for every step and the final
     state against the oracle on a sample of heads (all heads if None)."""
