@@ -7,7 +7,9 @@
  * attention (§3.3, eq. 9-12), its cumulative-sum gradients (§3.3.1,
  * eq. 13-15, completed with the denominator by the quotient rule), the
  * non-causal form with one shared S and Z ("Linear Attention/zh", kernel
- * reformulation), and the RNN-form decode step (§3.4, eq. 16-19).
+ * reformulation), the RNN-form decode step (§3.4, eq. 16-19), and the
+ * prefill that joins the two (the causal form started from a state, which
+ * hands its final state to the decode step).
  *
  * Conventions shared by every call
  * --------------------------------

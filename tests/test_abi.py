@@ -20,7 +20,8 @@ def declared_symbols():
 def test_header_declares_the_abi():
     names = declared_symbols()
     for n in ("la_causal_fwd", "la_causal_bwd", "la_noncausal_fwd", "la_noncausal_bwd",
-              "la_decode_step", "la_workspace_bytes", "la_status_string", "la_version"):
+              "la_decode_step", "la_causal_prefill", "la_workspace_bytes", "la_status_string",
+              "la_version", "la_device_status", "la_selftest_wait"):
         assert n in names
 
 
