@@ -521,7 +521,7 @@ def cpu_baseline(q, k, v, g, B, H, N, budget_s=12.0):
         oracle.causal_bwd(q, k, v, g, "recurrent", nthreads=cores)
         reps += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or reps >= 50:
+        if el >= budget_s or reps >= 200:
             break
     return {"value": round(reps * B * N / el, 1), "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
