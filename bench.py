@@ -189,9 +189,10 @@ def causal_bytes(B, H, N, D, M, elt):
 
 # ------------------------------------------------------------------ our arm
 
-def time_calls(fns, steps, flush, torch, dist, dev):
+def time_calls(fns, steps, flush, torch, dist, dev, with_median=False):
     """Runs `steps` iterations of the call sequence `fns`, with an L2 flush
-    before each; returns per-call mean ms and per-step mean ms (device time)."""
+    before each; returns per-call mean ms and per-step mean ms (device time),
+    and with_median the per-step median ms as well."""
     n = len(fns)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
     for i in range(steps):
@@ -203,8 +204,10 @@ def time_calls(fns, steps, flush, torch, dist, dev):
     torch.cuda.synchronize()
     per_call = [statistics.fmean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
                 for j in range(n)]
-    per_step = statistics.fmean(ev[i][0].elapsed_time(ev[i][n]) for i in range(steps))
-    return per_call, per_step
+    steps_ms = [ev[i][0].elapsed_time(ev[i][n]) for i in range(steps)]
+    if with_median:
+        return per_call, statistics.fmean(steps_ms), statistics.median(steps_ms)
+    return per_call, statistics.fmean(steps_ms)
 
 
 def run_ours(args, dist):
@@ -244,11 +247,14 @@ def run_ours(args, dist):
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    (ms_fwd, ms_bwd), ms_step = time_calls([fwd, bwd], args.steps, flush, torch, dist, dev)
+    (ms_fwd, ms_bwd), ms_step, ms_median = time_calls([fwd, bwd], args.steps, flush, torch, dist,
+                                                      dev, with_median=True)
     torch.cuda.synchronize()
     dist.barrier()
     wall = time.perf_counter() - t0
     clk = clocks.stop()
+    # the same step with L2 left warm (inputs partly resident), outside the timed region
+    _, ms_warm = time_calls([fwd, bwd], 200, lambda: None, torch, dist, dev)
 
     ms_step_max = dist.max(ms_step, dev)
     ms_bwd_max = dist.max(ms_bwd, dev)
@@ -283,7 +289,11 @@ def run_ours(args, dist):
                       "seq_len": N, "parallelism": f"replicas{dist.world}",
                       "l2": "flushed before every timed step (256 MiB write, untimed)"},
            "roofline": roofline, "step_roofline": step_roof, "e2e": e2e,
-           "gpu_launches": launches, "clocks": clk, "wall_s_timed_region": round(wall, 3)}
+           "gpu_launches": launches, "clocks": clk, "wall_s_timed_region": round(wall, 3),
+           "median_ms_per_step": round(dist.max(ms_median, dev), 5),
+           "warm": {"ms_per_step": round(dist.max(ms_warm, dev), 5),
+                    "value": round(dist.world * tokens / (dist.max(ms_warm, dev) / 1e3), 1),
+                    "steps": 200, "l2": "not flushed between steps"}}
     if not args.no_secondary:
         res["secondary"] = secondary(la, torch, dev, flush, peaks,
                                      with_cpu=dist.rank == 0 and not args.no_cpu)
