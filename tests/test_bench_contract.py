@@ -1,0 +1,39 @@
+"""bench.py's JSON line on the CPU: the reference arm (the fp64 oracle timed on
+the host cores) prints one complete line, and our arm without a GPU fails
+loudly instead of printing a number (there is no CPU fallback)."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args, env=None):
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                          capture_output=True, text=True, timeout=600, env=env)
+
+
+def test_reference_arm_prints_one_complete_line():
+    r = _run("--impl", "reference", "--steps", "1", "--warmup", "3")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["unit"] == "tokens/s" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["config"]["workload"] == "causal_cifar_bf16"
+    assert d["config"]["N"] == 3072 and d["config"]["D"] == 64
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+    assert abs(d["ms_per_step"] * 1e-3 * d["value"] - 4 * 3072) / (4 * 3072) < 1e-3
+
+
+def test_our_arm_without_a_gpu_fails_loudly():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = _run("--steps", "1", "--warmup", "3", "--no-secondary", "--no-cpu", env=env)
+    assert r.returncode != 0
+    assert r.stdout.strip() == ""
