@@ -1064,11 +1064,14 @@ cudaError_t run_bwd(const T* q, const T* k, const T* v, const int* lengths, cons
 }  // namespace
 
 // CTAs per (b, h): a power of two (clusters of 1, 2, 4 or 8 CTAs pack the
-// GPCs without holes), at most one per 128-token chunk, and about three
-// waves of one CTA per SM over all (b, h).
+// GPCs without holes), at most one per 128-token chunk, and about one and a
+// half waves of one CTA per SM over all (b, h): every CTA pays fixed costs
+// (first loads, the cluster barrier and sum, the last epilogue), so fewer,
+// longer CTAs win once the SMs are full (96 heads of 800-2048 tokens: 2 per
+// head beat 4 by 4-12 us per call, 1 per head leaves SMs idle).
 int noncausal_tc_nseg(int BH, int N) {
   const int nch = (N + CH - 1) / CH;
-  const int fill = (3 * 152 + BH - 1) / BH;
+  const int fill = (3 * 152 / 2 + BH - 1) / BH;
   int n = kMaxSeg;
   while (n > 1 && (n > nch || n > fill)) n >>= 1;
   return n;
