@@ -299,6 +299,50 @@ def test_noncausal_beyond_2_31_elements(cuda, linattn):
     linattn.check_device_status()
 
 
+def test_every_output_written_launch_after_launch(cuda, linattn):
+    """Outputs are filled with NaN before every call, over a sequence of
+    non-causal and causal calls in both dtypes and several cluster and
+    segment counts: every element must come back finite (written by the
+    kernels, and nothing one launch leaves in shared or tensor memory leaks
+    into the next)."""
+    la, nan = linattn, float("nan")
+    nc_cases = [(2, 3, 1000, "bf16", (0, 1000), 3000), (2, 3, 1000, "f32", (0, 1000), 3000),
+                (4, 2, 300, "f32", None, 0), (4, 2, 300, "bf16", None, 0),
+                (5, 1, 2500, "f32", (1, 2500), 4500), (100, 10, 100, "f32", (0, 100), 2100),
+                (2, 3, 1000, "bf16", (0, 1000), 77), (3, 2, 700, "bf16", (0, 20), 5)]
+    for B, H, N, dt, lr, seed in nc_cases:
+        D = M = 64
+        lengths, q, k, v, g = noncausal_inputs(B, H, N, D, M, dt, seed, lr)
+        qd, kd, vd, gd, ld = _to(cuda, q, k, v, g, lengths)
+        code = la.LA_F32 if dt == "f32" else la.LA_BF16
+        out, dq, dk, dv = (torch.full_like(x, nan) for x in (vd, qd, kd, vd))
+        den = torch.full((B, H, N), nan, device=cuda)
+        S = torch.full((B, H, D, M), nan, device=cuda)
+        Z = torch.full((B, H, D), nan, device=cuda)
+        la.la_noncausal_fwd(qd, kd, vd, ld, out, den, S, Z, None, B, H, N, D, M, code)
+        la.la_noncausal_bwd(qd, kd, vd, ld, out, den, S, Z, gd, dq, dk, dv, None, B, H, N, D, M,
+                            code)
+        torch.cuda.synchronize()
+        for name, t in (("out", out), ("den", den), ("S", S), ("Z", Z), ("dq", dq), ("dk", dk),
+                        ("dv", dv)):
+            assert torch.isfinite(t.float()).all(), f"non-causal {B}x{H}x{N} {dt} seed {seed}: {name}"
+    for B, H, N, D, M, dt in [(2, 3, 1000, 64, 64, "bf16"), (1, 2, 333, 64, 32, "f32"),
+                              (4, 8, 3072, 64, 64, "bf16"), (3, 1, 129, 16, 64, "f32")]:
+        q, k, v, g = causal_inputs(B, H, N, D, M, dt, 6000 + N)
+        qd, kd, vd, gd = _to(cuda, q, k, v, g)
+        code = la.LA_F32 if dt == "f32" else la.LA_BF16
+        out, dq, dk, dv = (torch.full_like(x, nan) for x in (vd, qd, kd, vd))
+        den = torch.full((B, H, N), nan, device=cuda)
+        wf = la.workspace(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, code, cuda)
+        wb = la.workspace(la.LA_OP_CAUSAL_BWD, B, H, N, D, M, code, cuda)
+        la.la_causal_fwd(qd, kd, vd, out, den, wf, B, H, N, D, M, code)
+        la.la_causal_bwd(qd, kd, vd, out, den, gd, dq, dk, dv, wb, B, H, N, D, M, code)
+        torch.cuda.synchronize()
+        for name, t in (("out", out), ("den", den), ("dq", dq), ("dk", dk), ("dv", dv)):
+            assert torch.isfinite(t.float()).all(), f"causal {B}x{H}x{N} {dt}: {name}"
+    la.check_device_status()
+
+
 def run_decode(la, dev, B, H, D, M, dtype, seed, T, sample_heads=None, chunk=64):
     """Runs T steps on the GPU; checks y_t for every step and the final
     state against the oracle on a sample of heads (all heads if None)."""
