@@ -301,8 +301,8 @@ def test_noncausal_beyond_2_31_elements(cuda, linattn):
 
 def test_every_output_written_launch_after_launch(cuda, linattn):
     """Outputs are filled with NaN before every call, over a sequence of
-    non-causal and causal calls in both dtypes and several cluster and
-    segment counts: every element must come back finite (written by the
+    non-causal, causal, prefill and decode calls in both dtypes and several
+    cluster and segment counts: every element must come back finite (written by the
     kernels, and nothing one launch leaves in shared or tensor memory leaks
     into the next)."""
     la, nan = linattn, float("nan")
@@ -339,6 +339,20 @@ def test_every_output_written_launch_after_launch(cuda, linattn):
         la.la_causal_bwd(qd, kd, vd, out, den, gd, dq, dk, dv, wb, B, H, N, D, M, code)
         torch.cuda.synchronize()
         for name, t in (("out", out), ("den", den), ("dq", dq), ("dk", dk), ("dv", dv)):
+            assert torch.isfinite(t.float()).all(), f"causal {B}x{H}x{N} {dt}: {name}"
+        # the same inputs through the prefill (from a finite state) and one decode step
+        S0 = torch.rand(B, H, D, M, device=cuda)
+        Z0 = torch.rand(B, H, D, device=cuda) + 1.0
+        wp = la.workspace(la.LA_OP_CAUSAL_PREFILL, B, H, N, D, M, code, cuda)
+        out.fill_(nan)
+        den.fill_(nan)
+        la.la_causal_prefill(qd, kd, vd, out, den, S0, Z0, wp, B, H, N, D, M, code)
+        y = torch.full_like(vd[:, :, 0], nan)
+        la.la_decode_step(qd[:, :, 0].contiguous(), kd[:, :, 0].contiguous(), vd[:, :, 0].contiguous(),
+                          S0, Z0, y, B, H, D, M, code)
+        torch.cuda.synchronize()
+        for name, t in (("prefill out", out), ("prefill den", den), ("S_N", S0), ("Z_N", Z0),
+                        ("decode y", y)):
             assert torch.isfinite(t.float()).all(), f"causal {B}x{H}x{N} {dt}: {name}"
     la.check_device_status()
 
