@@ -17,8 +17,9 @@
 // more bits, so n terms leave a remainder below 2^-9n |x|.  With two terms
 // a product is a_0 b_0 + a_0 b_1 + a_1 b_0 (error below 2^-16 |a| |b|); with
 // three, a_0 b_0 + a_0 b_1 + a_1 b_0 + a_0 b_2 + a_1 b_1 + a_2 b_0 (below
-// 2^-25 |a| |b|).  Products accumulate in fp32 in two 64-column halves of a
-// tensor-memory accumulator that the epilogue adds:
+// 2^-25 |a| |b|).  Token-form products accumulate in fp32 in two 64-column
+// halves of a tensor-memory accumulator that the epilogue adds (the state
+// form takes its products as quadrants instead, see mma_state):
 //   two terms:   A_0 [B_0 | B_1] (N = 128), A_1 B_0 -> first half
 //   three terms: A_0 [B_0 | B_1], A_1 [B_0 | B_1], A_0 B_2 -> first half,
 //                A_2 B_0 -> second half
@@ -29,7 +30,7 @@
 //
 // Layout of the work.  One thread-block cluster of nseg CTAs per (b, h); the
 // valid rows are cut into 128-token chunks and every CTA takes an equal run.
-//  forward   phase 1: S~ += phi(K)^T V                  (M = 64, state form)
+//  forward   phase 1: S~ += phi(K)^T V                  (state form, two A terms stacked to M = 128)
 //            cluster sum of the partial S, Z through distributed shared memory
 //            phase 2: O~ = phi(Q) S                     (M = 128, token form)
 //  backward  phase 1: R~ += phi(Q)^T gt, dQ~ = gt S^T
