@@ -357,6 +357,39 @@ def test_every_output_written_launch_after_launch(cuda, linattn):
     la.check_device_status()
 
 
+@pytest.mark.parametrize("D,M,dtype", [(64, 64, "bf16"), (32, 64, "f32")])
+def test_den_is_optional(cuda, linattn, D, M, dtype):
+    """den may be NULL for the causal forward, the prefill and the non-causal
+    forward: the other outputs are the same bits as with den."""
+    la = linattn
+    B, H, N = 2, 3, 700
+    q, k, v, _ = causal_inputs(B, H, N, D, M, dtype, 8800)
+    qd, kd, vd = _to(cuda, q, k, v)
+    code = la.LA_F32 if dtype == "f32" else la.LA_BF16
+    ws = la.workspace(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, code, cuda)
+    o1, o2 = torch.empty_like(vd), torch.empty_like(vd)
+    den = torch.empty(B, H, N, device=cuda)
+    la.la_causal_fwd(qd, kd, vd, o1, den, ws, B, H, N, D, M, code)
+    la.la_causal_fwd(qd, kd, vd, o2, None, ws, B, H, N, D, M, code)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    wp = la.workspace(la.LA_OP_CAUSAL_PREFILL, B, H, N, D, M, code, cuda)
+    S1, Z1 = torch.rand(B, H, D, M, device=cuda), torch.rand(B, H, D, device=cuda) + 1.0
+    S2, Z2 = S1.clone(), Z1.clone()
+    la.la_causal_prefill(qd, kd, vd, o1, den, S1, Z1, wp, B, H, N, D, M, code)
+    la.la_causal_prefill(qd, kd, vd, o2, None, S2, Z2, wp, B, H, N, D, M, code)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(S1, S2) and torch.equal(Z1, Z2)
+    if D == M:
+        wn = la.workspace(la.LA_OP_NONCAUSAL_FWD, B, H, N, D, M, code, cuda)
+        Sa, Za = torch.empty(B, H, D, M, device=cuda), torch.empty(B, H, D, device=cuda)
+        Sb, Zb = torch.empty_like(Sa), torch.empty_like(Za)
+        la.la_noncausal_fwd(qd, kd, vd, None, o1, den, Sa, Za, wn, B, H, N, D, M, code)
+        la.la_noncausal_fwd(qd, kd, vd, None, o2, None, Sb, Zb, wn, B, H, N, D, M, code)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(Sa, Sb) and torch.equal(Za, Zb)
+
+
 def run_decode(la, dev, B, H, D, M, dtype, seed, T, sample_heads=None, chunk=64):
     """Runs T steps on the GPU; checks y_t for every step and the final
     state against the oracle on a sample of heads (all heads if None)."""
