@@ -20,6 +20,11 @@ def test_threads_do_not_change_results(orc):
     b = orc.causal_bwd(q, k, v, g, "recurrent", nthreads=4)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+    S0, Z0 = P.rand((2, 3, 8, 6), 5), 1.0 + np.abs(P.rand((2, 3, 8), 6))
+    a = orc.causal_prefill(q, k, v, S0, Z0, nthreads=1)
+    b = orc.causal_prefill(q, k, v, S0, Z0, nthreads=4)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
 
 
 def test_fd_at_tiny_workload_size(orc):
