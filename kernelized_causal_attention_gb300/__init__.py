@@ -104,6 +104,9 @@ def _p(t):
         return None
     if not isinstance(t, torch.Tensor):
         return int(t)  # a raw address
+    if not t.is_cuda:
+        # the library takes device pointers; a host address would reach a kernel
+        raise ValueError("tensors must be on a CUDA device")
     if not t.is_contiguous():
         raise ValueError("tensors must be contiguous")
     return t.data_ptr()

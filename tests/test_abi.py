@@ -145,3 +145,14 @@ def test_binding_requires_library(monkeypatch, tmp_path):
     monkeypatch.setattr(la, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         la.lib()
+
+
+def test_binding_refuses_host_tensors(linattn):
+    """The binding passes device pointers only: a CPU tensor is refused before
+    anything reaches the library (no GPU needed)."""
+    import torch
+    q = torch.zeros(1, 1, 64, 16)
+    with pytest.raises(ValueError, match="CUDA device"):
+        linattn.la_causal_fwd(q, q, q, q, None, None, 1, 1, 64, 16, 16, linattn.LA_F32)
+    with pytest.raises(ValueError, match="CUDA device"):
+        linattn.la_decode_step(q[0, 0, 0], q[0, 0, 0], q[0, 0, 0], q, q, q, 1, 1, 16, 16, linattn.LA_F32)
