@@ -37,3 +37,26 @@ def test_our_arm_without_a_gpu_fails_loudly():
     r = _run("--steps", "1", "--warmup", "3", "--no-secondary", "--no-cpu", env=env)
     assert r.returncode != 0
     assert r.stdout.strip() == ""
+
+
+def _bench():
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    import bench
+    return bench
+
+
+def test_algorithmic_bytes_per_token_head():
+    """Every input read once, every output written once: bf16, D = M = 64 gives
+    516 B (fwd: q, k, v, out, den) and 1028 B (bwd: q, k, v, out, dout, den,
+    dq, dk, dv) per token-head."""
+    fwd, bwd = _bench().causal_bytes(4, 8, 3072, 64, 64, 2)
+    th = 4 * 8 * 3072
+    assert fwd == 516 * th and bwd == 1028 * th
+
+
+def test_stored_traffic_only_for_the_sources_it_was_taken_on(monkeypatch):
+    b = _bench()
+    assert b.stored_traffic("la_causal_bwd") is not None  # the committed summary matches
+    monkeypatch.setattr(b, "kernel_source_hash", lambda: "0000000000000000")
+    assert b.stored_traffic("la_causal_bwd") is None
