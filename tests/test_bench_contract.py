@@ -57,6 +57,8 @@ def test_algorithmic_bytes_per_token_head():
 
 def test_stored_traffic_only_for_the_sources_it_was_taken_on(monkeypatch):
     b = _bench()
-    assert b.stored_traffic("la_causal_bwd") is not None  # the committed summary matches
+    stored = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+    monkeypatch.setattr(b, "kernel_source_hash", lambda: stored["source_hash"])
+    assert b.stored_traffic("la_causal_bwd") == stored["per_call_dram_bytes"]["la_causal_bwd"]
     monkeypatch.setattr(b, "kernel_source_hash", lambda: "0000000000000000")
     assert b.stored_traffic("la_causal_bwd") is None
