@@ -156,3 +156,23 @@ def test_binding_refuses_host_tensors(linattn):
         linattn.la_causal_fwd(q, q, q, q, None, None, 1, 1, 64, 16, 16, linattn.LA_F32)
     with pytest.raises(ValueError, match="CUDA device"):
         linattn.la_decode_step(q[0, 0, 0], q[0, 0, 0], q[0, 0, 0], q, q, q, 1, 1, 16, 16, linattn.LA_F32)
+
+
+def test_kernel_launch_counts(linattn):
+    """The launch accounting behind bench.py's gpu_launches, per path."""
+    la = linattn
+    n = la.la_kernel_launches
+    # causal, tensor cores: a state pass only when a head has several segments
+    assert n(la.LA_OP_CAUSAL_FWD, 4, 8, 3072, 64, 64, la.LA_BF16) == 2
+    assert n(la.LA_OP_CAUSAL_FWD, 1, 160, 3072, 64, 64, la.LA_BF16) == 1   # one segment per head
+    assert n(la.LA_OP_CAUSAL_BWD, 4, 8, 3072, 64, 64, la.LA_BF16) == 2
+    # causal, CUDA cores: partial sums + scan + main with several segments
+    assert n(la.LA_OP_CAUSAL_FWD, 1, 1, 4096, 64, 64, la.LA_F32) == 3
+    assert n(la.LA_OP_CAUSAL_FWD, 1, 1, 64, 16, 16, la.LA_F32) == 1
+    # non-causal: one launch per direction on the tensor cores
+    for dt in (la.LA_F32, la.LA_BF16):
+        assert n(la.LA_OP_NONCAUSAL_FWD, 16, 6, 2048, 64, 64, dt) == 1
+        assert n(la.LA_OP_NONCAUSAL_BWD, 16, 6, 2048, 64, 64, dt) == 1
+    assert n(la.LA_OP_DECODE, 256, 8, 1, 64, 64, la.LA_F32) == 1
+    # invalid sizes count no launches
+    assert n(la.LA_OP_CAUSAL_FWD, 0, 8, 3072, 64, 64, la.LA_BF16) == 0
