@@ -58,17 +58,21 @@
 extern "C" {
 #endif
 
-/* status codes */
-#define LA_OK 0
-#define LA_ERR_INVALID_ARG 1 /* null/misaligned pointer, bad size, bad dtype */
-#define LA_ERR_UNSUPPORTED 2 /* valid but unsupported (D or M not in the set) */
-#define LA_ERR_CUDA 3        /* a CUDA launch or runtime call failed */
-#define LA_ERR_WORKSPACE 4   /* workspace missing or smaller than required */
-#define LA_ERR_TIMEOUT 5     /* a bounded wait inside a kernel ran out (la_device_status) */
+/* Status codes.  la_status is an int in the ABI (every call returns one);
+ * the values are fixed. */
+typedef int la_status;
+enum {
+  LA_OK = 0,
+  LA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, bad dtype */
+  LA_ERR_UNSUPPORTED = 2, /* valid but unsupported (D or M not in the set) */
+  LA_ERR_CUDA = 3,        /* a CUDA launch or runtime call failed */
+  LA_ERR_TIMEOUT = 4,     /* a bounded wait inside a kernel ran out (la_device_status) */
+  LA_ERR_WORKSPACE = 5    /* workspace missing or smaller than required */
+};
 
-/* element types */
-#define LA_F32 0
-#define LA_BF16 1
+/* Element types.  la_dtype is an int in the ABI. */
+typedef int la_dtype;
+enum { LA_F32 = 0, LA_BF16 = 1 };
 
 /* operation ids for la_workspace_bytes */
 #define LA_OP_CAUSAL_FWD 0
@@ -79,18 +83,18 @@ extern "C" {
 #define LA_OP_CAUSAL_PREFILL 5
 
 /* Human-readable name of a status code (static string, never NULL). */
-const char* la_status_string(int status);
+const char* la_status_string(la_status status);
 
 /* ABI version of this header (major * 100 + minor). */
 int la_version(void);
 
 /* Bytes of device workspace the operation needs for these sizes; 0 when it
  * needs none or when the arguments are invalid. */
-size_t la_workspace_bytes(int op, int B, int H, int N, int D, int M, int dtype);
+size_t la_workspace_bytes(int op, int B, int H, int N, int D, int M, la_dtype dtype);
 
 /* Number of kernel launches one call of `op` makes for these sizes (for
  * launch accounting by callers and benchmarks); 0 for invalid arguments. */
-int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype);
+int la_kernel_launches(int op, int B, int H, int N, int D, int M, la_dtype dtype);
 
 /*
  * Causal forward, eq. 9-12:
@@ -99,9 +103,9 @@ int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype);
  * Inputs q, k, v; outputs out (dtype) and den (float, may be NULL when no
  * backward pass follows; la_causal_bwd needs it).
  */
-int la_causal_fwd(const void* q, const void* k, const void* v, void* out, float* den,
+la_status la_causal_fwd(const void* q, const void* k, const void* v, void* out, float* den,
                   void* workspace, size_t workspace_bytes, int B, int H, int N, int D,
-                  int M, int dtype, void* stream);
+                  int M, la_dtype dtype, void* stream);
 
 /*
  * Causal backward: gradients of L = sum_i dout_i . out_i with respect to q, k
@@ -110,10 +114,10 @@ int la_causal_fwd(const void* q, const void* k, const void* v, void* out, float*
  * terms.  No S_i is stored.  out and den are the forward's outputs.
  * Outputs dq, dk (dtype, [B][H][N][D]) and dv ([B][H][N][M]).
  */
-int la_causal_bwd(const void* q, const void* k, const void* v, const void* out,
+la_status la_causal_bwd(const void* q, const void* k, const void* v, const void* out,
                   const float* den, const void* dout, void* dq, void* dk, void* dv,
                   void* workspace, size_t workspace_bytes, int B, int H, int N, int D,
-                  int M, int dtype, void* stream);
+                  int M, la_dtype dtype, void* stream);
 
 /*
  * Prefill: the causal forward started from the state (S, Z) instead of zero,
@@ -128,9 +132,9 @@ int la_causal_bwd(const void* q, const void* k, const void* v, const void* out,
  * LA_OP_CAUSAL_PREFILL, ...) bytes of workspace; other arguments and errors
  * as la_causal_fwd.
  */
-int la_causal_prefill(const void* q, const void* k, const void* v, void* out, float* den,
+la_status la_causal_prefill(const void* q, const void* k, const void* v, void* out, float* den,
                       float* S, float* Z, void* workspace, size_t workspace_bytes, int B, int H,
-                      int N, int D, int M, int dtype, void* stream);
+                      int N, int D, int M, la_dtype dtype, void* stream);
 
 /*
  * la_causal_fwd for callers that cannot allocate device memory: the same
@@ -144,15 +148,19 @@ int la_causal_prefill(const void* q, const void* k, const void* v, void* out, fl
  *    scratch than the array holds (la_workspace_bytes(LA_OP_CAUSAL_FWD, ...) >
  *    LA_NOALLOC_SCRATCH_BYTES); other errors as la_causal_fwd.
  *  - The first call on a device looks up the array's device address (with
- *    that device current); make that first call before any stream capture.
+ *    that device current) and keeps it for later calls; make that first call
+ *    before any stream capture, and do not reset the device (cudaDeviceReset)
+ *    after it, since the kept address would then be stale.
+ *  - Argument errors are reported exactly as la_causal_fwd reports them, and
+ *    before anything touches the device.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *  - Every call on a device shares the one array, which keeps the last call's
  *    contents; calls that overlap on the GPU (other streams, other threads)
  *    race on it, so order them on one stream or serialise them.
  */
 #define LA_NOALLOC_SCRATCH_BYTES (4u << 20)
-int la_causal_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* den,
-                          int B, int H, int N, int D, int M, int dtype, void* stream);
+la_status la_causal_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* den,
+                          int B, int H, int N, int D, int M, la_dtype dtype, void* stream);
 
 /*
  * Non-causal forward with one shared state per (b, h):
@@ -162,9 +170,9 @@ int la_causal_fwd_noalloc(const void* q, const void* k, const void* v, void* out
  * or NULL for "all N".  Outputs out, den (0 on padded rows), S and Z (both
  * required: the backward pass reads them).
  */
-int la_noncausal_fwd(const void* q, const void* k, const void* v, const int* lengths,
+la_status la_noncausal_fwd(const void* q, const void* k, const void* v, const int* lengths,
                      void* out, float* den, float* S, float* Z, void* workspace,
-                     size_t workspace_bytes, int B, int H, int N, int D, int M, int dtype,
+                     size_t workspace_bytes, int B, int H, int N, int D, int M, la_dtype dtype,
                      void* stream);
 
 /*
@@ -172,10 +180,10 @@ int la_noncausal_fwd(const void* q, const void* k, const void* v, const int* len
  * rows; eq. 13-15 with full sums in place of cumulative ones.  Padded rows
  * of dq, dk, dv are written as 0.  out, den, S, Z come from la_noncausal_fwd.
  */
-int la_noncausal_bwd(const void* q, const void* k, const void* v, const int* lengths,
+la_status la_noncausal_bwd(const void* q, const void* k, const void* v, const int* lengths,
                      const void* out, const float* den, const float* S, const float* Z,
                      const void* dout, void* dq, void* dk, void* dv, void* workspace,
-                     size_t workspace_bytes, int B, int H, int N, int D, int M, int dtype,
+                     size_t workspace_bytes, int B, int H, int N, int D, int M, la_dtype dtype,
                      void* stream);
 
 /*
@@ -186,8 +194,8 @@ int la_noncausal_bwd(const void* q, const void* k, const void* v, const int* len
  * zeros for eq. 16-17).  q, k [B][H][D], v and y [B][H][M] in dtype.
  * Needs no workspace.
  */
-int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z,
-                   void* y, int B, int H, int D, int M, int dtype, void* stream);
+la_status la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z,
+                   void* y, int B, int H, int D, int M, la_dtype dtype, void* stream);
 
 /*
  * Reads the status word of the current GPU after all work queued on
@@ -201,7 +209,7 @@ int la_decode_step(const void* q, const void* k, const void* v, float* S, float*
  * compute call) looks up the word's device address with that device
  * current.
  */
-int la_device_status(void* stream, int clear, int* code);
+la_status la_device_status(void* stream, int clear, int* code);
 
 /*
  * Diagnostic: launches on `stream` one kernel that waits, with the bounded
@@ -211,7 +219,7 @@ int la_device_status(void* stream, int clear, int* code);
  * host as LA_ERR_TIMEOUT and that the context stays usable.  Returns
  * LA_ERR_INVALID_ARG for a limit outside the range (nothing launched).
  */
-int la_selftest_wait(void* stream, unsigned long long limit_ns);
+la_status la_selftest_wait(void* stream, unsigned long long limit_ns);
 
 #ifdef __cplusplus
 }

@@ -29,7 +29,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "liblinattn.so")
 
-LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_WORKSPACE, LA_ERR_TIMEOUT = range(6)
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
 LA_F32, LA_BF16 = 0, 1
 (LA_OP_CAUSAL_FWD, LA_OP_CAUSAL_BWD, LA_OP_NONCAUSAL_FWD, LA_OP_NONCAUSAL_BWD, LA_OP_DECODE,
  LA_OP_CAUSAL_PREFILL) = range(6)

@@ -63,6 +63,18 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
 
 }  // namespace
 
+namespace la {
+
+int causal_fwd_check(const void* q, const void* k, const void* v, const void* out,
+                     const float* den, int B, int H, int N, int D, int M, int dtype) {
+  int rc = check_shape(B, H, N, D, M, dtype);
+  if (rc == LA_OK) rc = check_ptrs({q, k, v, out});
+  if (rc == LA_OK) rc = check_opt_ptr(den);
+  return rc;
+}
+
+}  // namespace la
+
 #define LA_TRY(x)              \
   do {                         \
     const int rc_ = (x);       \
@@ -83,7 +95,7 @@ const char* la_status_string(int status) {
   }
 }
 
-int la_version(void) { return 100; }
+int la_version(void) { return 200; }
 
 size_t la_workspace_bytes(int op, int B, int H, int N, int D, int M, int dtype) {
   if (op == LA_OP_DECODE) return 0;
@@ -112,9 +124,7 @@ int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype) {
 int la_causal_fwd(const void* q, const void* k, const void* v, void* out, float* den,
                   void* workspace, size_t workspace_bytes, int B, int H, int N, int D, int M,
                   int dtype, void* stream) {
-  LA_TRY(check_shape(B, H, N, D, M, dtype));
-  LA_TRY(check_ptrs({q, k, v, out}));
-  LA_TRY(check_opt_ptr(den));
+  LA_TRY(la::causal_fwd_check(q, k, v, out, den, B, H, N, D, M, dtype));
   const Shape s{B, H, N, D, M, dtype};
   LA_TRY(check_ws(LA_OP_CAUSAL_FWD, s, workspace, workspace_bytes));
   if (la::tc_eligible(s))

@@ -696,7 +696,7 @@ BwdWs bwd_ws(float* ws, int BH, int N, const BwdPlan& pl) {
 }  // namespace
 
 // workspace: records [BH][nsub][REC] | gt, phi(Q), phi(K) bf16 [BH][N][64] |
-// gam fp32 [BH][N] | status word
+// gam fp32 [BH][N]
 size_t causal_bwd_tc_ws_floats(const Shape& s) {
   const int BH = s.B * s.H;
   return bwd_ws(nullptr, BH, s.N, bwd_plan(BH, s.N)).floats;

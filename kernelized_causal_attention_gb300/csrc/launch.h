@@ -33,6 +33,11 @@ inline SegPlan plan_segments(int BH, int N, int chunk = kChunk, int target = kTa
   return p;
 }
 
+// The argument checks of la_causal_fwd other than the workspace (shape,
+// dtype, pointers): LA_OK or the error code that call would return.
+int causal_fwd_check(const void* q, const void* k, const void* v, const void* out,
+                     const float* den, int B, int H, int N, int D, int M, int dtype);
+
 struct Shape {
   int B, H, N, D, M;
   int dtype;  // 0 = fp32, 1 = bf16

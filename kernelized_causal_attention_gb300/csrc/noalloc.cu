@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "../../include/linattn.h"
+#include "launch.h"
 
 namespace {
 
@@ -25,7 +26,10 @@ std::mutex g_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once per
-// device (the array's name is only a host-side stand-in in host code).
+// device (in host code the array's name is only a host-side stand-in, never a
+// device address).  The cached address stays valid for the life of the CUDA
+// context; a cudaDeviceReset after the first call invalidates it (see the
+// header).
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LA_ERR_CUDA;
@@ -47,14 +51,19 @@ int scratch_address(void** out) {
 extern "C" int la_causal_fwd_noalloc(const void* q, const void* k, const void* v, void* out,
                                      float* den, int B, int H, int N, int D, int M, int dtype,
                                      void* stream) {
+  // the same argument checks as la_causal_fwd, first, so that a bad call gets
+  // the same error code whether or not a device is usable
+  const int chk = la::causal_fwd_check(q, k, v, out, den, B, H, N, D, M, dtype);
+  if (chk != LA_OK) return chk;
   const size_t need = la_workspace_bytes(LA_OP_CAUSAL_FWD, B, H, N, D, M, dtype);
   if (need > LA_NOALLOC_SCRATCH_BYTES) return LA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != LA_OK) return rc;
-  // The forward needs nothing in its workspace to start at zero: every entry
-  // it reads is written earlier in the same call, and the one status word it
-  // keeps there is cleared by the call itself.
+  // Nothing in the scratch array needs to start at zero: every entry the
+  // forward reads there was written earlier in the same call.  Timeouts of
+  // bounded waits are not kept here; they go to the library's status word,
+  // which stays set until the caller clears it with la_device_status.
   return la_causal_fwd(q, k, v, out, den, scratch, LA_NOALLOC_SCRATCH_BYTES, B, H, N, D, M, dtype,
                        stream);
 }

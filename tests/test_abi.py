@@ -32,8 +32,34 @@ def test_library_exports_every_declared_symbol(linattn):
     assert set(declared_symbols()) <= set(linattn.EXPORTED) | {"la_workspace_bytes"}
 
 
+def header_constants():
+    """name -> value of every LA_* constant the header's enums define."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for body in re.findall(r"enum\s*\{(.*?)\}", text, flags=re.S):
+        for name, val in re.findall(r"(LA_\w+)\s*=\s*(\d+)", body):
+            out[name] = int(val)
+    return out
+
+
+def test_status_and_dtype_values_match_the_header(linattn):
+    """The fixed numbering (LA_ERR_TIMEOUT = 4, LA_ERR_WORKSPACE = 5; LA_F32 = 0,
+    LA_BF16 = 1) is what the header states and what the binding uses."""
+    h = header_constants()
+    want = {"LA_OK": 0, "LA_ERR_INVALID_ARG": 1, "LA_ERR_UNSUPPORTED": 2, "LA_ERR_CUDA": 3,
+            "LA_ERR_TIMEOUT": 4, "LA_ERR_WORKSPACE": 5, "LA_F32": 0, "LA_BF16": 1}
+    for name, val in want.items():
+        assert h[name] == val, name
+        assert getattr(linattn, name) == val, name
+    text = open(HEADER).read()
+    assert re.search(r"typedef\s+int\s+la_status\s*;", text)
+    assert re.search(r"typedef\s+int\s+la_dtype\s*;", text)
+    assert linattn.status_string(4) == "a bounded wait inside a kernel ran out"
+    assert linattn.status_string(5) == "workspace missing or too small"
+
+
 def test_version_and_status_strings(linattn):
-    assert linattn.lib().la_version() == 100
+    assert linattn.lib().la_version() == 200
     for code in range(6):
         assert linattn.status_string(code) != "unknown status"
     assert linattn.status_string(99) == "unknown status"
@@ -88,8 +114,8 @@ def _fwd(la, **kw):
     (dict(N=0), 1), (dict(B=0), 1), (dict(H=-1), 1), (dict(N=(1 << 24) + 1), 1),
     (dict(dt=7), 1), (dict(D=48), 2), (dict(M=128), 2), (dict(D=0), 1),
     (dict(B=65536), 1), (dict(B=256, H=256), 1),     # B*H above the 65535 grid rows
-    (dict(B=4, H=8, N=3072, D=64, M=64), 4),          # needs workspace, none given
-    (dict(B=4, H=8, N=3072, D=64, M=64, ws=FAKE, wsb=16), 4),
+    (dict(B=4, H=8, N=3072, D=64, M=64), 5),          # needs workspace, none given
+    (dict(B=4, H=8, N=3072, D=64, M=64, ws=FAKE, wsb=16), 5),
     (dict(B=4, H=8, N=3072, D=64, M=64, ws=FAKE + 4, wsb=1 << 30), 1),
 ])
 def test_causal_fwd_rejects(linattn, kw, code):
@@ -104,7 +130,7 @@ def test_other_calls_reject(linattn):
     # non-causal: S and Z required, lengths optional but aligned
     assert L.la_noncausal_fwd(F, F, F, None, F, F, None, F, F, 1 << 30, 1, 1, 64, 16, 16, 0, None) == 1
     assert L.la_noncausal_fwd(F, F, F, F + 4, F, F, F, F, F, 1 << 30, 1, 1, 64, 16, 16, 0, None) == 1
-    assert L.la_noncausal_fwd(F, F, F, None, F, F, F, F, None, 0, 1, 1, 64, 16, 16, 0, None) == 4
+    assert L.la_noncausal_fwd(F, F, F, None, F, F, F, F, None, 0, 1, 1, 64, 16, 16, 0, None) == 5
     assert L.la_noncausal_bwd(F, F, F, None, F, F, F, F, F, F, F, None, F, 1 << 30, 1, 1, 64, 16,
                               16, 0, None) == 1
     # decode
