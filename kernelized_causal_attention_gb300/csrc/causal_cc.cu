@@ -6,7 +6,7 @@
 //
 // Work decomposition (the GB300 design, not the pages'): every (b, h)
 // sequence is cut into segments of whole 64-token chunks so that the grid
-// fills the 152 SMs.  A first kernel writes each segment's partial sums
+// fills the SMs.  A first kernel writes each segment's partial sums
 // (dS = sum phi(K) V^T, dz = sum phi(K); for the backward also
 // dR = sum phi(Q) gt^T, dr = sum gam phi(Q)) to the workspace, a scan kernel
 // turns them into exclusive prefix (S, z) and suffix (R, r) sums, and the

@@ -647,7 +647,7 @@ bool make_bf16_map(CUtensorMap* m, const void* base, int BH, int N) {
 
 SegPlan tc_plan(int BH, int N) {
   const int nch = (N + TC_C - 1) / TC_C;
-  int want = 152 / BH;  // whole segments per head so that all CTAs fit one wave
+  int want = sm_count() / BH;  // whole segments per head so that all CTAs fit one wave
   if (want < 1) want = 1;
   if (want > nch) want = nch;
   const int per = (nch + want - 1) / want;

@@ -656,12 +656,13 @@ struct BwdPlan {
 };
 
 BwdPlan bwd_plan(int BH, int N) {
+  const int nsm = sm_count();
   BwdPlan b;
   b.main = tc_plan(2 * BH, N);
   const int per = b.main.seg_len / TC_C;
   b.subs = 1;
   for (int f = per; f >= 1; --f)
-    if (per % f == 0 && static_cast<long>(b.main.nseg) * f * BH <= 152) {
+    if (per % f == 0 && static_cast<long>(b.main.nseg) * f * BH <= nsm) {
       b.subs = f;
       break;
     }

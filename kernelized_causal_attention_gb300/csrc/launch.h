@@ -12,8 +12,12 @@ namespace la {
 // a nonzero code there; la_device_status reads it.
 int* status_word();
 
-constexpr int kChunk = 64;            // tokens per chunk in the CUDA-core kernels
-constexpr int kTargetCtas = 2 * 152;  // segments are sized to fill GB300's 152 SMs twice
+// Streaming multiprocessors of the current device (cudaDevAttrMultiProcessorCount,
+// cached per device); 152, GB300's count, when no device can be queried (so
+// workspace sizes can be computed on a machine without one).
+int sm_count();
+
+constexpr int kChunk = 64;  // tokens per chunk in the CUDA-core kernels
 
 // Split of each (b, h) sequence into segments of whole chunks.
 struct SegPlan {
@@ -21,7 +25,9 @@ struct SegPlan {
   int seg_len;  // tokens per segment (a multiple of the chunk length)
 };
 
-inline SegPlan plan_segments(int BH, int N, int chunk = kChunk, int target = kTargetCtas) {
+// Segments are sized to fill the SMs twice unless `target` says otherwise.
+inline SegPlan plan_segments(int BH, int N, int chunk = kChunk, int target = 0) {
+  if (target <= 0) target = 2 * sm_count();
   const int nch = (N + chunk - 1) / chunk;
   int want = (target + BH - 1) / BH;
   if (want < 1) want = 1;

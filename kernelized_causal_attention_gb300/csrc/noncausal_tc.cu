@@ -1072,7 +1072,7 @@ cudaError_t run_bwd(const T* q, const T* k, const T* v, const int* lengths, cons
 // head beat 4 by 4-12 us per call, 1 per head leaves SMs idle).
 int noncausal_tc_nseg(int BH, int N) {
   const int nch = (N + CH - 1) / CH;
-  const int fill = (3 * 152 / 2 + BH - 1) / BH;
+  const int fill = (3 * sm_count() / 2 + BH - 1) / BH;
   int n = kMaxSeg;
   while (n > 1 && (n > nch || n > fill)) n >>= 1;
   return n;

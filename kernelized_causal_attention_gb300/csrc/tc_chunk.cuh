@@ -30,6 +30,41 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// 16-byte shared-memory store / load through an explicit shared-window
+// address.  The tiles are addressed through pointers aligned at run time, from
+// which the compiler cannot always tell that they point into shared memory;
+// these keep such accesses on the shared-memory path.
+__device__ __forceinline__ void sts128(const void* p, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p))
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float lds32f(const void* p) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 lds128f(const void* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_u32(p))
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts16(const void* p, uint16_t v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(smem_u32(p)), "h"(v) : "memory");
+}
+
 __device__ __forceinline__ void fail(int* err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
 }
@@ -72,14 +107,14 @@ __device__ __forceinline__ void phi_tiles(uint8_t* tile, int stride, int valid, 
   for (int k = 0; k < NTL; ++k)
 #pragma unroll
     for (int i = 0; i < PER; ++i)
-      u[k][i] = *reinterpret_cast<const uint4*>(tile + k * stride + (t + i * NT) * 16);
+      u[k][i] = lds128(tile + k * stride + (t + i * NT) * 16);
 #pragma unroll
   for (int k = 0; k < NTL; ++k)
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int v = t + i * NT;
       const uint4 r = (v >> 3) >= valid ? make_uint4(0u, 0u, 0u, 0u) : phi_vec(u[k][i]);
-      *reinterpret_cast<uint4*>(tile + k * stride + v * 16) = r;
+      sts128(tile + k * stride + v * 16, r);
     }
 }
 
@@ -129,9 +164,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // [rows][64] bf16 tile.
 __device__ __forceinline__ void st_row_chunk(uint8_t* tile, int r, int c, const float* x) {
   const uint32_t off = static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(c) ^ (r & 7u)) << 4);
-  *reinterpret_cast<uint4*>(tile + off) =
-      make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                 pack_bf16(x[6], x[7]));
+  sts128(tile + off, make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                                pack_bf16(x[6], x[7])));
 }
 
 // Loads the 80 fp32 columns of this thread's TMEM lane starting at `taddr`.
@@ -159,7 +193,7 @@ __device__ __forceinline__ void tile_row_cols(const uint8_t* tile, int r, int co
 #pragma unroll
   for (int c = 0; c < NC / 8; ++c) {
     const int c8 = (col0 >> 3) + c;
-    const uint4 u = *reinterpret_cast<const uint4*>(tile + r * 128 + ((c8 ^ (r & 7)) << 4));
+    const uint4 u = lds128(tile + r * 128 + ((c8 ^ (r & 7)) << 4));
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
