@@ -8,7 +8,8 @@ CUDA library.
 
 Sources: "Transformers are RNNs: Fast Autoregressive Transformers with Linear
 Attention -- part 2/3" (eq. 7, §3.3 eq. 8-12, §3.3.1 eq. 13-15, §3.4 eq. 16-19)
-and "Linear Attention/zh" (kernel reformulation; recurrent form).  Each C
+and "Linear Attention/zh" (kernel reformulation; recurrent form; the RetNet
+decay of "variants and extensions", taken with gamma in [0, 1]).  Each C
 function cites the passage it follows.
 
 Every function takes arrays of any float dtype (a bf16 input is passed already
@@ -43,6 +44,11 @@ _SIGS = {
     "orc_noncausal_bwd": "i i i i i p p p p p p p p i",
     "orc_noncausal_bwd_quadratic": "i i i i i p p p p p p p p i",
     "orc_decode": "i i i i p p p p p p i",
+    "orc_causal_fwd_quadratic_decay": "i i i i p p p d p p i",
+    "orc_causal_fwd_recurrent_decay": "i i i i p p p d p p i",
+    "orc_causal_bwd_recurrent_decay": "i i i i p p p p d p p p i",
+    "orc_causal_bwd_quadratic_decay": "i i i i p p p p d p p p i",
+    "orc_decode_decay": "i i i i p p p d p p p i",
     "orc_causal_prefill": "i i i i p p p p p p p i",
 }
 
@@ -100,7 +106,7 @@ class Oracle:
 
     def __init__(self, path: str):
         lib = ctypes.CDLL(path)
-        kinds = {"i": ctypes.c_int, "l": ctypes.c_long, "p": ctypes.c_void_p}
+        kinds = {"i": ctypes.c_int, "l": ctypes.c_long, "p": ctypes.c_void_p, "d": ctypes.c_double}
         for name, sig in _SIGS.items():
             fn = getattr(lib, name)
             fn.argtypes = [kinds[c] for c in sig.split()]
@@ -120,28 +126,42 @@ class Oracle:
         self.lib.orc_phi(x.size, _ptr(x), _ptr(y), _ptr(dy))
         return y, dy
 
-    def causal_fwd(self, q, k, v, form="recurrent", nthreads=0):
+    def causal_fwd(self, q, k, v, form="recurrent", nthreads=0, gamma=None):
         """Causal forward: (out [B,H,N,M], den [B,H,N]).  form = 'recurrent'
-        (eq. 10-12) or 'quadratic' (eq. 8 with sim = phi(q)^T phi(k))."""
+        (eq. 10-12) or 'quadratic' (eq. 8 with sim = phi(q)^T phi(k)).  gamma:
+        the RetNet decay in [0, 1] (None: the undecayed entry points)."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         B, H, N, D = q.shape
         M = v.shape[-1]
         out, den = np.empty((B, H, N, M)), np.empty((B, H, N))
-        fn = {"recurrent": self.lib.orc_causal_fwd_recurrent,
-              "quadratic": self.lib.orc_causal_fwd_quadratic}[form]
-        fn(B * H, N, D, M, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(den), nthreads)
+        if gamma is None:
+            fn = {"recurrent": self.lib.orc_causal_fwd_recurrent,
+                  "quadratic": self.lib.orc_causal_fwd_quadratic}[form]
+            fn(B * H, N, D, M, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(den), nthreads)
+        else:
+            fn = {"recurrent": self.lib.orc_causal_fwd_recurrent_decay,
+                  "quadratic": self.lib.orc_causal_fwd_quadratic_decay}[form]
+            fn(B * H, N, D, M, _ptr(q), _ptr(k), _ptr(v), float(gamma), _ptr(out), _ptr(den),
+               nthreads)
         return out, den
 
-    def causal_bwd(self, q, k, v, g, form="recurrent", nthreads=0):
-        """Gradients (dq, dk, dv) of sum(g * V') for the causal form."""
+    def causal_bwd(self, q, k, v, g, form="recurrent", nthreads=0, gamma=None):
+        """Gradients (dq, dk, dv) of sum(g * V') for the causal form (gamma:
+        the RetNet decay, None for the undecayed entry points)."""
         q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(g)
         B, H, N, D = q.shape
         M = v.shape[-1]
         dq, dk, dv = np.empty((B, H, N, D)), np.empty((B, H, N, D)), np.empty((B, H, N, M))
-        fn = {"recurrent": self.lib.orc_causal_bwd_recurrent,
-              "quadratic": self.lib.orc_causal_bwd_quadratic}[form]
-        fn(B * H, N, D, M, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-           _ptr(dq), _ptr(dk), _ptr(dv), nthreads)
+        if gamma is None:
+            fn = {"recurrent": self.lib.orc_causal_bwd_recurrent,
+                  "quadratic": self.lib.orc_causal_bwd_quadratic}[form]
+            fn(B * H, N, D, M, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+               _ptr(dq), _ptr(dk), _ptr(dv), nthreads)
+        else:
+            fn = {"recurrent": self.lib.orc_causal_bwd_recurrent_decay,
+                  "quadratic": self.lib.orc_causal_bwd_quadratic_decay}[form]
+            fn(B * H, N, D, M, _ptr(q), _ptr(k), _ptr(v), _ptr(g), float(gamma),
+               _ptr(dq), _ptr(dk), _ptr(dv), nthreads)
         return dq, dk, dv
 
     def noncausal_fwd(self, q, k, v, lengths=None, form="recurrent", nthreads=0):
@@ -174,18 +194,22 @@ class Oracle:
            _ptr(dq), _ptr(dk), _ptr(dv), nthreads)
         return dq, dk, dv
 
-    def decode(self, q, k, v, S=None, Z=None, nthreads=0):
+    def decode(self, q, k, v, S=None, Z=None, nthreads=0, gamma=None):
         """T RNN steps (eq. 16-19) over independent streams.  q, k: [T,B,H,D];
-        v: [T,B,H,M]; S, Z: initial state (zeros if None).
-        Returns (y [T,B,H,M], S_T [B,H,D,M], Z_T [B,H,D])."""
+        v: [T,B,H,M]; S, Z: initial state (zeros if None); gamma: the RetNet
+        decay (None: undecayed).  Returns (y [T,B,H,M], S_T [B,H,D,M], Z_T [B,H,D])."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         T, B, H, D = q.shape
         M = v.shape[-1]
         S = np.zeros((B, H, D, M)) if S is None else _f64(S).copy()
         Z = np.zeros((B, H, D)) if Z is None else _f64(Z).copy()
         y = np.empty((T, B, H, M))
-        self.lib.orc_decode(T, B * H, D, M, _ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(Z),
-                            _ptr(y), nthreads)
+        if gamma is None:
+            self.lib.orc_decode(T, B * H, D, M, _ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(Z),
+                                _ptr(y), nthreads)
+        else:
+            self.lib.orc_decode_decay(T, B * H, D, M, _ptr(q), _ptr(k), _ptr(v), float(gamma),
+                                      _ptr(S), _ptr(Z), _ptr(y), nthreads)
         return y, S, Z
 
     def causal_prefill(self, q, k, v, S=None, Z=None, nthreads=0):
@@ -220,12 +244,12 @@ def phi(x):
     return default().phi(x)
 
 
-def causal_fwd(q, k, v, form="recurrent", nthreads=0):
-    return default().causal_fwd(q, k, v, form, nthreads)
+def causal_fwd(q, k, v, form="recurrent", nthreads=0, gamma=None):
+    return default().causal_fwd(q, k, v, form, nthreads, gamma)
 
 
-def causal_bwd(q, k, v, g, form="recurrent", nthreads=0):
-    return default().causal_bwd(q, k, v, g, form, nthreads)
+def causal_bwd(q, k, v, g, form="recurrent", nthreads=0, gamma=None):
+    return default().causal_bwd(q, k, v, g, form, nthreads, gamma)
 
 
 def noncausal_fwd(q, k, v, lengths=None, form="recurrent", nthreads=0):
@@ -236,8 +260,8 @@ def noncausal_bwd(q, k, v, g, lengths=None, form="recurrent", nthreads=0):
     return default().noncausal_bwd(q, k, v, g, lengths, form, nthreads)
 
 
-def decode(q, k, v, S=None, Z=None, nthreads=0):
-    return default().decode(q, k, v, S, Z, nthreads)
+def decode(q, k, v, S=None, Z=None, nthreads=0, gamma=None):
+    return default().decode(q, k, v, S, Z, nthreads, gamma)
 
 
 def causal_prefill(q, k, v, S=None, Z=None, nthreads=0):

@@ -16,8 +16,10 @@
  *          "gradient derivation" (numerator gradients; the denominator is left
  *          to automatic differentiation there).
  *   [LA]   "Linear Attention/zh": "kernel reformulation" section (non-causal form
- *          with a shared S and z) and "recurrent form and autoregressive
- *          inference" section.
+ *          with a shared S and z), "recurrent form and autoregressive
+ *          inference" section, and the RetNet item of "variants and
+ *          extensions" (a decay factor gamma in (0, 1): S_t = gamma S_{t-1} +
+ *          phi(k_t) v_t^T).
  *
  * Layout: every array is a dense row-major double array.  Heads are flattened:
  * head index hh in [0, B*H) addresses q[hh][n][d], v[hh][n][m] and so on.
@@ -28,7 +30,10 @@
  * denominator; the denominator gradient follows the same cumulative-sum
  * structure as eq. 13-15 with V_j replaced by the constant 1; decode updates the
  * state before reading it (eq. 18-20 use s_i, not s_{i-1}); padded positions of
- * the non-causal form contribute nothing and receive zero output and gradient.
+ * the non-causal form contribute nothing and receive zero output and gradient;
+ * with the RetNet decay the normaliser z decays with S (z_t = gamma z_{t-1} +
+ * phi(k_t)), so that V'_i stays a convex combination of the values, and
+ * gamma = 1 is the undecayed method.
  *
  * Parity status: every function here is pinned by tests that do not retype its
  * formulas (two independent forms, closed forms, invariants, central finite
@@ -80,10 +85,12 @@ int orc_openmp_enabled(void) {
  *   A_ij  = phi(Q_i) . phi(K_j)                 for j <= i
  *   den_i = sum_{j<=i} A_ij
  *   V'_i  = sum_{j<=i} A_ij V_j / den_i
- * The N x N matrix is built explicitly, one row at a time. */
-void orc_causal_fwd_quadratic(int BH, int N, int D, int M, const double* q,
-                              const double* k, const double* v, double* out,
-                              double* den, int nthreads) {
+ * The N x N matrix is built explicitly, one row at a time.  With the RetNet
+ * decay of [LA] every pair is weighted by gamma^(i-j) in both sums (A_ij ->
+ * gamma^(i-j) A_ij); gamma = 1 is eq. 8 itself. */
+void orc_causal_fwd_quadratic_decay(int BH, int N, int D, int M, const double* q,
+                                    const double* k, const double* v, double gamma,
+                                    double* out, double* den, int nthreads) {
   set_threads(nthreads);
 #pragma omp parallel for schedule(dynamic)
   for (int hh = 0; hh < BH; ++hh) {
@@ -97,6 +104,7 @@ void orc_causal_fwd_quadratic(int BH, int N, int D, int M, const double* q,
       for (int j = 0; j <= i; ++j) {
         double a = 0.0;
         for (int d = 0; d < D; ++d) a += phi(Q[(size_t)i * D + d]) * phi(K[(size_t)j * D + d]);
+        a *= pow(gamma, (double)(i - j)); /* the decay of the pair: gamma^(i-j), 1 when gamma = 1 */
         row[j] = a;
         s += a;
       }
@@ -111,16 +119,24 @@ void orc_causal_fwd_quadratic(int BH, int N, int D, int M, const double* q,
   }
 }
 
+void orc_causal_fwd_quadratic(int BH, int N, int D, int M, const double* q,
+                              const double* k, const double* v, double* out,
+                              double* den, int nthreads) {
+  orc_causal_fwd_quadratic_decay(BH, N, D, M, q, k, v, 1.0, out, den, nthreads);
+}
+
 /* --------------------------------------------- causal, recurrent form (R) */
 
 /* [TR2] §3.3 eq. 10-12: walk i = 1..N,
  *   S_i = S_{i-1} + phi(K_i) V_i^T      (D x M)
  *   Z_i = Z_{i-1} + phi(K_i)            (D)
  *   V'_i = phi(Q_i)^T S_i / phi(Q_i)^T Z_i
- * Only the running S, Z are kept: linear time, constant state. */
-void orc_causal_fwd_recurrent(int BH, int N, int D, int M, const double* q,
-                              const double* k, const double* v, double* out,
-                              double* den, int nthreads) {
+ * Only the running S, Z are kept: linear time, constant state.  With the
+ * RetNet decay of [LA] the update is S_i = gamma S_{i-1} + phi(K_i) V_i^T and
+ * Z_i = gamma Z_{i-1} + phi(K_i) (multiplying by gamma = 1 changes nothing). */
+void orc_causal_fwd_recurrent_decay(int BH, int N, int D, int M, const double* q,
+                                    const double* k, const double* v, double gamma,
+                                    double* out, double* den, int nthreads) {
   set_threads(nthreads);
 #pragma omp parallel for schedule(dynamic)
   for (int hh = 0; hh < BH; ++hh) {
@@ -134,8 +150,9 @@ void orc_causal_fwd_recurrent(int BH, int N, int D, int M, const double* q,
     for (int i = 0; i < N; ++i) {
       for (int d = 0; d < D; ++d) {
         double fk = phi(K[(size_t)i * D + d]);
-        for (int m = 0; m < M; ++m) S[(size_t)d * M + m] += fk * V[(size_t)i * M + m];
-        Z[d] += fk;
+        for (int m = 0; m < M; ++m)
+          S[(size_t)d * M + m] = gamma * S[(size_t)d * M + m] + fk * V[(size_t)i * M + m];
+        Z[d] = gamma * Z[d] + fk;
       }
       double s = 0.0;
       for (int d = 0; d < D; ++d) {
@@ -155,6 +172,12 @@ void orc_causal_fwd_recurrent(int BH, int N, int D, int M, const double* q,
   }
 }
 
+void orc_causal_fwd_recurrent(int BH, int N, int D, int M, const double* q,
+                              const double* k, const double* v, double* out,
+                              double* den, int nthreads) {
+  orc_causal_fwd_recurrent_decay(BH, N, D, M, q, k, v, 1.0, out, den, nthreads);
+}
+
 /* ----------------------------------------- causal gradients, recurrent form */
 
 /* Gradients of L = sum_i G_i . V'_i with respect to Q, K, V.
@@ -171,10 +194,15 @@ void orc_causal_fwd_recurrent(int BH, int N, int D, int M, const double* q,
  * [TR2] §3.3.1 eq. 15:  grad V_i      = R_i^T phi(K_i)
  *   with R_i = sum_{j>=i} phi(Q_j) gt_j^T and r_i = sum_{j>=i} gam_j phi(Q_j),
  *   the reverse cumulative sums ([TRN] appendix A compares them to BPTT).
- * Finally dQ = grad phi(Q) * phi'(Q) and dK = grad phi(K) * phi'(K) (eq. 7). */
-void orc_causal_bwd_recurrent(int BH, int N, int D, int M, const double* q,
-                              const double* k, const double* v, const double* g,
-                              double* dq, double* dk, double* dv, int nthreads) {
+ * Finally dQ = grad phi(Q) * phi'(Q) and dK = grad phi(K) * phi'(K) (eq. 7).
+ * With the RetNet decay of [LA] the sums carry the same factor both ways:
+ * S_i, Z_i as in the decayed forward, and R_i = gamma R_{i+1} + phi(Q_i) gt_i^T,
+ * r_i = gamma r_{i+1} + gam_i phi(Q_i) (token j reaches query i >= j through
+ * gamma^(i-j) in either direction). */
+void orc_causal_bwd_recurrent_decay(int BH, int N, int D, int M, const double* q,
+                                    const double* k, const double* v, const double* g,
+                                    double gamma, double* dq, double* dk, double* dv,
+                                    int nthreads) {
   set_threads(nthreads);
 #pragma omp parallel for schedule(dynamic)
   for (int hh = 0; hh < BH; ++hh) {
@@ -198,8 +226,9 @@ void orc_causal_bwd_recurrent(int BH, int N, int D, int M, const double* q,
     for (int i = 0; i < N; ++i) {
       for (int d = 0; d < D; ++d) {
         double fk = phi(K[(size_t)i * D + d]);
-        for (int m = 0; m < M; ++m) S[(size_t)d * M + m] += fk * V[(size_t)i * M + m];
-        Z[d] += fk;
+        for (int m = 0; m < M; ++m)
+          S[(size_t)d * M + m] = gamma * S[(size_t)d * M + m] + fk * V[(size_t)i * M + m];
+        Z[d] = gamma * Z[d] + fk;
       }
       double s = 0.0;
       for (int d = 0; d < D; ++d) {
@@ -225,8 +254,9 @@ void orc_causal_bwd_recurrent(int BH, int N, int D, int M, const double* q,
     for (int i = N - 1; i >= 0; --i) {
       for (int d = 0; d < D; ++d) {
         double fqd = phi(Q[(size_t)i * D + d]);
-        for (int m = 0; m < M; ++m) R[(size_t)d * M + m] += fqd * gt[(size_t)i * M + m];
-        r[d] += gam[i] * fqd;
+        for (int m = 0; m < M; ++m)
+          R[(size_t)d * M + m] = gamma * R[(size_t)d * M + m] + fqd * gt[(size_t)i * M + m];
+        r[d] = gamma * r[d] + gam[i] * fqd;
       }
       for (int d = 0; d < D; ++d) {
         double acc = r[d];
@@ -243,6 +273,12 @@ void orc_causal_bwd_recurrent(int BH, int N, int D, int M, const double* q,
   }
 }
 
+void orc_causal_bwd_recurrent(int BH, int N, int D, int M, const double* q,
+                              const double* k, const double* v, const double* g,
+                              double* dq, double* dk, double* dv, int nthreads) {
+  orc_causal_bwd_recurrent_decay(BH, N, D, M, q, k, v, g, 1.0, dq, dk, dv, nthreads);
+}
+
 /* ----------------------------------------- causal gradients, quadratic form */
 
 /* Differentiates eq. 8 directly through the explicit masked matrix:
@@ -251,10 +287,12 @@ void orc_causal_bwd_recurrent(int BH, int N, int D, int M, const double* q,
  *   grad phi(K_j) = sum_{i>=j} dA_ij phi(Q_i)
  *   grad V_j      = sum_{i>=j} A_ij gt_i
  * with gt_i, gam_i as in the recurrent form.  Independent of the cumulative
- * sums: it touches every (i, j) pair. */
-void orc_causal_bwd_quadratic(int BH, int N, int D, int M, const double* q,
-                              const double* k, const double* v, const double* g,
-                              double* dq, double* dk, double* dv, int nthreads) {
+ * sums: it touches every (i, j) pair.  With the RetNet decay the pair's
+ * weight A_ij and its gradient dA_ij both carry gamma^(i-j). */
+void orc_causal_bwd_quadratic_decay(int BH, int N, int D, int M, const double* q,
+                                    const double* k, const double* v, const double* g,
+                                    double gamma, double* dq, double* dk, double* dv,
+                                    int nthreads) {
   set_threads(nthreads);
 #pragma omp parallel for schedule(dynamic)
   for (int hh = 0; hh < BH; ++hh) {
@@ -275,8 +313,10 @@ void orc_causal_bwd_quadratic(int BH, int N, int D, int M, const double* q,
       double s = 0.0;
       for (int j = 0; j < N; ++j) {
         double a = 0.0;
-        if (j <= i)
+        if (j <= i) {
           for (int d = 0; d < D; ++d) a += phi(Q[(size_t)i * D + d]) * phi(K[(size_t)j * D + d]);
+          a *= pow(gamma, (double)(i - j));
+        }
         A[(size_t)i * N + j] = a;
         s += a;
       }
@@ -293,6 +333,7 @@ void orc_causal_bwd_quadratic(int BH, int N, int D, int M, const double* q,
       for (int j = 0; j <= i; ++j) {
         double da = gam[i];
         for (int m = 0; m < M; ++m) da += gt[(size_t)i * M + m] * V[(size_t)j * M + m];
+        da *= pow(gamma, (double)(i - j)); /* d(loss)/d(phi(Q_i) . phi(K_j)) */
         for (int d = 0; d < D; ++d) {
           gfq[(size_t)i * D + d] += da * phi(K[(size_t)j * D + d]);
           gfk[(size_t)j * D + d] += da * phi(Q[(size_t)i * D + d]);
@@ -307,6 +348,12 @@ void orc_causal_bwd_quadratic(int BH, int N, int D, int M, const double* q,
       }
     free(A); free(gt); free(gam); free(gfq); free(gfk);
   }
+}
+
+void orc_causal_bwd_quadratic(int BH, int N, int D, int M, const double* q,
+                              const double* k, const double* v, const double* g,
+                              double* dq, double* dk, double* dv, int nthreads) {
+  orc_causal_bwd_quadratic_decay(BH, N, D, M, q, k, v, g, 1.0, dq, dk, dv, nthreads);
 }
 
 /* ---------------------------------------------------------- non-causal form */
@@ -604,9 +651,11 @@ void orc_causal_prefill(int BH, int N, int D, int M, const double* q, const doub
  * The state is updated before it is read, as in eq. 18-20.  The layer's f_l and
  * residual of eq. 20 are outside the attention and are not applied.  S [BH][D][M]
  * and Z [BH][D] hold the state on entry (zero for eq. 16-17) and on exit.
- * q, k: [T][BH][D]; v, y: [T][BH][M]. */
-void orc_decode(int T, int BH, int D, int M, const double* q, const double* k,
-                const double* v, double* S, double* Z, double* y, int nthreads) {
+ * q, k: [T][BH][D]; v, y: [T][BH][M].  With the RetNet decay of [LA]:
+ * s <- gamma s + phi(k_t) v_t^T and z <- gamma z + phi(k_t). */
+void orc_decode_decay(int T, int BH, int D, int M, const double* q, const double* k,
+                      const double* v, double gamma, double* S, double* Z, double* y,
+                      int nthreads) {
   set_threads(nthreads);
 #pragma omp parallel for schedule(dynamic)
   for (int hh = 0; hh < BH; ++hh) {
@@ -620,8 +669,8 @@ void orc_decode(int T, int BH, int D, int M, const double* q, const double* k,
       double* yt = y + ((size_t)t * BH + hh) * M;
       for (int d = 0; d < D; ++d) {
         double fk = phi(kt[d]);
-        for (int m = 0; m < M; ++m) s[(size_t)d * M + m] += fk * vt[m];
-        z[d] += fk;
+        for (int m = 0; m < M; ++m) s[(size_t)d * M + m] = gamma * s[(size_t)d * M + m] + fk * vt[m];
+        z[d] = gamma * z[d] + fk;
       }
       double den = 0.0;
       for (int d = 0; d < D; ++d) {
@@ -636,4 +685,9 @@ void orc_decode(int T, int BH, int D, int M, const double* q, const double* k,
     }
     free(fq);
   }
+}
+
+void orc_decode(int T, int BH, int D, int M, const double* q, const double* k,
+                const double* v, double* S, double* Z, double* y, int nthreads) {
+  orc_decode_decay(T, BH, D, M, q, k, v, 1.0, S, Z, y, nthreads);
 }

@@ -11,11 +11,14 @@ Sources: "Transformers are RNNs -- part 2/3": eq. 7 (phi = elu + 1), §3.3
 eq. 8 (masked quadratic form) and eq. 10-12 (recurrence), §3.3.1 eq. 13-15
 (gradients), §3.4 eq. 16-19 (RNN form, also run over a prompt from a given
 state); "Linear Attention/zh": kernel
-reformulation (shared S, z for the non-causal form).
+reformulation (shared S, z for the non-causal form) and the RetNet decay of
+"variants and extensions" (S_t = gamma S_{t-1} + phi(k_t) v_t^T, read with z
+decaying alongside S).
 """
 from __future__ import annotations
 
 import numpy as np
+import scipy.signal
 import torch
 
 RNG_SHAPES = [  # (B, H, N, D, M): D != M catches transposed operands
@@ -317,6 +320,145 @@ def pin_prefill(orc):
     assert rel(Sd, S_N) < 1e-13 and rel(Zd, Z_N) < 1e-13
 
 
+# ------------------------------------------------------------- RetNet decay
+
+DECAYS = (0.0, 0.5, 0.9, 0.99)
+
+
+def pin_decay_gamma_one(orc):
+    """gamma = 1 is the undecayed method itself: the decayed entry points give
+    the same bits as the (separately pinned) undecayed ones."""
+    B, H, N, D, M = 2, 2, 9, 3, 5
+    q, k, v, g = rand((B, H, N, D), 201), rand((B, H, N, D), 202), rand((B, H, N, M), 203), rand((B, H, N, M), 204)
+    for form in ("recurrent", "quadratic"):
+        a = orc.causal_fwd(q, k, v, form)
+        b = orc.causal_fwd(q, k, v, form, gamma=1.0)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b)), f"{form} forward: gamma = 1 changed it"
+        a = orc.causal_bwd(q, k, v, g, form)
+        b = orc.causal_bwd(q, k, v, g, form, gamma=1.0)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b)), f"{form} gradients: gamma = 1 changed them"
+    st = lambda x: np.ascontiguousarray(np.transpose(x, (2, 0, 1, 3)))
+    a = orc.decode(st(q), st(k), st(v))
+    b = orc.decode(st(q), st(k), st(v), gamma=1.0)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b)), "decode: gamma = 1 changed it"
+
+
+def pin_decay_gamma_zero(orc):
+    """gamma = 0 keeps only the pair i = j (gamma^0 = 1): V'_i = V_i,
+    den_i = phi(Q_i) . phi(K_i) (numpy), dV = G and dQ = dK = 0; the decode
+    state is the last token's phi(k) v^T."""
+    B, H, N, D, M = 1, 2, 8, 3, 4
+    q, k, v, g = rand((B, H, N, D), 211), rand((B, H, N, D), 212), rand((B, H, N, M), 213), rand((B, H, N, M), 214)
+    for form in ("recurrent", "quadratic"):
+        out, den = orc.causal_fwd(q, k, v, form, gamma=0.0)
+        assert rel(out, v) < 1e-14, f"{form}: gamma = 0 must return V"
+        assert rel(den, np.einsum("bhnd,bhnd->bhn", phi_lib(q), phi_lib(k))) < 1e-14
+        dq, dk, dv = orc.causal_bwd(q, k, v, g, form, gamma=0.0)
+        assert rel(dv, g) < 1e-14 and np.max(np.abs(dq)) < 1e-13 and np.max(np.abs(dk)) < 1e-13
+    st = lambda x: np.ascontiguousarray(np.transpose(x, (2, 0, 1, 3)))
+    y, S, Z = orc.decode(st(q), st(k), st(v), gamma=0.0)
+    assert rel(y, st(v)) < 1e-14
+    assert rel(S, np.einsum("bhd,bhm->bhdm", phi_lib(k[:, :, -1]), v[:, :, -1])) < 1e-14
+    assert rel(Z, phi_lib(k[:, :, -1])) < 1e-14
+
+
+def pin_decay_closed_form(orc):
+    """Q = K = 0 makes phi = 1, so every pair weighs D gamma^(i-j): V'_i is
+    the exponentially weighted mean of V_1..V_i and den_i = D sum_j gamma^(i-j),
+    both by scipy's IIR filter y_i = x_i + gamma y_{i-1}; constant V rows are
+    reproduced for any gamma."""
+    B, H, N, D, M = 1, 2, 17, 3, 4
+    z = np.zeros((B, H, N, D))
+    v = rand((B, H, N, M), 221)
+    for gm in DECAYS[1:]:
+        num = scipy.signal.lfilter([1.0], [1.0, -gm], v, axis=2)
+        cnt = scipy.signal.lfilter([1.0], [1.0, -gm], np.ones((B, H, N)), axis=2)
+        for form in ("recurrent", "quadratic"):
+            out, den = orc.causal_fwd(z, z, v, form, gamma=gm)
+            assert rel(out, num / cnt[..., None]) < 1e-13, f"{form} gamma={gm}: not the weighted mean"
+            assert rel(den, D * cnt) < 1e-13
+            c = np.broadcast_to(rand((1, 1, 1, M), 222), v.shape).copy()
+            outc, _ = orc.causal_fwd(rand((B, H, N, D), 223), rand((B, H, N, D), 224), c, form, gamma=gm)
+            assert rel(outc, c) < 1e-13, "constant V not reproduced"
+
+
+def pin_decay_forms_agree(orc):
+    """The decayed quadratic form (every pair weighted gamma^(i-j)) and the
+    decayed recurrence agree, forward and gradients."""
+    for gm in DECAYS:
+        for shp in RNG_SHAPES:
+            B, H, N, D, M = shp
+            q, k, v, g = rand((B, H, N, D), 231), rand((B, H, N, D), 232), rand((B, H, N, M), 233), rand((B, H, N, M), 234)
+            o1, d1 = orc.causal_fwd(q, k, v, "recurrent", gamma=gm)
+            o2, d2 = orc.causal_fwd(q, k, v, "quadratic", gamma=gm)
+            assert rel(o1, o2) < 1e-12 and rel(d1, d2) < 1e-12, f"forward forms differ at gamma={gm}"
+            if gm == 0.0:
+                continue  # dq = dk = 0 exactly there (pin_decay_gamma_zero); only rounding is left
+            a = orc.causal_bwd(q, k, v, g, "recurrent", gamma=gm)
+            b = orc.causal_bwd(q, k, v, g, "quadratic", gamma=gm)
+            for x, y, nm in zip(a, b, ("dq", "dk", "dv")):
+                assert rel(x, y, 1e-3) < 1e-11, f"{nm} forms differ at gamma={gm}"  # N = 1: exact zeros
+
+
+def pin_decay_grad_fd(orc):
+    """Both decayed gradient forms against central finite differences of the
+    decayed loss sum(G * V')."""
+    B, H, N, D, M = 1, 1, 9, 3, 4
+    q, k, v, g = rand((B, H, N, D), 241), rand((B, H, N, D), 242), rand((B, H, N, M), 243), rand((B, H, N, M), 244)
+    for gm in (0.5, 0.9):
+        loss = lambda q_, k_, v_: float(np.sum(g * orc.causal_fwd(q_, k_, v_, "recurrent", gamma=gm)[0]))
+        h = 1e-6
+        num = []
+        for x, idx in ((q, 0), (k, 1), (v, 2)):
+            gr = np.zeros_like(x)
+            for e in np.ndindex(x.shape):
+                args = [q.copy(), k.copy(), v.copy()]
+                args[idx][e] += h
+                up = loss(*args)
+                args[idx][e] -= 2 * h
+                gr[e] = (up - loss(*args)) / (2 * h)
+            num.append(gr)
+        for form in ("recurrent", "quadratic"):
+            an = orc.causal_bwd(q, k, v, g, form, gamma=gm)
+            for a_, n_, nm in zip(an, num, ("dq", "dk", "dv")):
+                assert rel(a_, n_) < 1e-6, f"{form} {nm} != finite differences at gamma={gm}"
+
+
+def pin_decay_invariants(orc):
+    """The decayed output is still a normalised weighted mean per row, so
+    phi(Q_i) . grad phi(Q_i) = 0, sum_j phi(K_j) . grad phi(K_j) = 0 and
+    sum_j dV_j = sum_i G_i (checked through dq / phi' and dk / phi')."""
+    B, H, N, D, M = 2, 1, 11, 3, 5
+    q, k, v, g = rand((B, H, N, D), 251), rand((B, H, N, D), 252), rand((B, H, N, M), 253), rand((B, H, N, M), 254)
+    fq, fk = phi_lib(q), phi_lib(k)
+    dfq = np.where(q > 0, 1.0, np.exp(q))
+    dfk = np.where(k > 0, 1.0, np.exp(k))
+    for gm in (0.3, 0.9):
+        dq, dk, dv = orc.causal_bwd(q, k, v, g, "recurrent", gamma=gm)
+        gq, gk = dq / dfq, dk / dfk
+        assert np.max(np.abs(np.sum(fq * gq, axis=-1))) < 1e-12, "phi(Q_i) . grad phi(Q_i) != 0"
+        assert np.max(np.abs(np.sum(fk * gk, axis=(2, 3)))) < 1e-11, "sum phi(K) . grad phi(K) != 0"
+        assert rel(dv.sum(axis=2), g.sum(axis=2)) < 1e-12, "sum dV != sum G"
+
+
+def pin_decay_decode(orc):
+    """Decayed RNN steps = the decayed causal form on the stacked sequence;
+    the final state is sum_t gamma^(T-1-t) phi(k_t) v_t^T (numpy einsum)."""
+    T, B, H, D, M = 10, 2, 2, 3, 4
+    q, k, v = rand((T, B, H, D), 261), rand((T, B, H, D), 262), rand((T, B, H, M), 263)
+    seq = lambda x: np.ascontiguousarray(np.transpose(x, (1, 2, 0, 3)))
+    for gm in (0.4, 0.95):
+        y, S, Z = orc.decode(q, k, v, gamma=gm)
+        o, _ = orc.causal_fwd(seq(q), seq(k), seq(v), "quadratic", gamma=gm)
+        assert rel(np.transpose(y, (1, 2, 0, 3)), o) < 1e-13, f"decode != decayed causal form at gamma={gm}"
+        w = gm ** np.arange(T - 1, -1, -1.0)
+        fk = phi_lib(k)
+        assert rel(S, np.einsum("t,tbhd,tbhm->bhdm", w, fk, v)) < 1e-13
+        assert rel(Z, np.einsum("t,tbhd->bhd", w, fk)) < 1e-13
+
+
 ALL_PINS = [pin_phi, pin_causal_forms_agree, pin_causal_closed_forms, pin_grad_single_token, pin_noncausal_gemm,
             pin_noncausal_last_row, pin_noncausal_lengths, pin_grad_fd, pin_grad_forms_agree,
-            pin_grad_invariants, pin_decode, pin_prefill]
+            pin_grad_invariants, pin_decode, pin_prefill, pin_decay_gamma_one, pin_decay_gamma_zero,
+            pin_decay_closed_form, pin_decay_forms_agree, pin_decay_grad_fd, pin_decay_invariants,
+            pin_decay_decode]

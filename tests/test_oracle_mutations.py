@@ -15,8 +15,8 @@ MUTATIONS = [
     ("phi_dropped_plus_one", "return x > 0.0 ? x + 1.0 : exp(x);", "return x > 0.0 ? x : exp(x);", 0),
     ("dphi_zero_for_negative", "return x > 0.0 ? 1.0 : exp(x);", "return x > 0.0 ? 1.0 : 0.0;", 0),
     ("quadratic_mask_strict", "for (int j = 0; j <= i; ++j) {\n        double a", "for (int j = 0; j < i; ++j) {\n        double a", 0),
-    ("recurrent_off_by_one_key", "        double fk = phi(K[(size_t)i * D + d]);\n        for (int m = 0; m < M; ++m) S[(size_t)d * M + m] += fk * V[(size_t)i * M + m];",
-     "        double fk = phi(K[(size_t)(i > 0 ? i - 1 : 0) * D + d]);\n        for (int m = 0; m < M; ++m) S[(size_t)d * M + m] += fk * V[(size_t)(i > 0 ? i - 1 : 0) * M + m];", 0),
+    ("recurrent_off_by_one_key", "        double fk = phi(K[(size_t)i * D + d]);\n        for (int m = 0; m < M; ++m)\n          S[(size_t)d * M + m] = gamma * S[(size_t)d * M + m] + fk * V[(size_t)i * M + m];",
+     "        double fk = phi(K[(size_t)(i > 0 ? i - 1 : 0) * D + d]);\n        for (int m = 0; m < M; ++m)\n          S[(size_t)d * M + m] = gamma * S[(size_t)d * M + m] + fk * V[(size_t)(i > 0 ? i - 1 : 0) * M + m];", 0),
     ("bwd_dropped_denominator_term", "double acc = gam[i] * Z[d];", "double acc = 0.0;", 0),
     ("bwd_gamma_sign", "gam[i] = -gv / s;", "gam[i] = gv / s;", 0),
     ("bwd_dropped_r", "        double acc = r[d];\n        for (int m = 0; m < M; ++m) acc += R[(size_t)d * M + m] * V[(size_t)i * M + m];",
@@ -26,7 +26,18 @@ MUTATIONS = [
     ("noncausal_ignores_length", "    for (int j = 0; j < L; ++j)\n      for (int d = 0; d < D; ++d) {\n        double fk", "    for (int j = 0; j < N; ++j)\n      for (int d = 0; d < D; ++d) {\n        double fk", 0),
     ("noncausal_bwd_missing_gamma", "double gam = -gv / s;", "double gam = 0.0 * gv / s;", 0),
     ("decode_no_denominator", "yt[m] = acc / den;", "yt[m] = acc;", 0),
-    ("decode_transposed_update", "s[(size_t)d * M + m] += fk * vt[m];", "s[(size_t)d * M + m] += fk * vt[d % M];", 0),
+    ("decode_transposed_update", "s[(size_t)d * M + m] = gamma * s[(size_t)d * M + m] + fk * vt[m];",
+     "s[(size_t)d * M + m] = gamma * s[(size_t)d * M + m] + fk * vt[d % M];", 0),
+    # the RetNet decay
+    ("decay_z_not_decayed", "Z[d] = gamma * Z[d] + fk;", "Z[d] = Z[d] + fk;", 0),
+    ("decay_exponent_flipped", "a *= pow(gamma, (double)(i - j));", "a *= pow(gamma, (double)(j - i));", 0),
+    ("decay_reverse_sum_undecayed", "R[(size_t)d * M + m] = gamma * R[(size_t)d * M + m] + fqd * gt[(size_t)i * M + m];",
+     "R[(size_t)d * M + m] = R[(size_t)d * M + m] + fqd * gt[(size_t)i * M + m];", 0),
+    ("decay_r_undecayed", "r[d] = gamma * r[d] + gam[i] * fqd;", "r[d] = r[d] + gam[i] * fqd;", 0),
+    ("decay_quadratic_grad_undecayed", "da *= pow(gamma, (double)(i - j));", "da *= 1.0;", 0),
+    ("decay_decode_z_not_decayed", "z[d] = gamma * z[d] + fk;", "z[d] = z[d] + fk;", 0),
+    ("decay_squared", "S[(size_t)d * M + m] = gamma * S[(size_t)d * M + m] + fk * V[(size_t)i * M + m];",
+     "S[(size_t)d * M + m] = gamma * gamma * S[(size_t)d * M + m] + fk * V[(size_t)i * M + m];", 0),
     ("prefill_starts_from_zero", "memcpy(sl, st, sizeof(double) * (size_t)D * M);", "memset(sl, 0, sizeof(double) * (size_t)D * M);", 0),
     ("prefill_den_without_z0", "for (int d = 0; d < D; ++d) zl[d] = zt[d];", "for (int d = 0; d < D; ++d) zl[d] = 0.0 * zt[d];", 0),
     ("prefill_state_not_returned", "for (size_t e = 0; e < (size_t)D * M; ++e) st[e] = sl[e];", "for (size_t e = 0; e < (size_t)D * M; ++e) (void)sl[e];", 0),
