@@ -81,6 +81,8 @@ enum { LA_F32 = 0, LA_BF16 = 1 };
 #define LA_OP_NONCAUSAL_BWD 3
 #define LA_OP_DECODE 4
 #define LA_OP_CAUSAL_PREFILL 5
+#define LA_OP_CAUSAL_FWD_DECAY 6
+#define LA_OP_CAUSAL_BWD_DECAY 7
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* la_status_string(la_status status);
@@ -196,6 +198,37 @@ la_status la_noncausal_bwd(const void* q, const void* k, const void* v, const in
  */
 la_status la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z,
                    void* y, int B, int H, int D, int M, la_dtype dtype, void* stream);
+
+/*
+ * The RetNet decay ("Linear Attention/zh", variants and extensions): the
+ * causal sums become S_i = gamma S_{i-1} + phi(K_i) V_i^T and, so that the
+ * output stays a weighted mean of the values, Z_i = gamma Z_{i-1} + phi(K_i):
+ *   out_i = phi(Q_i)^T S_i / phi(Q_i)^T Z_i
+ *         = sum_{j<=i} gamma^(i-j) phi(Q_i).phi(K_j) V_j / sum_{j<=i} gamma^(i-j) phi(Q_i).phi(K_j),
+ * den_i = phi(Q_i)^T Z_i.  gamma must lie in [0, 1] (else LA_ERR_INVALID_ARG);
+ * gamma = 1 is la_causal_fwd's operation and gamma = 0 returns V.  These calls
+ * run on the CUDA cores for every supported head size and dtype and take the
+ * workspace of la_workspace_bytes(LA_OP_CAUSAL_FWD_DECAY / _BWD_DECAY, ...);
+ * other arguments and errors as la_causal_fwd / la_causal_bwd.
+ * la_causal_bwd_decay's out and den are la_causal_fwd_decay's, with the same
+ * gamma.
+ */
+la_status la_causal_fwd_decay(const void* q, const void* k, const void* v, void* out, float* den,
+                              float gamma, void* workspace, size_t workspace_bytes, int B, int H,
+                              int N, int D, int M, la_dtype dtype, void* stream);
+la_status la_causal_bwd_decay(const void* q, const void* k, const void* v, const void* out,
+                              const float* den, const void* dout, void* dq, void* dk, void* dv,
+                              float gamma, void* workspace, size_t workspace_bytes, int B, int H,
+                              int N, int D, int M, la_dtype dtype, void* stream);
+
+/*
+ * One decayed RNN step (the decode step of the decayed causal form):
+ *   S <- gamma S + phi(k) v^T,  Z <- gamma Z + phi(k),  y = phi(q)^T S / phi(q)^T Z.
+ * gamma in [0, 1]; arguments otherwise as la_decode_step.
+ */
+la_status la_decode_step_decay(const void* q, const void* k, const void* v, float* S, float* Z,
+                               void* y, float gamma, int B, int H, int D, int M, la_dtype dtype,
+                               void* stream);
 
 /*
  * Reads the status word of the current GPU after all work queued on

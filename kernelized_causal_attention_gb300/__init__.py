@@ -9,7 +9,8 @@ the built library raises.
 
 Raw entry points (same names and argument order as the C ABI, tensors in
 place of pointers): ``la_causal_fwd``, ``la_causal_bwd``, ``la_causal_prefill``,
-``la_noncausal_fwd``, ``la_noncausal_bwd``, ``la_decode_step``,
+``la_noncausal_fwd``, ``la_noncausal_bwd``, ``la_decode_step``, the decayed
+``la_causal_fwd_decay``, ``la_causal_bwd_decay``, ``la_decode_step_decay``,
 ``la_workspace_bytes``, ``la_device_status``.
 Convenience wrappers that allocate outputs with torch: ``causal_fwd``,
 ``causal_bwd``, ``causal_prefill``, ``noncausal_fwd``, ``noncausal_bwd``, ``decode_step`` and the
@@ -32,7 +33,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "liblinattn.so")
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
 LA_F32, LA_BF16 = 0, 1
 (LA_OP_CAUSAL_FWD, LA_OP_CAUSAL_BWD, LA_OP_NONCAUSAL_FWD, LA_OP_NONCAUSAL_BWD, LA_OP_DECODE,
- LA_OP_CAUSAL_PREFILL) = range(6)
+ LA_OP_CAUSAL_PREFILL, LA_OP_CAUSAL_FWD_DECAY, LA_OP_CAUSAL_BWD_DECAY) = range(8)
 
 # exported symbols and their ctypes signatures ("p" pointer, "i" int, "z" size_t,
 # "u" unsigned long long)
@@ -47,6 +48,9 @@ _SIGS = {
     "la_noncausal_fwd": ("p p p p p p p p p z i i i i i i p", ctypes.c_int),
     "la_noncausal_bwd": ("p p p p p p p p p p p p p z i i i i i i p", ctypes.c_int),
     "la_decode_step": ("p p p p p p i i i i i p", ctypes.c_int),
+    "la_causal_fwd_decay": ("p p p p p f p z i i i i i i p", ctypes.c_int),
+    "la_causal_bwd_decay": ("p p p p p p p p p f p z i i i i i i p", ctypes.c_int),
+    "la_decode_step_decay": ("p p p p p p f i i i i i p", ctypes.c_int),
     "la_causal_fwd_noalloc": ("p p p p p i i i i i i p", ctypes.c_int),
     "la_device_status": ("p i p", ctypes.c_int),
     "la_selftest_wait": ("p u", ctypes.c_int),
@@ -78,7 +82,7 @@ def lib():
                     "`python -m kernelized_causal_attention_gb300._build` (needs nvcc).")
             h = ctypes.CDLL(LIB_PATH)
             kinds = {"p": ctypes.c_void_p, "i": ctypes.c_int, "z": ctypes.c_size_t,
-                     "u": ctypes.c_ulonglong}
+                     "u": ctypes.c_ulonglong, "f": ctypes.c_float}
             for name, (sig, res) in _SIGS.items():
                 fn = getattr(h, name)
                 fn.argtypes = [kinds[c] for c in sig.split()]
@@ -178,6 +182,25 @@ def la_decode_step(q, k, v, S, Z, y, B, H, D, M, dtype, stream=None):
                                 _stream(stream)), "la_decode_step")
 
 
+def la_causal_fwd_decay(q, k, v, out, den, gamma, workspace, B, H, N, D, M, dtype, stream=None):
+    _check(lib().la_causal_fwd_decay(_p(q), _p(k), _p(v), _p(out), _p(den), float(gamma),
+                                     _p(workspace), _nbytes(workspace), B, H, N, D, M, dtype,
+                                     _stream(stream)), "la_causal_fwd_decay")
+
+
+def la_causal_bwd_decay(q, k, v, out, den, dout, dq, dk, dv, gamma, workspace, B, H, N, D, M,
+                        dtype, stream=None):
+    _check(lib().la_causal_bwd_decay(_p(q), _p(k), _p(v), _p(out), _p(den), _p(dout), _p(dq),
+                                     _p(dk), _p(dv), float(gamma), _p(workspace),
+                                     _nbytes(workspace), B, H, N, D, M, dtype, _stream(stream)),
+           "la_causal_bwd_decay")
+
+
+def la_decode_step_decay(q, k, v, S, Z, y, gamma, B, H, D, M, dtype, stream=None):
+    _check(lib().la_decode_step_decay(_p(q), _p(k), _p(v), _p(S), _p(Z), _p(y), float(gamma), B,
+                                      H, D, M, dtype, _stream(stream)), "la_decode_step_decay")
+
+
 def la_causal_fwd_noalloc(q, k, v, out, den, B, H, N, D, M, dtype, stream=None):
     """la_causal_fwd with the library's built-in scratch instead of a workspace
     (for callers that may not allocate device memory)."""
@@ -226,6 +249,39 @@ def causal_fwd(q, k, v, stream=None):
     ws = workspace(LA_OP_CAUSAL_FWD, B, H, N, D, M, dt, q.device)
     la_causal_fwd(q, k, v, out, den, ws, B, H, N, D, M, dt, stream)
     return out, den
+
+
+def causal_fwd_decay(q, k, v, gamma, stream=None):
+    """(out, den) of the causal form with the RetNet decay gamma in [0, 1]."""
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    out = torch.empty(B, H, N, M, dtype=q.dtype, device=q.device)
+    den = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+    ws = workspace(LA_OP_CAUSAL_FWD_DECAY, B, H, N, D, M, dt, q.device)
+    la_causal_fwd_decay(q, k, v, out, den, gamma, ws, B, H, N, D, M, dt, stream)
+    return out, den
+
+
+def causal_bwd_decay(q, k, v, out, den, dout, gamma, stream=None):
+    """(dq, dk, dv) of sum(dout * out) for the decayed causal form."""
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = workspace(LA_OP_CAUSAL_BWD_DECAY, B, H, N, D, M, dt, q.device)
+    la_causal_bwd_decay(q, k, v, out, den, dout, dq, dk, dv, gamma, ws, B, H, N, D, M, dt, stream)
+    return dq, dk, dv
+
+
+def decode_step_decay(q, k, v, S, Z, gamma, stream=None):
+    """One decayed RNN step; S, Z updated in place.  Returns y [B,H,M]."""
+    B, H, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    y = torch.empty(B, H, M, dtype=q.dtype, device=q.device)
+    la_decode_step_decay(q, k, v, S, Z, y, gamma, B, H, D, M, dt, stream)
+    return y
 
 
 def causal_prefill(q, k, v, S=None, Z=None, stream=None):

@@ -45,6 +45,8 @@ size_t ws_bytes(int op, const Shape& s) {
       return 4 * (la::tc_eligible(s) ? la::causal_bwd_tc_ws_floats(s) : la::causal_bwd_ws_floats(s));
     case LA_OP_CAUSAL_PREFILL:
       return 4 * (la::tc_eligible(s) ? la::causal_fwd_tc_ws_floats(s) : la::causal_prefill_ws_floats(s));
+    case LA_OP_CAUSAL_FWD_DECAY: return 4 * la::causal_fwd_ws_floats(s);
+    case LA_OP_CAUSAL_BWD_DECAY: return 4 * la::causal_bwd_ws_floats(s);
     case LA_OP_NONCAUSAL_FWD: return 4 * la::noncausal_fwd_ws_floats(s);
     case LA_OP_NONCAUSAL_BWD: return 4 * la::noncausal_bwd_ws_floats(s);
     default: return 0;
@@ -60,6 +62,9 @@ int check_ws(int op, const Shape& s, const void* ws, size_t bytes) {
 }
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+// The RetNet decay must lie in [0, 1] (a NaN fails both comparisons).
+int check_gamma(float gamma) { return (gamma >= 0.f && gamma <= 1.f) ? LA_OK : LA_ERR_INVALID_ARG; }
 
 }  // namespace
 
@@ -114,6 +119,8 @@ int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype) {
     case LA_OP_CAUSAL_BWD:
       return la::tc_eligible(s) ? la::causal_bwd_tc_launches(s) : la::causal_bwd_launches(s);
     case LA_OP_CAUSAL_PREFILL: return la::tc_eligible(s) ? 3 : 4;
+    case LA_OP_CAUSAL_FWD_DECAY: return la::causal_fwd_launches(s);
+    case LA_OP_CAUSAL_BWD_DECAY: return la::causal_bwd_launches(s);
     case LA_OP_NONCAUSAL_FWD: return la::noncausal_fwd_launches(s);
     case LA_OP_NONCAUSAL_BWD: return la::noncausal_bwd_launches(s);
     case LA_OP_DECODE: return 1;
@@ -193,6 +200,40 @@ int la_noncausal_bwd(const void* q, const void* k, const void* v, const int* len
   return from_cuda(la::noncausal_bwd_cc(q, k, v, lengths, out, den, S, Z, dout, dq, dk, dv,
                                         static_cast<float*>(workspace), s,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+int la_causal_fwd_decay(const void* q, const void* k, const void* v, void* out, float* den,
+                        float gamma, void* workspace, size_t workspace_bytes, int B, int H, int N,
+                        int D, int M, int dtype, void* stream) {
+  LA_TRY(la::causal_fwd_check(q, k, v, out, den, B, H, N, D, M, dtype));
+  LA_TRY(check_gamma(gamma));
+  const Shape s{B, H, N, D, M, dtype};
+  LA_TRY(check_ws(LA_OP_CAUSAL_FWD_DECAY, s, workspace, workspace_bytes));
+  return from_cuda(la::causal_fwd_cc(q, k, v, out, den, static_cast<float*>(workspace), s,
+                                     static_cast<cudaStream_t>(stream), gamma));
+}
+
+int la_causal_bwd_decay(const void* q, const void* k, const void* v, const void* out,
+                        const float* den, const void* dout, void* dq, void* dk, void* dv,
+                        float gamma, void* workspace, size_t workspace_bytes, int B, int H, int N,
+                        int D, int M, int dtype, void* stream) {
+  LA_TRY(check_shape(B, H, N, D, M, dtype));
+  LA_TRY(check_ptrs({q, k, v, out, den, dout, dq, dk, dv}));
+  LA_TRY(check_gamma(gamma));
+  const Shape s{B, H, N, D, M, dtype};
+  LA_TRY(check_ws(LA_OP_CAUSAL_BWD_DECAY, s, workspace, workspace_bytes));
+  return from_cuda(la::causal_bwd_cc(q, k, v, out, den, dout, dq, dk, dv,
+                                     static_cast<float*>(workspace), s,
+                                     static_cast<cudaStream_t>(stream), gamma));
+}
+
+int la_decode_step_decay(const void* q, const void* k, const void* v, float* S, float* Z, void* y,
+                         float gamma, int B, int H, int D, int M, int dtype, void* stream) {
+  LA_TRY(check_shape(B, H, 1, D, M, dtype, 1ll << 20));
+  LA_TRY(check_ptrs({q, k, v, S, Z, y}));
+  LA_TRY(check_gamma(gamma));
+  const Shape s{B, H, 1, D, M, dtype};
+  return from_cuda(la::decode_step(q, k, v, S, Z, y, s, static_cast<cudaStream_t>(stream), gamma));
 }
 
 int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* y,

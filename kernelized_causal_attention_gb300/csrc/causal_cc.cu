@@ -14,6 +14,15 @@
 // backward) in fp32.  Inside a chunk the masked chunk-local terms are explicit
 // 64 x 64 products, exactly the quadratic form of eq. 8 restricted to the
 // chunk, and the earlier chunks enter through the carried state.
+//
+// The RetNet decay of "Linear Attention/zh" (variants and extensions),
+// S_t = gamma S_{t-1} + phi(k_t) v_t^T with z decaying alongside S, weighs the
+// pair (i, j) by gamma^(i-j).  With DECAY: the masks multiply each pair by
+// gamma^(i-j) (a table of gamma^0 .. gamma^C); a query row i of a chunk reads
+// the carried state with gamma^(i+1) and a key row j with gamma^(L-j) (L the
+// chunk's valid length); the carried state decays by gamma^L per chunk, and a
+// segment's record is taken relative to its last row (forward sums) or its
+// first row (reverse sums), the scan decaying it by gamma^(segment length).
 #include "common.cuh"
 #include "launch.h"
 
@@ -23,16 +32,32 @@ namespace {
 constexpr int C = kChunk;
 constexpr int NT = 256;
 
+// gamma^e from lg = log2(gamma) (lg = -inf for gamma = 0); gamma^0 = 1.
+__device__ __forceinline__ float decay_pow(float lg, int e) {
+  return e == 0 ? 1.f : exp2f(lg * static_cast<float>(e));
+}
+
+// Multiplies rows [0, C) of the [C][W+1] tile by gamma^(e0 + dir * row) for
+// rows below `valid` (rows past it are zero anyway).
+template <int W>
+__device__ __forceinline__ void scale_rows(float* tile, float lg, int e0, int dir, int valid) {
+  for (int e = threadIdx.x; e < C * W; e += NT) {
+    const int j = e / W, w = e % W;
+    if (j < valid) tile[j * (W + 1) + w] *= decay_pow(lg, e0 + dir * j);
+  }
+}
+
 // ---------------------------------------------------------------- partial sums
 
 // Per-segment sums of the forward state, eq. 10-11 restricted to the segment:
 //   ws[bh][p] = [ dS (D x M) | dz (D) ]  (nrec records per (b, h)).
 // The last segment's sums are only needed for the state after the sequence
 // (all != 0); the forward itself reads exclusive prefixes only.
-template <int D, int M, typename T>
+template <int D, int M, typename T, bool DECAY>
 __global__ void __launch_bounds__(NT) k_seg_state_fwd(const T* __restrict__ k,
                                                       const T* __restrict__ v, float* ws, int N,
-                                                      int nseg, int seg_len, int nrec, int all) {
+                                                      int nseg, int seg_len, int nrec, int all,
+                                                      float lg) {
   const int p = blockIdx.x, bh = blockIdx.y;
   if (p == nseg - 1 && !all) return;
   extern __shared__ float sm[];
@@ -48,6 +73,10 @@ __global__ void __launch_bounds__(NT) k_seg_state_fwd(const T* __restrict__ k,
     load_tile<T, C, D, false, kPhi>(sK, D + 1, kh, n0, ne);
     load_tile<T, C, M, false, kRaw>(sV, M + 1, vh, n0, ne);
     __syncthreads();
+    if (DECAY) {  // relative to the segment's last row: gamma^(ne - 1 - row)
+      scale_rows<D>(sK, lg, (int)(ne - 1 - n0), -1, (int)(ne - n0));
+      __syncthreads();
+    }
     smem_mm<D / 16, M / 16, C>(acc, sK, 1, D + 1, sV, M + 1, 1);
     if (threadIdx.x < D)
       for (int j = 0; j < C; ++j) zacc += sK[j * (D + 1) + threadIdx.x];
@@ -90,14 +119,14 @@ __device__ __forceinline__ void load_grad_terms(float* sG, float* sO, float* sde
 // with dR = sum_i phi(Q_i) gt_i^T and dr = sum_i gam_i phi(Q_i) (the terms of
 // the reverse cumulative sums of eq. 14-15).  dS/dz are skipped for the last
 // segment and dR/dr for the first (never read).
-template <int D, int M, typename T>
+template <int D, int M, typename T, bool DECAY>
 __global__ void __launch_bounds__(NT) k_seg_state_bwd(const T* __restrict__ q,
                                                       const T* __restrict__ k,
                                                       const T* __restrict__ v,
                                                       const T* __restrict__ o,
                                                       const float* __restrict__ den,
                                                       const T* __restrict__ g, float* ws, int N,
-                                                      int nseg, int seg_len) {
+                                                      int nseg, int seg_len, float lg) {
   const int p = blockIdx.x, bh = blockIdx.y;
   const bool want_s = p < nseg - 1, want_r = p > 0;
   extern __shared__ float sm[];
@@ -124,6 +153,11 @@ __global__ void __launch_bounds__(NT) k_seg_state_bwd(const T* __restrict__ q,
       load_grad_terms<T, M>(sG, sO, sden, sgam, g + hv, o + hv, den + (long)bh * N, n0, ne);
     }
     __syncthreads();
+    if (DECAY) {  // forward sums relative to the segment's last row, reverse sums to its first
+      if (want_s) scale_rows<D>(sK, lg, (int)(ne - 1 - n0), -1, (int)(ne - n0));
+      if (want_r) scale_rows<D>(sQ, lg, (int)(n0 - nb), 1, (int)(ne - n0));
+      __syncthreads();
+    }
     if (want_s) {
       smem_mm<D / 16, M / 16, C>(accS, sK, 1, D + 1, sV, M + 1, 1);
       if (threadIdx.x < D)
@@ -155,15 +189,20 @@ __global__ void __launch_bounds__(NT) k_seg_state_bwd(const T* __restrict__ q,
 // [0, wf) of every record become prefix sums over earlier segments, entries
 // [ro, ro + wr) suffix sums over later segments.  One thread per entry.
 // With nrec > nseg, record nseg receives the forward totals.
-__global__ void k_seg_scan(float* ws, int nseg, int stride, int wf, int ro, int wr, int nrec) {
+// With the decay (lg = log2 gamma != 0) a record is relative to its segment's
+// last row (forward) or first row (reverse), and the running sum decays by
+// gamma^(segment length) when it passes a segment; lg = 0 multiplies by one.
+__global__ void k_seg_scan(float* ws, int nseg, int stride, int wf, int ro, int wr, int nrec,
+                           float lg, int seg_len, int N) {
   float* base = ws + (long)blockIdx.x * nrec * stride;
   const int e = blockIdx.y * blockDim.x + threadIdx.x;
+  auto len = [&](int p) { return min(N - p * seg_len, seg_len); };
   if (e < wf) {
     float run = 0.f;
     for (int p = 0; p < nseg; ++p) {
       const float x = base[(long)p * stride + e];
       base[(long)p * stride + e] = run;
-      run += x;
+      run = lg != 0.f ? decay_pow(lg, len(p)) * run + x : run + x;
     }
     if (nrec > nseg) base[(long)nseg * stride + e] = run;
   }
@@ -172,7 +211,7 @@ __global__ void k_seg_scan(float* ws, int nseg, int stride, int wf, int ro, int 
     for (int p = nseg - 1; p >= 0; --p) {
       const float x = base[(long)p * stride + ro + e];
       base[(long)p * stride + ro + e] = run;
-      run += x;
+      run = lg != 0.f ? x + decay_pow(lg, len(p)) * run : run + x;
     }
   }
 }
@@ -185,7 +224,7 @@ __global__ void k_seg_scan(float* ws, int nseg, int stride, int wf, int ro, int 
 //   out = (A V + phi(Q) S) / den                 (eq. 12 numerator)
 //   S  += phi(K)^T V,  z += sum phi(K)           (eq. 10-11)
 // S0, Z0 (may be null): a state the sums start from (eq. 16-19 over a prompt).
-template <int D, int M, typename T>
+template <int D, int M, typename T, bool DECAY>
 __global__ void __launch_bounds__(NT) k_causal_fwd(const T* __restrict__ q,
                                                    const T* __restrict__ k,
                                                    const T* __restrict__ v, T* __restrict__ out,
@@ -193,7 +232,7 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(const T* __restrict__ q,
                                                    const float* __restrict__ ws, int N, int nseg,
                                                    int seg_len, int nrec,
                                                    const float* __restrict__ S0,
-                                                   const float* __restrict__ Z0) {
+                                                   const float* __restrict__ Z0, float lg) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ float sm[];
   float* sQ = sm;                  // phi(Q) [C][D+1]
@@ -203,9 +242,11 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(const T* __restrict__ q,
   float* sS = sA + C * (C + 1);    // S      [D][M+1]
   float* sz = sS + D * (M + 1);    // z      [D]
   float* sden = sz + D;            // [C]
+  float* spw = sden + C;           // gamma^0 .. gamma^C (with DECAY)
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const long nb = (long)p * seg_len, ne = min((long)N, nb + seg_len);
   const long hq = (long)bh * N * D, hv = (long)bh * N * M;
+  if (DECAY && threadIdx.x <= C) spw[threadIdx.x] = decay_pow(lg, threadIdx.x);
 
   // exclusive prefix state of this segment (plus the initial state)
   const float* pre = ws + ((long)bh * nrec + p) * (D * M + D);
@@ -236,7 +277,7 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(const T* __restrict__ q,
 #pragma unroll
         for (int c = 0; c < C / 16; ++c) {
           const int i = ty + 16 * r, j = tx + 16 * c;
-          sA[i * (C + 1) + j] = j <= i ? a[r][c] : 0.f;
+          sA[i * (C + 1) + j] = j <= i ? (DECAY ? a[r][c] * spw[i - j] : a[r][c]) : 0.f;
         }
     }
     __syncthreads();
@@ -244,7 +285,13 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(const T* __restrict__ q,
       const int i = threadIdx.x;
       float s = 0.f;
       for (int j = 0; j <= i; ++j) s += sA[i * (C + 1) + j];
-      for (int d = 0; d < D; ++d) s += sQ[i * (D + 1) + d] * sz[d];
+      if (DECAY) {  // the carried state reaches row i with gamma^(i+1)
+        float t = 0.f;
+        for (int d = 0; d < D; ++d) t += sQ[i * (D + 1) + d] * sz[d];
+        s += spw[i + 1] * t;
+      } else {
+        for (int d = 0; d < D; ++d) s += sQ[i * (D + 1) + d] * sz[d];
+      }
       sden[i] = s;
       if (den != nullptr && n0 + i < ne) den[(long)bh * N + n0 + i] = s;
     }
@@ -253,7 +300,17 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(const T* __restrict__ q,
       float o[C / 16][M / 16];
       zero_acc(o);
       smem_mm<C / 16, M / 16, C>(o, sA, C + 1, 1, sV, M + 1, 1);
-      smem_mm<C / 16, M / 16, D>(o, sQ, D + 1, 1, sS, M + 1, 1);
+      if (DECAY) {
+        float o2[C / 16][M / 16];
+        zero_acc(o2);
+        smem_mm<C / 16, M / 16, D>(o2, sQ, D + 1, 1, sS, M + 1, 1);
+#pragma unroll
+        for (int r = 0; r < C / 16; ++r)
+#pragma unroll
+          for (int c = 0; c < M / 16; ++c) o[r][c] += spw[ty + 16 * r + 1] * o2[r][c];
+      } else {
+        smem_mm<C / 16, M / 16, D>(o, sQ, D + 1, 1, sS, M + 1, 1);
+      }
 #pragma unroll
       for (int r = 0; r < C / 16; ++r) {
         const int i = ty + 16 * r;
@@ -266,7 +323,20 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(const T* __restrict__ q,
       }
     }
     __syncthreads();
-    // S += phi(K)^T V, z += sum phi(K)
+    // S += phi(K)^T V, z += sum phi(K); with DECAY S <- gamma^L S + sum_j
+    // gamma^(L-1-j) phi(K_j) V_j^T (L = the chunk's valid rows)
+    const int L = (int)min((long)C, ne - n0);
+    (void)L;
+    if (DECAY) {
+      scale_rows<D>(sK, lg, L - 1, -1, L);
+      const float dl = spw[L];
+#pragma unroll
+      for (int r = 0; r < D / 16; ++r)
+#pragma unroll
+        for (int c = 0; c < M / 16; ++c) accS[r][c] *= dl;
+      if (threadIdx.x < D) sz[threadIdx.x] *= dl;
+      __syncthreads();
+    }
     smem_mm<D / 16, M / 16, C>(accS, sK, 1, D + 1, sV, M + 1, 1);
 #pragma unroll
     for (int r = 0; r < D / 16; ++r)
@@ -293,12 +363,12 @@ __global__ void __launch_bounds__(NT) k_causal_fwd(const T* __restrict__ q,
 //   grad_phiK = dA^T phi(Q) + V R^T + r,        dk = grad_phiK * phi'(K)
 //   dv        = A^T gt + phi(K) R
 //   R += phi(Q)^T gt,  r += phi(Q)^T gam
-template <int D, int M, typename T>
+template <int D, int M, typename T, bool DECAY>
 __global__ void __launch_bounds__(NT) k_causal_bwd(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const T* __restrict__ o, const float* __restrict__ den, const T* __restrict__ g,
     T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv, const float* __restrict__ ws,
-    int N, int nseg, int seg_len) {
+    int N, int nseg, int seg_len, float lg) {
   const int p = blockIdx.x, bh = blockIdx.y, role = blockIdx.z;
   extern __shared__ float sm[];
   float* sQ = sm;                  // phi(Q) [C][D+1]
@@ -312,9 +382,11 @@ __global__ void __launch_bounds__(NT) k_causal_bwd(
   float* sz = sS + D * (M + 1);    // z or r [D]
   float* sden = sz + D;            // [C]
   float* sgam = sden + C;          // [C]
+  float* spw = sgam + C;           // gamma^0 .. gamma^C (with DECAY)
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const long nb = (long)p * seg_len, ne = min((long)N, nb + seg_len);
   const long hq = (long)bh * N * D, hv = (long)bh * N * M;
+  if (DECAY && threadIdx.x <= C) spw[threadIdx.x] = decay_pow(lg, threadIdx.x);
   const float* rec = ws + ((long)bh * nseg + p) * 2 * (D * M + D);
   // role 0: exclusive prefix (S, z) of the segment; role 1: exclusive suffix (R, r)
   const float* st = rec + (role == 0 ? 0 : D * M + D);
@@ -333,6 +405,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd(
   const int nchunks = (int)((ne - nb + C - 1) / C);
   for (int ci = 0; ci < nchunks; ++ci) {
     const long n0 = role == 0 ? nb + (long)ci * C : nb + (long)(nchunks - 1 - ci) * C;
+    const int L = (int)min((long)C, ne - n0);  // valid rows of the chunk
     if (role == 1) load_tile<T, C, D, false, kPhi>(sQ, D + 1, q + hq, n0, ne);
     load_tile<T, C, D, false, kPhi>(sK, D + 1, k + hq, n0, ne);
     load_tile<T, C, M, false, kRaw>(sV, M + 1, v + hv, n0, ne);
@@ -347,7 +420,7 @@ __global__ void __launch_bounds__(NT) k_causal_bwd(
 #pragma unroll
         for (int c = 0; c < C / 16; ++c) {
           const int i = ty + 16 * r, j = tx + 16 * c;
-          sdA[i * (C + 1) + j] = j <= i ? a[r][c] + sgam[i] : 0.f;
+          sdA[i * (C + 1) + j] = j <= i ? (DECAY ? (a[r][c] + sgam[i]) * spw[i - j] : a[r][c] + sgam[i]) : 0.f;
         }
       if (role == 1) {
         zero_acc(a);
@@ -357,16 +430,21 @@ __global__ void __launch_bounds__(NT) k_causal_bwd(
 #pragma unroll
           for (int c = 0; c < C / 16; ++c) {
             const int i = ty + 16 * r, j = tx + 16 * c;
-            sA[i * (C + 1) + j] = j <= i ? a[r][c] : 0.f;
+            sA[i * (C + 1) + j] = j <= i ? (DECAY ? a[r][c] * spw[i - j] : a[r][c]) : 0.f;
           }
       }
     }
     __syncthreads();
     if (role == 0) {
-      float t[C / 16][D / 16];
+      float t[C / 16][D / 16], t2[C / 16][D / 16];
       zero_acc(t);
       smem_mm<C / 16, D / 16, C>(t, sdA, C + 1, 1, sK, D + 1, 1);   // dA phi(K)
-      smem_mm<C / 16, D / 16, M>(t, sG, M + 1, 1, sS, 1, M + 1);    // gt S^T
+      if (DECAY) {  // the carried state reaches query row i with gamma^(i+1)
+        zero_acc(t2);
+        smem_mm<C / 16, D / 16, M>(t2, sG, M + 1, 1, sS, 1, M + 1);  // gt S^T
+      } else {
+        smem_mm<C / 16, D / 16, M>(t, sG, M + 1, 1, sS, 1, M + 1);   // gt S^T
+      }
 #pragma unroll
       for (int r = 0; r < C / 16; ++r) {
         const int i = ty + 16 * r;
@@ -375,16 +453,22 @@ __global__ void __launch_bounds__(NT) k_causal_bwd(
           for (int c = 0; c < D / 16; ++c) {
             const int d = tx + 16 * c;
             const long idx = hq + (n0 + i) * D + d;
-            const float gq = t[r][c] + sgam[i] * sz[d];
+            const float gq = DECAY ? t[r][c] + spw[i + 1] * (t2[r][c] + sgam[i] * sz[d])
+                                   : t[r][c] + sgam[i] * sz[d];
             dq[idx] = from_f<T>(gq * dphi(to_f(q[idx])));
           }
         }
       }
     } else {
-      float t[C / 16][D / 16];
+      float t[C / 16][D / 16], t2[C / 16][D / 16];
       zero_acc(t);
       smem_mm<C / 16, D / 16, C>(t, sdA, 1, C + 1, sQ, D + 1, 1);   // dA^T phi(Q)
-      smem_mm<C / 16, D / 16, M>(t, sV, M + 1, 1, sS, 1, M + 1);    // V R^T
+      if (DECAY) {  // the carried state (the sums after the chunk) reaches key row j with gamma^(L-j)
+        zero_acc(t2);
+        smem_mm<C / 16, D / 16, M>(t2, sV, M + 1, 1, sS, 1, M + 1);  // V R^T
+      } else {
+        smem_mm<C / 16, D / 16, M>(t, sV, M + 1, 1, sS, 1, M + 1);   // V R^T
+      }
 #pragma unroll
       for (int r = 0; r < C / 16; ++r) {
         const int j = ty + 16 * r;
@@ -393,25 +477,45 @@ __global__ void __launch_bounds__(NT) k_causal_bwd(
           for (int c = 0; c < D / 16; ++c) {
             const int d = tx + 16 * c;
             const long idx = hq + (n0 + j) * D + d;
-            const float gk = t[r][c] + sz[d];
+            const float gk = DECAY ? t[r][c] + spw[L - j] * (t2[r][c] + sz[d]) : t[r][c] + sz[d];
             dk[idx] = from_f<T>(gk * dphi(to_f(k[idx])));
           }
         }
       }
-      float u[C / 16][M / 16];
+      float u[C / 16][M / 16], u2[C / 16][M / 16];
       zero_acc(u);
       smem_mm<C / 16, M / 16, C>(u, sA, 1, C + 1, sG, M + 1, 1);    // A^T gt
-      smem_mm<C / 16, M / 16, D>(u, sK, D + 1, 1, sS, M + 1, 1);    // phi(K) R
+      if (DECAY) {
+        zero_acc(u2);
+        smem_mm<C / 16, M / 16, D>(u2, sK, D + 1, 1, sS, M + 1, 1);  // phi(K) R
+      } else {
+        smem_mm<C / 16, M / 16, D>(u, sK, D + 1, 1, sS, M + 1, 1);   // phi(K) R
+      }
 #pragma unroll
       for (int r = 0; r < C / 16; ++r) {
         const int j = ty + 16 * r;
         if (n0 + j < ne) {
 #pragma unroll
-          for (int c = 0; c < M / 16; ++c) dv[hv + (n0 + j) * M + tx + 16 * c] = from_f<T>(u[r][c]);
+          for (int c = 0; c < M / 16; ++c)
+            dv[hv + (n0 + j) * M + tx + 16 * c] =
+                from_f<T>(DECAY ? u[r][c] + spw[L - j] * u2[r][c] : u[r][c]);
         }
       }
     }
     __syncthreads();
+    if (DECAY) {  // the chunk's rows relative to where the carried state continues, and its decay
+      if (role == 0)
+        scale_rows<D>(sK, lg, L - 1, -1, L);  // gamma^(L-1-j)
+      else
+        scale_rows<D>(sQ, lg, 0, 1, L);       // gamma^i
+      const float dl = spw[L];
+#pragma unroll
+      for (int r = 0; r < D / 16; ++r)
+#pragma unroll
+        for (int c = 0; c < M / 16; ++c) acc[r][c] *= dl;
+      if (threadIdx.x < D) sz[threadIdx.x] *= dl;
+      __syncthreads();
+    }
     if (role == 0) {  // S += phi(K)^T V, z += sum phi(K)
       smem_mm<D / 16, M / 16, C>(acc, sK, 1, D + 1, sV, M + 1, 1);
       if (threadIdx.x < D) {
@@ -437,12 +541,12 @@ __global__ void __launch_bounds__(NT) k_causal_bwd(
 
 template <int D, int M>
 constexpr size_t fwd_smem() {
-  return sizeof(float) * (2 * C * (D + 1) + C * (M + 1) + C * (C + 1) + D * (M + 1) + D + C);
+  return sizeof(float) * (2 * C * (D + 1) + C * (M + 1) + C * (C + 1) + D * (M + 1) + D + C + C + 1);
 }
 template <int D, int M>
 constexpr size_t bwd_smem() {
   return sizeof(float) *
-         (2 * C * (D + 1) + 3 * C * (M + 1) + 2 * C * (C + 1) + D * (M + 1) + D + 2 * C);
+         (2 * C * (D + 1) + 3 * C * (M + 1) + 2 * C * (C + 1) + D * (M + 1) + D + 2 * C + C + 1);
 }
 template <int D, int M>
 constexpr size_t state_fwd_smem() {
@@ -458,24 +562,25 @@ cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <int D, int M, typename T>
+// lg = log2(gamma) of the RetNet decay (0: undecayed).
+template <int D, int M, typename T, bool DECAY>
 cudaError_t run_fwd(const T* q, const T* k, const T* v, T* out, float* den, float* ws,
-                    const Shape& s, cudaStream_t st) {
+                    const Shape& s, cudaStream_t st, float lg) {
   const int BH = s.B * s.H;
   const SegPlan pl = plan_segments(BH, s.N);
   cudaError_t e;
   if (pl.nseg > 1) {
-    auto ks = k_seg_state_fwd<D, M, T>;
+    auto ks = k_seg_state_fwd<D, M, T, DECAY>;
     if ((e = set_smem(ks, state_fwd_smem<D, M>())) != cudaSuccess) return e;
     ks<<<dim3(pl.nseg, BH), NT, state_fwd_smem<D, M>(), st>>>(k, v, ws, s.N, pl.nseg, pl.seg_len,
-                                                              pl.nseg, 0);
-    k_seg_scan<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(ws, pl.nseg, D * M + D,
-                                                                  D * M + D, 0, 0, pl.nseg);
+                                                              pl.nseg, 0, lg);
+    k_seg_scan<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(
+        ws, pl.nseg, D * M + D, D * M + D, 0, 0, pl.nseg, DECAY ? lg : 0.f, pl.seg_len, s.N);
   }
-  auto kf = k_causal_fwd<D, M, T>;
+  auto kf = k_causal_fwd<D, M, T, DECAY>;
   if ((e = set_smem(kf, fwd_smem<D, M>())) != cudaSuccess) return e;
   kf<<<dim3(pl.nseg, BH), NT, fwd_smem<D, M>(), st>>>(q, k, v, out, den, ws, s.N, pl.nseg,
-                                                      pl.seg_len, pl.nseg, nullptr, nullptr);
+                                                      pl.seg_len, pl.nseg, nullptr, nullptr, lg);
   return cudaGetLastError();
 }
 
@@ -490,38 +595,39 @@ cudaError_t run_prefill(const T* q, const T* k, const T* v, T* out, float* den, 
   const SegPlan pl = plan_segments(BH, s.N);
   const int nrec = pl.nseg + 1;
   cudaError_t e;
-  auto ks = k_seg_state_fwd<D, M, T>;
+  auto ks = k_seg_state_fwd<D, M, T, false>;
   if ((e = set_smem(ks, state_fwd_smem<D, M>())) != cudaSuccess) return e;
   ks<<<dim3(pl.nseg, BH), NT, state_fwd_smem<D, M>(), st>>>(k, v, ws, s.N, pl.nseg, pl.seg_len,
-                                                            nrec, 1);
+                                                            nrec, 1, 0.f);
   k_seg_scan<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(ws, pl.nseg, D * M + D, D * M + D,
-                                                                0, 0, nrec);
-  auto kf = k_causal_fwd<D, M, T>;
+                                                                0, 0, nrec, 0.f, pl.seg_len, s.N);
+  auto kf = k_causal_fwd<D, M, T, false>;
   if ((e = set_smem(kf, fwd_smem<D, M>())) != cudaSuccess) return e;
   kf<<<dim3(pl.nseg, BH), NT, fwd_smem<D, M>(), st>>>(q, k, v, out, den, ws, s.N, pl.nseg,
-                                                      pl.seg_len, nrec, S, Z);
+                                                      pl.seg_len, nrec, S, Z, 0.f);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return state_add_records(ws, BH, nrec, D * M + D, pl.nseg, nrec, D, M, M, D * M, 1, S, Z, st);
 }
 
-template <int D, int M, typename T>
+template <int D, int M, typename T, bool DECAY>
 cudaError_t run_bwd(const T* q, const T* k, const T* v, const T* o, const float* den, const T* g,
-                    T* dq, T* dk, T* dv, float* ws, const Shape& s, cudaStream_t st) {
+                    T* dq, T* dk, T* dv, float* ws, const Shape& s, cudaStream_t st, float lg) {
   const int BH = s.B * s.H;
   const SegPlan pl = plan_segments(BH, s.N);
   cudaError_t e;
   if (pl.nseg > 1) {
-    auto ks = k_seg_state_bwd<D, M, T>;
+    auto ks = k_seg_state_bwd<D, M, T, DECAY>;
     if ((e = set_smem(ks, state_bwd_smem<D, M>())) != cudaSuccess) return e;
     ks<<<dim3(pl.nseg, BH), NT, state_bwd_smem<D, M>(), st>>>(q, k, v, o, den, g, ws, s.N,
-                                                              pl.nseg, pl.seg_len);
+                                                              pl.nseg, pl.seg_len, lg);
     k_seg_scan<<<dim3(BH, (D * M + D + 255) / 256), 256, 0, st>>>(
-        ws, pl.nseg, 2 * (D * M + D), D * M + D, D * M + D, D * M + D, pl.nseg);
+        ws, pl.nseg, 2 * (D * M + D), D * M + D, D * M + D, D * M + D, pl.nseg, DECAY ? lg : 0.f,
+        pl.seg_len, s.N);
   }
-  auto kb = k_causal_bwd<D, M, T>;
+  auto kb = k_causal_bwd<D, M, T, DECAY>;
   if ((e = set_smem(kb, bwd_smem<D, M>())) != cudaSuccess) return e;
   kb<<<dim3(pl.nseg, BH, 2), NT, bwd_smem<D, M>(), st>>>(q, k, v, o, den, g, dq, dk, dv, ws,
-                                                         s.N, pl.nseg, pl.seg_len);
+                                                         s.N, pl.nseg, pl.seg_len, lg);
   return cudaGetLastError();
 }
 
@@ -530,7 +636,7 @@ cudaError_t run_bwd(const T* q, const T* k, const T* v, const T* o, const float*
 void k_seg_scan_ext(float* ws, int BH, int nseg, int stride, int wf, int ro, int wr,
                     cudaStream_t st) {
   const int w = wf > wr ? wf : wr;
-  k_seg_scan<<<dim3(BH, (w + 255) / 256), 256, 0, st>>>(ws, nseg, stride, wf, ro, wr, nseg);
+  k_seg_scan<<<dim3(BH, (w + 255) / 256), 256, 0, st>>>(ws, nseg, stride, wf, ro, wr, nseg, 0.f, 1, 1);
 }
 
 namespace {
@@ -603,35 +709,55 @@ int causal_bwd_launches(const Shape& s) {
 }
 
 cudaError_t causal_fwd_cc(const void* q, const void* k, const void* v, void* out, float* den,
-                          float* ws, const Shape& s, cudaStream_t st) {
+                          float* ws, const Shape& s, cudaStream_t st, float gamma) {
+  const bool dec = gamma != 1.f;
+  const float lg = dec ? log2f(gamma) : 0.f;  // -inf for gamma = 0
   if (s.dtype == 0) {
     using T = float;
-    LA_DISPATCH_DM(s.D, s.M, return (run_fwd<D_, M_, T>((const T*)q, (const T*)k, (const T*)v,
-                                                         (T*)out, den, ws, s, st)));
+    if (dec) {
+      LA_DISPATCH_DM(s.D, s.M, return (run_fwd<D_, M_, T, true>((const T*)q, (const T*)k, (const T*)v,
+                                                                (T*)out, den, ws, s, st, lg)));
+    } else {
+      LA_DISPATCH_DM(s.D, s.M, return (run_fwd<D_, M_, T, false>((const T*)q, (const T*)k, (const T*)v,
+                                                                 (T*)out, den, ws, s, st, 0.f)));
+    }
   } else {
     using T = __nv_bfloat16;
-    LA_DISPATCH_DM(s.D, s.M, return (run_fwd<D_, M_, T>((const T*)q, (const T*)k, (const T*)v,
-                                                         (T*)out, den, ws, s, st)));
+    if (dec) {
+      LA_DISPATCH_DM(s.D, s.M, return (run_fwd<D_, M_, T, true>((const T*)q, (const T*)k, (const T*)v,
+                                                                (T*)out, den, ws, s, st, lg)));
+    } else {
+      LA_DISPATCH_DM(s.D, s.M, return (run_fwd<D_, M_, T, false>((const T*)q, (const T*)k, (const T*)v,
+                                                                 (T*)out, den, ws, s, st, 0.f)));
+    }
   }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t causal_bwd_cc(const void* q, const void* k, const void* v, const void* out,
                           const float* den, const void* dout, void* dq, void* dk, void* dv,
-                          float* ws, const Shape& s, cudaStream_t st) {
+                          float* ws, const Shape& s, cudaStream_t st, float gamma) {
+  const bool dec = gamma != 1.f;
+  const float lg = dec ? log2f(gamma) : 0.f;
+#define LA_BWD_CALL(T, DEC, LG)                                                                    \
+  LA_DISPATCH_DM(s.D, s.M,                                                                         \
+                 return (run_bwd<D_, M_, T, DEC>((const T*)q, (const T*)k, (const T*)v,            \
+                                                 (const T*)out, den, (const T*)dout, (T*)dq,       \
+                                                 (T*)dk, (T*)dv, ws, s, st, LG)))
   if (s.dtype == 0) {
-    using T = float;
-    LA_DISPATCH_DM(s.D, s.M,
-                   return (run_bwd<D_, M_, T>((const T*)q, (const T*)k, (const T*)v,
-                                              (const T*)out, den, (const T*)dout, (T*)dq, (T*)dk,
-                                              (T*)dv, ws, s, st)));
+    if (dec) {
+      LA_BWD_CALL(float, true, lg);
+    } else {
+      LA_BWD_CALL(float, false, 0.f);
+    }
   } else {
-    using T = __nv_bfloat16;
-    LA_DISPATCH_DM(s.D, s.M,
-                   return (run_bwd<D_, M_, T>((const T*)q, (const T*)k, (const T*)v,
-                                              (const T*)out, den, (const T*)dout, (T*)dq, (T*)dk,
-                                              (T*)dv, ws, s, st)));
+    if (dec) {
+      LA_BWD_CALL(__nv_bfloat16, true, lg);
+    } else {
+      LA_BWD_CALL(__nv_bfloat16, false, 0.f);
+    }
   }
+#undef LA_BWD_CALL
   return cudaErrorInvalidValue;
 }
 

@@ -1,6 +1,8 @@
 // RNN-form decode step, "Transformers are RNNs" (part 2/3) §3.4 eq. 16-19:
 //   s <- s + phi(k) v^T,  z <- z + phi(k),  y = phi(q)^T s / phi(q)^T z
-// for B*H independent streams, with the fp32 state updated in place.
+// for B*H independent streams, with the fp32 state updated in place.  With the
+// RetNet decay of "Linear Attention/zh" (variants and extensions) the state is
+// decayed first: s <- gamma s + phi(k) v^T, z <- gamma z + phi(k).
 //
 // The step is bound by HBM traffic on the state (read and write D*M*4 bytes
 // per stream); the kernel streams each stream's S once with 16-byte
@@ -14,10 +16,11 @@ namespace {
 
 constexpr int NT = 256;
 
-template <int D, int M, typename T>
+template <int D, int M, typename T, bool DECAY>
 __global__ void __launch_bounds__(NT) k_decode(const T* __restrict__ q, const T* __restrict__ k,
                                                const T* __restrict__ v, float* __restrict__ S,
-                                               float* __restrict__ Z, T* __restrict__ y) {
+                                               float* __restrict__ Z, T* __restrict__ y,
+                                               float gamma) {
   constexpr int M4 = M / 4;                 // float4 columns of one state row
   constexpr int RG = NT / M4;               // threads sharing one column group
   constexpr int RPT = (D + RG - 1) / RG;    // state rows per thread
@@ -46,6 +49,12 @@ __global__ void __launch_bounds__(NT) k_decode(const T* __restrict__ q, const T*
     const int d = rg + r * RG;
     if (d < D) {
       const float fk = sfk[d], fq = sfq[d];
+      if (DECAY) {
+        s[r].x *= gamma;
+        s[r].y *= gamma;
+        s[r].z *= gamma;
+        s[r].w *= gamma;
+      }
       s[r].x = fmaf(fk, v0, s[r].x);
       s[r].y = fmaf(fk, v1, s[r].y);
       s[r].z = fmaf(fk, v2, s[r].z);
@@ -62,7 +71,7 @@ __global__ void __launch_bounds__(NT) k_decode(const T* __restrict__ q, const T*
   // z <- z + phi(k);  den = phi(q) . z
   float dp = 0.f;
   if (tid < D) {
-    const float z = Z[(long)bh * D + tid] + sfk[tid];
+    const float z = (DECAY ? gamma * Z[(long)bh * D + tid] : Z[(long)bh * D + tid]) + sfk[tid];
     Z[(long)bh * D + tid] = z;
     dp = sfq[tid] * z;
   }
@@ -87,18 +96,31 @@ __global__ void __launch_bounds__(NT) k_decode(const T* __restrict__ q, const T*
 }  // namespace
 
 cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* y,
-                        const Shape& s, cudaStream_t st) {
+                        const Shape& s, cudaStream_t st, float gamma) {
   const int BH = s.B * s.H;
+  const bool dec = gamma != 1.f;
   if (s.dtype == 0) {
     using T = float;
-    LA_DISPATCH_DM(s.D, s.M,
-                   (k_decode<D_, M_, T><<<BH, NT, 0, st>>>((const T*)q, (const T*)k, (const T*)v,
-                                                           S, Z, (T*)y)));
+    if (dec) {
+      LA_DISPATCH_DM(s.D, s.M,
+                     (k_decode<D_, M_, T, true><<<BH, NT, 0, st>>>((const T*)q, (const T*)k,
+                                                                   (const T*)v, S, Z, (T*)y, gamma)));
+    } else {
+      LA_DISPATCH_DM(s.D, s.M,
+                     (k_decode<D_, M_, T, false><<<BH, NT, 0, st>>>((const T*)q, (const T*)k,
+                                                                    (const T*)v, S, Z, (T*)y, 1.f)));
+    }
   } else {
     using T = __nv_bfloat16;
-    LA_DISPATCH_DM(s.D, s.M,
-                   (k_decode<D_, M_, T><<<BH, NT, 0, st>>>((const T*)q, (const T*)k, (const T*)v,
-                                                           S, Z, (T*)y)));
+    if (dec) {
+      LA_DISPATCH_DM(s.D, s.M,
+                     (k_decode<D_, M_, T, true><<<BH, NT, 0, st>>>((const T*)q, (const T*)k,
+                                                                   (const T*)v, S, Z, (T*)y, gamma)));
+    } else {
+      LA_DISPATCH_DM(s.D, s.M,
+                     (k_decode<D_, M_, T, false><<<BH, NT, 0, st>>>((const T*)q, (const T*)k,
+                                                                    (const T*)v, S, Z, (T*)y, 1.f)));
+    }
   }
   return cudaGetLastError();
 }

@@ -97,11 +97,12 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
                           float* ws, const Shape& s, cudaStream_t st);
 
 // CUDA-core (FFMA) paths; every kernel of the library is launched from these.
+// gamma: the RetNet decay in [0, 1] (1 = the undecayed method).
 cudaError_t causal_fwd_cc(const void* q, const void* k, const void* v, void* out, float* den,
-                          float* ws, const Shape& s, cudaStream_t st);
+                          float* ws, const Shape& s, cudaStream_t st, float gamma = 1.f);
 cudaError_t causal_bwd_cc(const void* q, const void* k, const void* v, const void* out,
                           const float* den, const void* dout, void* dq, void* dk, void* dv,
-                          float* ws, const Shape& s, cudaStream_t st);
+                          float* ws, const Shape& s, cudaStream_t st, float gamma = 1.f);
 cudaError_t noncausal_fwd_cc(const void* q, const void* k, const void* v, const int* lengths,
                              void* out, float* den, float* S, float* Z, float* ws, const Shape& s,
                              cudaStream_t st);
@@ -118,8 +119,9 @@ cudaError_t noncausal_tc_fwd(const void* q, const void* k, const void* v, const 
 cudaError_t noncausal_tc_bwd(const void* q, const void* k, const void* v, const int* lengths,
                              const float* den, const float* S, const float* Z, const void* dout,
                              void* dq, void* dk, void* dv, const Shape& s, cudaStream_t st);
+// gamma: the RetNet decay (1 = the undecayed step).
 cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* y,
-                        const Shape& s, cudaStream_t st);
+                        const Shape& s, cudaStream_t st, float gamma = 1.f);
 
 }  // namespace la
 
