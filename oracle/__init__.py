@@ -212,6 +212,24 @@ class Oracle:
                                       _ptr(S), _ptr(Z), _ptr(y), nthreads)
         return y, S, Z
 
+    def decode_proj(self, x, W, H, D, M, S=None, Z=None, nthreads=0):
+        """One RNN step (eq. 16-19) whose q_t, k_t, v_t are the projections
+        x_t W of the layer input (eq. 18-20 write phi(x_i W_Q), x_i W_K,
+        x_i W_V); f_l and the residual of eq. 20 are not applied.  x: [B,
+        d_model]; W: [d_model, H*(2D+M)] with columns [Q of heads 0..H-1 | K of
+        heads 0..H-1 | V of heads 0..H-1]; S, Z: state (zeros if None).  The
+        projection is a plain fp64 matmul (numpy); the step is orc_decode.
+        Returns (y [B,H,M], S_1 [B,H,D,M], Z_1 [B,H,D])."""
+        x, W = _f64(x), _f64(W)
+        B = x.shape[0]
+        assert W.shape == (x.shape[1], H * (2 * D + M))
+        p = x @ W  # [B, H*(2D+M)]
+        q = p[:, :H * D].reshape(1, B, H, D)
+        k = p[:, H * D:2 * H * D].reshape(1, B, H, D)
+        v = p[:, 2 * H * D:].reshape(1, B, H, M)
+        y, S1, Z1 = self.decode(q, k, v, S, Z, nthreads)
+        return y[0], S1, Z1
+
     def causal_prefill(self, q, k, v, S=None, Z=None, nthreads=0):
         """The causal form started from the state (S, Z) (zeros if None):
         eq. 16-19 over a prompt.  q, k: [B,H,N,D]; v: [B,H,N,M].
@@ -266,3 +284,7 @@ def decode(q, k, v, S=None, Z=None, nthreads=0, gamma=None):
 
 def causal_prefill(q, k, v, S=None, Z=None, nthreads=0):
     return default().causal_prefill(q, k, v, S, Z, nthreads)
+
+
+def decode_proj(x, W, H, D, M, S=None, Z=None, nthreads=0):
+    return default().decode_proj(x, W, H, D, M, S, Z, nthreads)

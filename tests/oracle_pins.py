@@ -457,8 +457,40 @@ def pin_decay_decode(orc):
         assert rel(Z, np.einsum("t,tbhd->bhd", w, fk)) < 1e-13
 
 
+# --------------------------------------------- decode with the projection
+
+def pin_decode_proj(orc):
+    """The projected step against things fixed outside it: with x = [q | k |
+    v] of every head side by side and W the matching block identity, it is the
+    plain decode step (orc_decode) on those q, k, v; for general W its state
+    is S_0 + phi(k) v^T with k, v from numpy's x @ W, and its output is the
+    quotient phi(q)^T S_1 / phi(q)^T Z_1 formed with numpy."""
+    B, H, D, M = 5, 3, 4, 6
+    q, k, v = rand((B, H, D), 301), rand((B, H, D), 302), rand((B, H, M), 303)
+    S0, Z0 = rand((B, H, D, M), 304), 2.0 * phi_lib(rand((B, H, D), 305))
+    x = np.concatenate([q.reshape(B, -1), k.reshape(B, -1), v.reshape(B, -1)], axis=1)
+    W = np.eye(x.shape[1])
+    y, S1, Z1 = orc.decode_proj(x, W, H, D, M, S0, Z0)
+    yd, Sd, Zd = orc.decode(q[None], k[None], v[None], S0, Z0)
+    assert np.array_equal(y, yd[0]) and np.array_equal(S1, Sd) and np.array_equal(Z1, Zd), \
+        "block-identity projection != the plain decode step"
+    dm = 7
+    x, W = rand((B, dm), 306), rand((dm, H * (2 * D + M)), 307, 0.5)
+    y, S1, Z1 = orc.decode_proj(x, W, H, D, M, S0, Z0)
+    p = x @ W
+    pq = p[:, :H * D].reshape(B, H, D)
+    pk = p[:, H * D:2 * H * D].reshape(B, H, D)
+    pv = p[:, 2 * H * D:].reshape(B, H, M)
+    fk, fq = phi_lib(pk), phi_lib(pq)
+    assert rel(S1, S0 + np.einsum("bhd,bhm->bhdm", fk, pv)) < 1e-13, "S_1 != S_0 + phi(k) v^T"
+    assert rel(Z1, Z0 + fk) < 1e-13
+    num = np.einsum("bhd,bhdm->bhm", fq, S1)
+    den = np.einsum("bhd,bhd->bh", fq, Z1)
+    assert rel(y, num / den[..., None]) < 1e-13, "y != phi(q)^T S_1 / phi(q)^T Z_1"
+
+
 ALL_PINS = [pin_phi, pin_causal_forms_agree, pin_causal_closed_forms, pin_grad_single_token, pin_noncausal_gemm,
             pin_noncausal_last_row, pin_noncausal_lengths, pin_grad_fd, pin_grad_forms_agree,
             pin_grad_invariants, pin_decode, pin_prefill, pin_decay_gamma_one, pin_decay_gamma_zero,
             pin_decay_closed_form, pin_decay_forms_agree, pin_decay_grad_fd, pin_decay_invariants,
-            pin_decay_decode]
+            pin_decay_decode, pin_decode_proj]
