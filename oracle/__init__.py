@@ -216,17 +216,18 @@ class Oracle:
         """One RNN step (eq. 16-19) whose q_t, k_t, v_t are the projections
         x_t W of the layer input (eq. 18-20 write phi(x_i W_Q), x_i W_K,
         x_i W_V); f_l and the residual of eq. 20 are not applied.  x: [B,
-        d_model]; W: [d_model, H*(2D+M)] with columns [Q of heads 0..H-1 | K of
-        heads 0..H-1 | V of heads 0..H-1]; S, Z: state (zeros if None).  The
-        projection is a plain fp64 matmul (numpy); the step is orc_decode.
-        Returns (y [B,H,M], S_1 [B,H,D,M], Z_1 [B,H,D])."""
+        d_model]; W: [d_model, H*(2D+M)] whose columns hold, head after head,
+        that head's W_Q (D columns), W_K (D) and W_V (M) side by side; S, Z:
+        state (zeros if None).  The projection is a plain fp64 matmul (numpy);
+        the step is orc_decode.  Returns (y [B,H,M], S_1 [B,H,D,M], Z_1
+        [B,H,D])."""
         x, W = _f64(x), _f64(W)
         B = x.shape[0]
         assert W.shape == (x.shape[1], H * (2 * D + M))
-        p = x @ W  # [B, H*(2D+M)]
-        q = p[:, :H * D].reshape(1, B, H, D)
-        k = p[:, H * D:2 * H * D].reshape(1, B, H, D)
-        v = p[:, 2 * H * D:].reshape(1, B, H, M)
+        p = (x @ W).reshape(B, H, 2 * D + M)  # [B, H, q | k | v]
+        q = p[:, :, :D].reshape(1, B, H, D)
+        k = p[:, :, D:2 * D].reshape(1, B, H, D)
+        v = p[:, :, 2 * D:].reshape(1, B, H, M)
         y, S1, Z1 = self.decode(q, k, v, S, Z, nthreads)
         return y[0], S1, Z1
 

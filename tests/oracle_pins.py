@@ -460,15 +460,16 @@ def pin_decay_decode(orc):
 # --------------------------------------------- decode with the projection
 
 def pin_decode_proj(orc):
-    """The projected step against things fixed outside it: with x = [q | k |
-    v] of every head side by side and W the matching block identity, it is the
-    plain decode step (orc_decode) on those q, k, v; for general W its state
-    is S_0 + phi(k) v^T with k, v from numpy's x @ W, and its output is the
-    quotient phi(q)^T S_1 / phi(q)^T Z_1 formed with numpy."""
+    """The projected step against things fixed outside it: with x = [q_h |
+    k_h | v_h] of every head h in turn and W the identity, it is the plain
+    decode step (orc_decode) on those q, k, v; for general W (columns grouped
+    per head: W_Q, W_K, W_V of head 0, then head 1, ...) its state is S_0 +
+    phi(k) v^T with k, v taken from numpy's x @ W by column slices, and its
+    output is the quotient phi(q)^T S_1 / phi(q)^T Z_1 formed with numpy."""
     B, H, D, M = 5, 3, 4, 6
     q, k, v = rand((B, H, D), 301), rand((B, H, D), 302), rand((B, H, M), 303)
     S0, Z0 = rand((B, H, D, M), 304), 2.0 * phi_lib(rand((B, H, D), 305))
-    x = np.concatenate([q.reshape(B, -1), k.reshape(B, -1), v.reshape(B, -1)], axis=1)
+    x = np.concatenate([q, k, v], axis=2).reshape(B, -1)
     W = np.eye(x.shape[1])
     y, S1, Z1 = orc.decode_proj(x, W, H, D, M, S0, Z0)
     yd, Sd, Zd = orc.decode(q[None], k[None], v[None], S0, Z0)
@@ -477,10 +478,10 @@ def pin_decode_proj(orc):
     dm = 7
     x, W = rand((B, dm), 306), rand((dm, H * (2 * D + M)), 307, 0.5)
     y, S1, Z1 = orc.decode_proj(x, W, H, D, M, S0, Z0)
-    p = x @ W
-    pq = p[:, :H * D].reshape(B, H, D)
-    pk = p[:, H * D:2 * H * D].reshape(B, H, D)
-    pv = p[:, 2 * H * D:].reshape(B, H, M)
+    p, n = x @ W, 2 * D + M
+    pq = np.stack([p[:, h * n:h * n + D] for h in range(H)], axis=1)
+    pk = np.stack([p[:, h * n + D:h * n + 2 * D] for h in range(H)], axis=1)
+    pv = np.stack([p[:, h * n + 2 * D:(h + 1) * n] for h in range(H)], axis=1)
     fk, fq = phi_lib(pk), phi_lib(pq)
     assert rel(S1, S0 + np.einsum("bhd,bhm->bhdm", fk, pv)) < 1e-13, "S_1 != S_0 + phi(k) v^T"
     assert rel(Z1, Z0 + fk) < 1e-13

@@ -69,3 +69,31 @@ def test_pins_catch_mutation(tmp_path, name, old, new, occ):
         except (AssertionError, FloatingPointError, ValueError) as e:
             failed.append(pin.__name__)
     assert failed, f"mutation {name} passed every pin"
+
+
+# Slips in the Python part of the oracle (the projection in front of the
+# decode step), planted in a copy of the method's source.
+PY_MUTATIONS = [
+    ("proj_k_and_v_swapped", "k = p[:, :, D:2 * D]", "k = p[:, :, 2 * D:3 * D]"),
+    ("proj_columns_grouped_by_kind", "p = (x @ W).reshape(B, H, 2 * D + M)",
+     "p = (x @ W).reshape(B, 2 * D + M, H).transpose(0, 2, 1)"),
+    ("proj_w_transposed", "p = (x @ W).reshape(B, H, 2 * D + M)",
+     "p = (x @ W.T.reshape(W.shape)).reshape(B, H, 2 * D + M)"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", PY_MUTATIONS, ids=[m[0] for m in PY_MUTATIONS])
+def test_pins_catch_projection_mutation(name, old, new):
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(oracle.Oracle.decode_proj))
+    assert src.count(old) == 1, f"mutation anchor not found: {old!r}"
+    ns = dict(vars(oracle))
+    exec(src.replace(old, new), ns)
+
+    class Mutated(oracle.Oracle):
+        decode_proj = ns["decode_proj"]
+
+    orc = Mutated(oracle.default().path)
+    with pytest.raises((AssertionError, ValueError)):
+        P.pin_decode_proj(orc)
