@@ -14,7 +14,8 @@ summed over ranks (independent replicas, weak scaling).  Extra objects:
                 its live CUDA-event duration, against the measured HBM copy rate
   cpu_baseline  the fp64 CPU oracle (recurrent form, fwd+bwd) on the host cores
   e2e           the same step with pinned host buffers and the copies inside
-  secondary     non-causal fwd+bwd and decode-step measurements
+  secondary     non-causal fwd+bwd, prefill, decode-step and projected
+                decode-step measurements
   clocks        nvidia-smi samples taken during the timed region
 
 `--impl reference` times the CPU oracle itself (rank 0 only) on the same
@@ -510,7 +511,41 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True):
             "timing": "CUDA graph of 64 steps, 20 replays, state kept warm"}
         if with_cpu and Bd == 256:
             res[f"decode_f32_B{Bd}"]["cpu_baseline"] = cpu_baseline_decode(Bd, Hd, Dd, Md)
+
+    # the decode step fed by its q/k/v projection (one launch: the bf16
+    # projection on the tensor cores, then the fp32 state update and read-out)
+    from kernelized_causal_attention_gb300.workloads import proj_inputs
+    for name in ("decode_proj_bf16", "decode_proj_mnist_bf16"):
+        wp = WORKLOADS[name]
+        B, H, D, M, dm = wp.B, wp.H, wp.D, wp.M, wp.d_model
+        x, W, S0, Z0 = proj_inputs(B, dm, H, D, M, t=wp.N, seed=wp.seed)
+        xd, Wd, Sd, Zd = (t.to(dev) for t in (x, W, S0, Z0))
+        y = torch.empty(B, H, M, dtype=torch.bfloat16, device=dev)
+        call = lambda: la.la_decode_step_proj(xd, Wd, Sd, Zd, y, B, H, dm, D, M, 1)
+        for _ in range(3):
+            call()
+        (mp,), _ = time_calls([call], 50, flush, torch, None, dev)
+        alg = proj_bytes(B, H, dm, D, M)
+        flops = 2 * B * dm * H * (2 * D + M)
+        gbs = alg / (mp / 1e3) / 1e9
+        res[name] = {
+            "value": round(B / (mp / 1e3), 1), "unit": "stream-steps/s", "us_per_step": round(mp * 1e3, 3),
+            "B": B, "H": H, "D": D, "M": M, "d_model": dm,
+            "launches": la.la_kernel_launches(la.LA_OP_DECODE_PROJ, B, H, dm, D, M, 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": alg,
+                         "bytes": "x, W read once; S, Z read and written once; y written"},
+            "projection_tflops": round(flops / (mp / 1e3) / 1e12, 2),
+            "timing": "CUDA events per call, L2 flushed before each (50 calls)"}
+        if with_cpu:
+            res[name]["cpu_baseline"] = cpu_baseline_decode_proj(x, W, S0, Z0, H, D, M)
     return res
+
+
+def proj_bytes(B, H, dm, D, M):
+    """Algorithmic bytes of one projected decode step: x and W (bf16) read
+    once, the fp32 state S, Z read and written once, y (bf16) written."""
+    return B * dm * 2 + dm * H * (2 * D + M) * 2 + B * H * (2 * 4 * (D * M + D) + 2 * M)
 
 
 # -------------------------------------------------------------- CPU oracle
@@ -602,6 +637,36 @@ def cpu_baseline_decode(B, H, D, M, steps=64, budget_s=5.0):
     return {"value": round(reps * steps * B * H / el, 1), "unit": "stream-steps/s",
             "cores": cores, "kind": "oracle",
             "sample": f"B={B} x H={H} streams, {reps} x {steps} steps, {el:.1f} s, fp64"}
+
+
+def cpu_baseline_decode_proj(x, W, S, Z, H, D, M, budget_s=4.0):
+    """The fp64 oracle's projected decode step (numpy x @ W, then the RNN
+    step) on all host cores, over the first n streams of the same inputs, n
+    doubled until one call takes about a second (or all streams are in),
+    repeated until about `budget_s` seconds; stream-steps per second."""
+    import oracle
+    cores = _cores(oracle)
+    B = x.shape[0]
+    n = min(B, 64)
+    while True:
+        t0 = time.perf_counter()
+        oracle.decode_proj(x[:n], W, H, D, M, S[:n], Z[:n], nthreads=cores)
+        one = time.perf_counter() - t0
+        if one >= 1.0 or n >= B:
+            break
+        n = min(B, 2 * n)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.decode_proj(x[:n], W, H, D, M, S[:n], Z[:n], nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 100:
+            break
+    return {"value": round(reps * n / el, 1), "unit": "stream-steps/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"first {n} of {B} streams (H={H}, D={D}, M={M}, d_model={x.shape[1]}) x {reps}, "
+                      f"{el:.1f} s, fp64 numpy projection + C step"}
 
 
 def run_reference(args, dist):

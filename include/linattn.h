@@ -13,8 +13,8 @@
  *
  * Conventions shared by every call
  * --------------------------------
- *  - Pointers named q, k, v, out, dout, dq, dk, dv, den, S, Z, lengths and
- *    workspace are DEVICE pointers (or managed memory) of the current CUDA
+ *  - Pointers named q, k, v, out, dout, dq, dk, dv, den, S, Z, x, W, y,
+ *    lengths and workspace are DEVICE pointers (or managed memory) of the current CUDA
  *    device.  The caller owns every buffer; the library never allocates,
  *    frees or retains memory and keeps no state between calls other than
  *    one device status word per GPU (see la_device_status).
@@ -83,6 +83,7 @@ enum { LA_F32 = 0, LA_BF16 = 1 };
 #define LA_OP_CAUSAL_PREFILL 5
 #define LA_OP_CAUSAL_FWD_DECAY 6
 #define LA_OP_CAUSAL_BWD_DECAY 7
+#define LA_OP_DECODE_PROJ 8 /* the N argument is d_model */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* la_status_string(la_status status);
@@ -229,6 +230,24 @@ la_status la_causal_bwd_decay(const void* q, const void* k, const void* v, const
 la_status la_decode_step_decay(const void* q, const void* k, const void* v, float* S, float* Z,
                                void* y, float gamma, int B, int H, int D, int M, la_dtype dtype,
                                void* stream);
+
+/*
+ * One RNN decode step fed by its own projection: "Transformers are RNNs"
+ * (part 2/3) §3.4 eq. 18-20 without the layer's f_l and residual, for B
+ * streams of H heads.  Per stream b and head h,
+ *   [q | k | v] = x_b W[:, h (2D+M) : (h+1) (2D+M)]   (q, k: D columns; v: M),
+ *   S <- S + phi(k) v^T,  Z <- Z + phi(k),  y = phi(q)^T S / phi(q)^T Z.
+ * x [B][d_model] and W [d_model][H (2D+M)] are bf16 (row-major; the columns of
+ * W hold head 0's q, k, v side by side, then head 1's, ...); y [B][H][M] is
+ * bf16; S [B][H][D][M] and Z [B][H][D] are float, updated in place.  The
+ * projection accumulates in fp32 on the tensor cores; phi and the step are
+ * fp32.  dtype must be LA_BF16 (LA_F32 gives LA_ERR_UNSUPPORTED); d_model a
+ * multiple of 64 in [64, 16384] (else LA_ERR_UNSUPPORTED when positive,
+ * LA_ERR_INVALID_ARG when not); 1 <= B*H <= 2^20, H <= 65535; D, M in {16,
+ * 32, 64}.  Needs no workspace; one kernel launch.
+ */
+la_status la_decode_step_proj(const void* x, const void* W, float* S, float* Z, void* y, int B,
+                              int H, int d_model, int D, int M, la_dtype dtype, void* stream);
 
 /*
  * Reads the status word of the current GPU after all work queued on

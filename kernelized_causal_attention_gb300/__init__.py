@@ -10,14 +10,14 @@ the built library raises.
 Raw entry points (same names and argument order as the C ABI, tensors in
 place of pointers): ``la_causal_fwd``, ``la_causal_bwd``, ``la_causal_prefill``,
 ``la_noncausal_fwd``, ``la_noncausal_bwd``, ``la_decode_step``, the decayed
-``la_causal_fwd_decay``, ``la_causal_bwd_decay``, ``la_decode_step_decay``,
-``la_workspace_bytes``, ``la_device_status``.
+``la_causal_fwd_decay``, ``la_causal_bwd_decay``, ``la_decode_step_decay``, the projected
+``la_decode_step_proj``, ``la_workspace_bytes``, ``la_device_status``.
 Convenience wrappers that allocate outputs with torch: ``causal_fwd``,
-``causal_bwd``, ``causal_prefill``, ``noncausal_fwd``, ``noncausal_bwd``, ``decode_step`` and the
+``causal_bwd``, ``causal_prefill``, ``noncausal_fwd``, ``noncausal_bwd``, ``decode_step``, ``decode_step_proj`` and the
 autograd functions ``causal_linear_attention`` / ``noncausal_linear_attention``.
 
 The method is Katharopoulos et al., "Transformers are RNNs" (part 2/3):
-eq. 7 (phi), §3.3 eq. 9-12, §3.3.1 eq. 13-15, §3.4 eq. 16-19.
+eq. 7 (phi), §3.3 eq. 9-12, §3.3.1 eq. 13-15, §3.4 eq. 16-20.
 """
 from __future__ import annotations
 
@@ -33,7 +33,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "liblinattn.so")
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
 LA_F32, LA_BF16 = 0, 1
 (LA_OP_CAUSAL_FWD, LA_OP_CAUSAL_BWD, LA_OP_NONCAUSAL_FWD, LA_OP_NONCAUSAL_BWD, LA_OP_DECODE,
- LA_OP_CAUSAL_PREFILL, LA_OP_CAUSAL_FWD_DECAY, LA_OP_CAUSAL_BWD_DECAY) = range(8)
+ LA_OP_CAUSAL_PREFILL, LA_OP_CAUSAL_FWD_DECAY, LA_OP_CAUSAL_BWD_DECAY, LA_OP_DECODE_PROJ) = range(9)
 
 # exported symbols and their ctypes signatures ("p" pointer, "i" int, "z" size_t,
 # "u" unsigned long long)
@@ -51,6 +51,7 @@ _SIGS = {
     "la_causal_fwd_decay": ("p p p p p f p z i i i i i i p", ctypes.c_int),
     "la_causal_bwd_decay": ("p p p p p p p p p f p z i i i i i i p", ctypes.c_int),
     "la_decode_step_decay": ("p p p p p p f i i i i i p", ctypes.c_int),
+    "la_decode_step_proj": ("p p p p p i i i i i i p", ctypes.c_int),
     "la_causal_fwd_noalloc": ("p p p p p i i i i i i p", ctypes.c_int),
     "la_device_status": ("p i p", ctypes.c_int),
     "la_selftest_wait": ("p u", ctypes.c_int),
@@ -201,6 +202,11 @@ def la_decode_step_decay(q, k, v, S, Z, y, gamma, B, H, D, M, dtype, stream=None
                                       H, D, M, dtype, _stream(stream)), "la_decode_step_decay")
 
 
+def la_decode_step_proj(x, W, S, Z, y, B, H, d_model, D, M, dtype, stream=None):
+    _check(lib().la_decode_step_proj(_p(x), _p(W), _p(S), _p(Z), _p(y), B, H, d_model, D, M, dtype,
+                                     _stream(stream)), "la_decode_step_proj")
+
+
 def la_causal_fwd_noalloc(q, k, v, out, den, B, H, N, D, M, dtype, stream=None):
     """la_causal_fwd with the library's built-in scratch instead of a workspace
     (for callers that may not allocate device memory)."""
@@ -346,6 +352,17 @@ def decode_step(q, k, v, S, Z, stream=None):
     dt = _dtype_code(q)
     y = torch.empty(B, H, M, dtype=q.dtype, device=q.device)
     la_decode_step(q, k, v, S, Z, y, B, H, D, M, dt, stream)
+    return y
+
+
+def decode_step_proj(x, W, S, Z, H, D, M, stream=None):
+    """One RNN step whose q, k, v are the projection x W (bf16): x [B, d_model],
+    W [d_model, H*(2D+M)] with each head's W_Q | W_K | W_V columns side by side,
+    head after head.  S [B,H,D,M] and Z [B,H,D] (float32) are updated in place.
+    Returns y [B,H,M] (bf16)."""
+    B, dm = x.shape
+    y = torch.empty(B, H, M, dtype=x.dtype, device=x.device)
+    la_decode_step_proj(x, W, S, Z, y, B, H, dm, D, M, _dtype_code(x), stream)
     return y
 
 

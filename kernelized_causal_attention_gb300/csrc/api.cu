@@ -66,6 +66,16 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
 // The RetNet decay must lie in [0, 1] (a NaN fails both comparisons).
 int check_gamma(float gamma) { return (gamma >= 0.f && gamma <= 1.f) ? LA_OK : LA_ERR_INVALID_ARG; }
 
+// The projected decode step: B*H streams as for the decode step, H grid rows,
+// d_model whole slabs of 64, bf16 only.
+int check_proj(int B, int H, int dm, int D, int M, int dtype) {
+  const int rc = check_shape(B, H, 1, D, M, dtype, 1ll << 20);
+  if (rc != LA_OK) return rc;
+  if (H > 65535 || dm < 1) return LA_ERR_INVALID_ARG;
+  if (dtype != LA_BF16 || dm % 64 != 0 || dm > 16384) return LA_ERR_UNSUPPORTED;
+  return LA_OK;
+}
+
 }  // namespace
 
 namespace la {
@@ -103,12 +113,13 @@ const char* la_status_string(int status) {
 int la_version(void) { return 200; }
 
 size_t la_workspace_bytes(int op, int B, int H, int N, int D, int M, int dtype) {
-  if (op == LA_OP_DECODE) return 0;
+  if (op == LA_OP_DECODE || op == LA_OP_DECODE_PROJ) return 0;
   if (check_shape(B, H, N, D, M, dtype) != LA_OK) return 0;
   return ws_bytes(op, Shape{B, H, N, D, M, dtype});
 }
 
 int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype) {
+  if (op == LA_OP_DECODE_PROJ) return check_proj(B, H, N, D, M, dtype) == LA_OK ? 1 : 0;
   if (check_shape(B, H, op == LA_OP_DECODE ? 1 : N, D, M, dtype,
                   op == LA_OP_DECODE ? (1ll << 20) : 65535) != LA_OK)
     return 0;
@@ -234,6 +245,14 @@ int la_decode_step_decay(const void* q, const void* k, const void* v, float* S, 
   LA_TRY(check_gamma(gamma));
   const Shape s{B, H, 1, D, M, dtype};
   return from_cuda(la::decode_step(q, k, v, S, Z, y, s, static_cast<cudaStream_t>(stream), gamma));
+}
+
+int la_decode_step_proj(const void* x, const void* W, float* S, float* Z, void* y, int B, int H,
+                        int d_model, int D, int M, int dtype, void* stream) {
+  LA_TRY(check_proj(B, H, d_model, D, M, dtype));
+  LA_TRY(check_ptrs({x, W, S, Z, y}));
+  return from_cuda(la::decode_step_proj(x, W, S, Z, y, B, H, d_model, D, M,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* y,

@@ -1,0 +1,311 @@
+// One RNN decode step fed by its own query/key/value projection, for many
+// independent streams in one launch: "Transformers are RNNs" (part 2/3) §3.4
+// eq. 18-20 without the layer's f_l and residual,
+//   [q | k | v] = x W_h  (per head h),
+//   s <- s + phi(k) v^T,  z <- z + phi(k),  y = phi(q)^T s / phi(q)^T z,
+// the batched-generation setting of §4.2.1 (thousands of images decoded at
+// once, one token per step).
+//
+// GB300 design: one CTA per (block of SB <= 64 streams, head).  The block's
+// projection is a tcgen05 product (M = 64 rows = streams, rows past the block
+// are don't-care; N = the head's 2D+M columns rounded up to whole 64-column
+// atoms; K = d_model in slabs of 64), its operands brought in by TMA through a
+// three-stage ring (x as K-major tiles, the head's contiguous columns of W as
+// MN-major atoms, both with the 128-byte swizzle) and its accumulator in
+// tensor memory.  While the product runs, every thread already has the first
+// streams' fp32 states in flight from HBM.  The CTA then applies phi, updates
+// the block's states (each read and written once, 16-byte accesses) and reads
+// y out, so q, k and v never leave the SM.
+#include "common.cuh"
+#include "launch.h"
+#include "tc.cuh"
+#include "tc_chunk.cuh"
+
+namespace la {
+namespace {
+
+using namespace tc;
+using namespace tcc;
+
+constexpr int P_NT = 256;    // threads
+constexpr int P_NW = P_NT / 32;
+constexpr int P_KS = 64;     // d_model per slab
+constexpr int P_NS = 3;      // stages of the slab ring
+constexpr int P_SBMAX = 64;  // streams per CTA at most (the MMA's M)
+
+template <int D, int M>
+struct ProjGeom {
+  static constexpr int NQKV = 2 * D + M;            // one head's q | k | v columns
+  static constexpr int NP = (NQKV + 63) / 64 * 64;  // whole 64-column atoms (the MMA's N)
+  static constexpr int NAT = NP / 64;
+  static constexpr int SQ = NQKV + 4;               // row stride of phi(q) | phi(k) | v in smem
+  static constexpr int A_BYTES = P_SBMAX * 128;     // [64 streams][64 of d_model] bf16
+  static constexpr int STAGE = A_BYTES + NAT * P_KS * 128;
+  static constexpr uint32_t TCOLS = NP <= 64 ? 64u : (NP <= 128 ? 128u : 256u);
+  static constexpr int M4 = M / 4;                  // float4 columns of a state row
+  static constexpr int RG = P_NT / M4;              // row groups of the state
+  static constexpr int RPT = (D + RG - 1) / RG;     // state rows per thread
+  // streams whose states are in flight together: about 32 KB per CTA
+  static constexpr int NSTR_RAW = 8192 / (D * M);
+  static constexpr int NSTR = NSTR_RAW < 2 ? 2 : (NSTR_RAW > 16 ? 16 : NSTR_RAW);
+};
+
+template <int D, int M>
+size_t proj_smem_bytes(int SB) {
+  using G = ProjGeom<D, M>;
+  return 1024 + static_cast<size_t>(P_NS) * G::STAGE + static_cast<size_t>(SB) * G::SQ * 4 +
+         static_cast<size_t>(G::NSTR) * P_NW * G::M4 * 16 + G::NSTR * 4;
+}
+
+__device__ __forceinline__ float comp(const float4& a, int i) {
+  return i == 0 ? a.x : (i == 1 ? a.y : (i == 2 ? a.z : a.w));
+}
+
+template <int D, int M>
+__global__ void __launch_bounds__(P_NT, 2)
+    k_decode_proj(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                  float* __restrict__ S, float* __restrict__ Z, bf16* __restrict__ y, int B, int H,
+                  int dm, int SB, int* err) {
+  using G = ProjGeom<D, M>;
+  const int b0 = blockIdx.x * SB, h = blockIdx.y;
+  const int nb = min(SB, B - b0);  // streams of this CTA
+  const int nslab = dm / P_KS;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  float* sqkv = reinterpret_cast<float*>(sm + P_NS * G::STAGE);  // [SB][SQ]
+  float4* sred = reinterpret_cast<float4*>(sqkv + SB * G::SQ);     // [NSTR][NW][M4]
+  float* sden = reinterpret_cast<float*>(sred + G::NSTR * P_NW * G::M4);
+  __shared__ uint64_t bar_full[P_NS], bar_empty[P_NS], bar_done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
+
+  if (t == 0) {
+    for (int s = 0; s < P_NS; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(&bar_done, 1);
+    fence_barrier_init();
+    s_abort = 0;
+    prefetch_tensormap(&tmX);
+    prefetch_tensormap(&tmW);
+  }
+  __syncwarp();
+  if (warp == 0) tmem_alloc(&tmem_base, G::TCOLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tacc = tmem_base;
+
+  // this thread's part of the states of streams j0 .. j0 + NSTR - 1
+  const int c4 = t % G::M4, rg = t / G::M4;
+  float4 sv[G::NSTR][G::RPT];
+  auto load_group = [&](int j0) {
+#pragma unroll
+    for (int j = 0; j < G::NSTR; ++j) {
+      if (j0 + j < nb) {
+        const float4* Sh =
+            reinterpret_cast<const float4*>(S + (static_cast<long>(b0 + j0 + j) * H + h) * (D * M));
+#pragma unroll
+        for (int r = 0; r < G::RPT; ++r) {
+          const int d = rg + r * G::RG;
+          if (d < D) sv[j][r] = Sh[d * G::M4 + c4];
+        }
+      }
+    }
+  };
+  load_group(0);  // in flight while the projection runs
+
+  // ---------------------------------- projection: [q | k | v] = x W_h (thread 0)
+  if (t == 0) {
+    const uint32_t tx = static_cast<uint32_t>(SB) * 128u + G::NAT * P_KS * 128u;
+    auto issue = [&](int ks) {
+      const int s = ks % P_NS;
+      uint8_t* A = sm + s * G::STAGE;
+      mbar_arrive_expect_tx(&bar_full[s], tx);
+      tma_load_3d(A, &tmX, &bar_full[s], ks * P_KS, b0, 0);
+#pragma unroll
+      for (int a = 0; a < G::NAT; ++a)
+        tma_load_3d(A + G::A_BYTES + a * (P_KS * 128), &tmW, &bar_full[s], h * G::NQKV + 64 * a,
+                    ks * P_KS, 0);
+    };
+    int issued = 0;
+    for (; issued < P_NS && issued < nslab; ++issued) issue(issued);
+    constexpr uint32_t ID = idesc_bf16(P_SBMAX, G::NP, false, true);
+    bool good = true;
+    for (int ks = 0; ks < nslab; ++ks) {
+      const int s = ks % P_NS;
+      if (!mbar_wait(&bar_full[s], (ks / P_NS) & 1, WAIT_NS)) {
+        fail(err, 61);
+        good = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a = smem_u32(sm + s * G::STAGE), b = a + G::A_BYTES;
+      const uint64_t dA = sdesc(a, 16, 1024), dB = sdesc(b, P_KS * 128, 1024);
+#pragma unroll
+      for (int kk = 0; kk < P_KS / 16; ++kk)
+        mma_bf16(tacc, dadd(dA, 32 * kk), dadd(dB, 2048 * kk), ID, (ks > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(&bar_empty[s]);
+      if (ks + P_NS < nslab) {  // refill the stage once its products have read it
+        if (!mbar_wait(&bar_empty[s], (ks / P_NS) & 1, WAIT_NS)) {
+          fail(err, 62);
+          good = false;
+          break;
+        }
+        issue(ks + P_NS);
+        ++issued;
+      }
+    }
+    mma_commit(&bar_done);  // every product issued so far has completed
+    if (!good) {
+      *reinterpret_cast<volatile int*>(&s_abort) = 1;
+      drain_loads<P_NS>(bar_full, issued);
+    }
+  }
+  bool done = mbar_wait(&bar_done, 0, WAIT_NS);
+  if (!done) fail(err, 63);
+  const bool ok = __syncthreads_and(done && !*reinterpret_cast<volatile int*>(&s_abort));
+  tc_fence_after();
+
+  // phi(q), phi(k) and v of the block's streams into shared memory: row r of
+  // the M = 64 accumulator sits in TMEM lane 32 (r / 16) + r % 16
+  if (ok && warp < 4) {
+    const uint32_t lq = static_cast<uint32_t>(32 * warp) << 16;
+    const int r = 16 * warp + lane;
+    const bool mine = lane < 16 && r < nb;
+#pragma unroll
+    for (int c0 = 0; c0 < G::NQKV; c0 += 16) {
+      float f[16];
+      tmem_ldn<1>(tacc + lq + c0, f);
+      if (mine) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const bool fm = c0 + i < 2 * D;  // q and k columns take the feature map
+          float4 o;
+          o.x = fm ? phi(f[i]) : f[i];
+          o.y = fm ? phi(f[i + 1]) : f[i + 1];
+          o.z = fm ? phi(f[i + 2]) : f[i + 2];
+          o.w = fm ? phi(f[i + 3]) : f[i + 3];
+          *reinterpret_cast<float4*>(sqkv + r * G::SQ + c0 + i) = o;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // ------------------------------------------- state update and read-out
+  for (int j0 = 0; ok && j0 < nb; j0 += G::NSTR) {
+#pragma unroll
+    for (int j = 0; j < G::NSTR; ++j) {
+      if (j0 + j < nb) {
+        const float* qkv = sqkv + (j0 + j) * G::SQ;
+        const float4 v4 = *reinterpret_cast<const float4*>(qkv + 2 * D + 4 * c4);
+        float4* Sh = reinterpret_cast<float4*>(S + (static_cast<long>(b0 + j0 + j) * H + h) * (D * M));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < G::RPT; ++r) {
+          const int d = rg + r * G::RG;
+          if (d < D) {
+            const float fk = qkv[D + d], fq = qkv[d];
+            float4 s4 = sv[j][r];
+            s4.x = fmaf(fk, v4.x, s4.x);
+            s4.y = fmaf(fk, v4.y, s4.y);
+            s4.z = fmaf(fk, v4.z, s4.z);
+            s4.w = fmaf(fk, v4.w, s4.w);
+            Sh[d * G::M4 + c4] = s4;
+            acc.x = fmaf(fq, s4.x, acc.x);
+            acc.y = fmaf(fq, s4.y, acc.y);
+            acc.z = fmaf(fq, s4.z, acc.z);
+            acc.w = fmaf(fq, s4.w, acc.w);
+          }
+        }
+        // sum over the lanes of this warp that hold the same columns
+#pragma unroll
+        for (int off = 16; off >= G::M4; off >>= 1) {
+          acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+          acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+          acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+          acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+        }
+        if (lane < G::M4) sred[(j * P_NW + warp) * G::M4 + lane] = acc;
+      }
+    }
+    // z <- z + phi(k) and den = phi(q) . z, one warp per stream
+    for (int j = warp; j < G::NSTR; j += P_NW) {
+      if (j0 + j < nb) {
+        const float* qkv = sqkv + (j0 + j) * G::SQ;
+        float* Zh = Z + (static_cast<long>(b0 + j0 + j) * H + h) * D;
+        float dp = 0.f;
+        for (int d = lane; d < D; d += 32) {
+          const float z = Zh[d] + qkv[D + d];
+          Zh[d] = z;
+          dp = fmaf(qkv[d], z, dp);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, off);
+        if (lane == 0) sden[j] = dp;
+      }
+    }
+    if (j0 + G::NSTR < nb) load_group(j0 + G::NSTR);  // the next streams' states, in flight
+    __syncthreads();
+    for (int i = t; i < G::NSTR * M; i += P_NT) {
+      const int j = i / M, m = i % M;
+      if (j0 + j < nb) {
+        float num = 0.f;
+#pragma unroll
+        for (int w = 0; w < P_NW; ++w) num += comp(sred[(j * P_NW + w) * G::M4 + m / 4], m & 3);
+        y[(static_cast<long>(b0 + j0 + j) * H + h) * M + m] = __float2bfloat16_rn(num / sden[j]);
+      }
+    }
+    __syncthreads();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tacc, G::TCOLS);
+}
+
+}  // namespace
+
+// Streams per CTA: the largest block that still gives two CTAs per SM.
+int decode_proj_block(int B, int H) {
+  const long want = 2l * sm_count();
+  for (int sb : {64, 32, 16})
+    if (static_cast<long>((B + sb - 1) / sb) * H >= want) return sb;
+  return 8;
+}
+
+namespace {
+
+template <int D, int M>
+cudaError_t launch_proj(const CUtensorMap& mx, const CUtensorMap& mw, float* S, float* Z, void* y,
+                        int B, int H, int dm, int SB, cudaStream_t st) {
+  const size_t smem = proj_smem_bytes<D, M>(SB);
+  cudaError_t e = cudaFuncSetAttribute(k_decode_proj<D, M>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k_decode_proj<D, M><<<dim3((B + SB - 1) / SB, H), P_NT, smem, st>>>(
+      mx, mw, S, Z, static_cast<bf16*>(y), B, H, dm, SB, status_word());
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t decode_step_proj(const void* x, const void* W, float* S, float* Z, void* y, int B,
+                             int H, int dm, int D, int M, cudaStream_t st) {
+  const int SB = decode_proj_block(B, H);
+  const long wcols = static_cast<long>(H) * (2 * D + M);
+  CUtensorMap mx, mw;
+  if (!make_bf16_map_2d(&mx, x, dm, B, SB) || !make_bf16_map_2d(&mw, W, wcols, dm, P_KS))
+    return cudaErrorInvalidValue;
+  LA_DISPATCH_DM(D, M, return (launch_proj<D_, M_>(mx, mw, S, Z, y, B, H, dm, SB, st)));
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace la

@@ -122,6 +122,11 @@ cudaError_t noncausal_tc_bwd(const void* q, const void* k, const void* v, const 
 // gamma: the RetNet decay (1 = the undecayed step).
 cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* y,
                         const Shape& s, cudaStream_t st, float gamma = 1.f);
+// The decode step fed by its projection (decode_proj.cu): x [B][dm] and W
+// [dm][H (2D+M)] in bf16, d_model dm a multiple of 64; streams per CTA.
+cudaError_t decode_step_proj(const void* x, const void* W, float* S, float* Z, void* y, int B,
+                             int H, int dm, int D, int M, cudaStream_t st);
+int decode_proj_block(int B, int H);
 
 }  // namespace la
 

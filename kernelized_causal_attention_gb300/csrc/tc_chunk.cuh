@@ -445,4 +445,8 @@ cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t sme
 // 128-byte swizzle (defined in causal_tc.cu).
 bool make_bf16_map(CUtensorMap* m, const void* base, int BH, int N);
 
+// [rows][cols] row-major bf16 as a 3-D TMA tensor with 64 x box_rows x 1 boxes
+// and the 128-byte swizzle (defined in causal_tc.cu).
+bool make_bf16_map_2d(CUtensorMap* m, const void* base, long cols, long rows, int box_rows);
+
 }  // namespace la
