@@ -190,6 +190,18 @@ def causal_bytes(B, H, N, D, M, elt):
 
 # ------------------------------------------------------------------ our arm
 
+LEAD_CYCLES = 200_000  # about 100 us of GPU idle after each flush, untimed
+
+
+def lead(torch):
+    """Keeps the GPU busy (untimed) for about 100 us after the L2 flush, so
+    that the host has enqueued the whole step before the step's first event
+    is reached: the device time then excludes host-side launch overhead (that
+    overhead is part of the e2e figure instead)."""
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(LEAD_CYCLES)
+
+
 def time_calls(fns, steps, flush, torch, dist, dev, with_median=False):
     """Runs `steps` iterations of the call sequence `fns`, with an L2 flush
     before each; returns per-call mean ms and per-step mean ms (device time),
@@ -198,6 +210,7 @@ def time_calls(fns, steps, flush, torch, dist, dev, with_median=False):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
     for i in range(steps):
         flush()
+        lead(torch)
         ev[i][0].record()
         for j, fn in enumerate(fns):
             fn()
@@ -288,7 +301,8 @@ def run_ours(args, dist):
            "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "M": M,
                       "in_dtype": "bf16", "accumulate": "fp32", "global_batch": B * dist.world,
                       "seq_len": N, "parallelism": f"replicas{dist.world}",
-                      "l2": "flushed before every timed step (256 MiB write, untimed)"},
+                      "l2": "flushed before every timed step (256 MiB write, untimed)",
+                      "enqueue": "GPU idles ~100 us after each flush (untimed) so the host enqueues the step ahead"},
            "roofline": roofline, "step_roofline": step_roof, "e2e": e2e,
            "gpu_launches": launches, "clocks": clk, "wall_s_timed_region": round(wall, 3),
            "median_ms_per_step": round(dist.max(ms_median, dev), 5),

@@ -45,16 +45,40 @@ struct ProjGeom {
   static constexpr int M4 = M / 4;                  // float4 columns of a state row
   static constexpr int RG = P_NT / M4;              // row groups of the state
   static constexpr int RPT = (D + RG - 1) / RG;     // state rows per thread
-  // streams whose states are in flight together: about 32 KB per CTA
-  static constexpr int NSTR_RAW = 8192 / (D * M);
-  static constexpr int NSTR = NSTR_RAW < 2 ? 2 : (NSTR_RAW > 16 ? 16 : NSTR_RAW);
+  // the states stream through a ring of NG groups of NSTR streams (about
+  // 16 KB a group) in the projection's stages, free once the product is done
+  static constexpr int NSTR = D * M >= 4096 ? 1 : 4096 / (D * M);
+  static constexpr int GROUP = NSTR * D * M * 4;
+  static constexpr int NG_RAW = P_NS * STAGE / GROUP;
+  static constexpr int NG = NG_RAW > 8 ? 8 : NG_RAW;
+  static_assert(NG >= 2, "the ring needs two groups");
 };
 
 template <int D, int M>
 size_t proj_smem_bytes(int SB) {
   using G = ProjGeom<D, M>;
   return 1024 + static_cast<size_t>(P_NS) * G::STAGE + static_cast<size_t>(SB) * G::SQ * 4 +
-         static_cast<size_t>(G::NSTR) * P_NW * G::M4 * 16 + G::NSTR * 4;
+         static_cast<size_t>(G::NSTR) * P_NW * G::M4 * 16 + static_cast<size_t>(G::NG) * G::NSTR * D * 4 +
+         G::NSTR * 4;
+}
+
+// phi(x) = elu(x) + 1 (eq. 7) with the exponential evaluated on both sides
+// of the select, so that a run of these has no branch: the same value as
+// phi() in every case.
+__device__ __forceinline__ float phi_select(float x) {
+  const float e = expf(fminf(x, 0.f));
+  return x > 0.f ? x + 1.f : e;
+}
+
+// 16-byte asynchronous copy global -> shared (bypassing L1), and its groups.
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ float comp(const float4& a, int i) {
@@ -74,7 +98,9 @@ __global__ void __launch_bounds__(P_NT, 2)
   uint8_t* sm = align1024(smraw);
   float* sqkv = reinterpret_cast<float*>(sm + P_NS * G::STAGE);  // [SB][SQ]
   float4* sred = reinterpret_cast<float4*>(sqkv + SB * G::SQ);     // [NSTR][NW][M4]
-  float* sden = reinterpret_cast<float*>(sred + G::NSTR * P_NW * G::M4);
+  float4* zring = sred + G::NSTR * P_NW * G::M4;                   // [NG][NSTR][D/4]
+  float* sden = reinterpret_cast<float*>(zring + G::NG * G::NSTR * (D / 4));  // [NSTR]
+  float4* ring = reinterpret_cast<float4*>(sm);                    // [NG][NSTR][D*M/4]
   __shared__ uint64_t bar_full[P_NS], bar_empty[P_NS], bar_done;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
@@ -98,26 +124,9 @@ __global__ void __launch_bounds__(P_NT, 2)
   tc_fence_after();
   const uint32_t tacc = tmem_base;
 
-  // this thread's part of the states of streams j0 .. j0 + NSTR - 1
-  const int c4 = t % G::M4, rg = t / G::M4;
-  float4 sv[G::NSTR][G::RPT];
-  auto load_group = [&](int j0) {
-#pragma unroll
-    for (int j = 0; j < G::NSTR; ++j) {
-      if (j0 + j < nb) {
-        const float4* Sh =
-            reinterpret_cast<const float4*>(S + (static_cast<long>(b0 + j0 + j) * H + h) * (D * M));
-#pragma unroll
-        for (int r = 0; r < G::RPT; ++r) {
-          const int d = rg + r * G::RG;
-          if (d < D) sv[j][r] = Sh[d * G::M4 + c4];
-        }
-      }
-    }
-  };
-  load_group(0);  // in flight while the projection runs
-
-  // ---------------------------------- projection: [q | k | v] = x W_h (thread 0)
+  // ------------------------- projection: [q | k | v] = x W_h (lane 0 of warp 0)
+  // The other lanes of warp 0 wait for it at __syncwarp, not on an mbarrier:
+  // a sibling path suspended in try_wait could hold back the issuing lane.
   if (t == 0) {
     const uint32_t tx = static_cast<uint32_t>(SB) * 128u + G::NAT * P_KS * 128u;
     auto issue = [&](int ks) {
@@ -164,13 +173,15 @@ __global__ void __launch_bounds__(P_NT, 2)
       drain_loads<P_NS>(bar_full, issued);
     }
   }
+  __syncwarp();
   bool done = mbar_wait(&bar_done, 0, WAIT_NS);
   if (!done) fail(err, 63);
   const bool ok = __syncthreads_and(done && !*reinterpret_cast<volatile int*>(&s_abort));
   tc_fence_after();
 
-  // phi(q), phi(k) and v of the block's streams into shared memory: row r of
-  // the M = 64 accumulator sits in TMEM lane 32 (r / 16) + r % 16
+  // q, k and v of the block's streams into shared memory (row r of the M = 64
+  // accumulator sits in TMEM lane 32 (r / 16) + r % 16), then phi over the q
+  // and k columns by all threads, element by element
   if (ok && warp < 4) {
     const uint32_t lq = static_cast<uint32_t>(32 * warp) << 16;
     const int r = 16 * warp + lane;
@@ -181,37 +192,67 @@ __global__ void __launch_bounds__(P_NT, 2)
       tmem_ldn<1>(tacc + lq + c0, f);
       if (mine) {
 #pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-          const bool fm = c0 + i < 2 * D;  // q and k columns take the feature map
-          float4 o;
-          o.x = fm ? phi(f[i]) : f[i];
-          o.y = fm ? phi(f[i + 1]) : f[i + 1];
-          o.z = fm ? phi(f[i + 2]) : f[i + 2];
-          o.w = fm ? phi(f[i + 3]) : f[i + 3];
-          *reinterpret_cast<float4*>(sqkv + r * G::SQ + c0 + i) = o;
-        }
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(sqkv + r * G::SQ + c0 + i) =
+              make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]);
       }
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  for (int e = t; ok && e < nb * 2 * D; e += P_NT) {
+    float* p = sqkv + (e / (2 * D)) * G::SQ + e % (2 * D);
+    *p = phi_select(*p);
+  }
+  __syncthreads();
 
   // ------------------------------------------- state update and read-out
-  for (int j0 = 0; ok && j0 < nb; j0 += G::NSTR) {
+  // Thread t owns float4 column c4 of state rows rg, rg + RG, ... of every
+  // stream, and warp j % NW lanes 0 .. D/4-1 own stream j's z (j within a
+  // group): each thread copies its own pieces into the ring with 16-byte
+  // cp.async and reads back only those, so a wait_group is all it needs.
+  const int c4 = t % G::M4, rg = t / G::M4;
+  const int ngroups = (nb + G::NSTR - 1) / G::NSTR;
+  auto issue = [&](int g) {
+    if (g < ngroups) {
+      float4* slot = ring + (g % G::NG) * (G::NSTR * D * M / 4);
+      float4* zslot = zring + (g % G::NG) * (G::NSTR * D / 4);
+#pragma unroll
+      for (int j = 0; j < G::NSTR; ++j) {
+        const int js = g * G::NSTR + j;
+        if (js < nb) {
+          const long sh = static_cast<long>(b0 + js) * H + h;
+          const float4* Sh = reinterpret_cast<const float4*>(S) + sh * (D * M / 4);
+#pragma unroll
+          for (int r = 0; r < G::RPT; ++r) {
+            const int d = rg + r * G::RG;
+            if (d < D) cp_async16(slot + j * (D * M / 4) + d * G::M4 + c4, Sh + d * G::M4 + c4);
+          }
+          if (warp == j % P_NW && lane < D / 4)
+            cp_async16(zslot + j * (D / 4) + lane, reinterpret_cast<const float4*>(Z) + sh * (D / 4) + lane);
+        }
+      }
+    }
+    cp_async_commit();  // one group per call, empty or not, to keep the count
+  };
+  auto process = [&](int g) {
+    const float4* slot = ring + (g % G::NG) * (G::NSTR * D * M / 4);
+    const float4* zslot = zring + (g % G::NG) * (G::NSTR * D / 4);
+    const int j0 = g * G::NSTR;
 #pragma unroll
     for (int j = 0; j < G::NSTR; ++j) {
       if (j0 + j < nb) {
         const float* qkv = sqkv + (j0 + j) * G::SQ;
         const float4 v4 = *reinterpret_cast<const float4*>(qkv + 2 * D + 4 * c4);
-        float4* Sh = reinterpret_cast<float4*>(S + (static_cast<long>(b0 + j0 + j) * H + h) * (D * M));
+        float4* Sh = reinterpret_cast<float4*>(S) + (static_cast<long>(b0 + j0 + j) * H + h) * (D * M / 4);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int r = 0; r < G::RPT; ++r) {
           const int d = rg + r * G::RG;
           if (d < D) {
             const float fk = qkv[D + d], fq = qkv[d];
-            float4 s4 = sv[j][r];
+            float4 s4 = slot[j * (D * M / 4) + d * G::M4 + c4];
             s4.x = fmaf(fk, v4.x, s4.x);
             s4.y = fmaf(fk, v4.y, s4.y);
             s4.z = fmaf(fk, v4.z, s4.z);
@@ -234,23 +275,23 @@ __global__ void __launch_bounds__(P_NT, 2)
         if (lane < G::M4) sred[(j * P_NW + warp) * G::M4 + lane] = acc;
       }
     }
-    // z <- z + phi(k) and den = phi(q) . z, one warp per stream
+    // z <- z + phi(k) and den = phi(q) . z: warp j % NW, four entries a lane
     for (int j = warp; j < G::NSTR; j += P_NW) {
       if (j0 + j < nb) {
-        const float* qkv = sqkv + (j0 + j) * G::SQ;
-        float* Zh = Z + (static_cast<long>(b0 + j0 + j) * H + h) * D;
         float dp = 0.f;
-        for (int d = lane; d < D; d += 32) {
-          const float z = Zh[d] + qkv[D + d];
-          Zh[d] = z;
-          dp = fmaf(qkv[d], z, dp);
+        if (lane < D / 4) {
+          const float* qkv = sqkv + (j0 + j) * G::SQ + 4 * lane;
+          const float4 z0 = zslot[j * (D / 4) + lane];
+          const float4 z = make_float4(z0.x + qkv[D], z0.y + qkv[D + 1], z0.z + qkv[D + 2],
+                                       z0.w + qkv[D + 3]);
+          reinterpret_cast<float4*>(Z)[(static_cast<long>(b0 + j0 + j) * H + h) * (D / 4) + lane] = z;
+          dp = qkv[0] * z.x + qkv[1] * z.y + qkv[2] * z.z + qkv[3] * z.w;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, off);
         if (lane == 0) sden[j] = dp;
       }
     }
-    if (j0 + G::NSTR < nb) load_group(j0 + G::NSTR);  // the next streams' states, in flight
     __syncthreads();
     for (int i = t; i < G::NSTR * M; i += P_NT) {
       const int j = i / M, m = i % M;
@@ -262,6 +303,15 @@ __global__ void __launch_bounds__(P_NT, 2)
       }
     }
     __syncthreads();
+  };
+  if (ok) {
+    fence_proxy_async();  // the ring reuses stages last touched by TMA and the tensor cores
+    for (int g = 0; g < G::NG - 1; ++g) issue(g);
+    for (int g = 0; g < ngroups; ++g) {
+      issue(g + G::NG - 1);  // into the slot that group g - 1 has left
+      cp_async_wait<G::NG - 1>();
+      process(g);
+    }
   }
 
   tc_fence_before();
