@@ -139,6 +139,83 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": n}
 
 
+class NvmlClocks:
+    """SM clock and clock-event reasons read through NVML (read-only queries,
+    ctypes on the driver's libnvidia-ml), one sample per call of sample():
+    time_calls takes one per timed step, right after the step's L2 flush is
+    enqueued, so the samples cover the timed region at any step count."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch, dev):
+        import ctypes
+        self.ok, self.sm, self.reasons = False, [], 0
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            bus = getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None)
+            dom = getattr(torch.cuda.get_device_properties(dev), "pci_domain_id", 0)
+            dv = getattr(torch.cuda.get_device_properties(dev), "pci_device_id", 0)
+            rc = 1
+            if bus is not None:
+                rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(
+                    f"{dom:08x}:{bus:02x}:{dv:02x}.0".encode(), ctypes.byref(self.h))
+            if rc != 0:
+                rc = self.lib.nvmlDeviceGetHandleByIndex_v2(dev.index or 0, ctypes.byref(self.h))
+            if rc != 0:
+                return
+            self.ct = ctypes
+            self.val = ctypes.c_uint()
+            self.rs = ctypes.c_ulonglong()
+            self.max_mhz = None
+            if self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(self.val)) == 0:
+                self.max_mhz = float(self.val.value)
+            self.get_reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def sample(self):
+        if not self.ok:
+            return
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(self.val)) == 0:
+            self.sm.append(float(self.val.value))
+        if self.get_reasons(self.h, self.ct.byref(self.rs)) == 0:
+            self.reasons |= int(self.rs.value)
+
+    def summary(self, ms_per_step):
+        if not self.ok or not self.sm:
+            return None
+        med = statistics.median(self.sm)
+        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASONS.items() if self.reasons & b),
+                "samples": len(self.sm), "sm_mhz_min": min(self.sm),
+                "source": "NVML, one sample per timed step",
+                "ms_x_mhz": round(ms_per_step * med, 3)}
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip() + f" ({platform.machine()})"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -202,7 +279,7 @@ def lead(torch):
         torch.cuda._sleep(LEAD_CYCLES)
 
 
-def time_calls(fns, steps, flush, torch, dist, dev, with_median=False):
+def time_calls(fns, steps, flush, torch, dist, dev, with_median=False, sample=None):
     """Runs `steps` iterations of the call sequence `fns`, with an L2 flush
     before each; returns per-call mean ms and per-step mean ms (device time),
     and with_median the per-step median ms as well."""
@@ -210,6 +287,8 @@ def time_calls(fns, steps, flush, torch, dist, dev, with_median=False):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
     for i in range(steps):
         flush()
+        if sample is not None:
+            sample()  # the GPU is busy with the flush meanwhile
         lead(torch)
         ev[i][0].record()
         for j, fn in enumerate(fns):
@@ -256,17 +335,20 @@ def run_ours(args, dist):
         bwd()
     torch.cuda.synchronize()
 
+    nv = NvmlClocks(torch, dev)
     clocks = ClockSampler(dist.local)
     clocks.start()
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     (ms_fwd, ms_bwd), ms_step, ms_median = time_calls([fwd, bwd], args.steps, flush, torch, dist,
-                                                      dev, with_median=True)
+                                                      dev, with_median=True, sample=nv.sample)
     torch.cuda.synchronize()
     dist.barrier()
     wall = time.perf_counter() - t0
-    clk = clocks.stop()
+    smi = clocks.stop()
+    clk = nv.summary(ms_step) or dict(smi)
+    clk["nvidia_smi"] = smi  # 100 ms samples over the same window (few or none for short runs)
     # the same step with L2 left warm (inputs partly resident), outside the timed region
     _, ms_warm = time_calls([fwd, bwd], 200, lambda: None, torch, dist, dev)
 
@@ -415,12 +497,43 @@ def measure_e2e(la, torch, dev, q, k, v, g, out, den, wsf, wsb, B, H, N, D, M, d
 
 
 def secondary(la, torch, dev, flush, peaks, with_cpu=True):
-    """Non-causal fwd+bwd (long speech-like sequences with padding), the
-    prefill (causal forward from a state), and the decode step (256 and 2048
-    streams x 8 heads), each against its roofline, and (with_cpu) the fp64
-    oracle timed beside each on the host cores."""
-    from kernelized_causal_attention_gb300.workloads import WORKLOADS, noncausal_inputs
+    """The 784-token causal fwd+bwd, non-causal fwd+bwd (long speech-like
+    sequences with padding), the prefill (causal forward from a state), the
+    decode step (256 and 2048 streams x 8 heads), the projected decode step
+    (256 and 10,000 streams), each against its roofline, and (with_cpu) the
+    fp64 oracle timed beside each on the host cores; then a short
+    sequence-length sweep."""
+    from kernelized_causal_attention_gb300.workloads import WORKLOADS, causal_inputs, noncausal_inputs
     res = {}
+    # the 784-token (28 x 28) image workload: causal fwd + bwd
+    wm = WORKLOADS["causal_mnist_bf16"]
+    B, H, N, D, M = wm.B, wm.H, wm.N, wm.D, wm.M
+    q, k, v, g = causal_inputs(B, H, N, D, M, wm.dtype, wm.seed)
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+    out = torch.empty_like(vd)
+    den = torch.empty(B, H, N, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    wf = la.workspace(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, 1, dev)
+    wb = la.workspace(la.LA_OP_CAUSAL_BWD, B, H, N, D, M, 1, dev)
+    fwd = lambda: la.la_causal_fwd(qd, kd, vd, out, den, wf, B, H, N, D, M, 1)
+    bwd = lambda: la.la_causal_bwd(qd, kd, vd, out, den, gd, dq, dk, dv, wb, B, H, N, D, M, 1)
+    for _ in range(3):
+        fwd()
+        bwd()
+    (mf, mb), ms = time_calls([fwd, bwd], 100, flush, torch, None, dev)
+    fb, bb = causal_bytes(B, H, N, D, M, 2)
+    gbs = (fb + bb) / (ms / 1e3) / 1e9
+    res["causal_mnist_bf16"] = {
+        "value": round(B * N / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+        "fwd_ms": round(mf, 5), "bwd_ms": round(mb, 5), "B": B, "H": H, "N": N, "D": D, "M": M,
+        "launches": la.la_kernel_launches(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, 1)
+        + la.la_kernel_launches(la.LA_OP_CAUSAL_BWD, B, H, N, D, M, 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": fb + bb,
+                     "bytes_per_token_head": (fb + bb) // (B * H * N)},
+        "timing": "CUDA events, L2 flushed before each step (100 steps)"}
+    if with_cpu:
+        res["causal_mnist_bf16"]["cpu_baseline"] = cpu_baseline(q, k, v, g, B, H, N, budget_s=5.0)
     w = WORKLOADS["noncausal_speech_f32"]
     B, H, N, D, M = w.B, w.H, w.N, w.D, w.M
     lengths, q, k, v, g = noncausal_inputs(B, H, N, D, M, w.dtype, w.seed, w.len_range)
@@ -553,6 +666,16 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True):
             "timing": "CUDA events per call, L2 flushed before each (50 calls)"}
         if with_cpu:
             res[name]["cpu_baseline"] = cpu_baseline_decode_proj(x, W, S0, Z0, H, D, M)
+
+    # a short sequence-length sweep (the full one is --sweep)
+    res["sweep_causal_bf16"] = {
+        "what": "causal fwd+bwd, B * N = 2^16, H = 8, D = M = 64, bf16, 10 L2-flushed steps a point",
+        "points": sweep_points(la, torch, dev, flush, peaks, [1 << 10, 1 << 12, 1 << 14, 1 << 16], 10)}
+    if with_cpu:
+        model = cpu_model()
+        for v in res.values():
+            if isinstance(v, dict) and "cpu_baseline" in v:
+                v["cpu_baseline"].setdefault("cpu_model", model)
     return res
 
 
@@ -582,10 +705,20 @@ def cpu_baseline(q, k, v, g, B, H, N, budget_s=12.0):
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= 200:
             break
+    # one core: the first (b, h) sequence alone, fwd then bwd; a token needs all H heads
+    q1, k1, v1, g1 = (t[:1, :1] for t in (q, k, v, g))
+    t1 = time.perf_counter()
+    oracle.causal_fwd(q1, k1, v1, "recurrent", nthreads=1)
+    oracle.causal_bwd(q1, k1, v1, g1, "recurrent", nthreads=1)
+    t1 = time.perf_counter() - t1
     return {"value": round(reps * B * N / el, 1), "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
             "sample": f"full workload (B={B}, H={H}, N={N}) x {reps} repetitions, "
-                      f"{el:.1f} s, fp64 recurrent form, fwd+bwd"}
+                      f"{el:.1f} s, fp64 recurrent form, fwd+bwd",
+            "cpu_model": cpu_model(),
+            "single_core": {"value": round(N / (H * t1), 1), "unit": "tokens/s",
+                            "sample": f"one (b, h) sequence of N={N}, fwd+bwd, {t1:.2f} s, "
+                                      f"scaled by 1/H"}}
 
 
 def cpu_baseline_noncausal(q, k, v, g, lengths, budget_s=5.0):
@@ -740,35 +873,25 @@ def run_secondary_only():
                                    with_cpu=False)}
 
 
-def run_sweep(steps=20):
-    """Causal attention and its gradients (la_causal_fwd + la_causal_bwd) for
-    N = 2^9 .. 2^16 with the batch inversely proportional to N (B * N = 2^16),
+def sweep_points(la, torch, dev, flush, peaks, Ns, steps, total=1 << 16):
+    """Causal attention and its gradients (la_causal_fwd + la_causal_bwd) at
+    each N in Ns with the batch inversely proportional to N (B * N = total),
     H = 8, D = M = 64, bf16 inputs: time and peak allocated device memory per
-    sample, the shape of the pages' memory/computation benchmark.  Peak memory
-    is torch's allocator high-water mark over the inputs, outputs, gradients
-    and workspaces (the library allocates nothing itself); time is the mean of
-    `steps` L2-flushed fwd+bwd pairs on CUDA events."""
-    import torch
-
-    import kernelized_causal_attention_gb300 as la
+    sample, the shape of the pages' memory/computation benchmark (§4.1,
+    Fig. 1).  Peak memory is torch's allocator high-water mark over the
+    inputs, outputs, gradients and workspaces (the library allocates nothing
+    itself); time is the mean of `steps` L2-flushed fwd+bwd pairs on CUDA
+    events."""
     from kernelized_causal_attention_gb300.workloads import causal_inputs
-
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    la.lib()
-    peaks = measured_peaks()
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush = lambda: flush_buf.zero_()
-    H, D, M, total = 8, 64, 64, 1 << 16
+    H, D, M = 8, 64, 64
     points = []
-    for e in range(9, 17):
-        N = 1 << e
-        B = total // N
+    for N in Ns:
+        B = max(1, total // N)
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         torch.cuda.reset_peak_memory_stats(dev)
         base = torch.cuda.memory_allocated(dev)
-        q, k, v, g = (t.to(dev) for t in causal_inputs(B, H, N, D, M, "bf16", 900 + e))
+        q, k, v, g = (t.to(dev) for t in causal_inputs(B, H, N, D, M, "bf16", 900 + N.bit_length()))
         out = torch.empty_like(v)
         den = torch.empty(B, H, N, device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -781,7 +904,7 @@ def run_sweep(steps=20):
             bwd()
         (mf, mb), ms = time_calls([fwd, bwd], steps, flush, torch, None, dev)
         peak = torch.cuda.max_memory_allocated(dev) - base
-        alg = B * H * N * (2 * (2 * D + M) + 2 * M + 4 + 5 * 2 * 64 + 4 + 3 * 2 * 64)
+        alg = sum(causal_bytes(B, H, N, D, M, 2))
         gbs = alg / (ms / 1e3) / 1e9
         points.append({"N": N, "B": B, "ms_fwd_bwd": round(ms, 5), "fwd_ms": round(mf, 5),
                        "bwd_ms": round(mb, 5), "ms_per_sample": round(ms / B, 6),
@@ -789,6 +912,21 @@ def run_sweep(steps=20):
                        "tokens_per_s": round(B * N / (ms / 1e3), 1),
                        "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)})
         del q, k, v, g, out, den, dq, dk, dv, wf, wb
+    return points
+
+
+def run_sweep(steps=20):
+    """The full sweep N = 2^9 .. 2^16 (B * N = 2^16) on cuda:0."""
+    import torch
+
+    import kernelized_causal_attention_gb300 as la
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    la.lib()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    points = sweep_points(la, torch, dev, lambda: flush_buf.zero_(), measured_peaks(),
+                          [1 << e for e in range(9, 17)], steps)
     la.check_device_status()
     return {"sweep": "causal fwd+bwd, N = 2^9 .. 2^16, B * N = 2^16, H = 8, D = M = 64, bf16",
             "data": "synthetic", "l2": "flushed before every timed pair", "points": points}

@@ -14,10 +14,7 @@ from kernelized_causal_attention_gb300.workloads import WORKLOADS, DecodeStream,
 TOL = {"f32": 1e-4, "bf16": 2e-2}
 
 
-def rel_err(gpu, ref):
-    g = gpu.detach().double().cpu().numpy()
-    assert np.all(np.isfinite(g)), "non-finite values in the GPU result"
-    return float(np.max(np.abs(g - ref)) / max(np.max(np.abs(ref)), 1e-30))
+from errstats import rel_err  # noqa: E402  (normwise; records the elementwise figure)
 
 
 def check_decay(la, dev, B, H, N, D, M, dtype, gamma, seed):

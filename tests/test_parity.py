@@ -19,12 +19,7 @@ pytestmark = pytest.mark.gpu
 TOL = {"f32": 1e-4, "bf16": 2e-2}
 
 
-def rel_err(gpu, ref):
-    g = gpu.detach().double().cpu().numpy() if isinstance(gpu, torch.Tensor) else gpu
-    ref = np.asarray(ref)
-    assert g.shape == ref.shape
-    assert np.all(np.isfinite(g)), "non-finite values in the GPU result"
-    return float(np.max(np.abs(g - ref)) / max(np.max(np.abs(ref)), 1e-30))
+from errstats import rel_err  # noqa: E402  (normwise; records the elementwise figure)
 
 
 def _to(dev, *ts):
