@@ -96,6 +96,12 @@ struct Lay {
   static constexpr int O_MISC = O_ST + N_ST;  // fp32: per-row [2][128] x 2, vector [64], sums [warps][64], [4][128]
   static constexpr int O_BAR = O_MISC + 4 * N_MISC;  // mbarriers: MMA done per buffer, final drain; TMEM address
   static constexpr int SMEM = O_BAR + 64 + 1024;     // + alignment slack
+  // The state form reaches a term pair's second tile through the descriptor's
+  // leading offset t[1] - t[0], taken unsigned: every second tile must lie
+  // above its first (X: consecutive tiles; Y: in-buffer for two terms, the
+  // shared pair above both buffers' Y_0 for three), so that no MMA reads a
+  // tile this launch has not written.
+  static_assert(NT == 2 || O_SHY > 1 * BUF + 3 * BT, "Y's shared terms must lie above every Y_0");
 };
 static_assert(Lay<3>::SMEM + 16 + 1024 <= 196 * 1024, "the three-term layout fits the 196 KB carveout");
 static_assert(Lay<2>::SMEM + 16 + 1024 <= 164 * 1024, "the two-term layout fits the 164 KB carveout");
