@@ -55,8 +55,10 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true", help="skip the non-causal/decode lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--secondary-only", action="store_true",
-                    help="run only the non-causal/decode measurements (one JSON object); for "
-                         "profiling those kernels")
+                    help="run only the secondary measurements (one JSON object); for profiling "
+                         "those kernels")
+    ap.add_argument("--only", default=None,
+                    help="with --secondary-only: a comma-separated subset of " + ", ".join(SECONDARY))
     ap.add_argument("--sweep", action="store_true",
                     help="sequence-length sweep N = 2^9 .. 2^16 with B * N fixed: causal fwd+bwd "
                          "time and peak allocated memory per sample (one JSON object)")
@@ -496,7 +498,7 @@ def measure_e2e(la, torch, dev, q, k, v, g, out, den, wsf, wsb, B, H, N, D, M, d
             "serial_ms_per_step": round(ms_serial, 5)}
 
 
-def secondary(la, torch, dev, flush, peaks, with_cpu=True):
+def secondary(la, torch, dev, flush, peaks, with_cpu=True, only=None):
     """The 784-token causal fwd+bwd, non-causal fwd+bwd (long speech-like
     sequences with padding), the prefill (causal forward from a state), the
     decode step (256 and 2048 streams x 8 heads), the projected decode step
@@ -505,7 +507,38 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True):
     sequence-length sweep."""
     from kernelized_causal_attention_gb300.workloads import WORKLOADS, causal_inputs, noncausal_inputs
     res = {}
+    want = lambda name: only is None or name in only
     # the 784-token (28 x 28) image workload: causal fwd + bwd
+    if want("causal_mnist_bf16"):
+        _causal_mnist(la, torch, dev, flush, peaks, with_cpu, res)
+    if want("noncausal_speech_f32"):
+        _noncausal(la, torch, dev, flush, peaks, with_cpu, res)
+    if want("prefill_cifar_bf16"):
+        _prefill(la, torch, dev, flush, peaks, with_cpu, res)
+    if want("decode_f32"):
+        _decode(la, torch, dev, peaks, with_cpu, res)
+    for name in ("decode_proj_bf16", "decode_proj_mnist_bf16"):
+        if want(name):
+            _decode_proj(la, torch, dev, flush, peaks, with_cpu, res, name)
+    # a short sequence-length sweep (the full one is --sweep)
+    if want("sweep_causal_bf16"):
+        res["sweep_causal_bf16"] = {
+            "what": "causal fwd+bwd, B * N = 2^16, H = 8, D = M = 64, bf16, 10 L2-flushed steps a point",
+            "points": sweep_points(la, torch, dev, flush, peaks, [1 << 10, 1 << 12, 1 << 14, 1 << 16], 10)}
+    if with_cpu:
+        model = cpu_model()
+        for v in res.values():
+            if isinstance(v, dict) and "cpu_baseline" in v:
+                v["cpu_baseline"].setdefault("cpu_model", model)
+    return res
+
+
+SECONDARY = ("causal_mnist_bf16", "noncausal_speech_f32", "prefill_cifar_bf16", "decode_f32",
+             "decode_proj_bf16", "decode_proj_mnist_bf16", "sweep_causal_bf16")
+
+
+def _causal_mnist(la, torch, dev, flush, peaks, with_cpu, res):
+    from kernelized_causal_attention_gb300.workloads import WORKLOADS, causal_inputs
     wm = WORKLOADS["causal_mnist_bf16"]
     B, H, N, D, M = wm.B, wm.H, wm.N, wm.D, wm.M
     q, k, v, g = causal_inputs(B, H, N, D, M, wm.dtype, wm.seed)
@@ -534,6 +567,10 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True):
         "timing": "CUDA events, L2 flushed before each step (100 steps)"}
     if with_cpu:
         res["causal_mnist_bf16"]["cpu_baseline"] = cpu_baseline(q, k, v, g, B, H, N, budget_s=5.0)
+
+
+def _noncausal(la, torch, dev, flush, peaks, with_cpu, res):
+    from kernelized_causal_attention_gb300.workloads import WORKLOADS, noncausal_inputs
     w = WORKLOADS["noncausal_speech_f32"]
     B, H, N, D, M = w.B, w.H, w.N, w.D, w.M
     lengths, q, k, v, g = noncausal_inputs(B, H, N, D, M, w.dtype, w.seed, w.len_range)
@@ -567,10 +604,13 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True):
     if with_cpu:
         res["noncausal_speech_f32"]["cpu_baseline"] = cpu_baseline_noncausal(q, k, v, g, lengths)
 
-    # prefill: the causal forward from a state, leaving the state after the
-    # sequence (the 3072-token image workload's shape; the state carries over
-    # from call to call like consecutive prompt segments)
-    from kernelized_causal_attention_gb300.workloads import causal_inputs
+
+
+def _prefill(la, torch, dev, flush, peaks, with_cpu, res):
+    """The causal forward from a state, leaving the state after the sequence
+    (the 3072-token image workload's shape; the state carries over from call
+    to call like consecutive prompt segments)."""
+    from kernelized_causal_attention_gb300.workloads import WORKLOADS, causal_inputs
     wc = WORKLOADS["causal_cifar_bf16"]
     B, H, N, D, M = wc.B, wc.H, wc.N, wc.D, wc.M
     q, k, v, _ = causal_inputs(B, H, N, D, M, wc.dtype, wc.seed)
@@ -594,6 +634,8 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True):
     if with_cpu:
         res["prefill_cifar_bf16"]["cpu_baseline"] = cpu_baseline_prefill(q, k, v, B, H, N)
 
+
+def _decode(la, torch, dev, peaks, with_cpu, res):
     for Bd in (256, 2048):
         Hd, Dd, Md = 8, 64, 64
         S = torch.zeros(Bd, Hd, Dd, Md, device=dev)
@@ -639,44 +681,34 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True):
         if with_cpu and Bd == 256:
             res[f"decode_f32_B{Bd}"]["cpu_baseline"] = cpu_baseline_decode(Bd, Hd, Dd, Md)
 
-    # the decode step fed by its q/k/v projection (one launch: the bf16
-    # projection on the tensor cores, then the fp32 state update and read-out)
-    from kernelized_causal_attention_gb300.workloads import proj_inputs
-    for name in ("decode_proj_bf16", "decode_proj_mnist_bf16"):
-        wp = WORKLOADS[name]
-        B, H, D, M, dm = wp.B, wp.H, wp.D, wp.M, wp.d_model
-        x, W, S0, Z0 = proj_inputs(B, dm, H, D, M, t=wp.N, seed=wp.seed)
-        xd, Wd, Sd, Zd = (t.to(dev) for t in (x, W, S0, Z0))
-        y = torch.empty(B, H, M, dtype=torch.bfloat16, device=dev)
-        call = lambda: la.la_decode_step_proj(xd, Wd, Sd, Zd, y, B, H, dm, D, M, 1)
-        for _ in range(3):
-            call()
-        (mp,), _ = time_calls([call], 50, flush, torch, None, dev)
-        alg = proj_bytes(B, H, dm, D, M)
-        flops = 2 * B * dm * H * (2 * D + M)
-        gbs = alg / (mp / 1e3) / 1e9
-        res[name] = {
-            "value": round(B / (mp / 1e3), 1), "unit": "stream-steps/s", "us_per_step": round(mp * 1e3, 3),
-            "B": B, "H": H, "D": D, "M": M, "d_model": dm,
-            "launches": la.la_kernel_launches(la.LA_OP_DECODE_PROJ, B, H, dm, D, M, 1),
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": alg,
-                         "bytes": "x, W read once; S, Z read and written once; y written"},
-            "projection_tflops": round(flops / (mp / 1e3) / 1e12, 2),
-            "timing": "CUDA events per call, L2 flushed before each (50 calls)"}
-        if with_cpu:
-            res[name]["cpu_baseline"] = cpu_baseline_decode_proj(x, W, S0, Z0, H, D, M)
 
-    # a short sequence-length sweep (the full one is --sweep)
-    res["sweep_causal_bf16"] = {
-        "what": "causal fwd+bwd, B * N = 2^16, H = 8, D = M = 64, bf16, 10 L2-flushed steps a point",
-        "points": sweep_points(la, torch, dev, flush, peaks, [1 << 10, 1 << 12, 1 << 14, 1 << 16], 10)}
+def _decode_proj(la, torch, dev, flush, peaks, with_cpu, res, name):
+    """The decode step fed by its q/k/v projection (one launch: the bf16
+    projection on the tensor cores, then the fp32 state update and read-out)."""
+    from kernelized_causal_attention_gb300.workloads import WORKLOADS, proj_inputs
+    wp = WORKLOADS[name]
+    B, H, D, M, dm = wp.B, wp.H, wp.D, wp.M, wp.d_model
+    x, W, S0, Z0 = proj_inputs(B, dm, H, D, M, t=wp.N, seed=wp.seed)
+    xd, Wd, Sd, Zd = (t.to(dev) for t in (x, W, S0, Z0))
+    y = torch.empty(B, H, M, dtype=torch.bfloat16, device=dev)
+    call = lambda: la.la_decode_step_proj(xd, Wd, Sd, Zd, y, B, H, dm, D, M, 1)
+    for _ in range(3):
+        call()
+    (mp,), _ = time_calls([call], 50, flush, torch, None, dev)
+    alg = proj_bytes(B, H, dm, D, M)
+    flops = 2 * B * dm * H * (2 * D + M)
+    gbs = alg / (mp / 1e3) / 1e9
+    res[name] = {
+        "value": round(B / (mp / 1e3), 1), "unit": "stream-steps/s", "us_per_step": round(mp * 1e3, 3),
+        "B": B, "H": H, "D": D, "M": M, "d_model": dm,
+        "launches": la.la_kernel_launches(la.LA_OP_DECODE_PROJ, B, H, dm, D, M, 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": alg,
+                     "bytes": "x, W read once; S, Z read and written once; y written"},
+        "projection_tflops": round(flops / (mp / 1e3) / 1e12, 2),
+        "timing": "CUDA events per call, L2 flushed before each (50 calls)"}
     if with_cpu:
-        model = cpu_model()
-        for v in res.values():
-            if isinstance(v, dict) and "cpu_baseline" in v:
-                v["cpu_baseline"].setdefault("cpu_model", model)
-    return res
+        res[name]["cpu_baseline"] = cpu_baseline_decode_proj(x, W, S0, Z0, H, D, M)
 
 
 def proj_bytes(B, H, dm, D, M):
@@ -859,8 +891,8 @@ def run_reference(args, dist):
                     "d2h_bytes_per_step": 0}}
 
 
-def run_secondary_only():
-    """The non-causal and decode measurements alone, on cuda:0."""
+def run_secondary_only(only=None):
+    """The secondary measurements alone (or the subset `only`), on cuda:0."""
     import torch
 
     import kernelized_causal_attention_gb300 as la
@@ -870,7 +902,7 @@ def run_secondary_only():
     la.lib()
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     return {"secondary": secondary(la, torch, dev, lambda: flush_buf.zero_(), measured_peaks(),
-                                   with_cpu=False)}
+                                   with_cpu=False, only=only)}
 
 
 def sweep_points(la, torch, dev, flush, peaks, Ns, steps, total=1 << 16):
@@ -937,7 +969,7 @@ def main():
     dist = Dist()
     if args.secondary_only:
         if dist.rank == 0:
-            print(json.dumps(run_secondary_only()), flush=True)
+            print(json.dumps(run_secondary_only(None if args.only is None else set(args.only.split(",")))), flush=True)
         return
     if args.sweep:
         if dist.rank == 0:
