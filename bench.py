@@ -509,8 +509,9 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True, only=None):
     res = {}
     want = lambda name: only is None or name in only
     # the 784-token (28 x 28) image workload: causal fwd + bwd
-    if want("causal_mnist_bf16"):
-        _causal_mnist(la, torch, dev, flush, peaks, with_cpu, res)
+    for name in ("causal_mnist_bf16", "causal_cifar_d32_bf16"):
+        if want(name):
+            _causal_line(la, torch, dev, flush, peaks, with_cpu, res, name)
     if want("noncausal_speech_f32"):
         _noncausal(la, torch, dev, flush, peaks, with_cpu, res)
     if want("prefill_cifar_bf16"):
@@ -533,13 +534,15 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True, only=None):
     return res
 
 
-SECONDARY = ("causal_mnist_bf16", "noncausal_speech_f32", "prefill_cifar_bf16", "decode_f32",
+SECONDARY = ("causal_mnist_bf16", "causal_cifar_d32_bf16", "noncausal_speech_f32", "prefill_cifar_bf16", "decode_f32",
              "decode_proj_bf16", "decode_proj_mnist_bf16", "sweep_causal_bf16")
 
 
-def _causal_mnist(la, torch, dev, flush, peaks, with_cpu, res):
+def _causal_line(la, torch, dev, flush, peaks, with_cpu, res, name):
+    """Causal fwd + bwd on a named bf16 workload (the 784-token images; the
+    3072-token images with the pages' 32-wide heads)."""
     from kernelized_causal_attention_gb300.workloads import WORKLOADS, causal_inputs
-    wm = WORKLOADS["causal_mnist_bf16"]
+    wm = WORKLOADS[name]
     B, H, N, D, M = wm.B, wm.H, wm.N, wm.D, wm.M
     q, k, v, g = causal_inputs(B, H, N, D, M, wm.dtype, wm.seed)
     qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
@@ -556,7 +559,7 @@ def _causal_mnist(la, torch, dev, flush, peaks, with_cpu, res):
     (mf, mb), ms = time_calls([fwd, bwd], 100, flush, torch, None, dev)
     fb, bb = causal_bytes(B, H, N, D, M, 2)
     gbs = (fb + bb) / (ms / 1e3) / 1e9
-    res["causal_mnist_bf16"] = {
+    res[name] = {
         "value": round(B * N / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
         "fwd_ms": round(mf, 5), "bwd_ms": round(mb, 5), "B": B, "H": H, "N": N, "D": D, "M": M,
         "launches": la.la_kernel_launches(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, 1)
@@ -566,7 +569,7 @@ def _causal_mnist(la, torch, dev, flush, peaks, with_cpu, res):
                      "bytes_per_token_head": (fb + bb) // (B * H * N)},
         "timing": "CUDA events, L2 flushed before each step (100 steps)"}
     if with_cpu:
-        res["causal_mnist_bf16"]["cpu_baseline"] = cpu_baseline(q, k, v, g, B, H, N, budget_s=5.0)
+        res[name]["cpu_baseline"] = cpu_baseline(q, k, v, g, B, H, N, budget_s=5.0)
 
 
 def _noncausal(la, torch, dev, flush, peaks, with_cpu, res):

@@ -44,7 +44,7 @@ size_t ws_bytes(int op, const Shape& s) {
     case LA_OP_CAUSAL_BWD:
       return 4 * (la::tc_eligible(s) ? la::causal_bwd_tc_ws_floats(s) : la::causal_bwd_ws_floats(s));
     case LA_OP_CAUSAL_PREFILL:
-      return 4 * (la::tc_eligible(s) ? la::causal_fwd_tc_ws_floats(s) : la::causal_prefill_ws_floats(s));
+      return 4 * (la::tc_prefill_eligible(s) ? la::causal_fwd_tc_ws_floats(s) : la::causal_prefill_ws_floats(s));
     case LA_OP_CAUSAL_FWD_DECAY: return 4 * la::causal_fwd_ws_floats(s);
     case LA_OP_CAUSAL_BWD_DECAY: return 4 * la::causal_bwd_ws_floats(s);
     case LA_OP_NONCAUSAL_FWD: return 4 * la::noncausal_fwd_ws_floats(s);
@@ -129,7 +129,7 @@ int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype) {
       return la::tc_eligible(s) ? la::causal_fwd_tc_launches(s) : la::causal_fwd_launches(s);
     case LA_OP_CAUSAL_BWD:
       return la::tc_eligible(s) ? la::causal_bwd_tc_launches(s) : la::causal_bwd_launches(s);
-    case LA_OP_CAUSAL_PREFILL: return la::tc_eligible(s) ? 3 : 4;
+    case LA_OP_CAUSAL_PREFILL: return la::tc_prefill_eligible(s) ? 3 : 4;
     case LA_OP_CAUSAL_FWD_DECAY: return la::causal_fwd_launches(s);
     case LA_OP_CAUSAL_BWD_DECAY: return la::causal_bwd_launches(s);
     case LA_OP_NONCAUSAL_FWD: return la::noncausal_fwd_launches(s);
@@ -160,7 +160,7 @@ int la_causal_prefill(const void* q, const void* k, const void* v, void* out, fl
   LA_TRY(check_opt_ptr(den));
   const Shape s{B, H, N, D, M, dtype};
   LA_TRY(check_ws(LA_OP_CAUSAL_PREFILL, s, workspace, workspace_bytes));
-  if (la::tc_eligible(s))
+  if (la::tc_prefill_eligible(s))
     return from_cuda(la::causal_prefill_tc(q, k, v, out, den, S, Z, static_cast<float*>(workspace),
                                            s, static_cast<cudaStream_t>(stream)));
   return from_cuda(la::causal_prefill_cc(q, k, v, out, den, S, Z, static_cast<float*>(workspace), s,

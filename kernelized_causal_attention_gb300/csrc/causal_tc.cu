@@ -1,5 +1,7 @@
 // Causal linear attention on the 5th-generation tensor cores (tcgen05), for
-// bf16 inputs with D = M = 64 and fp32 accumulation in tensor memory.
+// bf16 inputs with D, M in {16, 32, 64} and fp32 accumulation in tensor
+// memory.  Heads narrower than 64 use the same 64-wide tiles: the loads fill
+// the missing columns with zeros and phi is zeroed on those features.
 //
 // Method: "Transformers are RNNs" (part 2/3), §3.3 eq. 9-12.
 //
@@ -80,7 +82,7 @@ constexpr int W_PHI0 = 2, W_MASK0 = 10, W_EPI0 = 14;
 // ws[bh][p] ([64][80] fp32) for every segment p but the last.
 __global__ void __launch_bounds__(NTHR, 1)
     k_tc_fwd_state(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   float* __restrict__ ws, int N, int nseg, int seg_len, int* err) {
+                   float* __restrict__ ws, int N, int nseg, int seg_len, int dch, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int c = 0; c < nch; ++c) {
       const int s = c % SNST;
       if (wt(&bar_full[s], (c / SNST) & 1, 33))
-        phi_tiles<NCOMP, 1>(sm + s * S_STAGE, 0, min(TC_C, ne - (nb + c * TC_C)), t);
+        phi_tiles<NCOMP, 1>(sm + s * S_STAGE, 0, min(TC_C, ne - (nb + c * TC_C)), t, dch);
       fence_proxy_async();
       mbar_arrive(&bar_phi[s]);
     }
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     k_tc_fwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ out,
                   float* __restrict__ den, const float* __restrict__ ws, int N, int nseg,
-                  int seg_len, int out_v8, int* err, const float* __restrict__ S0,
+                  int seg_len, int out_v8, int dch, int M, int* err, const float* __restrict__ S0,
                   const float* __restrict__ Z0) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ uint8_t smraw[];
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         uint32_t pq[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint4 r = row < valid ? phi_vec(qv[i]) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 r = row < valid && 4 * h + i < dch ? phi_vec(qv[i]) : make_uint4(0u, 0u, 0u, 0u);
           pq[4 * i] = r.x;
           pq[4 * i + 1] = r.y;
           pq[4 * i + 2] = r.z;
@@ -415,8 +417,8 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int v = tt + i * NT;
-          *reinterpret_cast<uint4*>(st + v * 16) =
-              (v >> 3) >= valid ? make_uint4(0u, 0u, 0u, 0u) : phi_vec(kv[i]);
+          const bool pad = (v >> 3) >= valid || (((v & 7) ^ ((v >> 3) & 7)) >= dch);
+          *reinterpret_cast<uint4*>(st + v * 16) = pad ? make_uint4(0u, 0u, 0u, 0u) : phi_vec(kv[i]);
         }
         tmem_st_wait();
       }
@@ -597,7 +599,7 @@ __global__ void __launch_bounds__(NTHR, 1)
           for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16(o[2 * i] * inv, o[2 * i + 1] * inv);
           if (n0 + row < ne) {
             const long r = static_cast<long>(bh) * N + n0 + row;
-            store_row_bf16(out + r * 64, w, out_v8 != 0);
+            store_row_bf16(out + r * M, w, out_v8 != 0, M);
             if (den != nullptr) den[r] = d;
           }
         } else {
@@ -631,12 +633,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// [BH][N][64] bf16 viewed as a 3-D tensor, 64 x 128 x 1 boxes, 128-byte swizzle.
-bool make_bf16_map(CUtensorMap* m, const void* base, int BH, int N) {
+// [BH][N][W] bf16 viewed as a 3-D tensor, 64 x 128 x 1 boxes, 128-byte
+// swizzle; for W < 64 the box reaches past the row and the load fills the
+// rest with zeros (a store writes only the W columns).
+bool make_bf16_map(CUtensorMap* m, const void* base, int BH, int N, int W) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {64 * 2, static_cast<cuuint64_t>(N) * 64 * 2};
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(W) * 2, static_cast<cuuint64_t>(N) * W * 2};
   cuuint32_t box[3] = {64, TC_C, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
@@ -671,7 +675,14 @@ SegPlan tc_plan(int BH, int N) {
   return pl;
 }
 
-bool tc_eligible(const Shape& s) { return s.dtype == 1 && s.D == 64 && s.M == 64; }
+// bf16 with D, M in {16, 32, 64}: narrower heads ride in the 64-wide tiles,
+// zero-filled by the loads, with phi zeroed on the padded features.
+bool tc_eligible(const Shape& s) {
+  return s.dtype == 1 && (s.D == 16 || s.D == 32 || s.D == 64) && (s.M == 16 || s.M == 32 || s.M == 64);
+}
+
+// The prefill adds and returns the caller's [D][M] state, laid out for 64.
+bool tc_prefill_eligible(const Shape& s) { return s.dtype == 1 && s.D == 64 && s.M == 64; }
 
 size_t causal_fwd_tc_ws_floats(const Shape& s) {
   const SegPlan pl = tc_plan(s.B * s.H, s.N);
@@ -691,8 +702,8 @@ cudaError_t fwd_tc_launch(const void* q, const void* k, const void* v, void* out
   const int BH = s.B * s.H;
   const SegPlan pl = tc_plan(BH, s.N);
   CUtensorMap mq, mk, mv;
-  if (!make_bf16_map(&mq, q, BH, s.N) || !make_bf16_map(&mk, k, BH, s.N) ||
-      !make_bf16_map(&mv, v, BH, s.N))
+  if (!make_bf16_map(&mq, q, BH, s.N, s.D) || !make_bf16_map(&mk, k, BH, s.N, s.D) ||
+      !make_bf16_map(&mv, v, BH, s.N, s.M))
     return cudaErrorInvalidValue;
   const int out_v8 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
   int* err = status_word();
@@ -706,12 +717,12 @@ cudaError_t fwd_tc_launch(const void* q, const void* k, const void* v, void* out
   const int nrec = all_records ? pl.nseg : pl.nseg - 1;
   if (nrec > 0) {
     if ((e = launch_pdl(k_tc_fwd_state, dim3(nrec, BH), dim3(NTHR), S_SMEM, st, mk, mv, ws,
-                        s.N, pl.nseg, pl.seg_len, err)) != cudaSuccess)
+                        s.N, pl.nseg, pl.seg_len, s.D / 8, err)) != cudaSuccess)
       return e;
   }
   if ((e = launch_pdl(k_tc_fwd_main, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv,
                       static_cast<bf16*>(out), den, static_cast<const float*>(ws), s.N, pl.nseg,
-                      pl.seg_len, out_v8, err, S0, Z0)) != cudaSuccess)
+                      pl.seg_len, out_v8, s.D / 8, s.M, err, S0, Z0)) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }

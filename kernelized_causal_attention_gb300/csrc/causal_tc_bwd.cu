@@ -1,5 +1,6 @@
 // Backward of causal linear attention on the tcgen05 tensor cores, bf16 with
-// D = M = 64 and fp32 accumulation in tensor memory.
+// D, M in {16, 32, 64} (narrower heads zero-filled to the 64-wide tiles, phi
+// zeroed on the padded features) and fp32 accumulation in tensor memory.
 //
 // Method: "Transformers are RNNs" (part 2/3) §3.3.1 eq. 13-15, the gradients
 // of the numerator as cumulative sums, completed with the denominator by the
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     k_tc_bwd_state(const __grid_constant__ StateMaps maps, const float* __restrict__ den,
                    float* __restrict__ gam, bf16* __restrict__ gt_out, bf16* __restrict__ fq_out,
                    bf16* __restrict__ fk_out, float* __restrict__ rec, int N, int sub_len, int nsub,
-                   int* err) {
+                   int dch, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;  // the call's first kernel
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -569,10 +570,11 @@ __global__ void __launch_bounds__(NTHR, 1)
           const int v = t + i * NCOMP, r = v >> 3, lc = (v & 7) ^ (r & 7);
           const bool rv = r < valid;
           const long gofs = (hb + n0 + r) * 64 + lc * 8;
-          // phi(Q), phi(K): in place and to the workspace
+          // phi(Q), phi(K): in place and to the workspace (zero on padded
+          // features of a head narrower than 64: phi(0) = 1 would add them)
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
-            const uint4 f = rv ? phi_vec(x[k][i]) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 f = rv && lc < dch ? phi_vec(x[k][i]) : make_uint4(0u, 0u, 0u, 0u);
             *reinterpret_cast<uint4*>(st + k * TILE + v * 16) = f;
             if (rv) *reinterpret_cast<uint4*>((k == 0 ? fq_out : fk_out) + gofs) = f;
           }
@@ -712,12 +714,14 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
   const BwdPlan pl = bwd_plan(BH, s.N);
   const BwdWs w = bwd_ws(ws, BH, s.N, pl);
   BwdMaps m;
-  if (!make_bf16_map(&m.q, q, BH, s.N) || !make_bf16_map(&m.k, k, BH, s.N) ||
-      !make_bf16_map(&m.v, v, BH, s.N) || !make_bf16_map(&m.g, dout, BH, s.N) ||
-      !make_bf16_map(&m.o, out, BH, s.N) || !make_bf16_map(&m.fq, w.fq, BH, s.N) ||
+  // the caller's tensors at their own widths (loads zero-fill to 64, stores
+  // write only D or M columns); the workspace's phi(Q), phi(K), gt stay 64 wide
+  if (!make_bf16_map(&m.q, q, BH, s.N, s.D) || !make_bf16_map(&m.k, k, BH, s.N, s.D) ||
+      !make_bf16_map(&m.v, v, BH, s.N, s.M) || !make_bf16_map(&m.g, dout, BH, s.N, s.M) ||
+      !make_bf16_map(&m.o, out, BH, s.N, s.M) || !make_bf16_map(&m.fq, w.fq, BH, s.N) ||
       !make_bf16_map(&m.fk, w.fk, BH, s.N) || !make_bf16_map(&m.gt, w.gt, BH, s.N) ||
-      !make_bf16_map(&m.dq, dq, BH, s.N) || !make_bf16_map(&m.dk, dk, BH, s.N) ||
-      !make_bf16_map(&m.dv, dv, BH, s.N))
+      !make_bf16_map(&m.dq, dq, BH, s.N, s.D) || !make_bf16_map(&m.dk, dk, BH, s.N, s.D) ||
+      !make_bf16_map(&m.dv, dv, BH, s.N, s.M))
     return cudaErrorInvalidValue;
   StateMaps smap;
   smap.q = m.q;
@@ -733,7 +737,7 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
                                 M_SMEM)) != cudaSuccess)
     return e;
   if ((e = launch_pdl(k_tc_bwd_state, dim3(pl.nsub, BH), dim3(NTHR), SS_SMEM, st, smap, den, w.gam,
-                      w.gt, w.fq, w.fk, w.rec, s.N, pl.sub_len, pl.nsub, status_word())) != cudaSuccess)
+                      w.gt, w.fq, w.fk, w.rec, s.N, pl.sub_len, pl.nsub, s.D / 8, status_word())) != cudaSuccess)
     return e;
   if ((e = launch_pdl(k_tc_bwd_main, dim3(pl.main.nseg, BH, 2), dim3(NTHR), M_SMEM, st, m,
                       static_cast<const float*>(w.rec), static_cast<const float*>(w.gam), s.N,

@@ -85,7 +85,8 @@ cudaError_t causal_prefill_tc(const void* q, const void* k, const void* v, void*
 
 // tcgen05 path (bf16, D = M = 64).
 SegPlan tc_plan(int BH, int N);
-bool tc_eligible(const Shape& s);
+bool tc_eligible(const Shape& s);          // causal fwd / bwd on the tensor cores
+bool tc_prefill_eligible(const Shape& s);  // the prefill on the tensor cores (D = M = 64)
 size_t causal_fwd_tc_ws_floats(const Shape& s);
 int causal_fwd_tc_launches(const Shape& s);
 cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out, float* den,

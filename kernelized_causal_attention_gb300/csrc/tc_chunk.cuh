@@ -97,9 +97,11 @@ __device__ __forceinline__ uint4 phi_vec(uint4 u) {
 // bytes apart, by NT threads (t = 0 .. NT-1; elementwise, so the swizzle does
 // not matter).  Every thread first loads all of its vectors, then transforms
 // and stores them, so the loads and the exponentials overlap.  Rows at or past
-// `valid` are zeroed: a zero phi row adds nothing to any sum.
+// `valid` are zeroed: a zero phi row adds nothing to any sum.  So are the
+// columns at or past 8 dch (a head narrower than 64 whose tile the load
+// filled with zeros: phi(0) = 1, but a padded feature must add nothing).
 template <int NT, int NTL>
-__device__ __forceinline__ void phi_tiles(uint8_t* tile, int stride, int valid, int t) {
+__device__ __forceinline__ void phi_tiles(uint8_t* tile, int stride, int valid, int t, int dch = 8) {
   constexpr int PER = TILE / 16 / NT;  // vectors per thread and tile
   static_assert(PER * NT * 16 == TILE, "threads must divide the tile");
   uint4 u[NTL][PER];
@@ -113,7 +115,8 @@ __device__ __forceinline__ void phi_tiles(uint8_t* tile, int stride, int valid, 
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int v = t + i * NT;
-      const uint4 r = (v >> 3) >= valid ? make_uint4(0u, 0u, 0u, 0u) : phi_vec(u[k][i]);
+      const bool pad = (v >> 3) >= valid || (((v & 7) ^ ((v >> 3) & 7)) >= dch);
+      const uint4 r = pad ? make_uint4(0u, 0u, 0u, 0u) : phi_vec(u[k][i]);
       sts128(tile + k * stride + v * 16, r);
     }
 }
@@ -248,20 +251,22 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, int issued) {
     mbar_wait(&full[i % NS], (i / NS) & 1, WAIT_NS);
 }
 
-// 64 bf16 (32 packed words) to a 128-byte global row: 32-byte stores when
-// the row is 32-byte aligned, else 16-byte stores.
-__device__ __forceinline__ void store_row_bf16(bf16* dst, const uint32_t* w, bool v8) {
+// The first `ncols` (16, 32 or 64) of 64 bf16 (32 packed words) to a global
+// row: 32-byte stores when the row is 32-byte aligned, else 16-byte stores.
+__device__ __forceinline__ void store_row_bf16(bf16* dst, const uint32_t* w, bool v8, int ncols = 64) {
   if (v8) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * i),
-                   "r"(w[8 * i]), "r"(w[8 * i + 1]), "r"(w[8 * i + 2]), "r"(w[8 * i + 3]),
-                   "r"(w[8 * i + 4]), "r"(w[8 * i + 5]), "r"(w[8 * i + 6]), "r"(w[8 * i + 7])
-                   : "memory");
+      if (16 * i < ncols)
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * i),
+                     "r"(w[8 * i]), "r"(w[8 * i + 1]), "r"(w[8 * i + 2]), "r"(w[8 * i + 3]),
+                     "r"(w[8 * i + 4]), "r"(w[8 * i + 5]), "r"(w[8 * i + 6]), "r"(w[8 * i + 7])
+                     : "memory");
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      *reinterpret_cast<uint4*>(dst + 8 * i) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      if (8 * i < ncols)
+        *reinterpret_cast<uint4*>(dst + 8 * i) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
   }
 }
 
@@ -441,9 +446,11 @@ cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
 }
 
-// [BH][N][64] bf16 viewed as a 3-D TMA tensor with 64 x 128 x 1 boxes and the
-// 128-byte swizzle (defined in causal_tc.cu).
-bool make_bf16_map(CUtensorMap* m, const void* base, int BH, int N);
+// [BH][N][W] bf16 (W = 16, 32 or 64) viewed as a 3-D TMA tensor with
+// 64 x 128 x 1 boxes and the 128-byte swizzle (defined in causal_tc.cu): a
+// narrower row arrives zero-filled to 64 columns, and a store writes only
+// its W columns.
+bool make_bf16_map(CUtensorMap* m, const void* base, int BH, int N, int W = 64);
 
 // [rows][cols] row-major bf16 as a 3-D TMA tensor with 64 x box_rows x 1 boxes
 // and the 128-byte swizzle (defined in causal_tc.cu).

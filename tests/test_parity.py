@@ -63,6 +63,14 @@ SMALL = [
     (2, 2, 257, 64, 64, "bf16"),
     (1, 1, 2049, 32, 32, "bf16"),
     (2, 1, 77, 16, 16, "bf16"),
+    # bf16 heads narrower than 64 also run on the tensor cores (tiles zero-filled
+    # to 64 columns, phi zeroed on the padded features)
+    (1, 1, 1, 32, 32, "bf16"),
+    (2, 2, 1000, 32, 64, "bf16"),
+    (1, 3, 3001, 16, 32, "bf16"),
+    (3, 2, 129, 64, 16, "bf16"),
+    (1, 1, 4097, 32, 32, "bf16"),
+    (8, 8, 784, 32, 32, "bf16"),
     # bf16 with D = M = 64 runs on the tensor cores: 128-token chunks, segments
     (1, 1, 1, 64, 64, "bf16"),
     (1, 1, 100, 64, 64, "bf16"),
@@ -115,7 +123,7 @@ def test_causal_beyond_2_31_elements(cuda, linattn):
     linattn.check_device_status()
 
 
-@pytest.mark.parametrize("name", ["causal_tiny_f32", "causal_mnist_bf16", "causal_cifar_bf16"])
+@pytest.mark.parametrize("name", ["causal_tiny_f32", "causal_mnist_bf16", "causal_cifar_bf16", "causal_cifar_d32_bf16"])
 def test_causal_workloads(cuda, linattn, name):
     w = WORKLOADS[name]
     errs = check_causal(linattn, cuda, w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed)
