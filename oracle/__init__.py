@@ -50,6 +50,8 @@ _SIGS = {
     "orc_causal_bwd_quadratic_decay": "i i i i p p p p d p p p i",
     "orc_decode_decay": "i i i i p p p d p p p i",
     "orc_causal_prefill": "i i i i p p p p p p p i",
+    "orc_causal_fwd_poly": "i i i i p p p p p i",
+    "orc_causal_bwd_poly": "i i i i p p p p p p p i",
 }
 
 
@@ -162,6 +164,28 @@ class Oracle:
                   "quadratic": self.lib.orc_causal_bwd_quadratic_decay}[form]
             fn(B * H, N, D, M, _ptr(q), _ptr(k), _ptr(v), _ptr(g), float(gamma),
                _ptr(dq), _ptr(dk), _ptr(dv), nthreads)
+        return dq, dk, dv
+
+    def causal_fwd_poly(self, q, k, v, nthreads=0):
+        """Causal forward with the degree-2 polynomial kernel sim = (q . k)^2
+        (the quadratic form, every pair): (out [B,H,N,M], den [B,H,N])."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, H, N, D = q.shape
+        M = v.shape[-1]
+        out, den = np.empty((B, H, N, M)), np.empty((B, H, N))
+        self.lib.orc_causal_fwd_poly(B * H, N, D, M, _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                     _ptr(den), nthreads)
+        return out, den
+
+    def causal_bwd_poly(self, q, k, v, g, nthreads=0):
+        """Gradients (dq, dk, dv) of sum(g * V') with the degree-2 polynomial
+        kernel, by the pairwise rule."""
+        q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(g)
+        B, H, N, D = q.shape
+        M = v.shape[-1]
+        dq, dk, dv = np.empty((B, H, N, D)), np.empty((B, H, N, D)), np.empty((B, H, N, M))
+        self.lib.orc_causal_bwd_poly(B * H, N, D, M, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), nthreads)
         return dq, dk, dv
 
     def noncausal_fwd(self, q, k, v, lengths=None, form="recurrent", nthreads=0):
@@ -281,6 +305,14 @@ def noncausal_bwd(q, k, v, g, lengths=None, form="recurrent", nthreads=0):
 
 def decode(q, k, v, S=None, Z=None, nthreads=0, gamma=None):
     return default().decode(q, k, v, S, Z, nthreads, gamma)
+
+
+def causal_fwd_poly(q, k, v, nthreads=0):
+    return default().causal_fwd_poly(q, k, v, nthreads)
+
+
+def causal_bwd_poly(q, k, v, g, nthreads=0):
+    return default().causal_bwd_poly(q, k, v, g, nthreads)
 
 
 def causal_prefill(q, k, v, S=None, Z=None, nthreads=0):

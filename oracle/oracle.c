@@ -356,6 +356,103 @@ void orc_causal_bwd_quadratic(int BH, int N, int D, int M, const double* q,
   orc_causal_bwd_quadratic_decay(BH, N, D, M, q, k, v, g, 1.0, dq, dk, dv, nthreads);
 }
 
+/* --------------------------------- causal, degree-2 polynomial kernel */
+
+/* [TR2] the feature-map discussion that opens part 2/3 (§3.2.1): the
+ * polynomial kernel has an exact finite feature map, and linear attention
+ * with the degree-2 one costs O(N D^2 M).  Read as the homogeneous kernel
+ * sim(Q_i, K_j) = (Q_i . K_j)^2 in place of phi(Q_i) . phi(K_j) in eq. 8 and
+ * 12 (no feature map is applied to Q or K first):
+ *   A_ij = (Q_i . K_j)^2 for j <= i,  den_i = sum_j A_ij,
+ *   out_i = sum_j A_ij V_j / den_i.
+ * Written as the plain quadratic form: every (i, j) pair. */
+void orc_causal_fwd_poly(int BH, int N, int D, int M, const double* q, const double* k,
+                         const double* v, double* out, double* den, int nthreads) {
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic)
+  for (int hh = 0; hh < BH; ++hh) {
+    const double* Q = q + (size_t)hh * N * D;
+    const double* K = k + (size_t)hh * N * D;
+    const double* V = v + (size_t)hh * N * M;
+    double* O = out + (size_t)hh * N * M;
+    double* row = (double*)malloc(sizeof(double) * (size_t)N);
+    for (int i = 0; i < N; ++i) {
+      double s = 0.0;
+      for (int j = 0; j <= i; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += Q[(size_t)i * D + d] * K[(size_t)j * D + d];
+        row[j] = dot * dot;
+        s += row[j];
+      }
+      if (den) den[(size_t)hh * N + i] = s;
+      for (int m = 0; m < M; ++m) {
+        double acc = 0.0;
+        for (int j = 0; j <= i; ++j) acc += row[j] * V[(size_t)j * M + m];
+        O[(size_t)i * M + m] = acc / s;
+      }
+    }
+    free(row);
+  }
+}
+
+/* Gradients of L = sum_i G_i . out_i for the degree-2 polynomial kernel, by
+ * the pairwise rule: with gt_i = G_i / den_i and gam_i = -(G_i . out_i) /
+ * den_i as for eq. 13-15, dL/dA_ij = gt_i . V_j + gam_i (j <= i), and
+ * A_ij = (Q_i . K_j)^2 gives dA_ij/dQ_i = 2 (Q_i . K_j) K_j, dA_ij/dK_j =
+ * 2 (Q_i . K_j) Q_i:
+ *   dQ_i = sum_{j<=i} dA_ij 2 (Q_i . K_j) K_j,
+ *   dK_j = sum_{i>=j} dA_ij 2 (Q_i . K_j) Q_i,
+ *   dV_j = sum_{i>=j} A_ij gt_i. */
+void orc_causal_bwd_poly(int BH, int N, int D, int M, const double* q, const double* k,
+                         const double* v, const double* g, double* dq, double* dk, double* dv,
+                         int nthreads) {
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic)
+  for (int hh = 0; hh < BH; ++hh) {
+    const double* Q = q + (size_t)hh * N * D;
+    const double* K = k + (size_t)hh * N * D;
+    const double* V = v + (size_t)hh * N * M;
+    const double* G = g + (size_t)hh * N * M;
+    double* dQ = dq + (size_t)hh * N * D;
+    double* dK = dk + (size_t)hh * N * D;
+    double* dV = dv + (size_t)hh * N * M;
+    double* dots = (double*)malloc(sizeof(double) * (size_t)N);
+    double* gt = (double*)malloc(sizeof(double) * (size_t)M);
+    memset(dQ, 0, sizeof(double) * (size_t)N * D);
+    memset(dK, 0, sizeof(double) * (size_t)N * D);
+    memset(dV, 0, sizeof(double) * (size_t)N * M);
+    for (int i = 0; i < N; ++i) {
+      double s = 0.0;
+      for (int j = 0; j <= i; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += Q[(size_t)i * D + d] * K[(size_t)j * D + d];
+        dots[j] = dot;
+        s += dot * dot;
+      }
+      double gv = 0.0;
+      for (int m = 0; m < M; ++m) {
+        double acc = 0.0;
+        for (int j = 0; j <= i; ++j) acc += dots[j] * dots[j] * V[(size_t)j * M + m];
+        gv += G[(size_t)i * M + m] * (acc / s);
+        gt[m] = G[(size_t)i * M + m] / s;
+      }
+      const double gam = -gv / s;
+      for (int j = 0; j <= i; ++j) {
+        double da = gam;
+        for (int m = 0; m < M; ++m) da += gt[m] * V[(size_t)j * M + m];
+        const double w = 2.0 * da * dots[j];
+        for (int d = 0; d < D; ++d) {
+          dQ[(size_t)i * D + d] += w * K[(size_t)j * D + d];
+          dK[(size_t)j * D + d] += w * Q[(size_t)i * D + d];
+        }
+        for (int m = 0; m < M; ++m) dV[(size_t)j * M + m] += dots[j] * dots[j] * gt[m];
+      }
+    }
+    free(dots);
+    free(gt);
+  }
+}
+
 /* ---------------------------------------------------------- non-causal form */
 
 /* Valid length of batch entry b: lengths[b] if given, else N. */

@@ -490,8 +490,85 @@ def pin_decode_proj(orc):
     assert rel(y, num / den[..., None]) < 1e-13, "y != phi(q)^T S_1 / phi(q)^T Z_1"
 
 
+# ------------------------------------------- degree-2 polynomial kernel
+
+def _poly_features_full(x):
+    """All D^2 products x_a x_b (numpy outer product, flattened): an exact
+    feature map of (q . k)^2, independent of any packing the GPU uses."""
+    return np.einsum("...a,...b->...ab", x, x).reshape(*x.shape[:-1], x.shape[-1] ** 2)
+
+
+def pin_poly_feature_form(orc):
+    """The pairwise form of sim = (q . k)^2 equals linear attention on the
+    explicit D^2 features: S_i, Z_i as numpy cumulative sums of
+    f(K_j) V_j^T and f(K_j), out_i = f(Q_i)^T S_i / f(Q_i)^T Z_i."""
+    for B, H, N, D, M in ((1, 2, 11, 3, 5), (2, 1, 7, 4, 2)):
+        q, k, v = rand((B, H, N, D), 501), rand((B, H, N, D), 502), rand((B, H, N, M), 503)
+        out, den = orc.causal_fwd_poly(q, k, v)
+        fq, fk = _poly_features_full(q), _poly_features_full(k)
+        S = np.cumsum(np.einsum("bhnc,bhnm->bhncm", fk, v), axis=2)
+        Z = np.cumsum(fk, axis=2)
+        num = np.einsum("bhnc,bhncm->bhnm", fq, S)
+        dn = np.einsum("bhnc,bhnc->bhn", fq, Z)
+        assert rel(den, dn) < 1e-12, "den != f(Q) . Z"
+        assert rel(out, num / dn[..., None]) < 1e-12, "out != f(Q)^T S / f(Q)^T Z"
+
+
+def pin_poly_closed_forms(orc):
+    """out_1 = V_1; constant V rows come back unchanged; with D = 1 the
+    weights q_i^2 k_j^2 lose q_i in the quotient, so out_i is the k^2-weighted
+    running mean of V (numpy) and dq = 0 (its terms cancel, to rounding)."""
+    B, H, N, M = 1, 2, 9, 3
+    q, k, v, g = rand((B, H, N, 1), 511), rand((B, H, N, 1), 512), rand((B, H, N, M), 513), rand((B, H, N, M), 514)
+    out, _ = orc.causal_fwd_poly(q, k, v)
+    w = k[..., 0] ** 2
+    ref = np.cumsum(w[..., None] * v, axis=2) / np.cumsum(w, axis=2)[..., None]
+    assert rel(out, ref) < 1e-12, "D = 1 is not the k^2-weighted running mean"
+    dq, dk, _ = orc.causal_bwd_poly(q, k, v, g)
+    assert np.max(np.abs(dq)) < 1e-12 * np.max(np.abs(dk)), "D = 1: the output depends on q"
+    q, k = rand((B, H, N, 4), 515), rand((B, H, N, 4), 516)
+    out, _ = orc.causal_fwd_poly(q, k, v)
+    assert rel(out[:, :, 0], v[:, :, 0]) < 1e-13, "out_1 != V_1"
+    c = np.broadcast_to(rand((B, H, 1, M), 517), v.shape).copy()
+    out, _ = orc.causal_fwd_poly(q, k, c)
+    assert rel(out, c) < 1e-12, "a constant V is not reproduced"
+
+
+def pin_poly_grad_fd(orc):
+    """dq, dk, dv against central finite differences of sum(G * V')."""
+    B, H, N, D, M = 1, 2, 7, 3, 4
+    q, k, v, g = rand((B, H, N, D), 521), rand((B, H, N, D), 522), rand((B, H, N, M), 523), rand((B, H, N, M), 524)
+    loss = lambda q_, k_, v_: float(np.sum(g * orc.causal_fwd_poly(q_, k_, v_)[0]))
+    h = 1e-6
+    an = orc.causal_bwd_poly(q, k, v, g)
+    for x, idx, nm in ((q, 0, "dq"), (k, 1, "dk"), (v, 2, "dv")):
+        gr = np.zeros_like(x)
+        for e in np.ndindex(x.shape):
+            args = [q.copy(), k.copy(), v.copy()]
+            args[idx][e] += h
+            up = loss(*args)
+            args[idx][e] -= 2 * h
+            gr[e] = (up - loss(*args)) / (2 * h)
+        assert rel(an[idx], gr) < 1e-6, f"{nm} != finite differences"
+
+
+def pin_poly_invariants(orc):
+    """sim(c q_i, k) = c^2 sim(q_i, k) leaves out_i unchanged, so
+    q_i . dq_i = 0 for every i; a common scale of all k gives
+    sum_j k_j . dk_j = 0; a constant row added to V gives sum_j dV_j =
+    sum_i G_i."""
+    B, H, N, D, M = 2, 1, 10, 3, 4
+    q, k, v, g = rand((B, H, N, D), 531), rand((B, H, N, D), 532), rand((B, H, N, M), 533), rand((B, H, N, M), 534)
+    dq, dk, dv = orc.causal_bwd_poly(q, k, v, g)
+    scale = np.max(np.abs(dq)) * np.max(np.abs(q))
+    assert np.max(np.abs(np.sum(q * dq, axis=-1))) < 1e-12 * scale * D, "q_i . dq_i != 0"
+    assert np.max(np.abs(np.sum(k * dk, axis=(-2, -1)))) < 1e-11 * np.max(np.abs(dk)) * np.max(np.abs(k)) * N * D
+    assert rel(np.sum(dv, axis=2), np.sum(g, axis=2)) < 1e-12, "sum dV != sum G"
+
+
 ALL_PINS = [pin_phi, pin_causal_forms_agree, pin_causal_closed_forms, pin_grad_single_token, pin_noncausal_gemm,
             pin_noncausal_last_row, pin_noncausal_lengths, pin_grad_fd, pin_grad_forms_agree,
             pin_grad_invariants, pin_decode, pin_prefill, pin_decay_gamma_one, pin_decay_gamma_zero,
             pin_decay_closed_form, pin_decay_forms_agree, pin_decay_grad_fd, pin_decay_invariants,
-            pin_decay_decode, pin_decode_proj]
+            pin_decay_decode, pin_decode_proj, pin_poly_feature_form, pin_poly_closed_forms,
+            pin_poly_grad_fd, pin_poly_invariants]

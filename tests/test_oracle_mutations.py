@@ -38,6 +38,11 @@ MUTATIONS = [
     ("decay_decode_z_not_decayed", "z[d] = gamma * z[d] + fk;", "z[d] = z[d] + fk;", 0),
     ("decay_squared", "S[(size_t)d * M + m] = gamma * S[(size_t)d * M + m] + fk * V[(size_t)i * M + m];",
      "S[(size_t)d * M + m] = gamma * gamma * S[(size_t)d * M + m] + fk * V[(size_t)i * M + m];", 0),
+    # the degree-2 polynomial kernel
+    ("poly_sim_not_squared", "        row[j] = dot * dot;", "        row[j] = dot;", 0),
+    ("poly_grad_factor_dropped", "const double w = 2.0 * da * dots[j];", "const double w = da * dots[j];", 0),
+    ("poly_dk_uses_k", "dK[(size_t)j * D + d] += w * Q[(size_t)i * D + d];", "dK[(size_t)j * D + d] += w * K[(size_t)j * D + d];", 0),
+    ("poly_dv_unsquared", "dV[(size_t)j * M + m] += dots[j] * dots[j] * gt[m];", "dV[(size_t)j * M + m] += dots[j] * gt[m];", 0),
     ("prefill_starts_from_zero", "memcpy(sl, st, sizeof(double) * (size_t)D * M);", "memset(sl, 0, sizeof(double) * (size_t)D * M);", 0),
     ("prefill_den_without_z0", "for (int d = 0; d < D; ++d) zl[d] = zt[d];", "for (int d = 0; d < D; ++d) zl[d] = 0.0 * zt[d];", 0),
     ("prefill_state_not_returned", "for (size_t e = 0; e < (size_t)D * M; ++e) st[e] = sl[e];", "for (size_t e = 0; e < (size_t)D * M; ++e) (void)sl[e];", 0),
