@@ -512,6 +512,8 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True, only=None):
     for name in ("causal_mnist_bf16", "causal_cifar_d32_bf16"):
         if want(name):
             _causal_line(la, torch, dev, flush, peaks, with_cpu, res, name)
+    if want("causal_poly_bf16"):
+        _causal_poly(la, torch, dev, flush, peaks, with_cpu, res)
     if want("noncausal_speech_f32"):
         _noncausal(la, torch, dev, flush, peaks, with_cpu, res)
     if want("prefill_cifar_bf16"):
@@ -534,7 +536,7 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True, only=None):
     return res
 
 
-SECONDARY = ("causal_mnist_bf16", "causal_cifar_d32_bf16", "noncausal_speech_f32", "prefill_cifar_bf16", "decode_f32",
+SECONDARY = ("causal_mnist_bf16", "causal_cifar_d32_bf16", "causal_poly_bf16", "noncausal_speech_f32", "prefill_cifar_bf16", "decode_f32",
              "decode_proj_bf16", "decode_proj_mnist_bf16", "sweep_causal_bf16")
 
 
@@ -570,6 +572,50 @@ def _causal_line(la, torch, dev, flush, peaks, with_cpu, res, name):
         "timing": "CUDA events, L2 flushed before each step (100 steps)"}
     if with_cpu:
         res[name]["cpu_baseline"] = cpu_baseline(q, k, v, g, B, H, N, budget_s=5.0)
+
+
+def _causal_poly(la, torch, dev, flush, peaks, with_cpu, res):
+    """Causal fwd + bwd with the degree-2 polynomial kernel sim = (q . k)^2 on
+    the 3072-token shape with 8-wide heads (36 features): q, k, v, out, den
+    in and out once, 872 bytes per token-head."""
+    from kernelized_causal_attention_gb300.workloads import causal_inputs
+    B, H, N, D, M = 4, 8, 3072, 8, 64
+    q, k, v, g = causal_inputs(B, H, N, D, M, "bf16", 12)
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+    out = torch.empty_like(vd)
+    den = torch.empty(B, H, N, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    wf = la.workspace(la.LA_OP_CAUSAL_FWD_POLY, B, H, N, D, M, 1, dev)
+    wb = la.workspace(la.LA_OP_CAUSAL_BWD_POLY, B, H, N, D, M, 1, dev)
+    fwd = lambda: la.la_causal_fwd_poly(qd, kd, vd, out, den, wf, B, H, N, D, M, 1)
+    bwd = lambda: la.la_causal_bwd_poly(qd, kd, vd, out, den, gd, dq, dk, dv, wb, B, H, N, D, M, 1)
+    for _ in range(3):
+        fwd()
+        bwd()
+    (mf, mb), ms = time_calls([fwd, bwd], 100, flush, torch, None, dev)
+    fb, bb = causal_bytes(B, H, N, D, M, 2)
+    gbs = (fb + bb) / (ms / 1e3) / 1e9
+    res["causal_poly_bf16"] = {
+        "value": round(B * N / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+        "fwd_ms": round(mf, 5), "bwd_ms": round(mb, 5), "B": B, "H": H, "N": N, "D": D, "M": M,
+        "features": D * (D + 1) // 2,
+        "launches": la.la_kernel_launches(la.LA_OP_CAUSAL_FWD_POLY, B, H, N, D, M, 1)
+        + la.la_kernel_launches(la.LA_OP_CAUSAL_BWD_POLY, B, H, N, D, M, 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": fb + bb,
+                     "bytes_per_token_head": (fb + bb) // (B * H * N)},
+        "timing": "CUDA events, L2 flushed before each step (100 steps)"}
+    if with_cpu:
+        import oracle
+        cores = _cores(oracle)
+        q1, k1, v1, g1 = (t[:1] for t in (q, k, v, g))  # one batch entry: H sequences
+        t0 = time.perf_counter()
+        oracle.causal_fwd_poly(q1, k1, v1, nthreads=cores)
+        oracle.causal_bwd_poly(q1, k1, v1, g1, nthreads=cores)
+        el = time.perf_counter() - t0
+        res["causal_poly_bf16"]["cpu_baseline"] = {
+            "value": round(N / el, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"one batch entry (H={H} sequences of N={N}), fwd+bwd pairwise form, {el:.1f} s"}
 
 
 def _noncausal(la, torch, dev, flush, peaks, with_cpu, res):

@@ -84,6 +84,8 @@ enum { LA_F32 = 0, LA_BF16 = 1 };
 #define LA_OP_CAUSAL_FWD_DECAY 6
 #define LA_OP_CAUSAL_BWD_DECAY 7
 #define LA_OP_DECODE_PROJ 8 /* the N argument is d_model */
+#define LA_OP_CAUSAL_FWD_POLY 9
+#define LA_OP_CAUSAL_BWD_POLY 10
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* la_status_string(la_status status);
@@ -230,6 +232,28 @@ la_status la_causal_bwd_decay(const void* q, const void* k, const void* v, const
 la_status la_decode_step_decay(const void* q, const void* k, const void* v, float* S, float* Z,
                                void* y, float gamma, int B, int H, int D, int M, la_dtype dtype,
                                void* stream);
+
+/*
+ * Causal linear attention with the degree-2 polynomial kernel ("Transformers
+ * are RNNs", part 2/3, the feature-map discussion before eq. 7: an exact finite
+ * feature map, O(N D^2 M) at degree 2), read as sim(q, k) = (q . k)^2 in
+ * eq. 8-12 with no elu feature map:
+ *   out_i = sum_{j<=i} (Q_i . K_j)^2 V_j / den_i,  den_i = sum_{j<=i} (Q_i . K_j)^2,
+ * and its gradients.  bf16 only (LA_F32 gives LA_ERR_UNSUPPORTED); D in [1, 10]
+ * (the D (D + 1) / 2 features fill at most a 64-wide row; larger D gives
+ * LA_ERR_UNSUPPORTED); M in {16, 32, 64}; q, k [B][H][N][D], v, out, dout, dv
+ * [B][H][N][M], den [B][H][N] float (may be NULL in the forward).  A
+ * denominator of zero (every Q_i . K_j = 0 for j <= i) gives a non-finite row.
+ * Workspace: la_workspace_bytes(LA_OP_CAUSAL_FWD_POLY / _BWD_POLY, ...) bytes
+ * (it holds the feature rows); errors and the rest as la_causal_fwd / _bwd.
+ */
+la_status la_causal_fwd_poly(const void* q, const void* k, const void* v, void* out, float* den,
+                             void* workspace, size_t workspace_bytes, int B, int H, int N, int D,
+                             int M, la_dtype dtype, void* stream);
+la_status la_causal_bwd_poly(const void* q, const void* k, const void* v, const void* out,
+                             const float* den, const void* dout, void* dq, void* dk, void* dv,
+                             void* workspace, size_t workspace_bytes, int B, int H, int N, int D,
+                             int M, la_dtype dtype, void* stream);
 
 /*
  * One RNN decode step fed by its own projection: "Transformers are RNNs"

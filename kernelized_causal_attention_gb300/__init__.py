@@ -11,9 +11,11 @@ Raw entry points (same names and argument order as the C ABI, tensors in
 place of pointers): ``la_causal_fwd``, ``la_causal_bwd``, ``la_causal_prefill``,
 ``la_noncausal_fwd``, ``la_noncausal_bwd``, ``la_decode_step``, the decayed
 ``la_causal_fwd_decay``, ``la_causal_bwd_decay``, ``la_decode_step_decay``, the projected
-``la_decode_step_proj``, ``la_workspace_bytes``, ``la_device_status``.
+``la_decode_step_proj``, the degree-2 polynomial ``la_causal_fwd_poly``,
+``la_causal_bwd_poly``, ``la_workspace_bytes``, ``la_device_status``.
 Convenience wrappers that allocate outputs with torch: ``causal_fwd``,
-``causal_bwd``, ``causal_prefill``, ``noncausal_fwd``, ``noncausal_bwd``, ``decode_step``, ``decode_step_proj`` and the
+``causal_bwd``, ``causal_prefill``, ``noncausal_fwd``, ``noncausal_bwd``, ``decode_step``, ``decode_step_proj``,
+``causal_fwd_poly``, ``causal_bwd_poly`` and the
 autograd functions ``causal_linear_attention`` / ``noncausal_linear_attention``.
 
 The method is Katharopoulos et al., "Transformers are RNNs" (part 2/3):
@@ -33,7 +35,8 @@ LIB_PATH = os.path.join(_HERE, "_lib", "liblinattn.so")
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
 LA_F32, LA_BF16 = 0, 1
 (LA_OP_CAUSAL_FWD, LA_OP_CAUSAL_BWD, LA_OP_NONCAUSAL_FWD, LA_OP_NONCAUSAL_BWD, LA_OP_DECODE,
- LA_OP_CAUSAL_PREFILL, LA_OP_CAUSAL_FWD_DECAY, LA_OP_CAUSAL_BWD_DECAY, LA_OP_DECODE_PROJ) = range(9)
+ LA_OP_CAUSAL_PREFILL, LA_OP_CAUSAL_FWD_DECAY, LA_OP_CAUSAL_BWD_DECAY, LA_OP_DECODE_PROJ,
+ LA_OP_CAUSAL_FWD_POLY, LA_OP_CAUSAL_BWD_POLY) = range(11)
 
 # exported symbols and their ctypes signatures ("p" pointer, "i" int, "z" size_t,
 # "u" unsigned long long)
@@ -52,6 +55,8 @@ _SIGS = {
     "la_causal_bwd_decay": ("p p p p p p p p p f p z i i i i i i p", ctypes.c_int),
     "la_decode_step_decay": ("p p p p p p f i i i i i p", ctypes.c_int),
     "la_decode_step_proj": ("p p p p p i i i i i i p", ctypes.c_int),
+    "la_causal_fwd_poly": ("p p p p p p z i i i i i i p", ctypes.c_int),
+    "la_causal_bwd_poly": ("p p p p p p p p p p z i i i i i i p", ctypes.c_int),
     "la_causal_fwd_noalloc": ("p p p p p i i i i i i p", ctypes.c_int),
     "la_device_status": ("p i p", ctypes.c_int),
     "la_selftest_wait": ("p u", ctypes.c_int),
@@ -202,6 +207,19 @@ def la_decode_step_decay(q, k, v, S, Z, y, gamma, B, H, D, M, dtype, stream=None
                                       H, D, M, dtype, _stream(stream)), "la_decode_step_decay")
 
 
+def la_causal_fwd_poly(q, k, v, out, den, workspace, B, H, N, D, M, dtype, stream=None):
+    _check(lib().la_causal_fwd_poly(_p(q), _p(k), _p(v), _p(out), _p(den), _p(workspace),
+                                    _nbytes(workspace), B, H, N, D, M, dtype, _stream(stream)),
+           "la_causal_fwd_poly")
+
+
+def la_causal_bwd_poly(q, k, v, out, den, dout, dq, dk, dv, workspace, B, H, N, D, M, dtype,
+                       stream=None):
+    _check(lib().la_causal_bwd_poly(_p(q), _p(k), _p(v), _p(out), _p(den), _p(dout), _p(dq), _p(dk),
+                                    _p(dv), _p(workspace), _nbytes(workspace), B, H, N, D, M, dtype,
+                                    _stream(stream)), "la_causal_bwd_poly")
+
+
 def la_decode_step_proj(x, W, S, Z, y, B, H, d_model, D, M, dtype, stream=None):
     _check(lib().la_decode_step_proj(_p(x), _p(W), _p(S), _p(Z), _p(y), B, H, d_model, D, M, dtype,
                                      _stream(stream)), "la_decode_step_proj")
@@ -277,6 +295,30 @@ def causal_bwd_decay(q, k, v, out, den, dout, gamma, stream=None):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = workspace(LA_OP_CAUSAL_BWD_DECAY, B, H, N, D, M, dt, q.device)
     la_causal_bwd_decay(q, k, v, out, den, dout, dq, dk, dv, gamma, ws, B, H, N, D, M, dt, stream)
+    return dq, dk, dv
+
+
+def causal_fwd_poly(q, k, v, stream=None):
+    """(out, den) of causal attention with the degree-2 polynomial kernel
+    sim = (q . k)^2 (bf16, D <= 10)."""
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    out = torch.empty(B, H, N, M, dtype=q.dtype, device=q.device)
+    den = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+    ws = workspace(LA_OP_CAUSAL_FWD_POLY, B, H, N, D, M, dt, q.device)
+    la_causal_fwd_poly(q, k, v, out, den, ws, B, H, N, D, M, dt, stream)
+    return out, den
+
+
+def causal_bwd_poly(q, k, v, out, den, dout, stream=None):
+    """(dq, dk, dv) of sum(dout * out) with the degree-2 polynomial kernel."""
+    B, H, N, D = q.shape
+    M = v.shape[-1]
+    dt = _dtype_code(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = workspace(LA_OP_CAUSAL_BWD_POLY, B, H, N, D, M, dt, q.device)
+    la_causal_bwd_poly(q, k, v, out, den, dout, dq, dk, dv, ws, B, H, N, D, M, dt, stream)
     return dq, dk, dv
 
 

@@ -66,6 +66,25 @@ int from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
 // The RetNet decay must lie in [0, 1] (a NaN fails both comparisons).
 int check_gamma(float gamma) { return (gamma >= 0.f && gamma <= 1.f) ? LA_OK : LA_ERR_INVALID_ARG; }
 
+// Workspace of the polynomial calls (their own op ids: the features live there).
+int check_ws_poly(int op, const Shape& s, const void* ws, size_t bytes) {
+  const size_t need = la::causal_poly_ws_bytes(s, op == LA_OP_CAUSAL_BWD_POLY);
+  if (ws == nullptr || bytes < need) return LA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LA_ERR_INVALID_ARG;
+  return LA_OK;
+}
+
+// The degree-2 polynomial kernel: D in [1, 10] (its D (D + 1) / 2 features fit
+// a 64-wide row), M as elsewhere, bf16 (the tensor-core path).
+int check_poly(int B, int H, int N, int D, int M, int dtype) {
+  if (B < 1 || H < 1 || N < 1 || D < 1 || M < 1) return LA_ERR_INVALID_ARG;
+  if ((long long)B * H > 65535 || N > (1 << 24)) return LA_ERR_INVALID_ARG;
+  if ((long long)B * H * N > (1ll << 31)) return LA_ERR_INVALID_ARG;  // the feature kernels' grids
+  if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
+  if (D > la::POLY_MAX_D || !supported_dim(M) || dtype != LA_BF16) return LA_ERR_UNSUPPORTED;
+  return LA_OK;
+}
+
 // The projected decode step: B*H streams as for the decode step, H grid rows,
 // d_model whole slabs of 64, bf16 only.
 int check_proj(int B, int H, int dm, int D, int M, int dtype) {
@@ -114,12 +133,20 @@ int la_version(void) { return 200; }
 
 size_t la_workspace_bytes(int op, int B, int H, int N, int D, int M, int dtype) {
   if (op == LA_OP_DECODE || op == LA_OP_DECODE_PROJ) return 0;
+  if (op == LA_OP_CAUSAL_FWD_POLY || op == LA_OP_CAUSAL_BWD_POLY) {
+    if (check_poly(B, H, N, D, M, dtype) != LA_OK) return 0;
+    return la::causal_poly_ws_bytes(Shape{B, H, N, D, M, dtype}, op == LA_OP_CAUSAL_BWD_POLY);
+  }
   if (check_shape(B, H, N, D, M, dtype) != LA_OK) return 0;
   return ws_bytes(op, Shape{B, H, N, D, M, dtype});
 }
 
 int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype) {
   if (op == LA_OP_DECODE_PROJ) return check_proj(B, H, N, D, M, dtype) == LA_OK ? 1 : 0;
+  if (op == LA_OP_CAUSAL_FWD_POLY || op == LA_OP_CAUSAL_BWD_POLY)
+    return check_poly(B, H, N, D, M, dtype) == LA_OK
+               ? la::causal_poly_launches(Shape{B, H, N, D, M, dtype}, op == LA_OP_CAUSAL_BWD_POLY)
+               : 0;
   if (check_shape(B, H, op == LA_OP_DECODE ? 1 : N, D, M, dtype,
                   op == LA_OP_DECODE ? (1ll << 20) : 65535) != LA_OK)
     return 0;
@@ -253,6 +280,29 @@ int la_decode_step_proj(const void* x, const void* W, float* S, float* Z, void* 
   LA_TRY(check_ptrs({x, W, S, Z, y}));
   return from_cuda(la::decode_step_proj(x, W, S, Z, y, B, H, d_model, D, M,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+int la_causal_fwd_poly(const void* q, const void* k, const void* v, void* out, float* den,
+                       void* workspace, size_t workspace_bytes, int B, int H, int N, int D, int M,
+                       int dtype, void* stream) {
+  LA_TRY(check_poly(B, H, N, D, M, dtype));
+  LA_TRY(check_ptrs({q, k, v, out}));
+  LA_TRY(check_opt_ptr(den));
+  const Shape s{B, H, N, D, M, dtype};
+  LA_TRY(check_ws_poly(LA_OP_CAUSAL_FWD_POLY, s, workspace, workspace_bytes));
+  return from_cuda(la::causal_fwd_poly(q, k, v, out, den, workspace, s, static_cast<cudaStream_t>(stream)));
+}
+
+int la_causal_bwd_poly(const void* q, const void* k, const void* v, const void* out, const float* den,
+                       const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                       size_t workspace_bytes, int B, int H, int N, int D, int M, int dtype,
+                       void* stream) {
+  LA_TRY(check_poly(B, H, N, D, M, dtype));
+  LA_TRY(check_ptrs({q, k, v, out, den, dout, dq, dk, dv}));
+  const Shape s{B, H, N, D, M, dtype};
+  LA_TRY(check_ws_poly(LA_OP_CAUSAL_BWD_POLY, s, workspace, workspace_bytes));
+  return from_cuda(la::causal_bwd_poly(q, k, v, out, den, dout, dq, dk, dv, workspace, s,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 int la_decode_step(const void* q, const void* k, const void* v, float* S, float* Z, void* y,

@@ -82,7 +82,8 @@ constexpr int W_PHI0 = 2, W_MASK0 = 10, W_EPI0 = 14;
 // ws[bh][p] ([64][80] fp32) for every segment p but the last.
 __global__ void __launch_bounds__(NTHR, 1)
     k_tc_fwd_state(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   float* __restrict__ ws, int N, int nseg, int seg_len, int dch, int* err) {
+                   float* __restrict__ ws, int N, int nseg, int seg_len, int dch, int feat,
+                   int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int c = 0; c < nch; ++c) {
       const int s = c % SNST;
       if (wt(&bar_full[s], (c / SNST) & 1, 33))
-        phi_tiles<NCOMP, 1>(sm + s * S_STAGE, 0, min(TC_C, ne - (nb + c * TC_C)), t, dch);
+        phi_tiles<NCOMP, 1>(sm + s * S_STAGE, 0, min(TC_C, ne - (nb + c * TC_C)), t, dch, feat != 0);
       fence_proxy_async();
       mbar_arrive(&bar_phi[s]);
     }
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     k_tc_fwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ out,
                   float* __restrict__ den, const float* __restrict__ ws, int N, int nseg,
-                  int seg_len, int out_v8, int dch, int M, int* err, const float* __restrict__ S0,
+                  int seg_len, int out_v8, int dch, int M, int feat, int* err, const float* __restrict__ S0,
                   const float* __restrict__ Z0) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ uint8_t smraw[];
@@ -407,7 +408,8 @@ __global__ void __launch_bounds__(NTHR, 1)
         uint32_t pq[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint4 r = row < valid && 4 * h + i < dch ? phi_vec(qv[i]) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 r = row < valid && 4 * h + i < dch ? (feat ? qv[i] : phi_vec(qv[i]))
+                                                         : make_uint4(0u, 0u, 0u, 0u);
           pq[4 * i] = r.x;
           pq[4 * i + 1] = r.y;
           pq[4 * i + 2] = r.z;
@@ -418,7 +420,8 @@ __global__ void __launch_bounds__(NTHR, 1)
         for (int i = 0; i < 4; ++i) {
           const int v = tt + i * NT;
           const bool pad = (v >> 3) >= valid || (((v & 7) ^ ((v >> 3) & 7)) >= dch);
-          *reinterpret_cast<uint4*>(st + v * 16) = pad ? make_uint4(0u, 0u, 0u, 0u) : phi_vec(kv[i]);
+          *reinterpret_cast<uint4*>(st + v * 16) =
+              pad ? make_uint4(0u, 0u, 0u, 0u) : (feat ? kv[i] : phi_vec(kv[i]));
         }
         tmem_st_wait();
       }
@@ -698,7 +701,7 @@ namespace {
 // whose sums start from (S0, Z0) when S0 is not null.
 cudaError_t fwd_tc_launch(const void* q, const void* k, const void* v, void* out, float* den,
                           float* ws, const Shape& s, cudaStream_t st, const float* S0,
-                          const float* Z0, bool all_records) {
+                          const float* Z0, bool all_records, bool feat = false) {
   const int BH = s.B * s.H;
   const SegPlan pl = tc_plan(BH, s.N);
   CUtensorMap mq, mk, mv;
@@ -717,12 +720,12 @@ cudaError_t fwd_tc_launch(const void* q, const void* k, const void* v, void* out
   const int nrec = all_records ? pl.nseg : pl.nseg - 1;
   if (nrec > 0) {
     if ((e = launch_pdl(k_tc_fwd_state, dim3(nrec, BH), dim3(NTHR), S_SMEM, st, mk, mv, ws,
-                        s.N, pl.nseg, pl.seg_len, s.D / 8, err)) != cudaSuccess)
+                        s.N, pl.nseg, pl.seg_len, s.D / 8, feat ? 1 : 0, err)) != cudaSuccess)
       return e;
   }
   if ((e = launch_pdl(k_tc_fwd_main, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv,
                       static_cast<bf16*>(out), den, static_cast<const float*>(ws), s.N, pl.nseg,
-                      pl.seg_len, out_v8, s.D / 8, s.M, err, S0, Z0)) != cudaSuccess)
+                      pl.seg_len, out_v8, s.D / 8, s.M, feat ? 1 : 0, err, S0, Z0)) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }
@@ -730,8 +733,8 @@ cudaError_t fwd_tc_launch(const void* q, const void* k, const void* v, void* out
 }  // namespace
 
 cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out, float* den,
-                          float* ws, const Shape& s, cudaStream_t st) {
-  return fwd_tc_launch(q, k, v, out, den, ws, s, st, nullptr, nullptr, false);
+                          float* ws, const Shape& s, cudaStream_t st, bool feat) {
+  return fwd_tc_launch(q, k, v, out, den, ws, s, st, nullptr, nullptr, false, feat);
 }
 
 // The state pass writes every segment's record, the main pass adds (S, Z) to

@@ -85,7 +85,7 @@ struct BwdMaps {
 __global__ void __launch_bounds__(NTHR, 1)
     k_tc_bwd_main(const __grid_constant__ BwdMaps maps, const float* __restrict__ rec,
                   const float* __restrict__ gam, int N, int seg_len, int nsub, int subs_per_seg,
-                  int* err) {
+                  int feat, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;
   const int role = static_cast<int>(blockIdx.z);  // 0 dq, 1 dk / dv
   extern __shared__ uint8_t smraw[];
@@ -375,12 +375,12 @@ __global__ void __launch_bounds__(NTHR, 1)
         if (role == 0) {  // dq = (grad_phiQ + gam z_prev) * phi'(Q)
           tile_row_cols<OW>(st, row, c0, x);
 #pragma unroll
-          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + gm * vcur[c0 + i]) * fminf(x[i], 1.f);
+          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + gm * vcur[c0 + i]) * (feat ? 1.f : fminf(x[i], 1.f));
           tile_put_cols<OW>(sm + M_DP, row, c0, gv);
         } else {          // dk = (grad_phiK + r_next) * phi'(K), dv
           tile_row_cols<OW>(st + TILE, row, c0, x);
 #pragma unroll
-          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + vcur[c0 + i]) * fminf(x[i], 1.f);
+          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + vcur[c0 + i]) * (feat ? 1.f : fminf(x[i], 1.f));
           tile_put_cols<OW>(sm + M_P, row, c0, gv);
           tmem_ldn<OW / 16>(TG2 + lq + c0, gv);
           tile_put_cols<OW>(sm + M_P + TILE, row, c0, gv);
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     k_tc_bwd_state(const __grid_constant__ StateMaps maps, const float* __restrict__ den,
                    float* __restrict__ gam, bf16* __restrict__ gt_out, bf16* __restrict__ fq_out,
                    bf16* __restrict__ fk_out, float* __restrict__ rec, int N, int sub_len, int nsub,
-                   int dch, int* err) {
+                   int dch, int feat, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;  // the call's first kernel
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(NTHR, 1)
           // features of a head narrower than 64: phi(0) = 1 would add them)
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
-            const uint4 f = rv && lc < dch ? phi_vec(x[k][i]) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 f = rv && lc < dch ? (feat ? x[k][i] : phi_vec(x[k][i])) : make_uint4(0u, 0u, 0u, 0u);
             *reinterpret_cast<uint4*>(st + k * TILE + v * 16) = f;
             if (rv) *reinterpret_cast<uint4*>((k == 0 ? fq_out : fk_out) + gofs) = f;
           }
@@ -709,7 +709,7 @@ int causal_bwd_tc_launches(const Shape&) { return 2; }
 
 cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const void* out,
                           const float* den, const void* dout, void* dq, void* dk, void* dv,
-                          float* ws, const Shape& s, cudaStream_t st) {
+                          float* ws, const Shape& s, cudaStream_t st, bool feat) {
   const int BH = s.B * s.H;
   const BwdPlan pl = bwd_plan(BH, s.N);
   const BwdWs w = bwd_ws(ws, BH, s.N, pl);
@@ -737,11 +737,12 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
                                 M_SMEM)) != cudaSuccess)
     return e;
   if ((e = launch_pdl(k_tc_bwd_state, dim3(pl.nsub, BH), dim3(NTHR), SS_SMEM, st, smap, den, w.gam,
-                      w.gt, w.fq, w.fk, w.rec, s.N, pl.sub_len, pl.nsub, s.D / 8, status_word())) != cudaSuccess)
+                      w.gt, w.fq, w.fk, w.rec, s.N, pl.sub_len, pl.nsub, s.D / 8, feat ? 1 : 0,
+                      status_word())) != cudaSuccess)
     return e;
   if ((e = launch_pdl(k_tc_bwd_main, dim3(pl.main.nseg, BH, 2), dim3(NTHR), M_SMEM, st, m,
                       static_cast<const float*>(w.rec), static_cast<const float*>(w.gam), s.N,
-                      pl.main.seg_len, pl.nsub, pl.subs, status_word())) != cudaSuccess)
+                      pl.main.seg_len, pl.nsub, pl.subs, feat ? 1 : 0, status_word())) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }

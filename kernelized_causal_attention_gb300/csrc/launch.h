@@ -83,19 +83,34 @@ cudaError_t causal_prefill_cc(const void* q, const void* k, const void* v, void*
 cudaError_t causal_prefill_tc(const void* q, const void* k, const void* v, void* out, float* den,
                               float* S, float* Z, float* ws, const Shape& s, cudaStream_t st);
 
-// tcgen05 path (bf16, D = M = 64).
+// tcgen05 path (bf16, D and M in {16, 32, 64}).
 SegPlan tc_plan(int BH, int N);
 bool tc_eligible(const Shape& s);          // causal fwd / bwd on the tensor cores
 bool tc_prefill_eligible(const Shape& s);  // the prefill on the tensor cores (D = M = 64)
 size_t causal_fwd_tc_ws_floats(const Shape& s);
 int causal_fwd_tc_launches(const Shape& s);
+// feat: q and k already hold features (a feature map applied before the call,
+// e.g. the degree-2 polynomial one); the kernels then apply no phi.
 cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out, float* den,
-                          float* ws, const Shape& s, cudaStream_t st);
+                          float* ws, const Shape& s, cudaStream_t st, bool feat = false);
 size_t causal_bwd_tc_ws_floats(const Shape& s);
 int causal_bwd_tc_launches(const Shape& s);
 cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const void* out,
                           const float* den, const void* dout, void* dq, void* dk, void* dv,
-                          float* ws, const Shape& s, cudaStream_t st);
+                          float* ws, const Shape& s, cudaStream_t st, bool feat = false);
+
+// The degree-2 polynomial kernel (poly.cu): features f(x) = [x_a^2, sqrt(2)
+// x_a x_b (a < b)] zero-padded to 64, then the tensor-core kernels with
+// feat = true; D in [1, 10], bf16.  Workspace: the feature tensors (and
+// their gradients) followed by the tensor-core workspace.
+constexpr int POLY_MAX_D = 10;
+size_t causal_poly_ws_bytes(const Shape& s, bool bwd);
+int causal_poly_launches(const Shape& s, bool bwd);
+cudaError_t causal_fwd_poly(const void* q, const void* k, const void* v, void* out, float* den,
+                            void* ws, const Shape& s, cudaStream_t st);
+cudaError_t causal_bwd_poly(const void* q, const void* k, const void* v, const void* out,
+                            const float* den, const void* dout, void* dq, void* dk, void* dv,
+                            void* ws, const Shape& s, cudaStream_t st);
 
 // CUDA-core (FFMA) paths; every kernel of the library is launched from these.
 // gamma: the RetNet decay in [0, 1] (1 = the undecayed method).

@@ -100,8 +100,11 @@ __device__ __forceinline__ uint4 phi_vec(uint4 u) {
 // `valid` are zeroed: a zero phi row adds nothing to any sum.  So are the
 // columns at or past 8 dch (a head narrower than 64 whose tile the load
 // filled with zeros: phi(0) = 1, but a padded feature must add nothing).
+// ident: the tiles already hold features (a feature map applied before the
+// call); only the masking applies.
 template <int NT, int NTL>
-__device__ __forceinline__ void phi_tiles(uint8_t* tile, int stride, int valid, int t, int dch = 8) {
+__device__ __forceinline__ void phi_tiles(uint8_t* tile, int stride, int valid, int t, int dch = 8,
+                                          bool ident = false) {
   constexpr int PER = TILE / 16 / NT;  // vectors per thread and tile
   static_assert(PER * NT * 16 == TILE, "threads must divide the tile");
   uint4 u[NTL][PER];
@@ -116,7 +119,7 @@ __device__ __forceinline__ void phi_tiles(uint8_t* tile, int stride, int valid, 
     for (int i = 0; i < PER; ++i) {
       const int v = t + i * NT;
       const bool pad = (v >> 3) >= valid || (((v & 7) ^ ((v >> 3) & 7)) >= dch);
-      const uint4 r = pad ? make_uint4(0u, 0u, 0u, 0u) : phi_vec(u[k][i]);
+      const uint4 r = pad ? make_uint4(0u, 0u, 0u, 0u) : (ident ? u[k][i] : phi_vec(u[k][i]));
       sts128(tile + k * stride + v * 16, r);
     }
 }
