@@ -12,10 +12,11 @@
 // atoms; K = d_model in slabs of 64), its operands brought in by TMA through a
 // three-stage ring (x as K-major tiles, the head's contiguous columns of W as
 // MN-major atoms, both with the 128-byte swizzle) and its accumulator in
-// tensor memory.  While the product runs, every thread already has the first
-// streams' fp32 states in flight from HBM.  The CTA then applies phi, updates
-// the block's states (each read and written once, 16-byte accesses) and reads
-// y out, so q, k and v never leave the SM.
+// tensor memory.  The CTA then applies phi and streams the block's fp32
+// states through a ring of ~32 KB groups in the freed stages (16-byte
+// cp.async, each thread copying and reading back its own pieces), updates
+// them (each read and written once) and reads y out, so q, k and v never
+// leave the SM.
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
@@ -30,10 +31,10 @@ using namespace tcc;
 constexpr int P_NT = 256;    // threads
 constexpr int P_NW = P_NT / 32;
 constexpr int P_KS = 64;     // d_model per slab
-constexpr int P_NS = 3;      // stages of the slab ring
 constexpr int P_SBMAX = 64;  // streams per CTA at most (the MMA's M)
 
-template <int D, int M>
+// NS: stages of the slab ring.
+template <int D, int M, int NS>
 struct ProjGeom {
   static constexpr int NQKV = 2 * D + M;            // one head's q | k | v columns
   static constexpr int NP = (NQKV + 63) / 64 * 64;  // whole 64-column atoms (the MMA's N)
@@ -46,20 +47,27 @@ struct ProjGeom {
   static constexpr int RG = P_NT / M4;              // row groups of the state
   static constexpr int RPT = (D + RG - 1) / RG;     // state rows per thread
   // the states stream through a ring of NG groups of NSTR streams (about
-  // 16 KB a group) in the projection's stages, free once the product is done
-  static constexpr int NSTR = D * M >= 4096 ? 1 : 4096 / (D * M);
+  // 32 KB a group) in the projection's stages, free once the product is done
+  static constexpr int NSTR_RAW = 8192 / (D * M);
+  static constexpr int NSTR_FIT = NS * STAGE / (2 * D * M * 4);  // the ring holds two groups at least
+  static constexpr int NSTR_MIN = NSTR_RAW < NSTR_FIT ? NSTR_RAW : NSTR_FIT;
+  static constexpr int NSTR = NSTR_MIN > 16 ? 16 : (NSTR_MIN < 1 ? 1 : NSTR_MIN);
   static constexpr int GROUP = NSTR * D * M * 4;
-  static constexpr int NG_RAW = P_NS * STAGE / GROUP;
+  static constexpr int NG_RAW = NS * STAGE / GROUP;
   static constexpr int NG = NG_RAW > 8 ? 8 : NG_RAW;
+  // the cross-warp sums of a group, [NSTR][NW][M4] float4, two buffers: the
+  // second in the ring's spare bytes where they suffice
+  static constexpr int RED = NSTR * (P_NT / 32) * (M / 4) * 16;
+  static constexpr bool RED_IN_RING = NS * STAGE - NG * GROUP >= RED;
   static_assert(NG >= 2, "the ring needs two groups");
 };
 
-template <int D, int M>
+template <int D, int M, int NS>
 size_t proj_smem_bytes(int SB) {
-  using G = ProjGeom<D, M>;
-  return 1024 + static_cast<size_t>(P_NS) * G::STAGE + static_cast<size_t>(SB) * G::SQ * 4 +
-         static_cast<size_t>(G::NSTR) * P_NW * G::M4 * 16 + static_cast<size_t>(G::NG) * G::NSTR * D * 4 +
-         G::NSTR * 4;
+  using G = ProjGeom<D, M, NS>;
+  return 1024 + static_cast<size_t>(NS) * G::STAGE + static_cast<size_t>(SB) * G::SQ * 4 +
+         (G::RED_IN_RING ? 1 : 2) * static_cast<size_t>(G::RED) + static_cast<size_t>(G::NG) * G::NSTR * D * 4 +
+         2 * G::NSTR * 4;
 }
 
 // phi(x) = elu(x) + 1 (eq. 7) with the exponential evaluated on both sides
@@ -85,29 +93,34 @@ __device__ __forceinline__ float comp(const float4& a, int i) {
   return i == 0 ? a.x : (i == 1 ? a.y : (i == 2 ? a.z : a.w));
 }
 
-template <int D, int M>
-__global__ void __launch_bounds__(P_NT, 2)
+template <int D, int M, int NS>
+__global__ void __launch_bounds__(P_NT, NS <= 3 ? 2 : 1)
     k_decode_proj(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   float* __restrict__ S, float* __restrict__ Z, bf16* __restrict__ y, int B, int H,
                   int dm, int SB, int* err) {
-  using G = ProjGeom<D, M>;
+  using G = ProjGeom<D, M, NS>;
   const int b0 = blockIdx.x * SB, h = blockIdx.y;
   const int nb = min(SB, B - b0);  // streams of this CTA
   const int nslab = dm / P_KS;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
-  float* sqkv = reinterpret_cast<float*>(sm + P_NS * G::STAGE);  // [SB][SQ]
+  float* sqkv = reinterpret_cast<float*>(sm + NS * G::STAGE);  // [SB][SQ]
+  // the cross-warp sums of a group, double-buffered by group parity: a thread
+  // is at most one group ahead of the slowest (the next group's barrier holds
+  // it), so one barrier a group suffices
   float4* sred = reinterpret_cast<float4*>(sqkv + SB * G::SQ);     // [NSTR][NW][M4]
-  float4* zring = sred + G::NSTR * P_NW * G::M4;                   // [NG][NSTR][D/4]
-  float* sden = reinterpret_cast<float*>(zring + G::NG * G::NSTR * (D / 4));  // [NSTR]
+  float4* sred1 = G::RED_IN_RING ? reinterpret_cast<float4*>(sm + G::NG * G::GROUP)
+                                 : sred + G::NSTR * P_NW * G::M4;  // the second buffer
+  float4* zring = sred + (G::RED_IN_RING ? 1 : 2) * G::NSTR * P_NW * G::M4;  // [NG][NSTR][D/4]
+  float* sden = reinterpret_cast<float*>(zring + G::NG * G::NSTR * (D / 4));  // [2][NSTR]
   float4* ring = reinterpret_cast<float4*>(sm);                    // [NG][NSTR][D*M/4]
-  __shared__ uint64_t bar_full[P_NS], bar_empty[P_NS], bar_done;
+  __shared__ uint64_t bar_full[NS], bar_empty[NS], bar_done;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
 
   if (t == 0) {
-    for (int s = 0; s < P_NS; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
@@ -130,7 +143,7 @@ __global__ void __launch_bounds__(P_NT, 2)
   if (t == 0) {
     const uint32_t tx = static_cast<uint32_t>(SB) * 128u + G::NAT * P_KS * 128u;
     auto issue = [&](int ks) {
-      const int s = ks % P_NS;
+      const int s = ks % NS;
       uint8_t* A = sm + s * G::STAGE;
       mbar_arrive_expect_tx(&bar_full[s], tx);
       tma_load_3d(A, &tmX, &bar_full[s], ks * P_KS, b0, 0);
@@ -140,12 +153,12 @@ __global__ void __launch_bounds__(P_NT, 2)
                     ks * P_KS, 0);
     };
     int issued = 0;
-    for (; issued < P_NS && issued < nslab; ++issued) issue(issued);
+    for (; issued < NS && issued < nslab; ++issued) issue(issued);
     constexpr uint32_t ID = idesc_bf16(P_SBMAX, G::NP, false, true);
     bool good = true;
     for (int ks = 0; ks < nslab; ++ks) {
-      const int s = ks % P_NS;
-      if (!mbar_wait(&bar_full[s], (ks / P_NS) & 1, WAIT_NS)) {
+      const int s = ks % NS;
+      if (!mbar_wait(&bar_full[s], (ks / NS) & 1, WAIT_NS)) {
         fail(err, 61);
         good = false;
         break;
@@ -157,20 +170,20 @@ __global__ void __launch_bounds__(P_NT, 2)
       for (int kk = 0; kk < P_KS / 16; ++kk)
         mma_bf16(tacc, dadd(dA, 32 * kk), dadd(dB, 2048 * kk), ID, (ks > 0 || kk > 0) ? 1u : 0u);
       mma_commit(&bar_empty[s]);
-      if (ks + P_NS < nslab) {  // refill the stage once its products have read it
-        if (!mbar_wait(&bar_empty[s], (ks / P_NS) & 1, WAIT_NS)) {
+      if (ks + NS < nslab) {  // refill the stage once its products have read it
+        if (!mbar_wait(&bar_empty[s], (ks / NS) & 1, WAIT_NS)) {
           fail(err, 62);
           good = false;
           break;
         }
-        issue(ks + P_NS);
+        issue(ks + NS);
         ++issued;
       }
     }
     mma_commit(&bar_done);  // every product issued so far has completed
     if (!good) {
       *reinterpret_cast<volatile int*>(&s_abort) = 1;
-      drain_loads<P_NS>(bar_full, issued);
+      drain_loads<NS>(bar_full, issued);
     }
   }
   __syncwarp();
@@ -237,6 +250,8 @@ __global__ void __launch_bounds__(P_NT, 2)
     cp_async_commit();  // one group per call, empty or not, to keep the count
   };
   auto process = [&](int g) {
+    float4* red = (g & 1) ? sred1 : sred;
+    float* dn = sden + (g & 1) * G::NSTR;
     const float4* slot = ring + (g % G::NG) * (G::NSTR * D * M / 4);
     const float4* zslot = zring + (g % G::NG) * (G::NSTR * D / 4);
     const int j0 = g * G::NSTR;
@@ -272,7 +287,7 @@ __global__ void __launch_bounds__(P_NT, 2)
           acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
           acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
         }
-        if (lane < G::M4) sred[(j * P_NW + warp) * G::M4 + lane] = acc;
+        if (lane < G::M4) red[(j * P_NW + warp) * G::M4 + lane] = acc;
       }
     }
     // z <- z + phi(k) and den = phi(q) . z: warp j % NW, four entries a lane
@@ -289,7 +304,7 @@ __global__ void __launch_bounds__(P_NT, 2)
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, off);
-        if (lane == 0) sden[j] = dp;
+        if (lane == 0) dn[j] = dp;
       }
     }
     __syncthreads();
@@ -298,11 +313,10 @@ __global__ void __launch_bounds__(P_NT, 2)
       if (j0 + j < nb) {
         float num = 0.f;
 #pragma unroll
-        for (int w = 0; w < P_NW; ++w) num += comp(sred[(j * P_NW + w) * G::M4 + m / 4], m & 3);
-        y[(static_cast<long>(b0 + j0 + j) * H + h) * M + m] = __float2bfloat16_rn(num / sden[j]);
+        for (int w = 0; w < P_NW; ++w) num += comp(red[(j * P_NW + w) * G::M4 + m / 4], m & 3);
+        y[(static_cast<long>(b0 + j0 + j) * H + h) * M + m] = __float2bfloat16_rn(num / dn[j]);
       }
     }
-    __syncthreads();
   };
   if (ok) {
     fence_proxy_async();  // the ring reuses stages last touched by TMA and the tensor cores
@@ -322,39 +336,50 @@ __global__ void __launch_bounds__(P_NT, 2)
 
 }  // namespace
 
-// Streams per CTA: the largest block that still gives two CTAs per SM.
-int decode_proj_block(int B, int H) {
-  const long want = 2l * sm_count();
+// Streams per CTA: the largest block that still gives two CTAs per SM, with
+// three stages.  (Six stages at one CTA per SM, for grids that fit one wave,
+// measured slower at 256 streams: 25.0 against 23.4 us.)
+ProjPlan decode_proj_plan(int B, int H) {
+  const long sms = sm_count();
+  auto ctas = [&](int sb) { return static_cast<long>((B + sb - 1) / sb) * H; };
   for (int sb : {64, 32, 16})
-    if (static_cast<long>((B + sb - 1) / sb) * H >= want) return sb;
-  return 8;
+    if (ctas(sb) >= 2 * sms) return ProjPlan{sb, 3};
+  return ProjPlan{8, 3};
 }
+
+int decode_proj_block(int B, int H) { return decode_proj_plan(B, H).SB; }
 
 namespace {
 
-template <int D, int M>
-cudaError_t launch_proj(const CUtensorMap& mx, const CUtensorMap& mw, float* S, float* Z, void* y,
-                        int B, int H, int dm, int SB, cudaStream_t st) {
-  const size_t smem = proj_smem_bytes<D, M>(SB);
-  cudaError_t e = cudaFuncSetAttribute(k_decode_proj<D, M>,
+template <int D, int M, int NS>
+cudaError_t launch_proj_ns(const CUtensorMap& mx, const CUtensorMap& mw, float* S, float* Z, void* y,
+                           int B, int H, int dm, int SB, cudaStream_t st) {
+  const size_t smem = proj_smem_bytes<D, M, NS>(SB);
+  cudaError_t e = cudaFuncSetAttribute(k_decode_proj<D, M, NS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k_decode_proj<D, M><<<dim3((B + SB - 1) / SB, H), P_NT, smem, st>>>(
+  k_decode_proj<D, M, NS><<<dim3((B + SB - 1) / SB, H), P_NT, smem, st>>>(
       mx, mw, S, Z, static_cast<bf16*>(y), B, H, dm, SB, status_word());
   return cudaGetLastError();
+}
+
+template <int D, int M>
+cudaError_t launch_proj(const CUtensorMap& mx, const CUtensorMap& mw, float* S, float* Z, void* y,
+                        int B, int H, int dm, const ProjPlan& pl, cudaStream_t st) {
+  return launch_proj_ns<D, M, 3>(mx, mw, S, Z, y, B, H, dm, pl.SB, st);
 }
 
 }  // namespace
 
 cudaError_t decode_step_proj(const void* x, const void* W, float* S, float* Z, void* y, int B,
                              int H, int dm, int D, int M, cudaStream_t st) {
-  const int SB = decode_proj_block(B, H);
+  const ProjPlan pl = decode_proj_plan(B, H);
   const long wcols = static_cast<long>(H) * (2 * D + M);
   CUtensorMap mx, mw;
-  if (!make_bf16_map_2d(&mx, x, dm, B, SB) || !make_bf16_map_2d(&mw, W, wcols, dm, P_KS))
+  if (!make_bf16_map_2d(&mx, x, dm, B, pl.SB) || !make_bf16_map_2d(&mw, W, wcols, dm, P_KS))
     return cudaErrorInvalidValue;
-  LA_DISPATCH_DM(D, M, return (launch_proj<D_, M_>(mx, mw, S, Z, y, B, H, dm, SB, st)));
+  LA_DISPATCH_DM(D, M, return (launch_proj<D_, M_>(mx, mw, S, Z, y, B, H, dm, pl, st)));
   return cudaErrorInvalidValue;
 }
 

@@ -142,6 +142,11 @@ cudaError_t decode_step(const void* q, const void* k, const void* v, float* S, f
 // [dm][H (2D+M)] in bf16, d_model dm a multiple of 64; streams per CTA.
 cudaError_t decode_step_proj(const void* x, const void* W, float* S, float* Z, void* y, int B,
                              int H, int dm, int D, int M, cudaStream_t st);
+struct ProjPlan {
+  int SB;  // streams per CTA
+  int NS;  // stages of the slab ring
+};
+ProjPlan decode_proj_plan(int B, int H);
 int decode_proj_block(int B, int H);
 
 }  // namespace la
