@@ -512,6 +512,8 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True, only=None):
     for name in ("causal_mnist_bf16", "causal_cifar_d32_bf16"):
         if want(name):
             _causal_line(la, torch, dev, flush, peaks, with_cpu, res, name)
+    if want("causal_decay_bf16"):
+        _causal_decay(la, torch, dev, flush, peaks, with_cpu, res)
     if want("causal_poly_bf16"):
         _causal_poly(la, torch, dev, flush, peaks, with_cpu, res)
     if want("noncausal_speech_f32"):
@@ -536,7 +538,7 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True, only=None):
     return res
 
 
-SECONDARY = ("causal_mnist_bf16", "causal_cifar_d32_bf16", "causal_poly_bf16", "noncausal_speech_f32", "prefill_cifar_bf16", "decode_f32",
+SECONDARY = ("causal_mnist_bf16", "causal_cifar_d32_bf16", "causal_decay_bf16", "causal_poly_bf16", "noncausal_speech_f32", "prefill_cifar_bf16", "decode_f32",
              "decode_proj_bf16", "decode_proj_mnist_bf16", "sweep_causal_bf16")
 
 
@@ -572,6 +574,50 @@ def _causal_line(la, torch, dev, flush, peaks, with_cpu, res, name):
         "timing": "CUDA events, L2 flushed before each step (100 steps)"}
     if with_cpu:
         res[name]["cpu_baseline"] = cpu_baseline(q, k, v, g, B, H, N, budget_s=5.0)
+
+
+def _causal_decay(la, torch, dev, flush, peaks, with_cpu, res, gamma=0.99):
+    """Causal fwd + bwd with the RetNet decay gamma on the 3072-token image
+    workload (the same 1544 bytes per token-head as the undecayed step)."""
+    from kernelized_causal_attention_gb300.workloads import WORKLOADS, causal_inputs
+    w = WORKLOADS["causal_cifar_bf16"]
+    B, H, N, D, M = w.B, w.H, w.N, w.D, w.M
+    q, k, v, g = causal_inputs(B, H, N, D, M, w.dtype, w.seed)
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+    out = torch.empty_like(vd)
+    den = torch.empty(B, H, N, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    wf = la.workspace(la.LA_OP_CAUSAL_FWD_DECAY, B, H, N, D, M, 1, dev)
+    wb = la.workspace(la.LA_OP_CAUSAL_BWD_DECAY, B, H, N, D, M, 1, dev)
+    fwd = lambda: la.la_causal_fwd_decay(qd, kd, vd, out, den, gamma, wf, B, H, N, D, M, 1)
+    bwd = lambda: la.la_causal_bwd_decay(qd, kd, vd, out, den, gd, dq, dk, dv, gamma, wb, B, H, N, D,
+                                         M, 1)
+    for _ in range(3):
+        fwd()
+        bwd()
+    (mf, mb), ms = time_calls([fwd, bwd], 50, flush, torch, None, dev)
+    fb, bb = causal_bytes(B, H, N, D, M, 2)
+    gbs = (fb + bb) / (ms / 1e3) / 1e9
+    res["causal_decay_bf16"] = {
+        "value": round(B * N / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+        "fwd_ms": round(mf, 5), "bwd_ms": round(mb, 5), "gamma": gamma,
+        "B": B, "H": H, "N": N, "D": D, "M": M,
+        "launches": la.la_kernel_launches(la.LA_OP_CAUSAL_FWD_DECAY, B, H, N, D, M, 1)
+        + la.la_kernel_launches(la.LA_OP_CAUSAL_BWD_DECAY, B, H, N, D, M, 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": fb + bb},
+        "timing": "CUDA events, L2 flushed before each step (50 steps)"}
+    if with_cpu:
+        import oracle
+        cores = _cores(oracle)
+        q1, k1, v1, g1 = (t[:1] for t in (q, k, v, g))  # one batch entry: H sequences
+        t0 = time.perf_counter()
+        oracle.causal_fwd(q1, k1, v1, "recurrent", nthreads=cores, gamma=gamma)
+        oracle.causal_bwd(q1, k1, v1, g1, "recurrent", nthreads=cores, gamma=gamma)
+        el = time.perf_counter() - t0
+        res["causal_decay_bf16"]["cpu_baseline"] = {
+            "value": round(N / el, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"one batch entry (H={H} sequences of N={N}), fwd+bwd recurrent form, {el:.2f} s"}
 
 
 def _causal_poly(la, torch, dev, flush, peaks, with_cpu, res):
