@@ -80,10 +80,11 @@ constexpr int W_PHI0 = 2, W_MASK0 = 10, W_EPI0 = 14;
 // ------------------------------------------------------------- state pass
 // Partial state dS~ = sum over the segment of phi(K) V~^T, written to
 // ws[bh][p] ([64][80] fp32) for every segment p but the last.
+template <bool DECAY>
 __global__ void __launch_bounds__(NTHR, 1)
     k_tc_fwd_state(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    float* __restrict__ ws, int N, int nseg, int seg_len, int dch, int feat,
-                   int* err) {
+                   float lg, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -168,7 +169,8 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int c = 0; c < nch; ++c) {
       const int s = c % SNST;
       if (wt(&bar_full[s], (c / SNST) & 1, 33))
-        phi_tiles<NCOMP, 1>(sm + s * S_STAGE, 0, min(TC_C, ne - (nb + c * TC_C)), t, dch, feat != 0);
+        phi_tiles<NCOMP, 1>(sm + s * S_STAGE, 0, min(TC_C, ne - (nb + c * TC_C)), t, dch, feat != 0,
+                            DECAY ? lg : 0.f, (ne - 1) - (nb + c * TC_C));  // decay: phi(K_j) gamma^(ne-1-j)
       fence_proxy_async();
       mbar_arrive(&bar_phi[s]);
     }
@@ -209,11 +211,13 @@ __global__ void __launch_bounds__(NTHR, 1)
 }
 
 // -------------------------------------------------------------- main pass
+template <bool DECAY>
 __global__ void __launch_bounds__(NTHR, 1)
     k_tc_fwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ out,
                   float* __restrict__ den, const float* __restrict__ ws, int N, int nseg,
-                  int seg_len, int out_v8, int dch, int M, int feat, int* err, const float* __restrict__ S0,
+                  int seg_len, int out_v8, int dch, int M, int feat, float lg, int* err,
+                  const float* __restrict__ S0,
                   const float* __restrict__ Z0) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ uint8_t smraw[];
@@ -420,8 +424,10 @@ __global__ void __launch_bounds__(NTHR, 1)
         for (int i = 0; i < 4; ++i) {
           const int v = tt + i * NT;
           const bool pad = (v >> 3) >= valid || (((v & 7) ^ ((v >> 3) & 7)) >= dch);
-          *reinterpret_cast<uint4*>(st + v * 16) =
-              pad ? make_uint4(0u, 0u, 0u, 0u) : (feat ? kv[i] : phi_vec(kv[i]));
+          uint4 fk = pad ? make_uint4(0u, 0u, 0u, 0u) : (feat ? kv[i] : phi_vec(kv[i]));
+          // decay: key j' of the chunk enters both products scaled by gamma^(127-j')
+          if (DECAY && !pad) fk = scale_vec(fk, exp2f(lg * static_cast<float>(127 - (v >> 3))));
+          *reinterpret_cast<uint4*>(st + v * 16) = fk;
         }
         tmem_st_wait();
       }
@@ -445,6 +451,10 @@ __global__ void __launch_bounds__(NTHR, 1)
       const float4* rec = reinterpret_cast<const float4*>(ws + static_cast<long>(bh) * nseg * 64 * TC_MA) + tr * 5;
       int pp = 0;
       for (; pp + 1 < p; pp += 2) {  // two records per round trip
+        // decay: record pp (summed to its segment's end) reaches this segment's start
+        // through gamma^((p-1-pp) seg_len); 1 exactly without decay
+        const float f0 = DECAY ? exp2f(lg * static_cast<float>((p - 1 - pp) * seg_len)) : 1.f;
+        const float f1 = DECAY ? exp2f(lg * static_cast<float>((p - 2 - pp) * seg_len)) : 1.f;
         float4 x[10];
 #pragma unroll
         for (int j = 0; j < 5; ++j) {
@@ -453,20 +463,21 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
 #pragma unroll
         for (int j = 0; j < 5; ++j) {
-          acc[4 * j] += x[j].x + x[5 + j].x;
-          acc[4 * j + 1] += x[j].y + x[5 + j].y;
-          acc[4 * j + 2] += x[j].z + x[5 + j].z;
-          acc[4 * j + 3] += x[j].w + x[5 + j].w;
+          acc[4 * j] += f0 * x[j].x + f1 * x[5 + j].x;
+          acc[4 * j + 1] += f0 * x[j].y + f1 * x[5 + j].y;
+          acc[4 * j + 2] += f0 * x[j].z + f1 * x[5 + j].z;
+          acc[4 * j + 3] += f0 * x[j].w + f1 * x[5 + j].w;
         }
       }
       if (pp < p) {
+        const float f0 = DECAY ? exp2f(lg * static_cast<float>((p - 1 - pp) * seg_len)) : 1.f;
 #pragma unroll
         for (int j = 0; j < 5; ++j) {
           const float4 x = rec[pp * (64 * TC_MA / 4) + j];
-          acc[4 * j] += x.x;
-          acc[4 * j + 1] += x.y;
-          acc[4 * j + 2] += x.z;
-          acc[4 * j + 3] += x.w;
+          acc[4 * j] += f0 * x.x;
+          acc[4 * j + 1] += f0 * x.y;
+          acc[4 * j + 2] += f0 * x.z;
+          acc[4 * j + 3] += f0 * x.w;
         }
       }
       if (S0 != nullptr) {  // a state the sums start from (eq. 16-19 over a prompt)
@@ -494,6 +505,9 @@ __global__ void __launch_bounds__(NTHR, 1)
       // Row i keeps keys j <= i.  Key group g (32 keys) is fully kept for
       // g < qd, masked on its diagonal for g == qd and zero for g > qd, where
       // qd = i / 32 is the same for the whole warp.
+      // decay: A'_ij = gamma^(127-j') A_ij, and P_ij = gamma^-128 A'_ij = gamma^-(j'+1) A_ij is
+      // gamma^(i'-j') A_ij in a row frame scaled by gamma^-(i'+1), which out's quotient cancels
+      const float cm = DECAY ? exp2f(-128.f * lg) : 1.f;
       for (int c = 0; c < nch; ++c) {
         const uint32_t ta = tm + (c & 1) * T_BUF + lq;
         if (wtu(&bar_a[c & 1], (c >> 1) & 1, 15)) {
@@ -506,11 +520,14 @@ __global__ void __launch_bounds__(NTHR, 1)
               tmem_ldn<2>(ta + 32 * g, a);
               if (g < qd) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(a[2 * i], a[2 * i + 1]);
+                for (int i = 0; i < 16; ++i)
+                  pk[i] = DECAY ? pack_bf16(a[2 * i] * cm, a[2 * i + 1] * cm) : pack_bf16(a[2 * i], a[2 * i + 1]);
               } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  pk[i] = pack_bf16(2 * i <= lane ? a[2 * i] : 0.f, 2 * i + 1 <= lane ? a[2 * i + 1] : 0.f);
+                for (int i = 0; i < 16; ++i) {
+                  const float x0 = DECAY ? a[2 * i] * cm : a[2 * i], x1 = DECAY ? a[2 * i + 1] * cm : a[2 * i + 1];
+                  pk[i] = pack_bf16(2 * i <= lane ? x0 : 0.f, 2 * i + 1 <= lane ? x1 : 0.f);
+                }
               }
             } else {
 #pragma unroll
@@ -528,6 +545,9 @@ __global__ void __launch_bounds__(NTHR, 1)
       const int te = threadIdx.x - 32 * W_EPI0;  // 0 .. 127
       const bool has_s = lane < 16;  // M=64 accumulators: row 16*qd + lane in lane 32*qd + lane
       const int srow = 16 * qd + lane;
+      // decay: the state the next chunk's keys add to is gamma^128 times the last one
+      // (a full chunk); the read-out operand S~_prev stays unscaled
+      const float g128 = DECAY ? exp2f(128.f * lg) : 1.f;
       {
         const float4* src = reinterpret_cast<const float4*>(sm + F_SCR) + srow * (TC_MA / 4);
 #pragma unroll
@@ -541,7 +561,14 @@ __global__ void __launch_bounds__(NTHR, 1)
             sv[4 * i + 2] = x.z;
             sv[4 * i + 3] = x.w;
           }
-          tmem_st16(tm + T_S + lq + 16 * j, sv);
+          if (DECAY) {
+            float sc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sc[i] = sv[i] * g128;
+            tmem_st16(tm + T_S + lq + 16 * j, sc);
+          } else {
+            tmem_st16(tm + T_S + lq + 16 * j, sv);
+          }
           if (has_s) {
             if (j < 4) {
               tile_put_cols<16>(sm + F_SP, srow, 16 * j, sv);
@@ -569,14 +596,36 @@ __global__ void __launch_bounds__(NTHR, 1)
           uint8_t* sp = sm + F_SP + ((c + 1) & 1) * 16384;
           if (wtu(&bar_s, c & 1, 18)) {
             tc_fence_after();
-            float sv[48];
-            tmem_ldn<3>(tm + T_S + lq, sv);  // columns 0-47
-            if (has_s) tile_put_cols<48>(sp, srow, 0, sv);
-            tmem_ldn<2>(tm + T_S + lq + 48, sv);  // columns 48-79: S and z
-            if (has_s) {
-              tile_put_cols<16>(sp, srow, 48, sv);
-              const float z8[8] = {sv[16], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-              st_row_chunk(sp + 8192, srow, 0, z8);
+            if (DECAY) {
+              // 16 columns at a time: to the tile, then S~ <- gamma^128 S~ in place for
+              // the next chunk's keys (few registers live: this role shares the kernel's)
+#pragma unroll 1
+              for (int j = 0; j < TC_MA / 16; ++j) {
+                float sv[16];
+                tmem_ldn<1>(tm + T_S + lq + 16 * j, sv);
+                if (has_s) {
+                  if (j < 4) {
+                    tile_put_cols<16>(sp, srow, 16 * j, sv);
+                  } else {
+                    const float z8[8] = {sv[0], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    st_row_chunk(sp + 8192, srow, 0, z8);
+                  }
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) sv[i] *= g128;
+                tmem_st16(tm + T_S + lq + 16 * j, sv);
+                tmem_st_wait();
+              }
+            } else {
+              float sv[48];
+              tmem_ldn<3>(tm + T_S + lq, sv);  // columns 0-47
+              if (has_s) tile_put_cols<48>(sp, srow, 0, sv);
+              tmem_ldn<2>(tm + T_S + lq + 48, sv);  // columns 48-79: S and z
+              if (has_s) {
+                tile_put_cols<16>(sp, srow, 48, sv);
+                const float z8[8] = {sv[16], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                st_row_chunk(sp + 8192, srow, 0, z8);
+              }
             }
           }
           fence_proxy_async();
@@ -603,7 +652,8 @@ __global__ void __launch_bounds__(NTHR, 1)
           if (n0 + row < ne) {
             const long r = static_cast<long>(bh) * N + n0 + row;
             store_row_bf16(out + r * M, w, out_v8 != 0, M);
-            if (den != nullptr) den[r] = d;
+            // decay: the row came out scaled by gamma^-(row+1), which out's quotient cancels
+            if (den != nullptr) den[r] = DECAY ? d * exp2f(lg * static_cast<float>(row + 1)) : d;
           }
         } else {
           tc_fence_before();
@@ -701,7 +751,8 @@ namespace {
 // whose sums start from (S0, Z0) when S0 is not null.
 cudaError_t fwd_tc_launch(const void* q, const void* k, const void* v, void* out, float* den,
                           float* ws, const Shape& s, cudaStream_t st, const float* S0,
-                          const float* Z0, bool all_records, bool feat = false) {
+                          const float* Z0, bool all_records, bool feat = false, float gamma = 1.f) {
+  const float lg = gamma == 1.f ? 0.f : log2f(gamma);
   const int BH = s.B * s.H;
   const SegPlan pl = tc_plan(BH, s.N);
   CUtensorMap mq, mk, mv;
@@ -711,21 +762,23 @@ cudaError_t fwd_tc_launch(const void* q, const void* k, const void* v, void* out
   const int out_v8 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
   int* err = status_word();
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_tc_fwd_state, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                S_SMEM)) != cudaSuccess)
+  auto kstate = lg != 0.f ? k_tc_fwd_state<true> : k_tc_fwd_state<false>;
+  auto kmain = lg != 0.f ? k_tc_fwd_main<true> : k_tc_fwd_main<false>;
+  if ((e = cudaFuncSetAttribute(kstate, cudaFuncAttributeMaxDynamicSharedMemorySize, S_SMEM)) !=
+      cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(k_tc_fwd_main, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                F_SMEM)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(kmain, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM)) !=
+      cudaSuccess)
     return e;
   const int nrec = all_records ? pl.nseg : pl.nseg - 1;
   if (nrec > 0) {
-    if ((e = launch_pdl(k_tc_fwd_state, dim3(nrec, BH), dim3(NTHR), S_SMEM, st, mk, mv, ws,
-                        s.N, pl.nseg, pl.seg_len, s.D / 8, feat ? 1 : 0, err)) != cudaSuccess)
+    if ((e = launch_pdl(kstate, dim3(nrec, BH), dim3(NTHR), S_SMEM, st, mk, mv, ws,
+                        s.N, pl.nseg, pl.seg_len, s.D / 8, feat ? 1 : 0, lg, err)) != cudaSuccess)
       return e;
   }
-  if ((e = launch_pdl(k_tc_fwd_main, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv,
+  if ((e = launch_pdl(kmain, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv,
                       static_cast<bf16*>(out), den, static_cast<const float*>(ws), s.N, pl.nseg,
-                      pl.seg_len, out_v8, s.D / 8, s.M, feat ? 1 : 0, err, S0, Z0)) != cudaSuccess)
+                      pl.seg_len, out_v8, s.D / 8, s.M, feat ? 1 : 0, lg, err, S0, Z0)) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }
@@ -733,8 +786,8 @@ cudaError_t fwd_tc_launch(const void* q, const void* k, const void* v, void* out
 }  // namespace
 
 cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out, float* den,
-                          float* ws, const Shape& s, cudaStream_t st, bool feat) {
-  return fwd_tc_launch(q, k, v, out, den, ws, s, st, nullptr, nullptr, false, feat);
+                          float* ws, const Shape& s, cudaStream_t st, bool feat, float gamma) {
+  return fwd_tc_launch(q, k, v, out, den, ws, s, st, nullptr, nullptr, false, feat, gamma);
 }
 
 // The state pass writes every segment's record, the main pass adds (S, Z) to

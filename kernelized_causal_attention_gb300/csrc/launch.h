@@ -91,8 +91,12 @@ size_t causal_fwd_tc_ws_floats(const Shape& s);
 int causal_fwd_tc_launches(const Shape& s);
 // feat: q and k already hold features (a feature map applied before the call,
 // e.g. the degree-2 polynomial one); the kernels then apply no phi.
+// gamma: the RetNet decay (1 = none); the tensor-core forward takes gamma in
+// [TC_DECAY_MIN, 1] (its row and column factors stay inside fp32 and bf16).
+constexpr float TC_DECAY_MIN = 0.75f;
 cudaError_t causal_fwd_tc(const void* q, const void* k, const void* v, void* out, float* den,
-                          float* ws, const Shape& s, cudaStream_t st, bool feat = false);
+                          float* ws, const Shape& s, cudaStream_t st, bool feat = false,
+                          float gamma = 1.f);
 size_t causal_bwd_tc_ws_floats(const Shape& s);
 int causal_bwd_tc_launches(const Shape& s);
 cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const void* out,

@@ -93,6 +93,21 @@ __device__ __forceinline__ uint4 phi_vec(uint4 u) {
   return make_uint4(phi_bf16x2(u.x), phi_bf16x2(u.y), phi_bf16x2(u.z), phi_bf16x2(u.w));
 }
 
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Eight packed bf16 values times an fp32 factor, rounded once.
+__device__ __forceinline__ uint4 scale_vec(uint4 u, float f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    r[i] = pack_bf16(__uint_as_float(w[i] << 16) * f, __uint_as_float(w[i] & 0xffff0000u) * f);
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 // phi applied in place to NTL swizzled [128][64] bf16 tiles spaced `stride`
 // bytes apart, by NT threads (t = 0 .. NT-1; elementwise, so the swizzle does
 // not matter).  Every thread first loads all of its vectors, then transforms
@@ -101,10 +116,11 @@ __device__ __forceinline__ uint4 phi_vec(uint4 u) {
 // columns at or past 8 dch (a head narrower than 64 whose tile the load
 // filled with zeros: phi(0) = 1, but a padded feature must add nothing).
 // ident: the tiles already hold features (a feature map applied before the
-// call); only the masking applies.
+// call); only the masking applies.  lg != 0: row r is also scaled by
+// 2^(lg (e0 - r)), i.e. gamma^(e0 - r) with lg = log2 gamma (the decay).
 template <int NT, int NTL>
 __device__ __forceinline__ void phi_tiles(uint8_t* tile, int stride, int valid, int t, int dch = 8,
-                                          bool ident = false) {
+                                          bool ident = false, float lg = 0.f, int e0 = 0) {
   constexpr int PER = TILE / 16 / NT;  // vectors per thread and tile
   static_assert(PER * NT * 16 == TILE, "threads must divide the tile");
   uint4 u[NTL][PER];
@@ -119,7 +135,8 @@ __device__ __forceinline__ void phi_tiles(uint8_t* tile, int stride, int valid, 
     for (int i = 0; i < PER; ++i) {
       const int v = t + i * NT;
       const bool pad = (v >> 3) >= valid || (((v & 7) ^ ((v >> 3) & 7)) >= dch);
-      const uint4 r = pad ? make_uint4(0u, 0u, 0u, 0u) : (ident ? u[k][i] : phi_vec(u[k][i]));
+      uint4 r = pad ? make_uint4(0u, 0u, 0u, 0u) : (ident ? u[k][i] : phi_vec(u[k][i]));
+      if (lg != 0.f && !pad) r = scale_vec(r, exp2f(lg * static_cast<float>(e0 - (v >> 3))));
       sts128(tile + k * stride + v * 16, r);
     }
 }
@@ -161,10 +178,6 @@ __device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t bytes) {
 // stream has completed and its memory is visible.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
 
 // Writes 8 consecutive values (columns 8c .. 8c+7) of row r of a swizzled
 // [rows][64] bf16 tile.

@@ -47,6 +47,11 @@ SMALL = [
     (2, 2, 2049, 64, 64, "bf16", 0.99),
     (1, 1, 500, 32, 64, "f32", 0.0),     # gamma = 0: out = v
     (1, 2, 300, 16, 16, "f32", 0.3),
+    # bf16 forwards on the tensor cores for gamma >= 0.75, on the CUDA cores below
+    (1, 2, 1000, 64, 64, "bf16", 0.75),
+    (2, 1, 3001, 32, 32, "bf16", 0.95),
+    (1, 2, 777, 64, 64, "bf16", 0.5),
+    (1, 1, 1, 64, 64, "bf16", 0.9),
 ]
 
 
@@ -145,11 +150,14 @@ def test_decay_rejects_gamma_outside_0_1(linattn, gamma):
 
 def test_decay_workspace_and_launches(linattn):
     la = linattn
-    # the decayed calls run on the CUDA cores: their sizes, not the tensor-core ones
+    # the decayed forward's workspace covers both paths
     n = la.la_workspace_bytes(la.LA_OP_CAUSAL_FWD_DECAY, 4, 8, 3072, 64, 64, la.LA_BF16)
+    assert n >= la.la_workspace_bytes(la.LA_OP_CAUSAL_FWD, 4, 8, 3072, 64, 64, la.LA_BF16)
     assert n > 0 and n % 16 == 0
     assert la.la_workspace_bytes(la.LA_OP_CAUSAL_BWD_DECAY, 4, 8, 3072, 64, 64, la.LA_BF16) > n
-    assert la.la_kernel_launches(la.LA_OP_CAUSAL_FWD_DECAY, 4, 8, 3072, 64, 64, la.LA_BF16) == 3
+    assert la.la_kernel_launches(la.LA_OP_CAUSAL_FWD_DECAY, 4, 8, 3072, 64, 64, la.LA_BF16) == \
+        la.la_kernel_launches(la.LA_OP_CAUSAL_FWD, 4, 8, 3072, 64, 64, la.LA_BF16)  # tensor cores
+    assert la.la_kernel_launches(la.LA_OP_CAUSAL_FWD_DECAY, 4, 8, 3072, 64, 64, la.LA_F32) == 3
     assert la.la_kernel_launches(la.LA_OP_CAUSAL_BWD_DECAY, 1, 1, 64, 16, 16, la.LA_F32) == 1
     # a missing workspace is reported before launching
     assert la.lib().la_causal_fwd_decay(FAKE, FAKE, FAKE, FAKE, FAKE, 0.9, None, 0, 4, 8, 3072, 64, 64,
