@@ -209,10 +209,10 @@ la_status la_decode_step(const void* q, const void* k, const void* v, float* S, 
  *   out_i = phi(Q_i)^T S_i / phi(Q_i)^T Z_i
  *         = sum_{j<=i} gamma^(i-j) phi(Q_i).phi(K_j) V_j / sum_{j<=i} gamma^(i-j) phi(Q_i).phi(K_j),
  * den_i = phi(Q_i)^T Z_i.  gamma must lie in [0, 1] (else LA_ERR_INVALID_ARG);
- * gamma = 1 is la_causal_fwd's operation and gamma = 0 returns V.  The
- * forward runs on the tensor cores for the shapes la_causal_fwd runs there
- * (bf16, D and M in {16, 32, 64}) when gamma >= 0.75, else on the CUDA cores;
- * the backward runs on the CUDA cores.  They take the workspace of
+ * gamma = 1 is la_causal_fwd's operation and gamma = 0 returns V.  Both
+ * calls run on the tensor cores for the shapes la_causal_fwd runs there (bf16,
+ * D and M in {16, 32, 64}) when gamma >= 0.75, else on the CUDA cores.  They
+ * take the workspace of
  * la_workspace_bytes(LA_OP_CAUSAL_FWD_DECAY / _BWD_DECAY, ...) (enough for
  * either path; la_kernel_launches counts the tensor-core path where it applies);
  * other arguments and errors as la_causal_fwd / la_causal_bwd.

@@ -49,7 +49,9 @@ size_t ws_bytes(int op, const Shape& s) {
     case LA_OP_CAUSAL_FWD_DECAY:  // either path, whichever gamma picks
       return 4 * (la::tc_eligible(s) ? std::max(la::causal_fwd_tc_ws_floats(s), la::causal_fwd_ws_floats(s))
                                      : la::causal_fwd_ws_floats(s));
-    case LA_OP_CAUSAL_BWD_DECAY: return 4 * la::causal_bwd_ws_floats(s);
+    case LA_OP_CAUSAL_BWD_DECAY:  // either path, whichever gamma picks
+      return 4 * (la::tc_eligible(s) ? std::max(la::causal_bwd_tc_ws_floats(s), la::causal_bwd_ws_floats(s))
+                                     : la::causal_bwd_ws_floats(s));
     case LA_OP_NONCAUSAL_FWD: return 4 * la::noncausal_fwd_ws_floats(s);
     case LA_OP_NONCAUSAL_BWD: return 4 * la::noncausal_bwd_ws_floats(s);
     default: return 0;
@@ -162,7 +164,8 @@ int la_kernel_launches(int op, int B, int H, int N, int D, int M, int dtype) {
     case LA_OP_CAUSAL_PREFILL: return la::tc_prefill_eligible(s) ? 3 : 4;
     case LA_OP_CAUSAL_FWD_DECAY:  // gamma in [0.75, 1] on the tensor-core path
       return la::tc_eligible(s) ? la::causal_fwd_tc_launches(s) : la::causal_fwd_launches(s);
-    case LA_OP_CAUSAL_BWD_DECAY: return la::causal_bwd_launches(s);
+    case LA_OP_CAUSAL_BWD_DECAY:  // gamma in [0.75, 1] on the tensor-core path
+      return la::tc_eligible(s) ? la::causal_bwd_tc_launches(s) : la::causal_bwd_launches(s);
     case LA_OP_NONCAUSAL_FWD: return la::noncausal_fwd_launches(s);
     case LA_OP_NONCAUSAL_BWD: return la::noncausal_bwd_launches(s);
     case LA_OP_DECODE: return 1;
@@ -267,6 +270,10 @@ int la_causal_bwd_decay(const void* q, const void* k, const void* v, const void*
   LA_TRY(check_gamma(gamma));
   const Shape s{B, H, N, D, M, dtype};
   LA_TRY(check_ws(LA_OP_CAUSAL_BWD_DECAY, s, workspace, workspace_bytes));
+  if (la::tc_eligible(s) && gamma >= la::TC_DECAY_MIN)
+    return from_cuda(la::causal_bwd_tc(q, k, v, out, den, dout, dq, dk, dv,
+                                       static_cast<float*>(workspace), s,
+                                       static_cast<cudaStream_t>(stream), false, gamma));
   return from_cuda(la::causal_bwd_cc(q, k, v, out, den, dout, dq, dk, dv,
                                      static_cast<float*>(workspace), s,
                                      static_cast<cudaStream_t>(stream), gamma));

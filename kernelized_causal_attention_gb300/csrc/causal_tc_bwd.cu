@@ -51,7 +51,8 @@ static_assert(M_SMEM + 2048 <= 232448, "shared memory");
 // Role 1: the masked bf16 rows of dA (+ gam) and of A for this warpgroup's
 // KW keys from key0, loaded together so that one wait covers both.
 __device__ __forceinline__ void mask2_cols(uint32_t tda, uint32_t ta, float add, uint8_t* ddst,
-                                           uint8_t* adst, int row, int key0) {
+                                           uint8_t* adst, int row, int key0, float dscale = 1.f,
+                                           float ascale = 1.f) {
   float d[KW], a[KW];
 #pragma unroll
   for (int i = 0; i < KW / 16; ++i) {
@@ -62,8 +63,8 @@ __device__ __forceinline__ void mask2_cols(uint32_t tda, uint32_t ta, float add,
 #pragma unroll
   for (int i = 0; i < KW; ++i) {
     const bool keep = key0 + i <= row;
-    d[i] = keep ? d[i] + add : 0.f;
-    a[i] = keep ? a[i] : 0.f;
+    d[i] = keep ? (d[i] + add) * dscale : 0.f;
+    a[i] = keep ? a[i] * ascale : 0.f;
   }
   tile_put_cols<KW>(ddst, row, key0 & 63, d);
   tile_put_cols<KW>(adst, row, key0 & 63, a);
@@ -82,10 +83,11 @@ struct BwdMaps {
 // read the next state out while the gradient products run), then the gradient
 // products.  The vector terms gam z_prev (dq) and r_next (dk) are added in the
 // epilogues.
+template <bool DECAY>
 __global__ void __launch_bounds__(NTHR, 1)
     k_tc_bwd_main(const __grid_constant__ BwdMaps maps, const float* __restrict__ rec,
                   const float* __restrict__ gam, int N, int seg_len, int nsub, int subs_per_seg,
-                  int feat, int* err) {
+                  int feat, float lg, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;
   const int role = static_cast<int>(blockIdx.z);  // 0 dq, 1 dk / dv
   extern __shared__ uint8_t smraw[];
@@ -269,23 +271,42 @@ __global__ void __launch_bounds__(NTHR, 1)
       const int hi = role == 0 ? p * subs_per_seg : nsub;
       const int off = role == 0 ? 0 : DM + 64;
       float* scr = reinterpret_cast<float*>(sm + M_P);
+      // decay: a forward record (summed to its sub-segment's end) reaches this
+      // segment's start through gamma^((lo' - 1 - pp) sub_len), lo' = p subs; a
+      // reverse record (summed from its start) reaches the next segment's start
+      // through gamma^((pp - (p+1) subs) sub_len)
+      const int sub_len = seg_len / subs_per_seg;
+      auto wrec = [&](int pp) {
+        if (!DECAY) return 1.f;
+        const int e = role == 0 ? (hi - 1 - pp) : (pp - lo);
+        return exp2f(lg * static_cast<float>(e) * static_cast<float>(sub_len));
+      };
       for (int j = t; j < (DM + 64) / 4; j += NCOMP) {  // 1040 float4 per state
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         int pp = lo;
         for (; pp + 1 < hi; pp += 2) {  // two records per round trip
           const float4 x = reinterpret_cast<const float4*>(rec + (static_cast<long>(bh) * nsub + pp) * REC + off)[j];
           const float4 y = reinterpret_cast<const float4*>(rec + (static_cast<long>(bh) * nsub + pp + 1) * REC + off)[j];
-          acc.x += x.x + y.x;
-          acc.y += x.y + y.y;
-          acc.z += x.z + y.z;
-          acc.w += x.w + y.w;
+          if (DECAY) {
+            const float fx = wrec(pp), fy = wrec(pp + 1);
+            acc.x += fx * x.x + fy * y.x;
+            acc.y += fx * x.y + fy * y.y;
+            acc.z += fx * x.z + fy * y.z;
+            acc.w += fx * x.w + fy * y.w;
+          } else {
+            acc.x += x.x + y.x;
+            acc.y += x.y + y.y;
+            acc.z += x.z + y.z;
+            acc.w += x.w + y.w;
+          }
         }
         if (pp < hi) {
           const float4 x = reinterpret_cast<const float4*>(rec + (static_cast<long>(bh) * nsub + pp) * REC + off)[j];
-          acc.x += x.x;
-          acc.y += x.y;
-          acc.z += x.z;
-          acc.w += x.w;
+          const float fx = wrec(pp);
+          acc.x += fx * x.x;
+          acc.y += fx * x.y;
+          acc.z += fx * x.z;
+          acc.w += fx * x.w;
         }
         reinterpret_cast<float4*>(scr)[j] = acc;
       }
@@ -299,9 +320,14 @@ __global__ void __launch_bounds__(NTHR, 1)
             const int col = 16 * j + i;
             sv[i] = !has_s ? 0.f : col < 64 ? scr[srow * 64 + col] : col == 64 ? scr[DM + srow] : 0.f;
           }
-          tmem_st16(TST + lq + 16 * j, sv);
           if (has_s && j < 4) tile_put_cols<16>(sm + M_RP, srow, 16 * j, sv);
           if (has_s && j == 4) s_vec[0][srow] = sv[0];
+          if (DECAY) {  // the state the first chunk adds to: gamma^128 times the carried one
+            const float g128 = exp2f(128.f * lg);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sv[i] *= g128;
+          }
+          tmem_st16(TST + lq + 16 * j, sv);
         }
         tmem_st_wait();
       }
@@ -329,11 +355,15 @@ __global__ void __launch_bounds__(NTHR, 1)
       if (t == 0) bulk_wait_read();  // the previous chunk's output tiles have left P / dP
       compute_sync();
       if (ok_a) {
+        // decay: with the workspace's phi(Q) rows scaled by gamma^i' and phi(K) rows by
+        // gamma^(127-j'), every weight gamma^(i'-j') becomes the constant gamma^-128 in a
+        // row frame that the epilogues take back
+        const float cm = DECAY ? exp2f(-128.f * lg) : 1.f;
         if (role == 1)
           mask2_cols(TDA + lq + k0, TA + lq + k0, gm, sm + M_DP + (k0 >> 6) * TILE,
-                     sm + M_P + (k0 >> 6) * TILE, row, k0);
+                     sm + M_P + (k0 >> 6) * TILE, row, k0, cm, cm);
         else
-          mask_cols<KW>(TDA + lq + k0, gm, sm + M_DP + (k0 >> 6) * TILE, row, k0);
+          mask_cols<KW>(TDA + lq + k0, gm, sm + M_DP + (k0 >> 6) * TILE, row, k0, cm);
       }
       fence_proxy_async();
       tc_fence_before();
@@ -349,6 +379,19 @@ __global__ void __launch_bounds__(NTHR, 1)
           if (has_s) {
             tile_put_cols<OW>(sm + M_RP + ((c + 1) & 1) * 8192, srow, c0, sv);
             if (wg == 0) s_vec[(c + 1) & 1][srow] = vv[0];
+          }
+          if (DECAY) {  // the next chunk adds to gamma^128 times this state
+            const float g128 = exp2f(128.f * lg);
+#pragma unroll
+            for (int i = 0; i < OW; ++i) sv[i] *= g128;
+#pragma unroll
+            for (int i = 0; i < OW / 16; ++i) tmem_st16(TST + lq + c0 + 16 * i, sv + 16 * i);
+            if (wg == 0) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) vv[i] *= g128;
+              tmem_st16(TST + lq + 64, vv);
+            }
+            tmem_st_wait();
           }
         }
         fence_proxy_async();
@@ -374,15 +417,29 @@ __global__ void __launch_bounds__(NTHR, 1)
         tmem_ldn<OW / 16>(TG1 + lq + c0, gv);
         if (role == 0) {  // dq = (grad_phiQ + gam z_prev) * phi'(Q)
           tile_row_cols<OW>(st, row, c0, x);
+          // decay: the row frame gamma^-(i'+1) back; the tile holds gamma^i' phi(Q)
+          const float fo = DECAY ? exp2f(lg * static_cast<float>(row + 1)) : 1.f;
+          const float fx = DECAY ? exp2f(-lg * static_cast<float>(row)) : 1.f;
 #pragma unroll
-          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + gm * vcur[c0 + i]) * (feat ? 1.f : fminf(x[i], 1.f));
+          for (int i = 0; i < OW; ++i)
+            gv[i] = (gv[i] + gm * vcur[c0 + i]) * fo * (feat ? 1.f : fminf(x[i] * fx, 1.f));
           tile_put_cols<OW>(sm + M_DP, row, c0, gv);
         } else {          // dk = (grad_phiK + r_next) * phi'(K), dv
           tile_row_cols<OW>(st + TILE, row, c0, x);
+          // decay: dk's row frame gamma^-(128-j') back, the tile holds gamma^(127-j')
+          // phi(K), and dv comes out gamma^-1 times the true one
+          const float fo = DECAY ? exp2f(lg * static_cast<float>(128 - row)) : 1.f;
+          const float fx = DECAY ? exp2f(-lg * static_cast<float>(127 - row)) : 1.f;
 #pragma unroll
-          for (int i = 0; i < OW; ++i) gv[i] = (gv[i] + vcur[c0 + i]) * (feat ? 1.f : fminf(x[i], 1.f));
+          for (int i = 0; i < OW; ++i)
+            gv[i] = (gv[i] + vcur[c0 + i]) * fo * (feat ? 1.f : fminf(x[i] * fx, 1.f));
           tile_put_cols<OW>(sm + M_P, row, c0, gv);
           tmem_ldn<OW / 16>(TG2 + lq + c0, gv);
+          if (DECAY) {
+            const float g1 = exp2f(lg);
+#pragma unroll
+            for (int i = 0; i < OW; ++i) gv[i] *= g1;
+          }
           tile_put_cols<OW>(sm + M_P + TILE, row, c0, gv);
         }
       }
@@ -438,11 +495,12 @@ __device__ __forceinline__ void ones_tile(uint8_t* tile, int t, int nthr) {
   }
 }
 
+template <bool DECAY>
 __global__ void __launch_bounds__(NTHR, 1)
     k_tc_bwd_state(const __grid_constant__ StateMaps maps, const float* __restrict__ den,
                    float* __restrict__ gam, bf16* __restrict__ gt_out, bf16* __restrict__ fq_out,
                    bf16* __restrict__ fk_out, float* __restrict__ rec, int N, int sub_len, int nsub,
-                   int dch, int feat, int* err) {
+                   int dch, int feat, float lg, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;  // the call's first kernel
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -575,8 +633,18 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const uint4 f = rv && lc < dch ? (feat ? x[k][i] : phi_vec(x[k][i])) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(st + k * TILE + v * 16) = f;
-            if (rv) *reinterpret_cast<uint4*>((k == 0 ? fq_out : fk_out) + gofs) = f;
+            if (DECAY) {
+              // the workspace takes chunk-scaled rows for the main pass (phi(Q) gamma^r,
+              // phi(K) gamma^(127-r)); the records take sub-segment-scaled ones (the
+              // reverse sums from the sub-segment's start, the forward sums to its end)
+              const float fw = exp2f(lg * static_cast<float>(k == 0 ? r : 127 - r));
+              const float fs = exp2f(lg * static_cast<float>(k == 0 ? n0 + r - nb : ne - 1 - n0 - r));
+              *reinterpret_cast<uint4*>(st + k * TILE + v * 16) = scale_vec(f, fs);
+              if (rv) *reinterpret_cast<uint4*>((k == 0 ? fq_out : fk_out) + gofs) = scale_vec(f, fw);
+            } else {
+              *reinterpret_cast<uint4*>(st + k * TILE + v * 16) = f;
+              if (rv) *reinterpret_cast<uint4*>((k == 0 ? fq_out : fk_out) + gofs) = f;
+            }
           }
           // gt = dout / den in place and to the workspace; gam = -(gt . out)
           float dot = 0.f;
@@ -709,7 +777,7 @@ int causal_bwd_tc_launches(const Shape&) { return 2; }
 
 cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const void* out,
                           const float* den, const void* dout, void* dq, void* dk, void* dv,
-                          float* ws, const Shape& s, cudaStream_t st, bool feat) {
+                          float* ws, const Shape& s, cudaStream_t st, bool feat, float gamma) {
   const int BH = s.B * s.H;
   const BwdPlan pl = bwd_plan(BH, s.N);
   const BwdWs w = bwd_ws(ws, BH, s.N, pl);
@@ -730,19 +798,22 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
   smap.g = m.g;
   smap.o = m.o;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_tc_bwd_state, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SS_SMEM)) != cudaSuccess)
+  const float lg = gamma == 1.f ? 0.f : log2f(gamma);
+  auto kstate = lg != 0.f ? k_tc_bwd_state<true> : k_tc_bwd_state<false>;
+  auto kmain = lg != 0.f ? k_tc_bwd_main<true> : k_tc_bwd_main<false>;
+  if ((e = cudaFuncSetAttribute(kstate, cudaFuncAttributeMaxDynamicSharedMemorySize, SS_SMEM)) !=
+      cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(k_tc_bwd_main, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                M_SMEM)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(kmain, cudaFuncAttributeMaxDynamicSharedMemorySize, M_SMEM)) !=
+      cudaSuccess)
     return e;
-  if ((e = launch_pdl(k_tc_bwd_state, dim3(pl.nsub, BH), dim3(NTHR), SS_SMEM, st, smap, den, w.gam,
-                      w.gt, w.fq, w.fk, w.rec, s.N, pl.sub_len, pl.nsub, s.D / 8, feat ? 1 : 0,
+  if ((e = launch_pdl(kstate, dim3(pl.nsub, BH), dim3(NTHR), SS_SMEM, st, smap, den, w.gam,
+                      w.gt, w.fq, w.fk, w.rec, s.N, pl.sub_len, pl.nsub, s.D / 8, feat ? 1 : 0, lg,
                       status_word())) != cudaSuccess)
     return e;
-  if ((e = launch_pdl(k_tc_bwd_main, dim3(pl.main.nseg, BH, 2), dim3(NTHR), M_SMEM, st, m,
+  if ((e = launch_pdl(kmain, dim3(pl.main.nseg, BH, 2), dim3(NTHR), M_SMEM, st, m,
                       static_cast<const float*>(w.rec), static_cast<const float*>(w.gam), s.N,
-                      pl.main.seg_len, pl.nsub, pl.subs, feat ? 1 : 0, status_word())) != cudaSuccess)
+                      pl.main.seg_len, pl.nsub, pl.subs, feat ? 1 : 0, lg, status_word())) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }

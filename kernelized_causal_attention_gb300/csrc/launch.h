@@ -101,7 +101,8 @@ size_t causal_bwd_tc_ws_floats(const Shape& s);
 int causal_bwd_tc_launches(const Shape& s);
 cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const void* out,
                           const float* den, const void* dout, void* dq, void* dk, void* dv,
-                          float* ws, const Shape& s, cudaStream_t st, bool feat = false);
+                          float* ws, const Shape& s, cudaStream_t st, bool feat = false,
+                          float gamma = 1.f);
 
 // The degree-2 polynomial kernel (poly.cu): features f(x) = [x_a^2, sqrt(2)
 // x_a x_b (a < b)] zero-padded to 64, then the tensor-core kernels with

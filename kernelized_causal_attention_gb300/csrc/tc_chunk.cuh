@@ -245,11 +245,11 @@ __device__ __forceinline__ void store_bf16(bf16* dst, const float* f) {
 // columns (key0 & 63) .. of row `row` of the swizzled tile `dst`.
 template <int NC>
 __device__ __forceinline__ void mask_cols(uint32_t taddr, float add, uint8_t* dst, int row,
-                                          int key0) {
+                                          int key0, float scale = 1.f) {
   float a[NC];
   tmem_ldn<NC / 16>(taddr, a);
 #pragma unroll
-  for (int i = 0; i < NC; ++i) a[i] = (key0 + i <= row) ? a[i] + add : 0.f;
+  for (int i = 0; i < NC; ++i) a[i] = (key0 + i <= row) ? (a[i] + add) * scale : 0.f;
   tile_put_cols<NC>(dst, row, key0 & 63, a);
 }
 

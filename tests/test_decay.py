@@ -155,10 +155,14 @@ def test_decay_workspace_and_launches(linattn):
     assert n >= la.la_workspace_bytes(la.LA_OP_CAUSAL_FWD, 4, 8, 3072, 64, 64, la.LA_BF16)
     assert n > 0 and n % 16 == 0
     assert la.la_workspace_bytes(la.LA_OP_CAUSAL_BWD_DECAY, 4, 8, 3072, 64, 64, la.LA_BF16) > n
+    assert la.la_workspace_bytes(la.LA_OP_CAUSAL_BWD_DECAY, 4, 8, 3072, 64, 64, la.LA_BF16) >= \
+        la.la_workspace_bytes(la.LA_OP_CAUSAL_BWD, 4, 8, 3072, 64, 64, la.LA_BF16)
     assert la.la_kernel_launches(la.LA_OP_CAUSAL_FWD_DECAY, 4, 8, 3072, 64, 64, la.LA_BF16) == \
         la.la_kernel_launches(la.LA_OP_CAUSAL_FWD, 4, 8, 3072, 64, 64, la.LA_BF16)  # tensor cores
     assert la.la_kernel_launches(la.LA_OP_CAUSAL_FWD_DECAY, 4, 8, 3072, 64, 64, la.LA_F32) == 3
     assert la.la_kernel_launches(la.LA_OP_CAUSAL_BWD_DECAY, 1, 1, 64, 16, 16, la.LA_F32) == 1
+    assert la.la_kernel_launches(la.LA_OP_CAUSAL_BWD_DECAY, 4, 8, 3072, 64, 64, la.LA_BF16) == \
+        la.la_kernel_launches(la.LA_OP_CAUSAL_BWD, 4, 8, 3072, 64, 64, la.LA_BF16)  # tensor cores
     # a missing workspace is reported before launching
     assert la.lib().la_causal_fwd_decay(FAKE, FAKE, FAKE, FAKE, FAKE, 0.9, None, 0, 4, 8, 3072, 64, 64,
                                         la.LA_BF16, None) == la.LA_ERR_WORKSPACE
