@@ -158,3 +158,14 @@ def test_decode_proj_workspace_and_launches(linattn):
     assert la.la_kernel_launches(la.LA_OP_DECODE_PROJ, 10000, 8, 256, 32, 32, la.LA_BF16) == 1
     assert la.la_kernel_launches(la.LA_OP_DECODE_PROJ, 10000, 8, 100, 32, 32, la.LA_BF16) == 0
     assert la.la_kernel_launches(la.LA_OP_DECODE_PROJ, 10000, 8, 256, 32, 32, la.LA_F32) == 0
+
+
+@pytest.mark.gpu
+def test_decode_proj_limits(cuda, linattn):
+    """The largest stream count (B*H = 2^20, 16-wide heads) on sampled streams,
+    and the widest layer input (d_model = 16384: 256 slabs through the ring)."""
+    B, H, D, M, dm = (1 << 20) // 8, 8, 16, 16, 64
+    gen = torch.Generator().manual_seed(5)
+    rows = torch.cat([torch.randperm(B - 64, generator=gen)[:400], torch.arange(B - 64, B)])
+    print(check(linattn, cuda, B, dm, H, D, M, seed=96, rows=rows))
+    print(check(linattn, cuda, 100, 16384, 2, 64, 64, seed=97))
