@@ -32,6 +32,17 @@
 //                S~_prev(c+1) in bf16 for the next chunk's read-out
 // and the issuer polls for whichever product can go next, so a late phi never
 // holds back a read-out.
+//
+// Variants on the same kernels.  feat: q and k already hold features (the
+// degree-2 polynomial map), so no phi is applied.  DECAY (the RetNet decay
+// gamma of "Linear Attention/zh", variants; a template flag, so the plain
+// kernels keep their code): key j' of a chunk is scaled by gamma^(127-j') as
+// phi is applied, the mask multiplies by the constant gamma^-128, so
+// P_ij = gamma^-(j'+1) A_ij and output row i' comes out gamma^-(i'+1) times
+// the decayed one -- out's quotient cancels that and den takes it back -- and
+// the epilogue writes gamma^128 S~ back to tensor memory before the next
+// chunk's keys; the state pass scales key j by gamma^(segment end - 1 - j)
+// and the record sum weights each record by its distance.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"

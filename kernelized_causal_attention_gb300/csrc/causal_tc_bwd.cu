@@ -23,6 +23,16 @@
 // Every product, including the vector sums z and r (against a ones column
 // or the gam column), runs on tcgen05 with TMA-fed operands; dq, dk and dv
 // are staged in shared memory and written with TMA stores.
+//
+// Variants on the same kernels.  feat: phi(Q), phi(K) are the given rows (the
+// degree-2 polynomial map) and phi' = 1.  DECAY (a template flag): the state
+// pass writes phi(Q) rows scaled by gamma^i' and phi(K) rows by gamma^(127-j')
+// (within the chunk) to the workspace and scales its own copies by the
+// distance to its sub-segment's start (phi(Q), reverse records) or end
+// (phi(K), forward records); the main pass then masks with the constant
+// gamma^-128, carries S~ and R~ with a gamma^128 write-back after each
+// read-out, and its epilogues restore the row frames (dq by gamma^(i'+1), dk
+// by gamma^(128-j'), dv by gamma).
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
