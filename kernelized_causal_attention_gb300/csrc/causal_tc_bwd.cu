@@ -13,13 +13,18 @@
 // with P = bf16(mask(phi(Q) phi(K)^T)) and dP = bf16(mask(dA)); then
 // dq = grad_phiQ * phi'(Q), dk = grad_phiK * phi'(K), and phi'(x) = min(phi(x), 1).
 //
-// Two kernels.  The state pass k_tc_bwd_state (one CTA per sub-segment of
-// whole 128-token chunks) reads q, k, v, dout, out and den once; it stores
-// phi(Q), phi(K) and gt = dout / den (bf16) and gam (fp32) in the workspace,
-// and the sub-segment's partial S, z, R, r.  The main pass k_tc_bwd_main
-// runs two roles per segment (grid z): role 0 walks forward carrying S, z
-// and writes dq; role 1 walks backward carrying R, r and writes dk and dv.  Each CTA first adds up the
-// partial states of the sub-segments before (role 0) or after (role 1) it.
+// Two kernels.  The state pass k_tc_bwd_state (one CTA per one or two
+// sub-segments of whole 128-token chunks) reads q, k, v, dout, out and den
+// once; it stores phi(Q), phi(K) and gt = dout / den (bf16) and gam (fp32) in
+// the workspace, and each sub-segment's partial S, z, R, r.  The main pass
+// k_tc_bwd_main fills one wave of CTAs with runs of whole sub-segments: role 0
+// walks its run forward carrying S, z and writes dq; role 1 walks backward
+// carrying R, r and writes dk and dv.  A run may cross from one (b, h) into
+// the next (the state restarts from zero there), so the roles can be given
+// different run lengths: a dk / dv chunk costs about 1.4 times a dq chunk,
+// and the 3072-token workload runs 64 dq runs of 12 chunks beside 86 dk / dv
+// runs of 9.  Each CTA first adds up the partial states of the sub-segments
+// before (role 0) or after (role 1) its run.
 // Every product, including the vector sums z and r (against a ones column
 // or the gam column), runs on tcgen05 with TMA-fed operands; dq, dk and dv
 // are staged in shared memory and written with TMA stores.
@@ -33,6 +38,8 @@
 // gamma^-128, carries S~ and R~ with a gamma^128 write-back after each
 // read-out, and its epilogues restore the row frames (dq by gamma^(i'+1), dk
 // by gamma^(128-j'), dv by gamma).
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
@@ -86,9 +93,14 @@ struct BwdMaps {
   CUtensorMap dq, dk, dv;     // main-pass outputs (TMA stores)
 };
 
-// Main pass: two roles per segment (grid z).  Role 0 walks the segment's
-// chunks forward carrying S~ = [S | z] and writes dq; role 1 walks them
-// backward carrying R~ = [R | r] and writes dk and dv.  Per chunk: A and dA,
+// Main pass: each CTA takes one role over a run of whole sub-segments, a
+// contiguous range [F0, F1) of flat chunk indices bh * nchh + chunk that may
+// cross from one (b, h) into the next.  Role 0 (the first n0cta CTAs, upc0
+// sub-segments each) walks its run forward carrying S~ = [S | z] and writes
+// dq; role 1 (upc1 sub-segments each) walks it backward carrying R~ = [R | r]
+// and writes dk and dv.  The run starts from the records of the sub-segments
+// before it (role 0) or after it (role 1) in its first (b, h); where it enters
+// the next (b, h) the carried state restarts from zero.  Per chunk: A and dA,
 // then the carried-state update (it only needs the stage, so the compute warps
 // read the next state out while the gradient products run), then the gradient
 // products.  The vector terms gam z_prev (dq) and r_next (dk) are added in the
@@ -96,10 +108,15 @@ struct BwdMaps {
 template <bool DECAY>
 __global__ void __launch_bounds__(NTHR, 1)
     k_tc_bwd_main(const __grid_constant__ BwdMaps maps, const float* __restrict__ rec,
-                  const float* __restrict__ gam, int N, int seg_len, int nsub, int subs_per_seg,
-                  int feat, float lg, int* err) {
-  const int p = blockIdx.x, bh = blockIdx.y;
-  const int role = static_cast<int>(blockIdx.z);  // 0 dq, 1 dk / dv
+                  const float* __restrict__ gam, int N, int nchh, int cps, int nsub, int BH,
+                  int n0cta, int upc0, int upc1, int feat, float lg, int* err) {
+  const int role = static_cast<int>(blockIdx.x) < n0cta ? 0 : 1;  // 0 dq, 1 dk / dv
+  const int idx = static_cast<int>(blockIdx.x) - (role == 0 ? 0 : n0cta);
+  const int upc = role == 0 ? upc0 : upc1;
+  const int u0 = idx * upc, u1 = min(BH * nsub, u0 + upc);  // sub-segments [u0, u1) of BH * nsub
+  const int F0 = (u0 / nsub) * nchh + (u0 % nsub) * cps;
+  const int F1 = ((u1 - 1) / nsub) * nchh + min(nchh, ((u1 - 1) % nsub + 1) * cps);
+  const int nch = F1 - F0;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   __shared__ uint64_t bar_full[NST], bar_empty[NST];
@@ -108,9 +125,6 @@ __global__ void __launch_bounds__(NTHR, 1)
   __shared__ float s_vec[2][64];  // carried z (role 0) or r (role 1) before chunk c, by c & 1
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = p * seg_len;
-  const int ne = min(N, nb + seg_len);
-  const int nch = (ne - nb + TC_C - 1) / TC_C;
   uint8_t* vec = sm + M_VEC;
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -158,7 +172,14 @@ __global__ void __launch_bounds__(NTHR, 1)
   grid_dep_wait();  // the state pass's outputs are visible from here on
   const uint32_t tm = tmem_base;
   const uint32_t TA = tm, TDA = tm + 128, TG1 = tm + 256, TG2 = tm + 320, TST = tm + 384;
-  auto chunk_at = [&](int c) { return role == 1 ? nch - 1 - c : c; };
+  // the c-th chunk in walking order: its flat index, (b, h) and first token
+  auto flat_at = [&](int c) { return role == 1 ? F1 - 1 - c : F0 + c; };
+  auto bh_at = [&](int c) { return flat_at(c) / nchh; };
+  auto n0_at = [&](int c) { return (flat_at(c) % nchh) * TC_C; };
+  // chunk c opens a new (b, h) within the run: the carried state restarts at zero
+  auto head_first = [&](int c) {
+    return c > 0 && flat_at(c) % nchh == (role == 0 ? 0 : nchh - 1);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -169,7 +190,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         if (c >= NST && !wt(&bar_empty[s], ((c / NST) - 1) & 1, 21)) break;
         uint8_t* st = sm + s * M_STAGE;
         mbar_arrive_expect_tx(&bar_full[s], 4 * TILE);
-        const int n0 = nb + chunk_at(c) * TC_C;
+        const int n0 = n0_at(c), bh = bh_at(c);
         tma_load_3d(st, &maps.fq, &bar_full[s], 0, n0, bh);
         tma_load_3d(st + TILE, &maps.fk, &bar_full[s], 0, n0, bh);
         tma_load_3d(st + 2 * TILE, &maps.v, &bar_full[s], 0, n0, bh);
@@ -209,16 +230,17 @@ __global__ void __launch_bounds__(NTHR, 1)
         mma_commit(&bar_a);
         if (!wt(&bar_rp, c & 1, 23)) break;  // the carried state has been read out
         tc_fence_after();
+        const bool fresh = head_first(c);  // a new (b, h): the state restarts from zero
         if (role == 0) {
           const uint64_t dVt = sdesc(vs, vaddr - vs, 1024);  // [V | 1]
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // S~ += phi(K)^T [V | 1]
-            mma_bf16(TST, dadd(dK, kk * 2048), dadd(dVt, kk * 2048), ID_ST, 1);
+            mma_bf16(TST, dadd(dK, kk * 2048), dadd(dVt, kk * 2048), ID_ST, kk > 0 || !fresh);
         } else {
           const uint64_t dGt = sdesc(gs, vaddr - gs, 1024);  // [gt | gam]
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // R~ += phi(Q)^T [gt | gam]
-            mma_bf16(TST, dadd(dQ, kk * 2048), dadd(dGt, kk * 2048), ID_ST, 1);
+            mma_bf16(TST, dadd(dQ, kk * 2048), dadd(dGt, kk * 2048), ID_ST, kk > 0 || !fresh);
         }
         mma_commit(&bar_s);
         if (!wt(&bar_p, c & 1, 23)) break;
@@ -264,59 +286,52 @@ __global__ void __launch_bounds__(NTHR, 1)
     const bool has_s = lane < 16;  // M=64 accumulators: row 16*qd + lane in lane 32*qd + lane
     const int srow = 16 * qd + lane;
     const int c0 = OW * wg, k0 = KW * wg;
-    const long hb = static_cast<long>(bh) * N;
     auto gam_at = [&](int c) {  // gam of this thread's row in chunk c
-      const int n0 = nb + chunk_at(c) * TC_C;
-      return row < min(TC_C, ne - n0) ? gam[hb + n0 + row] : 0.f;
+      const int n0 = n0_at(c);
+      return row < min(TC_C, N - n0) ? gam[static_cast<long>(bh_at(c)) * N + n0 + row] : 0.f;
     };
     // gam_i into row i, column 0 of the vector atom (128-byte swizzle)
     auto put_gam = [&](float g) {
       *reinterpret_cast<bf16*>(vec + row * 128 + ((row & 7) << 4)) = __float2bfloat16_rn(g);
     };
     {
-      // carried state: role 0 sums the records of the sub-segments before this
-      // segment ([S | z]), role 1 those after it ([R | r]); every compute
-      // thread adds up a slice, into the P tile (free until the first mask)
-      const int lo = role == 0 ? 0 : (p + 1) * subs_per_seg;
-      const int hi = role == 0 ? p * subs_per_seg : nsub;
+      // carried state: role 0 sums the records of the sub-segments before its
+      // run ([S | z]), role 1 those after it ([R | r]), in the (b, h) where the
+      // walk starts; every compute thread adds up a slice, into the P tile
+      // (free until the first mask)
+      const int ui = role == 0 ? u0 : u1 - 1;  // the first sub-segment walked
+      const int bhi = ui / nsub;
+      const int lo = role == 0 ? 0 : ui % nsub + 1;
+      const int hi = role == 0 ? ui % nsub : nsub;
       const int off = role == 0 ? 0 : DM + 64;
       float* scr = reinterpret_cast<float*>(sm + M_P);
-      // decay: a forward record (summed to its sub-segment's end) reaches this
-      // segment's start through gamma^((lo' - 1 - pp) sub_len), lo' = p subs; a
-      // reverse record (summed from its start) reaches the next segment's start
-      // through gamma^((pp - (p+1) subs) sub_len)
-      const int sub_len = seg_len / subs_per_seg;
+      // decay: a forward record (summed to its sub-segment's end) reaches the
+      // run's start (sub-segment hi) through gamma^((hi - 1 - pp) sub_len); a
+      // reverse record (summed from its start) reaches the run's end (the start
+      // of sub-segment lo) through gamma^((pp - lo) sub_len)
+      const int sub_len = cps * TC_C;
       auto wrec = [&](int pp) {
         if (!DECAY) return 1.f;
         const int e = role == 0 ? (hi - 1 - pp) : (pp - lo);
         return exp2f(lg * static_cast<float>(e) * static_cast<float>(sub_len));
       };
+      const float4* rb = reinterpret_cast<const float4*>(rec + static_cast<long>(bhi) * nsub * REC + off);
+      constexpr int RV = REC / 4;  // float4 per record
       for (int j = t; j < (DM + 64) / 4; j += NCOMP) {  // 1040 float4 per state
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        int pp = lo;
-        for (; pp + 1 < hi; pp += 2) {  // two records per round trip
-          const float4 x = reinterpret_cast<const float4*>(rec + (static_cast<long>(bh) * nsub + pp) * REC + off)[j];
-          const float4 y = reinterpret_cast<const float4*>(rec + (static_cast<long>(bh) * nsub + pp + 1) * REC + off)[j];
-          if (DECAY) {
-            const float fx = wrec(pp), fy = wrec(pp + 1);
-            acc.x += fx * x.x + fy * y.x;
-            acc.y += fx * x.y + fy * y.y;
-            acc.z += fx * x.z + fy * y.z;
-            acc.w += fx * x.w + fy * y.w;
-          } else {
-            acc.x += x.x + y.x;
-            acc.y += x.y + y.y;
-            acc.z += x.z + y.z;
-            acc.w += x.w + y.w;
+        for (int pp = lo; pp < hi; pp += 8) {  // up to eight records per round trip
+          float4 x[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            x[i] = pp + i < hi ? rb[static_cast<long>(pp + i) * RV + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float f = DECAY && pp + i < hi ? wrec(pp + i) : 1.f;
+            acc.x += f * x[i].x;
+            acc.y += f * x[i].y;
+            acc.z += f * x[i].z;
+            acc.w += f * x[i].w;
           }
-        }
-        if (pp < hi) {
-          const float4 x = reinterpret_cast<const float4*>(rec + (static_cast<long>(bh) * nsub + pp) * REC + off)[j];
-          const float fx = wrec(pp);
-          acc.x += fx * x.x;
-          acc.y += fx * x.y;
-          acc.z += fx * x.z;
-          acc.w += fx * x.w;
         }
         reinterpret_cast<float4*>(scr)[j] = acc;
       }
@@ -357,7 +372,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     float gm = gam_at(0);
     for (int c = 0; c < nch; ++c) {
       const int s = c % NST;
-      const int n0 = nb + chunk_at(c) * TC_C;
+      const int n0 = n0_at(c), bh = bh_at(c);
       uint8_t* st = sm + s * M_STAGE;
       // P, dP of chunk c
       const bool ok_a = wtu(&bar_a, c & 1, 26);
@@ -381,16 +396,24 @@ __global__ void __launch_bounds__(NTHR, 1)
       // carried state for chunk c+1 (after this chunk's update); it must be
       // read before the next chunk's gam replaces this chunk's in the vector atom
       if (c + 1 < nch) {
+        const bool fresh = head_first(c + 1);  // a new (b, h): it starts from a zero state
         if (wtu(&bar_s, c & 1, 28)) {
           tc_fence_after();
           float sv[OW], vv[16];
-          tmem_ldn<OW / 16>(TST + lq + c0, sv);
-          tmem_ldn<1>(TST + lq + 64, vv);
+          if (fresh) {
+#pragma unroll
+            for (int i = 0; i < OW; ++i) sv[i] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) vv[i] = 0.f;
+          } else {
+            tmem_ldn<OW / 16>(TST + lq + c0, sv);
+            tmem_ldn<1>(TST + lq + 64, vv);
+          }
           if (has_s) {
             tile_put_cols<OW>(sm + M_RP + ((c + 1) & 1) * 8192, srow, c0, sv);
             if (wg == 0) s_vec[(c + 1) & 1][srow] = vv[0];
           }
-          if (DECAY) {  // the next chunk adds to gamma^128 times this state
+          if (DECAY && !fresh) {  // the next chunk adds to gamma^128 times this state
             const float g128 = exp2f(128.f * lg);
 #pragma unroll
             for (int i = 0; i < OW; ++i) sv[i] *= g128;
@@ -477,12 +500,14 @@ __global__ void __launch_bounds__(NTHR, 1)
 }
 
 // ------------------------------------------------------------- state pass
-// One CTA per sub-segment.  Per chunk: phi(Q), phi(K) in place (and to the
-// workspace), gt = dout / den in place over dout (and to the workspace), gam
-// = -(gt . out) (to the workspace and as column 0 of the gam tile), then
+// One CTA per spc consecutive sub-segments (one or two).  Per chunk: phi(Q),
+// phi(K) in place (and to the workspace), gt = dout / den in place over dout
+// (and to the workspace), gam = -(gt . out) (to the workspace and as column 0
+// of the gam tile), then
 //   S~ += phi(K)^T [V | 1]   and   R~ += phi(Q)^T [gt | gam]
 // as two 64 x 80 products whose last atoms are the ones tile and the gam
-// tile.  The sub-segment's partial [S | z | R | r] leaves by one bulk copy.
+// tile, into the accumulator pair of the chunk's sub-segment.  Each
+// sub-segment's partial [S | z | R | r] leaves by one bulk copy.
 // smem: two stages of [Q | K | V | dout -> gt | out], the ones tile, two gam
 // tiles (one per stage).
 constexpr int SS_STAGE = 5 * TILE;
@@ -510,7 +535,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     k_tc_bwd_state(const __grid_constant__ StateMaps maps, const float* __restrict__ den,
                    float* __restrict__ gam, bf16* __restrict__ gt_out, bf16* __restrict__ fq_out,
                    bf16* __restrict__ fk_out, float* __restrict__ rec, int N, int sub_len, int nsub,
-                   int dch, int feat, float lg, int* err) {
+                   int spc, int dch, int feat, float lg, int* err) {
   const int p = blockIdx.x, bh = blockIdx.y;  // the call's first kernel
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -518,8 +543,11 @@ __global__ void __launch_bounds__(NTHR, 1)
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = p * sub_len;
-  const int ne = min(N, nb + sub_len);
+  const int sub0 = p * spc;                 // this CTA's first sub-segment
+  const int nsb = min(spc, nsub - sub0);    // and how many
+  const int cps = sub_len / TC_C;           // chunks per sub-segment
+  const int nb = sub0 * sub_len;
+  const int ne = min(N, nb + nsb * sub_len);
   const int nch = (ne - nb + TC_C - 1) / TC_C;
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -538,7 +566,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     prefetch_tensormap(&maps.o);
     s_abort = 0;
   }
-  if (warp == 1) tmem_alloc(&tmem_base, 256);
+  if (warp == 1) tmem_alloc(&tmem_base, 512);
   if (warp >= 2) {
     const int t = threadIdx.x - 64;
     ones_tile(sm + SS_ONES, t, NCOMP);
@@ -561,7 +589,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   tc_fence_after();
   grid_dep_wait();
-  const uint32_t tm = tmem_base;  // S~ at column 0, R~ at column 128
+  const uint32_t tm = tmem_base;  // sub-segment j: S~ at column 256 j, R~ at 256 j + 128
 
   if (warp == 0) {
     if (lane == 0) {
@@ -593,12 +621,14 @@ __global__ void __launch_bounds__(NTHR, 1)
         const uint64_t dVt = sdesc(v, ones - v, 1024), dGt = sdesc(g, gt - g, 1024);
         if (!wt(&bar_phi[s], (c >> 1) & 1, 42)) break;
         tc_fence_after();
+        const uint32_t tj = tm + 256 * static_cast<uint32_t>(c / cps);  // the chunk's sub-segment
+        const bool first = c % cps == 0;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // S~ += phi(K)^T [V | 1]
-          mma_bf16(tm, dadd(dK, kk * 2048), dadd(dVt, kk * 2048), ID_ST80, c > 0 || kk > 0);
+          mma_bf16(tj, dadd(dK, kk * 2048), dadd(dVt, kk * 2048), ID_ST80, !first || kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // R~ += phi(Q)^T [gt | gam]
-          mma_bf16(tm + 128, dadd(dQ, kk * 2048), dadd(dGt, kk * 2048), ID_ST80, c > 0 || kk > 0);
+          mma_bf16(tj + 128, dadd(dQ, kk * 2048), dadd(dGt, kk * 2048), ID_ST80, !first || kk > 0);
         mma_commit(&bar_empty[s]);
       }
       mma_commit(&bar_done);  // also after an early exit: every issued MMA has finished
@@ -620,6 +650,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       const int s = c & 1;
       const int n0 = nb + c * TC_C;
       const int valid = min(TC_C, ne - n0);
+      const int nbj = nb + (c / cps) * sub_len, nej = min(N, nbj + sub_len);  // the chunk's sub-segment
       uint8_t* st = sm + s * SS_STAGE;
       const float inv[2] = {1.f / dn_next[0], 1.f / dn_next[1]};
       load_inv(c + 1, dn_next);
@@ -648,7 +679,7 @@ __global__ void __launch_bounds__(NTHR, 1)
               // phi(K) gamma^(127-r)); the records take sub-segment-scaled ones (the
               // reverse sums from the sub-segment's start, the forward sums to its end)
               const float fw = exp2f(lg * static_cast<float>(k == 0 ? r : 127 - r));
-              const float fs = exp2f(lg * static_cast<float>(k == 0 ? n0 + r - nb : ne - 1 - n0 - r));
+              const float fs = exp2f(lg * static_cast<float>(k == 0 ? n0 + r - nbj : nej - 1 - n0 - r));
               *reinterpret_cast<uint4*>(st + k * TILE + v * 16) = scale_vec(f, fs);
               if (rv) *reinterpret_cast<uint4*>((k == 0 ? fq_out : fk_out) + gofs) = scale_vec(f, fw);
             } else {
@@ -689,18 +720,20 @@ __global__ void __launch_bounds__(NTHR, 1)
       fence_proxy_async();
       mbar_arrive(&bar_phi[s]);
     }
-    // the partial states [S | z | R | r]: TMEM -> shared memory (stage 0) -> one bulk copy
+    // the partial states [S | z | R | r] of each sub-segment: TMEM -> shared
+    // memory (stage 0, one record after the other) -> one bulk copy each
     const int qd = warp & 3, wq = (warp - 2) >> 2;  // lane quarter, warp within it
     const uint32_t lq = static_cast<uint32_t>(32 * qd) << 16;
     const int srow = 16 * qd + lane;
     float* stg = reinterpret_cast<float*>(sm);
+    static_assert(2 * REC * 4 <= SS_STAGE, "two records fit stage 0");
     if (wtu(&bar_done, 0, 44)) {
       tc_fence_after();
-      for (int blk = wq; blk < 10; blk += 4) {  // 16-column blocks: S~ 0-4, R~ 5-9
-        const int which = blk / 5, col = (blk % 5) * 16;
+      for (int blk = wq; blk < 10 * nsb; blk += 4) {  // 16-column blocks: S~ 0-4, R~ 5-9 per record
+        const int j = blk / 10, which = (blk % 10) / 5, col = (blk % 5) * 16;
         float sv[16];
-        tmem_ldn<1>(tm + which * 128 + lq + col, sv);
-        float* base = stg + which * (DM + 64);
+        tmem_ldn<1>(tm + 256 * j + which * 128 + lq + col, sv);
+        float* base = stg + j * REC + which * (DM + 64);
         if (lane < 16) {
           if (col < 64) {
 #pragma unroll
@@ -716,7 +749,8 @@ __global__ void __launch_bounds__(NTHR, 1)
     fence_proxy_async();
     compute_sync();
     if (t == 0 && !*reinterpret_cast<volatile int*>(&s_abort)) {
-      bulk_store(rec + (static_cast<long>(bh) * nsub + p) * REC, stg, REC * 4);
+      for (int j = 0; j < nsb; ++j)
+        bulk_store(rec + (static_cast<long>(bh) * nsub + sub0 + j) * REC, stg + j * REC, REC * 4);
       bulk_commit();
       bulk_wait_all();
     }
@@ -725,30 +759,62 @@ __global__ void __launch_bounds__(NTHR, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tm, 256);
+  if (warp == 1) tmem_dealloc(tm, 512);
 }
 
 struct BwdPlan {
-  SegPlan main;   // segments of the second pass (two roles each)
-  int subs;       // sub-segments per segment in the first pass
-  int sub_len;    // tokens per sub-segment
-  int nsub;       // sub-segments per (b, h)
+  int g;           // chunks per sub-segment
+  int sub_len;     // tokens per sub-segment
+  int nsub;        // sub-segments per (b, h)
+  int spc;         // sub-segments per state-pass CTA (1 or 2)
+  int nchh;        // chunks per (b, h)
+  int n0, upc0;    // main pass, role 0 (dq): CTAs and sub-segments per CTA
+  int n1, upc1;    // role 1 (dk, dv)
 };
 
+// The runs of the main pass: one wave of CTAs, the dq role on n0 of them and
+// the dk / dv role on the rest, each run upc whole sub-segments of the flat
+// (b, h, sub-segment) order.  The sub-segment length g and the split are
+// chosen to minimise the state pass's time plus the longest run, in units of
+// a dq chunk (about 2.4 us on the 3072-token, 64-wide workload): a dk / dv
+// chunk weighs 1.4 (3.4 us), each record a run adds up at its start 0.1, a
+// state-pass chunk 1.3 and a state-pass CTA's fixed cost 1.
 BwdPlan bwd_plan(int BH, int N) {
-  const int nsm = sm_count();
-  BwdPlan b;
-  b.main = tc_plan(2 * BH, N);
-  const int per = b.main.seg_len / TC_C;
-  b.subs = 1;
-  for (int f = per; f >= 1; --f)
-    if (per % f == 0 && static_cast<long>(b.main.nseg) * f * BH <= nsm) {
-      b.subs = f;
-      break;
+  constexpr double W1 = 1.4, WREC = 0.1, WS = 1.3, FS = 1.0;
+  const int slots = sm_count() < 2 ? 2 : sm_count();
+  const int nchh = (N + TC_C - 1) / TC_C;
+  auto cdiv = [](long a, long b) { return (a + b - 1) / b; };
+  BwdPlan best{};
+  double best_cost = 1e300;
+  for (int g = nchh; g >= 1; --g) {  // larger sub-segments first: fewer records on a tie
+    const int nsub = static_cast<int>(cdiv(nchh, g));
+    const long U = static_cast<long>(BH) * nsub;
+    const int spc = U <= slots ? 1 : 2;
+    const double state = static_cast<double>(cdiv(BH * cdiv(nsub, spc), slots)) * (FS + WS * spc * g);
+    const long lo0 = cdiv(U, slots - 1);  // leave at least one CTA to role 1
+    for (long upc0 = lo0; upc0 <= U && upc0 <= lo0 + 64; ++upc0) {
+      const long n0 = cdiv(U, upc0);
+      const long upc1 = cdiv(U, slots - n0);
+      const long n1 = cdiv(U, upc1);
+      const double cost = state + WREC * nsub +
+                          std::max(static_cast<double>(upc0 * g), W1 * static_cast<double>(upc1 * g));
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best.g = g;
+        best.nsub = nsub;
+        best.n0 = static_cast<int>(n0);
+        best.upc0 = static_cast<int>(upc0);
+        best.n1 = static_cast<int>(n1);
+        best.upc1 = static_cast<int>(upc1);
+      }
     }
-  b.sub_len = b.main.seg_len / b.subs;
-  b.nsub = (N + b.sub_len - 1) / b.sub_len;
-  return b;
+  }
+  best.nchh = nchh;
+  best.sub_len = best.g * TC_C;
+  // state pass: one sub-segment per CTA while that fits one wave, else two
+  // (two accumulator pairs fill the 512 tensor-memory columns)
+  best.spc = static_cast<long>(BH) * best.nsub <= slots ? 1 : 2;
+  return best;
 }
 
 struct BwdWs {
@@ -817,13 +883,15 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
   if ((e = cudaFuncSetAttribute(kmain, cudaFuncAttributeMaxDynamicSharedMemorySize, M_SMEM)) !=
       cudaSuccess)
     return e;
-  if ((e = launch_pdl(kstate, dim3(pl.nsub, BH), dim3(NTHR), SS_SMEM, st, smap, den, w.gam,
-                      w.gt, w.fq, w.fk, w.rec, s.N, pl.sub_len, pl.nsub, s.D / 8, feat ? 1 : 0, lg,
-                      status_word())) != cudaSuccess)
+  const int nstate = (pl.nsub + pl.spc - 1) / pl.spc;
+  if ((e = launch_pdl(kstate, dim3(nstate, BH), dim3(NTHR), SS_SMEM, st, smap, den, w.gam,
+                      w.gt, w.fq, w.fk, w.rec, s.N, pl.sub_len, pl.nsub, pl.spc, s.D / 8,
+                      feat ? 1 : 0, lg, status_word())) != cudaSuccess)
     return e;
-  if ((e = launch_pdl(kmain, dim3(pl.main.nseg, BH, 2), dim3(NTHR), M_SMEM, st, m,
+  if ((e = launch_pdl(kmain, dim3(pl.n0 + pl.n1), dim3(NTHR), M_SMEM, st, m,
                       static_cast<const float*>(w.rec), static_cast<const float*>(w.gam), s.N,
-                      pl.main.seg_len, pl.nsub, pl.subs, feat ? 1 : 0, lg, status_word())) != cudaSuccess)
+                      pl.nchh, pl.g, pl.nsub, BH, pl.n0, pl.upc0, pl.upc1, feat ? 1 : 0, lg,
+                      status_word())) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }
