@@ -517,7 +517,8 @@ constexpr int SS_SMEM = SS_GAMT + 2 * TILE + 1024;
 constexpr uint32_t ID_ST80 = idesc_bf16(64, 80, true, true);
 
 struct StateMaps {
-  CUtensorMap q, k, v, g, o;
+  CUtensorMap q, k, v, g, o;  // inputs
+  CUtensorMap fq, fk, gt;     // the workspace rows the main pass reads (TMA stores)
 };
 
 // The constant ones tile ([128][64] bf16, column 0 = 1): the second N atom of
@@ -539,7 +540,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int p = blockIdx.x, bh = blockIdx.y;  // the call's first kernel
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
-  __shared__ uint64_t bar_full[2], bar_empty[2], bar_phi[2], bar_done;
+  __shared__ uint64_t bar_full[2], bar_empty[2], bar_phi[2], bar_done, bar_st;
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -558,6 +559,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       mbar_init(&bar_phi[s], NCOMP);
     }
     mbar_init(&bar_done, 1);
+    mbar_init(&bar_st, 1);
     fence_barrier_init();
     prefetch_tensormap(&maps.q);
     prefetch_tensormap(&maps.k);
@@ -593,10 +595,29 @@ __global__ void __launch_bounds__(NTHR, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
-      for (int c = 0; c < nch; ++c) {
+      // Without decay the stage's phi(Q), phi(K) and gt tiles are the
+      // workspace rows: TMA stores write them once the compute warps are done
+      // with the chunk (rows past N are clipped), and a stage is reloaded only
+      // after its stores have read it.
+      auto store_ws = [&](int c) {
         const int s = c & 1;
-        if (c >= 2 && !wt(&bar_empty[s], ((c >> 1) - 1) & 1, 41)) break;
+        if (!wt(&bar_phi[s], (c >> 1) & 1, 45)) return false;
+        const uint8_t* st = sm + s * SS_STAGE;
+        const int n0 = nb + c * TC_C;
+        tma_store_3d(&maps.fq, st, 0, n0, bh);
+        tma_store_3d(&maps.fk, st + TILE, 0, n0, bh);
+        tma_store_3d(&maps.gt, st + 3 * TILE, 0, n0, bh);
+        bulk_commit();
+        return true;
+      };
+      int issued = 0;
+      bool ok = true;
+      for (int c = 0; c < nch && ok; ++c) {
+        const int s = c & 1;
+        if (c >= 2) {
+          if (!(ok = wt(&bar_empty[s], ((c >> 1) - 1) & 1, 41))) break;
+          if (!DECAY) bulk_wait_read();  // chunk c-2's stores (the only ones in flight) have read the stage
+        }
         uint8_t* st = sm + s * SS_STAGE;
         const int n0 = nb + c * TC_C;
         mbar_arrive_expect_tx(&bar_full[s], 5 * TILE);
@@ -606,9 +627,14 @@ __global__ void __launch_bounds__(NTHR, 1)
         tma_load_3d(st + 3 * TILE, &maps.g, &bar_full[s], 0, n0, bh);
         tma_load_3d(st + 4 * TILE, &maps.o, &bar_full[s], 0, n0, bh);
         ++issued;
+        if (!DECAY && c >= 1) ok = store_ws(c - 1);
       }
+      if (!DECAY && ok && nch > 0) store_ws(nch - 1);
       for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)  // no load in flight at exit
         mbar_wait(&bar_full[i & 1], (i >> 1) & 1, WAIT_NS);
+      bulk_wait_read();
+      mbar_arrive(&bar_st);  // stage 0 may take the records
+      bulk_wait_all();
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -669,8 +695,9 @@ __global__ void __launch_bounds__(NTHR, 1)
           const int v = t + i * NCOMP, r = v >> 3, lc = (v & 7) ^ (r & 7);
           const bool rv = r < valid;
           const long gofs = (hb + n0 + r) * 64 + lc * 8;
-          // phi(Q), phi(K): in place and to the workspace (zero on padded
-          // features of a head narrower than 64: phi(0) = 1 would add them)
+          // phi(Q), phi(K): in place (zero on padded features of a head
+          // narrower than 64: phi(0) = 1 would add them); with decay also to
+          // the workspace, scaled by chunk (the TMA stores copy the tiles else)
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const uint4 f = rv && lc < dch ? (feat ? x[k][i] : phi_vec(x[k][i])) : make_uint4(0u, 0u, 0u, 0u);
@@ -684,7 +711,6 @@ __global__ void __launch_bounds__(NTHR, 1)
               if (rv) *reinterpret_cast<uint4*>((k == 0 ? fq_out : fk_out) + gofs) = scale_vec(f, fw);
             } else {
               *reinterpret_cast<uint4*>(st + k * TILE + v * 16) = f;
-              if (rv) *reinterpret_cast<uint4*>((k == 0 ? fq_out : fk_out) + gofs) = f;
             }
           }
           // gt = dout / den in place and to the workspace; gam = -(gt . out)
@@ -703,7 +729,7 @@ __global__ void __launch_bounds__(NTHR, 1)
               rw[j] = pack_bf16(g0, g1);
             }
             gv = make_uint4(rw[0], rw[1], rw[2], rw[3]);
-            *reinterpret_cast<uint4*>(gt_out + gofs) = gv;
+            if (DECAY) *reinterpret_cast<uint4*>(gt_out + gofs) = gv;
           }
           *reinterpret_cast<uint4*>(st + 3 * TILE + v * 16) = gv;
           dot += __shfl_xor_sync(0xffffffffu, dot, 1);  // the 8 vectors of row r
@@ -727,7 +753,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     const int srow = 16 * qd + lane;
     float* stg = reinterpret_cast<float*>(sm);
     static_assert(2 * REC * 4 <= SS_STAGE, "two records fit stage 0");
-    if (wtu(&bar_done, 0, 44)) {
+    if (wtu(&bar_done, 0, 44) && wtu(&bar_st, 0, 46)) {
       tc_fence_after();
       for (int blk = wq; blk < 10 * nsb; blk += 4) {  // 16-column blocks: S~ 0-4, R~ 5-9 per record
         const int j = blk / 10, which = (blk % 10) / 5, col = (blk % 5) * 16;
@@ -873,6 +899,9 @@ cudaError_t causal_bwd_tc(const void* q, const void* k, const void* v, const voi
   smap.v = m.v;
   smap.g = m.g;
   smap.o = m.o;
+  smap.fq = m.fq;
+  smap.fk = m.fk;
+  smap.gt = m.gt;
   cudaError_t e;
   const float lg = gamma == 1.f ? 0.f : log2f(gamma);
   auto kstate = lg != 0.f ? k_tc_bwd_state<true> : k_tc_bwd_state<false>;
