@@ -107,7 +107,6 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int ne = min(N, nb + seg_len);
   const int nch = (ne - nb + TC_C - 1) / TC_C;
 
-  grid_dep_launch();
   if (threadIdx.x == 0) {
     for (int s = 0; s < SNST; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -141,6 +140,9 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   tc_fence_after();
   grid_dep_wait();
+  // dependents start only once every earlier kernel has completed: the main
+  // pass then reads q, k and v without waiting for this grid
+  grid_dep_launch();
   const uint32_t TS = tmem_base;
 
   if (warp == 0) {
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                   float* __restrict__ den, const float* __restrict__ ws, int N, int nseg,
                   int seg_len, int out_v8, int dch, int M, int feat, float lg, int* err,
                   const float* __restrict__ S0,
-                  const float* __restrict__ Z0) {
+                  const float* __restrict__ Z0, int early) {
   const int p = blockIdx.x, bh = blockIdx.y;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -286,7 +288,11 @@ __global__ void __launch_bounds__(NTHR, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  grid_dep_wait();  // the state pass's records are visible from here on
+  // With a state pass before it (early), this kernel starts only after every
+  // kernel before that pass has completed, so only the warps that read the
+  // pass's records or write out and den wait for it: the loads, phi and the
+  // score products of the first chunks overlap the pass's last CTAs.
+  if (!early || warp >= W_MASK0) grid_dep_wait();
   const uint32_t tm = tmem_base;
 
   if (warp == 0) {
@@ -789,7 +795,8 @@ cudaError_t fwd_tc_launch(const void* q, const void* k, const void* v, void* out
   }
   if ((e = launch_pdl(kmain, dim3(pl.nseg, BH), dim3(NTHR), F_SMEM, st, mq, mk, mv,
                       static_cast<bf16*>(out), den, static_cast<const float*>(ws), s.N, pl.nseg,
-                      pl.seg_len, out_v8, s.D / 8, s.M, feat ? 1 : 0, lg, err, S0, Z0)) != cudaSuccess)
+                      pl.seg_len, out_v8, s.D / 8, s.M, feat ? 1 : 0, lg, err, S0, Z0,
+                      nrec > 0 ? 1 : 0)) != cudaSuccess)
     return e;
   return cudaGetLastError();
 }
