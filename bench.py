@@ -281,12 +281,19 @@ def lead(torch):
         torch.cuda._sleep(LEAD_CYCLES)
 
 
-def time_calls(fns, steps, flush, torch, dist, dev, with_median=False, sample=None):
+def time_calls(fns, steps, flush, torch, dist, dev, with_median=False, sample=None, split=True):
     """Runs `steps` iterations of the call sequence `fns`, with an L2 flush
-    before each; returns per-call mean ms and per-step mean ms (device time),
-    and with_median the per-step median ms as well."""
+    before each; returns per-call mean ms (None unless split) and per-step
+    mean ms (device time), and with_median the per-step median ms as well.
+
+    With split an event follows every call.  An event between two calls ends
+    the overlap that programmatic dependent launch gives the second call's
+    first kernel with the first call's last one (its CTAs start and run their
+    prologue while the other drains), so a step is timed without them: events
+    at the step's start and end only."""
     n = len(fns)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    ne = n + 1 if split else 2
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ne)] for _ in range(steps)]
     for i in range(steps):
         flush()
         if sample is not None:
@@ -295,14 +302,25 @@ def time_calls(fns, steps, flush, torch, dist, dev, with_median=False, sample=No
         ev[i][0].record()
         for j, fn in enumerate(fns):
             fn()
-            ev[i][j + 1].record()
+            if split:
+                ev[i][j + 1].record()
+        if not split:
+            ev[i][1].record()
     torch.cuda.synchronize()
-    per_call = [statistics.fmean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
-                for j in range(n)]
-    steps_ms = [ev[i][0].elapsed_time(ev[i][n]) for i in range(steps)]
+    per_call = ([statistics.fmean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
+                 for j in range(n)] if split else None)
+    steps_ms = [ev[i][0].elapsed_time(ev[i][ne - 1]) for i in range(steps)]
     if with_median:
         return per_call, statistics.fmean(steps_ms), statistics.median(steps_ms)
     return per_call, statistics.fmean(steps_ms)
+
+
+def step_and_calls(fns, steps, flush, torch, dev):
+    """(per-call mean ms from a pass with an event after each call, step mean
+    ms from a pass with events at the step boundaries only)."""
+    per_call, _ = time_calls(fns, steps, flush, torch, None, dev)
+    _, ms = time_calls(fns, steps, flush, torch, None, dev, split=False)
+    return per_call, ms
 
 
 def run_ours(args, dist):
@@ -343,16 +361,19 @@ def run_ours(args, dist):
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    (ms_fwd, ms_bwd), ms_step, ms_median = time_calls([fwd, bwd], args.steps, flush, torch, dist,
-                                                      dev, with_median=True, sample=nv.sample)
+    _, ms_step, ms_median = time_calls([fwd, bwd], args.steps, flush, torch, dist, dev,
+                                       with_median=True, sample=nv.sample, split=False)
     torch.cuda.synchronize()
     dist.barrier()
     wall = time.perf_counter() - t0
     smi = clocks.stop()
     clk = nv.summary(ms_step) or dict(smi)
     clk["nvidia_smi"] = smi  # 100 ms samples over the same window (few or none for short runs)
-    # the same step with L2 left warm (inputs partly resident), outside the timed region
-    _, ms_warm = time_calls([fwd, bwd], 200, lambda: None, torch, dist, dev)
+    # outside the timed region: the per-call times (a second pass of as many
+    # steps with an event after each call, which serialises the two calls)
+    # and the same step with L2 left warm (inputs partly resident)
+    (ms_fwd, ms_bwd), ms_split = time_calls([fwd, bwd], args.steps, flush, torch, dist, dev)
+    _, ms_warm = time_calls([fwd, bwd], 200, lambda: None, torch, dist, dev, split=False)
 
     ms_step_max = dist.max(ms_step, dev)
     ms_bwd_max = dist.max(ms_bwd, dev)
@@ -373,7 +394,11 @@ def run_ours(args, dist):
     step_alg = (fwd_b + bwd_b) / (ms_step_max / 1e3) / 1e9
     step_roof = {"alg_bytes": fwd_b + bwd_b, "achieved_gbs": round(step_alg, 1),
                  "frac": round(step_alg / peaks["hbm_gbs"], 4), "fwd_ms": round(ms_fwd_max, 5),
-                 "fwd_gbs": round(fwd_b / (ms_fwd_max / 1e3) / 1e9, 1)}
+                 "fwd_gbs": round(fwd_b / (ms_fwd_max / 1e3) / 1e9, 1),
+                 "split_step_ms": round(dist.max(ms_split, dev), 5),
+                 "per_call_timing": "fwd_ms and the roofline's ms come from a second pass with an "
+                                    "event after each call; that event keeps the backward's first "
+                                    "kernel from overlapping the forward's last (split_step_ms)"}
 
     e2e = measure_e2e(la, torch, dev, q, k, v, g, out, den, wsf, wsb, B, H, N, D, M, dt,
                       max(3, min(args.steps, 200)), flush, dist)
@@ -386,7 +411,8 @@ def run_ours(args, dist):
                       "in_dtype": "bf16", "accumulate": "fp32", "global_batch": B * dist.world,
                       "seq_len": N, "parallelism": f"replicas{dist.world}",
                       "l2": "flushed before every timed step (256 MiB write, untimed)",
-                      "enqueue": "GPU idles ~100 us after each flush (untimed) so the host enqueues the step ahead"},
+                      "enqueue": "GPU idles ~100 us after each flush (untimed) so the host enqueues the step ahead",
+                      "timing": "CUDA events at each step's start and end (none between the calls)"},
            "roofline": roofline, "step_roofline": step_roof, "e2e": e2e,
            "gpu_launches": launches, "clocks": clk, "wall_s_timed_region": round(wall, 3),
            "median_ms_per_step": round(dist.max(ms_median, dev), 5),
@@ -560,7 +586,7 @@ def _causal_line(la, torch, dev, flush, peaks, with_cpu, res, name):
     for _ in range(3):
         fwd()
         bwd()
-    (mf, mb), ms = time_calls([fwd, bwd], 100, flush, torch, None, dev)
+    (mf, mb), ms = step_and_calls([fwd, bwd], 100, flush, torch, dev)
     fb, bb = causal_bytes(B, H, N, D, M, 2)
     gbs = (fb + bb) / (ms / 1e3) / 1e9
     res[name] = {
@@ -595,7 +621,7 @@ def _causal_decay(la, torch, dev, flush, peaks, with_cpu, res, gamma=0.99):
     for _ in range(3):
         fwd()
         bwd()
-    (mf, mb), ms = time_calls([fwd, bwd], 50, flush, torch, None, dev)
+    (mf, mb), ms = step_and_calls([fwd, bwd], 50, flush, torch, dev)
     fb, bb = causal_bytes(B, H, N, D, M, 2)
     gbs = (fb + bb) / (ms / 1e3) / 1e9
     res["causal_decay_bf16"] = {
@@ -638,7 +664,7 @@ def _causal_poly(la, torch, dev, flush, peaks, with_cpu, res):
     for _ in range(3):
         fwd()
         bwd()
-    (mf, mb), ms = time_calls([fwd, bwd], 100, flush, torch, None, dev)
+    (mf, mb), ms = step_and_calls([fwd, bwd], 100, flush, torch, dev)
     fb, bb = causal_bytes(B, H, N, D, M, 2)
     gbs = (fb + bb) / (ms / 1e3) / 1e9
     res["causal_poly_bf16"] = {
@@ -683,7 +709,7 @@ def _noncausal(la, torch, dev, flush, peaks, with_cpu, res):
     for _ in range(3):
         fwd()
         bwd()
-    (mf, mb), ms = time_calls([fwd, bwd], 50, flush, torch, None, dev)
+    (mf, mb), ms = step_and_calls([fwd, bwd], 50, flush, torch, dev)
     valid = int(lengths.sum()) * H  # valid token-heads
     # fwd: q, k, v in, out and den out; bwd: q, k, v, dout and den in (out is
     # not needed: gt . out = phi(Q) . S gt / den), dq, dk, dv out; valid rows only
@@ -1029,7 +1055,7 @@ def sweep_points(la, torch, dev, flush, peaks, Ns, steps, total=1 << 16):
         for _ in range(3):
             fwd()
             bwd()
-        (mf, mb), ms = time_calls([fwd, bwd], steps, flush, torch, None, dev)
+        (mf, mb), ms = step_and_calls([fwd, bwd], steps, flush, torch, dev)
         peak = torch.cuda.max_memory_allocated(dev) - base
         alg = sum(causal_bytes(B, H, N, D, M, 2))
         gbs = alg / (ms / 1e3) / 1e9
