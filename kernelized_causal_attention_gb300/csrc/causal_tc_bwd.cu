@@ -316,25 +316,36 @@ __global__ void __launch_bounds__(NTHR, 1)
         return exp2f(lg * static_cast<float>(e) * static_cast<float>(sub_len));
       };
       const float4* rb = reinterpret_cast<const float4*>(rec + static_cast<long>(bhi) * nsub * REC + off);
-      constexpr int RV = REC / 4;  // float4 per record
-      for (int j = t; j < (DM + 64) / 4; j += NCOMP) {  // 1040 float4 per state
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int pp = lo; pp < hi; pp += 8) {  // up to eight records per round trip
-          float4 x[8];
+      constexpr int RV = REC / 4;       // float4 per record
+      constexpr int SV = (DM + 64) / 4; // float4 per state: 1040, columns t, t + 512, t + 1024
+      float4 acc[3];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            x[i] = pp + i < hi ? rb[static_cast<long>(pp + i) * RV + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int jj = 0; jj < 3; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int pp = lo; pp < hi; pp += 4) {  // four records of all three columns per round trip
+        float4 x[4][3];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float f = DECAY && pp + i < hi ? wrec(pp + i) : 1.f;
-            acc.x += f * x[i].x;
-            acc.y += f * x[i].y;
-            acc.z += f * x[i].z;
-            acc.w += f * x[i].w;
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jj = 0; jj < 3; ++jj) {
+            const int j = t + jj * NCOMP;
+            x[i][jj] = pp + i < hi && j < SV ? rb[static_cast<long>(pp + i) * RV + j]
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float f = DECAY && pp + i < hi ? wrec(pp + i) : 1.f;
+#pragma unroll
+          for (int jj = 0; jj < 3; ++jj) {
+            acc[jj].x += f * x[i][jj].x;
+            acc[jj].y += f * x[i][jj].y;
+            acc[jj].z += f * x[i][jj].z;
+            acc[jj].w += f * x[i][jj].w;
           }
         }
-        reinterpret_cast<float4*>(scr)[j] = acc;
       }
+#pragma unroll
+      for (int jj = 0; jj < 3; ++jj)
+        if (t + jj * NCOMP < SV) reinterpret_cast<float4*>(scr)[t + jj * NCOMP] = acc[jj];
       compute_sync();
       if (wg == 0) {  // into TMEM (the MMA's accumulator) and the bf16 state tile
         float sv[16];
