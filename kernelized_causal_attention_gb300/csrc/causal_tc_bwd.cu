@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   __shared__ uint64_t bar_full[NST], bar_empty[NST];
-  __shared__ uint64_t bar_in, bar_a, bar_p, bar_rp, bar_o, bar_s;
+  __shared__ uint64_t bar_in, bar_a, bar_p, bar_rp, bar_o, bar_o2, bar_s;
   __shared__ uint32_t tmem_base;
   __shared__ float s_vec[2][64];  // carried z (role 0) or r (role 1) before chunk c, by c & 1
   __shared__ int s_abort;
@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(NTHR, 1)
     mbar_init(&bar_a, 1);
     mbar_init(&bar_p, NCOMP);
     mbar_init(&bar_rp, NCOMP);
-    mbar_init(&bar_o, 1);
+    mbar_init(&bar_o, 1);   // dq (role 0) or dk (role 1) products done
+    mbar_init(&bar_o2, 1);  // role 1: the dv products done
     mbar_init(&bar_s, 1);
     fence_barrier_init();
     s_abort = 0;
@@ -260,6 +261,7 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // + V R^T
             mma_bf16(TG1, dadd(dV, 32 * kk), dadd(dRP, 32 * kk), ID_G, 1);
+          mma_commit(&bar_o);  // the dk epilogue may start while the dv products run
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // P^T gt
             mma_bf16(TG2, dadd(dP0, kk * 2048), dadd(dG, kk * 2048), ID_GTT, kk > 0);
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(NTHR, 1)
           for (int kk = 0; kk < 4; ++kk)  // + phi(K) R
             mma_bf16(TG2, dadd(dK, 32 * kk), dadd(dRP, kk * 2048), ID_GMN, 1);
         }
-        mma_commit(&bar_o);
+        mma_commit(role == 0 ? &bar_o : &bar_o2);
         mma_commit(&bar_empty[s]);
       }
       // every issued MMA has finished before the exit (also after an early break)
@@ -453,7 +455,9 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
         mbar_arrive(&bar_in);
       }
-      // gradients of chunk c, staged in the free P / dP tiles and TMA-stored
+      // gradients of chunk c, staged in the free P / dP tiles and TMA-stored:
+      // dq and dk over dP (read only by their own products), dv over P's
+      // second half once the dv products are done
       if (wtu(&bar_o, c & 1, 27)) {
         tc_fence_after();
         const float* vcur = s_vec[c & 1];
@@ -477,14 +481,17 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
           for (int i = 0; i < OW; ++i)
             gv[i] = (gv[i] + vcur[c0 + i]) * fo * (feat ? 1.f : fminf(x[i] * fx, 1.f));
-          tile_put_cols<OW>(sm + M_P, row, c0, gv);
-          tmem_ldn<OW / 16>(TG2 + lq + c0, gv);
-          if (DECAY) {
-            const float g1 = exp2f(lg);
+          tile_put_cols<OW>(sm + M_DP, row, c0, gv);
+          if (wtu(&bar_o2, c & 1, 29)) {
+            tc_fence_after();
+            tmem_ldn<OW / 16>(TG2 + lq + c0, gv);
+            if (DECAY) {
+              const float g1 = exp2f(lg);
 #pragma unroll
-            for (int i = 0; i < OW; ++i) gv[i] *= g1;
+              for (int i = 0; i < OW; ++i) gv[i] *= g1;
+            }
+            tile_put_cols<OW>(sm + M_P + TILE, row, c0, gv);
           }
-          tile_put_cols<OW>(sm + M_P + TILE, row, c0, gv);
         }
       }
       fence_proxy_async();
@@ -495,7 +502,7 @@ __global__ void __launch_bounds__(NTHR, 1)
         if (role == 0) {
           tma_store_3d(&maps.dq, sm + M_DP, 0, n0, bh);
         } else {
-          tma_store_3d(&maps.dk, sm + M_P, 0, n0, bh);
+          tma_store_3d(&maps.dk, sm + M_DP, 0, n0, bh);
           tma_store_3d(&maps.dv, sm + M_P + TILE, 0, n0, bh);
         }
         bulk_commit();
