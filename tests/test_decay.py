@@ -52,6 +52,9 @@ SMALL = [
     (2, 1, 3001, 32, 32, "bf16", 0.95),
     (1, 2, 777, 64, 64, "bf16", 0.5),
     (1, 1, 1, 64, 64, "bf16", 0.9),
+    # backward runs that cross heads with record sums at both ends
+    (3, 7, 777, 64, 64, "bf16", 0.95),
+    (1, 17, 2500, 64, 64, "bf16", 0.9),
     # long sequences: many segments, records weighted over long distances
     (1, 2, 65536, 64, 64, "bf16", 0.999),
     (1, 1, 20000, 32, 32, "bf16", 0.9),

@@ -78,6 +78,12 @@ SMALL = [
     (3, 1, 1000, 64, 64, "bf16"),
     (40, 4, 300, 64, 64, "bf16"),
     (1, 1, 4097, 64, 64, "bf16"),
+    # backward runs over whole sub-segments that cross from one (b, h) into the
+    # next, start or end mid-head (record sums at both ends), ragged last chunks
+    (3, 7, 777, 64, 64, "bf16"),     # both roles cross heads
+    (2, 5, 2000, 64, 64, "bf16"),    # two sub-segments per state-pass CTA
+    (1, 17, 2500, 32, 64, "bf16"),   # 2-chunk sub-segments, dq runs cross heads
+    (1, 2, 6000, 64, 64, "bf16"),    # a one-chunk last sub-segment
 ]
 
 
