@@ -535,7 +535,7 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True, only=None):
     res = {}
     want = lambda name: only is None or name in only
     # the 784-token (28 x 28) image workload: causal fwd + bwd
-    for name in ("causal_mnist_bf16", "causal_cifar_d32_bf16"):
+    for name in ("causal_mnist_bf16", "causal_cifar_d32_bf16", "causal_cifar_f32"):
         if want(name):
             _causal_line(la, torch, dev, flush, peaks, with_cpu, res, name)
     if want("causal_decay_bf16"):
@@ -564,36 +564,39 @@ def secondary(la, torch, dev, flush, peaks, with_cpu=True, only=None):
     return res
 
 
-SECONDARY = ("causal_mnist_bf16", "causal_cifar_d32_bf16", "causal_decay_bf16", "causal_poly_bf16", "noncausal_speech_f32", "prefill_cifar_bf16", "decode_f32",
+SECONDARY = ("causal_mnist_bf16", "causal_cifar_d32_bf16", "causal_cifar_f32", "causal_decay_bf16", "causal_poly_bf16", "noncausal_speech_f32", "prefill_cifar_bf16", "decode_f32",
              "decode_proj_bf16", "decode_proj_mnist_bf16", "sweep_causal_bf16")
 
 
 def _causal_line(la, torch, dev, flush, peaks, with_cpu, res, name):
-    """Causal fwd + bwd on a named bf16 workload (the 784-token images; the
-    3072-token images with the pages' 32-wide heads)."""
+    """Causal fwd + bwd on a named workload (the 784-token images; the
+    3072-token images with the pages' 32-wide heads, or with fp32 inputs)."""
     from kernelized_causal_attention_gb300.workloads import WORKLOADS, causal_inputs
     wm = WORKLOADS[name]
     B, H, N, D, M = wm.B, wm.H, wm.N, wm.D, wm.M
+    dt, elt = (la.LA_BF16, 2) if wm.dtype == "bf16" else (la.LA_F32, 4)
     q, k, v, g = causal_inputs(B, H, N, D, M, wm.dtype, wm.seed)
     qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
     out = torch.empty_like(vd)
     den = torch.empty(B, H, N, device=dev)
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    wf = la.workspace(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, 1, dev)
-    wb = la.workspace(la.LA_OP_CAUSAL_BWD, B, H, N, D, M, 1, dev)
-    fwd = lambda: la.la_causal_fwd(qd, kd, vd, out, den, wf, B, H, N, D, M, 1)
-    bwd = lambda: la.la_causal_bwd(qd, kd, vd, out, den, gd, dq, dk, dv, wb, B, H, N, D, M, 1)
+    wf = la.workspace(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, dt, dev)
+    wb = la.workspace(la.LA_OP_CAUSAL_BWD, B, H, N, D, M, dt, dev)
+    fwd = lambda: la.la_causal_fwd(qd, kd, vd, out, den, wf, B, H, N, D, M, dt)
+    bwd = lambda: la.la_causal_bwd(qd, kd, vd, out, den, gd, dq, dk, dv, wb, B, H, N, D, M, dt)
     for _ in range(3):
         fwd()
         bwd()
     (mf, mb), ms = step_and_calls([fwd, bwd], 100, flush, torch, dev)
-    fb, bb = causal_bytes(B, H, N, D, M, 2)
+    fb, bb = causal_bytes(B, H, N, D, M, elt)
     gbs = (fb + bb) / (ms / 1e3) / 1e9
     res[name] = {
         "value": round(B * N / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
         "fwd_ms": round(mf, 5), "bwd_ms": round(mb, 5), "B": B, "H": H, "N": N, "D": D, "M": M,
-        "launches": la.la_kernel_launches(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, 1)
-        + la.la_kernel_launches(la.LA_OP_CAUSAL_BWD, B, H, N, D, M, 1),
+        "dtype": wm.dtype,
+        "path": "tcgen05" if dt == la.LA_BF16 else "CUDA cores (fp32 FFMA)",
+        "launches": la.la_kernel_launches(la.LA_OP_CAUSAL_FWD, B, H, N, D, M, dt)
+        + la.la_kernel_launches(la.LA_OP_CAUSAL_BWD, B, H, N, D, M, dt),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "alg_bytes": fb + bb,
                      "bytes_per_token_head": (fb + bb) // (B * H * N)},

@@ -56,6 +56,8 @@ WORKLOADS = {
     "causal_cifar_bf16": Workload("causal_cifar_bf16", "causal", 4, 8, 3072, 64, 64, "bf16", 3),
     # the pages' models' head size: 256 / 8 = 32
     "causal_cifar_d32_bf16": Workload("causal_cifar_d32_bf16", "causal", 4, 8, 3072, 32, 32, "bf16", 8),
+    # the 3072-token images with fp32 inputs (the fp32-accurate path)
+    "causal_cifar_f32": Workload("causal_cifar_f32", "causal", 4, 8, 3072, 64, 64, "f32", 9),
     "noncausal_speech_f32": Workload("noncausal_speech_f32", "noncausal", 16, 6, 2048, 64, 64,
                                      "f32", 4, (800, 2048)),
     "decode_f32": Workload("decode_f32", "decode", 256, 8, 3072, 64, 64, "f32", 5),

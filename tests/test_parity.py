@@ -129,7 +129,8 @@ def test_causal_beyond_2_31_elements(cuda, linattn):
     linattn.check_device_status()
 
 
-@pytest.mark.parametrize("name", ["causal_tiny_f32", "causal_mnist_bf16", "causal_cifar_bf16", "causal_cifar_d32_bf16"])
+@pytest.mark.parametrize("name", ["causal_tiny_f32", "causal_mnist_bf16", "causal_cifar_bf16", "causal_cifar_d32_bf16",
+                                  "causal_cifar_f32"])
 def test_causal_workloads(cuda, linattn, name):
     w = WORKLOADS[name]
     errs = check_causal(linattn, cuda, w.B, w.H, w.N, w.D, w.M, w.dtype, w.seed)
