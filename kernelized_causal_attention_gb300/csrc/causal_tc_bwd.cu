@@ -826,12 +826,21 @@ struct BwdPlan {
 BwdPlan bwd_plan(int BH, int N) {
   constexpr double W1 = 1.4, WREC = 0.1, WS = 1.3, FS = 1.0;
   const int slots = sm_count() < 2 ? 2 : sm_count();
+  // the last plan of this thread (every backward call and workspace query asks)
+  thread_local int c_bh = -1, c_n = -1, c_slots = -1;
+  thread_local BwdPlan c_plan{};
+  if (BH == c_bh && N == c_n && slots == c_slots) return c_plan;
   const int nchh = (N + TC_C - 1) / TC_C;
   auto cdiv = [](long a, long b) { return (a + b - 1) / b; };
   BwdPlan best{};
   double best_cost = 1e300;
-  for (int g = nchh; g >= 1; --g) {  // larger sub-segments first: fewer records on a tie
+  // For a given number of sub-segments the shortest length that gives it is
+  // the best one (the costs grow with g), so only those lengths are tried
+  // (about 2 sqrt(nchh) of them), longest first: fewer records on a tie.
+  for (int k = 1; k <= nchh; ++k) {
+    const int g = static_cast<int>(cdiv(nchh, k));
     const int nsub = static_cast<int>(cdiv(nchh, g));
+    if (nsub != k) continue;  // no sub-segment length gives k of them
     const long U = static_cast<long>(BH) * nsub;
     const int spc = U <= slots ? 1 : 2;
     const double state = static_cast<double>(cdiv(BH * cdiv(nsub, spc), slots)) * (FS + WS * spc * g);
@@ -858,6 +867,10 @@ BwdPlan bwd_plan(int BH, int N) {
   // state pass: one sub-segment per CTA while that fits one wave, else two
   // (two accumulator pairs fill the 512 tensor-memory columns)
   best.spc = static_cast<long>(BH) * best.nsub <= slots ? 1 : 2;
+  c_bh = BH;
+  c_n = N;
+  c_slots = slots;
+  c_plan = best;
   return best;
 }
 
