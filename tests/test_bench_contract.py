@@ -62,3 +62,68 @@ def test_stored_traffic_only_for_the_sources_it_was_taken_on(monkeypatch):
     assert b.stored_traffic("la_causal_bwd") == stored["per_call_dram_bytes"]["la_causal_bwd"]
     monkeypatch.setattr(b, "kernel_source_hash", lambda: "0000000000000000")
     assert b.stored_traffic("la_causal_bwd") is None
+
+
+def test_fp32_algorithmic_bytes_per_token_head():
+    """fp32 inputs and outputs, D = M = 64: 1028 B forward and 2052 B backward
+    per token-head (the same tensors at four bytes an element)."""
+    fwd, bwd = _bench().causal_bytes(4, 8, 3072, 64, 64, 4)
+    th = 4 * 8 * 3072
+    assert fwd == 1028 * th and bwd == 2052 * th
+
+
+class _FakeCuda:
+    """A device clock for time_calls on the CPU: a call advances it by its
+    cost; an event records the clock when the 'stream' reaches it."""
+
+    def __init__(self):
+        self.t = 0.0
+
+    def make_torch(self):
+        clock = self
+
+        class FakeEvent:
+            def __init__(self, enable_timing=False):
+                self.at = None
+
+            def record(self, stream=None):
+                self.at = clock.t
+
+            def elapsed_time(self, other):
+                return other.at - self.at
+
+        class Cuda:
+            Event = FakeEvent
+
+            @staticmethod
+            def synchronize():
+                pass
+
+            @staticmethod
+            def _sleep(cycles):
+                pass
+
+        class Torch:
+            cuda = Cuda
+
+        return Torch
+
+
+def test_time_calls_with_and_without_events_between_calls():
+    b = _bench()
+    fake = _FakeCuda()
+    torch = fake.make_torch()
+
+    def call(ms):
+        def f():
+            fake.t += ms
+        return f
+
+    fns = [call(0.25), call(0.5)]
+    per_call, step = b.time_calls(fns, 4, lambda: None, torch, None, None)
+    assert per_call == [0.25, 0.5] and abs(step - 0.75) < 1e-12
+    none, step2, median = b.time_calls(fns, 4, lambda: None, torch, None, None, with_median=True,
+                                       split=False)
+    assert none is None and abs(step2 - 0.75) < 1e-12 and abs(median - 0.75) < 1e-12
+    per_call3, step3 = b.step_and_calls(fns, 3, lambda: None, torch, None)
+    assert per_call3 == [0.25, 0.5] and abs(step3 - 0.75) < 1e-12
