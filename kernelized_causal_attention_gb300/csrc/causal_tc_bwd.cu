@@ -189,6 +189,9 @@ __global__ void __launch_bounds__(NTHR, 1)
       for (int c = 0; c < nch; ++c) {
         const int s = c % NST;
         if (c >= NST && !wt(&bar_empty[s], ((c / NST) - 1) & 1, 21)) break;
+        // every CTA starts at once: chunk 0's tiles come in alone (they gate
+        // the first products), chunk 1's follow while chunk 0 is worked on
+        if (c == 1 && !wt(&bar_full[0], 0, 21)) break;
         uint8_t* st = sm + s * M_STAGE;
         mbar_arrive_expect_tx(&bar_full[s], 4 * TILE);
         const int n0 = n0_at(c), bh = bh_at(c);
@@ -636,6 +639,7 @@ __global__ void __launch_bounds__(NTHR, 1)
           if (!(ok = wt(&bar_empty[s], ((c >> 1) - 1) & 1, 41))) break;
           if (!DECAY) bulk_wait_read();  // chunk c-2's stores (the only ones in flight) have read the stage
         }
+        if (c == 1 && !(ok = wt(&bar_full[0], 0, 41))) break;  // chunk 0's tiles first, alone
         uint8_t* st = sm + s * SS_STAGE;
         const int n0 = nb + c * TC_C;
         mbar_arrive_expect_tx(&bar_full[s], 5 * TILE);
