@@ -557,6 +557,47 @@ constexpr size_t state_bwd_smem() {
   return sizeof(float) * (2 * C * (D + 1) + 3 * C * (M + 1) + 2 * C);
 }
 
+// Segments of the main kernels, planned in whole waves: CTAs of the given
+// dynamic shared memory fit two to an SM below half of it (else one; the
+// registers of 256 threads allow no more), `roles` CTAs run per segment, and
+// the plan minimises waves x (chunks per segment + 1) -- the longest chain of
+// CTAs an SM runs, each CTA's fixed cost (its prefix state, the first loads)
+// taken as about one chunk -- preferring fewer segments on a tie.  (Rounding
+// the segment count up to fill one wave can leave a few CTAs for a second
+// wave, which costs a whole segment's time.)
+SegPlan cc_plan(int BH, int N, int roles, size_t smem) {
+  const long occ = smem + 1024 <= 232448 / 2 ? 2 : 1;
+  const long slots = occ * (sm_count() < 1 ? 1 : sm_count());
+  const int nch = (N + C - 1) / C;
+  SegPlan best{1, nch * C};
+  long best_cost = -1;
+  for (int want = 1; want <= nch; ++want) {
+    const int per = (nch + want - 1) / want;  // chunks per segment
+    const int nseg = (nch + per - 1) / per;
+    if (nseg != want) continue;  // the shortest segments for this count only
+    const long waves = (static_cast<long>(nseg) * BH * roles + slots - 1) / slots;
+    const long cost = waves * (per + 1);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = SegPlan{nseg, per * C};
+    }
+  }
+  return best;
+}
+
+// The dynamic shared memory of the main kernels, as the launches give it.
+size_t fwd_smem_rt(int D, int M) {
+  return sizeof(float) * (2 * C * (D + 1) + C * (M + 1) + C * (C + 1) + D * (M + 1) + D + C + C + 1);
+}
+size_t bwd_smem_rt(int D, int M) {
+  return sizeof(float) *
+         (2 * C * (D + 1) + 3 * C * (M + 1) + 2 * C * (C + 1) + D * (M + 1) + D + 2 * C + C + 1);
+}
+static_assert(fwd_smem<64, 64>() == sizeof(float) * 20993 && bwd_smem<64, 64>() == sizeof(float) * 33537,
+              "the run-time sizes follow the templates");
+SegPlan fwd_plan(int BH, int N, int D, int M) { return cc_plan(BH, N, 1, fwd_smem_rt(D, M)); }
+SegPlan bwd_plan_cc(int BH, int N, int D, int M) { return cc_plan(BH, N, 2, bwd_smem_rt(D, M)); }
+
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -567,7 +608,7 @@ template <int D, int M, typename T, bool DECAY>
 cudaError_t run_fwd(const T* q, const T* k, const T* v, T* out, float* den, float* ws,
                     const Shape& s, cudaStream_t st, float lg) {
   const int BH = s.B * s.H;
-  const SegPlan pl = plan_segments(BH, s.N);
+  const SegPlan pl = fwd_plan(BH, s.N, D, M);
   cudaError_t e;
   if (pl.nseg > 1) {
     auto ks = k_seg_state_fwd<D, M, T, DECAY>;
@@ -592,7 +633,7 @@ template <int D, int M, typename T>
 cudaError_t run_prefill(const T* q, const T* k, const T* v, T* out, float* den, float* S, float* Z,
                         float* ws, const Shape& s, cudaStream_t st) {
   const int BH = s.B * s.H;
-  const SegPlan pl = plan_segments(BH, s.N);
+  const SegPlan pl = fwd_plan(BH, s.N, D, M);
   const int nrec = pl.nseg + 1;
   cudaError_t e;
   auto ks = k_seg_state_fwd<D, M, T, false>;
@@ -613,7 +654,7 @@ template <int D, int M, typename T, bool DECAY>
 cudaError_t run_bwd(const T* q, const T* k, const T* v, const T* o, const float* den, const T* g,
                     T* dq, T* dk, T* dv, float* ws, const Shape& s, cudaStream_t st, float lg) {
   const int BH = s.B * s.H;
-  const SegPlan pl = plan_segments(BH, s.N);
+  const SegPlan pl = bwd_plan_cc(BH, s.N, D, M);
   cudaError_t e;
   if (pl.nseg > 1) {
     auto ks = k_seg_state_bwd<D, M, T, DECAY>;
@@ -672,7 +713,7 @@ cudaError_t state_add_records(const float* ws, int BH, int nrec, int rstride, in
 }
 
 size_t causal_prefill_ws_floats(const Shape& s) {
-  const SegPlan pl = plan_segments(s.B * s.H, s.N);
+  const SegPlan pl = fwd_plan(s.B * s.H, s.N, s.D, s.M);
   return (size_t)s.B * s.H * (pl.nseg + 1) * (s.D * s.M + s.D);
 }
 
@@ -691,21 +732,21 @@ cudaError_t causal_prefill_cc(const void* q, const void* k, const void* v, void*
 }
 
 size_t causal_fwd_ws_floats(const Shape& s) {
-  const SegPlan pl = plan_segments(s.B * s.H, s.N);
+  const SegPlan pl = fwd_plan(s.B * s.H, s.N, s.D, s.M);
   return pl.nseg > 1 ? (size_t)s.B * s.H * pl.nseg * (s.D * s.M + s.D) : 0;
 }
 
 size_t causal_bwd_ws_floats(const Shape& s) {
-  const SegPlan pl = plan_segments(s.B * s.H, s.N);
+  const SegPlan pl = bwd_plan_cc(s.B * s.H, s.N, s.D, s.M);
   return pl.nseg > 1 ? (size_t)s.B * s.H * pl.nseg * 2 * (s.D * s.M + s.D) : 0;
 }
 
 int causal_fwd_launches(const Shape& s) {
-  return plan_segments(s.B * s.H, s.N).nseg > 1 ? 3 : 1;
+  return fwd_plan(s.B * s.H, s.N, s.D, s.M).nseg > 1 ? 3 : 1;
 }
 
 int causal_bwd_launches(const Shape& s) {
-  return plan_segments(s.B * s.H, s.N).nseg > 1 ? 3 : 1;
+  return bwd_plan_cc(s.B * s.H, s.N, s.D, s.M).nseg > 1 ? 3 : 1;
 }
 
 cudaError_t causal_fwd_cc(const void* q, const void* k, const void* v, void* out, float* den,
