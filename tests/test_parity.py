@@ -84,6 +84,8 @@ SMALL = [
     (2, 5, 2000, 64, 64, "bf16"),    # two sub-segments per state-pass CTA
     (1, 17, 2500, 32, 64, "bf16"),   # 2-chunk sub-segments, dq runs cross heads
     (1, 2, 6000, 64, 64, "bf16"),    # a one-chunk last sub-segment
+    (64, 64, 100, 64, 64, "bf16"),   # one-chunk heads: each run crosses ~28 heads
+    (32, 64, 129, 64, 64, "bf16"),   # two-chunk heads, a one-token last chunk
 ]
 
 
